@@ -1,0 +1,415 @@
+"""Benchmark: MoE decode tokens/s of the 30-layer routed + shared FFN stack.
+
+Workload (default): the 30-layer decode stack at full shape (d=2816, f=704,
+128 experts, top-8, shared expert f=2816, int4 affine groups of 64), every
+expert resident in HBM, one token per step (B = 1) through all 30 layers,
+512 synthetic tokens (bf16 N(0,1)) cycled, router logits biased by the
+Zipf(s=1.1) / reuse-0.6 expert trace of the slot-cache workload.  Each step
+streams 1.2 GB of expert weights, far more than the 129 MB L2, so no flush is
+needed between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead (bounded sample, same metric and config).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE decode tokens/s (30-layer routed+shared FFN), % of 8 TB/s HBM roofline"
+UNIT = "tokens/s"
+N_LAYERS = 30
+N_TOKENS = 512
+SEED = 2
+NOMINAL_HBM = 8e12
+
+
+def _shape():
+    from workload import FULL
+    return FULL
+
+
+def bytes_per_token_layer(sh) -> dict:
+    """Algorithmic bytes of one B=1 token through one layer, per kernel kind."""
+    nG_d = sh.d // 64
+    gu_r = (sh.f // 8) * nG_d * 576
+    gu_s = (sh.f_shared // 8) * nG_d * 576
+    dn_r = (sh.d // 16) * (sh.f // 64) * 576
+    dn_s = (sh.d // 16) * (sh.f_shared // 64) * 576
+    router = sh.n_experts * sh.d * 2
+    return {"router_topk_plan": router + sh.d * 2,
+            "gateup_gelu_gemv": gu_s + sh.top_k * gu_r,
+            "down_combine_gemv": dn_s + sh.top_k * dn_r,
+            "ffn_total": gu_s + dn_s + sh.top_k * (gu_r + dn_r)}
+
+
+def config_dict(sh):
+    return {"workload": "decode30_resident_zipf", "layers": N_LAYERS, "tokens": N_TOKENS, "B": 1,
+            "d": sh.d, "f": sh.f, "f_shared": sh.f_shared, "experts": sh.n_experts, "top_k": sh.top_k,
+            "group": sh.group, "weights": "int4 affine g64, fp16 scale+bias", "residency": "all experts in HBM",
+            "routing": "router logits + Zipf(1.1)/reuse-0.6 bias trace",
+            "l2": "no flush: 1.2 GB of weights per step vs 129 MB L2"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if still current."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    src = os.path.join(ROOT, "bit_routed_expert_router_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(src)):
+        with open(os.path.join(src, name), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    with open(path) as fh:
+        for line in fh:
+            parts = line.split()
+            if len(parts) == 3 and not line.startswith("#") and parts[2] == digest:
+                out[parts[0]] = float(parts[1])
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def result(self):
+        if self.proc is None:
+            return None
+        try:
+            with open(self.file.name) as fh:
+                rows = [r.split(",") for r in fh.read().strip().splitlines() if r.strip()]
+            os.unlink(self.file.name)
+        except Exception:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def maybe_init_dist(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def aggregate(dist, local_seconds: float, local_units: float):
+    """Max time over ranks and summed units (replicas: no data-path collective)."""
+    if dist is None:
+        return local_seconds, local_units
+    import torch
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+def oracle_token_layer_seconds(layers_cpu: list, H, bias, n_samples: int, budget_s: float):
+    """Time the oracle on (token, layer) samples; returns (mean seconds, samples, cores)."""
+    import oracle
+    lays = [oracle.Layer(w, _shape().top_k) for w in layers_cpu]
+    times = []
+    t_start = time.perf_counter()
+    for i in range(n_samples):
+        li = i % len(lays)
+        t = i % H.shape[0]
+        x = oracle.rmsnorm_bf16(oracle.as_bits(H[t]), 1e-6)
+        b = bias[t, li] if bias is not None else None
+        t0 = time.perf_counter()
+        lays[li].forward(x, b)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    return statistics.mean(times), len(times), 1
+
+
+def gen_cpu_layers(n: int):
+    """A few full-shape layers on the host (generated on the GPU when one is present)."""
+    import torch
+    from workload import gen_layer
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    out = []
+    for layer in range(n):
+        w = gen_layer(_shape(), seed=SEED, layer=layer, device=dev)
+        out.append({"router_w": w["router_w"].cpu(),
+                    "experts": {k: v.cpu() for k, v in w["experts"].items()},
+                    "shared": {k: v.cpu() for k, v in w["shared"].items()}})
+        del w
+    return out
+
+
+def host_inputs():
+    import numpy as np
+    from workload import bias_from_targets, gen_hidden, zipf_reuse_targets
+    sh = _shape()
+    H = gen_hidden(N_TOKENS, sh.d, seed=SEED)
+    tg = zipf_reuse_targets(N_TOKENS, N_LAYERS, sh.n_experts, sh.top_k, seed=SEED)
+    bias = bias_from_targets(tg, sh.n_experts).astype(np.float32)
+    return H, bias
+
+
+# ---------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    sh = _shape()
+    H, bias = host_inputs()
+    layers = gen_cpu_layers(2)
+    # one untimed evaluation warms the oracle; the timed sample is bounded by
+    # --cpu-budget seconds so the run ends within a few minutes whatever K is
+    oracle_token_layer_seconds(layers, H, bias, 1, 1e9)
+    t0 = time.perf_counter()
+    mean_s, n, cores = oracle_token_layer_seconds(layers, H, bias, args.steps, args.cpu_budget * 4)
+    wall = time.perf_counter() - t0
+    tok_s = 1.0 / (N_LAYERS * mean_s)
+    sample = f"{n} (token, layer) oracle evaluations on layers 0-1, extrapolated x{N_LAYERS} layers per token"
+    line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": ws,
+            "steps": n, "warmup": 1, "ms_per_step": wall / max(n, 1) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(sh),
+            "cpu_baseline": {"value": tok_s, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": tok_s, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import bit_routed_expert_router_gb300 as moe
+    from workload import gen_layer
+
+    ws, rank, local = dist_env()
+    dist = maybe_init_dist(ws, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sh = _shape()
+
+    cfg = moe.make_config(sh.d, sh.f, sh.f_shared, sh.n_experts, sh.top_k, n_layers=N_LAYERS, prenorm=1,
+                          max_tokens=32)
+    st, ctx = moe.moe_create(cfg, local)
+    if st != moe.MOE_OK:
+        raise moe.MoeError(st, moe.moe_last_error(None))
+    for layer in range(N_LAYERS):
+        w = gen_layer(sh, seed=SEED, layer=layer, device=dev)
+        moe.check(moe.moe_init_layer(ctx, layer, w["router_w"], w["experts"], w["shared"]), ctx)
+        del w
+    torch.cuda.synchronize()
+    H_host, bias_host = host_inputs()
+    H = H_host.to(dev)
+    bias = torch.from_numpy(bias_host).to(dev)          # [T, L, E]
+    out = torch.empty(1, sh.d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        t = i % N_TOKENS
+        s, _ = moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, N_LAYERS, bias[t], out, None, None, stream)
+        if s != moe.MOE_OK:
+            moe.check(s, ctx)
+
+    # warm-up
+    for i in range(args.warmup):
+        step(i)
+    moe.check(moe.moe_sync(ctx, stream), ctx)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    # timed region: K graph-replayed decode steps, CUDA events on the launch stream
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        e1.record(stream)
+        e1.synchronize()
+    moe.check(moe.moe_sync(ctx, stream), ctx)
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_max, units = aggregate(dist, elapsed, float(args.steps))
+    value = units / t_max
+    clocks = clk.result()
+
+    # per-kernel durations (event pairs around each launch, same stream, same workload)
+    n_prof = min(args.steps, 32)
+    moe.check(moe.moe_profile(ctx, True), ctx)
+    moe.moe_get_profile(ctx)
+    for i in range(n_prof):
+        step(i)
+    moe.check(moe.moe_profile(ctx, False), ctx)
+    _, prof = moe.moe_get_profile(ctx)
+    bpl = bytes_per_token_layer(sh)
+    kinds = {moe.KERNEL_KINDS[i]: {"launches": n, "ms": t} for i, (n, t) in enumerate(prof) if n}
+    dom = max(kinds, key=lambda k: kinds[k]["ms"])
+    dur = kinds[dom]["ms"] / kinds[dom]["launches"] / 1e3
+    peak, peak_kind = load_peaks()
+    achieved = bpl[dom] / dur / 1e9
+    traffic = load_traffic().get(dom)
+    shares = {k: round(v["ms"] / sum(x["ms"] for x in kinds.values()), 4) for k, v in kinds.items()}
+
+    # end to end through the C ABI with host buffers: H2D inputs, D2H output, every step
+    h_pin = H_host.pin_memory()
+    b_pin = torch.from_numpy(bias_host).pin_memory()
+    o_pin = torch.empty(1, sh.d, dtype=torch.bfloat16).pin_memory()
+    h_dev = torch.empty(1, sh.d, dtype=torch.bfloat16, device=dev)
+    b_dev = torch.empty(N_LAYERS, sh.n_experts, dtype=torch.float32, device=dev)
+
+    def e2e_step(i):
+        t = i % N_TOKENS
+        h_dev.copy_(h_pin[t:t + 1], non_blocking=True)
+        b_dev.copy_(b_pin[t], non_blocking=True)
+        s, _ = moe.moe_decode_step(ctx, h_dev, 1, 0, N_LAYERS, b_dev, out, None, None, stream)
+        if s != moe.MOE_OK:
+            moe.check(s, ctx)
+        o_pin.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    f1.record(stream)
+    f1.synchronize()
+    e2e_t, e2e_units = aggregate(dist, f0.elapsed_time(f1) / 1e3, float(args.steps))
+    e2e_value = e2e_units / e2e_t
+
+    # CPU oracle on the host cores (rank 0, one GPU only), bounded sample
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        layers_cpu = gen_cpu_layers(2)
+        mean_s, n, cores = oracle_token_layer_seconds(layers_cpu, H_host, bias_host, 64, args.cpu_budget)
+        cpu = {"value": 1.0 / (N_LAYERS * mean_s), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n} (token, layer) evaluations on layers 0-1, {mean_s:.2f} s each, "
+                         f"extrapolated x{N_LAYERS} layers per token"}
+
+    moe.moe_destroy(ctx)
+    if rank == 0:
+        ffn_bytes = bpl["ffn_total"] * N_LAYERS
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16xint4->f32 (router int64)",
+            "data": "synthetic", "config": config_dict(sh),
+            "hbm_roofline_frac_8tbs": value / ws * ffn_bytes / NOMINAL_HBM,
+            "bytes_per_token": ffn_bytes,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "bytes_per_launch": bpl[dom],
+                         "avg_launch_us": dur * 1e6},
+            "kernel_shares": shares,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": sh.d * 2 + N_LAYERS * sh.n_experts * 4,
+                    "d2h_bytes_per_step": sh.d * 2},
+            "gpu_launches": 3 * N_LAYERS * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

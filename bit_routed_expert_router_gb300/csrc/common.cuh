@@ -1,0 +1,125 @@
+// Device-side helpers shared by the libmoe kernels (sm_103a).
+//
+// Inline PTX for the pieces the kernels are built from: mbarriers, 1-D bulk
+// (TMA engine) copies global -> shared, the register-sourced bf16 tensor-core
+// MMA used by the int4 GEMVs, and bounded spin-waits that report a timeout
+// through a device error word instead of hanging.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace moe {
+
+// Roughly 2 s at GB300 clocks: far beyond any legitimate wait in these kernels.
+constexpr long long kSpinLimitCycles = 4000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and flags the error word)
+// if the phase did not complete within kSpinLimitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kSpinLimitCycles) {
+      atomicOr(err, ERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> shared through the TMA engine, completing on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// D = A * B + D, m16n8k16, bf16 inputs, fp32 accumulators, A/B from registers.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Eight packed nibbles -> four bf16x2 registers holding (128 + q).
+// The word's nibble i sits at bits [4i, 4i+4); register r receives nibbles r
+// and r+4 (low and high half).  0x4300 is bf16 128.0, whose unit in the last
+// place is 1, so OR-ing a nibble into the mantissa gives exactly 128 + q.
+__device__ __forceinline__ void nibbles_to_bf16x2(uint32_t w, uint32_t (&a)[4]) {
+  a[0] = (w & 0x000F000Fu) | 0x43004300u;
+  a[1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
+  a[2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
+  a[3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ float half_lo(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<uint16_t>(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<uint16_t>(v >> 16)));
+}
+
+// Programmatic dependent launch controls (no-ops when launched without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ int64_t shfl_xor_i64(int64_t v, int m) {
+  int lo = static_cast<int>(v & 0xFFFFFFFFLL);
+  int hi = static_cast<int>(v >> 32);
+  lo = __shfl_xor_sync(0xFFFFFFFFu, lo, m);
+  hi = __shfl_xor_sync(0xFFFFFFFFu, hi, m);
+  return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
+}
+
+}  // namespace moe

@@ -1,0 +1,914 @@
+// Host side of libmoe: the C ABI declared in include/moe.h.
+//
+// Owns the device weights (repacked), the pinned host expert pool and the
+// per-layer device slots of host-pool contexts, the per-call scratch, a side
+// stream for staging copies, and the CUDA graphs that replay a resident
+// decode step (router, gate/up, down per layer) with one launch.
+#include "moe.h"
+
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <thread>
+#include <tuple>
+#include <vector>
+
+#include "internal.h"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kArgRing = 32;
+
+struct LayerStore {
+  bool ready = false;
+  uint16_t* router_w = nullptr;       // device fp16 [E][d]
+  uint8_t* shared = nullptr;          // device layout
+  uint8_t* experts = nullptr;         // resident: E * stride
+  uint8_t* slots = nullptr;           // host pool: N * stride
+  int32_t* slot_of_expert = nullptr;  // [E]
+  int32_t* expert_of_slot = nullptr;  // [N]
+  long long* last_use = nullptr;      // [N]
+};
+
+template <class T>
+T* dalloc(size_t n, std::vector<void*>& owned, size_t& bytes) {
+  void* p = nullptr;
+  if (cudaMalloc(&p, n * sizeof(T) > 0 ? n * sizeof(T) : 16) != cudaSuccess) return nullptr;
+  owned.push_back(p);
+  bytes += n * sizeof(T);
+  return static_cast<T*>(p);
+}
+
+}  // namespace
+
+struct moe_ctx {
+  moe_config cfg{};
+  int device = 0;
+  int n_sm = 148;
+  bool poisoned = false;
+  std::string err;
+  int residency = -1;
+  int n_slots = 0;
+  long long expert_bytes = 0, shared_bytes = 0, stride = 0;
+  int n_sc = 1, cg = 1, Bd = 1;
+  std::vector<LayerStore> L;
+  uint8_t* pool = nullptr;
+  size_t pool_bytes = 0;
+  std::vector<void*> owned;           // scratch allocations
+  size_t device_bytes = 0;
+  // scratch
+  uint16_t* hbuf[2] = {nullptr, nullptr};
+  uint16_t* x_perm = nullptr;
+  float* xg = nullptr;
+  long long* logits = nullptr;
+  int32_t* ids = nullptr;
+  float* gates = nullptr;
+  int32_t* tok_cnt = nullptr;
+  int32_t* all_cnt = nullptr;
+  PlanHdr* plan = nullptr;
+  int32_t *act_expert = nullptr, *act_off = nullptr, *act_cnt = nullptr, *act_pass = nullptr;
+  int32_t* pair_tok = nullptr;
+  float* pair_gate = nullptr;
+  int32_t* pos_of = nullptr;
+  uint16_t *a_s = nullptr, *a_r = nullptr;
+  float *asum_s = nullptr, *asum_r = nullptr, *part_s = nullptr, *y_r = nullptr;
+  int32_t* row_cnt = nullptr;
+  uint32_t* err_word = nullptr;
+  long long* lru_counts = nullptr;
+  DevCallArgs* dargs = nullptr;
+  DevCallArgs* args_ring = nullptr;   // pinned host ring of argument blocks
+  cudaEvent_t ring_ev[kArgRing] = {};
+  bool ring_used[kArgRing] = {};
+  int ring_pos = 0;
+  int32_t* host_rec = nullptr;        // pinned, mapped
+  int32_t* host_rec_dev = nullptr;
+  cudaStream_t side = nullptr;
+  cudaStream_t cap = nullptr;
+  cudaEvent_t ev_route = nullptr, ev_copy = nullptr;
+  // debug capture
+  uint16_t* dbg_x = nullptr;
+  int32_t* dbg_ids = nullptr;
+  float* dbg_gates = nullptr;
+  float* dbg_y = nullptr;
+  int dbg_layers = 0;
+  // counters
+  long long step = 0, steps = 0, staged = 0;
+  // hooks
+  bool hook_fail_copy = false;
+  long long wait_limit_us = 20000000;
+  bool pdl = true;
+  std::map<std::tuple<int, int, int>, cudaGraphExec_t> graphs;
+  // per-kernel timing
+  bool profiling = false;
+  std::vector<cudaEvent_t> prof_ev;
+  std::vector<int> prof_kind;
+  int prof_n = 0;
+  moe_kernel_time prof[MOE_N_KERNEL_KINDS] = {};
+};
+
+namespace {
+
+thread_local std::string g_create_error;  // why the last moe_create failed
+
+moe_status fail(moe_ctx* c, moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (c) {
+    c->err = buf;
+    if (s == MOE_ECUDA || s == MOE_ETIMEOUT) c->poisoned = true;
+  }
+  return s;
+}
+
+#define CK(call)                                                                              \
+  do {                                                                                        \
+    cudaError_t e_ = (call);                                                                  \
+    if (e_ != cudaSuccess) return fail(ctx, MOE_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+bool cfg_valid(const moe_config* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    if (why) *why = m;
+    return false;
+  };
+  if (!c) return bad("config is NULL");
+  if (c->group != 64) return bad("group must be 64");
+  if (c->d <= 0 || c->d % 64 || c->d > 3072) return bad("d must be a positive multiple of 64, at most 3072");
+  if (c->f <= 0 || c->f % 64) return bad("f must be a positive multiple of 64");
+  if (c->f_shared <= 0 || c->f_shared % 64) return bad("f_shared must be a positive multiple of 64");
+  if (c->n_experts < 1 || c->n_experts > 256) return bad("n_experts must be in [1, 256]");
+  if (c->top_k < 1 || c->top_k > c->n_experts || c->top_k > 32) return bad("top_k must be in [1, min(n_experts, 32)]");
+  if (c->n_layers < 1 || c->n_layers > 4096) return bad("n_layers must be in [1, 4096]");
+  if (c->gelu_variant != 0 && c->gelu_variant != 1) return bad("gelu_variant must be 0 or 1");
+  if (c->prenorm != 0 && c->prenorm != 1) return bad("prenorm must be 0 or 1");
+  if (c->max_tokens < 1 || c->max_tokens > 65536) return bad("max_tokens must be in [1, 65536]");
+  if (!(c->norm_eps >= 0.f) || c->norm_eps > 1.f) return bad("norm_eps must be in [0, 1]");
+  return true;
+}
+
+long long expert_bytes_of(int d, int f) { return static_cast<long long>(f) * d * 27 / 16; }
+
+long long now_us() {
+  return std::chrono::duration_cast<std::chrono::microseconds>(
+             std::chrono::steady_clock::now().time_since_epoch())
+      .count();
+}
+
+// Bounded host wait on an event.
+moe_status wait_event(moe_ctx* ctx, cudaEvent_t ev, const char* what) {
+  const long long t0 = now_us();
+  int spins = 0;
+  for (;;) {
+    cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return MOE_OK;
+    if (e != cudaErrorNotReady) return fail(ctx, MOE_ECUDA, "waiting for %s: %s", what, cudaGetErrorString(e));
+    if (now_us() - t0 > ctx->wait_limit_us) return fail(ctx, MOE_ETIMEOUT, "waiting for %s: time limit", what);
+    if (++spins > 64) std::this_thread::yield();
+  }
+}
+
+KParams base_params(moe_ctx* ctx, int layer, int rel, int first, int last, int B) {
+  KParams p{};
+  const moe_config& c = ctx->cfg;
+  p.d = c.d;
+  p.f = c.f;
+  p.fs = c.f_shared;
+  p.E = c.n_experts;
+  p.k = c.top_k;
+  p.B = B;
+  p.prenorm = c.prenorm;
+  p.gelu = c.gelu_variant;
+  p.eps = c.norm_eps;
+  p.n_sc = ctx->n_sc;
+  p.cg = ctx->cg;
+  p.layer = layer;
+  p.rel_layer = rel;
+  p.first = first;
+  p.last = last;
+  p.pool = ctx->residency == MOE_HOST_POOL;
+  p.pass = -1;
+  p.n_slots = ctx->n_slots;
+  const LayerStore& Ls = ctx->L[layer];
+  p.router_w = Ls.router_w;
+  p.shared = Ls.shared;
+  p.experts = p.pool ? Ls.slots : Ls.experts;
+  p.expert_stride = ctx->stride;
+  p.slot_of_expert = Ls.slot_of_expert;
+  p.expert_of_slot = Ls.expert_of_slot;
+  p.last_use = Ls.last_use;
+  p.lru_counts = ctx->lru_counts;
+  p.host_rec = ctx->host_rec_dev;
+  p.args = ctx->dargs;
+  p.x_perm = ctx->x_perm;
+  p.xg = ctx->xg;
+  p.logits = ctx->logits;
+  p.ids = ctx->ids;
+  p.gates = ctx->gates;
+  p.tok_cnt = ctx->tok_cnt;
+  p.all_cnt = ctx->all_cnt;
+  p.plan = ctx->plan;
+  p.act_expert = ctx->act_expert;
+  p.act_off = ctx->act_off;
+  p.act_cnt = ctx->act_cnt;
+  p.act_pass = ctx->act_pass;
+  p.pair_tok = ctx->pair_tok;
+  p.pair_gate = ctx->pair_gate;
+  p.pos_of = ctx->pos_of;
+  p.a_s = ctx->a_s;
+  p.a_r = ctx->a_r;
+  p.asum_s = ctx->asum_s;
+  p.asum_r = ctx->asum_r;
+  p.part_s = ctx->part_s;
+  p.y_r = ctx->y_r;
+  p.row_cnt = ctx->row_cnt;
+  p.err = ctx->err_word;
+  return p;
+}
+
+int gu_max_items(const moe_ctx* ctx, int B) {
+  const moe_config& c = ctx->cfg;
+  const int maxU = std::min(c.n_experts, B * c.top_k);
+  return c.f_shared / 8 + maxU * (c.f / 8);
+}
+
+int dn_max_items(const moe_ctx* ctx, int B) {
+  const moe_config& c = ctx->cfg;
+  const int maxU = std::min(c.n_experts, B * c.top_k);
+  return (c.d / 16) * (ctx->n_sc + maxU);
+}
+
+// Event pair around one launch while profiling.
+moe_status prof_mark(moe_ctx* ctx, int kind, cudaStream_t s) {
+  if (!ctx->profiling) return MOE_OK;
+  if (ctx->prof_n + 1 >= static_cast<int>(ctx->prof_ev.size())) {
+    for (int i = 0; i < 256; ++i) {
+      cudaEvent_t e;
+      CK(cudaEventCreate(&e));
+      ctx->prof_ev.push_back(e);
+    }
+    ctx->prof_kind.resize(ctx->prof_ev.size() / 2 + 1);
+  }
+  if (kind >= 0) ctx->prof_kind[ctx->prof_n / 2] = kind;
+  CK(cudaEventRecord(ctx->prof_ev[ctx->prof_n++], s));
+  return MOE_OK;
+}
+
+#define PROF(kind, s)                              \
+  do {                                             \
+    moe_status ps_ = prof_mark(ctx, (kind), (s));  \
+    if (ps_ != MOE_OK) return ps_;                 \
+  } while (0)
+
+moe_status prof_collect(moe_ctx* ctx, cudaStream_t s) {
+  if (!ctx->profiling || ctx->prof_n == 0) return MOE_OK;
+  CK(cudaStreamSynchronize(s));
+  for (int i = 0; i + 1 < ctx->prof_n; i += 2) {
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, ctx->prof_ev[i], ctx->prof_ev[i + 1]));
+    moe_kernel_time& t = ctx->prof[ctx->prof_kind[i / 2]];
+    t.launches += 1;
+    t.total_ms += ms;
+  }
+  ctx->prof_n = 0;
+  return MOE_OK;
+}
+
+// Enqueue the three kernels of one resident layer on stream s.
+moe_status enqueue_layer(moe_ctx* ctx, int layer, int rel, int n_rel, int B, cudaStream_t s) {
+  KParams p = base_params(ctx, layer, rel, rel == 0, rel == n_rel - 1, B);
+  p.h_src = rel == 0 ? nullptr : ctx->hbuf[(rel - 1) & 1];
+  p.h_dst = rel == n_rel - 1 ? nullptr : ctx->hbuf[rel & 1];
+  const bool pdl = ctx->pdl && !ctx->profiling;
+  PROF(0, s);
+  CK(launch_router(p, B, s, pdl));
+  PROF(-1, s);
+  PROF(1, s);
+  CK(launch_gateup(p, B, gu_max_items(ctx, B), ctx->n_sm, s, pdl));
+  PROF(-1, s);
+  PROF(2, s);
+  CK(launch_down(p, B, dn_max_items(ctx, B), ctx->n_sm, s, pdl));
+  PROF(-1, s);
+  return MOE_OK;
+}
+
+// Write the per-call argument block through a pinned ring slot.
+moe_status put_args(moe_ctx* ctx, const DevCallArgs& a, cudaStream_t s) {
+  const int i = ctx->ring_pos;
+  ctx->ring_pos = (ctx->ring_pos + 1) % kArgRing;
+  if (ctx->ring_used[i]) {
+    moe_status st = wait_event(ctx, ctx->ring_ev[i], "argument ring slot");
+    if (st != MOE_OK) return st;
+  }
+  ctx->args_ring[i] = a;
+  CK(cudaMemcpyAsync(ctx->dargs, &ctx->args_ring[i], sizeof(DevCallArgs), cudaMemcpyHostToDevice, s));
+  CK(cudaEventRecord(ctx->ring_ev[i], s));
+  ctx->ring_used[i] = true;
+  return MOE_OK;
+}
+
+DevCallArgs make_args(moe_ctx* ctx, const void* h_in, void* h_out, float* y_last, const float* bias, int B,
+                      int tok_total, int tok_off) {
+  DevCallArgs a{};
+  a.h_in = static_cast<const uint16_t*>(h_in);
+  a.h_out = static_cast<uint16_t*>(h_out);
+  a.y_last = y_last;
+  a.bias = bias;
+  a.dbg_x = ctx->dbg_x;
+  a.dbg_ids = ctx->dbg_ids;
+  a.dbg_gates = ctx->dbg_gates;
+  a.dbg_y = ctx->dbg_y;
+  a.dbg_layers = (ctx->dbg_x || ctx->dbg_ids || ctx->dbg_gates || ctx->dbg_y) ? ctx->dbg_layers : 0;
+  a.B = B;
+  a.tok_total = tok_total;
+  a.tok_off = tok_off;
+  a.step = ctx->step;
+  return a;
+}
+
+moe_status check_ready(moe_ctx* ctx, int l0, int l1) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  if (l0 < 0 || l1 > ctx->cfg.n_layers || l0 >= l1) return fail(ctx, MOE_EINVAL, "bad layer range [%d, %d)", l0, l1);
+  for (int l = l0; l < l1; ++l)
+    if (!ctx->L[l].ready) return fail(ctx, MOE_ESTATE, "layer %d is not initialised", l);
+  return MOE_OK;
+}
+
+// Resident decode of B tokens through [l0, l1): one graph launch (or, while
+// profiling, direct launches with event pairs).
+moe_status resident_run(moe_ctx* ctx, int B, int l0, int l1, cudaStream_t s) {
+  if (ctx->profiling) {
+    for (int l = l0; l < l1; ++l) {
+      moe_status st = enqueue_layer(ctx, l, l - l0, l1 - l0, B, s);
+      if (st != MOE_OK) return st;
+    }
+    return prof_collect(ctx, s);
+  }
+  const auto key = std::make_tuple(B, l0, l1);
+  auto it = ctx->graphs.find(key);
+  if (it == ctx->graphs.end()) {
+    cudaGraph_t g = nullptr;
+    CK(cudaStreamBeginCapture(ctx->cap, cudaStreamCaptureModeThreadLocal));
+    moe_status st = MOE_OK;
+    for (int l = l0; l < l1 && st == MOE_OK; ++l) st = enqueue_layer(ctx, l, l - l0, l1 - l0, B, ctx->cap);
+    cudaError_t e = cudaStreamEndCapture(ctx->cap, &g);
+    if (st != MOE_OK) {
+      if (g) cudaGraphDestroy(g);
+      return st;
+    }
+    CK(e);
+    cudaGraphExec_t ex = nullptr;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    CK(e);
+    it = ctx->graphs.emplace(key, ex).first;
+  }
+  CK(cudaGraphLaunch(it->second, s));
+  return MOE_OK;
+}
+
+// Host-pool decode of one token through [l0, l1): per layer, route + LRU,
+// shared and hit experts while the misses are staged, then the misses, then down.
+moe_status pool_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec* trace, int trace_cap,
+                    int* trace_len) {
+  const int k = ctx->cfg.top_k;
+  int n_rec = 0;
+  for (int l = l0; l < l1; ++l) {
+    const int rel = l - l0, n_rel = l1 - l0;
+    KParams p = base_params(ctx, l, rel, rel == 0, rel == n_rel - 1, 1);
+    p.h_src = rel == 0 ? nullptr : ctx->hbuf[(rel - 1) & 1];
+    p.h_dst = rel == n_rel - 1 ? nullptr : ctx->hbuf[rel & 1];
+    CK(launch_router(p, 1, s, false));
+    CK(cudaEventRecord(ctx->ev_route, s));
+    p.pass = 0;
+    CK(launch_gateup(p, 1, gu_max_items(ctx, 1), ctx->n_sm, s, false));
+    moe_status st = wait_event(ctx, ctx->ev_route, "router / LRU step");
+    if (st != MOE_OK) return st;
+    const volatile int32_t* rec = ctx->host_rec + static_cast<size_t>(rel) * (1 + 6 * k);
+    const int n_miss = rec[0];
+    if (n_miss < 0 || n_miss > k) return fail(ctx, MOE_ECUDA, "corrupt miss record (%d)", n_miss);
+    const LayerStore& Ls = ctx->L[l];
+    for (int m = 0; m < n_miss; ++m) {
+      const int ex = rec[1 + 2 * m], slot = rec[2 + 2 * m];
+      if (ex < 0 || ex >= ctx->cfg.n_experts || slot < 0 || slot >= ctx->n_slots)
+        return fail(ctx, MOE_ECUDA, "corrupt miss record (expert %d, slot %d)", ex, slot);
+      if (ctx->hook_fail_copy) {
+        ctx->hook_fail_copy = false;
+        return fail(ctx, MOE_ECUDA, "staging copy failed (injected by test hook)");
+      }
+      const uint8_t* src = ctx->pool + (static_cast<size_t>(l) * ctx->cfg.n_experts + ex) * ctx->stride;
+      CK(cudaMemcpyAsync(Ls.slots + static_cast<size_t>(slot) * ctx->stride, src, ctx->expert_bytes,
+                         cudaMemcpyHostToDevice, ctx->side));
+      ctx->staged += ctx->expert_bytes;
+    }
+    CK(cudaEventRecord(ctx->ev_copy, ctx->side));
+    CK(cudaStreamWaitEvent(s, ctx->ev_copy, 0));
+    if (n_miss > 0) {
+      p.pass = 1;
+      CK(launch_gateup(p, 1, gu_max_items(ctx, 1), ctx->n_sm, s, false));
+    }
+    p.pass = -1;
+    CK(launch_down(p, 1, dn_max_items(ctx, 1), ctx->n_sm, s, false));
+    if (trace) {
+      for (int j = 0; j < k && n_rec < trace_cap; ++j) {
+        const volatile int32_t* tr = rec + 1 + 2 * k + 4 * j;
+        moe_trace_rec r;
+        r.token = static_cast<int32_t>(ctx->step);
+        r.layer = l;
+        r.k_pos = j;
+        r.expert = tr[0];
+        r.hit = tr[1];
+        r.slot = tr[2];
+        r.evicted = tr[3];
+        trace[n_rec++] = r;
+      }
+    }
+  }
+  if (trace_len) *trace_len = n_rec;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_EINVAL: return "MOE_EINVAL";
+    case MOE_ENOMEM: return "MOE_ENOMEM";
+    case MOE_ECUDA: return "MOE_ECUDA";
+    case MOE_ESTATE: return "MOE_ESTATE";
+    case MOE_ETIMEOUT: return "MOE_ETIMEOUT";
+    case MOE_EDOMAIN: return "MOE_EDOMAIN";
+  }
+  return "unknown";
+}
+
+const char* moe_last_error(const moe_ctx* ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
+
+int64_t moe_expert_bytes(const moe_config* cfg) {
+  if (!cfg_valid(cfg, nullptr)) return 0;
+  return expert_bytes_of(cfg->d, cfg->f);
+}
+
+int64_t moe_shared_bytes(const moe_config* cfg) {
+  if (!cfg_valid(cfg, nullptr)) return 0;
+  return expert_bytes_of(cfg->d, cfg->f_shared);
+}
+
+moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
+  g_create_error.clear();
+  if (!out) {
+    g_create_error = "out is NULL";
+    return MOE_EINVAL;
+  }
+  *out = nullptr;
+  std::string why;
+  if (!cfg_valid(cfg, &why)) {
+    g_create_error = why;
+    return MOE_EINVAL;
+  }
+  int n_dev = 0;
+  if (cudaGetDeviceCount(&n_dev) != cudaSuccess || device < 0 || device >= n_dev) {
+    cudaGetLastError();
+    g_create_error = "no such CUDA device";
+    return MOE_EINVAL;
+  }
+  moe_ctx* ctx = new moe_ctx();
+  ctx->cfg = *cfg;
+  ctx->device = device;
+  int bail_line = 0;
+  auto bail_at = [&](moe_status s, int line) {
+    cudaError_t ce = cudaGetLastError();
+    char buf[256];
+    snprintf(buf, sizeof(buf), "moe_create failed (%s) at moe_api.cu:%d, last CUDA error: %s", moe_status_string(s),
+             line, cudaGetErrorString(ce));
+    moe_destroy(ctx);
+    g_create_error = buf;
+    return s;
+  };
+#define bail(s) bail_at((s), __LINE__)
+  (void)bail_line;
+  if (cudaSetDevice(device) != cudaSuccess) return bail(MOE_ECUDA);
+  cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, device);
+  const moe_config& c = ctx->cfg;
+  ctx->expert_bytes = expert_bytes_of(c.d, c.f);
+  ctx->shared_bytes = expert_bytes_of(c.d, c.f_shared);
+  ctx->stride = (ctx->expert_bytes + 255) / 256 * 256;
+  ctx->cg = c.f / 64;
+  ctx->n_sc = (c.f_shared / 64 + ctx->cg - 1) / ctx->cg;
+  ctx->Bd = std::min(c.max_tokens, kMaxDecodeB);
+  ctx->L.resize(c.n_layers);
+  const size_t Bd = ctx->Bd, P = Bd * c.top_k;
+  size_t& nb = ctx->device_bytes;
+  auto& o = ctx->owned;
+  ctx->hbuf[0] = dalloc<uint16_t>(Bd * c.d, o, nb);
+  ctx->hbuf[1] = dalloc<uint16_t>(Bd * c.d, o, nb);
+  ctx->x_perm = dalloc<uint16_t>(Bd * c.d, o, nb);
+  ctx->xg = dalloc<float>(Bd * (c.d / 64), o, nb);
+  ctx->logits = dalloc<long long>(Bd * c.n_experts, o, nb);
+  ctx->ids = dalloc<int32_t>(P, o, nb);
+  ctx->gates = dalloc<float>(P, o, nb);
+  ctx->tok_cnt = dalloc<int32_t>(Bd, o, nb);
+  ctx->all_cnt = dalloc<int32_t>(1, o, nb);
+  ctx->plan = dalloc<PlanHdr>(1, o, nb);
+  ctx->act_expert = dalloc<int32_t>(P, o, nb);
+  ctx->act_off = dalloc<int32_t>(P, o, nb);
+  ctx->act_cnt = dalloc<int32_t>(P, o, nb);
+  ctx->act_pass = dalloc<int32_t>(P, o, nb);
+  ctx->pair_tok = dalloc<int32_t>(P, o, nb);
+  ctx->pair_gate = dalloc<float>(P, o, nb);
+  ctx->pos_of = dalloc<int32_t>(P, o, nb);
+  ctx->a_s = dalloc<uint16_t>(Bd * c.f_shared * 2, o, nb);
+  ctx->a_r = dalloc<uint16_t>(P * c.f * 2, o, nb);
+  ctx->asum_s = dalloc<float>(Bd * (c.f_shared / 8) * 2, o, nb);
+  ctx->asum_r = dalloc<float>(P * (c.f / 8) * 2, o, nb);
+  ctx->part_s = dalloc<float>(static_cast<size_t>(ctx->n_sc) * Bd * c.d, o, nb);
+  ctx->y_r = dalloc<float>(P * c.d, o, nb);
+  ctx->row_cnt = dalloc<int32_t>(c.d / 16, o, nb);
+  ctx->err_word = dalloc<uint32_t>(1, o, nb);
+  ctx->lru_counts = dalloc<long long>(static_cast<size_t>(c.n_layers) * 2, o, nb);
+  ctx->dargs = dalloc<DevCallArgs>(1, o, nb);
+  for (void* ptr : o)
+    if (!ptr) return bail(MOE_ENOMEM);
+  if (!ctx->hbuf[0] || !ctx->hbuf[1] || !ctx->x_perm || !ctx->dargs || !ctx->y_r || !ctx->part_s || !ctx->a_r)
+    return bail(MOE_ENOMEM);
+  // zero counters and tables
+  if (cudaMemset(ctx->tok_cnt, 0, Bd * 4) != cudaSuccess || cudaMemset(ctx->all_cnt, 0, 4) != cudaSuccess ||
+      cudaMemset(ctx->row_cnt, 0, (c.d / 16) * 4) != cudaSuccess || cudaMemset(ctx->err_word, 0, 4) != cudaSuccess ||
+      cudaMemset(ctx->plan, 0, sizeof(PlanHdr)) != cudaSuccess ||
+      cudaMemset(ctx->lru_counts, 0, static_cast<size_t>(c.n_layers) * 16) != cudaSuccess)
+    return bail(MOE_ECUDA);
+  if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->args_ring), sizeof(DevCallArgs) * kArgRing, cudaHostAllocDefault) !=
+      cudaSuccess)
+    return bail(MOE_ENOMEM);
+  const size_t rec_bytes = static_cast<size_t>(c.n_layers) * (1 + 6 * c.top_k) * sizeof(int32_t);
+  if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->host_rec), rec_bytes, cudaHostAllocMapped) != cudaSuccess)
+    return bail(MOE_ENOMEM);
+  memset(ctx->host_rec, 0, rec_bytes);
+  if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&ctx->host_rec_dev), ctx->host_rec, 0) != cudaSuccess)
+    return bail(MOE_ECUDA);
+  for (int i = 0; i < kArgRing; ++i)
+    if (cudaEventCreateWithFlags(&ctx->ring_ev[i], cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ECUDA);
+  if (cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&ctx->cap, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->ev_route, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->ev_copy, cudaEventDisableTiming) != cudaSuccess)
+    return bail(MOE_ECUDA);
+  int max_smem = 0;
+  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (gateup_smem(c.d) > static_cast<size_t>(max_smem) || down_smem(ctx->cg, 8) > static_cast<size_t>(max_smem))
+    return bail(MOE_EINVAL);
+  if (set_kernel_attrs(max_smem) != cudaSuccess) return bail(MOE_ECUDA);
+  if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ECUDA);
+  *out = ctx;
+  return MOE_OK;
+#undef bail
+}
+
+void moe_destroy(moe_ctx* ctx) {
+  if (!ctx) return;
+  cudaSetDevice(ctx->device);
+  cudaDeviceSynchronize();
+  for (auto& kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& Ls : ctx->L) {
+    cudaFree(Ls.router_w);
+    cudaFree(Ls.shared);
+    cudaFree(Ls.experts);
+    cudaFree(Ls.slots);
+    cudaFree(Ls.slot_of_expert);
+    cudaFree(Ls.expert_of_slot);
+    cudaFree(Ls.last_use);
+  }
+  for (void* p : ctx->owned) cudaFree(p);
+  if (ctx->pool) cudaFreeHost(ctx->pool);
+  if (ctx->args_ring) cudaFreeHost(ctx->args_ring);
+  if (ctx->host_rec) cudaFreeHost(ctx->host_rec);
+  for (auto& e : ctx->ring_ev)
+    if (e) cudaEventDestroy(e);
+  for (auto& e : ctx->prof_ev) cudaEventDestroy(e);
+  if (ctx->ev_route) cudaEventDestroy(ctx->ev_route);
+  if (ctx->ev_copy) cudaEventDestroy(ctx->ev_copy);
+  if (ctx->side) cudaStreamDestroy(ctx->side);
+  if (ctx->cap) cudaStreamDestroy(ctx->cap);
+  delete ctx;
+}
+
+moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, const moe_expert_weights* experts,
+                          const moe_expert_weights* shared, int residency) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  const moe_config& c = ctx->cfg;
+  if (layer < 0 || layer >= c.n_layers) return fail(ctx, MOE_EINVAL, "layer %d out of range", layer);
+  if (residency != MOE_RESIDENT_HBM && residency != MOE_HOST_POOL)
+    return fail(ctx, MOE_EINVAL, "unknown residency %d", residency);
+  if (ctx->residency >= 0 && residency != ctx->residency)
+    return fail(ctx, MOE_EINVAL, "all layers of a context must use the same residency");
+  if (!router_w || !experts || !shared) return fail(ctx, MOE_EINVAL, "NULL weights");
+  for (int e = 0; e <= c.n_experts; ++e) {
+    const moe_expert_weights& w = e < c.n_experts ? experts[e] : *shared;
+    if (!w.gate_q || !w.gate_sb || !w.up_q || !w.up_sb || !w.down_q || !w.down_sb)
+      return fail(ctx, MOE_EINVAL, "NULL projection pointer (expert %d)", e);
+  }
+  CK(cudaSetDevice(ctx->device));
+  LayerStore& Ls = ctx->L[layer];
+  const bool pool = residency == MOE_HOST_POOL;
+  // memory budget before allocating
+  size_t free_b = 0, total_b = 0;
+  CK(cudaMemGetInfo(&free_b, &total_b));
+  const size_t fs_can = static_cast<size_t>(c.f_shared) * c.d * 27 / 16 + 64;
+  size_t need = static_cast<size_t>(c.n_experts) * c.d * 2 + ctx->shared_bytes + 3 * fs_can;
+  need += static_cast<size_t>(c.n_experts) * ctx->stride;  // resident experts or the staging buffer
+  if (!Ls.ready && need + (256u << 20) > free_b)
+    return fail(ctx, MOE_ENOMEM, "layer needs %zu bytes, %zu free", need, free_b);
+  if (pool && !ctx->pool) {
+    const size_t pb = static_cast<size_t>(c.n_layers) * c.n_experts * ctx->stride;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->pool), pb, cudaHostAllocDefault) != cudaSuccess) {
+      ctx->pool = nullptr;
+      cudaGetLastError();
+      return fail(ctx, MOE_ENOMEM, "pinned host pool of %zu bytes", pb);
+    }
+    ctx->pool_bytes = pb;
+  }
+  ctx->residency = residency;
+  if (!Ls.router_w) CK(cudaMalloc(&Ls.router_w, static_cast<size_t>(c.n_experts) * c.d * 2));
+  if (!Ls.shared) CK(cudaMalloc(&Ls.shared, ctx->shared_bytes));
+  if (!pool && !Ls.experts) CK(cudaMalloc(&Ls.experts, static_cast<size_t>(c.n_experts) * ctx->stride));
+  if (pool && !Ls.slot_of_expert) CK(cudaMalloc(&Ls.slot_of_expert, static_cast<size_t>(c.n_experts) * 4));
+  CK(cudaMemcpy(Ls.router_w, router_w, static_cast<size_t>(c.n_experts) * c.d * 2, cudaMemcpyDefault));
+
+  // canonical staging buffers (largest f), then repack on the device
+  const int fmax = std::max(c.f, c.f_shared);
+  const size_t q_b = static_cast<size_t>(fmax) * c.d / 2;
+  const size_t sb_b = static_cast<size_t>(fmax) * (c.d / 64) * 4;
+  uint8_t* can = nullptr;
+  CK(cudaMalloc(&can, 3 * q_b + 3 * sb_b));
+  uint8_t* tmp = nullptr;
+  if (pool) {
+    cudaError_t e = cudaMalloc(&tmp, static_cast<size_t>(c.n_experts) * ctx->stride);
+    if (e != cudaSuccess) {
+      cudaFree(can);
+      return fail(ctx, MOE_ECUDA, "staging buffer: %s", cudaGetErrorString(e));
+    }
+  }
+  auto stage = [&](const moe_expert_weights& w, int f, uint8_t* dst) -> cudaError_t {
+    const size_t gq = static_cast<size_t>(f) * c.d / 2, gsb = static_cast<size_t>(f) * (c.d / 64) * 4;
+    const size_t dsb = static_cast<size_t>(c.d) * (f / 64) * 4;
+    uint8_t* p_gq = can;
+    uint8_t* p_uq = can + q_b;
+    uint8_t* p_dq = can + 2 * q_b;
+    uint8_t* p_gs = can + 3 * q_b;
+    uint8_t* p_us = p_gs + sb_b;
+    uint8_t* p_ds = p_us + sb_b;
+    cudaError_t e;
+    if ((e = cudaMemcpy(p_gq, w.gate_q, gq, cudaMemcpyDefault)) != cudaSuccess) return e;
+    if ((e = cudaMemcpy(p_uq, w.up_q, gq, cudaMemcpyDefault)) != cudaSuccess) return e;
+    if ((e = cudaMemcpy(p_dq, w.down_q, gq, cudaMemcpyDefault)) != cudaSuccess) return e;
+    if ((e = cudaMemcpy(p_gs, w.gate_sb, gsb, cudaMemcpyDefault)) != cudaSuccess) return e;
+    if ((e = cudaMemcpy(p_us, w.up_sb, gsb, cudaMemcpyDefault)) != cudaSuccess) return e;
+    if ((e = cudaMemcpy(p_ds, w.down_sb, dsb, cudaMemcpyDefault)) != cudaSuccess) return e;
+    return launch_repack(p_gq, reinterpret_cast<uint16_t*>(p_gs), p_uq, reinterpret_cast<uint16_t*>(p_us), p_dq,
+                         reinterpret_cast<uint16_t*>(p_ds), c.d, f, dst, nullptr);
+  };
+  cudaError_t e = stage(*shared, c.f_shared, Ls.shared);
+  for (int ex = 0; ex < c.n_experts && e == cudaSuccess; ++ex) {
+    uint8_t* dst = (pool ? tmp : Ls.experts) + static_cast<size_t>(ex) * ctx->stride;
+    e = stage(experts[ex], c.f, dst);
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess && pool)
+    e = cudaMemcpy(ctx->pool + static_cast<size_t>(layer) * c.n_experts * ctx->stride, tmp,
+                   static_cast<size_t>(c.n_experts) * ctx->stride, cudaMemcpyDeviceToHost);
+  cudaFree(can);
+  if (tmp) cudaFree(tmp);
+  if (e != cudaSuccess) return fail(ctx, MOE_ECUDA, "init_layer %d: %s", layer, cudaGetErrorString(e));
+  if (pool && ctx->n_slots > 0 && Ls.slot_of_expert) CK(cudaMemset(Ls.slot_of_expert, 0xFF, c.n_experts * 4));
+  Ls.ready = true;
+  return MOE_OK;
+}
+
+moe_status moe_set_slots(moe_ctx* ctx, int n_slots) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  const moe_config& c = ctx->cfg;
+  if (ctx->residency != MOE_HOST_POOL) return fail(ctx, MOE_ESTATE, "slots need a host-pool context");
+  if (n_slots < c.top_k || n_slots > c.n_experts)
+    return fail(ctx, MOE_EINVAL, "n_slots %d outside [top_k=%d, n_experts=%d]", n_slots, c.top_k, c.n_experts);
+  CK(cudaSetDevice(ctx->device));
+  CK(cudaDeviceSynchronize());
+  const size_t per_layer = static_cast<size_t>(n_slots) * ctx->stride + static_cast<size_t>(n_slots) * 12;
+  const size_t need = per_layer * c.n_layers;
+  size_t have = 0;
+  for (auto& Ls : ctx->L)
+    if (Ls.slots) have += static_cast<size_t>(ctx->n_slots) * ctx->stride + static_cast<size_t>(ctx->n_slots) * 12;
+  size_t free_b = 0, total_b = 0;
+  CK(cudaMemGetInfo(&free_b, &total_b));
+  if (need > free_b + have || need + (256u << 20) > free_b + have)
+    return fail(ctx, MOE_ENOMEM, "%d slots x %d layers need %zu bytes, %zu available", n_slots, c.n_layers, need,
+                free_b + have);
+  for (auto& Ls : ctx->L) {
+    cudaFree(Ls.slots);
+    cudaFree(Ls.expert_of_slot);
+    cudaFree(Ls.last_use);
+    Ls.slots = nullptr;
+    Ls.expert_of_slot = nullptr;
+    Ls.last_use = nullptr;
+  }
+  ctx->n_slots = 0;
+  for (auto& Ls : ctx->L) {
+    CK(cudaMalloc(&Ls.slots, static_cast<size_t>(n_slots) * ctx->stride));
+    CK(cudaMalloc(&Ls.expert_of_slot, static_cast<size_t>(n_slots) * 4));
+    CK(cudaMalloc(&Ls.last_use, static_cast<size_t>(n_slots) * 8));
+    if (!Ls.slot_of_expert) CK(cudaMalloc(&Ls.slot_of_expert, static_cast<size_t>(c.n_experts) * 4));
+  }
+  ctx->n_slots = n_slots;
+  return moe_reset_cache(ctx);
+}
+
+moe_status moe_reset_cache(moe_ctx* ctx) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  CK(cudaSetDevice(ctx->device));
+  CK(cudaDeviceSynchronize());
+  const moe_config& c = ctx->cfg;
+  for (auto& Ls : ctx->L) {
+    if (Ls.slot_of_expert) CK(cudaMemset(Ls.slot_of_expert, 0xFF, static_cast<size_t>(c.n_experts) * 4));
+    if (Ls.expert_of_slot) CK(cudaMemset(Ls.expert_of_slot, 0xFF, static_cast<size_t>(ctx->n_slots) * 4));
+    if (Ls.last_use) CK(cudaMemset(Ls.last_use, 0xFF, static_cast<size_t>(ctx->n_slots) * 8));
+  }
+  CK(cudaMemset(ctx->lru_counts, 0, static_cast<size_t>(c.n_layers) * 16));
+  ctx->step = 0;
+  ctx->steps = 0;
+  ctx->staged = 0;
+  return MOE_OK;
+}
+
+moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begin, int layer_end,
+                           const float* logit_bias, void* h_out, float* y_last, moe_trace_rec* trace, int trace_cap,
+                           int* trace_len, void* stream) {
+  moe_status st = check_ready(ctx, layer_begin, layer_end);
+  if (st != MOE_OK) return st;
+  if (!h_in || !h_out) return fail(ctx, MOE_EINVAL, "NULL h_in / h_out");
+  const bool pool = ctx->residency == MOE_HOST_POOL;
+  if (B < 1 || B > ctx->Bd) return fail(ctx, MOE_EINVAL, "B=%d outside [1, %d]", B, ctx->Bd);
+  if (pool && B != 1) return fail(ctx, MOE_EINVAL, "host-pool decode takes one token per call");
+  if (pool && ctx->n_slots < ctx->cfg.top_k) return fail(ctx, MOE_ESTATE, "slots are not set");
+  if (trace && trace_cap < 0) return fail(ctx, MOE_EINVAL, "negative trace_cap");
+  if (trace_len) *trace_len = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CK(cudaSetDevice(ctx->device));
+  st = put_args(ctx, make_args(ctx, h_in, h_out, y_last, logit_bias, B, B, 0), s);
+  if (st != MOE_OK) return st;
+  if (pool) {
+    st = pool_run(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len);
+    ++ctx->step;
+    ++ctx->steps;
+    return st;
+  }
+  return resident_run(ctx, B, layer_begin, layer_end, s);
+}
+
+moe_status moe_prefill(moe_ctx* ctx, const void* h, int T, int layer_begin, int layer_end, const float* logit_bias,
+                       void* h_out, float* y_last, void* stream) {
+  moe_status st = check_ready(ctx, layer_begin, layer_end);
+  if (st != MOE_OK) return st;
+  if (!h || !h_out) return fail(ctx, MOE_EINVAL, "NULL h / h_out");
+  if (ctx->residency != MOE_RESIDENT_HBM) return fail(ctx, MOE_EINVAL, "prefill needs a resident context");
+  if (T < 1 || T > ctx->cfg.max_tokens) return fail(ctx, MOE_EINVAL, "T=%d outside [1, %d]", T, ctx->cfg.max_tokens);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CK(cudaSetDevice(ctx->device));
+  const int d = ctx->cfg.d, E = ctx->cfg.n_experts;
+  for (int t0 = 0; t0 < T; t0 += ctx->Bd) {
+    const int B = std::min(ctx->Bd, T - t0);
+    const uint16_t* hi = static_cast<const uint16_t*>(h) + static_cast<size_t>(t0) * d;
+    uint16_t* ho = static_cast<uint16_t*>(h_out) + static_cast<size_t>(t0) * d;
+    float* yl = y_last ? y_last + static_cast<size_t>(t0) * d : nullptr;
+    DevCallArgs a = make_args(ctx, hi, ho, yl, logit_bias, B, T, t0);
+    st = put_args(ctx, a, s);
+    if (st != MOE_OK) return st;
+    (void)E;
+    st = resident_run(ctx, B, layer_begin, layer_end, s);
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_set_debug(moe_ctx* ctx, uint16_t* x_layers, int32_t* ids, float* gates, float* y_layers,
+                         int max_layers) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  if (max_layers < 0) return fail(ctx, MOE_EINVAL, "negative max_layers");
+  ctx->dbg_x = x_layers;
+  ctx->dbg_ids = ids;
+  ctx->dbg_gates = gates;
+  ctx->dbg_y = y_layers;
+  ctx->dbg_layers = max_layers;
+  return MOE_OK;
+}
+
+moe_status moe_sync(moe_ctx* ctx, void* stream) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  CK(cudaSetDevice(ctx->device));
+  CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  CK(cudaStreamSynchronize(ctx->side));
+  uint32_t w = 0;
+  CK(cudaMemcpy(&w, ctx->err_word, 4, cudaMemcpyDeviceToHost));
+  if (w) CK(cudaMemset(ctx->err_word, 0, 4));
+  if (w & ERR_WAIT_TIMEOUT) return fail(ctx, MOE_ETIMEOUT, "a device wait ran out (error word 0x%x)", w);
+  if (w & ERR_PLAN) return fail(ctx, MOE_ECUDA, "device plan overflow (error word 0x%x)", w);
+  if (w & ERR_ROUTER_DOMAIN) return fail(ctx, MOE_EDOMAIN, "router input outside the exact fixed-point domain");
+  return MOE_OK;
+}
+
+moe_status moe_get_stats(moe_ctx* ctx, moe_stats* out) {
+  if (!ctx || !out) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  CK(cudaSetDevice(ctx->device));
+  CK(cudaDeviceSynchronize());
+  std::vector<long long> cnt(static_cast<size_t>(ctx->cfg.n_layers) * 2);
+  CK(cudaMemcpy(cnt.data(), ctx->lru_counts, cnt.size() * 8, cudaMemcpyDeviceToHost));
+  memset(out, 0, sizeof(*out));
+  for (int l = 0; l < ctx->cfg.n_layers; ++l) {
+    out->hits += cnt[2 * l];
+    out->misses += cnt[2 * l + 1];
+  }
+  out->steps = ctx->steps;
+  out->staged_bytes = ctx->staged;
+  out->n_slots = ctx->n_slots;
+  out->expert_bytes = ctx->expert_bytes;
+  out->shared_bytes = ctx->shared_bytes;
+  size_t dev = ctx->device_bytes;
+  for (auto& Ls : ctx->L) {
+    if (Ls.router_w) dev += static_cast<size_t>(ctx->cfg.n_experts) * ctx->cfg.d * 2;
+    if (Ls.shared) dev += ctx->shared_bytes;
+    if (Ls.experts) dev += static_cast<size_t>(ctx->cfg.n_experts) * ctx->stride;
+    if (Ls.slots) dev += static_cast<size_t>(ctx->n_slots) * ctx->stride;
+  }
+  out->device_bytes = static_cast<int64_t>(dev);
+  out->host_pool_bytes = static_cast<int64_t>(ctx->pool_bytes);
+  return MOE_OK;
+}
+
+moe_status moe_get_cache_state(moe_ctx* ctx, int layer, int32_t* expert_of_slot, int64_t* last_use) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  if (layer < 0 || layer >= ctx->cfg.n_layers) return fail(ctx, MOE_EINVAL, "layer %d out of range", layer);
+  if (ctx->residency != MOE_HOST_POOL || ctx->n_slots == 0) return fail(ctx, MOE_ESTATE, "no slot cache");
+  CK(cudaSetDevice(ctx->device));
+  CK(cudaDeviceSynchronize());
+  if (expert_of_slot)
+    CK(cudaMemcpy(expert_of_slot, ctx->L[layer].expert_of_slot, ctx->n_slots * 4, cudaMemcpyDeviceToHost));
+  if (last_use) CK(cudaMemcpy(last_use, ctx->L[layer].last_use, ctx->n_slots * 8, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+moe_status moe_profile(moe_ctx* ctx, int enable) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  ctx->profiling = enable != 0;
+  ctx->prof_n = 0;
+  return MOE_OK;
+}
+
+moe_status moe_get_profile(moe_ctx* ctx, moe_kernel_time* out, int n) {
+  if (!ctx || !out || n < 0) return MOE_EINVAL;
+  for (int i = 0; i < n && i < MOE_N_KERNEL_KINDS; ++i) {
+    out[i] = ctx->prof[i];
+    ctx->prof[i] = moe_kernel_time{};
+  }
+  return MOE_OK;
+}
+
+moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
+  if (!ctx) return MOE_EINVAL;
+  switch (hook) {
+    case 1: ctx->hook_fail_copy = value != 0; return MOE_OK;
+    case 2:
+      if (value < 0) return fail(ctx, MOE_EINVAL, "negative wait limit");
+      ctx->wait_limit_us = value;
+      return MOE_OK;
+    case 3: {  // programmatic dependent launch on/off
+      const bool want = value != 0;
+      if (want != ctx->pdl) {
+        for (auto& kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
+        ctx->graphs.clear();
+        ctx->pdl = want;
+      }
+      return MOE_OK;
+    }
+    default: return fail(ctx, MOE_EINVAL, "unknown hook %d", hook);
+  }
+}
+
+}  // extern "C"

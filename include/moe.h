@@ -1,0 +1,237 @@
+/*
+ * libmoe — routed mixture-of-experts FFN of a decode step, on one GB300 (sm_103a).
+ *
+ * Per layer and token the library computes what the TurboFieldfare write-up
+ * ("Optimizing a 14.3 GB model for an 8 GB machine") and its video
+ * walkthrough describe for Gemma 4 26B-A4B:
+ *
+ *   - a router over E experts whose top k run ("the router picks the top
+ *     eight [of 128] and only those eight run", video transcript), with
+ *     softmax gates over the k picked logits;
+ *   - for each picked expert and for the always-on shared expert ("one shared
+ *     expert that always runs", same transcript): an int4-affine gate and up
+ *     projection (groups of 64 inputs with a 16-bit scale and bias each,
+ *     section "Vectorization helped when it respected the storage layout"),
+ *     the GELU-gated product GELU(gate) * up, and the down projection;
+ *   - the combine y = y_shared + sum_j gate_j * y_{e_j};
+ *   - optionally, a per-layer bounded expert-slot cache with LRU eviction
+ *     that stages missing experts into fixed device slots (section "MoE
+ *     needed parallel work, reuse, and coarse overlap"; goinfer, "When the
+ *     model doesn't fit"), the copies overlapped with the shared expert.
+ *
+ * Conventions for every entry point:
+ *   - Every call returns a moe_status and never aborts, throws or exits.
+ *   - Argument errors (MOE_EINVAL) are detected before anything is enqueued
+ *     or allocated.
+ *   - A failed CUDA call or an expired bounded wait poisons the context:
+ *     every later call on it returns MOE_ESTATE until moe_destroy.
+ *   - One context is used by one host thread at a time.
+ *   - "device" pointers are CUDA device (or managed) memory on the context's
+ *     device; "host" pointers are ordinary or pinned host memory.
+ *   - Nothing in the library ever falls back to a CPU implementation.
+ */
+#ifndef LIBMOE_MOE_H
+#define LIBMOE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx moe_ctx; /* opaque, owned by the library */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_EINVAL = 1,   /* invalid argument; nothing enqueued, nothing changed */
+    MOE_ENOMEM = 2,   /* computed budget exceeds free device memory, or an allocation failed;
+                         the context is unchanged */
+    MOE_ECUDA = 3,    /* a CUDA call failed; the context is now poisoned */
+    MOE_ESTATE = 4,   /* poisoned context, or a call in the wrong state (layer not initialised,
+                         slots not set) */
+    MOE_ETIMEOUT = 5, /* a bounded wait expired; the context is now poisoned */
+    MOE_EDOMAIN = 6   /* the device saw a router input outside the exact fixed-point domain
+                         (|W_r[e,i] * x[i]| >= 2^11 or non-finite); reported by moe_sync */
+} moe_status;
+
+enum { MOE_RESIDENT_HBM = 0, MOE_HOST_POOL = 1 };
+enum { MOE_GELU_ERF = 0, MOE_GELU_TANH = 1 };
+
+/* Model dimensions.  Constraints (checked by moe_create): d, f and f_shared
+ * are multiples of 64; group == 64; 1 <= top_k <= n_experts <= 256;
+ * d <= 3072 (keeps the int64 router sum exact); n_layers >= 1;
+ * 1 <= max_tokens <= 65536. */
+typedef struct {
+    int32_t d;            /* hidden size */
+    int32_t f;            /* routed-expert intermediate size */
+    int32_t f_shared;     /* shared-expert intermediate size */
+    int32_t n_experts;    /* E */
+    int32_t top_k;        /* k */
+    int32_t group;        /* int4 affine group length along the input dimension (64) */
+    int32_t n_layers;     /* layers held by the context */
+    int32_t gelu_variant; /* MOE_GELU_ERF (exact erf form) or MOE_GELU_TANH */
+    int32_t prenorm;      /* 1: a layer's FFN input is x = bf16(h / sqrt(mean(h^2) + norm_eps));
+                             0: the FFN input is h itself */
+    int32_t max_tokens;   /* largest B of moe_decode_step and T of moe_prefill */
+    float norm_eps;       /* epsilon of the RMS normalisation (used when prenorm = 1) */
+} moe_config;
+
+/* One expert's weights in canonical layout.  Every projection is row-major
+ * [out][in]; int4 values are unsigned 0..15 packed two per byte (byte m of a
+ * row holds element 2m in its low nibble, 2m+1 in its high nibble); each run
+ * of 64 consecutive inputs of a row has an fp16 (scale, bias) pair, stored
+ * sb[row][in/64][2]; the weight is scale * q + bias.
+ *   gate_q [f][d/2]  gate_sb [f][d/64][2]
+ *   up_q   [f][d/2]  up_sb   [f][d/64][2]
+ *   down_q [d][f/2]  down_sb [d][f/64][2]
+ * (f is f_shared for the shared expert.) */
+typedef struct {
+    const uint8_t *gate_q;
+    const uint16_t *gate_sb;
+    const uint8_t *up_q;
+    const uint16_t *up_sb;
+    const uint8_t *down_q;
+    const uint16_t *down_sb;
+} moe_expert_weights;
+
+/* One record per (token step, layer, top-k position) of the slot cache. */
+typedef struct {
+    int32_t token;   /* step counter value of the decode call (see moe_decode_step) */
+    int32_t layer;
+    int32_t k_pos;   /* top-k position j, 0 = highest logit */
+    int32_t expert;  /* picked expert */
+    int32_t hit;     /* 1 if the expert was already in a slot */
+    int32_t slot;    /* slot index that holds it after the step */
+    int32_t evicted; /* expert that a miss replaced, or -1 (slot was empty, or hit) */
+} moe_trace_rec;
+
+typedef struct {
+    int64_t steps;         /* decode calls on a host-pool context since create/reset */
+    int64_t hits;          /* summed over layers */
+    int64_t misses;
+    int64_t staged_bytes;  /* host-pool -> slot bytes copied */
+    int64_t n_slots;
+    int64_t expert_bytes;  /* bytes of one routed expert (device layout == canonical size) */
+    int64_t shared_bytes;
+    int64_t device_bytes;  /* device memory held by the context */
+    int64_t host_pool_bytes;
+} moe_stats;
+
+/* Create a context on CUDA device `device`.  Allocates the per-call scratch
+ * sized for cfg->max_tokens.  MOE_EINVAL on a bad config, MOE_ENOMEM if the
+ * scratch does not fit. */
+moe_status moe_create(const moe_config *cfg, int device, moe_ctx **out);
+
+/* Copy one layer's weights into the context (synchronous; the caller may free
+ * its buffers on return).  Pointers may be host or device memory.
+ *   router_w: fp16 [n_experts][d], row-major
+ *   experts:  array of n_experts moe_expert_weights (canonical layout above)
+ *   shared:   the shared expert (intermediate size f_shared)
+ *   residency: MOE_RESIDENT_HBM keeps every expert in device memory;
+ *              MOE_HOST_POOL keeps routed experts in a pinned host pool and
+ *              serves them from per-layer device slots (see moe_set_slots).
+ *              All layers of a context use the same residency.
+ * The library repacks the weights into its own device layout: a permutation
+ * of the same bytes (nibbles and (scale, bias) pairs), never a re-encoding. */
+moe_status moe_init_layer(moe_ctx *ctx, int layer, const uint16_t *router_w,
+                          const moe_expert_weights *experts, const moe_expert_weights *shared,
+                          int residency);
+
+/* Host-pool contexts: give every layer n_slots device slots (top_k <= n_slots
+ * <= n_experts) and empty the LRU tables.  The byte budget
+ * n_layers * n_slots * expert_bytes is checked against free device memory
+ * before anything is allocated (MOE_ENOMEM, context unchanged). */
+moe_status moe_set_slots(moe_ctx *ctx, int n_slots);
+
+/* Run layers [layer_begin, layer_end) for B tokens, each layer
+ *   x = prenorm ? bf16(RMSNorm(h)) : h;  y = MoE-FFN(x);  h <- bf16(h + y).
+ *   h_in:  device bf16 [B][d] residual entering layer_begin (not modified)
+ *   h_out: device bf16 [B][d] residual after layer_end - 1 (may equal h_in)
+ *   logit_bias: device fp32 [layer_end - layer_begin][B][n_experts] added to the
+ *          router logits, or NULL
+ *   y_last: device fp32 [B][d], the FFN output y of the last layer, or NULL
+ *   trace / trace_cap / trace_len: host-pool contexts only, host array that
+ *          receives (layer_end - layer_begin) * top_k records, or NULL
+ *   stream: cudaStream_t to run on (NULL = legacy default stream)
+ * Resident contexts accept 1 <= B <= min(max_tokens, 64) and return without
+ * synchronising.  Host-pool contexts need B == 1 and slots set; every call is
+ * one LRU step (the step counter increments per call) and the call returns
+ * after the last layer's staging decision, with the compute still enqueued.
+ * Waits inside the call are bounded (MOE_ETIMEOUT). */
+moe_status moe_decode_step(moe_ctx *ctx, const void *h_in, int B, int layer_begin, int layer_end,
+                           const float *logit_bias, void *h_out, float *y_last, moe_trace_rec *trace,
+                           int trace_cap, int *trace_len, void *stream);
+
+/* Prefill: T tokens at once through layers [layer_begin, layer_end), same
+ * per-layer arithmetic as moe_decode_step.  Resident contexts only,
+ * 1 <= T <= max_tokens.  Tokens are permuted by expert, each expert's tokens
+ * run through a grouped int4 -> bf16 tensor-core GEMM, and the outputs are
+ * combined per token in top-k order. */
+moe_status moe_prefill(moe_ctx *ctx, const void *h, int T, int layer_begin, int layer_end,
+                       const float *logit_bias, void *h_out, float *y_last, void *stream);
+
+/* Capture per-layer values of the next decode/prefill calls into caller device
+ * buffers (any may be NULL; max_layers bounds the layers written):
+ *   x_layers  bf16 [max_layers][B][d]   FFN input of each layer
+ *   ids       int32 [max_layers][B][k]  picked experts, top-k order
+ *   gates     fp32 [max_layers][B][k]
+ *   y_layers  fp32 [max_layers][B][d]   FFN output of each layer
+ * Pass all NULL to stop capturing. */
+moe_status moe_set_debug(moe_ctx *ctx, uint16_t *x_layers, int32_t *ids, float *gates,
+                         float *y_layers, int max_layers);
+
+/* Synchronise `stream`, then report device-side conditions raised since the
+ * last moe_sync: MOE_EDOMAIN (router input domain), MOE_ETIMEOUT (a device
+ * wait ran out; poisons).  Clears the reported conditions. */
+moe_status moe_sync(moe_ctx *ctx, void *stream);
+
+moe_status moe_get_stats(moe_ctx *ctx, moe_stats *out);
+
+/* Host-pool contexts: copy layer `layer`'s slot table to host arrays of
+ * n_slots entries (expert_of_slot: -1 = empty; last_use: step counter, -1 = empty). */
+moe_status moe_get_cache_state(moe_ctx *ctx, int layer, int32_t *expert_of_slot, int64_t *last_use);
+
+/* Empty every LRU table, zero the counters and the step counter. */
+moe_status moe_reset_cache(moe_ctx *ctx);
+
+/* Bytes of one routed expert / of the shared expert for a config (0 on a bad config). */
+int64_t moe_expert_bytes(const moe_config *cfg);
+int64_t moe_shared_bytes(const moe_config *cfg);
+
+/* Per-kernel timing.  While enabled, decode and prefill calls launch their
+ * kernels one by one (no graph replay), record a CUDA event pair around every
+ * launch on the call's stream, and synchronise that stream before returning
+ * to add the durations to the running totals.  kind: 0 router/top-k/plan,
+ * 1 gate/up GEMV, 2 down GEMV + combine, 3.. prefill kernels. */
+typedef struct {
+    int64_t launches;
+    double total_ms;
+} moe_kernel_time;
+
+#define MOE_N_KERNEL_KINDS 8
+
+moe_status moe_profile(moe_ctx *ctx, int enable);
+
+/* Copy min(n, MOE_N_KERNEL_KINDS) totals to out and reset them. */
+moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
+
+/* Test hook.  hook 1: the next host-pool staging copy reports a CUDA error
+ * (the call returns MOE_ECUDA and poisons the context).  hook 2: host waits
+ * use a limit of `value` microseconds.  hook 3: programmatic dependent launch
+ * between consecutive kernels on (value != 0, the default) or off.  Other
+ * hooks: MOE_EINVAL. */
+moe_status moe_test_hook(moe_ctx *ctx, int hook, int64_t value);
+
+const char *moe_status_string(moe_status s);
+
+/* Last error message of the context (static string if ctx is NULL). */
+const char *moe_last_error(const moe_ctx *ctx);
+
+void moe_destroy(moe_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMOE_MOE_H */
