@@ -79,6 +79,8 @@ _SIGS = {
     "moe_expert_bytes": (C.c_int64, [C.POINTER(MoeConfig)]),
     "moe_shared_bytes": (C.c_int64, [C.POINTER(MoeConfig)]),
     "moe_test_hook": (C.c_int, [C.c_void_p, C.c_int, C.c_int64]),
+    "moe_route_noalloc": (C.c_int, [C.POINTER(MoeConfig), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                    C.c_void_p, C.c_void_p, C.c_void_p]),
     "moe_profile": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_get_profile": (C.c_int, [C.c_void_p, C.POINTER(MoeKernelTime), C.c_int]),
     "moe_status_string": (C.c_char_p, [C.c_int]),
@@ -222,6 +224,15 @@ def moe_shared_bytes(cfg: MoeConfig) -> int:
 
 def moe_test_hook(ctx, hook: int, value: int) -> int:
     return lib().moe_test_hook(ctx, hook, value)
+
+
+ROUTE_NOALLOC_MAX_B = 64
+
+
+def moe_route_noalloc(cfg: MoeConfig, router_w, h, B: int, logit_bias, ids, gates, stream=None) -> int:
+    """Routing without any device allocation (see include/moe.h); every buffer is the caller's."""
+    return lib().moe_route_noalloc(C.byref(cfg), _ptr(router_w), _ptr(h), B, _ptr(logit_bias), _ptr(ids),
+                                   _ptr(gates), _stream(stream))
 
 
 def moe_profile(ctx, enable: bool) -> int:

@@ -199,6 +199,35 @@ moe_status moe_reset_cache(moe_ctx *ctx);
 int64_t moe_expert_bytes(const moe_config *cfg);
 int64_t moe_shared_bytes(const moe_config *cfg);
 
+/* Routing only (logits, top-k, gates) without any device allocation.  The
+ * write-ups this library follows have no counterpart to this call.  It is for
+ * callers that cannot call cudaMalloc where they route: a host that reserves
+ * all device memory up front and forbids later allocation, or a real-time
+ * serving loop that cannot afford cudaMalloc's blocking, its implicit device
+ * synchronisation or its failure under memory pressure.  The caller passes
+ * every input and output; the arithmetic is that of the router phase of
+ * moe_decode_step (optional RMS norm, exact fixed-point logits, top-k with
+ * lower-index ties, softmax gates over the k picked).
+ *   cfg:        d, n_experts (<= 256), top_k, group, prenorm and norm_eps are used
+ *   router_w:   device fp16 [n_experts][d]
+ *   h:          device bf16 [B][d]
+ *   logit_bias: device fp32 [B][n_experts], or NULL
+ *   ids:        device int32 [B][top_k] (output); gates: device fp32 [B][top_k] (output)
+ *   B:          1 <= B <= MOE_ROUTE_NOALLOC_MAX_B; a larger B returns MOE_EINVAL
+ * Runs on the current CUDA device, on `stream`.  Its only scratch is a fixed
+ * 131,328-byte device array that every GPU loading this library holds until
+ * the process exits.  The first call on each device looks up that array's
+ * address once (cudaGetSymbolAddress), so make the first call on a device
+ * before any stream capture.  All calls share the array and it keeps the last
+ * call's contents: calls that overlap on the GPU (unordered streams) race.
+ * Router products outside the exact domain (|W_r[e,i] * x[i]| >= 2^11) are
+ * dropped rather than reported.  Returns MOE_EINVAL or MOE_ECUDA on failure
+ * (there is no context to poison). */
+#define MOE_ROUTE_NOALLOC_MAX_B 64
+
+moe_status moe_route_noalloc(const moe_config *cfg, const uint16_t *router_w, const void *h, int B,
+                             const float *logit_bias, int32_t *ids, float *gates, void *stream);
+
 /* Per-kernel timing.  While enabled, decode and prefill calls launch their
  * kernels one by one (no graph replay), record a CUDA event pair around every
  * launch on the call's stream, and synchronise that stream before returning
