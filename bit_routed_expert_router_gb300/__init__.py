@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTATE, MOE_ETIMEOUT, MOE_EDOMAIN = range(7)
 MOE_RESIDENT_HBM, MOE_HOST_POOL = 0, 1
 MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
-HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL = 1, 2, 3
+HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6
 
 
 class MoeConfig(C.Structure):
@@ -49,7 +49,7 @@ class MoeKernelTime(C.Structure):
 
 
 N_KERNEL_KINDS = 8
-KERNEL_KINDS = {0: "router_topk_plan", 1: "gateup_gelu_gemv", 2: "down_combine_gemv"}
+KERNEL_KINDS = {0: "router_topk_plan", 1: "gateup_gelu_gemv", 2: "down_combine_gemv", 3: "decode_persistent"}
 
 
 class MoeError(RuntimeError):
@@ -104,9 +104,13 @@ def lib():
     return _lib
 
 
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
 def status_name(status: int) -> str:
     try:
-        return lib().moe_status_string(int(status)).decode()
+        return moe_status_string(status)
     except Exception:  # pragma: no cover
         return f"status {status}"
 

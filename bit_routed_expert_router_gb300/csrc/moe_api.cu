@@ -101,9 +101,24 @@ struct moe_ctx {
   long long step = 0, steps = 0, staged = 0;
   // hooks
   bool hook_fail_copy = false;
+  bool hook_force_timeout = false;     // the next host wait reports a timeout
+  long long hook_free_bytes = -1;      // >= 0: budget checks use this as free device memory
   long long wait_limit_us = 20000000;
   bool pdl = true;
   std::map<std::tuple<int, int, int>, cudaGraphExec_t> graphs;
+  // persistent decode kernel (resident, B = 1)
+  bool use_persistent = true;
+  bool p_ok = false;                   // one CTA per SM fits
+  PLayer* p_layers = nullptr;          // device [n_layers]
+  long long* p_logits = nullptr;
+  unsigned* p_counters = nullptr;
+  int p_n_counters = 0;
+  unsigned* p_exit = nullptr;          // exit counter, abort flag
+  uint16_t *p_a_s = nullptr, *p_a_r = nullptr;
+  float *p_asum_s = nullptr, *p_asum_r = nullptr, *p_part = nullptr;
+  int p_n_sc = 1;
+  float* p_gates = nullptr;            // [n_layers][k]
+  unsigned long long* p_timeline = nullptr;   // caller device buffer [n_layers][16], test hook 5
   // per-kernel timing
   bool profiling = false;
   std::vector<cudaEvent_t> prof_ev;
@@ -165,6 +180,11 @@ long long now_us() {
 
 // Bounded host wait on an event.
 moe_status wait_event(moe_ctx* ctx, cudaEvent_t ev, const char* what) {
+  if (ctx->hook_force_timeout) {
+    ctx->hook_force_timeout = false;
+    cudaEventSynchronize(ev);  // leave no work of ours in flight
+    return fail(ctx, MOE_ETIMEOUT, "waiting for %s: time limit (forced by test hook)", what);
+  }
   const long long t0 = now_us();
   int spins = 0;
   for (;;) {
@@ -174,6 +194,13 @@ moe_status wait_event(moe_ctx* ctx, cudaEvent_t ev, const char* what) {
     if (now_us() - t0 > ctx->wait_limit_us) return fail(ctx, MOE_ETIMEOUT, "waiting for %s: time limit", what);
     if (++spins > 64) std::this_thread::yield();
   }
+}
+
+cudaError_t free_device_bytes(moe_ctx* ctx, size_t* free_b) {
+  size_t total_b = 0;
+  cudaError_t e = cudaMemGetInfo(free_b, &total_b);
+  if (e == cudaSuccess && ctx->hook_free_bytes >= 0) *free_b = static_cast<size_t>(ctx->hook_free_bytes);
+  return e;
 }
 
 KParams base_params(moe_ctx* ctx, int layer, int rel, int first, int last, int B) {
@@ -341,6 +368,51 @@ moe_status check_ready(moe_ctx* ctx, int l0, int l1) {
   for (int l = l0; l < l1; ++l)
     if (!ctx->L[l].ready) return fail(ctx, MOE_ESTATE, "layer %d is not initialised", l);
   return MOE_OK;
+}
+
+// Resident decode of one token through [l0, l1) with the persistent kernel.
+moe_status persistent_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
+  PParams p{};
+  p.d = c.d;
+  p.f = c.f;
+  p.fs = c.f_shared;
+  p.E = c.n_experts;
+  p.k = c.top_k;
+  p.prenorm = c.prenorm;
+  p.gelu = c.gelu_variant;
+  p.eps = c.norm_eps;
+  p.l0 = l0;
+  p.l1 = l1;
+  p.n_sc = ctx->p_n_sc;
+  p.expert_stride = ctx->stride;
+  p.layers = ctx->p_layers;
+  p.args = ctx->dargs;
+  p.hbuf0 = ctx->hbuf[0];
+  p.hbuf1 = ctx->hbuf[1];
+  p.logits = ctx->p_logits;
+  p.counters = ctx->p_counters;
+  p.n_counters = ctx->p_n_counters;
+  const int pparts = ctx->p_n_sc + c.top_k;
+  p.logit_cnt = ctx->p_counters;
+  p.gu_cnt = p.logit_cnt + c.n_layers;
+  p.row_cnt = p.gu_cnt + static_cast<size_t>(c.n_layers) * pparts;
+  p.rows_done = p.row_cnt + static_cast<size_t>(c.n_layers) * (c.d / 16);
+  p.exit_cnt = ctx->p_exit;
+  p.abort_flag = ctx->p_exit + 1;
+  p.a_s = ctx->p_a_s;
+  p.a_r = ctx->p_a_r;
+  p.asum_s = ctx->p_asum_s;
+  p.asum_r = ctx->p_asum_r;
+  p.part = ctx->p_part;
+  p.err = ctx->err_word;
+  p.timeline = ctx->p_timeline;
+  p.gates_g = ctx->p_gates;
+  p.n_layers_tl = c.n_layers;
+  PROF(3, s);
+  CK(launch_persistent(p, ctx->n_sm, s));
+  PROF(-1, s);
+  return prof_collect(ctx, s);
 }
 
 // Resident decode of B tokens through [l0, l1): one graph launch (or, while
@@ -539,6 +611,19 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->err_word = dalloc<uint32_t>(1, o, nb);
   ctx->lru_counts = dalloc<long long>(static_cast<size_t>(c.n_layers) * 2, o, nb);
   ctx->dargs = dalloc<DevCallArgs>(1, o, nb);
+  ctx->p_n_sc = (c.f_shared / 64 + kPStageGroups - 1) / kPStageGroups;
+  const int pparts = ctx->p_n_sc + c.top_k;
+  ctx->p_n_counters = c.n_layers * (1 + pparts + c.d / 16 + 1);
+  ctx->p_layers = dalloc<PLayer>(c.n_layers, o, nb);
+  ctx->p_logits = dalloc<long long>(static_cast<size_t>(c.n_layers) * c.n_experts, o, nb);
+  ctx->p_counters = dalloc<unsigned>(ctx->p_n_counters, o, nb);
+  ctx->p_exit = dalloc<unsigned>(2, o, nb);
+  ctx->p_a_s = dalloc<uint16_t>(static_cast<size_t>(c.f_shared) * 2, o, nb);
+  ctx->p_a_r = dalloc<uint16_t>(static_cast<size_t>(c.top_k) * c.f * 2, o, nb);
+  ctx->p_asum_s = dalloc<float>(static_cast<size_t>(c.f_shared / 8) * 2, o, nb);
+  ctx->p_asum_r = dalloc<float>(static_cast<size_t>(c.top_k) * (c.f / 8) * 2, o, nb);
+  ctx->p_part = dalloc<float>(static_cast<size_t>(2) * pparts * c.d, o, nb);
+  ctx->p_gates = dalloc<float>(static_cast<size_t>(c.n_layers) * c.top_k, o, nb);
   for (void* ptr : o)
     if (!ptr) return bail(MOE_ENOMEM);
   if (!ctx->hbuf[0] || !ctx->hbuf[1] || !ctx->x_perm || !ctx->dargs || !ctx->y_r || !ctx->part_s || !ctx->a_r)
@@ -547,7 +632,10 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   if (cudaMemset(ctx->tok_cnt, 0, Bd * 4) != cudaSuccess || cudaMemset(ctx->all_cnt, 0, 4) != cudaSuccess ||
       cudaMemset(ctx->row_cnt, 0, (c.d / 16) * 4) != cudaSuccess || cudaMemset(ctx->err_word, 0, 4) != cudaSuccess ||
       cudaMemset(ctx->plan, 0, sizeof(PlanHdr)) != cudaSuccess ||
-      cudaMemset(ctx->lru_counts, 0, static_cast<size_t>(c.n_layers) * 16) != cudaSuccess)
+      cudaMemset(ctx->lru_counts, 0, static_cast<size_t>(c.n_layers) * 16) != cudaSuccess ||
+      cudaMemset(ctx->p_counters, 0, static_cast<size_t>(ctx->p_n_counters) * 4) != cudaSuccess ||
+      cudaMemset(ctx->p_exit, 0, 8) != cudaSuccess ||
+      cudaMemset(ctx->p_layers, 0, sizeof(PLayer) * c.n_layers) != cudaSuccess)
     return bail(MOE_ECUDA);
   if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->args_ring), sizeof(DevCallArgs) * kArgRing, cudaHostAllocDefault) !=
       cudaSuccess)
@@ -570,6 +658,21 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   if (gateup_smem(c.d) > static_cast<size_t>(max_smem) || down_smem(ctx->cg, 8) > static_cast<size_t>(max_smem))
     return bail(MOE_EINVAL);
   if (set_kernel_attrs(max_smem) != cudaSuccess) return bail(MOE_ECUDA);
+  // the persistent kernel's shape limits: gate/up tiles of at most 4 chunks of
+  // 11 groups, routed down tiles of one chunk, shared down tiles of at most 4
+  const int n_cta = ctx->n_sm;
+  const int nT = c.d / 16;
+  const int tiles_per_cta = (c.f_shared / 8 + n_cta - 1) / n_cta + (c.top_k * (c.f / 8) + n_cta - 1) / n_cta;
+  const int stages_per_cta = 2 + (c.n_experts + n_cta - 1) / n_cta + tiles_per_cta + (nT + n_cta - 1) / n_cta +
+                             (c.top_k * ((nT + 3) / 4) + n_cta - 1) / n_cta;
+  if (n_cta >= 2 && c.d <= 44 * 64 && c.f_shared <= 44 * 64 && c.f <= 11 * 64 &&
+      tiles_per_cta <= persistent_max_tiles_per_cta() && stages_per_cta <= persistent_max_tasks() &&
+      persistent_smem() + 8192 <= static_cast<size_t>(max_smem)) {
+    int per_sm = 0;
+    if (persistent_attrs() == cudaSuccess && persistent_occupancy(&per_sm) == cudaSuccess && per_sm >= 1)
+      ctx->p_ok = true;
+    cudaGetLastError();
+  }
   if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ECUDA);
   *out = ctx;
   return MOE_OK;
@@ -624,8 +727,8 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
   LayerStore& Ls = ctx->L[layer];
   const bool pool = residency == MOE_HOST_POOL;
   // memory budget before allocating
-  size_t free_b = 0, total_b = 0;
-  CK(cudaMemGetInfo(&free_b, &total_b));
+  size_t free_b = 0;
+  CK(free_device_bytes(ctx, &free_b));
   const size_t fs_can = static_cast<size_t>(c.f_shared) * c.d * 27 / 16 + 64;
   size_t need = static_cast<size_t>(c.n_experts) * c.d * 2 + ctx->shared_bytes + 3 * fs_can;
   need += static_cast<size_t>(c.n_experts) * ctx->stride;  // resident experts or the staging buffer
@@ -693,6 +796,8 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
   if (tmp) cudaFree(tmp);
   if (e != cudaSuccess) return fail(ctx, MOE_ECUDA, "init_layer %d: %s", layer, cudaGetErrorString(e));
   if (pool && ctx->n_slots > 0 && Ls.slot_of_expert) CK(cudaMemset(Ls.slot_of_expert, 0xFF, c.n_experts * 4));
+  PLayer pl{Ls.router_w, Ls.shared, Ls.experts};
+  CK(cudaMemcpy(ctx->p_layers + layer, &pl, sizeof(PLayer), cudaMemcpyHostToDevice));
   Ls.ready = true;
   return MOE_OK;
 }
@@ -711,8 +816,8 @@ moe_status moe_set_slots(moe_ctx* ctx, int n_slots) {
   size_t have = 0;
   for (auto& Ls : ctx->L)
     if (Ls.slots) have += static_cast<size_t>(ctx->n_slots) * ctx->stride + static_cast<size_t>(ctx->n_slots) * 12;
-  size_t free_b = 0, total_b = 0;
-  CK(cudaMemGetInfo(&free_b, &total_b));
+  size_t free_b = 0;
+  CK(free_device_bytes(ctx, &free_b));
   if (need > free_b + have || need + (256u << 20) > free_b + have)
     return fail(ctx, MOE_ENOMEM, "%d slots x %d layers need %zu bytes, %zu available", n_slots, c.n_layers, need,
                 free_b + have);
@@ -775,6 +880,7 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
     ++ctx->steps;
     return st;
   }
+  if (B == 1 && ctx->use_persistent && ctx->p_ok) return persistent_run(ctx, layer_begin, layer_end, s);
   return resident_run(ctx, B, layer_begin, layer_end, s);
 }
 
@@ -895,6 +1001,10 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
   switch (hook) {
     case 1: ctx->hook_fail_copy = value != 0; return MOE_OK;
     case 2:
+      if (value == -1) {
+        ctx->hook_force_timeout = true;
+        return MOE_OK;
+      }
       if (value < 0) return fail(ctx, MOE_EINVAL, "negative wait limit");
       ctx->wait_limit_us = value;
       return MOE_OK;
@@ -907,6 +1017,13 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
       }
       return MOE_OK;
     }
+    case 4: ctx->use_persistent = value != 0; return MOE_OK;  // persistent B = 1 decode kernel on/off
+    case 6:  // budget checks see `value` bytes of free device memory (-1: the real figure)
+      ctx->hook_free_bytes = value;
+      return MOE_OK;
+    case 5:  // event timeline of the persistent kernel into a caller device buffer (0 = off)
+      ctx->p_timeline = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
+      return MOE_OK;
     default: return fail(ctx, MOE_EINVAL, "unknown hook %d", hook);
   }
 }

@@ -232,7 +232,8 @@ moe_status moe_route_noalloc(const moe_config *cfg, const uint16_t *router_w, co
  * kernels one by one (no graph replay), record a CUDA event pair around every
  * launch on the call's stream, and synchronise that stream before returning
  * to add the durations to the running totals.  kind: 0 router/top-k/plan,
- * 1 gate/up GEMV, 2 down GEMV + combine, 3.. prefill kernels. */
+ * 1 gate/up GEMV, 2 down GEMV + combine, 3 persistent one-token decode
+ * (all layers), 4.. prefill kernels. */
 typedef struct {
     int64_t launches;
     double total_ms;
@@ -247,9 +248,17 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
 
 /* Test hook.  hook 1: the next host-pool staging copy reports a CUDA error
  * (the call returns MOE_ECUDA and poisons the context).  hook 2: host waits
- * use a limit of `value` microseconds.  hook 3: programmatic dependent launch
- * between consecutive kernels on (value != 0, the default) or off.  Other
- * hooks: MOE_EINVAL. */
+ * use a limit of `value` microseconds; value -1 makes the next host wait
+ * report a timeout (after letting the awaited work finish).  hook 6: budget
+ * checks see `value` bytes of free device memory (-1 restores the real
+ * figure).  hook 3: programmatic dependent launch
+ * between consecutive kernels on (value != 0, the default) or off.  hook 4:
+ * the single-launch persistent kernel for resident one-token decode on
+ * (value != 0, the default) or off (per-layer kernels).  hook 5: `value` is
+ * the address of a caller device buffer of 2 * n_layers * 16 uint64 into
+ * which the persistent kernel records event times (%globaltimer ns): rows
+ * [0, n_layers) min or max over CTAs, rows [n_layers, 2 n_layers) steps of
+ * the first routed CTA (see persistent.cu), or 0 to stop.  Other hooks: MOE_EINVAL. */
 moe_status moe_test_hook(moe_ctx *ctx, int hook, int64_t value);
 
 const char *moe_status_string(moe_status s);

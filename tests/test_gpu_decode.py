@@ -53,9 +53,11 @@ def _tiny_ctx(shape=TINY, prenorm=0, seed=0, gelu=0):
     return ctx, oracle.Layer(w, shape.top_k, gelu_variant=gelu)
 
 
-def test_tiny_layer_single_tokens():
+@pytest.mark.parametrize("persistent", [1, 0])
+def test_tiny_layer_single_tokens(persistent):
     ctx, lay = _tiny_ctx()
     with ctx:
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PERSISTENT, persistent), ctx.h)
         H = gen_hidden(16, TINY.d, seed=0).cuda()
         for t in range(16):
             _check_layer_outputs(ctx, lay, H[t:t + 1])
@@ -84,6 +86,7 @@ def test_tanh_gelu_variant():
     with ctx:
         H = gen_hidden(4, TINY.d, seed=5).cuda()
         _check_layer_outputs(ctx, lay, H)
+        _check_layer_outputs(ctx, lay, H[1:2])
 
 
 def test_prenorm_input_matches_oracle_rmsnorm():
@@ -103,6 +106,20 @@ def test_odd_shapes_and_uneven_shared_chunks():
     ctx, lay = _tiny_ctx(sh, seed=21)
     with ctx:
         H = gen_hidden(5, sh.d, seed=21).cuda()
+        _check_layer_outputs(ctx, lay, H)
+        for t in range(5):
+            _check_layer_outputs(ctx, lay, H[t:t + 1])
+
+
+def test_long_rows_several_stages_per_task():
+    # d/64 = 24 groups (gate/up tiles span 3 stages), f/64 = 13 (down tiles span 2 stages),
+    # f_shared/64 = 23 (three shared down chunks, the last one short)
+    sh = Shape(d=1536, f=832, f_shared=1472, n_experts=16, top_k=4)
+    ctx, lay = _tiny_ctx(sh, seed=23)
+    with ctx:
+        H = gen_hidden(4, sh.d, seed=23).cuda()
+        for t in range(4):
+            _check_layer_outputs(ctx, lay, H[t:t + 1])
         _check_layer_outputs(ctx, lay, H)
 
 
@@ -192,8 +209,13 @@ def test_full_shape_layer_sampled_tokens():
         for t in range(0, 256, 5):
             lg, st = oracle.router_logits(rw, oracle.as_bits(H[t]))
             assert list(ids_all[t]) == list(oracle.topk(lg, sh.top_k)), f"token {t}"
-        # full FFN parity on sampled single tokens, at the bench launch shape (B = 1)
+        # full FFN parity on sampled single tokens, at the bench launch shape (B = 1),
+        # through the persistent kernel and through the per-layer kernels
         for t in (0, 1, 517, 1023):
             _check_layer_outputs(ctx, lay, H[t:t + 1])
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PERSISTENT, 0), ctx.h)
+        for t in (2, 700):
+            _check_layer_outputs(ctx, lay, H[t:t + 1])
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PERSISTENT, 1), ctx.h)
         # and a ragged batch
         _check_layer_outputs(ctx, lay, H[100:105])

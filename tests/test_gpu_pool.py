@@ -1,0 +1,239 @@
+"""Host-pool contexts: the per-layer LRU expert-slot cache (TurboFieldfare,
+"MoE needed parallel work, reuse, and coarse overlap": a bounded per-layer
+cache of routed experts; goinfer, "When the model doesn't fit": LRU slots).
+
+Checks: the cache trace and counters are bit-identical to the oracle's LRU;
+misses are staged from the pinned pool; outputs do not depend on the slot
+count; host-side failures (argument errors, budget, a failed staging copy, a
+timed-out wait) are reported and poison the context as documented."""
+
+import ctypes as C
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import bit_routed_expert_router_gb300 as moe
+import oracle
+from workload import FULL, Shape, bias_from_targets, gen_hidden, gen_layer, zipf_reuse_targets
+
+from moe_harness import Ctx, assert_ffn_close, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _pool_ctx(shape, L, n_slots, weights, prenorm=1):
+    ctx = Ctx(shape, n_layers=L, prenorm=prenorm)
+    for l in range(L):
+        ctx.init_layer(l, weights[l], residency=moe.MOE_HOST_POOL)
+    moe.check(moe.moe_set_slots(ctx.h, n_slots), ctx.h)
+    return ctx
+
+
+def _decode_trace(ctx, h, L, bias):
+    k = ctx.shape.top_k
+    tr = (moe.MoeTraceRec * (L * k))()
+    _, y, n = ctx.decode(h, 0, L, bias=bias, trace=tr)
+    assert n == L * k
+    return y, [(r.layer, r.k_pos, r.expert, r.hit, r.slot, r.evicted) for r in tr]
+
+
+def test_hand_worked_lru_trace():
+    with open(os.path.join(GOLDEN, "lru_hand_trace.json")) as fh:
+        g = json.load(fh)
+    sh = Shape(d=128, f=64, f_shared=64, n_experts=g["n_experts"], top_k=g["top_k"])
+    w = gen_layer(sh, seed=101, layer=0)
+    with _pool_ctx(sh, 1, g["n_slots"], [to_device(w)]) as ctx:
+        H = gen_hidden(len(g["steps"]), sh.d, seed=101).cuda()
+        for t, st in enumerate(g["steps"]):
+            bias = torch.zeros(1, 1, sh.n_experts, dtype=torch.float32)
+            bias[0, 0, st["ids"][0]] = 32.0     # forces the pick and its order
+            bias[0, 0, st["ids"][1]] = 16.0
+            _, rec = _decode_trace(ctx, H[t:t + 1], 1, bias.cuda())
+            assert [r[2] for r in rec] == st["ids"]
+            assert [r[3] for r in rec] == st["hit"]
+            assert [r[4] for r in rec] == st["slot"]
+            assert [r[5] for r in rec] == st["evicted"]
+        st_, stats = moe.moe_get_stats(ctx.h)
+        assert stats.hits == g["total_hits"] and stats.misses == g["total_misses"]
+        assert stats.staged_bytes == g["total_misses"] * stats.expert_bytes
+        _, eos, _ = moe.moe_get_cache_state(ctx.h, 0, g["n_slots"])
+        assert list(eos) == g["final_expert_of_slot"]
+
+
+def test_random_traces_match_oracle_lru_and_outputs_match_oracle():
+    sh = Shape(d=256, f=128, f_shared=128, n_experts=16, top_k=4)
+    L, N, T = 3, 6, 40
+    ws = [gen_layer(sh, seed=110, layer=l) for l in range(L)]
+    tg = zipf_reuse_targets(T, L, sh.n_experts, sh.top_k, seed=110)
+    bias = torch.from_numpy(bias_from_targets(tg, sh.n_experts))          # [T, L, E]
+    with _pool_ctx(sh, L, N, [to_device(w) for w in ws]) as ctx:
+        H = gen_hidden(T, sh.d, seed=110).cuda()
+        lrus = [oracle.LRU(N) for _ in range(L)]
+        xs = torch.zeros(L, 1, sh.d, dtype=torch.bfloat16, device="cuda")
+        ys = torch.zeros(L, 1, sh.d, dtype=torch.float32, device="cuda")
+        lays = [oracle.Layer(w, sh.top_k) for w in ws]
+        for t in range(T):
+            moe.check(moe.moe_set_debug(ctx.h, xs, None, None, ys, L), ctx.h)
+            _, rec = _decode_trace(ctx, H[t:t + 1], L, bias[t].unsqueeze(1).contiguous().cuda())
+            ctx.sync()
+            for l in range(L):
+                rows = [r for r in rec if r[0] == l]
+                ids = [r[2] for r in rows]
+                hit, slot, ev = lrus[l].step(ids, t)
+                assert [r[3] for r in rows] == list(hit), f"t={t} l={l}"
+                assert [r[4] for r in rows] == list(slot), f"t={t} l={l}"
+                assert [r[5] for r in rows] == list(ev), f"t={t} l={l}"
+                if t % 13 == 0:
+                    rid, _, _, ry, _ = lays[l].forward(oracle.as_bits(xs[l, 0]), bias[t, l].numpy())
+                    assert list(rid) == ids
+                    assert_ffn_close(ys[l, 0].cpu().numpy(), ry, f"t={t} l={l}")
+        moe.check(moe.moe_set_debug(ctx.h), ctx.h)
+        _, stats = moe.moe_get_stats(ctx.h)
+        assert stats.hits + stats.misses == T * L * sh.top_k
+        assert stats.steps == T
+        assert stats.staged_bytes == stats.misses * stats.expert_bytes
+        for l in range(L):
+            _, eos, lu = moe.moe_get_cache_state(ctx.h, l, N)
+            assert list(eos) == list(lrus[l].expert_of_slot)
+            assert list(lu) == list(lrus[l].last_use)
+
+
+def test_outputs_do_not_depend_on_slot_count():
+    sh = Shape(d=256, f=128, f_shared=128, n_experts=16, top_k=4)
+    L, T = 2, 12
+    ws = [gen_layer(sh, seed=120, layer=l) for l in range(L)]
+    tg = zipf_reuse_targets(T, L, sh.n_experts, sh.top_k, seed=120)
+    bias = torch.from_numpy(bias_from_targets(tg, sh.n_experts)).cuda()
+    H = gen_hidden(T, sh.d, seed=120).cuda()
+    outs = {}
+    for n_slots in (4, 7, 16, None):
+        if n_slots is None:
+            ctx = Ctx(sh, n_layers=L, prenorm=1)
+            for l in range(L):
+                ctx.init_layer(l, to_device(ws[l]))
+            moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PERSISTENT, 0), ctx.h)
+        else:
+            ctx = _pool_ctx(sh, L, n_slots, [to_device(w) for w in ws])
+        with ctx:
+            res = []
+            for t in range(T):
+                h_out, y, _ = ctx.decode(H[t:t + 1], 0, L, bias=bias[t].unsqueeze(1).contiguous())
+                res.append((h_out.clone(), y.clone()))
+            ctx.sync()
+            outs[n_slots] = res
+    for n_slots in (7, 16, None):
+        for t in range(T):
+            assert torch.equal(outs[n_slots][t][0], outs[4][t][0]), f"h_out differs, N={n_slots} t={t}"
+            assert torch.equal(outs[n_slots][t][1], outs[4][t][1]), f"y differs, N={n_slots} t={t}"
+
+
+def test_full_shape_pool_three_layers():
+    sh = FULL
+    L, N, T = 3, 16, 6
+    wd = [gen_layer(sh, seed=130, layer=l, device="cuda") for l in range(L)]
+    tg = zipf_reuse_targets(T, L, sh.n_experts, sh.top_k, seed=130)
+    bias = torch.from_numpy(bias_from_targets(tg, sh.n_experts))
+    with _pool_ctx(sh, L, N, wd) as ctx:
+        hosts = [to_host(w) for w in wd]
+        del wd
+        H = gen_hidden(T, sh.d, seed=130, device="cuda")
+        lrus = [oracle.LRU(N) for _ in range(L)]
+        xs = torch.zeros(L, 1, sh.d, dtype=torch.bfloat16, device="cuda")
+        ys = torch.zeros(L, 1, sh.d, dtype=torch.float32, device="cuda")
+        for t in range(T):
+            moe.check(moe.moe_set_debug(ctx.h, xs, None, None, ys, L), ctx.h)
+            _, rec = _decode_trace(ctx, H[t:t + 1], L, bias[t].unsqueeze(1).contiguous().cuda())
+            ctx.sync()
+            for l in range(L):
+                rows = [r for r in rec if r[0] == l]
+                hit, slot, ev = lrus[l].step([r[2] for r in rows], t)
+                assert [r[3] for r in rows] == list(hit)
+                assert [r[4] for r in rows] == list(slot)
+                assert [r[5] for r in rows] == list(ev)
+            if t in (0, T - 1):
+                l = t % L
+                lay = oracle.Layer(hosts[l], sh.top_k)
+                rid, _, _, ry, _ = lay.forward(oracle.as_bits(xs[l, 0]), bias[t, l].numpy())
+                assert list(rid) == [r[2] for r in rec if r[0] == l]
+                assert_ffn_close(ys[l, 0].cpu().numpy(), ry, f"t={t} l={l}")
+        moe.check(moe.moe_set_debug(ctx.h), ctx.h)
+
+
+def _small_pool(n_slots=4):
+    sh = Shape(d=128, f=64, f_shared=64, n_experts=8, top_k=2)
+    ws = [to_device(gen_layer(sh, seed=140, layer=0))]
+    return sh, _pool_ctx(sh, 1, n_slots, ws)
+
+
+def test_argument_and_state_errors():
+    sh, ctx = _small_pool()
+    with ctx:
+        assert moe.moe_set_slots(ctx.h, 1) == moe.MOE_EINVAL          # fewer than top_k
+        assert moe.moe_set_slots(ctx.h, 9) == moe.MOE_EINVAL          # more than n_experts
+        H = gen_hidden(2, sh.d, seed=140).cuda()
+        out = torch.empty_like(H)
+        st, _ = moe.moe_decode_step(ctx.h, H, 2, 0, 1, None, out)     # one token per call
+        assert st == moe.MOE_EINVAL
+        st, _ = moe.moe_decode_step(ctx.h, H, 1, 0, 2, None, out)     # layer range
+        assert st == moe.MOE_EINVAL
+        ctx.decode(H[:1])                                              # still usable
+    with Ctx(sh, n_layers=1) as res:
+        res.init_layer(0, to_device(gen_layer(sh, seed=141, layer=0)))
+        assert moe.moe_set_slots(res.h, 4) == moe.MOE_ESTATE           # resident context
+
+
+def test_budget_is_checked_before_allocating():
+    sh, ctx = _small_pool(4)
+    with ctx:
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_FREE_BYTES, 1 << 20), ctx.h)
+        assert moe.moe_set_slots(ctx.h, 8) == moe.MOE_ENOMEM
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_FREE_BYTES, -1), ctx.h)
+        _, stats = moe.moe_get_stats(ctx.h)
+        assert stats.n_slots == 4                                      # unchanged
+        H = gen_hidden(1, sh.d, seed=142).cuda()
+        ctx.decode(H)                                                  # still usable
+
+
+def test_failed_staging_copy_poisons_the_context():
+    sh, ctx = _small_pool(4)
+    with ctx:
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_FAIL_NEXT_COPY, 1), ctx.h)
+        H = gen_hidden(1, sh.d, seed=143).cuda()
+        out = torch.empty_like(H)
+        st, _ = moe.moe_decode_step(ctx.h, H, 1, 0, 1, None, out)
+        assert st == moe.MOE_ECUDA                                     # first token misses
+        st, _ = moe.moe_decode_step(ctx.h, H, 1, 0, 1, None, out)
+        assert st == moe.MOE_ESTATE
+        assert moe.moe_sync(ctx.h) == moe.MOE_ESTATE
+        torch.cuda.synchronize()
+
+
+def test_timed_out_wait_poisons_the_context():
+    sh, ctx = _small_pool(4)
+    with ctx:
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_WAIT_LIMIT_US, -1), ctx.h)
+        H = gen_hidden(1, sh.d, seed=144).cuda()
+        out = torch.empty_like(H)
+        st, _ = moe.moe_decode_step(ctx.h, H, 1, 0, 1, None, out)
+        assert st == moe.MOE_ETIMEOUT
+        st, _ = moe.moe_decode_step(ctx.h, H, 1, 0, 1, None, out)
+        assert st == moe.MOE_ESTATE
+        torch.cuda.synchronize()
+
+
+def test_reset_cache_empties_slots():
+    sh, ctx = _small_pool(4)
+    with ctx:
+        H = gen_hidden(3, sh.d, seed=145).cuda()
+        for t in range(3):
+            ctx.decode(H[t:t + 1])
+        moe.check(moe.moe_reset_cache(ctx.h), ctx.h)
+        _, eos, lu = moe.moe_get_cache_state(ctx.h, 0, 4)
+        assert list(eos) == [-1] * 4 and list(lu) == [-1] * 4
+        _, stats = moe.moe_get_stats(ctx.h)
+        assert stats.hits == 0 and stats.misses == 0 and stats.steps == 0
