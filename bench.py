@@ -49,14 +49,17 @@ def bytes_per_token_layer(sh) -> dict:
     dn_r = (sh.d // 16) * (sh.f // 64) * 576
     dn_s = (sh.d // 16) * (sh.f_shared // 64) * 576
     router = sh.n_experts * sh.d * 2
+    ffn = gu_s + dn_s + sh.top_k * (gu_r + dn_r)
     return {"router_topk_plan": router + sh.d * 2,
             "gateup_gelu_gemv": gu_s + sh.top_k * gu_r,
             "down_combine_gemv": dn_s + sh.top_k * dn_r,
-            "ffn_total": gu_s + dn_s + sh.top_k * (gu_r + dn_r)}
+            "ffn_total": ffn,
+            # one launch of the persistent kernel runs the token through every layer
+            "decode_persistent": N_LAYERS * (router + ffn)}
 
 
 def config_dict(sh):
-    return {"workload": "decode30_resident_zipf", "layers": N_LAYERS, "tokens": N_TOKENS, "B": 1,
+    return {"workload": f"decode{N_LAYERS}_resident_zipf", "layers": N_LAYERS, "tokens": N_TOKENS, "B": 1,
             "d": sh.d, "f": sh.f, "f_shared": sh.f_shared, "experts": sh.n_experts, "top_k": sh.top_k,
             "group": sh.group, "weights": "int4 affine g64, fp16 scale+bias", "residency": "all experts in HBM",
             "routing": "router logits + Zipf(1.1)/reuse-0.6 bias trace",
@@ -325,6 +328,7 @@ def run_ours(args):
     kinds = {moe.KERNEL_KINDS[i]: {"launches": n, "ms": t} for i, (n, t) in enumerate(prof) if n}
     dom = max(kinds, key=lambda k: kinds[k]["ms"])
     dur = kinds[dom]["ms"] / kinds[dom]["launches"] / 1e3
+    launches_per_step = sum(v["launches"] for v in kinds.values()) / n_prof
     peak, peak_kind = load_peaks()
     achieved = bpl[dom] / dur / 1e9
     traffic = load_traffic().get(dom)
@@ -384,7 +388,7 @@ def run_ours(args):
             "kernel_shares": shares,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": sh.d * 2 + N_LAYERS * sh.n_experts * 4,
                     "d2h_bytes_per_step": sh.d * 2},
-            "gpu_launches": 3 * N_LAYERS * args.steps,
+            "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
@@ -403,7 +407,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--layers", type=int, default=30,
+                    help="layers in the stack (30 is the benchmark; fewer only for small profiler captures)")
     args = ap.parse_args(argv)
+    global N_LAYERS
+    N_LAYERS = args.layers
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
