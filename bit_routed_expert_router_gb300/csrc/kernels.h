@@ -16,7 +16,7 @@ constexpr int kPConsumers = 16;        // consumer warps per CTA
 constexpr int kPStages = 5;            // shared-memory ring slots of four 11-group chunks
 constexpr int kPStageGroups = 11;      // int4 groups (576 B each) per stage
 constexpr int kPMaxD = 3072;
-constexpr int kPThreads = 32 * (kPConsumers + 1);
+constexpr int kPThreads = 32 * (kPConsumers + 2);  // producer, consumers, top-k warp
 
 struct PLayer {                        // device addresses of one layer's weights
   const uint16_t* router_w;

@@ -1017,7 +1017,11 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
       }
       return MOE_OK;
     }
-    case 4: ctx->use_persistent = value != 0; return MOE_OK;  // persistent B = 1 decode kernel on/off
+    case 4:  // persistent B = 1 decode kernel on/off; asking for it where it cannot run is an error
+      if (value != 0 && !ctx->p_ok)
+        return fail(ctx, MOE_ESTATE, "persistent decode kernel unavailable for this configuration or device");
+      ctx->use_persistent = value != 0;
+      return MOE_OK;
     case 6:  // budget checks see `value` bytes of free device memory (-1: the real figure)
       ctx->hook_free_bytes = value;
       return MOE_OK;

@@ -9,11 +9,11 @@
 // routed gate/up -> down -> h_{l+1}).
 //
 // Per CTA:
-//   warp 0 (producer) walks the CTA's stage list and streams every stage's
-//     weight bytes into a ring of five 25 KB shared-memory slots with 1-D bulk
-//     copies (TMA engine).  A stage is one gate/up tile (8 gate + 8 up rows,
-//     all of d), four consecutive 16-row down tiles of one routed expert, the
-//     16-row down tile of the shared expert, or one router row; copies this
+//   warp 0, lane 0 (producer) walks the CTA's stage list and streams every
+//     stage's weight bytes into a ring of five 25 KB shared-memory slots with
+//     1-D bulk copies (TMA engine).  A stage is one gate/up tile (8 gate + 8 up
+//     rows, all of d), four consecutive 16-row down tiles of one routed expert,
+//     the 16-row down tile of the shared expert, or one router row; copies this
 //     large keep the copy engine near the HBM rate, where 6 KB copies do not.
 //     The producer needs the routing only for the routed experts' addresses;
 //     while a layer routes it asks L2 to prefetch the next layer's router rows
@@ -23,6 +23,10 @@
 //     warps together), gate/up chunks (int4 on mma.sync, GELU(gate)*up once a
 //     tile's chunks are summed), and down chunks whose last finisher per row
 //     tile does the fixed-order combine and the residual.
+//   warp 17 (top-k) waits for a layer's logits, takes the top-k and the gates
+//     and hands the experts to the producer through an mbarrier.  It is a warp
+//     of its own because warp-wide shuffles measured several times slower in
+//     the warp whose lane 0 issues the copies.
 // Cross-CTA dependencies are monotone counters in global memory polled by one
 // lane; every wait is bounded and gives up through an abort flag, and the last
 // CTA to leave zeroes the counters for the next launch.  Each CTA computes the
@@ -80,6 +84,7 @@ struct Smem {
   int32_t ids[2][32];
   float gates[2][32];
   alignas(8) uint64_t cbar;                     // consumer-warp barrier (one arrival per consumer warp)
+  alignas(8) uint64_t topk_bar;                 // one phase per layer: the top-k warp has published ids
 };
 
 static_assert(offsetof(Smem, ring) % 128 == 0, "ring must be 128-byte aligned");
@@ -114,6 +119,20 @@ __device__ __forceinline__ void tl_min(const PParams& p, int l, int ev) {
 }
 __device__ __forceinline__ void acc_add(const PParams& p, int l, int slot, unsigned long long v) {
   if (p.timeline && blockIdx.x == 0) atomicAdd(p.timeline + (p.n_layers_tl + l) * 16 + slot, v);
+}
+// Per-CTA stamps of the step's third layer (the last one if fewer) at row
+// 2 * n_layers + blockIdx.x: cta_stamp keeps the first time, cta_stamp_max the last.
+__device__ __forceinline__ bool stamped_layer(const PParams& p, int rel) {
+  const int n_rel = p.l1 - p.l0;
+  return p.timeline && rel == (n_rel > 2 ? 2 : n_rel - 1);
+}
+__device__ __forceinline__ void cta_stamp(const PParams& p, int rel, int k) {
+  if (!stamped_layer(p, rel)) return;
+  atomicCAS(p.timeline + (2 * p.n_layers_tl + blockIdx.x) * 16 + k, 0ull, gtimer());
+}
+__device__ __forceinline__ void cta_stamp_max(const PParams& p, int rel, int k) {
+  if (!stamped_layer(p, rel)) return;
+  atomicMax(p.timeline + (2 * p.n_layers_tl + blockIdx.x) * 16 + k, gtimer());
 }
 
 // ------------------------------------------------------------------ sync helpers
@@ -150,28 +169,25 @@ __device__ __forceinline__ void raise_abort(const PParams& p) {
   atomicExch(p.abort_flag, 1u);
 }
 
-// One thread waits until *ctr >= target (acquire).  False on abort or timeout.
-__device__ bool wait_counter(const PParams& p, const unsigned* ctr, unsigned target) {
-  if (ld_acquire(ctr) >= target) return true;
+// The whole warp waits until *ctr >= target (acquire).  False on abort or
+// timeout.  Every lane polls (the loads of one instruction hit one address, so
+// this costs one request): a loop run by one lane while the others wait leaves
+// the warp diverged, and every later warp-wide instruction (shuffle, vote,
+// mma.sync) then measured about six times slower until the warp reconverged.
+__device__ bool warp_wait_counter(const PParams& p, const unsigned* ctr, unsigned target) {
+  if (__all_sync(0xFFFFFFFFu, ld_acquire(ctr) >= target)) return true;
   const long long t0 = clock64();
   for (unsigned it = 1;; ++it) {
     __nanosleep(64);
-    if (ld_acquire(ctr) >= target) return true;
+    if (__all_sync(0xFFFFFFFFu, ld_acquire(ctr) >= target)) return true;
     if ((it & 255) == 0) {
-      if (aborted(p)) return false;
-      if (clock64() - t0 > kSpinLimitCycles) {
-        raise_abort(p);
+      if (__any_sync(0xFFFFFFFFu, aborted(p))) return false;
+      if (__any_sync(0xFFFFFFFFu, clock64() - t0 > kSpinLimitCycles)) {
+        if ((threadIdx.x & 31) == 0) raise_abort(p);
         return false;
       }
     }
   }
-}
-
-// Lane 0 polls, the warp learns the outcome.
-__device__ __forceinline__ bool warp_wait_counter(const PParams& p, const unsigned* ctr, unsigned target) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = wait_counter(p, ctr, target) ? 1 : 0;
-  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
@@ -355,23 +371,22 @@ __device__ __forceinline__ int afrag_index(int r, int par) {
 
 // ------------------------------------------------------------------ producer
 
-// Lane 0 issues every stage; the whole warp joins only for the top-k.
+// One thread (lane 0 of warp 0) issues every stage.  At a layer's top-k marker
+// it asks L2 for the next layer's routing-independent bytes, then waits for the
+// top-k warp to publish the layer's experts.
 __device__ void producer(const PParams& p, Smem& S) {
-  const int lane = threadIdx.x & 31;
   const int n_rel = p.l1 - p.l0;
   const int n_tasks = S.n_tasks, spl = S.stages_per_layer;
-  bool ok = true;          // lane 0's view; shared with the warp at each top-k
-  uint32_t u_issued = 0;   // lane 0: ring uses issued so far
+  uint32_t u_issued = 0;   // ring uses issued so far
   for (int rel = 0; rel < n_rel; ++rel) {
     const int l = p.l0 + rel;
-    PLayer Lc{};
-    if (lane == 0) Lc = p.layers[l];
+    const PLayer Lc = p.layers[l];
     for (int i = 0; i < n_tasks; ++i) {
       const PTask e = S.tasks[i];
       if (e.kind == T_PREP) continue;
       if (e.kind == T_TOPK) {
-        // next layer's routing-independent bytes go to L2 while this layer routes
-        if (lane == 0 && ok && rel + 1 < n_rel) {
+        cta_stamp(p, rel, 0);
+        if (rel + 1 < n_rel) {
           const PLayer Ln = p.layers[l + 1];
           for (int i2 = 0; i2 < n_tasks; ++i2) {
             const PTask e2 = S.tasks[i2];
@@ -381,34 +396,18 @@ __device__ void producer(const PParams& p, Smem& S) {
             }
           }
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-        if (!ok) return;
-        if (!warp_wait_counter(p, p.logit_cnt + l, static_cast<unsigned>(p.E))) return;
-        if (lane == 0) tl_max(p, l, EV_LOGITS_ALL);
-        int32_t* sid = S.ids[rel & 1];
-        float* sg = S.gates[rel & 1];
-        warp_topk(p, l, sid, sg);
-        if (lane < p.k) p.gates_g[static_cast<size_t>(l) * p.k + lane] = sg[lane];
-        if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
-          const DevCallArgs* A = &S.args;
-          const size_t o = (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.k + lane;
-          if (A->dbg_ids) A->dbg_ids[o] = sid[lane];
-          if (A->dbg_gates) A->dbg_gates[o] = sg[lane];
+        cta_stamp(p, rel, 1);
+        if (!mbar_wait_bounded(&S.topk_bar, static_cast<uint32_t>(rel) & 1u, p.err)) {
+          raise_abort(p);
+          break;
         }
-        __syncwarp();
-        if (lane == 0) tl_max(p, l, EV_TOPK);
         continue;
       }
-      if (lane != 0 || !ok) continue;
       const uint32_t u = static_cast<uint32_t>(rel) * spl + e.u;
       const int slot = u % kNS;
       if (!mbar_wait_bounded(&S.empty[slot], ((u / kNS) & 1) ^ 1, p.err)) {
         raise_abort(p);
-        ok = false;
-        // the last min(u_issued, kNS) stages may still be in flight: wait for each, bounded
-        for (uint32_t v = (u_issued > static_cast<uint32_t>(kNS) ? u_issued - kNS : 0); v < u_issued; ++v)
-          mbar_wait_bounded(&S.full[v % kNS], (v / kNS) & 1, p.err);
-        continue;
+        break;
       }
       const StageSrc ss = stage_src(p, Lc, e, S.ids[rel & 1]);
       fence_proxy_async_smem();
@@ -418,10 +417,48 @@ __device__ void producer(const PParams& p, Smem& S) {
       if (p.timeline) {
         if (e.kind == T_GUR) tl_max(p, l, EV_GUR_ISSUE0);
         if (e.kind == T_DNR) tl_max(p, l, EV_DNR_ISSUED);
+        if (e.kind == T_GUR) cta_stamp(p, rel, 4);
+        if (e.kind == T_DNR) cta_stamp(p, rel, 5);
       }
     }
+    if (aborted(p)) break;
   }
-  __syncwarp();
+  // on abort, the last min(u_issued, kNS) stages may still be in flight: wait for each, bounded
+  if (aborted(p))
+    for (uint32_t v = (u_issued > static_cast<uint32_t>(kNS) ? u_issued - kNS : 0); v < u_issued; ++v)
+      mbar_wait_bounded(&S.full[v % kNS], (v / kNS) & 1, p.err);
+}
+
+// The top-k warp: per layer, waits for every router row, takes the top-k and
+// the gates, publishes them (shared memory for the producer, global memory for
+// the combine) and releases the producer.
+__device__ void topk_warp(const PParams& p, Smem& S) {
+  const int lane = threadIdx.x & 31;
+  const int n_rel = p.l1 - p.l0;
+  for (int rel = 0; rel < n_rel; ++rel) {
+    const int l = p.l0 + rel;
+    if (!warp_wait_counter(p, p.logit_cnt + l, static_cast<unsigned>(p.E))) return;
+    if (lane == 0) {
+      tl_max(p, l, EV_LOGITS_ALL);
+      cta_stamp(p, rel, 2);
+    }
+    int32_t* sid = S.ids[rel & 1];
+    float* sg = S.gates[rel & 1];
+    warp_topk(p, l, sid, sg);
+    if (lane < p.k) p.gates_g[static_cast<size_t>(l) * p.k + lane] = sg[lane];
+    if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
+      const DevCallArgs* A = &S.args;
+      const size_t o = (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.k + lane;
+      if (A->dbg_ids) A->dbg_ids[o] = sid[lane];
+      if (A->dbg_gates) A->dbg_gates[o] = sg[lane];
+    }
+    __syncwarp();
+    if (lane == 0) {
+      tl_max(p, l, EV_TOPK);
+      cta_stamp(p, rel, 3);
+      mbarrier_arrive(&S.topk_bar);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ consumers
@@ -435,14 +472,13 @@ __device__ bool prep(const PParams& p, Smem& S, int cw, int rel, int& round) {
   const DevCallArgs* A = &S.args;
   const int l = p.l0 + rel;
   if (lane == 0) tl_min(p, l, EV_PREP_IN);
+  if (lane == 0 && cw == 0) cta_stamp(p, rel, 8);
   if (rel > 0) {
-    int okw = 1;
-    if (cw == 0 && lane == 0) okw = wait_counter(p, p.rows_done + (l - 1), static_cast<unsigned>(d / 16)) ? 1 : 0;
-    okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-    if (!okw) return false;
+    if (cw == 0 && !warp_wait_counter(p, p.rows_done + (l - 1), static_cast<unsigned>(d / 16))) return false;
     if (!consumer_barrier(p, S, ++round)) return false;
   }
   if (lane == 0) tl_max(p, l, EV_H_READY);
+  if (lane == 0 && cw == 0) cta_stamp(p, rel, 9);
   const uint16_t* h = rel == 0 ? A->h_in : ((rel - 1) & 1 ? p.hbuf1 : p.hbuf0);
   // this warp's groups G = cw, cw + kNC, ...; lane holds elements 64G + 2*lane, +1
   uint32_t hv[(kPMaxD / 64 + kNC - 1) / kNC];
@@ -488,6 +524,7 @@ __device__ bool prep(const PParams& p, Smem& S, int cw, int rel, int& round) {
   }
   const bool okb = consumer_barrier(p, S, ++round);  // x complete
   if (lane == 0) tl_max(p, l, EV_PREP_DONE);
+  if (lane == 0 && cw == 0) cta_stamp(p, rel, 10);
   return okb;
 }
 
@@ -502,9 +539,12 @@ __device__ bool task_router(const PParams& p, Smem& S, int rel, int l, int e_row
   const uint4* xv4 = reinterpret_cast<const uint4*>(S.xs);
   long long acc = 0;
   bool bad = false;
-  for (int c = cw * 32 + lane; c < p.d / 8; c += 32 * kNC) {
-    const uint4 wv = wr[c];
+  for (int c0 = cw * 32; c0 < p.d / 8; c0 += 32 * kNC) {
+    const int c = min(c0 + lane, p.d / 8 - 1);
+    const bool live = c0 + lane < p.d / 8;   // the clamped lanes of a ragged tail add nothing
+    uint4 wv = wr[c];
     const uint4 xv = xv4[c];
+    if (!live) wv = make_uint4(0u, 0u, 0u, 0u);
     const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
     const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
@@ -644,15 +684,21 @@ __device__ bool dn_operands(const PParams& p, Smem& S, int cw, int l, bool route
   const uint16_t* abase = routed ? p.a_r + static_cast<size_t>(src) * 2 * p.f : p.a_s;
   const float* sbase = routed ? p.asum_r + static_cast<size_t>(src) * (p.f / 8) * 2 : p.asum_s;
   const uint8_t* asrc = reinterpret_cast<const uint8_t*>(abase) + static_cast<size_t>(g0) * 256;
-  for (int i = lane; i < ng * 16; i += 32) cp_async16(S.abuf[cw] + i * 16, asrc + i * 16);
+  // uniform loops with predicated bodies keep the warp converged (see warp_wait_counter)
+  for (int i0 = 0; i0 < ng * 16; i0 += 32)
+    if (i0 + lane < ng * 16) cp_async16(S.abuf[cw] + (i0 + lane) * 16, asrc + (i0 + lane) * 16);
   const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(sbase + static_cast<size_t>(g0) * 16);
-  for (int i = lane; i < ng * 4; i += 32) cp_async16(reinterpret_cast<uint8_t*>(S.asb[cw]) + i * 16, ssrc + i * 16);
+  for (int i0 = 0; i0 < ng * 4; i0 += 32)
+    if (i0 + lane < ng * 4)
+      cp_async16(reinterpret_cast<uint8_t*>(S.asb[cw]) + (i0 + lane) * 16, ssrc + (i0 + lane) * 16);
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   __syncwarp();
-  if (lane < ng) {
+  {
+    const int gl = min(lane, ng - 1);
     float a = 0.f;
-    for (int i = 0; i < 8; ++i) a += S.asb[cw][lane * 16 + 2 * i] + S.asb[cw][lane * 16 + 2 * i + 1];
-    S.asg[cw][lane] = a;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a += S.asb[cw][gl * 16 + 2 * i] + S.asb[cw][gl * 16 + 2 * i + 1];
+    if (lane < ng) S.asg[cw][lane] = a;
   }
   __syncwarp();
   return true;
@@ -711,15 +757,18 @@ __device__ void dn_chunk(const PParams& p, Smem& S, int cw, int rel, int l, int 
   const uint16_t* hin = rel == 0 ? A->h_in : ((rel - 1) & 1 ? p.hbuf1 : p.hbuf0);
   uint16_t* hout = last_layer ? A->h_out : (rel & 1 ? p.hbuf1 : p.hbuf0);
   const float* pp = p.part + static_cast<size_t>(rel & 1) * n_parts * p.d;
-  if (lane < 16) {
-    const int row = T * 16 + lane;
+  {
+    // all 32 lanes run the sums (lanes 16..31 repeat rows 0..15) so the warp stays converged
+    const int row = T * 16 + (lane & 15);
     float y = 0.f;
     for (int c2 = 0; c2 < p.n_sc; ++c2) y += __ldcg(&pp[static_cast<size_t>(c2) * p.d + row]);
     for (int j = 0; j < p.k; ++j) y += __ldcg(&gates[j]) * __ldcg(&pp[static_cast<size_t>(p.n_sc + j) * p.d + row]);
     const float hv = bf16_bits_to_float(__ldcg(&hin[row]));
-    hout[row] = float_to_bf16_bits(hv + y);
-    if (last_layer && A->y_last) A->y_last[row] = y;
-    if (A->dbg_y && rel < A->dbg_layers) A->dbg_y[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.d + row] = y;
+    if (lane < 16) {
+      hout[row] = float_to_bf16_bits(hv + y);
+      if (last_layer && A->y_last) A->y_last[row] = y;
+      if (A->dbg_y && rel < A->dbg_layers) A->dbg_y[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.d + row] = y;
+    }
   }
   fence_acq_rel_gpu();
   __syncwarp();
@@ -754,6 +803,7 @@ __device__ void consumer(const PParams& p, Smem& S, int cw) {
           return;
         }
         if (!task_router(p, S, rel, l, e.a, S.ring[slot], cw, round, (rel * rpl + e.seq) & 1)) return;
+        if (lane == 0 && cw == 0) cta_stamp(p, rel, 11);
         // every warp has read the row once the reduction barrier passed; warp 0 frees the slot
         if (cw == 0) {
           __syncwarp();
@@ -773,9 +823,12 @@ __device__ void consumer(const PParams& p, Smem& S, int cw) {
         }
         const unsigned long long t1 = p.timeline ? gtimer() : 0ull;
         if (e.kind == T_GUR && lane == 0) tl_min(p, l, EV_GUR_START);
+        if (e.kind == T_GUR && lane == 0) cta_stamp(p, rel, 12);
+        if (e.kind == T_GUS && lane == 0) cta_stamp(p, rel, 6);
         const int gslot = (rel * tpl + e.seq) % kGuSlots;
         if (e.kind == T_GUS) task_gu(p, S, l, S.ring[slot], s, -1, e.a, gslot);
         else task_gu(p, S, l, S.ring[slot], s, e.a / (p.f / 8), e.a % (p.f / 8), gslot);
+        if (lane == 0) cta_stamp_max(p, rel, e.kind == T_GUR ? 7 : 13);
         if (lane == 0 && e.kind == T_GUR && p.timeline) {
           acc_add(p, l, 0, t1 - t0);
           acc_add(p, l, 1, gtimer() - t1);
@@ -794,6 +847,7 @@ __device__ void consumer(const PParams& p, Smem& S, int cw) {
         const unsigned long long t2 = p.timeline ? gtimer() : 0ull;
         if (ok) ok = mbar_wait_bounded(&S.full[slot], par, p.err);
         const unsigned long long t3 = p.timeline ? gtimer() : 0ull;
+        if (lane == 0 && ok) cta_stamp(p, rel, 14);
         if (ok) dn_chunk(p, S, cw, rel, l, e.b + s, p.n_sc + e.a, S.ring[slot] + s * nGf * kGroupBytes, nGf);
         if (lane == 0 && p.timeline) {
           acc_add(p, l, 3, t2 - t0);
@@ -809,9 +863,12 @@ __device__ void consumer(const PParams& p, Smem& S, int cw) {
       __syncwarp();
       if (lane == 0) mbar_arrive_n(&S.empty[slot], s == 0 ? 1 + kSub - e.n_sub : 1);
     }
+    if (lane == 0) cta_stamp_max(p, rel, 15);
   }
 }
 
+// 18 warps put five on two of the SM's four schedulers; each scheduler has 16 K
+// registers, so a thread may hold at most 96 (launch bounds give exactly that).
 __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -822,6 +879,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PParams p) {
       mbar_init(&S.empty[i], kSub);
     }
     mbar_init(&S.cbar, kNC);
+    mbar_init(&S.topk_bar, 1);
     fence_mbar_init();
     S.args = *p.args;
     // this CTA's stage pattern for one layer
@@ -851,8 +909,13 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PParams p) {
   if (threadIdx.x < kGuSlots) S.gu_cnt[threadIdx.x] = 0;
   if (threadIdx.x == 0) tl_min(p, p.l0, EV_START);
   __syncthreads();
-  if (warp == 0) producer(p, S);
-  else consumer(p, S, warp - 1);
+  if (warp == 0) {
+    if ((threadIdx.x & 31) == 0) producer(p, S);
+  } else if (warp <= kNC) {
+    consumer(p, S, warp - 1);
+  } else {
+    topk_warp(p, S);
+  }
   __syncthreads();
   // the last CTA out zeroes the dependency counters for the next launch
   __shared__ int s_last;
