@@ -19,6 +19,7 @@ MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTATE, MOE_ETIMEOUT, MOE_EDOMAIN
 MOE_RESIDENT_HBM, MOE_HOST_POOL = 0, 1
 MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
 HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6
+HOOK_PREFILL_TC = 7
 
 
 class MoeConfig(C.Structure):
@@ -49,7 +50,8 @@ class MoeKernelTime(C.Structure):
 
 
 N_KERNEL_KINDS = 8
-KERNEL_KINDS = {0: "router_topk_plan", 1: "gateup_gelu_gemv", 2: "down_combine_gemv", 3: "decode_persistent"}
+KERNEL_KINDS = {0: "router_topk_plan", 1: "gateup_gelu_gemv", 2: "down_combine_gemv", 3: "decode_persistent",
+                4: "prefill_route_group", 5: "prefill_tcgen05_gemm"}
 
 
 class MoeError(RuntimeError):

@@ -1,6 +1,7 @@
 // Launchers of the libmoe kernels (host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -60,6 +61,45 @@ int persistent_max_tasks();
 cudaError_t persistent_attrs();
 cudaError_t persistent_occupancy(int* blocks_per_sm);
 cudaError_t launch_persistent(PParams& p, int grid, cudaStream_t s);
+
+// Prefill (tcgen05 grouped GEMM over int4 weights).
+constexpr int kPfTileN = 128;          // token rows per GEMM tile
+enum : int { PF_GU = 0, PF_DN_ROUTED = 1, PF_DN_SHARED = 2 };
+
+struct PfGemm {
+  const uint8_t* w;                    // weight region (gate/up or down) of expert 0, device layout
+  long long w_stride;                  // bytes between experts (0: one matrix)
+  int nG;                              // K / 64
+  const int32_t* items;                // [n][3] expert, first row, rows; null: 128-row tiles of rows_total
+  const int32_t* n_items_dev;          // item count on the device (null: n_items)
+  int n_items, rows_total;
+  int mode;                            // PF_*
+  int d, k, gelu;
+  uint16_t* out16;                     // PF_GU: fp16 [rows][f_out]
+  int f_out;
+  float* out32;                        // PF_DN_ROUTED: fp32 [T*k][d] by pair
+  const int32_t* pair_of_row;          // PF_DN_ROUTED: pair of each expert-ordered row
+  const float* gates;                  // PF_DN_SHARED: [T][k]
+  const float* ytok;                   // PF_DN_SHARED: [T*k][d]
+  const uint16_t* hin;                 // PF_DN_SHARED: residual in, bf16 [T][d]
+  uint16_t* hout;                      // PF_DN_SHARED: bf16 [T][d]
+  float* y_last;                       // PF_DN_SHARED: optional fp32 [T][d]
+  float* dbg_y;                        // PF_DN_SHARED: optional fp32 [T][d]
+  uint32_t* err;
+};
+
+size_t pf_gemm_smem();
+cudaError_t pf_set_attrs();
+cudaError_t launch_pf_gemm(const CUtensorMap& tmap_b, const PfGemm& p, int m_tiles, int max_items, cudaStream_t s);
+cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
+                           uint16_t* dbg_x, uint32_t* err, cudaStream_t s);
+cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
+                             int k, int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err,
+                             cudaStream_t s);
+cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int32_t* cnt, int32_t* row_pair, int32_t* items,
+                           int32_t* n_items, cudaStream_t s);
+cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,
+                             cudaStream_t s);
 
 size_t gateup_smem(int d);
 size_t down_smem(int cg, int nb4);

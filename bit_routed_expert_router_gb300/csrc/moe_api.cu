@@ -16,6 +16,8 @@
 #include <tuple>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
 #include "internal.h"
 #include "kernels.h"
 
@@ -118,6 +120,16 @@ struct moe_ctx {
   float *p_asum_s = nullptr, *p_asum_r = nullptr, *p_part = nullptr;
   int p_n_sc = 1;
   float* p_gates = nullptr;            // [n_layers][k]
+  // batched prefill on tcgen05 (resident contexts): scratch for max_tokens tokens, made on first use
+  bool pf_ok = false;                  // shapes and device allow it
+  bool use_pf = true;                  // test hook 7
+  bool pf_ready = false;
+  std::vector<void*> pf_owned;
+  uint16_t *pf_xbf = nullptr, *pf_x16 = nullptr, *pf_xp = nullptr, *pf_ar = nullptr, *pf_as = nullptr;
+  uint16_t* pf_h[2] = {nullptr, nullptr};
+  int32_t *pf_ids = nullptr, *pf_cnt = nullptr, *pf_rowpair = nullptr, *pf_items = nullptr, *pf_nitems = nullptr;
+  float *pf_gates = nullptr, *pf_ytok = nullptr;
+  CUtensorMap pf_map_xp{}, pf_map_x16{}, pf_map_ar{}, pf_map_as{};
   unsigned long long* p_timeline = nullptr;   // caller device buffer [n_layers][16], test hook 5
   // per-kernel timing
   bool profiling = false;
@@ -673,6 +685,12 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       ctx->p_ok = true;
     cudaGetLastError();
   }
+  // the tcgen05 prefill: 128-row weight tiles of the down projection, one router
+  // CTA column of 128 experts, and its shared memory
+  if (c.d % 128 == 0 && c.n_experts <= 128 && pf_gemm_smem() <= static_cast<size_t>(max_smem)) {
+    if (pf_set_attrs() == cudaSuccess) ctx->pf_ok = true;
+    cudaGetLastError();
+  }
   if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ECUDA);
   *out = ctx;
   return MOE_OK;
@@ -694,6 +712,7 @@ void moe_destroy(moe_ctx* ctx) {
     cudaFree(Ls.last_use);
   }
   for (void* p : ctx->owned) cudaFree(p);
+  for (void* p : ctx->pf_owned) cudaFree(p);
   if (ctx->pool) cudaFreeHost(ctx->pool);
   if (ctx->args_ring) cudaFreeHost(ctx->args_ring);
   if (ctx->host_rec) cudaFreeHost(ctx->host_rec);
@@ -884,6 +903,146 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
   return resident_run(ctx, B, layer_begin, layer_end, s);
 }
 
+namespace {
+
+// 2-D tensor map over a row-major fp16 matrix [rows][K]: boxes of 64 columns x
+// kPfTileN rows with the 128-byte swizzle the GEMM's operand tiles use.
+// The driver entry point is looked up through the runtime, so the library does
+// not link libcuda itself (it loads on machines without a driver).
+bool encode_rows(CUtensorMap* m, void* base, int K, long long rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q{};
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPfTileN)};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Scratch of the tcgen05 prefill for max_tokens tokens (made once).
+moe_status pf_alloc(moe_ctx* ctx) {
+  if (ctx->pf_ready) return MOE_OK;
+  const moe_config& c = ctx->cfg;
+  const size_t T = c.max_tokens, P = T * c.top_k;
+  size_t nb = 0;
+  auto& o = ctx->pf_owned;
+  ctx->pf_xbf = dalloc<uint16_t>(T * c.d, o, nb);
+  ctx->pf_x16 = dalloc<uint16_t>(T * c.d, o, nb);
+  ctx->pf_xp = dalloc<uint16_t>(P * c.d, o, nb);
+  ctx->pf_ar = dalloc<uint16_t>(P * c.f, o, nb);
+  ctx->pf_as = dalloc<uint16_t>(T * c.f_shared, o, nb);
+  ctx->pf_h[0] = dalloc<uint16_t>(T * c.d, o, nb);
+  ctx->pf_h[1] = dalloc<uint16_t>(T * c.d, o, nb);
+  ctx->pf_ids = dalloc<int32_t>(P, o, nb);
+  ctx->pf_gates = dalloc<float>(P, o, nb);
+  ctx->pf_cnt = dalloc<int32_t>(c.n_experts, o, nb);
+  ctx->pf_rowpair = dalloc<int32_t>(P, o, nb);
+  ctx->pf_items = dalloc<int32_t>(3 * (P / kPfTileN + c.n_experts + 1), o, nb);
+  ctx->pf_nitems = dalloc<int32_t>(1, o, nb);
+  ctx->pf_ytok = dalloc<float>(P * c.d, o, nb);
+  if (!ctx->pf_xbf || !ctx->pf_x16 || !ctx->pf_xp || !ctx->pf_ar || !ctx->pf_as || !ctx->pf_h[0] || !ctx->pf_h[1] ||
+      !ctx->pf_ids || !ctx->pf_gates || !ctx->pf_cnt || !ctx->pf_rowpair || !ctx->pf_items || !ctx->pf_nitems ||
+      !ctx->pf_ytok)
+    return fail(ctx, MOE_ENOMEM, "prefill scratch (%zu bytes for %zu tokens) does not fit", nb, T);
+  if (!encode_rows(&ctx->pf_map_xp, ctx->pf_xp, c.d, static_cast<long long>(P)) ||
+      !encode_rows(&ctx->pf_map_x16, ctx->pf_x16, c.d, static_cast<long long>(T)) ||
+      !encode_rows(&ctx->pf_map_ar, ctx->pf_ar, c.f, static_cast<long long>(P)) ||
+      !encode_rows(&ctx->pf_map_as, ctx->pf_as, c.f_shared, static_cast<long long>(T)))
+    return fail(ctx, MOE_ECUDA, "cuTensorMapEncodeTiled failed for the prefill operands");
+  ctx->device_bytes += nb;
+  ctx->pf_ready = true;
+  return MOE_OK;
+}
+
+// One layer of the batched prefill: route, group by expert, four grouped GEMMs.
+moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin, uint16_t* hout, int T,
+                    const float* bias, float* y_last, cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
+  const LayerStore& L = ctx->L[l];
+  const int d = c.d, E = c.n_experts, k = c.top_k, P = T * k;
+  const bool dbg = rel < ctx->dbg_layers;
+  const size_t xo = static_cast<size_t>(rel) * T;
+  PROF(4, s);
+  CK(launch_pf_prep(hin, T, d, c.prenorm, c.norm_eps, ctx->pf_xbf, ctx->pf_x16,
+                    dbg && ctx->dbg_x ? ctx->dbg_x + xo * d : nullptr, ctx->err_word, s));
+  CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_ids,
+                      ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
+                      dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr, ctx->err_word, s));
+  CK(launch_pf_plan(ctx->pf_ids, P, E, ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items, ctx->pf_nitems, s));
+  CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
+  PROF(-1, s);
+  const size_t gu_r = static_cast<size_t>(c.f / 8) * (d / 64) * kGroupBytes;
+  const size_t gu_s = static_cast<size_t>(c.f_shared / 8) * (d / 64) * kGroupBytes;
+  const int max_items = P / kPfTileN + E + 1;
+  const int t_items = (T + kPfTileN - 1) / kPfTileN;
+  PfGemm g{};
+  g.d = d;
+  g.k = k;
+  g.gelu = c.gelu_variant;
+  g.err = ctx->err_word;
+  PROF(5, s);
+  // routed gate/up: expert-ordered rows -> GELU(gate) * up, fp16 [P][f]
+  PfGemm a = g;
+  a.w = L.experts;
+  a.w_stride = ctx->stride;
+  a.nG = d / 64;
+  a.items = ctx->pf_items;
+  a.n_items_dev = ctx->pf_nitems;
+  a.mode = PF_GU;
+  a.out16 = ctx->pf_ar;
+  a.f_out = c.f;
+  CK(launch_pf_gemm(ctx->pf_map_xp, a, c.f / 64, max_items, s));
+  // shared gate/up over every token
+  PfGemm b = g;
+  b.w = L.shared;
+  b.nG = d / 64;
+  b.n_items = t_items;
+  b.rows_total = T;
+  b.mode = PF_GU;
+  b.out16 = ctx->pf_as;
+  b.f_out = c.f_shared;
+  CK(launch_pf_gemm(ctx->pf_map_x16, b, c.f_shared / 64, t_items, s));
+  // routed down: per pair, fp32 [T*k][d]
+  PfGemm r = g;
+  r.w = L.experts + gu_r;
+  r.w_stride = ctx->stride;
+  r.nG = c.f / 64;
+  r.items = ctx->pf_items;
+  r.n_items_dev = ctx->pf_nitems;
+  r.mode = PF_DN_ROUTED;
+  r.out32 = ctx->pf_ytok;
+  r.pair_of_row = ctx->pf_rowpair;
+  CK(launch_pf_gemm(ctx->pf_map_ar, r, d / 128, max_items, s));
+  // shared down + routed combine (top-k order) + residual
+  PfGemm q = g;
+  q.w = L.shared + gu_s;
+  q.nG = c.f_shared / 64;
+  q.n_items = t_items;
+  q.rows_total = T;
+  q.mode = PF_DN_SHARED;
+  q.gates = ctx->pf_gates;
+  q.ytok = ctx->pf_ytok;
+  q.hin = hin;
+  q.hout = hout;
+  q.y_last = rel == n_rel - 1 ? y_last : nullptr;
+  q.dbg_y = dbg && ctx->dbg_y ? ctx->dbg_y + xo * d : nullptr;
+  CK(launch_pf_gemm(ctx->pf_map_as, q, d / 128, t_items, s));
+  PROF(-1, s);
+  return MOE_OK;
+}
+
+}  // namespace
+
 moe_status moe_prefill(moe_ctx* ctx, const void* h, int T, int layer_begin, int layer_end, const float* logit_bias,
                        void* h_out, float* y_last, void* stream) {
   moe_status st = check_ready(ctx, layer_begin, layer_end);
@@ -893,7 +1052,20 @@ moe_status moe_prefill(moe_ctx* ctx, const void* h, int T, int layer_begin, int 
   if (T < 1 || T > ctx->cfg.max_tokens) return fail(ctx, MOE_EINVAL, "T=%d outside [1, %d]", T, ctx->cfg.max_tokens);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CK(cudaSetDevice(ctx->device));
-  const int d = ctx->cfg.d, E = ctx->cfg.n_experts;
+  const int d = ctx->cfg.d;
+  if (ctx->pf_ok && ctx->use_pf) {
+    st = pf_alloc(ctx);
+    if (st != MOE_OK) return st;
+    const int n_rel = layer_end - layer_begin;
+    for (int rel = 0; rel < n_rel; ++rel) {
+      const uint16_t* hin = rel == 0 ? static_cast<const uint16_t*>(h) : ctx->pf_h[(rel - 1) & 1];
+      uint16_t* hout = rel == n_rel - 1 ? static_cast<uint16_t*>(h_out) : ctx->pf_h[rel & 1];
+      st = pf_layer(ctx, layer_begin + rel, rel, n_rel, hin, hout, T, logit_bias, y_last, s);
+      if (st != MOE_OK) return st;
+    }
+    return prof_collect(ctx, s);
+  }
+  // otherwise: the batched decode kernels, kMaxDecodeB tokens at a time
   for (int t0 = 0; t0 < T; t0 += ctx->Bd) {
     const int B = std::min(ctx->Bd, T - t0);
     const uint16_t* hi = static_cast<const uint16_t*>(h) + static_cast<size_t>(t0) * d;
@@ -902,7 +1074,6 @@ moe_status moe_prefill(moe_ctx* ctx, const void* h, int T, int layer_begin, int 
     DevCallArgs a = make_args(ctx, hi, ho, yl, logit_bias, B, T, t0);
     st = put_args(ctx, a, s);
     if (st != MOE_OK) return st;
-    (void)E;
     st = resident_run(ctx, B, layer_begin, layer_end, s);
     if (st != MOE_OK) return st;
   }
@@ -934,6 +1105,7 @@ moe_status moe_sync(moe_ctx* ctx, void* stream) {
   if (w & ERR_WAIT_TIMEOUT) return fail(ctx, MOE_ETIMEOUT, "a device wait ran out (error word 0x%x)", w);
   if (w & ERR_PLAN) return fail(ctx, MOE_ECUDA, "device plan overflow (error word 0x%x)", w);
   if (w & ERR_ROUTER_DOMAIN) return fail(ctx, MOE_EDOMAIN, "router input outside the exact fixed-point domain");
+  if (w & ERR_PF_RANGE) return fail(ctx, MOE_EDOMAIN, "prefill: an fp16 matrix operand is outside [-65504, 65504]");
   return MOE_OK;
 }
 
@@ -1017,6 +1189,11 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
       }
       return MOE_OK;
     }
+    case 7:  // tcgen05 batched prefill on/off; asking for it where it cannot run is an error
+      if (value != 0 && !ctx->pf_ok)
+        return fail(ctx, MOE_ESTATE, "tcgen05 prefill unavailable for this configuration or device");
+      ctx->use_pf = value != 0;
+      return MOE_OK;
     case 4:  // persistent B = 1 decode kernel on/off; asking for it where it cannot run is an error
       if (value != 0 && !ctx->p_ok)
         return fail(ctx, MOE_ESTATE, "persistent decode kernel unavailable for this configuration or device");

@@ -396,7 +396,6 @@ __device__ void producer(const PParams& p, Smem& S) {
             }
           }
         }
-        cta_stamp(p, rel, 1);
         if (!mbar_wait_bounded(&S.topk_bar, static_cast<uint32_t>(rel) & 1u, p.err)) {
           raise_abort(p);
           break;
@@ -824,6 +823,7 @@ __device__ void consumer(const PParams& p, Smem& S, int cw) {
         const unsigned long long t1 = p.timeline ? gtimer() : 0ull;
         if (e.kind == T_GUR && lane == 0) tl_min(p, l, EV_GUR_START);
         if (e.kind == T_GUR && lane == 0) cta_stamp(p, rel, 12);
+        if (e.kind == T_GUR && lane == 0) cta_stamp_max(p, rel, 1);
         if (e.kind == T_GUS && lane == 0) cta_stamp(p, rel, 6);
         const int gslot = (rel * tpl + e.seq) % kGuSlots;
         if (e.kind == T_GUS) task_gu(p, S, l, S.ring[slot], s, -1, e.a, gslot);

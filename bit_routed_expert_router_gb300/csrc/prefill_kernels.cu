@@ -1,4 +1,622 @@
-// Prefill-path kernels of libmoe (sm_103a).  Placeholder translation unit.
+// Prefill kernels of libmoe (sm_103a): T tokens through one layer at once.
+//
+// "Optimizing a 14.3 GB model for an 8 GB machine", section "Splitting the work
+// improved attention and prefill": batched prefill dequantises a small 16-bit
+// tile of the affine int4 weights, runs the hardware matrix primitive on it and
+// throws the tile away, so the stored weights never change.  Here that
+// primitive is tcgen05 (fifth-generation tensor cores, accumulators in tensor
+// memory), and the batch is grouped by expert first:
+//
+//   k_pf_prep     RMS norm (or copy) of every token: x in bf16 (router) and
+//                 fp16 (matrix operand).
+//   k_pf_router   exact fixed-point logits of every (token, expert), top-k and
+//                 softmax gates per token.
+//   k_pf_count /  stable counting sort of the T*k (token, position) pairs by
+//   k_pf_scatter  expert, and the list of 128-row work items per expert.
+//   k_pf_gather   the pairs' x rows, in that order, as one fp16 matrix.
+//   k_pf_gemm     grouped int4 x fp16 GEMM on tcgen05.  A CTA owns 128 weight
+//                 rows and 128 token rows of one expert: a producer thread
+//                 streams the int4 blocks (bulk copies) and the token rows
+//                 (TMA tensor loads, 128-byte swizzle), four warps dequantise
+//                 each 64-wide k step into an fp16 tile in the same swizzled
+//                 layout, one thread issues the MMAs into a 128 x 128 fp32
+//                 accumulator in tensor memory, and the four warps then read
+//                 it back for the epilogue: GELU(gate) * up (gate/up pass),
+//                 the expert output per pair (routed down pass), or the
+//                 shared-expert output plus the gate-weighted routed outputs
+//                 in top-k order plus the residual (shared down pass).
+#include <cuda.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kM = 128;                 // weight rows per CTA tile
+constexpr int kN = kPfTileN;            // token rows per CTA tile
+constexpr int kSlots = 4;               // k-step slots (A + B tiles)
+constexpr int kRawG = 4;                // int4 groups per raw stage
+constexpr int kRawStages = 2;
+constexpr int kTileBytes = 128 * 128;   // one 128-row x 64-col fp16 tile (16 KB)
+constexpr int kRawStride = kRawG * kGroupBytes;   // bytes of one 16-row tile in a raw stage
+constexpr int kRawBytes = 8 * kRawStride;         // 8 tiles of 16 rows = 128 rows
+constexpr int kThreads = 192;           // warp 0 producer, warp 1 MMA + TMEM, warps 2..5 dequant + epilogue
+
+struct GemmSmem {
+  uint8_t a[kSlots][kTileBytes];        // fp16 weight tiles, K-major, 128-byte swizzle (1024-aligned)
+  uint8_t b[kSlots][kTileBytes];        // fp16 token tiles, same layout (TMA writes them)
+  uint8_t raw[kRawStages][kRawBytes];   // int4 blocks as stored
+  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+  uint64_t b_full[kSlots], a_full[kSlots], slot_empty[kSlots];
+  uint64_t acc_full;
+  uint32_t tmem_base;
+  int abort;
+  int row_info[kN];                     // epilogue: pair index (routed down) of each token row
+};
+static_assert(kTileBytes % 1024 == 0 && offsetof(GemmSmem, b) % 1024 == 0, "swizzled tiles need 1 KB alignment");
+static_assert(offsetof(GemmSmem, raw) % 128 == 0 && kRawStride % 16 == 0, "bulk copy targets need 16 B");
+static_assert(offsetof(GemmSmem, raw_full) % 8 == 0, "mbarriers need 8 B");
+
+// ------------------------------------------------------------------ tcgen05 / TMA primitives
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major tile whose rows are 128 bytes, with
+// the 128-byte swizzle; 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu)   // start address
+         | (static_cast<uint64_t>(1) << 16)              // leading byte offset (unused with this swizzle)
+         | (static_cast<uint64_t>(1024 >> 4) << 32)      // stride byte offset: 8 rows x 128 B
+         | (static_cast<uint64_t>(1) << 46)              // descriptor version
+         | (static_cast<uint64_t>(2) << 61);             // 128-byte swizzle
+}
+
+// Instruction descriptor: fp16 A and B (both K-major), fp32 accumulator, M x N.
+__host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 accumulator columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float gelu_f(float v, int variant) {
+  if (variant == 1) return 0.5f * v * (1.f + tanhf(0.7978845608028654f * (v + 0.044715f * v * v * v)));
+  return 0.5f * v * (1.f + erff(v * 0.7071067811865476f));
+}
+
+__device__ __forceinline__ bool wait_or_abort(GemmSmem& S, uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_wait_bounded(bar, parity, err)) return true;
+  S.abort = 1;
+  return false;
+}
+
+// ------------------------------------------------------------------ dequantisation
+
+// One 16-row tile x 64-column group of int4 weights (a block as stored: lane
+// fragments + per-row fp16 scale/bias) to fp16 w = s*q + b, written into rows
+// 16*blk .. 16*blk+15 of a swizzled 128-row tile.  Lane (g, t4) owns rows g and
+// g+8 at columns 16*st + 2*t4 (+1) and 16*st + 8 + 2*t4 (+1) of each k16 step.
+__device__ __forceinline__ void dequant_block(const uint8_t* blk, uint8_t* tile, int b16) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const uint4 q = *reinterpret_cast<const uint4*>(blk + lane * 16);
+  const uint2 sb = *reinterpret_cast<const uint2*>(blk + kFragBytes + g * 8);
+  const __half2 s0 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.x & 0xFFFFu)));
+  const __half2 c0 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.x >> 16)));
+  const __half2 s1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.y & 0xFFFFu)));
+  const __half2 c1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.y >> 16)));
+  const __half2 k1024 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400u)));
+  const int r0 = 16 * b16 + g, r1 = r0 + 8;   // r0 & 7 == r1 & 7 == g
+  uint8_t* row0 = tile + r0 * 128;
+  uint8_t* row1 = tile + r1 * 128;
+  const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const uint32_t w = words[st];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      // nibbles r (low half) and r + 4 (high half) as fp16 1024 + q, then exact q
+      const uint32_t bits = ((w >> (4 * r)) & 0x000F000Fu) | 0x64006400u;
+      const __half2 qh = __hsub2(*reinterpret_cast<const __half2*>(&bits), k1024);
+      const bool hi_row = (r & 1) != 0;
+      const __half2 v = __hfma2(qh, hi_row ? s1 : s0, hi_row ? c1 : c0);
+      const int chunk = 2 * st + (r >> 1);
+      uint8_t* dst = (hi_row ? row1 : row0) + (((chunk ^ g) & 7) << 4) + 4 * t4;
+      *reinterpret_cast<__half2*>(dst) = v;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the GEMM
+
+__global__ void __launch_bounds__(kThreads, 1) k_pf_gemm(const __grid_constant__ CUtensorMap tmap_b, PfGemm p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  GemmSmem& S = *reinterpret_cast<GemmSmem*>(smem_raw + pad);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x;
+  const int item = blockIdx.y;
+  const int n_items = p.n_items_dev ? *p.n_items_dev : p.n_items;
+  if (item >= n_items) return;  // uniform over the CTA: nothing allocated yet
+  const int expert = p.items ? p.items[3 * item] : 0;
+  const int row0 = p.items ? p.items[3 * item + 1] : item * kN;
+  const int nrows = p.items ? p.items[3 * item + 2] : min(kN, p.rows_total - row0);
+  const int nG = p.nG;
+  const uint8_t* wbase = p.w + static_cast<long long>(expert) * p.w_stride +
+                         static_cast<size_t>(8 * m_tile) * nG * kGroupBytes;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(&S.raw_full[i], 1);
+      mbar_init(&S.raw_empty[i], 4);
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&S.b_full[i], 1);
+      mbar_init(&S.a_full[i], 4);
+      mbar_init(&S.slot_empty[i], 1);
+    }
+    mbar_init(&S.acc_full, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {  // the whole warp allocates the 128 accumulator columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&S.tmem_base)),
+                 "r"(kN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (warp >= 2 && p.mode == PF_DN_ROUTED)
+    for (int c = threadIdx.x - 64; c < kN; c += 128) S.row_info[c] = c < nrows ? p.pair_of_row[row0 + c] : 0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // producer: raw int4 stages (every kRawG k steps) and one token tile per k step
+      uint32_t raw_issued = 0, b_issued = 0;
+      for (int G = 0; G < nG && !S.abort; ++G) {
+        if (G % kRawG == 0) {
+          const int s = G / kRawG, rs = s % kRawStages;
+          const int ng = min(kRawG, nG - G);
+          if (!wait_or_abort(S, &S.raw_empty[rs], ((s / kRawStages) & 1) ^ 1, p.err)) break;
+          const uint32_t bytes = static_cast<uint32_t>(8 * ng * kGroupBytes);
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&S.raw_full[rs], bytes);
+          for (int t = 0; t < 8; ++t)
+            bulk_g2s(S.raw[rs] + t * kRawStride, wbase + (static_cast<size_t>(t) * nG + G) * kGroupBytes,
+                     static_cast<uint32_t>(ng * kGroupBytes), &S.raw_full[rs]);
+          raw_issued = s + 1;
+        }
+        const int slot = G % kSlots;
+        if (!wait_or_abort(S, &S.slot_empty[slot], ((G / kSlots) & 1) ^ 1, p.err)) break;
+        mbar_arrive_expect_tx(&S.b_full[slot], kTileBytes);
+        tma_load_2d(S.b[slot], &tmap_b, 64 * G, row0, &S.b_full[slot]);
+        b_issued = G + 1;
+      }
+      if (S.abort) {  // let the copies already issued land before the CTA leaves
+        for (uint32_t s = raw_issued > kRawStages ? raw_issued - kRawStages : 0; s < raw_issued; ++s)
+          mbar_wait_bounded(&S.raw_full[s % kRawStages], (s / kRawStages) & 1, p.err);
+        for (uint32_t G = b_issued > kSlots ? b_issued - kSlots : 0; G < b_issued; ++G)
+          mbar_wait_bounded(&S.b_full[G % kSlots], (G / kSlots) & 1, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = f16_idesc(kM, kN);
+      for (int G = 0; G < nG; ++G) {
+        const int slot = G % kSlots;
+        const uint32_t par = (G / kSlots) & 1;
+        if (!wait_or_abort(S, &S.a_full[slot], par, p.err)) break;
+        if (!wait_or_abort(S, &S.b_full[slot], par, p.err)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(S.a[slot]), b0 = smem_u32(S.b[slot]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // four k16 steps: +32 bytes inside the swizzled rows
+          tc_mma(tmem, sw128_desc(a0 + 32 * kk), sw128_desc(b0 + 32 * kk), idesc, (G | kk) != 0);
+        tc_commit(&S.slot_empty[slot]);
+      }
+      tc_commit(&S.acc_full);  // fires once every MMA above has completed
+    }
+  } else {
+    // dequant warps: warp w takes 16-row tiles 2q, 2q+1 of each k step (q = w % 4)
+    const int q = warp & 3;
+    for (int G = 0; G < nG; ++G) {
+      const int s = G / kRawG, rs = s % kRawStages, gi = G % kRawG;
+      if (gi == 0 && !wait_or_abort(S, &S.raw_full[rs], (s / kRawStages) & 1, p.err)) break;
+      const int slot = G % kSlots;
+      if (!wait_or_abort(S, &S.slot_empty[slot], ((G / kSlots) & 1) ^ 1, p.err)) break;
+      dequant_block(S.raw[rs] + (2 * q) * kRawStride + gi * kGroupBytes, S.a[slot], 2 * q);
+      dequant_block(S.raw[rs] + (2 * q + 1) * kRawStride + gi * kGroupBytes, S.a[slot], 2 * q + 1);
+      fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+      __syncwarp();
+      if (lane == 0) mbarrier_arrive(&S.a_full[slot]);
+      if ((gi == kRawG - 1 || G == nG - 1) && lane == 0) mbarrier_arrive(&S.raw_empty[rs]);
+    }
+    // epilogue: this warp reads accumulator lanes 32q .. 32q + 31 (weight rows of the tile)
+    const bool ok = wait_or_abort(S, &S.acc_full, 0, p.err);
+    tc_fence_after();
+    if (ok) {
+      const int row_in_tile = 32 * q + lane;
+      for (int c0 = 0; c0 < kN; c0 += 32) {
+        float v[32];
+        tc_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+        if (p.mode == PF_GU) {
+          // lanes 0-7 / 16-23 hold gate rows, lanes 8-15 / 24-31 the up rows of the same features
+          const int feat = 8 * (8 * m_tile + 2 * q + (lane >> 4)) + (lane & 7);
+          const bool gate_lane = (lane & 8) == 0;
+          bool bad = false;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float up = __shfl_xor_sync(0xFFFFFFFFu, v[j], 8);
+            const int c = c0 + j;
+            if (gate_lane && c < nrows) {
+              const float a = gelu_f(v[j], p.gelu) * up;
+              if (!(fabsf(a) < 65504.f)) bad = true;
+              p.out16[static_cast<size_t>(row0 + c) * p.f_out + feat] = __half_as_ushort(__float2half_rn(a));
+            }
+          }
+          if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.err, ERR_PF_RANGE);
+        } else if (p.mode == PF_DN_ROUTED) {
+          const int R = kM * m_tile + row_in_tile;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = c0 + j;
+            if (c < nrows) p.out32[static_cast<size_t>(S.row_info[c]) * p.d + R] = v[j];
+          }
+        } else {  // PF_DN_SHARED: y = shared + sum_j g_j y_j (top-k order); h' = bf16(h + y)
+          const int R = kM * m_tile + row_in_tile;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int t = row0 + c0 + j;
+            if (c0 + j >= nrows) continue;
+            float y = v[j];
+            for (int jj = 0; jj < p.k; ++jj) {
+              const size_t pr = static_cast<size_t>(t) * p.k + jj;
+              y += p.gates[pr] * p.ytok[pr * p.d + R];
+            }
+            const size_t o = static_cast<size_t>(t) * p.d + R;
+            p.hout[o] = float_to_bf16_bits(bf16_bits_to_float(p.hin[o]) + y);
+            if (p.y_last) p.y_last[o] = y;
+            if (p.dbg_y) p.dbg_y[o] = y;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kN) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ token-side kernels
+
+// One CTA per token: x = RMSnorm(h) (or h) as bf16 and fp16; the sum of squares
+// is taken in a fixed order.  fp16 overflow / underflow of x is flagged.
+__global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int prenorm, float eps, uint16_t* x_bf,
+                                                 uint16_t* x16, uint16_t* dbg_x, uint32_t* err) {
+  __shared__ float red[8];
+  const int t = blockIdx.x;
+  const uint16_t* hr = h + static_cast<size_t>(t) * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += 256) {
+    const float a = bf16_bits_to_float(hr[i]);
+    ss += a * a;
+  }
+#pragma unroll
+  for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float r = 1.f;
+  if (prenorm) {
+    float tot = 0.f;
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    r = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
+  }
+  bool bad = false;
+  for (int i = threadIdx.x; i < d; i += 256) {
+    const uint16_t hb = hr[i];
+    const uint16_t xb = prenorm ? float_to_bf16_bits(bf16_bits_to_float(hb) * r) : hb;
+    const float xf = bf16_bits_to_float(xb);
+    x_bf[static_cast<size_t>(t) * d + i] = xb;
+    const __half xh = __float2half_rn(xf);   // exact unless |x| < 2^-14 (then off by < 2^-25)
+    if (!(fabsf(xf) < 65504.f)) bad = true;
+    x16[static_cast<size_t>(t) * d + i] = __half_as_ushort(xh);
+    if (dbg_x) dbg_x[static_cast<size_t>(t) * d + i] = xb;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, ERR_PF_RANGE);
+}
+
+// Router: a CTA takes kRT tokens and every expert.  Each product W_r[e][i] *
+// x[i] is exact in fp32 (11-bit x 8-bit significands); scaled by 2^40 it is
+// rounded to the nearest integer (ties to even) and summed in int64, so the
+// logit is exact and independent of the summation order.  Then one warp per
+// token takes the top-k (ties to the lower index) and the softmax gates.
+constexpr int kRT = 32;       // tokens per CTA
+constexpr int kRK = 64;       // k chunk
+__global__ void __launch_bounds__(256) k_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias,
+                                                   int T, int d, int E, int k, int32_t* ids, float* gates,
+                                                   int32_t* dbg_ids, float* dbg_gates, uint32_t* err) {
+  // x * 2^40 (exact) and W_r as fp32 while the logits accumulate; the logits afterwards
+  constexpr int kXs = kRT * (kRK + 1) * 4, kWs = 128 * (kRK + 1) * 4, kLg = kRT * 129 * 8;
+  __shared__ __align__(16) unsigned char buf[(kXs + kWs) > kLg ? (kXs + kWs) : kLg];
+  float (*xs)[kRK + 1] = reinterpret_cast<float (*)[kRK + 1]>(buf);
+  float (*ws)[kRK + 1] = reinterpret_cast<float (*)[kRK + 1]>(buf + kXs);
+  long long (*lg)[129] = reinterpret_cast<long long (*)[129]>(buf);
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * kRT;
+  const int tx = tid & 31;                  // experts tx, tx + 32, tx + 64, tx + 96
+  const int ty = tid >> 5;                  // tokens ty, ty + 8, ty + 16, ty + 24
+  long long acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0;
+  bool bad = false;
+  for (int k0 = 0; k0 < d; k0 += kRK) {
+    __syncthreads();
+    for (int i = tid; i < kRT * kRK; i += 256) {
+      const int tt = i / kRK, kk = i % kRK;
+      const int t = t0 + tt;
+      xs[tt][kk] = t < T ? bf16_bits_to_float(x_bf[static_cast<size_t>(t) * d + k0 + kk]) * 1099511627776.0f : 0.f;
+    }
+    for (int i = tid; i < 128 * kRK; i += 256) {
+      const int e = i / kRK, kk = i % kRK;
+      ws[e][kk] = e < E ? __half2float(__ushort_as_half(router_w[static_cast<size_t>(e) * d + k0 + kk])) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < kRK; ++kk) {
+      float xv[4], wv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) xv[a] = xs[ty + 8 * a][kk];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) wv[b] = ws[tx + 32 * b][kk];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float prod = xv[a] * wv[b];
+          if (!(fabsf(prod) < 2251799813685248.0f)) bad = true;   // |x w| must stay below 2^11
+          else acc[a][b] += __float2ll_rn(prod);
+        }
+    }
+  }
+  if (__syncthreads_or(bad) && tid == 0) atomicOr(err, ERR_ROUTER_DOMAIN);  // also: x / w reads are done
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) lg[ty + 8 * a][tx + 32 * b] = acc[a][b];
+  __syncthreads();
+  // one warp per token: bias, top-k, gates
+  const int lane = tid & 31;
+  for (int tt = ty; tt < kRT; tt += 8) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    unsigned long long key[4];
+    int idx[4];
+    bool bbad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = 0ull;
+      idx[i] = 0x7fffffff;
+      if (e < E) {
+        long long v = lg[tt][e];
+        if (bias) {
+          const float bv = bias[static_cast<size_t>(t) * E + e];
+          if (!(fabsf(bv) < 1048576.f)) bbad = true;
+          else v += __float2ll_rn(bv * 1099511627776.0f);
+        }
+        key[i] = static_cast<unsigned long long>(v) ^ 0x8000000000000000ull;
+        idx[i] = e;
+      }
+    }
+    if (__any_sync(0xFFFFFFFFu, bbad) && lane == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
+    // each lane's four candidates sorted by (key desc, index asc)
+#pragma unroll
+    for (int i = 1; i < 4; ++i)
+#pragma unroll
+      for (int j = i; j > 0; --j)
+        if (key[j] > key[j - 1] || (key[j] == key[j - 1] && idx[j] < idx[j - 1])) {
+          const unsigned long long tk = key[j];
+          key[j] = key[j - 1];
+          key[j - 1] = tk;
+          const int ti = idx[j];
+          idx[j] = idx[j - 1];
+          idx[j - 1] = ti;
+        }
+    int head = 0, my_id = 0;
+    long long my_v = 0;
+    for (int j = 0; j < k; ++j) {
+      unsigned long long hk = 0ull;
+      int he = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (i == head) {
+          hk = key[i];
+          he = idx[i];
+        }
+      const bool has = head < 4 && he != 0x7fffffff;
+      const unsigned hi = has ? static_cast<unsigned>(hk >> 32) : 0u;
+      const unsigned lo = has ? static_cast<unsigned>(hk) : 0u;
+      const unsigned mh = __reduce_max_sync(0xFFFFFFFFu, hi);
+      const bool c1 = has && hi == mh;
+      const unsigned ml = __reduce_max_sync(0xFFFFFFFFu, c1 ? lo : 0u);
+      const bool c2 = c1 && lo == ml;
+      const unsigned me = __reduce_min_sync(0xFFFFFFFFu, c2 ? static_cast<unsigned>(he) : 0xFFFFFFFFu);
+      if (c2 && static_cast<unsigned>(he) == me) ++head;
+      if (lane == j) {
+        my_id = static_cast<int>(me);
+        my_v = static_cast<long long>((static_cast<unsigned long long>(mh) << 32 | ml) ^ 0x8000000000000000ull);
+      }
+    }
+    const long long top = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+    float ex = 0.f;
+    if (lane < k) ex = expf(__ll2float_rn(my_v - top) * 9.094947017729282e-13f);
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
+    if (lane < k) {
+      const size_t o = static_cast<size_t>(t) * k + lane;
+      ids[o] = my_id;
+      gates[o] = ex / sum;
+      if (dbg_ids) dbg_ids[o] = my_id;
+      if (dbg_gates) dbg_gates[o] = ex / sum;
+    }
+  }
+}
+
+// Pairs per expert.  One CTA per expert scans every (token, position) pair.
+__global__ void __launch_bounds__(256) k_pf_count(const int32_t* ids, int P, int32_t* cnt) {
+  const int e = blockIdx.x;
+  int n = 0;
+  for (int i = threadIdx.x; i < P; i += 256) n += ids[i] == e;
+  __shared__ int red[8];
+#pragma unroll
+  for (int m = 16; m; m >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = n;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int s = 0;
+    for (int w = 0; w < 8; ++w) s += red[w];
+    cnt[e] = s;
+  }
+}
+
+// Stable placement: expert e's pairs in increasing pair order at
+// [off_e, off_e + n_e), and its 128-row work items.
+__global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, int E, const int32_t* cnt,
+                                                    int32_t* row_pair, int32_t* items, int32_t* n_items) {
+  const int e = blockIdx.x;
+  __shared__ int s_off, s_base;
+  __shared__ int wsum[8];
+  if (threadIdx.x == 0) {
+    int off = 0, it = 0;
+    for (int e2 = 0; e2 < e; ++e2) {
+      off += cnt[e2];
+      it += (cnt[e2] + kPfTileN - 1) / kPfTileN;
+    }
+    s_off = off;
+    s_base = 0;
+    const int n_e = cnt[e];
+    for (int i = 0; i * kPfTileN < n_e; ++i) {
+      items[3 * (it + i)] = e;
+      items[3 * (it + i) + 1] = off + i * kPfTileN;
+      items[3 * (it + i) + 2] = min(kPfTileN, n_e - i * kPfTileN);
+    }
+    if (e == E - 1) *n_items = it + (n_e + kPfTileN - 1) / kPfTileN;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int c0 = 0; c0 < P; c0 += 256) {
+    const int i = c0 + threadIdx.x;
+    const bool mine = i < P && ids[i] == e;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, mine);
+    if (lane == 0) wsum[w] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w2 = 0; w2 < 8; ++w2) {
+      if (w2 < w) before += wsum[w2];
+      total += wsum[w2];
+    }
+    if (mine) row_pair[s_off + s_base + before + __popc(bal & ((1u << lane) - 1u))] = i;
+    __syncthreads();
+    if (threadIdx.x == 0) s_base += total;
+    __syncthreads();
+  }
+}
+
+// Row r of the expert-ordered matrix = fp16 x of the pair's token.
+__global__ void __launch_bounds__(256) k_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k,
+                                                   uint16_t* xp) {
+  const int r = blockIdx.x;
+  if (r >= P) return;
+  const int t = row_pair[r] / k;
+  const uint4* src = reinterpret_cast<const uint4*>(x16 + static_cast<size_t>(t) * d);
+  uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(r) * d);
+  for (int i = threadIdx.x; i < d / 8; i += 256) dst[i] = src[i];
+}
+
+}  // namespace
+
+size_t pf_gemm_smem() { return sizeof(GemmSmem) + 1024; }
+
+cudaError_t pf_set_attrs() {
+  return cudaFuncSetAttribute((const void*)k_pf_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(pf_gemm_smem()));
+}
+
+cudaError_t launch_pf_gemm(const CUtensorMap& tmap_b, const PfGemm& p, int m_tiles, int max_items, cudaStream_t s) {
+  if (m_tiles <= 0 || max_items <= 0) return cudaSuccess;
+  k_pf_gemm<<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(), s>>>(tmap_b, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
+                           uint16_t* dbg_x, uint32_t* err, cudaStream_t s) {
+  k_pf_prep<<<T, 256, 0, s>>>(h, d, prenorm, eps, x_bf, x16, dbg_x, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
+                             int k, int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err,
+                             cudaStream_t s) {
+  k_pf_router<<<(T + kRT - 1) / kRT, 256, 0, s>>>(x_bf, router_w, bias, T, d, E, k, ids, gates, dbg_ids, dbg_gates,
+                                                  err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int32_t* cnt, int32_t* row_pair, int32_t* items,
+                           int32_t* n_items, cudaStream_t s) {
+  k_pf_count<<<E, 256, 0, s>>>(ids, P, cnt);
+  k_pf_scatter<<<E, 256, 0, s>>>(ids, P, E, cnt, row_pair, items, n_items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,
+                             cudaStream_t s) {
+  k_pf_gather<<<P, 256, 0, s>>>(x16, row_pair, P, d, k, xp);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
