@@ -399,6 +399,165 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------- prefill workload
+
+PF_TOKENS = 4096
+PF_SEED = 4
+
+
+def prefill_flops_per_layer(sh, T):
+    """Dense FLOPs of one prefill layer: routed gate/up + down per (token, k) pair, shared per token."""
+    routed = 2 * T * sh.top_k * 3 * sh.d * sh.f
+    shared = 2 * T * 3 * sh.d * sh.f_shared
+    return routed + shared
+
+
+def prefill_config(sh):
+    return {"workload": f"prefill{PF_TOKENS}_resident_mixture", "layers": N_LAYERS, "tokens": PF_TOKENS,
+            "d": sh.d, "f": sh.f, "f_shared": sh.f_shared, "experts": sh.n_experts, "top_k": sh.top_k,
+            "group": sh.group, "weights": "int4 affine g64, fp16 scale+bias", "residency": "all experts in HBM",
+            "routing": "router logits + 50/50 uniform/Zipf(0.8) bias over a per-layer permutation",
+            "matrix_path": "int4 -> fp16 tiles, tcgen05 fp16 x fp16 -> fp32",
+            "l2": "no flush: 12.9 GB of weights and 0.7 GB of activations per step vs 129 MB L2"}
+
+
+def load_bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def run_ours_prefill(args):
+    import numpy as np
+    import torch
+
+    import bit_routed_expert_router_gb300 as moe
+    from workload import bias_from_targets, gen_hidden, gen_layer, mixture_targets
+
+    ws, rank, local = dist_env()
+    dist = maybe_init_dist(ws, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sh = _shape()
+    T = PF_TOKENS
+    cfg = moe.make_config(sh.d, sh.f, sh.f_shared, sh.n_experts, sh.top_k, n_layers=N_LAYERS, prenorm=1,
+                          max_tokens=T)
+    st, ctx = moe.moe_create(cfg, local)
+    if st != moe.MOE_OK:
+        raise moe.MoeError(st, moe.moe_last_error(None))
+    for layer in range(N_LAYERS):
+        w = gen_layer(sh, seed=PF_SEED, layer=layer, device=dev)
+        moe.check(moe.moe_init_layer(ctx, layer, w["router_w"], w["experts"], w["shared"]), ctx)
+        del w
+    moe.check(moe.moe_test_hook(ctx, moe.HOOK_PREFILL_TC, 1), ctx)
+    H_host = gen_hidden(T, sh.d, seed=PF_SEED)
+    tg = mixture_targets(T, N_LAYERS, sh.n_experts, sh.top_k, seed=PF_SEED)
+    bias_host = np.ascontiguousarray(bias_from_targets(tg, sh.n_experts).astype(np.float32).transpose(1, 0, 2))
+    H = H_host.to(dev)
+    bias = torch.from_numpy(bias_host).to(dev)           # [L, T, E]
+    out = torch.empty_like(H)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.check(moe.moe_prefill(ctx, H, T, 0, N_LAYERS, bias, out, None, stream), ctx)
+
+    for _ in range(args.warmup):
+        step()
+    moe.check(moe.moe_sync(ctx, stream), ctx)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+    moe.check(moe.moe_sync(ctx, stream), ctx)
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_max, units = aggregate(dist, elapsed, float(args.steps * T))
+    value = units / t_max
+    clocks = clk.result()
+
+    # per-kind durations (event pairs around the routing/grouping kernels and the four GEMMs of a layer)
+    moe.check(moe.moe_profile(ctx, True), ctx)
+    moe.moe_get_profile(ctx)
+    step()
+    moe.check(moe.moe_profile(ctx, False), ctx)
+    _, prof = moe.moe_get_profile(ctx)
+    kinds = {moe.KERNEL_KINDS[i]: {"launches": n, "ms": t} for i, (n, t) in enumerate(prof) if n}
+    shares = {k: round(v["ms"] / sum(x["ms"] for x in kinds.values()), 4) for k, v in kinds.items()}
+    g = kinds["prefill_tcgen05_gemm"]
+    flops_layer = prefill_flops_per_layer(sh, T)
+    dur = g["ms"] / g["launches"] / 1e3                  # one layer's four GEMM launches
+    peak_burst, peak_sus, peak_kind = load_bf16_peak()
+    achieved = flops_layer / dur / 1e12
+
+    # end to end with host buffers
+    h_pin = H_host.pin_memory()
+    b_pin = torch.from_numpy(bias_host).pin_memory()
+    o_pin = torch.empty_like(h_pin).pin_memory()
+    h_dev = torch.empty_like(H)
+    b_dev = torch.empty_like(bias)
+
+    def e2e_step():
+        h_dev.copy_(h_pin, non_blocking=True)
+        b_dev.copy_(b_pin, non_blocking=True)
+        moe.check(moe.moe_prefill(ctx, h_dev, T, 0, N_LAYERS, b_dev, out, None, stream), ctx)
+        o_pin.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(1, min(args.steps, 3))
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    f1.record(stream)
+    f1.synchronize()
+    e2e_t, e2e_units = aggregate(dist, f0.elapsed_time(f1) / 1e3, float(n_e2e * T))
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        layers_cpu = gen_cpu_layers(2)
+        mean_s, n, cores = oracle_token_layer_seconds(layers_cpu, H_host, None, 64, args.cpu_budget)
+        cpu = {"value": 1.0 / (N_LAYERS * mean_s), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n} (token, layer) evaluations on layers 0-1, {mean_s:.2f} s each, "
+                         f"extrapolated x{N_LAYERS} layers per token"}
+    moe.moe_destroy(ctx)
+    if rank == 0:
+        line = {
+            "metric": "MoE prefill tokens/s (30-layer routed+shared FFN, T=4096)", "value": value,
+            "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16xint4->f32 (router int64)", "data": "synthetic",
+            "config": prefill_config(sh),
+            "roofline": {"bound": "tensor", "kernel": "prefill_tcgen05_gemm", "achieved": achieved,
+                         "peak": peak_sus, "peak_kind": f"{peak_kind} bf16 sustained (fp16 runs at the bf16 rate)",
+                         "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": None,
+                         "flops_per_launch": flops_layer, "avg_launch_us": dur * 1e6},
+            "kernel_shares": shares,
+            "e2e": {"value": e2e_units / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": int(H.numel() * 2 + bias.numel() * 4),
+                    "d2h_bytes_per_step": int(out.numel() * 2)},
+            "gpu_launches": int(round(N_LAYERS * 9 * args.steps)),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,6 +566,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
+                    help="decode: the B=1 30-layer decode stack (the headline); prefill: T=4096 tokens per step")
     ap.add_argument("--layers", type=int, default=30,
                     help="layers in the stack (30 is the benchmark; fewer only for small profiler captures)")
     args = ap.parse_args(argv)
@@ -416,6 +577,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "prefill":
+        return run_ours_prefill(args)
     return run_ours(args)
 
 

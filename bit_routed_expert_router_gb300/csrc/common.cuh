@@ -120,6 +120,44 @@ __device__ __forceinline__ float half_hi(uint32_t v) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Exact sum of products rounded onto the 2^-40 grid, without 64-bit float ->
+// integer conversions (which issue at a small fraction of the fp32 rate).
+// A product v = x * w * 2^40 (|v| < 2^51, at most 24 significant bits) is cut
+// as RNE(v) = q2 * 2^44 + q1 * 2^22 + q0: adding and subtracting 1.5 * 2^67
+// rounds v to a multiple of 2^44 (the binade of that constant has that unit),
+// the remainder is exact and is cut the same way at 2^22, and the last
+// remainder (|r| <= 2^21) is rounded to an integer, ties to even, by adding
+// 1.5 * 2^23.  Each q is the difference of the sum's bit pattern and the
+// constant's, so the three partial sums are plain int32 additions of bit
+// patterns, corrected by the number of terms at the end.  At most 512 terms
+// may go into one accumulator before fix40_value.
+struct Fix40 {
+  uint32_t b2 = 0, b1 = 0, b0 = 0;   // sums of bit patterns (mod 2^32)
+  uint32_t n = 0;                    // terms
+};
+
+__device__ __forceinline__ void fix40_add(Fix40& A, float v) {
+  const float M2 = 221360928884514619392.0f;   // 1.5 * 2^67
+  const float M1 = 52776558133248.0f;          // 1.5 * 2^45
+  const float M0 = 12582912.0f;                // 1.5 * 2^23
+  const float s2 = __fadd_rn(v, M2);
+  const float r2 = __fsub_rn(v, __fsub_rn(s2, M2));
+  const float s1 = __fadd_rn(r2, M1);
+  const float r1 = __fsub_rn(r2, __fsub_rn(s1, M1));
+  const float s0 = __fadd_rn(r1, M0);
+  A.b2 += __float_as_uint(s2);
+  A.b1 += __float_as_uint(s1);
+  A.b0 += __float_as_uint(s0);
+  A.n += 1u;
+}
+
+__device__ __forceinline__ long long fix40_value(const Fix40& A) {
+  const int q2 = static_cast<int>(A.b2 - A.n * 0x61400000u);   // bit pattern of 1.5 * 2^67
+  const int q1 = static_cast<int>(A.b1 - A.n * 0x56400000u);   // 1.5 * 2^45
+  const int q0 = static_cast<int>(A.b0 - A.n * 0x4B400000u);   // 1.5 * 2^23
+  return (static_cast<long long>(q2) << 44) + (static_cast<long long>(q1) << 22) + q0;
+}
+
 __device__ __forceinline__ int64_t shfl_xor_i64(int64_t v, int m) {
   int lo = static_cast<int>(v & 0xFFFFFFFFLL);
   int hi = static_cast<int>(v >> 32);

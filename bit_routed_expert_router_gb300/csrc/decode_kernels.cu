@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256) k_router(KParams p) {
   if (e < p.E) {
     const uint4* wr = reinterpret_cast<const uint4*>(p.router_w + static_cast<size_t>(e) * d);
     const uint4* xv4 = reinterpret_cast<const uint4*>(xs);
-    long long acc = 0;
+    Fix40 fx;
     bool bad = false;
     for (int c = lane; c < d / 8; c += 32) {
       const uint4 wv = __ldg(wr + c);
@@ -87,14 +87,13 @@ __global__ void __launch_bounds__(256) k_router(KParams p) {
           const float pw = hh ? half_hi(wa[i]) : half_lo(wa[i]);
           const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xa[i] >> 16) : (xa[i] & 0xFFFFu)));
           const float prod = pw * px;  // exact: 11-bit x 8-bit significands
-          if (!(fabsf(prod) < 2048.f)) {
-            bad = true;
-          } else {
-            acc += __float2ll_rn(prod * 1099511627776.0f);  // RNE onto the 2^-40 grid
-          }
+          const bool ok = fabsf(prod) < 2048.f;
+          bad |= !ok;
+          fix40_add(fx, ok ? prod * 1099511627776.0f : 0.f);  // RNE onto the 2^-40 grid, summed exactly
         }
       }
     }
+    long long acc = fix40_value(fx);
 #pragma unroll
     for (int m = 16; m; m >>= 1) acc += shfl_xor_i64(acc, m);
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);

@@ -77,7 +77,7 @@ struct PfGemm {
   int d, k, gelu;
   uint16_t* out16;                     // PF_GU: fp16 [rows][f_out]
   int f_out;
-  float* out32;                        // PF_DN_ROUTED: fp32 [T*k][d] by pair
+  float* out32;                        // PF_DN_ROUTED: fp32 [T*k][d] by pair; PF_DN_SHARED: fp32 [T][d]
   const int32_t* pair_of_row;          // PF_DN_ROUTED: pair of each expert-ordered row
   const float* gates;                  // PF_DN_SHARED: [T][k]
   const float* ytok;                   // PF_DN_SHARED: [T*k][d]
@@ -86,6 +86,7 @@ struct PfGemm {
   float* y_last;                       // PF_DN_SHARED: optional fp32 [T][d]
   float* dbg_y;                        // PF_DN_SHARED: optional fp32 [T][d]
   uint32_t* err;
+  unsigned long long* tl;              // optional: 16 event times (ns) of CTA (0, 0), null = off
 };
 
 size_t pf_gemm_smem();
@@ -94,10 +95,12 @@ cudaError_t launch_pf_gemm(const CUtensorMap& tmap_b, const PfGemm& p, int m_til
 cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
                            uint16_t* dbg_x, uint32_t* err, cudaStream_t s);
 cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
-                             int k, int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err,
-                             cudaStream_t s);
+                             int k, long long* logits, int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates,
+                             uint32_t* err, int n_sm, cudaStream_t s);
 cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int32_t* cnt, int32_t* row_pair, int32_t* items,
                            int32_t* n_items, cudaStream_t s);
+cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* gates, const uint16_t* hin,
+                              uint16_t* hout, float* y_last, float* dbg_y, int T, int d, int k, cudaStream_t s);
 cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,
                              cudaStream_t s);
 

@@ -129,6 +129,9 @@ struct moe_ctx {
   uint16_t* pf_h[2] = {nullptr, nullptr};
   int32_t *pf_ids = nullptr, *pf_cnt = nullptr, *pf_rowpair = nullptr, *pf_items = nullptr, *pf_nitems = nullptr;
   float *pf_gates = nullptr, *pf_ytok = nullptr;
+  long long* pf_logits = nullptr;
+  float* pf_ys = nullptr;
+  unsigned long long* pf_timeline = nullptr;   // test hook 8: [4][16] GEMM event times of the first layer
   CUtensorMap pf_map_xp{}, pf_map_x16{}, pf_map_ar{}, pf_map_as{};
   unsigned long long* p_timeline = nullptr;   // caller device buffer [n_layers][16], test hook 5
   // per-kernel timing
@@ -950,9 +953,11 @@ moe_status pf_alloc(moe_ctx* ctx) {
   ctx->pf_items = dalloc<int32_t>(3 * (P / kPfTileN + c.n_experts + 1), o, nb);
   ctx->pf_nitems = dalloc<int32_t>(1, o, nb);
   ctx->pf_ytok = dalloc<float>(P * c.d, o, nb);
+  ctx->pf_logits = dalloc<long long>(T * c.n_experts, o, nb);
+  ctx->pf_ys = dalloc<float>(T * c.d, o, nb);
   if (!ctx->pf_xbf || !ctx->pf_x16 || !ctx->pf_xp || !ctx->pf_ar || !ctx->pf_as || !ctx->pf_h[0] || !ctx->pf_h[1] ||
       !ctx->pf_ids || !ctx->pf_gates || !ctx->pf_cnt || !ctx->pf_rowpair || !ctx->pf_items || !ctx->pf_nitems ||
-      !ctx->pf_ytok)
+      !ctx->pf_ytok || !ctx->pf_logits || !ctx->pf_ys)
     return fail(ctx, MOE_ENOMEM, "prefill scratch (%zu bytes for %zu tokens) does not fit", nb, T);
   if (!encode_rows(&ctx->pf_map_xp, ctx->pf_xp, c.d, static_cast<long long>(P)) ||
       !encode_rows(&ctx->pf_map_x16, ctx->pf_x16, c.d, static_cast<long long>(T)) ||
@@ -975,9 +980,9 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   PROF(4, s);
   CK(launch_pf_prep(hin, T, d, c.prenorm, c.norm_eps, ctx->pf_xbf, ctx->pf_x16,
                     dbg && ctx->dbg_x ? ctx->dbg_x + xo * d : nullptr, ctx->err_word, s));
-  CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_ids,
-                      ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
-                      dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr, ctx->err_word, s));
+  CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_logits,
+                      ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
+                      dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr, ctx->err_word, ctx->n_sm, s));
   CK(launch_pf_plan(ctx->pf_ids, P, E, ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items, ctx->pf_nitems, s));
   CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
   PROF(-1, s);
@@ -986,6 +991,7 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   const int max_items = P / kPfTileN + E + 1;
   const int t_items = (T + kPfTileN - 1) / kPfTileN;
   PfGemm g{};
+  g.tl = nullptr;
   g.d = d;
   g.k = k;
   g.gelu = c.gelu_variant;
@@ -1001,6 +1007,7 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   a.mode = PF_GU;
   a.out16 = ctx->pf_ar;
   a.f_out = c.f;
+  if (ctx->pf_timeline && rel == 0) a.tl = ctx->pf_timeline;
   CK(launch_pf_gemm(ctx->pf_map_xp, a, c.f / 64, max_items, s));
   // shared gate/up over every token
   PfGemm b = g;
@@ -1011,6 +1018,7 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   b.mode = PF_GU;
   b.out16 = ctx->pf_as;
   b.f_out = c.f_shared;
+  if (ctx->pf_timeline && rel == 0) b.tl = ctx->pf_timeline + 16;
   CK(launch_pf_gemm(ctx->pf_map_x16, b, c.f_shared / 64, t_items, s));
   // routed down: per pair, fp32 [T*k][d]
   PfGemm r = g;
@@ -1022,21 +1030,20 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   r.mode = PF_DN_ROUTED;
   r.out32 = ctx->pf_ytok;
   r.pair_of_row = ctx->pf_rowpair;
+  if (ctx->pf_timeline && rel == 0) r.tl = ctx->pf_timeline + 32;
   CK(launch_pf_gemm(ctx->pf_map_ar, r, d / 128, max_items, s));
-  // shared down + routed combine (top-k order) + residual
+  // shared down, then the combine: shared + routed in top-k order + residual
   PfGemm q = g;
   q.w = L.shared + gu_s;
   q.nG = c.f_shared / 64;
   q.n_items = t_items;
   q.rows_total = T;
   q.mode = PF_DN_SHARED;
-  q.gates = ctx->pf_gates;
-  q.ytok = ctx->pf_ytok;
-  q.hin = hin;
-  q.hout = hout;
-  q.y_last = rel == n_rel - 1 ? y_last : nullptr;
-  q.dbg_y = dbg && ctx->dbg_y ? ctx->dbg_y + xo * d : nullptr;
+  q.out32 = ctx->pf_ys;
+  if (ctx->pf_timeline && rel == 0) q.tl = ctx->pf_timeline + 48;
   CK(launch_pf_gemm(ctx->pf_map_as, q, d / 128, t_items, s));
+  CK(launch_pf_combine(ctx->pf_ys, ctx->pf_ytok, ctx->pf_gates, hin, hout, rel == n_rel - 1 ? y_last : nullptr,
+                       dbg && ctx->dbg_y ? ctx->dbg_y + xo * d : nullptr, T, d, k, s));
   PROF(-1, s);
   return MOE_OK;
 }
@@ -1189,6 +1196,9 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
       }
       return MOE_OK;
     }
+    case 8:  // event times of the prefill GEMMs' CTA (0, 0), first layer of a call, into [4][16] (0 = off)
+      ctx->pf_timeline = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));
+      return MOE_OK;
     case 7:  // tcgen05 batched prefill on/off; asking for it where it cannot run is an error
       if (value != 0 && !ctx->pf_ok)
         return fail(ctx, MOE_ESTATE, "tcgen05 prefill unavailable for this configuration or device");

@@ -536,7 +536,7 @@ __device__ bool task_router(const PParams& p, Smem& S, int rel, int l, int e_row
   const int lane = threadIdx.x & 31;
   const uint4* wr = reinterpret_cast<const uint4*>(stage);
   const uint4* xv4 = reinterpret_cast<const uint4*>(S.xs);
-  long long acc = 0;
+  Fix40 fx;
   bool bad = false;
   for (int c0 = cw * 32; c0 < p.d / 8; c0 += 32 * kNC) {
     const int c = min(c0 + lane, p.d / 8 - 1);
@@ -553,11 +553,13 @@ __device__ bool task_router(const PParams& p, Smem& S, int rel, int l, int e_row
         const float pw = hh ? half_hi(wa[i]) : half_lo(wa[i]);
         const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xa[i] >> 16) : (xa[i] & 0xFFFFu)));
         const float prod = pw * px;  // exact: 11-bit x 8-bit significands
-        if (!(fabsf(prod) < 2048.f)) bad = true;
-        else acc += __float2ll_rn(prod * 1099511627776.0f);  // RNE onto the 2^-40 grid
+        const bool ok = fabsf(prod) < 2048.f;
+        bad |= !ok;
+        fix40_add(fx, ok ? prod * 1099511627776.0f : 0.f);  // RNE onto the 2^-40 grid, summed exactly
       }
     }
   }
+  long long acc = fix40_value(fx);
 #pragma unroll
   for (int m = 16; m; m >>= 1) acc += shfl_xor_i64(acc, m);
   if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);

@@ -37,13 +37,14 @@ namespace {
 
 constexpr int kM = 128;                 // weight rows per CTA tile
 constexpr int kN = kPfTileN;            // token rows per CTA tile
-constexpr int kSlots = 4;               // k-step slots (A + B tiles)
+constexpr int kSlots = 2;               // k-step slots (A + B tiles)
 constexpr int kRawG = 4;                // int4 groups per raw stage
 constexpr int kRawStages = 2;
 constexpr int kTileBytes = 128 * 128;   // one 128-row x 64-col fp16 tile (16 KB)
 constexpr int kRawStride = kRawG * kGroupBytes;   // bytes of one 16-row tile in a raw stage
 constexpr int kRawBytes = 8 * kRawStride;         // 8 tiles of 16 rows = 128 rows
-constexpr int kThreads = 192;           // warp 0 producer, warp 1 MMA + TMEM, warps 2..5 dequant + epilogue
+constexpr int kDqWarps = 8;             // dequant + epilogue warps, one 16-row tile each per k step
+constexpr int kThreads = 32 * (2 + kDqWarps);  // warp 0 producer, warp 1 MMA + TMEM, warps 2..9 dequant + epilogue
 
 struct GemmSmem {
   uint8_t a[kSlots][kTileBytes];        // fp16 weight tiles, K-major, 128-byte swizzle (1024-aligned)
@@ -121,6 +122,15 @@ __device__ __forceinline__ float gelu_f(float v, int variant) {
   return 0.5f * v * (1.f + erff(v * 0.7071067811865476f));
 }
 
+// Event time k of CTA (0, 0) when a timeline is attached (diagnostics).
+__device__ __forceinline__ void pf_stamp(const PfGemm& p, int k) {
+  if (p.tl && blockIdx.x == 0 && blockIdx.y == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p.tl[k] = t;
+  }
+}
+
 __device__ __forceinline__ bool wait_or_abort(GemmSmem& S, uint64_t* bar, uint32_t parity, uint32_t* err) {
   if (mbar_wait_bounded(bar, parity, err)) return true;
   S.abort = 1;
@@ -165,7 +175,8 @@ __device__ __forceinline__ void dequant_block(const uint8_t* blk, uint8_t* tile,
 
 // ------------------------------------------------------------------ the GEMM
 
-__global__ void __launch_bounds__(kThreads, 1) k_pf_gemm(const __grid_constant__ CUtensorMap tmap_b, PfGemm p) {
+// Two CTAs share an SM, so one's epilogue overlaps the other's main loop.
+__global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__ CUtensorMap tmap_b, PfGemm p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   GemmSmem& S = *reinterpret_cast<GemmSmem*>(smem_raw + pad);
@@ -174,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pf_gemm(const __grid_constant__
   const int item = blockIdx.y;
   const int n_items = p.n_items_dev ? *p.n_items_dev : p.n_items;
   if (item >= n_items) return;  // uniform over the CTA: nothing allocated yet
+  if (threadIdx.x == 0) pf_stamp(p, 0);
   const int expert = p.items ? p.items[3 * item] : 0;
   const int row0 = p.items ? p.items[3 * item + 1] : item * kN;
   const int nrows = p.items ? p.items[3 * item + 2] : min(kN, p.rows_total - row0);
@@ -184,11 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_pf_gemm(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
       mbar_init(&S.raw_full[i], 1);
-      mbar_init(&S.raw_empty[i], 4);
+      mbar_init(&S.raw_empty[i], kDqWarps);
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&S.b_full[i], 1);
-      mbar_init(&S.a_full[i], 4);
+      mbar_init(&S.a_full[i], kDqWarps);
       mbar_init(&S.slot_empty[i], 1);
     }
     mbar_init(&S.acc_full, 1);
@@ -202,15 +214,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_pf_gemm(const __grid_constant__
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (warp >= 2 && p.mode == PF_DN_ROUTED)
-    for (int c = threadIdx.x - 64; c < kN; c += 128) S.row_info[c] = c < nrows ? p.pair_of_row[row0 + c] : 0;
+    for (int c = threadIdx.x - 64; c < kN; c += 32 * kDqWarps) S.row_info[c] = c < nrows ? p.pair_of_row[row0 + c] : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  if (threadIdx.x == 0) pf_stamp(p, 1);
 
   if (warp == 0) {
     if (lane == 0) {
-      // producer: raw int4 stages (every kRawG k steps) and one token tile per k step
+      // producer: the tile's weights go to L2 at once (HBM streams them at full rate while the
+      // ring below is filled from L2), then raw int4 stages (every kRawG k steps) and one
+      // token tile per k step
+      for (int t = 0; t < 8; ++t)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(wbase + static_cast<size_t>(t) * nG * kGroupBytes),
+                     "r"(static_cast<uint32_t>(nG * kGroupBytes))
+                     : "memory");
       uint32_t raw_issued = 0, b_issued = 0;
       for (int G = 0; G < nG && !S.abort; ++G) {
         if (G % kRawG == 0) {
@@ -245,7 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_pf_gemm(const __grid_constant__
         const int slot = G % kSlots;
         const uint32_t par = (G / kSlots) & 1;
         if (!wait_or_abort(S, &S.a_full[slot], par, p.err)) break;
+        if (G == 0) pf_stamp(p, 3);
         if (!wait_or_abort(S, &S.b_full[slot], par, p.err)) break;
+        if (G == 0) pf_stamp(p, 4);
+        if (G == p.nG - 1) pf_stamp(p, 5);
         tc_fence_after();
         const uint32_t a0 = smem_u32(S.a[slot]), b0 = smem_u32(S.b[slot]);
 #pragma unroll
@@ -256,26 +278,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_pf_gemm(const __grid_constant__
       tc_commit(&S.acc_full);  // fires once every MMA above has completed
     }
   } else {
-    // dequant warps: warp w takes 16-row tiles 2q, 2q+1 of each k step (q = w % 4)
-    const int q = warp & 3;
+    // dequant warps: warp w takes 16-row tile w - 2 of each k step; in the epilogue it reads
+    // accumulator lanes 32q .. 32q + 31 (q = w % 4, the lanes its warp may access) and the
+    // column half (w - 2) / 4
+    const int dw = warp - 2, q = warp & 3, c_lo = (dw >> 2) * (kN / 2);
     for (int G = 0; G < nG; ++G) {
       const int s = G / kRawG, rs = s % kRawStages, gi = G % kRawG;
       if (gi == 0 && !wait_or_abort(S, &S.raw_full[rs], (s / kRawStages) & 1, p.err)) break;
+      if (G == 0 && threadIdx.x == 64) pf_stamp(p, 2);
       const int slot = G % kSlots;
       if (!wait_or_abort(S, &S.slot_empty[slot], ((G / kSlots) & 1) ^ 1, p.err)) break;
-      dequant_block(S.raw[rs] + (2 * q) * kRawStride + gi * kGroupBytes, S.a[slot], 2 * q);
-      dequant_block(S.raw[rs] + (2 * q + 1) * kRawStride + gi * kGroupBytes, S.a[slot], 2 * q + 1);
+      dequant_block(S.raw[rs] + dw * kRawStride + gi * kGroupBytes, S.a[slot], dw);
       fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
       __syncwarp();
       if (lane == 0) mbarrier_arrive(&S.a_full[slot]);
       if ((gi == kRawG - 1 || G == nG - 1) && lane == 0) mbarrier_arrive(&S.raw_empty[rs]);
     }
     // epilogue: this warp reads accumulator lanes 32q .. 32q + 31 (weight rows of the tile)
+    if (threadIdx.x == 64) pf_stamp(p, 6);
     const bool ok = wait_or_abort(S, &S.acc_full, 0, p.err);
+    if (threadIdx.x == 64) pf_stamp(p, 7);
     tc_fence_after();
     if (ok) {
       const int row_in_tile = 32 * q + lane;
-      for (int c0 = 0; c0 < kN; c0 += 32) {
+      for (int c0 = c_lo; c0 < c_lo + kN / 2; c0 += 32) {
         float v[32];
         tc_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
         if (p.mode == PF_GU) {
@@ -301,28 +327,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_pf_gemm(const __grid_constant__
             const int c = c0 + j;
             if (c < nrows) p.out32[static_cast<size_t>(S.row_info[c]) * p.d + R] = v[j];
           }
-        } else {  // PF_DN_SHARED: y = shared + sum_j g_j y_j (top-k order); h' = bf16(h + y)
+        } else {  // PF_DN_SHARED: the shared expert's output per token, fp32 [T][d]
           const int R = kM * m_tile + row_in_tile;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int t = row0 + c0 + j;
-            if (c0 + j >= nrows) continue;
-            float y = v[j];
-            for (int jj = 0; jj < p.k; ++jj) {
-              const size_t pr = static_cast<size_t>(t) * p.k + jj;
-              y += p.gates[pr] * p.ytok[pr * p.d + R];
-            }
-            const size_t o = static_cast<size_t>(t) * p.d + R;
-            p.hout[o] = float_to_bf16_bits(bf16_bits_to_float(p.hin[o]) + y);
-            if (p.y_last) p.y_last[o] = y;
-            if (p.dbg_y) p.dbg_y[o] = y;
-          }
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < nrows) p.out32[static_cast<size_t>(row0 + c0 + j) * p.d + R] = v[j];
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) pf_stamp(p, 8);
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kN) : "memory");
@@ -367,142 +383,147 @@ __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int p
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, ERR_PF_RANGE);
 }
 
-// Router: a CTA takes kRT tokens and every expert.  Each product W_r[e][i] *
-// x[i] is exact in fp32 (11-bit x 8-bit significands); scaled by 2^40 it is
-// rounded to the nearest integer (ties to even) and summed in int64, so the
-// logit is exact and independent of the summation order.  Then one warp per
-// token takes the top-k (ties to the lower index) and the softmax gates.
+// Router logits: a CTA takes 32 tokens x 32 experts over one slice of d.  Each
+// product W_r[e][i] * x[i] is exact in fp32 (11-bit x 8-bit significands);
+// scaled by 2^40 it is rounded to the nearest integer (ties to even) and summed
+// exactly (Fix40 per 64-wide chunk, int64 across chunks), so a logit does not
+// depend on the order of its terms or on how d is sliced.  With several slices
+// (small T, to fill the GPU) the slices meet in int64 atomic adds.
 constexpr int kRT = 32;       // tokens per CTA
+constexpr int kRE = 32;       // experts per CTA
 constexpr int kRK = 64;       // k chunk
-__global__ void __launch_bounds__(256) k_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias,
-                                                   int T, int d, int E, int k, int32_t* ids, float* gates,
-                                                   int32_t* dbg_ids, float* dbg_gates, uint32_t* err) {
-  // x * 2^40 (exact) and W_r as fp32 while the logits accumulate; the logits afterwards
-  constexpr int kXs = kRT * (kRK + 1) * 4, kWs = 128 * (kRK + 1) * 4, kLg = kRT * 129 * 8;
-  __shared__ __align__(16) unsigned char buf[(kXs + kWs) > kLg ? (kXs + kWs) : kLg];
-  float (*xs)[kRK + 1] = reinterpret_cast<float (*)[kRK + 1]>(buf);
-  float (*ws)[kRK + 1] = reinterpret_cast<float (*)[kRK + 1]>(buf + kXs);
-  long long (*lg)[129] = reinterpret_cast<long long (*)[129]>(buf);
+__global__ void __launch_bounds__(256) k_pf_logits(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
+                                                   int E, int k_slice, long long* logits, uint32_t* err) {
+  __shared__ float xs[kRT][kRK + 1];   // x * 2^40 (exact)
+  __shared__ float ws[kRE][kRK + 1];   // W_r as fp32
   const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * kRT;
-  const int tx = tid & 31;                  // experts tx, tx + 32, tx + 64, tx + 96
-  const int ty = tid >> 5;                  // tokens ty, ty + 8, ty + 16, ty + 24
-  long long acc[4][4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) acc[a][b] = 0;
+  const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE, kb = blockIdx.z * k_slice;
+  const int tx = tid & 15;             // experts e0 + tx, e0 + tx + 16
+  const int ty = tid >> 4;             // tokens t0 + ty, t0 + ty + 16
+  long long acc[2][2] = {{0, 0}, {0, 0}};
   bool bad = false;
-  for (int k0 = 0; k0 < d; k0 += kRK) {
+  for (int k0 = kb; k0 < kb + k_slice; k0 += kRK) {
     __syncthreads();
     for (int i = tid; i < kRT * kRK; i += 256) {
-      const int tt = i / kRK, kk = i % kRK;
-      const int t = t0 + tt;
+      const int tt = i / kRK, kk = i % kRK, t = t0 + tt;
       xs[tt][kk] = t < T ? bf16_bits_to_float(x_bf[static_cast<size_t>(t) * d + k0 + kk]) * 1099511627776.0f : 0.f;
     }
-    for (int i = tid; i < 128 * kRK; i += 256) {
-      const int e = i / kRK, kk = i % kRK;
-      ws[e][kk] = e < E ? __half2float(__ushort_as_half(router_w[static_cast<size_t>(e) * d + k0 + kk])) : 0.f;
+    for (int i = tid; i < kRE * kRK; i += 256) {
+      const int ee = i / kRK, kk = i % kRK, e = e0 + ee;
+      ws[ee][kk] = e < E ? __half2float(__ushort_as_half(router_w[static_cast<size_t>(e) * d + k0 + kk])) : 0.f;
     }
     __syncthreads();
+    Fix40 f[2][2];
 #pragma unroll 4
     for (int kk = 0; kk < kRK; ++kk) {
-      float xv[4], wv[4];
+      const float x0 = xs[ty][kk], x1 = xs[ty + 16][kk];
+      const float w0 = ws[tx][kk], w1 = ws[tx + 16][kk];
+      const float pr[2][2] = {{x0 * w0, x0 * w1}, {x1 * w0, x1 * w1}};
 #pragma unroll
-      for (int a = 0; a < 4; ++a) xv[a] = xs[ty + 8 * a][kk];
+      for (int a = 0; a < 2; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) wv[b] = ws[tx + 32 * b][kk];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const float prod = xv[a] * wv[b];
-          if (!(fabsf(prod) < 2251799813685248.0f)) bad = true;   // |x w| must stay below 2^11
-          else acc[a][b] += __float2ll_rn(prod);
+        for (int b = 0; b < 2; ++b) {
+          const bool ok = fabsf(pr[a][b]) < 2251799813685248.0f;   // |x w| below 2^11
+          bad |= !ok;
+          fix40_add(f[a][b], ok ? pr[a][b] : 0.f);
         }
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b) acc[a][b] += fix40_value(f[a][b]);
+  }
+  if (__syncthreads_or(bad) && tid == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int t = t0 + ty + 16 * a, e = e0 + tx + 16 * b;
+      if (t < T && e < E) {
+        long long* dst = logits + static_cast<size_t>(t) * E + e;
+        if (gridDim.z == 1) *dst = acc[a][b];
+        else atomicAdd(reinterpret_cast<unsigned long long*>(dst), static_cast<unsigned long long>(acc[a][b]));
+      }
+    }
+}
+
+// One warp per token: bias (rounded onto the same grid), top-k (ties to the
+// lower index) and the softmax gates of the selected logits.
+__global__ void __launch_bounds__(256) k_pf_topk(const long long* logits, const float* bias, int T, int E, int k,
+                                                 int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates,
+                                                 uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;   // whole warps leave
+  unsigned long long key[4];
+  int idx[4];
+  bool bbad = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = 0ull;
+    idx[i] = 0x7fffffff;
+    if (e < E) {
+      long long v = logits[static_cast<size_t>(t) * E + e];
+      if (bias) {
+        const float bv = bias[static_cast<size_t>(t) * E + e];
+        if (!(fabsf(bv) < 1048576.f)) bbad = true;
+        else v += __float2ll_rn(bv * 1099511627776.0f);
+      }
+      key[i] = static_cast<unsigned long long>(v) ^ 0x8000000000000000ull;
+      idx[i] = e;
     }
   }
-  if (__syncthreads_or(bad) && tid == 0) atomicOr(err, ERR_ROUTER_DOMAIN);  // also: x / w reads are done
+  if (__any_sync(0xFFFFFFFFu, bbad) && lane == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
+  // each lane's four candidates sorted by (key desc, index asc)
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int i = 1; i < 4; ++i)
 #pragma unroll
-    for (int b = 0; b < 4; ++b) lg[ty + 8 * a][tx + 32 * b] = acc[a][b];
-  __syncthreads();
-  // one warp per token: bias, top-k, gates
-  const int lane = tid & 31;
-  for (int tt = ty; tt < kRT; tt += 8) {
-    const int t = t0 + tt;
-    if (t >= T) break;
-    unsigned long long key[4];
-    int idx[4];
-    bool bbad = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = lane + 32 * i;
-      key[i] = 0ull;
-      idx[i] = 0x7fffffff;
-      if (e < E) {
-        long long v = lg[tt][e];
-        if (bias) {
-          const float bv = bias[static_cast<size_t>(t) * E + e];
-          if (!(fabsf(bv) < 1048576.f)) bbad = true;
-          else v += __float2ll_rn(bv * 1099511627776.0f);
-        }
-        key[i] = static_cast<unsigned long long>(v) ^ 0x8000000000000000ull;
-        idx[i] = e;
+    for (int j = i; j > 0; --j)
+      if (key[j] > key[j - 1] || (key[j] == key[j - 1] && idx[j] < idx[j - 1])) {
+        const unsigned long long tk = key[j];
+        key[j] = key[j - 1];
+        key[j - 1] = tk;
+        const int ti = idx[j];
+        idx[j] = idx[j - 1];
+        idx[j - 1] = ti;
       }
-    }
-    if (__any_sync(0xFFFFFFFFu, bbad) && lane == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
-    // each lane's four candidates sorted by (key desc, index asc)
+  int head = 0, my_id = 0;
+  long long my_v = 0;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long hk = 0ull;
+    int he = 0x7fffffff;
 #pragma unroll
-    for (int i = 1; i < 4; ++i)
-#pragma unroll
-      for (int j = i; j > 0; --j)
-        if (key[j] > key[j - 1] || (key[j] == key[j - 1] && idx[j] < idx[j - 1])) {
-          const unsigned long long tk = key[j];
-          key[j] = key[j - 1];
-          key[j - 1] = tk;
-          const int ti = idx[j];
-          idx[j] = idx[j - 1];
-          idx[j - 1] = ti;
-        }
-    int head = 0, my_id = 0;
-    long long my_v = 0;
-    for (int j = 0; j < k; ++j) {
-      unsigned long long hk = 0ull;
-      int he = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (i == head) {
-          hk = key[i];
-          he = idx[i];
-        }
-      const bool has = head < 4 && he != 0x7fffffff;
-      const unsigned hi = has ? static_cast<unsigned>(hk >> 32) : 0u;
-      const unsigned lo = has ? static_cast<unsigned>(hk) : 0u;
-      const unsigned mh = __reduce_max_sync(0xFFFFFFFFu, hi);
-      const bool c1 = has && hi == mh;
-      const unsigned ml = __reduce_max_sync(0xFFFFFFFFu, c1 ? lo : 0u);
-      const bool c2 = c1 && lo == ml;
-      const unsigned me = __reduce_min_sync(0xFFFFFFFFu, c2 ? static_cast<unsigned>(he) : 0xFFFFFFFFu);
-      if (c2 && static_cast<unsigned>(he) == me) ++head;
-      if (lane == j) {
-        my_id = static_cast<int>(me);
-        my_v = static_cast<long long>((static_cast<unsigned long long>(mh) << 32 | ml) ^ 0x8000000000000000ull);
+    for (int i = 0; i < 4; ++i)
+      if (i == head) {
+        hk = key[i];
+        he = idx[i];
       }
+    const bool has = head < 4 && he != 0x7fffffff;
+    const unsigned hi = has ? static_cast<unsigned>(hk >> 32) : 0u;
+    const unsigned lo = has ? static_cast<unsigned>(hk) : 0u;
+    const unsigned mh = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const bool c1 = has && hi == mh;
+    const unsigned ml = __reduce_max_sync(0xFFFFFFFFu, c1 ? lo : 0u);
+    const bool c2 = c1 && lo == ml;
+    const unsigned me = __reduce_min_sync(0xFFFFFFFFu, c2 ? static_cast<unsigned>(he) : 0xFFFFFFFFu);
+    if (c2 && static_cast<unsigned>(he) == me) ++head;
+    if (lane == j) {
+      my_id = static_cast<int>(me);
+      my_v = static_cast<long long>((static_cast<unsigned long long>(mh) << 32 | ml) ^ 0x8000000000000000ull);
     }
-    const long long top = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-    float ex = 0.f;
-    if (lane < k) ex = expf(__ll2float_rn(my_v - top) * 9.094947017729282e-13f);
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
-    if (lane < k) {
-      const size_t o = static_cast<size_t>(t) * k + lane;
-      ids[o] = my_id;
-      gates[o] = ex / sum;
-      if (dbg_ids) dbg_ids[o] = my_id;
-      if (dbg_gates) dbg_gates[o] = ex / sum;
-    }
+  }
+  const long long top = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+  float ex = 0.f;
+  if (lane < k) ex = expf(__ll2float_rn(my_v - top) * 9.094947017729282e-13f);
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
+  if (lane < k) {
+    const size_t o = static_cast<size_t>(t) * k + lane;
+    ids[o] = my_id;
+    gates[o] = ex / sum;
+    if (dbg_ids) dbg_ids[o] = my_id;
+    if (dbg_gates) dbg_gates[o] = ex / sum;
   }
 }
 
@@ -566,6 +587,24 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
   }
 }
 
+// y = shared + sum_j g_j * y_j in top-k order, h' = bf16(h + y): one CTA per token.
+__global__ void __launch_bounds__(256) k_pf_combine(const float* ys, const float* ytok, const float* gates,
+                                                    const uint16_t* hin, uint16_t* hout, float* y_last, float* dbg_y,
+                                                    int d, int k) {
+  const int t = blockIdx.x;
+  __shared__ float g[32];
+  if (threadIdx.x < k) g[threadIdx.x] = gates[static_cast<size_t>(t) * k + threadIdx.x];
+  __syncthreads();
+  for (int R = threadIdx.x; R < d; R += 256) {
+    const size_t o = static_cast<size_t>(t) * d + R;
+    float y = ys[o];
+    for (int j = 0; j < k; ++j) y += g[j] * ytok[(static_cast<size_t>(t) * k + j) * d + R];
+    hout[o] = float_to_bf16_bits(bf16_bits_to_float(hin[o]) + y);
+    if (y_last) y_last[o] = y;
+    if (dbg_y) dbg_y[o] = y;
+  }
+}
+
 // Row r of the expert-ordered matrix = fp16 x of the pair's token.
 __global__ void __launch_bounds__(256) k_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k,
                                                    uint16_t* xp) {
@@ -599,10 +638,24 @@ cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float e
 }
 
 cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
-                             int k, int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err,
-                             cudaStream_t s) {
-  k_pf_router<<<(T + kRT - 1) / kRT, 256, 0, s>>>(x_bf, router_w, bias, T, d, E, k, ids, gates, dbg_ids, dbg_gates,
-                                                  err);
+                             int k, long long* logits, int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates,
+                             uint32_t* err, int n_sm, cudaStream_t s) {
+  const int tiles = ((T + kRT - 1) / kRT) * ((E + kRE - 1) / kRE);
+  // slice d (in 64-wide chunks, a divisor of d/64) until the grid covers the GPU twice
+  const int nc = d / kRK;
+  int slices = 1;
+  for (int c = 1; c <= nc; ++c)
+    if (nc % c == 0) {
+      slices = c;
+      if (tiles * c >= 2 * n_sm) break;
+    }
+  if (slices > 1) {
+    const cudaError_t e = cudaMemsetAsync(logits, 0, static_cast<size_t>(T) * E * sizeof(long long), s);
+    if (e != cudaSuccess) return e;
+  }
+  k_pf_logits<<<dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), 256, 0, s>>>(x_bf, router_w, T, d, E,
+                                                                                    d / slices, logits, err);
+  k_pf_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, bias, T, E, k, ids, gates, dbg_ids, dbg_gates, err);
   return cudaGetLastError();
 }
 
@@ -610,6 +663,12 @@ cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int32_t* cnt, int32
                            int32_t* n_items, cudaStream_t s) {
   k_pf_count<<<E, 256, 0, s>>>(ids, P, cnt);
   k_pf_scatter<<<E, 256, 0, s>>>(ids, P, E, cnt, row_pair, items, n_items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* gates, const uint16_t* hin,
+                              uint16_t* hout, float* y_last, float* dbg_y, int T, int d, int k, cudaStream_t s) {
+  k_pf_combine<<<T, 256, 0, s>>>(ys, ytok, gates, hin, hout, y_last, dbg_y, d, k);
   return cudaGetLastError();
 }
 
