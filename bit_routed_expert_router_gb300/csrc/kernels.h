@@ -95,8 +95,9 @@ cudaError_t launch_pf_gemm(const CUtensorMap& tmap_b, const PfGemm& p, int m_til
 cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
                            uint16_t* dbg_x, uint32_t* err, cudaStream_t s);
 cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
-                             int k, long long* logits, int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates,
-                             uint32_t* err, int n_sm, cudaStream_t s);
+                             int k, float* approx, float* xn2, float* wn2, float* xmax, float* wmax, int32_t* ids,
+                             float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err, int n_sm,
+                             cudaStream_t s);
 cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int32_t* cnt, int32_t* row_pair, int32_t* items,
                            int32_t* n_items, cudaStream_t s);
 cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* gates, const uint16_t* hin,

@@ -129,7 +129,7 @@ struct moe_ctx {
   uint16_t* pf_h[2] = {nullptr, nullptr};
   int32_t *pf_ids = nullptr, *pf_cnt = nullptr, *pf_rowpair = nullptr, *pf_items = nullptr, *pf_nitems = nullptr;
   float *pf_gates = nullptr, *pf_ytok = nullptr;
-  long long* pf_logits = nullptr;
+  float *pf_approx = nullptr, *pf_xn2 = nullptr, *pf_wn2 = nullptr, *pf_xmax = nullptr, *pf_wmax = nullptr;
   float* pf_ys = nullptr;
   unsigned long long* pf_timeline = nullptr;   // test hook 8: [4][16] GEMM event times of the first layer
   CUtensorMap pf_map_xp{}, pf_map_x16{}, pf_map_ar{}, pf_map_as{};
@@ -953,11 +953,15 @@ moe_status pf_alloc(moe_ctx* ctx) {
   ctx->pf_items = dalloc<int32_t>(3 * (P / kPfTileN + c.n_experts + 1), o, nb);
   ctx->pf_nitems = dalloc<int32_t>(1, o, nb);
   ctx->pf_ytok = dalloc<float>(P * c.d, o, nb);
-  ctx->pf_logits = dalloc<long long>(T * c.n_experts, o, nb);
+  ctx->pf_approx = dalloc<float>(T * c.n_experts, o, nb);
+  ctx->pf_xn2 = dalloc<float>(T, o, nb);
+  ctx->pf_wn2 = dalloc<float>(c.n_experts, o, nb);
+  ctx->pf_xmax = dalloc<float>(T, o, nb);
+  ctx->pf_wmax = dalloc<float>(c.n_experts, o, nb);
   ctx->pf_ys = dalloc<float>(T * c.d, o, nb);
   if (!ctx->pf_xbf || !ctx->pf_x16 || !ctx->pf_xp || !ctx->pf_ar || !ctx->pf_as || !ctx->pf_h[0] || !ctx->pf_h[1] ||
       !ctx->pf_ids || !ctx->pf_gates || !ctx->pf_cnt || !ctx->pf_rowpair || !ctx->pf_items || !ctx->pf_nitems ||
-      !ctx->pf_ytok || !ctx->pf_logits || !ctx->pf_ys)
+      !ctx->pf_ytok || !ctx->pf_approx || !ctx->pf_xn2 || !ctx->pf_wn2 || !ctx->pf_xmax || !ctx->pf_wmax || !ctx->pf_ys)
     return fail(ctx, MOE_ENOMEM, "prefill scratch (%zu bytes for %zu tokens) does not fit", nb, T);
   if (!encode_rows(&ctx->pf_map_xp, ctx->pf_xp, c.d, static_cast<long long>(P)) ||
       !encode_rows(&ctx->pf_map_x16, ctx->pf_x16, c.d, static_cast<long long>(T)) ||
@@ -980,8 +984,8 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   PROF(4, s);
   CK(launch_pf_prep(hin, T, d, c.prenorm, c.norm_eps, ctx->pf_xbf, ctx->pf_x16,
                     dbg && ctx->dbg_x ? ctx->dbg_x + xo * d : nullptr, ctx->err_word, s));
-  CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_logits,
-                      ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
+  CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_approx,
+                      ctx->pf_xn2, ctx->pf_wn2, ctx->pf_xmax, ctx->pf_wmax, ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
                       dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr, ctx->err_word, ctx->n_sm, s));
   CK(launch_pf_plan(ctx->pf_ids, P, E, ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items, ctx->pf_nitems, s));
   CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));

@@ -383,99 +383,223 @@ __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int p
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, ERR_PF_RANGE);
 }
 
-// Router logits: a CTA takes 32 tokens x 32 experts over one slice of d.  Each
-// product W_r[e][i] * x[i] is exact in fp32 (11-bit x 8-bit significands);
-// scaled by 2^40 it is rounded to the nearest integer (ties to even) and summed
-// exactly (Fix40 per 64-wide chunk, int64 across chunks), so a logit does not
-// depend on the order of its terms or on how d is sliced.  With several slices
-// (small T, to fill the GPU) the slices meet in int64 atomic adds.
+// Router, in two passes.
+//
+// Pass 1 (k_pf_logits_approx): every (token, expert) logit in fp32 with a
+// rigorous error bound.  A CTA takes 32 tokens x 32 experts over one slice of
+// d; each thread sums 2 x 2 logits with fused multiply-adds in 64-term chunks
+// (the products are exact in fp32: 11-bit x 8-bit significands), so the sum
+// differs from the exact one by at most about (64 + 2 * 44) u * sum|x_i w_i|
+// with u = 2^-24 (chunk sums, slice sums and the adds across slices), and
+// sum|x_i w_i| <= |x| |w| (Cauchy-Schwarz).  The CTAs of the first expert /
+// token block also store |x_t|^2, |w_e|^2 and the rows' largest |x_i|, |w_i|.
+//
+// Pass 2 (k_pf_route): one CTA per token.  With L~_e the approximate logit
+// plus bias and eps_e its bound, tau = the k-th largest L~_e - eps_e is below
+// the exact k-th largest logit, so an expert with L~_e + eps_e < tau cannot be
+// selected.  An expert whose largest |x_i| |w_i| could leave the exact domain
+// (|x_i w_i| < 2^11), or whose bound is not finite, is always a candidate, so
+// the exact pass still flags such inputs.  The candidates (usually k or k + 1) get their exact
+// fixed-point logits (products rounded onto the 2^-40 grid, summed exactly with
+// Fix40), and the top-k (ties to the lower index) and the softmax gates are
+// taken from those, so the result is the exact router's.
 constexpr int kRT = 32;       // tokens per CTA
 constexpr int kRE = 32;       // experts per CTA
 constexpr int kRK = 64;       // k chunk
-__global__ void __launch_bounds__(256) k_pf_logits(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
-                                                   int E, int k_slice, long long* logits, uint32_t* err) {
-  __shared__ float xs[kRT][kRK + 1];   // x * 2^40 (exact)
-  __shared__ float ws[kRE][kRK + 1];   // W_r as fp32
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
+                                                          int E, int k_slice, float* approx, float* xn2, float* wn2,
+                                                          float* xmax, float* wmax) {
+  __shared__ float xs[kRT][kRK + 1];
+  __shared__ float ws[kRE][kRK + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE, kb = blockIdx.z * k_slice;
+  // squared norms (for the error bound), full d, by the CTAs of the first slice
+  if (blockIdx.z == 0 && (blockIdx.y == 0 || blockIdx.x == 0)) {
+    for (int r = warp; r < kRT + kRE; r += 8) {
+      const bool is_x = r < kRT;
+      if (is_x && blockIdx.y != 0) continue;
+      if (!is_x && blockIdx.x != 0) continue;
+      const int row = is_x ? t0 + r : e0 + r - kRT;
+      if (row >= (is_x ? T : E)) continue;
+      float ss = 0.f, mx = 0.f;
+      for (int i = lane; i < d; i += 32) {
+        const float v = is_x ? bf16_bits_to_float(x_bf[static_cast<size_t>(row) * d + i])
+                             : __half2float(__ushort_as_half(router_w[static_cast<size_t>(row) * d + i]));
+        ss = fmaf(v, v, ss);
+        mx = fmaxf(mx, fabsf(v));   // NaN is dropped here but makes ss NaN
+      }
+#pragma unroll
+      for (int m = 16; m; m >>= 1) {
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, m);
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, m));
+      }
+      if (lane == 0) {
+        (is_x ? xn2 : wn2)[row] = ss;
+        (is_x ? xmax : wmax)[row] = mx;
+      }
+    }
+  }
   const int tx = tid & 15;             // experts e0 + tx, e0 + tx + 16
   const int ty = tid >> 4;             // tokens t0 + ty, t0 + ty + 16
-  long long acc[2][2] = {{0, 0}, {0, 0}};
-  bool bad = false;
+  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
   for (int k0 = kb; k0 < kb + k_slice; k0 += kRK) {
     __syncthreads();
     for (int i = tid; i < kRT * kRK; i += 256) {
       const int tt = i / kRK, kk = i % kRK, t = t0 + tt;
-      xs[tt][kk] = t < T ? bf16_bits_to_float(x_bf[static_cast<size_t>(t) * d + k0 + kk]) * 1099511627776.0f : 0.f;
+      xs[tt][kk] = t < T ? bf16_bits_to_float(x_bf[static_cast<size_t>(t) * d + k0 + kk]) : 0.f;
     }
     for (int i = tid; i < kRE * kRK; i += 256) {
       const int ee = i / kRK, kk = i % kRK, e = e0 + ee;
       ws[ee][kk] = e < E ? __half2float(__ushort_as_half(router_w[static_cast<size_t>(e) * d + k0 + kk])) : 0.f;
     }
     __syncthreads();
-    Fix40 f[2][2];
-#pragma unroll 4
+    float c[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll 8
     for (int kk = 0; kk < kRK; ++kk) {
       const float x0 = xs[ty][kk], x1 = xs[ty + 16][kk];
       const float w0 = ws[tx][kk], w1 = ws[tx + 16][kk];
-      const float pr[2][2] = {{x0 * w0, x0 * w1}, {x1 * w0, x1 * w1}};
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const bool ok = fabsf(pr[a][b]) < 2251799813685248.0f;   // |x w| below 2^11
-          bad |= !ok;
-          fix40_add(f[a][b], ok ? pr[a][b] : 0.f);
-        }
+      c[0][0] = fmaf(x0, w0, c[0][0]);
+      c[0][1] = fmaf(x0, w1, c[0][1]);
+      c[1][0] = fmaf(x1, w0, c[1][0]);
+      c[1][1] = fmaf(x1, w1, c[1][1]);
     }
 #pragma unroll
     for (int a = 0; a < 2; ++a)
 #pragma unroll
-      for (int b = 0; b < 2; ++b) acc[a][b] += fix40_value(f[a][b]);
+      for (int b = 0; b < 2; ++b) acc[a][b] += c[a][b];
   }
-  if (__syncthreads_or(bad) && tid == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
       const int t = t0 + ty + 16 * a, e = e0 + tx + 16 * b;
       if (t < T && e < E) {
-        long long* dst = logits + static_cast<size_t>(t) * E + e;
+        float* dst = approx + static_cast<size_t>(t) * E + e;
         if (gridDim.z == 1) *dst = acc[a][b];
-        else atomicAdd(reinterpret_cast<unsigned long long*>(dst), static_cast<unsigned long long>(acc[a][b]));
+        else atomicAdd(dst, acc[a][b]);
       }
     }
 }
 
-// One warp per token: bias (rounded onto the same grid), top-k (ties to the
-// lower index) and the softmax gates of the selected logits.
-__global__ void __launch_bounds__(256) k_pf_topk(const long long* logits, const float* bias, int T, int E, int k,
-                                                 int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates,
-                                                 uint32_t* err) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;   // whole warps leave
-  unsigned long long key[4];
-  int idx[4];
-  bool bbad = false;
+// Pass 2: candidates, their exact logits, top-k and gates.  One CTA per token.
+__global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const uint16_t* router_w, const float* approx,
+                                                  const float* xn2, const float* wn2, const float* xmax,
+                                                  const float* wmax, const float* bias, int T, int d,
+                                                  int E, int k, int32_t* ids, float* gates, int32_t* dbg_ids,
+                                                  float* dbg_gates, uint32_t* err) {
+  __shared__ int cand[128];
+  __shared__ long long exact[128];
+  __shared__ int n_cand;
+  __shared__ int s_bad;
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    n_cand = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // candidates: L~_e + eps_e >= tau, tau = k-th largest of L~_e - eps_e
+    const float u = 5.9604645e-8f;                                  // 2^-24
+    const float xn = sqrtf(xn2[t]) * 1.01f;
+    const float xm = xmax[t];
+    float lo[4], hi[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = 0ull;
-    idx[i] = 0x7fffffff;
-    if (e < E) {
-      long long v = logits[static_cast<size_t>(t) * E + e];
-      if (bias) {
-        const float bv = bias[static_cast<size_t>(t) * E + e];
-        if (!(fabsf(bv) < 1048576.f)) bbad = true;
-        else v += __float2ll_rn(bv * 1099511627776.0f);
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane + 32 * i;
+      lo[i] = -INFINITY;
+      hi[i] = -INFINITY;
+      if (e < E) {
+        const float s = approx[static_cast<size_t>(t) * E + e];
+        const float b = bias ? bias[static_cast<size_t>(t) * E + e] : 0.f;
+        const float L = s + b;
+        const float eps = 160.f * u * xn * (sqrtf(wn2[e]) * 1.01f) + static_cast<float>(d + 1) * 4.5474735e-13f +
+                          2.f * u * (fabsf(s) + fabsf(b)) + 1e-30f;
+        lo[i] = L - eps * 1.01f;
+        hi[i] = L + eps * 1.01f;
+        if (!(xm * wmax[e] < 2048.f) || !(fabsf(lo[i]) < 3.0e38f) || !(fabsf(hi[i]) < 3.0e38f)) {
+          lo[i] = -INFINITY;   // always a candidate: the exact pass decides (and flags the domain)
+          hi[i] = INFINITY;
+        }
+        if (!(fabsf(b) < 1048576.f)) s_bad = 1;
       }
-      key[i] = static_cast<unsigned long long>(v) ^ 0x8000000000000000ull;
-      idx[i] = e;
+    }
+    // tau: the k-th largest lower bound (repeated warp max, removing one entry each round)
+    float tau = -INFINITY;
+    {
+      float v[4] = {lo[0], lo[1], lo[2], lo[3]};
+      for (int j = 0; j < k; ++j) {
+        float m = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        tau = m;
+        // remove one occurrence of m: the lowest lane / slot that holds it
+        int mine = -1;
+#pragma unroll
+        for (int i = 3; i >= 0; --i)
+          if (v[i] == m) mine = i;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, mine >= 0);
+        if (mine >= 0 && lane == __ffs(bal) - 1) v[mine] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane + 32 * i;
+      const bool c = e < E && hi[i] >= tau;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, c);
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&n_cand, __popc(bal));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      if (c) cand[base + __popc(bal & ((1u << lane) - 1u))] = e;
     }
   }
-  if (__any_sync(0xFFFFFFFFu, bbad) && lane == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
-  // each lane's four candidates sorted by (key desc, index asc)
+  __syncthreads();
+  // exact logits of the candidates, one warp per candidate
+  const uint16_t* xr = x_bf + static_cast<size_t>(t) * d;
+  bool bad = false;
+  for (int ci = warp; ci < n_cand; ci += 8) {
+    const int e = cand[ci];
+    const uint16_t* wr = router_w + static_cast<size_t>(e) * d;
+    Fix40 fx;
+    for (int i0 = 0; i0 < d; i0 += 64) {   // 2 products per lane per 64 columns: at most 2 d / 64 <= 96 terms
+      const uint32_t xv = *reinterpret_cast<const uint32_t*>(xr + i0 + 2 * lane);
+      const uint32_t wv = *reinterpret_cast<const uint32_t*>(wr + i0 + 2 * lane);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xv >> 16) : (xv & 0xFFFFu)));
+        const float pw = hh ? half_hi(wv) : half_lo(wv);
+        const float prod = pw * px;
+        const bool ok = fabsf(prod) < 2048.f;
+        bad |= !ok;
+        fix40_add(fx, ok ? prod * 1099511627776.0f : 0.f);
+      }
+    }
+    long long v = fix40_value(fx);
+#pragma unroll
+    for (int m = 16; m; m >>= 1) v += shfl_xor_i64(v, m);
+    if (lane == 0) {
+      if (bias) {
+        const float bv = bias[static_cast<size_t>(t) * E + e];
+        if (fabsf(bv) < 1048576.f) v += __float2ll_rn(bv * 1099511627776.0f);
+      }
+      exact[ci] = v;
+    }
+  }
+  if (__syncthreads_or(bad || s_bad) && tid == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
+  if (warp != 0) return;
+  // top-k over the candidates: a lane holds candidates lane, lane + 32, ...
+  unsigned long long key[4];
+  int idx[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int ci = lane + 32 * i;
+    key[i] = 0ull;
+    idx[i] = 0x7fffffff;
+    if (ci < n_cand) {
+      key[i] = static_cast<unsigned long long>(exact[ci]) ^ 0x8000000000000000ull;
+      idx[i] = cand[ci];
+    }
+  }
 #pragma unroll
   for (int i = 1; i < 4; ++i)
 #pragma unroll
@@ -638,8 +762,9 @@ cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float e
 }
 
 cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
-                             int k, long long* logits, int32_t* ids, float* gates, int32_t* dbg_ids, float* dbg_gates,
-                             uint32_t* err, int n_sm, cudaStream_t s) {
+                             int k, float* approx, float* xn2, float* wn2, float* xmax, float* wmax, int32_t* ids,
+                             float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err, int n_sm,
+                             cudaStream_t s) {
   const int tiles = ((T + kRT - 1) / kRT) * ((E + kRE - 1) / kRE);
   // slice d (in 64-wide chunks, a divisor of d/64) until the grid covers the GPU twice
   const int nc = d / kRK;
@@ -650,12 +775,13 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
       if (tiles * c >= 2 * n_sm) break;
     }
   if (slices > 1) {
-    const cudaError_t e = cudaMemsetAsync(logits, 0, static_cast<size_t>(T) * E * sizeof(long long), s);
+    const cudaError_t e = cudaMemsetAsync(approx, 0, static_cast<size_t>(T) * E * sizeof(float), s);
     if (e != cudaSuccess) return e;
   }
-  k_pf_logits<<<dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), 256, 0, s>>>(x_bf, router_w, T, d, E,
-                                                                                    d / slices, logits, err);
-  k_pf_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, bias, T, E, k, ids, gates, dbg_ids, dbg_gates, err);
+  k_pf_logits_approx<<<dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), 256, 0, s>>>(
+      x_bf, router_w, T, d, E, d / slices, approx, xn2, wn2, xmax, wmax);
+  k_pf_route<<<T, 256, 0, s>>>(x_bf, router_w, approx, xn2, wn2, xmax, wmax, bias, T, d, E, k, ids, gates, dbg_ids,
+                               dbg_gates, err);
   return cudaGetLastError();
 }
 

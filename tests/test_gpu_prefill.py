@@ -182,3 +182,35 @@ def test_prefill_full_shape_sampled_tokens():
             assert st == 0
             assert list(ids_np[t]) == list(oracle.topk(lg, sh.top_k)), f"token {t}"
         _check_tokens(lay, H, xs[0], ids[0], gs[0], ys[0], h_out, (0, 1, 2047, 4095), bias=bias[0], prenorm=1)
+
+
+def test_prefill_router_exact_ties_and_zero_rows():
+    """Duplicated router rows tie exactly (ties go to the lower index) and an
+    all-zero router with a bias that ties on some tokens: the candidate filter
+    must keep every tied expert."""
+    w = gen_layer(TINY, seed=31, layer=0)
+    rw = w["router_w"].clone()
+    rw[5] = rw[2]
+    rw[7] = rw[0]
+    w["router_w"] = rw
+    ctx = Ctx(TINY, n_layers=1, max_tokens=512)
+    with ctx:
+        ctx.init_layer(0, to_device(w))
+        lay = oracle.Layer(w, TINY.top_k)
+        H = gen_hidden(200, TINY.d, seed=31).cuda()
+        h_out, y, xs, ids, gs, ys = _run_prefill(ctx, H)
+        _check_tokens(lay, H, xs[0], ids[0], gs[0], ys[0], h_out, range(200))
+    w2 = gen_layer(TINY, seed=41, layer=0)
+    w2["router_w"] = torch.zeros_like(w2["router_w"])
+    ctx = Ctx(TINY, n_layers=1, max_tokens=512)
+    with ctx:
+        ctx.init_layer(0, to_device(w2))
+        lay = oracle.Layer(w2, TINY.top_k)
+        T = 40
+        H = gen_hidden(T, TINY.d, seed=41).cuda()
+        bias = torch.zeros(1, T, TINY.n_experts, dtype=torch.float32)
+        bias[0, :, 3] = 16.0
+        bias[0, :20, 6] = 16.0
+        bias = bias.cuda()
+        h_out, y, xs, ids, gs, ys = _run_prefill(ctx, H, bias=bias)
+        _check_tokens(lay, H, xs[0], ids[0], gs[0], ys[0], h_out, range(T), bias=bias[0])
