@@ -403,17 +403,17 @@ __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int p
 // fixed-point logits (products rounded onto the 2^-40 grid, summed exactly with
 // Fix40), and the top-k (ties to the lower index) and the softmax gates are
 // taken from those, so the result is the exact router's.
-constexpr int kRT = 32;       // tokens per CTA
-constexpr int kRE = 32;       // experts per CTA
-constexpr int kRK = 64;       // k chunk
+constexpr int kRT = 64;       // tokens per CTA
+constexpr int kRE = 64;       // experts per CTA
+constexpr int kRK = 64;       // k chunk (one partial sum per chunk)
 __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
                                                           int E, int k_slice, float* approx, float* xn2, float* wn2,
                                                           float* xmax, float* wmax) {
-  __shared__ float xs[kRT][kRK + 1];
-  __shared__ float ws[kRE][kRK + 1];
+  __shared__ __align__(16) float xs[kRK][kRT];   // K-major, so a thread reads four tokens as one float4
+  __shared__ __align__(16) float ws[kRK][kRE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE, kb = blockIdx.z * k_slice;
-  // squared norms (for the error bound), full d, by the CTAs of the first slice
+  // squared norms and largest magnitudes (for the error bound), full d, by the CTAs of the first slice
   if (blockIdx.z == 0 && (blockIdx.y == 0 || blockIdx.x == 0)) {
     for (int r = warp; r < kRT + kRE; r += 8) {
       const bool is_x = r < kRT;
@@ -439,40 +439,57 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
       }
     }
   }
-  const int tx = tid & 15;             // experts e0 + tx, e0 + tx + 16
-  const int ty = tid >> 4;             // tokens t0 + ty, t0 + ty + 16
-  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  const int tx = tid & 15;             // experts e0 + 4 tx .. + 3
+  const int ty = tid >> 4;             // tokens t0 + 4 ty .. + 3
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
   for (int k0 = kb; k0 < kb + k_slice; k0 += kRK) {
     __syncthreads();
-    for (int i = tid; i < kRT * kRK; i += 256) {
-      const int tt = i / kRK, kk = i % kRK, t = t0 + tt;
-      xs[tt][kk] = t < T ? bf16_bits_to_float(x_bf[static_cast<size_t>(t) * d + k0 + kk]) : 0.f;
-    }
-    for (int i = tid; i < kRE * kRK; i += 256) {
-      const int ee = i / kRK, kk = i % kRK, e = e0 + ee;
-      ws[ee][kk] = e < E ? __half2float(__ushort_as_half(router_w[static_cast<size_t>(e) * d + k0 + kk])) : 0.f;
+    // 64 rows x 64 columns of x and of W_r: each thread converts two runs of eight
+    for (int i = tid; i < kRT * kRK / 8; i += 256) {
+      const int r = i / (kRK / 8), c8 = (i % (kRK / 8)) * 8;
+      const int t = t0 + r, e = e0 + r;
+      uint4 xv = make_uint4(0u, 0u, 0u, 0u), wv = make_uint4(0u, 0u, 0u, 0u);
+      if (t < T) xv = *reinterpret_cast<const uint4*>(x_bf + static_cast<size_t>(t) * d + k0 + c8);
+      if (e < E) wv = *reinterpret_cast<const uint4*>(router_w + static_cast<size_t>(e) * d + k0 + c8);
+      const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        xs[c8 + 2 * u][r] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] & 0xFFFFu));
+        xs[c8 + 2 * u + 1][r] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] >> 16));
+        ws[c8 + 2 * u][r] = half_lo(wa[u]);
+        ws[c8 + 2 * u + 1][r] = half_hi(wa[u]);
+      }
     }
     __syncthreads();
-    float c[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll 8
+    float c[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) c[a][b] = 0.f;
+#pragma unroll 4
     for (int kk = 0; kk < kRK; ++kk) {
-      const float x0 = xs[ty][kk], x1 = xs[ty + 16][kk];
-      const float w0 = ws[tx][kk], w1 = ws[tx + 16][kk];
-      c[0][0] = fmaf(x0, w0, c[0][0]);
-      c[0][1] = fmaf(x0, w1, c[0][1]);
-      c[1][0] = fmaf(x1, w0, c[1][0]);
-      c[1][1] = fmaf(x1, w1, c[1][1]);
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) c[a][b] = fmaf(xa[a], wa[b], c[a][b]);
     }
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
+    for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 2; ++b) acc[a][b] += c[a][b];
+      for (int b = 0; b < 4; ++b) acc[a][b] += c[a][b];
   }
 #pragma unroll
-  for (int a = 0; a < 2; ++a)
+  for (int a = 0; a < 4; ++a)
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const int t = t0 + ty + 16 * a, e = e0 + tx + 16 * b;
+    for (int b = 0; b < 4; ++b) {
+      const int t = t0 + 4 * ty + a, e = e0 + 4 * tx + b;
       if (t < T && e < E) {
         float* dst = approx + static_cast<size_t>(t) * E + e;
         if (gridDim.z == 1) *dst = acc[a][b];
@@ -481,24 +498,28 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
     }
 }
 
-// Pass 2: candidates, their exact logits, top-k and gates.  One CTA per token.
+// Pass 2: candidates, their exact logits, top-k and gates.  A CTA takes eight
+// tokens (one warp each for the candidates and the top-k); all warps share the
+// exact dot products.
 __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const uint16_t* router_w, const float* approx,
                                                   const float* xn2, const float* wn2, const float* xmax,
                                                   const float* wmax, const float* bias, int T, int d,
                                                   int E, int k, int32_t* ids, float* gates, int32_t* dbg_ids,
                                                   float* dbg_gates, uint32_t* err) {
-  __shared__ int cand[128];
-  __shared__ long long exact[128];
-  __shared__ int n_cand;
+  __shared__ int cand_all[8][128];
+  __shared__ long long exact_all[8][128];
+  __shared__ int n_cand_all[8];
   __shared__ int s_bad;
-  const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    n_cand = 0;
-    s_bad = 0;
-  }
+  const int t = blockIdx.x * 8 + warp;
+  const bool live = t < T;                       // warp-uniform
+  int* cand = cand_all[warp];
+  long long* exact = exact_all[warp];
+  int& n_cand = n_cand_all[warp];
+  if (lane == 0) n_cand = 0;
+  if (tid == 0) s_bad = 0;
   __syncthreads();
-  if (warp == 0) {
+  if (live) {
     // candidates: L~_e + eps_e >= tau, tau = k-th largest of L~_e - eps_e
     const float u = 5.9604645e-8f;                                  // 2^-24
     const float xn = sqrtf(xn2[t]) * 1.01f;
@@ -554,24 +575,41 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
     }
   }
   __syncthreads();
-  // exact logits of the candidates, one warp per candidate
-  const uint16_t* xr = x_bf + static_cast<size_t>(t) * d;
+  // exact logits of every (token, candidate) of the CTA, one warp per pair
+  int total = 0, first[9];
+  for (int w = 0; w < 8; ++w) {
+    first[w] = total;
+    total += n_cand_all[w];
+  }
+  first[8] = total;
   bool bad = false;
-  for (int ci = warp; ci < n_cand; ci += 8) {
-    const int e = cand[ci];
+  for (int pi = warp; pi < total; pi += 8) {
+    int tw = 0;
+    while (pi >= first[tw + 1]) ++tw;
+    const int ci = pi - first[tw];
+    const int tt = blockIdx.x * 8 + tw;
+    const int e = cand_all[tw][ci];
+    const uint16_t* xr = x_bf + static_cast<size_t>(tt) * d;
     const uint16_t* wr = router_w + static_cast<size_t>(e) * d;
     Fix40 fx;
-    for (int i0 = 0; i0 < d; i0 += 64) {   // 2 products per lane per 64 columns: at most 2 d / 64 <= 96 terms
-      const uint32_t xv = *reinterpret_cast<const uint32_t*>(xr + i0 + 2 * lane);
-      const uint32_t wv = *reinterpret_cast<const uint32_t*>(wr + i0 + 2 * lane);
+    // eight products per lane per 256 columns (at most d / 32 <= 96 terms), two loads in flight
+#pragma unroll 2
+    for (int i0 = 0; i0 < d; i0 += 256) {
+      if (i0 + 8 * lane < d) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xr + i0 + 8 * lane);
+        const uint4 wv = *reinterpret_cast<const uint4*>(wr + i0 + 8 * lane);
+        const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xv >> 16) : (xv & 0xFFFFu)));
-        const float pw = hh ? half_hi(wv) : half_lo(wv);
-        const float prod = pw * px;
-        const bool ok = fabsf(prod) < 2048.f;
-        bad |= !ok;
-        fix40_add(fx, ok ? prod * 1099511627776.0f : 0.f);
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xa[u] >> 16) : (xa[u] & 0xFFFFu)));
+            const float pw = hh ? half_hi(wa[u]) : half_lo(wa[u]);
+            const float prod = pw * px;
+            const bool ok = fabsf(prod) < 2048.f;
+            bad |= !ok;
+            fix40_add(fx, ok ? prod * 1099511627776.0f : 0.f);
+          }
       }
     }
     long long v = fix40_value(fx);
@@ -579,14 +617,14 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
     for (int m = 16; m; m >>= 1) v += shfl_xor_i64(v, m);
     if (lane == 0) {
       if (bias) {
-        const float bv = bias[static_cast<size_t>(t) * E + e];
+        const float bv = bias[static_cast<size_t>(tt) * E + e];
         if (fabsf(bv) < 1048576.f) v += __float2ll_rn(bv * 1099511627776.0f);
       }
-      exact[ci] = v;
+      exact_all[tw][ci] = v;
     }
   }
   if (__syncthreads_or(bad || s_bad) && tid == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
-  if (warp != 0) return;
+  if (!live) return;
   // top-k over the candidates: a lane holds candidates lane, lane + 32, ...
   unsigned long long key[4];
   int idx[4];
@@ -719,10 +757,19 @@ __global__ void __launch_bounds__(256) k_pf_combine(const float* ys, const float
   __shared__ float g[32];
   if (threadIdx.x < k) g[threadIdx.x] = gates[static_cast<size_t>(t) * k + threadIdx.x];
   __syncthreads();
+  const float* yt = ytok + static_cast<size_t>(t) * k * d;
   for (int R = threadIdx.x; R < d; R += 256) {
     const size_t o = static_cast<size_t>(t) * d + R;
     float y = ys[o];
-    for (int j = 0; j < k; ++j) y += g[j] * ytok[(static_cast<size_t>(t) * k + j) * d + R];
+    int j = 0;
+    for (; j + 8 <= k; j += 8) {   // eight independent loads in flight, summed in top-k order
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcs(yt + static_cast<size_t>(j + u) * d + R);   // read once: stream
+#pragma unroll
+      for (int u = 0; u < 8; ++u) y += g[j + u] * v[u];
+    }
+    for (; j < k; ++j) y += g[j] * __ldcs(yt + static_cast<size_t>(j) * d + R);
     hout[o] = float_to_bf16_bits(bf16_bits_to_float(hin[o]) + y);
     if (y_last) y_last[o] = y;
     if (dbg_y) dbg_y[o] = y;
@@ -780,7 +827,7 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
   }
   k_pf_logits_approx<<<dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), 256, 0, s>>>(
       x_bf, router_w, T, d, E, d / slices, approx, xn2, wn2, xmax, wmax);
-  k_pf_route<<<T, 256, 0, s>>>(x_bf, router_w, approx, xn2, wn2, xmax, wmax, bias, T, d, E, k, ids, gates, dbg_ids,
+  k_pf_route<<<(T + 7) / 8, 256, 0, s>>>(x_bf, router_w, approx, xn2, wn2, xmax, wmax, bias, T, d, E, k, ids, gates, dbg_ids,
                                dbg_gates, err);
   return cudaGetLastError();
 }
