@@ -51,7 +51,7 @@ class MoeKernelTime(C.Structure):
 
 N_KERNEL_KINDS = 8
 KERNEL_KINDS = {0: "router_topk_plan", 1: "gateup_gelu_gemv", 2: "down_combine_gemv", 3: "decode_persistent",
-                4: "prefill_route_group", 5: "prefill_tcgen05_gemm"}
+                4: "prefill_route_group", 5: "prefill_tcgen05_gemm", 6: "prefill_combine"}
 
 
 class MoeError(RuntimeError):

@@ -1046,6 +1046,8 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   q.out32 = ctx->pf_ys;
   if (ctx->pf_timeline && rel == 0) q.tl = ctx->pf_timeline + 48;
   CK(launch_pf_gemm(ctx->pf_map_as, q, d / 128, t_items, s));
+  PROF(-1, s);
+  PROF(6, s);
   CK(launch_pf_combine(ctx->pf_ys, ctx->pf_ytok, ctx->pf_gates, hin, hout, rel == n_rel - 1 ? y_last : nullptr,
                        dbg && ctx->dbg_y ? ctx->dbg_y + xo * d : nullptr, T, d, k, s));
   PROF(-1, s);

@@ -163,11 +163,21 @@ moe_status moe_decode_step(moe_ctx *ctx, const void *h_in, int B, int layer_begi
                            const float *logit_bias, void *h_out, float *y_last, moe_trace_rec *trace,
                            int trace_cap, int *trace_len, void *stream);
 
-/* Prefill: T tokens at once through layers [layer_begin, layer_end), same
- * per-layer arithmetic as moe_decode_step.  Resident contexts only,
- * 1 <= T <= max_tokens.  Tokens are permuted by expert, each expert's tokens
- * run through a grouped int4 -> bf16 tensor-core GEMM, and the outputs are
- * combined per token in top-k order. */
+/* Prefill: T tokens at once through layers [layer_begin, layer_end)
+ * ("Optimizing a 14.3 GB model for an 8 GB machine", section "Splitting the
+ * work improved attention and prefill": dequantise a small 16-bit tile, run
+ * the matrix primitive, discard the tile).  Resident contexts only,
+ * 1 <= T <= max_tokens; h, h_out bf16 [T][d] and y_last fp32 [T][d] (nullable)
+ * on the device; logit_bias (nullable) fp32 [layer_end - layer_begin][T][E].
+ * When d % 128 == 0 and n_experts <= 128 (else the batched decode kernels run,
+ * 32 tokens at a time): the routing is exact (the same ids and gates as
+ * moe_decode_step), the (token, k) pairs are grouped by expert, and each
+ * expert's rows run through int4 -> fp16 tiles on tcgen05 tensor cores with
+ * fp32 accumulation (weights rounded once to fp16, activations in fp16), then
+ * are combined per token as shared + routed outputs in top-k order; an fp16
+ * operand outside [-65504, 65504] is reported by moe_sync as MOE_EDOMAIN.  The
+ * first call allocates scratch for max_tokens tokens (about 180 KB per token at
+ * the full shape).  Returns without synchronising. */
 moe_status moe_prefill(moe_ctx *ctx, const void *h, int T, int layer_begin, int layer_end,
                        const float *logit_bias, void *h_out, float *y_last, void *stream);
 
@@ -233,7 +243,9 @@ moe_status moe_route_noalloc(const moe_config *cfg, const uint16_t *router_w, co
  * launch on the call's stream, and synchronise that stream before returning
  * to add the durations to the running totals.  kind: 0 router/top-k/plan,
  * 1 gate/up GEMV, 2 down GEMV + combine, 3 persistent one-token decode
- * (all layers), 4.. prefill kernels. */
+ * (all layers), 4 prefill routing and grouping (norm, router, expert
+ * grouping, gather; one pair of events per layer), 5 prefill GEMMs (the four
+ * tcgen05 GEMMs of one layer), 6 prefill combine. */
 typedef struct {
     int64_t launches;
     double total_ms;
@@ -258,7 +270,14 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
  * the address of a caller device buffer of 2 * n_layers * 16 uint64 into
  * which the persistent kernel records event times (%globaltimer ns): rows
  * [0, n_layers) min or max over CTAs, rows [n_layers, 2 n_layers) steps of
- * the first routed CTA (see persistent.cu), or 0 to stop.  Other hooks: MOE_EINVAL. */
+ * the first routed CTA (see persistent.cu); with 2 * n_layers + gridDim.x rows
+ * it also gets per-CTA event times of the step's third layer; 0 stops it.
+ * hook 4 or 7 with a non-zero value on a configuration where that kernel path
+ * cannot run returns MOE_ESTATE.  hook 7: the tcgen05 prefill on (value != 0,
+ * the default when the shape allows it) or off (batched decode kernels).
+ * hook 8: `value` is a caller device buffer of 4 * 16 uint64 receiving event
+ * times of CTA (0, 0) of each prefill GEMM of the first layer of a call, or
+ * 0 to stop.  Other hooks: MOE_EINVAL. */
 moe_status moe_test_hook(moe_ctx *ctx, int hook, int64_t value);
 
 const char *moe_status_string(moe_status s);
