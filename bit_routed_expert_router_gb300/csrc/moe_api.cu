@@ -682,7 +682,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
                              (c.top_k * ((nT + 3) / 4) + n_cta - 1) / n_cta;
   if (n_cta >= 2 && c.d <= 44 * 64 && c.f_shared <= 44 * 64 && c.f <= 11 * 64 &&
       tiles_per_cta <= persistent_max_tiles_per_cta() && stages_per_cta <= persistent_max_tasks() &&
-      persistent_smem() + 8192 <= static_cast<size_t>(max_smem)) {
+      persistent_smem() + 2048 <= static_cast<size_t>(max_smem)) {   // + the kernel's static shared memory
     int per_sm = 0;
     if (persistent_attrs() == cudaSuccess && persistent_occupancy(&per_sm) == cudaSuccess && per_sm >= 1)
       ctx->p_ok = true;
