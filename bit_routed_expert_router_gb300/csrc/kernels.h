@@ -63,7 +63,9 @@ cudaError_t persistent_occupancy(int* blocks_per_sm);
 cudaError_t launch_persistent(PParams& p, int grid, cudaStream_t s);
 
 // Prefill (tcgen05 grouped GEMM over int4 weights).
-constexpr int kPfTileN = 128;          // token rows per GEMM tile
+constexpr int kPfTileN = 128;          // token rows per GEMM tile (large groups)
+constexpr int kPfTileNSmall = 32;      // token rows per GEMM tile when every expert has only a few rows
+constexpr int kPfMinDecodeB = 20;     // resident decode steps of at least this many tokens take the tcgen05 path
 enum : int { PF_GU = 0, PF_DN_ROUTED = 1, PF_DN_SHARED = 2 };
 
 struct PfGemm {
@@ -89,17 +91,19 @@ struct PfGemm {
   unsigned long long* tl;              // optional: 16 event times (ns) of CTA (0, 0), null = off
 };
 
-size_t pf_gemm_smem();
+size_t pf_gemm_smem(int n);
 cudaError_t pf_set_attrs();
-cudaError_t launch_pf_gemm(const CUtensorMap& tmap_b, const PfGemm& p, int m_tiles, int max_items, cudaStream_t s);
+cudaError_t launch_pf_gemm(int n, const CUtensorMap& tmap_b, const PfGemm& p, int m_tiles, int max_items,
+                           cudaStream_t s);
 cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
-                           uint16_t* dbg_x, uint32_t* err, cudaStream_t s);
+                           uint16_t* dbg_x, float* xn2, float* xmax, uint32_t* err, cudaStream_t s);
+cudaError_t launch_pf_row_stats(const uint16_t* rows, int n, int d, float* n2, float* mx, cudaStream_t s);
 cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
                              int k, float* approx, float* xn2, float* wn2, float* xmax, float* wmax, int32_t* ids,
                              float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err, int n_sm,
                              cudaStream_t s);
-cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int32_t* cnt, int32_t* row_pair, int32_t* items,
-                           int32_t* n_items, cudaStream_t s);
+cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int tile, int32_t* cnt, int32_t* row_pair,
+                           int32_t* items, int32_t* n_items, cudaStream_t s);
 cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* gates, const uint16_t* hin,
                               uint16_t* hout, float* y_last, float* dbg_y, int T, int d, int k, cudaStream_t s);
 cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,

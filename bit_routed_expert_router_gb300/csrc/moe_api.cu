@@ -30,6 +30,7 @@ constexpr int kArgRing = 32;
 struct LayerStore {
   bool ready = false;
   uint16_t* router_w = nullptr;       // device fp16 [E][d]
+  float* router_stats = nullptr;      // device [2][E]: |row|^2 and max |row_i| (prefill router bound)
   uint8_t* shared = nullptr;          // device layout
   uint8_t* experts = nullptr;         // resident: E * stride
   uint8_t* slots = nullptr;           // host pool: N * stride
@@ -129,10 +130,10 @@ struct moe_ctx {
   uint16_t* pf_h[2] = {nullptr, nullptr};
   int32_t *pf_ids = nullptr, *pf_cnt = nullptr, *pf_rowpair = nullptr, *pf_items = nullptr, *pf_nitems = nullptr;
   float *pf_gates = nullptr, *pf_ytok = nullptr;
-  float *pf_approx = nullptr, *pf_xn2 = nullptr, *pf_wn2 = nullptr, *pf_xmax = nullptr, *pf_wmax = nullptr;
+  float *pf_approx = nullptr, *pf_xn2 = nullptr, *pf_xmax = nullptr;
   float* pf_ys = nullptr;
   unsigned long long* pf_timeline = nullptr;   // test hook 8: [4][16] GEMM event times of the first layer
-  CUtensorMap pf_map_xp{}, pf_map_x16{}, pf_map_ar{}, pf_map_as{};
+  CUtensorMap pf_map_xp[2]{}, pf_map_x16[2]{}, pf_map_ar[2]{}, pf_map_as[2]{};   // [0]: 128-row boxes, [1]: 32
   unsigned long long* p_timeline = nullptr;   // caller device buffer [n_layers][16], test hook 5
   // per-kernel timing
   bool profiling = false;
@@ -690,7 +691,8 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   }
   // the tcgen05 prefill: 128-row weight tiles of the down projection, one router
   // CTA column of 128 experts, and its shared memory
-  if (c.d % 128 == 0 && c.n_experts <= 128 && pf_gemm_smem() <= static_cast<size_t>(max_smem)) {
+  if (c.d % 128 == 0 && c.n_experts <= 128 && pf_gemm_smem(kPfTileN) <= static_cast<size_t>(max_smem) &&
+      pf_gemm_smem(kPfTileNSmall) <= static_cast<size_t>(max_smem)) {
     if (pf_set_attrs() == cudaSuccess) ctx->pf_ok = true;
     cudaGetLastError();
   }
@@ -707,6 +709,7 @@ void moe_destroy(moe_ctx* ctx) {
   for (auto& kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
   for (auto& Ls : ctx->L) {
     cudaFree(Ls.router_w);
+    cudaFree(Ls.router_stats);
     cudaFree(Ls.shared);
     cudaFree(Ls.experts);
     cudaFree(Ls.slots);
@@ -771,6 +774,8 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
   if (!pool && !Ls.experts) CK(cudaMalloc(&Ls.experts, static_cast<size_t>(c.n_experts) * ctx->stride));
   if (pool && !Ls.slot_of_expert) CK(cudaMalloc(&Ls.slot_of_expert, static_cast<size_t>(c.n_experts) * 4));
   CK(cudaMemcpy(Ls.router_w, router_w, static_cast<size_t>(c.n_experts) * c.d * 2, cudaMemcpyDefault));
+  if (!Ls.router_stats) CK(cudaMalloc(&Ls.router_stats, static_cast<size_t>(c.n_experts) * 2 * sizeof(float)));
+  CK(launch_pf_row_stats(Ls.router_w, c.n_experts, c.d, Ls.router_stats, Ls.router_stats + c.n_experts, nullptr));
 
   // canonical staging buffers (largest f), then repack on the device
   const int fmax = std::max(c.f, c.f_shared);
@@ -880,6 +885,11 @@ moe_status moe_reset_cache(moe_ctx* ctx) {
   return MOE_OK;
 }
 
+namespace {
+moe_status pf_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const float* logit_bias, void* h_out,
+                  float* y_last, cudaStream_t s);
+}  // namespace
+
 moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begin, int layer_end,
                            const float* logit_bias, void* h_out, float* y_last, moe_trace_rec* trace, int trace_cap,
                            int* trace_len, void* stream) {
@@ -903,16 +913,19 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
     return st;
   }
   if (B == 1 && ctx->use_persistent && ctx->p_ok) return persistent_run(ctx, layer_begin, layer_end, s);
+  // from about 20 tokens on, the grouped tcgen05 path beats the mma.sync GEMVs (measured crossover)
+  if (B >= kPfMinDecodeB && ctx->pf_ok && ctx->use_pf) return pf_run(ctx, h_in, B, layer_begin, layer_end, logit_bias,
+                                                                  h_out, y_last, s);
   return resident_run(ctx, B, layer_begin, layer_end, s);
 }
 
 namespace {
 
 // 2-D tensor map over a row-major fp16 matrix [rows][K]: boxes of 64 columns x
-// kPfTileN rows with the 128-byte swizzle the GEMM's operand tiles use.
+// box_rows rows with the 128-byte swizzle the GEMM's operand tiles use.
 // The driver entry point is looked up through the runtime, so the library does
 // not link libcuda itself (it loads on machines without a driver).
-bool encode_rows(CUtensorMap* m, void* base, int K, long long rows) {
+bool encode_rows(CUtensorMap* m, void* base, int K, long long rows, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     cudaDriverEntryPointQueryResult q{};
@@ -925,7 +938,7 @@ bool encode_rows(CUtensorMap* m, void* base, int K, long long rows) {
   }
   cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPfTileN)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -950,24 +963,25 @@ moe_status pf_alloc(moe_ctx* ctx) {
   ctx->pf_gates = dalloc<float>(P, o, nb);
   ctx->pf_cnt = dalloc<int32_t>(c.n_experts, o, nb);
   ctx->pf_rowpair = dalloc<int32_t>(P, o, nb);
-  ctx->pf_items = dalloc<int32_t>(3 * (P / kPfTileN + c.n_experts + 1), o, nb);
+  ctx->pf_items = dalloc<int32_t>(3 * (P / kPfTileNSmall + c.n_experts + 1), o, nb);
   ctx->pf_nitems = dalloc<int32_t>(1, o, nb);
   ctx->pf_ytok = dalloc<float>(P * c.d, o, nb);
   ctx->pf_approx = dalloc<float>(T * c.n_experts, o, nb);
   ctx->pf_xn2 = dalloc<float>(T, o, nb);
-  ctx->pf_wn2 = dalloc<float>(c.n_experts, o, nb);
   ctx->pf_xmax = dalloc<float>(T, o, nb);
-  ctx->pf_wmax = dalloc<float>(c.n_experts, o, nb);
   ctx->pf_ys = dalloc<float>(T * c.d, o, nb);
   if (!ctx->pf_xbf || !ctx->pf_x16 || !ctx->pf_xp || !ctx->pf_ar || !ctx->pf_as || !ctx->pf_h[0] || !ctx->pf_h[1] ||
       !ctx->pf_ids || !ctx->pf_gates || !ctx->pf_cnt || !ctx->pf_rowpair || !ctx->pf_items || !ctx->pf_nitems ||
-      !ctx->pf_ytok || !ctx->pf_approx || !ctx->pf_xn2 || !ctx->pf_wn2 || !ctx->pf_xmax || !ctx->pf_wmax || !ctx->pf_ys)
+      !ctx->pf_ytok || !ctx->pf_approx || !ctx->pf_xn2 || !ctx->pf_xmax || !ctx->pf_ys)
     return fail(ctx, MOE_ENOMEM, "prefill scratch (%zu bytes for %zu tokens) does not fit", nb, T);
-  if (!encode_rows(&ctx->pf_map_xp, ctx->pf_xp, c.d, static_cast<long long>(P)) ||
-      !encode_rows(&ctx->pf_map_x16, ctx->pf_x16, c.d, static_cast<long long>(T)) ||
-      !encode_rows(&ctx->pf_map_ar, ctx->pf_ar, c.f, static_cast<long long>(P)) ||
-      !encode_rows(&ctx->pf_map_as, ctx->pf_as, c.f_shared, static_cast<long long>(T)))
-    return fail(ctx, MOE_ECUDA, "cuTensorMapEncodeTiled failed for the prefill operands");
+  for (int i = 0; i < 2; ++i) {
+    const int br = i == 0 ? kPfTileN : kPfTileNSmall;
+    if (!encode_rows(&ctx->pf_map_xp[i], ctx->pf_xp, c.d, static_cast<long long>(P), br) ||
+        !encode_rows(&ctx->pf_map_x16[i], ctx->pf_x16, c.d, static_cast<long long>(T), br) ||
+        !encode_rows(&ctx->pf_map_ar[i], ctx->pf_ar, c.f, static_cast<long long>(P), br) ||
+        !encode_rows(&ctx->pf_map_as[i], ctx->pf_as, c.f_shared, static_cast<long long>(T), br))
+      return fail(ctx, MOE_ECUDA, "cuTensorMapEncodeTiled failed for the prefill operands");
+  }
   ctx->device_bytes += nb;
   ctx->pf_ready = true;
   return MOE_OK;
@@ -983,17 +997,20 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   const size_t xo = static_cast<size_t>(rel) * T;
   PROF(4, s);
   CK(launch_pf_prep(hin, T, d, c.prenorm, c.norm_eps, ctx->pf_xbf, ctx->pf_x16,
-                    dbg && ctx->dbg_x ? ctx->dbg_x + xo * d : nullptr, ctx->err_word, s));
+                    dbg && ctx->dbg_x ? ctx->dbg_x + xo * d : nullptr, ctx->pf_xn2, ctx->pf_xmax, ctx->err_word, s));
   CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_approx,
-                      ctx->pf_xn2, ctx->pf_wn2, ctx->pf_xmax, ctx->pf_wmax, ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
+                      ctx->pf_xn2, L.router_stats, ctx->pf_xmax, L.router_stats + E, ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
                       dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr, ctx->err_word, ctx->n_sm, s));
-  CK(launch_pf_plan(ctx->pf_ids, P, E, ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items, ctx->pf_nitems, s));
+  // token tiles of 32 rows when the experts' groups are small (a few rows each), else 128
+  const int nr = P <= 16 * E ? kPfTileNSmall : kPfTileN, ns = T <= 48 ? kPfTileNSmall : kPfTileN;
+  const int mr = nr == kPfTileN ? 0 : 1, ms = ns == kPfTileN ? 0 : 1;
+  CK(launch_pf_plan(ctx->pf_ids, P, E, nr, ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items, ctx->pf_nitems, s));
   CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
   PROF(-1, s);
   const size_t gu_r = static_cast<size_t>(c.f / 8) * (d / 64) * kGroupBytes;
   const size_t gu_s = static_cast<size_t>(c.f_shared / 8) * (d / 64) * kGroupBytes;
-  const int max_items = P / kPfTileN + E + 1;
-  const int t_items = (T + kPfTileN - 1) / kPfTileN;
+  const int max_items = P / nr + E + 1;
+  const int t_items = (T + ns - 1) / ns;
   PfGemm g{};
   g.tl = nullptr;
   g.d = d;
@@ -1012,7 +1029,7 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   a.out16 = ctx->pf_ar;
   a.f_out = c.f;
   if (ctx->pf_timeline && rel == 0) a.tl = ctx->pf_timeline;
-  CK(launch_pf_gemm(ctx->pf_map_xp, a, c.f / 64, max_items, s));
+  CK(launch_pf_gemm(nr, ctx->pf_map_xp[mr], a, c.f / 64, max_items, s));
   // shared gate/up over every token
   PfGemm b = g;
   b.w = L.shared;
@@ -1023,7 +1040,7 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   b.out16 = ctx->pf_as;
   b.f_out = c.f_shared;
   if (ctx->pf_timeline && rel == 0) b.tl = ctx->pf_timeline + 16;
-  CK(launch_pf_gemm(ctx->pf_map_x16, b, c.f_shared / 64, t_items, s));
+  CK(launch_pf_gemm(ns, ctx->pf_map_x16[ms], b, c.f_shared / 64, t_items, s));
   // routed down: per pair, fp32 [T*k][d]
   PfGemm r = g;
   r.w = L.experts + gu_r;
@@ -1035,7 +1052,7 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   r.out32 = ctx->pf_ytok;
   r.pair_of_row = ctx->pf_rowpair;
   if (ctx->pf_timeline && rel == 0) r.tl = ctx->pf_timeline + 32;
-  CK(launch_pf_gemm(ctx->pf_map_ar, r, d / 128, max_items, s));
+  CK(launch_pf_gemm(nr, ctx->pf_map_ar[mr], r, d / 128, max_items, s));
   // shared down, then the combine: shared + routed in top-k order + residual
   PfGemm q = g;
   q.w = L.shared + gu_s;
@@ -1045,13 +1062,28 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   q.mode = PF_DN_SHARED;
   q.out32 = ctx->pf_ys;
   if (ctx->pf_timeline && rel == 0) q.tl = ctx->pf_timeline + 48;
-  CK(launch_pf_gemm(ctx->pf_map_as, q, d / 128, t_items, s));
+  CK(launch_pf_gemm(ns, ctx->pf_map_as[ms], q, d / 128, t_items, s));
   PROF(-1, s);
   PROF(6, s);
   CK(launch_pf_combine(ctx->pf_ys, ctx->pf_ytok, ctx->pf_gates, hin, hout, rel == n_rel - 1 ? y_last : nullptr,
                        dbg && ctx->dbg_y ? ctx->dbg_y + xo * d : nullptr, T, d, k, s));
   PROF(-1, s);
   return MOE_OK;
+}
+
+// The tcgen05 path over [l0, l1) for T tokens.
+moe_status pf_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const float* logit_bias, void* h_out,
+                  float* y_last, cudaStream_t s) {
+  moe_status st = pf_alloc(ctx);
+  if (st != MOE_OK) return st;
+  const int n_rel = l1 - l0;
+  for (int rel = 0; rel < n_rel; ++rel) {
+    const uint16_t* hin = rel == 0 ? static_cast<const uint16_t*>(h) : ctx->pf_h[(rel - 1) & 1];
+    uint16_t* hout = rel == n_rel - 1 ? static_cast<uint16_t*>(h_out) : ctx->pf_h[rel & 1];
+    st = pf_layer(ctx, l0 + rel, rel, n_rel, hin, hout, T, logit_bias, y_last, s);
+    if (st != MOE_OK) return st;
+  }
+  return prof_collect(ctx, s);
 }
 
 }  // namespace
@@ -1066,18 +1098,7 @@ moe_status moe_prefill(moe_ctx* ctx, const void* h, int T, int layer_begin, int 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CK(cudaSetDevice(ctx->device));
   const int d = ctx->cfg.d;
-  if (ctx->pf_ok && ctx->use_pf) {
-    st = pf_alloc(ctx);
-    if (st != MOE_OK) return st;
-    const int n_rel = layer_end - layer_begin;
-    for (int rel = 0; rel < n_rel; ++rel) {
-      const uint16_t* hin = rel == 0 ? static_cast<const uint16_t*>(h) : ctx->pf_h[(rel - 1) & 1];
-      uint16_t* hout = rel == n_rel - 1 ? static_cast<uint16_t*>(h_out) : ctx->pf_h[rel & 1];
-      st = pf_layer(ctx, layer_begin + rel, rel, n_rel, hin, hout, T, logit_bias, y_last, s);
-      if (st != MOE_OK) return st;
-    }
-    return prof_collect(ctx, s);
-  }
+  if (ctx->pf_ok && ctx->use_pf) return pf_run(ctx, h, T, layer_begin, layer_end, logit_bias, h_out, y_last, s);
   // otherwise: the batched decode kernels, kMaxDecodeB tokens at a time
   for (int t0 = 0; t0 < T; t0 += ctx->Bd) {
     const int B = std::min(ctx->Bd, T - t0);

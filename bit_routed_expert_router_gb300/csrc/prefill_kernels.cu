@@ -36,8 +36,13 @@ namespace moe {
 namespace {
 
 constexpr int kM = 128;                 // weight rows per CTA tile
-constexpr int kN = kPfTileN;            // token rows per CTA tile
-constexpr int kSlots = 2;               // k-step slots (A + B tiles)
+// Token rows per CTA tile: 128 for large groups, 32 when every expert has only
+// a few rows (then the MMA is 4x shorter and a third k-step slot fits).
+template <int N>
+struct Tile {
+  static constexpr int kSlots = N == 128 ? 2 : 3;     // k-step slots (A + B tiles)
+  static constexpr int kBBytes = N * 128;              // one N-row x 64-col fp16 tile
+};
 constexpr int kRawG = 4;                // int4 groups per raw stage
 constexpr int kRawStages = 2;
 constexpr int kTileBytes = 128 * 128;   // one 128-row x 64-col fp16 tile (16 KB)
@@ -46,20 +51,27 @@ constexpr int kRawBytes = 8 * kRawStride;         // 8 tiles of 16 rows = 128 ro
 constexpr int kDqWarps = 8;             // dequant + epilogue warps, one 16-row tile each per k step
 constexpr int kThreads = 32 * (2 + kDqWarps);  // warp 0 producer, warp 1 MMA + TMEM, warps 2..9 dequant + epilogue
 
+template <int N>
 struct GemmSmem {
+  static constexpr int kSlots = Tile<N>::kSlots;
   uint8_t a[kSlots][kTileBytes];        // fp16 weight tiles, K-major, 128-byte swizzle (1024-aligned)
-  uint8_t b[kSlots][kTileBytes];        // fp16 token tiles, same layout (TMA writes them)
+  uint8_t b[kSlots][Tile<N>::kBBytes];  // fp16 token tiles, same layout (TMA writes them)
   uint8_t raw[kRawStages][kRawBytes];   // int4 blocks as stored
   uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   uint64_t b_full[kSlots], a_full[kSlots], slot_empty[kSlots];
   uint64_t acc_full;
   uint32_t tmem_base;
   int abort;
-  int row_info[kN];                     // epilogue: pair index (routed down) of each token row
+  int row_info[N];                      // epilogue: pair index (routed down) of each token row
 };
-static_assert(kTileBytes % 1024 == 0 && offsetof(GemmSmem, b) % 1024 == 0, "swizzled tiles need 1 KB alignment");
-static_assert(offsetof(GemmSmem, raw) % 128 == 0 && kRawStride % 16 == 0, "bulk copy targets need 16 B");
-static_assert(offsetof(GemmSmem, raw_full) % 8 == 0, "mbarriers need 8 B");
+static_assert(kTileBytes % 1024 == 0 && offsetof(GemmSmem<128>, b) % 1024 == 0 &&
+                  offsetof(GemmSmem<32>, b) % 1024 == 0 && Tile<32>::kBBytes % 1024 == 0,
+              "swizzled tiles need 1 KB alignment");
+static_assert(offsetof(GemmSmem<128>, raw) % 128 == 0 && offsetof(GemmSmem<32>, raw) % 128 == 0 &&
+                  kRawStride % 16 == 0,
+              "bulk copy targets need 16 B");
+static_assert(offsetof(GemmSmem<128>, raw_full) % 8 == 0 && offsetof(GemmSmem<32>, raw_full) % 8 == 0,
+              "mbarriers need 8 B");
 
 // ------------------------------------------------------------------ tcgen05 / TMA primitives
 
@@ -131,7 +143,8 @@ __device__ __forceinline__ void pf_stamp(const PfGemm& p, int k) {
   }
 }
 
-__device__ __forceinline__ bool wait_or_abort(GemmSmem& S, uint64_t* bar, uint32_t parity, uint32_t* err) {
+template <class Sm>
+__device__ __forceinline__ bool wait_or_abort(Sm& S, uint64_t* bar, uint32_t parity, uint32_t* err) {
   if (mbar_wait_bounded(bar, parity, err)) return true;
   S.abort = 1;
   return false;
@@ -176,10 +189,12 @@ __device__ __forceinline__ void dequant_block(const uint8_t* blk, uint8_t* tile,
 // ------------------------------------------------------------------ the GEMM
 
 // Two CTAs share an SM, so one's epilogue overlaps the other's main loop.
+template <int kN>
 __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__ CUtensorMap tmap_b, PfGemm p) {
+  constexpr int kSlots = Tile<kN>::kSlots;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  GemmSmem& S = *reinterpret_cast<GemmSmem*>(smem_raw + pad);
+  GemmSmem<kN>& S = *reinterpret_cast<GemmSmem<kN>*>(smem_raw + pad);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x;
   const int item = blockIdx.y;
@@ -246,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
         }
         const int slot = G % kSlots;
         if (!wait_or_abort(S, &S.slot_empty[slot], ((G / kSlots) & 1) ^ 1, p.err)) break;
-        mbar_arrive_expect_tx(&S.b_full[slot], kTileBytes);
+        mbar_arrive_expect_tx(&S.b_full[slot], Tile<kN>::kBBytes);
         tma_load_2d(S.b[slot], &tmap_b, 64 * G, row0, &S.b_full[slot]);
         b_issued = G + 1;
       }
@@ -281,7 +296,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
     // dequant warps: warp w takes 16-row tile w - 2 of each k step; in the epilogue it reads
     // accumulator lanes 32q .. 32q + 31 (q = w % 4, the lanes its warp may access) and the
     // column half (w - 2) / 4
-    const int dw = warp - 2, q = warp & 3, c_lo = (dw >> 2) * (kN / 2);
+    const int dw = warp - 2, q = warp & 3;
+    // column range of this warp's epilogue: two halves of 128 columns, or all 32 for warps 2..5
+    const int c_lo = kN == 128 ? (dw >> 2) * 64 : 0;
+    const int c_hi = kN == 128 ? c_lo + 64 : ((dw >> 2) == 0 ? 32 : 0);
     for (int G = 0; G < nG; ++G) {
       const int s = G / kRawG, rs = s % kRawStages, gi = G % kRawG;
       if (gi == 0 && !wait_or_abort(S, &S.raw_full[rs], (s / kRawStages) & 1, p.err)) break;
@@ -301,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
     tc_fence_after();
     if (ok) {
       const int row_in_tile = 32 * q + lane;
-      for (int c0 = c_lo; c0 < c_lo + kN / 2; c0 += 32) {
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
         float v[32];
         tc_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
         if (p.mode == PF_GU) {
@@ -350,8 +368,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
 // One CTA per token: x = RMSnorm(h) (or h) as bf16 and fp16; the sum of squares
 // is taken in a fixed order.  fp16 overflow / underflow of x is flagged.
 __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int prenorm, float eps, uint16_t* x_bf,
-                                                 uint16_t* x16, uint16_t* dbg_x, uint32_t* err) {
-  __shared__ float red[8];
+                                                 uint16_t* x16, uint16_t* dbg_x, float* xn2, float* xmax,
+                                                 uint32_t* err) {
+  __shared__ float red[8], red2[8], redm[8];
   const int t = blockIdx.x;
   const uint16_t* hr = h + static_cast<size_t>(t) * d;
   float ss = 0.f;
@@ -370,17 +389,59 @@ __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int p
     r = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
   }
   bool bad = false;
+  float s2 = 0.f, mx = 0.f;
   for (int i = threadIdx.x; i < d; i += 256) {
     const uint16_t hb = hr[i];
     const uint16_t xb = prenorm ? float_to_bf16_bits(bf16_bits_to_float(hb) * r) : hb;
     const float xf = bf16_bits_to_float(xb);
+    s2 = fmaf(xf, xf, s2);
+    mx = fmaxf(mx, fabsf(xf));   // NaN is dropped here but makes s2 NaN
     x_bf[static_cast<size_t>(t) * d + i] = xb;
     const __half xh = __float2half_rn(xf);   // exact unless |x| < 2^-14 (then off by < 2^-25)
     if (!(fabsf(xf) < 65504.f)) bad = true;
     x16[static_cast<size_t>(t) * d + i] = __half_as_ushort(xh);
     if (dbg_x) dbg_x[static_cast<size_t>(t) * d + i] = xb;
   }
+#pragma unroll
+  for (int m = 16; m; m >>= 1) {
+    s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, m);
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, m));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red2[threadIdx.x >> 5] = s2;
+    redm[threadIdx.x >> 5] = mx;
+  }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, ERR_PF_RANGE);
+  if (threadIdx.x == 0) {
+    float a = 0.f, b = 0.f;
+    for (int w = 0; w < 8; ++w) {
+      a += red2[w];
+      b = fmaxf(b, redm[w]);
+    }
+    xn2[t] = a;       // for the router's error bound
+    xmax[t] = b;
+  }
+}
+
+// |row|^2 and max |row_i| of fp16 rows (the router's rows, once per layer), one warp per row.
+__global__ void __launch_bounds__(256) k_pf_row_stats(const uint16_t* rows, int n, int d, float* n2, float* mx) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= n) return;
+  float ss = 0.f, m = 0.f;
+  for (int i = lane; i < d; i += 32) {
+    const float v = __half2float(__ushort_as_half(rows[static_cast<size_t>(r) * d + i]));
+    ss = fmaf(v, v, ss);
+    m = fmaxf(m, fabsf(v));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  }
+  if (lane == 0) {
+    n2[r] = ss;
+    mx[r] = m;
+  }
 }
 
 // Router, in two passes.
@@ -391,8 +452,8 @@ __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int p
 // (the products are exact in fp32: 11-bit x 8-bit significands), so the sum
 // differs from the exact one by at most about (64 + 2 * 44) u * sum|x_i w_i|
 // with u = 2^-24 (chunk sums, slice sums and the adds across slices), and
-// sum|x_i w_i| <= |x| |w| (Cauchy-Schwarz).  The CTAs of the first expert /
-// token block also store |x_t|^2, |w_e|^2 and the rows' largest |x_i|, |w_i|.
+// sum|x_i w_i| <= |x| |w| (Cauchy-Schwarz).  |x_t|^2 and max|x_t,i| come from
+// k_pf_prep, |w_e|^2 and max|w_e,i| from k_pf_row_stats when the layer is loaded.
 //
 // Pass 2 (k_pf_route): one CTA per token.  With L~_e the approximate logit
 // plus bias and eps_e its bound, tau = the k-th largest L~_e - eps_e is below
@@ -407,38 +468,11 @@ constexpr int kRT = 64;       // tokens per CTA
 constexpr int kRE = 64;       // experts per CTA
 constexpr int kRK = 64;       // k chunk (one partial sum per chunk)
 __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
-                                                          int E, int k_slice, float* approx, float* xn2, float* wn2,
-                                                          float* xmax, float* wmax) {
+                                                          int E, int k_slice, float* approx) {
   __shared__ __align__(16) float xs[kRK][kRT];   // K-major, so a thread reads four tokens as one float4
   __shared__ __align__(16) float ws[kRK][kRE];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE, kb = blockIdx.z * k_slice;
-  // squared norms and largest magnitudes (for the error bound), full d, by the CTAs of the first slice
-  if (blockIdx.z == 0 && (blockIdx.y == 0 || blockIdx.x == 0)) {
-    for (int r = warp; r < kRT + kRE; r += 8) {
-      const bool is_x = r < kRT;
-      if (is_x && blockIdx.y != 0) continue;
-      if (!is_x && blockIdx.x != 0) continue;
-      const int row = is_x ? t0 + r : e0 + r - kRT;
-      if (row >= (is_x ? T : E)) continue;
-      float ss = 0.f, mx = 0.f;
-      for (int i = lane; i < d; i += 32) {
-        const float v = is_x ? bf16_bits_to_float(x_bf[static_cast<size_t>(row) * d + i])
-                             : __half2float(__ushort_as_half(router_w[static_cast<size_t>(row) * d + i]));
-        ss = fmaf(v, v, ss);
-        mx = fmaxf(mx, fabsf(v));   // NaN is dropped here but makes ss NaN
-      }
-#pragma unroll
-      for (int m = 16; m; m >>= 1) {
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, m);
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, m));
-      }
-      if (lane == 0) {
-        (is_x ? xn2 : wn2)[row] = ss;
-        (is_x ? xmax : wmax)[row] = mx;
-      }
-    }
-  }
   const int tx = tid & 15;             // experts e0 + 4 tx .. + 3
   const int ty = tid >> 4;             // tokens t0 + 4 ty .. + 3
   float acc[4][4];
@@ -708,7 +742,7 @@ __global__ void __launch_bounds__(256) k_pf_count(const int32_t* ids, int P, int
 
 // Stable placement: expert e's pairs in increasing pair order at
 // [off_e, off_e + n_e), and its 128-row work items.
-__global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, int E, const int32_t* cnt,
+__global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, int E, const int32_t* cnt, int tile,
                                                     int32_t* row_pair, int32_t* items, int32_t* n_items) {
   const int e = blockIdx.x;
   __shared__ int s_off, s_base;
@@ -717,17 +751,17 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
     int off = 0, it = 0;
     for (int e2 = 0; e2 < e; ++e2) {
       off += cnt[e2];
-      it += (cnt[e2] + kPfTileN - 1) / kPfTileN;
+      it += (cnt[e2] + tile - 1) / tile;
     }
     s_off = off;
     s_base = 0;
     const int n_e = cnt[e];
-    for (int i = 0; i * kPfTileN < n_e; ++i) {
+    for (int i = 0; i * tile < n_e; ++i) {
       items[3 * (it + i)] = e;
-      items[3 * (it + i) + 1] = off + i * kPfTileN;
-      items[3 * (it + i) + 2] = min(kPfTileN, n_e - i * kPfTileN);
+      items[3 * (it + i) + 1] = off + i * tile;
+      items[3 * (it + i) + 2] = min(tile, n_e - i * tile);
     }
-    if (e == E - 1) *n_items = it + (n_e + kPfTileN - 1) / kPfTileN;
+    if (e == E - 1) *n_items = it + (n_e + tile - 1) / tile;
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -789,22 +823,32 @@ __global__ void __launch_bounds__(256) k_pf_gather(const uint16_t* x16, const in
 
 }  // namespace
 
-size_t pf_gemm_smem() { return sizeof(GemmSmem) + 1024; }
+size_t pf_gemm_smem(int n) { return (n == 32 ? sizeof(GemmSmem<32>) : sizeof(GemmSmem<128>)) + 1024; }
 
 cudaError_t pf_set_attrs() {
-  return cudaFuncSetAttribute((const void*)k_pf_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(pf_gemm_smem()));
+  cudaError_t e = cudaFuncSetAttribute((const void*)k_pf_gemm<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(pf_gemm_smem(128)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute((const void*)k_pf_gemm<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(pf_gemm_smem(32)));
 }
 
-cudaError_t launch_pf_gemm(const CUtensorMap& tmap_b, const PfGemm& p, int m_tiles, int max_items, cudaStream_t s) {
+cudaError_t launch_pf_gemm(int n, const CUtensorMap& tmap_b, const PfGemm& p, int m_tiles, int max_items,
+                           cudaStream_t s) {
   if (m_tiles <= 0 || max_items <= 0) return cudaSuccess;
-  k_pf_gemm<<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(), s>>>(tmap_b, p);
+  if (n == 32) k_pf_gemm<32><<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(32), s>>>(tmap_b, p);
+  else k_pf_gemm<128><<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(128), s>>>(tmap_b, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
-                           uint16_t* dbg_x, uint32_t* err, cudaStream_t s) {
-  k_pf_prep<<<T, 256, 0, s>>>(h, d, prenorm, eps, x_bf, x16, dbg_x, err);
+                           uint16_t* dbg_x, float* xn2, float* xmax, uint32_t* err, cudaStream_t s) {
+  k_pf_prep<<<T, 256, 0, s>>>(h, d, prenorm, eps, x_bf, x16, dbg_x, xn2, xmax, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pf_row_stats(const uint16_t* rows, int n, int d, float* n2, float* mx, cudaStream_t s) {
+  k_pf_row_stats<<<(n + 7) / 8, 256, 0, s>>>(rows, n, d, n2, mx);
   return cudaGetLastError();
 }
 
@@ -826,16 +870,16 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
     if (e != cudaSuccess) return e;
   }
   k_pf_logits_approx<<<dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), 256, 0, s>>>(
-      x_bf, router_w, T, d, E, d / slices, approx, xn2, wn2, xmax, wmax);
+      x_bf, router_w, T, d, E, d / slices, approx);
   k_pf_route<<<(T + 7) / 8, 256, 0, s>>>(x_bf, router_w, approx, xn2, wn2, xmax, wmax, bias, T, d, E, k, ids, gates, dbg_ids,
                                dbg_gates, err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int32_t* cnt, int32_t* row_pair, int32_t* items,
-                           int32_t* n_items, cudaStream_t s) {
+cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int tile, int32_t* cnt, int32_t* row_pair,
+                           int32_t* items, int32_t* n_items, cudaStream_t s) {
   k_pf_count<<<E, 256, 0, s>>>(ids, P, cnt);
-  k_pf_scatter<<<E, 256, 0, s>>>(ids, P, E, cnt, row_pair, items, n_items);
+  k_pf_scatter<<<E, 256, 0, s>>>(ids, P, E, cnt, tile, row_pair, items, n_items);
   return cudaGetLastError();
 }
 
