@@ -83,6 +83,8 @@ def lib():
             L.or_residual_bf16.argtypes = [vp, vp, i32, vp]
             L.or_lru_step.restype = i32
             L.or_lru_step.argtypes = [i32, vp, vp, vp, i32, i64, vp, vp, vp]
+            L.or_lfu_step.restype = i32
+            L.or_lfu_step.argtypes = [i32, vp, vp, vp, vp, i32, i64, vp, vp, vp]
             _lib = L
     return _lib
 
@@ -254,6 +256,29 @@ class LRU:
         ev = np.zeros(k, dtype=np.int32)
         m = lib().or_lru_step(self.n, _p(self.expert_of_slot), _p(self.last_use), _p(ii), k, int(t),
                               _p(hit), _p(slot), _p(ev))
+        if m < 0:
+            raise ValueError("n_slots < k")
+        return hit, slot, ev
+
+
+class LFU:
+    """One layer's LFU slot table: expert_of_slot, last_use and the whole-run
+    use count of every expert (or_lfu_step rules)."""
+
+    def __init__(self, n_slots: int, n_experts: int):
+        self.n = n_slots
+        self.expert_of_slot = np.full(n_slots, -1, dtype=np.int32)
+        self.last_use = np.full(n_slots, -1, dtype=np.int64)
+        self.use_count = np.zeros(n_experts, dtype=np.int64)
+
+    def step(self, ids, t: int):
+        ii = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        k = ii.shape[0]
+        hit = np.zeros(k, dtype=np.int32)
+        slot = np.zeros(k, dtype=np.int32)
+        ev = np.zeros(k, dtype=np.int32)
+        m = lib().or_lfu_step(self.n, _p(self.expert_of_slot), _p(self.last_use), _p(self.use_count), _p(ii), k,
+                              int(t), _p(hit), _p(slot), _p(ev))
         if m < 0:
             raise ValueError("n_slots < k")
         return hit, slot, ev

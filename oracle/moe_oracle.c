@@ -346,3 +346,60 @@ int or_lru_step(int n_slots, int32_t *expert_of_slot, int64_t *last_use, const i
     free(used);
     return misses;
 }
+
+/* ---- per-layer LFU expert-slot cache ---- */
+
+/* One step of one layer with least-frequently-used eviction.  use_count[E]
+ * counts, over the whole run, how often each expert was picked (hit or miss);
+ * it is incremented for every top-k position of this step.  Hits refresh
+ * their slot's last_use; misses, in top-k order, take the slot that has the
+ * smallest (use count of its expert, last_use, slot index) among slots
+ * neither hit nor filled in this step, an empty slot counting -1 for both.
+ * Outputs and return value as or_lru_step. */
+int or_lfu_step(int n_slots, int32_t *expert_of_slot, int64_t *last_use, int64_t *use_count,
+                const int32_t *ids, int k, int64_t t, int32_t *hit, int32_t *slot, int32_t *evicted)
+{
+    if (n_slots < k)
+        return -1;
+    char *used = (char *)calloc((size_t)n_slots, 1);
+    for (int j = 0; j < k; ++j) {
+        hit[j] = 0;
+        slot[j] = -1;
+        evicted[j] = -1;
+        for (int s = 0; s < n_slots; ++s) {
+            if (expert_of_slot[s] == ids[j]) {
+                hit[j] = 1;
+                slot[j] = s;
+                used[s] = 1;
+                last_use[s] = t;
+                break;
+            }
+        }
+    }
+    int misses = 0;
+    for (int j = 0; j < k; ++j) {
+        if (hit[j])
+            continue;
+        int victim = -1;
+        int64_t vc = 0;
+        for (int s = 0; s < n_slots; ++s) {
+            if (used[s])
+                continue;
+            const int64_t c = expert_of_slot[s] < 0 ? -1 : use_count[expert_of_slot[s]];
+            if (victim < 0 || c < vc || (c == vc && last_use[s] < last_use[victim])) {
+                victim = s;     /* strict comparisons keep the lower slot index on full ties */
+                vc = c;
+            }
+        }
+        evicted[j] = expert_of_slot[victim];
+        expert_of_slot[victim] = ids[j];
+        last_use[victim] = t;
+        used[victim] = 1;
+        slot[j] = victim;
+        ++misses;
+    }
+    for (int j = 0; j < k; ++j)
+        use_count[ids[j]] += 1;
+    free(used);
+    return misses;
+}

@@ -375,3 +375,58 @@ def test_lru_agrees_with_move_to_front_formulation():
 def test_lru_rejects_fewer_slots_than_k():
     with pytest.raises(ValueError):
         oracle.LRU(1).step([0, 1], 0)
+
+
+# ----------------------------------------------------------------- LFU slot cache
+
+def test_lfu_hand_worked_traces():
+    with open(os.path.join(GOLDEN, "lfu_hand_traces.json")) as fh:
+        g = json.load(fh)
+    for tr in g["traces"]:
+        lfu = oracle.LFU(tr["n_slots"], tr["n_experts"])
+        hits = misses = 0
+        for st in tr["steps"]:
+            hit, slot, ev = lfu.step(st["ids"], st["t"])
+            assert list(hit) == st["hit"], st
+            assert list(slot) == st["slot"], st
+            assert list(ev) == st["evicted"], st
+            hits += int(hit.sum())
+            misses += int(len(hit) - hit.sum())
+        assert hits == tr["total_hits"] and misses == tr["total_misses"]
+        assert list(lfu.expert_of_slot) == tr["final_expert_of_slot"]
+        assert list(lfu.use_count) == tr["final_use_count"]
+
+
+def test_lfu_reduces_to_lru_when_no_expert_repeats():
+    """If no expert is picked twice, every cached expert has count 1 and the
+    eviction order falls back to (last_use, slot): exactly LRU."""
+    rng = np.random.default_rng(11)
+    for trial in range(50):
+        k = int(rng.integers(1, 5))
+        n = int(rng.integers(k, 12))
+        steps = 30
+        E = steps * k
+        seq = rng.permutation(E).astype(np.int32).reshape(steps, k)
+        a, b = oracle.LFU(n, E), oracle.LRU(n)
+        for t in range(steps):
+            h1, s1, e1 = a.step(seq[t], t)
+            h2, s2, e2 = b.step(seq[t], t)
+            assert list(h1) == list(h2) and list(s1) == list(s2) and list(e1) == list(e2)
+
+
+def test_lfu_keeps_a_hot_expert_through_a_scan():
+    """A hot expert picked often survives a scan of one-off experts under LFU,
+    and is evicted by it under LRU."""
+    n, E = 4, 64
+    lfu, lru = oracle.LFU(n, E), oracle.LRU(n)
+    t = 0
+    for _ in range(5):
+        for pol in (lfu, lru):
+            pol.step([7], t)
+        t += 1
+    for e in range(20, 30):
+        for pol in (lfu, lru):
+            pol.step([e], t)
+        t += 1
+    assert 7 in list(lfu.expert_of_slot)
+    assert 7 not in list(lru.expert_of_slot)
