@@ -723,29 +723,34 @@ def run_ours_pool(args):
     out = torch.empty(1, sh.d, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
     n_tok = min(N_TOKENS, max(args.steps, 16))
-    sweep = {}
-    for n_slots in (8, 16, 32, 64):
-        moe.check(moe.moe_set_slots(ctx, n_slots), ctx)
-        for t in range(args.warmup):
-            moe.check(moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, N_LAYERS, bias[t], out, None, None, stream)[0], ctx)
-        moe.check(moe.moe_sync(ctx, stream), ctx)
-        _, s0 = moe.moe_get_stats(ctx)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for i in range(n_tok):
-            t = (args.warmup + i) % N_TOKENS
-            moe.check(moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, N_LAYERS, bias[t], out, None, None, stream)[0], ctx)
-        moe.check(moe.moe_sync(ctx, stream), ctx)
-        torch.cuda.synchronize()
-        dt = time.perf_counter() - t0
-        _, s1 = moe.moe_get_stats(ctx)
-        hits, misses = s1.hits - s0.hits, s1.misses - s0.misses
-        staged = s1.staged_bytes - s0.staged_bytes
-        sweep[str(n_slots)] = {"tokens_per_s": n_tok / dt, "hit_rate": hits / max(hits + misses, 1),
-                               "misses_per_token": misses / n_tok, "staged_bytes_per_token": staged / n_tok,
-                               "host_link_gbs": staged / dt / 1e9}
+    sweeps = {}
+    for policy in (moe.MOE_CACHE_LRU, moe.MOE_CACHE_LFU):
+        sweep = sweeps.setdefault("lru" if policy == moe.MOE_CACHE_LRU else "lfu", {})
+        for n_slots in (8, 16, 32, 64):
+            moe.check(moe.moe_set_slots(ctx, n_slots), ctx)
+            moe.check(moe.moe_set_cache_policy(ctx, policy), ctx)
+            for t in range(args.warmup):
+                moe.check(moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, N_LAYERS, bias[t], out, None, None,
+                                              stream)[0], ctx)
+            moe.check(moe.moe_sync(ctx, stream), ctx)
+            _, s0 = moe.moe_get_stats(ctx)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i in range(n_tok):
+                t = (args.warmup + i) % N_TOKENS
+                moe.check(moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, N_LAYERS, bias[t], out, None, None,
+                                              stream)[0], ctx)
+            moe.check(moe.moe_sync(ctx, stream), ctx)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            _, s1 = moe.moe_get_stats(ctx)
+            hits, misses = s1.hits - s0.hits, s1.misses - s0.misses
+            staged = s1.staged_bytes - s0.staged_bytes
+            sweep[str(n_slots)] = {"tokens_per_s": n_tok / dt, "hit_rate": hits / max(hits + misses, 1),
+                                   "misses_per_token": misses / n_tok, "staged_bytes_per_token": staged / n_tok,
+                                   "host_link_gbs": staged / dt / 1e9}
     moe.moe_destroy(ctx)
-    best = sweep["64"]
+    best = sweeps["lru"]["64"]
     line = {
         "metric": "MoE decode tokens/s with a per-layer LRU slot cache over a pinned host expert pool (30 layers)",
         "value": best["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1, "steps": n_tok, "warmup": args.warmup,
@@ -754,7 +759,7 @@ def run_ours_pool(args):
         "config": {"workload": "decode30_hostpool_lru_zipf", "layers": N_LAYERS, "B": 1, "slots_reported": 64,
                    "routing": "router logits + Zipf(1.1)/reuse-0.6 bias trace",
                    "timing": "host wall clock around the synchronised token loop (the host drives the staging)"},
-        "sweep_by_slots": sweep,
+        "sweep_by_slots": sweeps["lru"], "sweep_by_slots_lfu": sweeps["lfu"],
         "roofline": {"bound": "host link", "achieved": best["host_link_gbs"], "peak": None, "unit": "GB/s",
                      "frac": None, "traffic": None},
         "gpu_launches": None, "cpu_baseline": None,

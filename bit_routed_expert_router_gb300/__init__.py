@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
 
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTATE, MOE_ETIMEOUT, MOE_EDOMAIN = range(7)
 MOE_RESIDENT_HBM, MOE_HOST_POOL = 0, 1
+MOE_CACHE_LRU, MOE_CACHE_LFU = 0, 1
 MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
 HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6
 HOOK_PREFILL_TC = 7
@@ -68,6 +69,7 @@ _SIGS = {
     "moe_init_layer": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.POINTER(MoeExpertWeights),
                                  C.POINTER(MoeExpertWeights), C.c_int]),
     "moe_set_slots": (C.c_int, [C.c_void_p, C.c_int]),
+    "moe_set_cache_policy": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_decode_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                                   C.c_void_p, C.POINTER(MoeTraceRec), C.c_int, C.POINTER(C.c_int),
                                   C.c_void_p]),
@@ -176,6 +178,10 @@ def moe_init_layer(ctx, layer: int, router_w, experts: dict, shared: dict, resid
 
 def moe_set_slots(ctx, n_slots: int) -> int:
     return lib().moe_set_slots(ctx, n_slots)
+
+
+def moe_set_cache_policy(ctx, policy: int) -> int:
+    return lib().moe_set_cache_policy(ctx, policy)
 
 
 def moe_decode_step(ctx, h_in, B: int, layer_begin: int, layer_end: int, logit_bias=None, h_out=None,

@@ -230,18 +230,22 @@ __device__ __forceinline__ void build_plan_and_lru(const KParams& p, const DevCa
   const int E = p.E, k = p.k, nP = B * k;
 
   if (p.pool && warp == 0) {
-    // LRU over this layer's slots (B == 1): hits refresh; misses in top-k
-    // order take the smallest (last_use, slot) among slots untouched this step.
+    // Slot cache over this layer's slots (B == 1): hits refresh; misses in
+    // top-k order take, among slots untouched this step, the smallest
+    // (last_use, slot) under LRU, or (use count of its expert, last_use, slot)
+    // under LFU (an empty slot counts -1).
     const int N = p.n_slots;
     const long long t = A->step;
+    const bool lfu = p.policy == 1;
     int eos[8];
-    long long lu[8];
+    long long lu[8], uc[8];
     unsigned used = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int s = lane + 32 * i;
       eos[i] = (s < N) ? p.expert_of_slot[s] : -1;
       lu[i] = (s < N) ? p.last_use[s] : LLONG_MAX;
+      uc[i] = (!lfu || s >= N) ? 0 : (eos[i] >= 0 ? p.use_count[eos[i]] : -1);
       if (s >= N) used |= 1u << i;
     }
     int n_hit = 0, n_miss = 0;
@@ -268,21 +272,25 @@ __device__ __forceinline__ void build_plan_and_lru(const KParams& p, const DevCa
       if (s_hit[j]) {
         slot = p.slot_of_expert[ej];
       } else {
-        long long bv = LLONG_MAX;
+        long long bc = LLONG_MAX, bv = LLONG_MAX;
         int bs = INT_MAX;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int s = lane + 32 * i;
-          if (!(used & (1u << i)) && (lu[i] < bv || (lu[i] == bv && s < bs))) {
+          const bool better = uc[i] < bc || (uc[i] == bc && (lu[i] < bv || (lu[i] == bv && s < bs)));
+          if (!(used & (1u << i)) && better) {
+            bc = uc[i];
             bv = lu[i];
             bs = s;
           }
         }
 #pragma unroll
         for (int m = 16; m; m >>= 1) {
+          const long long oc = shfl_xor_i64(bc, m);
           const long long ov = shfl_xor_i64(bv, m);
           const int os = __shfl_xor_sync(0xFFFFFFFFu, bs, m);
-          if (ov < bv || (ov == bv && os < bs)) {
+          if (oc < bc || (oc == bc && (ov < bv || (ov == bv && os < bs)))) {
+            bc = oc;
             bv = ov;
             bs = os;
           }
@@ -323,6 +331,8 @@ __device__ __forceinline__ void build_plan_and_lru(const KParams& p, const DevCa
         p.last_use[s] = lu[i];
       }
     }
+    if (lane == 0 && lfu)
+      for (int j = 0; j < k; ++j) p.use_count[__ldcg(&p.ids[j])] += 1;
     if (lane == 0) {
       rec[0] = n_miss;
       p.plan->n_miss = n_miss;

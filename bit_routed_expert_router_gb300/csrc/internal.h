@@ -85,6 +85,8 @@ struct KParams {
   int32_t* expert_of_slot;             // [N]
   long long* last_use;                 // [N]
   long long* lru_counts;               // [L][2] hits, misses
+  int policy;                          // 0 LRU, 1 LFU (host-pool mode)
+  long long* use_count;                // [E] whole-run picks per expert of this layer (LFU)
   int32_t* host_rec;                   // mapped host [L][1 + 2k + 4k] record of this layer
   // residual stream
   const uint16_t* h_src;               // layer input (null: read call args h_in)

@@ -37,6 +37,7 @@ struct LayerStore {
   int32_t* slot_of_expert = nullptr;  // [E]
   int32_t* expert_of_slot = nullptr;  // [N]
   long long* last_use = nullptr;      // [N]
+  long long* use_count = nullptr;     // [E] whole-run picks per expert (LFU)
 };
 
 template <class T>
@@ -84,6 +85,7 @@ struct moe_ctx {
   int32_t* row_cnt = nullptr;
   uint32_t* err_word = nullptr;
   long long* lru_counts = nullptr;
+  int policy = MOE_CACHE_LRU;         // slot cache eviction policy (host-pool contexts)
   DevCallArgs* dargs = nullptr;
   DevCallArgs* args_ring = nullptr;   // pinned host ring of argument blocks
   cudaEvent_t ring_ev[kArgRing] = {};
@@ -249,6 +251,8 @@ KParams base_params(moe_ctx* ctx, int layer, int rel, int first, int last, int B
   p.expert_of_slot = Ls.expert_of_slot;
   p.last_use = Ls.last_use;
   p.lru_counts = ctx->lru_counts;
+  p.policy = ctx->policy;
+  p.use_count = Ls.use_count;
   p.host_rec = ctx->host_rec_dev;
   p.args = ctx->dargs;
   p.x_perm = ctx->x_perm;
@@ -716,6 +720,7 @@ void moe_destroy(moe_ctx* ctx) {
     cudaFree(Ls.slot_of_expert);
     cudaFree(Ls.expert_of_slot);
     cudaFree(Ls.last_use);
+    cudaFree(Ls.use_count);
   }
   for (void* p : ctx->owned) cudaFree(p);
   for (void* p : ctx->pf_owned) cudaFree(p);
@@ -862,8 +867,18 @@ moe_status moe_set_slots(moe_ctx* ctx, int n_slots) {
     CK(cudaMalloc(&Ls.expert_of_slot, static_cast<size_t>(n_slots) * 4));
     CK(cudaMalloc(&Ls.last_use, static_cast<size_t>(n_slots) * 8));
     if (!Ls.slot_of_expert) CK(cudaMalloc(&Ls.slot_of_expert, static_cast<size_t>(c.n_experts) * 4));
+    if (!Ls.use_count) CK(cudaMalloc(&Ls.use_count, static_cast<size_t>(c.n_experts) * 8));
   }
   ctx->n_slots = n_slots;
+  return moe_reset_cache(ctx);
+}
+
+moe_status moe_set_cache_policy(moe_ctx* ctx, int policy) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  if (policy != MOE_CACHE_LRU && policy != MOE_CACHE_LFU) return fail(ctx, MOE_EINVAL, "unknown policy %d", policy);
+  if (ctx->residency != MOE_HOST_POOL) return fail(ctx, MOE_ESTATE, "cache policy needs a host-pool context");
+  ctx->policy = policy;
   return moe_reset_cache(ctx);
 }
 
@@ -877,6 +892,7 @@ moe_status moe_reset_cache(moe_ctx* ctx) {
     if (Ls.slot_of_expert) CK(cudaMemset(Ls.slot_of_expert, 0xFF, static_cast<size_t>(c.n_experts) * 4));
     if (Ls.expert_of_slot) CK(cudaMemset(Ls.expert_of_slot, 0xFF, static_cast<size_t>(ctx->n_slots) * 4));
     if (Ls.last_use) CK(cudaMemset(Ls.last_use, 0xFF, static_cast<size_t>(ctx->n_slots) * 8));
+    if (Ls.use_count) CK(cudaMemset(Ls.use_count, 0, static_cast<size_t>(c.n_experts) * 8));
   }
   CK(cudaMemset(ctx->lru_counts, 0, static_cast<size_t>(c.n_layers) * 16));
   ctx->step = 0;

@@ -56,6 +56,7 @@ typedef enum {
 } moe_status;
 
 enum { MOE_RESIDENT_HBM = 0, MOE_HOST_POOL = 1 };
+enum { MOE_CACHE_LRU = 0, MOE_CACHE_LFU = 1 };
 enum { MOE_GELU_ERF = 0, MOE_GELU_TANH = 1 };
 
 /* Model dimensions.  Constraints (checked by moe_create): d, f and f_shared
@@ -204,8 +205,20 @@ moe_status moe_get_stats(moe_ctx *ctx, moe_stats *out);
  * n_slots entries (expert_of_slot: -1 = empty; last_use: step counter, -1 = empty). */
 moe_status moe_get_cache_state(moe_ctx *ctx, int layer, int32_t *expert_of_slot, int64_t *last_use);
 
-/* Empty every LRU table, zero the counters and the step counter. */
+/* Empty every slot table and the LFU use counts, zero the counters and the step counter. */
 moe_status moe_reset_cache(moe_ctx *ctx);
+
+/* Host-pool contexts: the slot cache's eviction policy, then an empty cache
+ * (as moe_reset_cache).  MOE_CACHE_LRU (the default; goinfer, "When the model
+ * doesn't fit": plain LRU over the slots): a miss takes the slot least
+ * recently used.  MOE_CACHE_LFU (the TurboFieldfare video walkthrough: the
+ * expert used least often leaves): every pick adds one to its expert's
+ * whole-run count, and a miss takes the slot with the smallest (count of its
+ * expert, last use, slot index); an empty slot counts -1.  In both, hits are
+ * taken first and misses in top-k order among the slots this step has not
+ * touched.  MOE_EINVAL for an unknown policy, MOE_ESTATE for a resident
+ * context. */
+moe_status moe_set_cache_policy(moe_ctx *ctx, int policy);
 
 /* Bytes of one routed expert / of the shared expert for a config (0 on a bad config). */
 int64_t moe_expert_bytes(const moe_config *cfg);

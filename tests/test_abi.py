@@ -73,6 +73,7 @@ def test_bad_configs_are_rejected_before_cuda(lib, kw):
 def test_null_context_is_rejected(lib):
     assert lib.moe_set_slots(None, 4) == moe.MOE_EINVAL
     assert lib.moe_reset_cache(None) == moe.MOE_EINVAL
+    assert lib.moe_set_cache_policy(None, 1) == moe.MOE_EINVAL
     assert lib.moe_sync(None, None) == moe.MOE_EINVAL
     assert lib.moe_profile(None, 1) == moe.MOE_EINVAL
     assert lib.moe_test_hook(None, 1, 0) == moe.MOE_EINVAL

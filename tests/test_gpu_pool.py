@@ -237,3 +237,69 @@ def test_reset_cache_empties_slots():
         assert list(eos) == [-1] * 4 and list(lu) == [-1] * 4
         _, stats = moe.moe_get_stats(ctx.h)
         assert stats.hits == 0 and stats.misses == 0 and stats.steps == 0
+
+
+# ----------------------------------------------------------------- LFU eviction
+
+def test_hand_worked_lfu_traces():
+    with open(os.path.join(GOLDEN, "lfu_hand_traces.json")) as fh:
+        g = json.load(fh)
+    for ti, tr in enumerate(g["traces"]):
+        sh = Shape(d=128, f=64, f_shared=64, n_experts=tr["n_experts"], top_k=tr["top_k"])
+        w = gen_layer(sh, seed=150 + ti, layer=0)
+        with _pool_ctx(sh, 1, tr["n_slots"], [to_device(w)]) as ctx:
+            moe.check(moe.moe_set_cache_policy(ctx.h, moe.MOE_CACHE_LFU), ctx.h)
+            H = gen_hidden(len(tr["steps"]), sh.d, seed=150 + ti).cuda()
+            for t, st in enumerate(tr["steps"]):
+                bias = torch.zeros(1, 1, sh.n_experts, dtype=torch.float32)
+                for j, e in enumerate(st["ids"]):
+                    bias[0, 0, e] = 32.0 - 16.0 * j     # forces the picks and their order
+                _, rec = _decode_trace(ctx, H[t:t + 1], 1, bias.cuda())
+                assert [r[2] for r in rec] == st["ids"]
+                assert [r[3] for r in rec] == st["hit"], (ti, t)
+                assert [r[4] for r in rec] == st["slot"], (ti, t)
+                assert [r[5] for r in rec] == st["evicted"], (ti, t)
+            _, stats = moe.moe_get_stats(ctx.h)
+            assert stats.hits == tr["total_hits"] and stats.misses == tr["total_misses"]
+            _, eos, _ = moe.moe_get_cache_state(ctx.h, 0, tr["n_slots"])
+            assert list(eos) == tr["final_expert_of_slot"]
+
+
+def test_random_traces_match_oracle_lfu():
+    sh = Shape(d=256, f=128, f_shared=128, n_experts=16, top_k=4)
+    L, N, T = 2, 6, 60
+    ws = [gen_layer(sh, seed=160, layer=l) for l in range(L)]
+    tg = zipf_reuse_targets(T, L, sh.n_experts, sh.top_k, seed=160)
+    bias = torch.from_numpy(bias_from_targets(tg, sh.n_experts))          # [T, L, E]
+    with _pool_ctx(sh, L, N, [to_device(w) for w in ws]) as ctx:
+        moe.check(moe.moe_set_cache_policy(ctx.h, moe.MOE_CACHE_LFU), ctx.h)
+        H = gen_hidden(T, sh.d, seed=160).cuda()
+        lfus = [oracle.LFU(N, sh.n_experts) for _ in range(L)]
+        for t in range(T):
+            _, rec = _decode_trace(ctx, H[t:t + 1], L, bias[t].unsqueeze(1).contiguous().cuda())
+            for l in range(L):
+                rows = [r for r in rec if r[0] == l]
+                hit, slot, ev = lfus[l].step([r[2] for r in rows], t)
+                assert [r[3] for r in rows] == list(hit), f"t={t} l={l}"
+                assert [r[4] for r in rows] == list(slot), f"t={t} l={l}"
+                assert [r[5] for r in rows] == list(ev), f"t={t} l={l}"
+        ctx.sync()
+        for l in range(L):
+            _, eos, lu = moe.moe_get_cache_state(ctx.h, l, N)
+            assert list(eos) == list(lfus[l].expert_of_slot)
+            assert list(lu) == list(lfus[l].last_use)
+        # switching the policy empties the cache
+        moe.check(moe.moe_set_cache_policy(ctx.h, moe.MOE_CACHE_LRU), ctx.h)
+        _, eos, _ = moe.moe_get_cache_state(ctx.h, 0, N)
+        assert list(eos) == [-1] * N
+
+
+def test_cache_policy_argument_errors():
+    sh = Shape(d=128, f=64, f_shared=64, n_experts=8, top_k=2)
+    w = to_device(gen_layer(sh, seed=170, layer=0))
+    with _pool_ctx(sh, 1, 4, [w]) as ctx:
+        assert moe.moe_set_cache_policy(ctx.h, 7) == moe.MOE_EINVAL
+    res = Ctx(sh, n_layers=1)
+    with res:
+        res.init_layer(0, w)
+        assert moe.moe_set_cache_policy(res.h, moe.MOE_CACHE_LFU) == moe.MOE_ESTATE
