@@ -40,12 +40,12 @@ constexpr int kM = 128;                 // weight rows per CTA tile
 // a few rows (then the MMA is 4x shorter and a third k-step slot fits).
 template <int N>
 struct Tile {
-  static constexpr int kSlots = N == 128 ? 2 : 3;     // k-step slots (A + B tiles)
+  static constexpr int kSlots = 4;                     // k-step slots (A in tensor memory, B in shared)
   static constexpr int kBBytes = N * 128;              // one N-row x 64-col fp16 tile
+  static constexpr int kRawStages = N == 128 ? 2 : 4;  // int4 stages (more when the tokens are few)
+  static constexpr int kTmemCols = 256;                // accumulator (N) + four 32-column A slots
 };
 constexpr int kRawG = 4;                // int4 groups per raw stage
-constexpr int kRawStages = 2;
-constexpr int kTileBytes = 128 * 128;   // one 128-row x 64-col fp16 tile (16 KB)
 constexpr int kRawStride = kRawG * kGroupBytes;   // bytes of one 16-row tile in a raw stage
 constexpr int kRawBytes = 8 * kRawStride;         // 8 tiles of 16 rows = 128 rows
 constexpr int kDqWarps = 8;             // dequant + epilogue warps, one 16-row tile each per k step
@@ -54,8 +54,8 @@ constexpr int kThreads = 32 * (2 + kDqWarps);  // warp 0 producer, warp 1 MMA + 
 template <int N>
 struct GemmSmem {
   static constexpr int kSlots = Tile<N>::kSlots;
-  uint8_t a[kSlots][kTileBytes];        // fp16 weight tiles, K-major, 128-byte swizzle (1024-aligned)
-  uint8_t b[kSlots][Tile<N>::kBBytes];  // fp16 token tiles, same layout (TMA writes them)
+  static constexpr int kRawStages = Tile<N>::kRawStages;
+  uint8_t b[kSlots][Tile<N>::kBBytes];  // fp16 token tiles, K-major, 128-byte swizzle (1024-aligned, TMA)
   uint8_t raw[kRawStages][kRawBytes];   // int4 blocks as stored
   uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   uint64_t b_full[kSlots], a_full[kSlots], slot_empty[kSlots];
@@ -64,8 +64,8 @@ struct GemmSmem {
   int abort;
   int row_info[N];                      // epilogue: pair index (routed down) of each token row
 };
-static_assert(kTileBytes % 1024 == 0 && offsetof(GemmSmem<128>, b) % 1024 == 0 &&
-                  offsetof(GemmSmem<32>, b) % 1024 == 0 && Tile<32>::kBBytes % 1024 == 0,
+static_assert(offsetof(GemmSmem<128>, b) % 1024 == 0 && offsetof(GemmSmem<32>, b) % 1024 == 0 &&
+                  Tile<32>::kBBytes % 1024 == 0,
               "swizzled tiles need 1 KB alignment");
 static_assert(offsetof(GemmSmem<128>, raw) % 128 == 0 && offsetof(GemmSmem<32>, raw) % 128 == 0 &&
                   kRawStride % 16 == 0,
@@ -100,11 +100,12 @@ __host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
+// D (tensor memory) += A (tensor memory) x B (shared-memory descriptor).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, int acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -152,12 +153,25 @@ __device__ __forceinline__ bool wait_or_abort(Sm& S, uint64_t* bar, uint32_t par
 
 // ------------------------------------------------------------------ dequantisation
 
+// Column order of the 16-bit operands inside every 16-wide k block.  The
+// tensor-memory store shape .16x256b gives lane (g, t4) of a warp the 32-bit
+// columns 2 t4 and 2 t4 + 1 of rows g and g + 8; the stored int4 fragments give
+// the same lane the k pairs {2 t4, 2 t4 + 1} and {2 t4 + 8, 2 t4 + 9}.  So the A
+// operand in tensor memory holds k in the order pi(k) below, and every B operand
+// (activations, GELU products) is written in the same order; the products pair
+// up unchanged.
+__host__ __device__ __forceinline__ int k16_pos(int i) {
+  const int k = i & 15;
+  return (i & ~15) | (4 * ((k & 7) >> 1) + (k & 1) + 2 * (k >> 3));
+}
+
 // One 16-row tile x 64-column group of int4 weights (a block as stored: lane
-// fragments + per-row fp16 scale/bias) to fp16 w = s*q + b, written into rows
-// 16*blk .. 16*blk+15 of a swizzled 128-row tile.  Lane (g, t4) owns rows g and
-// g+8 at columns 16*st + 2*t4 (+1) and 16*st + 8 + 2*t4 (+1) of each k16 step.
-__device__ __forceinline__ void dequant_block(const uint8_t* blk, uint8_t* tile, int b16) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+// fragments + per-row fp16 scale/bias) to fp16 w = s*q + b, stored into
+// tensor-memory lanes lane0 .. lane0 + 15 and 32 columns from col (the A operand
+// of four k16 MMAs), with one .16x256b store.  The caller's warp must own
+// those lanes (warp % 4 == lane0 / 32).
+__device__ __forceinline__ void dequant_block_tmem(const uint8_t* blk, uint32_t taddr) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
   const uint4 q = *reinterpret_cast<const uint4*>(blk + lane * 16);
   const uint2 sb = *reinterpret_cast<const uint2*>(blk + kFragBytes + g * 8);
   const __half2 s0 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.x & 0xFFFFu)));
@@ -165,25 +179,29 @@ __device__ __forceinline__ void dequant_block(const uint8_t* blk, uint8_t* tile,
   const __half2 s1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.y & 0xFFFFu)));
   const __half2 c1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.y >> 16)));
   const __half2 k1024 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400u)));
-  const int r0 = 16 * b16 + g, r1 = r0 + 8;   // r0 & 7 == r1 & 7 == g
-  uint8_t* row0 = tile + r0 * 128;
-  uint8_t* row1 = tile + r1 * 128;
   const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+  uint32_t r[16];
 #pragma unroll
   for (int st = 0; st < 4; ++st) {
     const uint32_t w = words[st];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      // nibbles r (low half) and r + 4 (high half) as fp16 1024 + q, then exact q
-      const uint32_t bits = ((w >> (4 * r)) & 0x000F000Fu) | 0x64006400u;
+    for (int j = 0; j < 4; ++j) {
+      // nibbles j (low half) and j + 4 (high half) as fp16 1024 + q, then exact q, then s*q + b;
+      // j = 0: row g, k 2t4..; 1: row g+8, k 2t4..; 2: row g, k 2t4+8..; 3: row g+8, k 2t4+8..
+      const uint32_t bits = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
       const __half2 qh = __hsub2(*reinterpret_cast<const __half2*>(&bits), k1024);
-      const bool hi_row = (r & 1) != 0;
+      const bool hi_row = (j & 1) != 0;
       const __half2 v = __hfma2(qh, hi_row ? s1 : s0, hi_row ? c1 : c0);
-      const int chunk = 2 * st + (r >> 1);
-      uint8_t* dst = (hi_row ? row1 : row0) + (((chunk ^ g) & 7) << 4) + 4 * t4;
-      *reinterpret_cast<__half2*>(dst) = v;
+      // .16x256b registers of repetition st: (row g, col 2t4), (row g, col 2t4+1), (row g+8, ...)
+      const int slot = 4 * st + (hi_row ? 2 : 0) + (j >> 1);
+      r[slot] = *reinterpret_cast<const uint32_t*>(&v);
     }
   }
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
 }
 
 // ------------------------------------------------------------------ the GEMM
@@ -192,6 +210,8 @@ __device__ __forceinline__ void dequant_block(const uint8_t* blk, uint8_t* tile,
 template <int kN>
 __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__ CUtensorMap tmap_b, PfGemm p) {
   constexpr int kSlots = Tile<kN>::kSlots;
+  constexpr int kRawStages = Tile<kN>::kRawStages;
+  constexpr int kCols = Tile<kN>::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   GemmSmem<kN>& S = *reinterpret_cast<GemmSmem<kN>*>(smem_raw + pad);
@@ -222,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
     S.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {  // the whole warp allocates the 128 accumulator columns
+  if (warp == 1) {  // the whole warp allocates the accumulator and the A slots
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&S.tmem_base)),
-                 "r"(kN)
+                 "r"(kCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -284,19 +304,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
         if (G == 0) pf_stamp(p, 4);
         if (G == p.nG - 1) pf_stamp(p, 5);
         tc_fence_after();
-        const uint32_t a0 = smem_u32(S.a[slot]), b0 = smem_u32(S.b[slot]);
+        const uint32_t a0 = tmem + kN + 32 * slot, b0 = smem_u32(S.b[slot]);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // four k16 steps: +32 bytes inside the swizzled rows
-          tc_mma(tmem, sw128_desc(a0 + 32 * kk), sw128_desc(b0 + 32 * kk), idesc, (G | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk)  // four k16 steps: 8 columns of A, +32 bytes inside B's swizzled rows
+          tc_mma_ts(tmem, a0 + 8 * kk, sw128_desc(b0 + 32 * kk), idesc, (G | kk) != 0);
         tc_commit(&S.slot_empty[slot]);
       }
       tc_commit(&S.acc_full);  // fires once every MMA above has completed
     }
   } else {
-    // dequant warps: warp w takes 16-row tile w - 2 of each k step; in the epilogue it reads
-    // accumulator lanes 32q .. 32q + 31 (q = w % 4, the lanes its warp may access) and the
-    // column half (w - 2) / 4
-    const int dw = warp - 2, q = warp & 3;
+    // dequant warps: warp w takes 16-row tile 2q + (w - 2) / 4 of each k step (q = w % 4: the
+    // tensor-memory lanes 32q .. 32q + 31 its warp may access); in the epilogue it reads those
+    // accumulator lanes and the column half (w - 2) / 4
+    const int dw = warp - 2, q = warp & 3, b16 = 2 * q + (dw >> 2);
     // column range of this warp's epilogue: two halves of 128 columns, or all 32 for warps 2..5
     const int c_lo = kN == 128 ? (dw >> 2) * 64 : 0;
     const int c_hi = kN == 128 ? c_lo + 64 : ((dw >> 2) == 0 ? 32 : 0);
@@ -306,8 +326,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
       if (G == 0 && threadIdx.x == 64) pf_stamp(p, 2);
       const int slot = G % kSlots;
       if (!wait_or_abort(S, &S.slot_empty[slot], ((G / kSlots) & 1) ^ 1, p.err)) break;
-      dequant_block(S.raw[rs] + dw * kRawStride + gi * kGroupBytes, S.a[slot], dw);
-      fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+      dequant_block_tmem(S.raw[rs] + b16 * kRawStride + gi * kGroupBytes,
+                         tmem + (static_cast<uint32_t>(16 * b16) << 16) + kN + 32 * slot);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbarrier_arrive(&S.a_full[slot]);
       if ((gi == kRawG - 1 || G == nG - 1) && lane == 0) mbarrier_arrive(&S.raw_empty[rs]);
@@ -334,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
             if (gate_lane && c < nrows) {
               const float a = gelu_f(v[j], p.gelu) * up;
               if (!(fabsf(a) < 65504.f)) bad = true;
-              p.out16[static_cast<size_t>(row0 + c) * p.f_out + feat] = __half_as_ushort(__float2half_rn(a));
+              p.out16[static_cast<size_t>(row0 + c) * p.f_out + k16_pos(feat)] = __half_as_ushort(__float2half_rn(a));
             }
           }
           if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.err, ERR_PF_RANGE);
@@ -359,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
   if (threadIdx.x == 0) pf_stamp(p, 8);
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
   }
 }
 
@@ -399,7 +421,7 @@ __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int p
     x_bf[static_cast<size_t>(t) * d + i] = xb;
     const __half xh = __float2half_rn(xf);   // exact unless |x| < 2^-14 (then off by < 2^-25)
     if (!(fabsf(xf) < 65504.f)) bad = true;
-    x16[static_cast<size_t>(t) * d + i] = __half_as_ushort(xh);
+    x16[static_cast<size_t>(t) * d + k16_pos(i)] = __half_as_ushort(xh);   // operand order (k16_pos)
     if (dbg_x) dbg_x[static_cast<size_t>(t) * d + i] = xb;
   }
 #pragma unroll
