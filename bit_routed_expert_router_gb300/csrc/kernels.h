@@ -65,7 +65,8 @@ cudaError_t launch_persistent(PParams& p, int grid, cudaStream_t s);
 // Prefill (tcgen05 grouped GEMM over int4 weights).
 constexpr int kPfTileN = 128;          // token rows per GEMM tile (large groups)
 constexpr int kPfTileNSmall = 32;      // token rows per GEMM tile when every expert has only a few rows
-constexpr int kPfMinDecodeB = 20;     // resident decode steps of at least this many tokens take the tcgen05 path
+constexpr int kPfMinDecodeB = 16;     // resident decode steps of at least this many tokens take the tcgen05 path
+constexpr int kPfGraphMaxT = 512;     // tcgen05-path calls of at most this many tokens replay a CUDA graph
 enum : int { PF_GU = 0, PF_DN_ROUTED = 1, PF_DN_SHARED = 2 };
 
 struct PfGemm {

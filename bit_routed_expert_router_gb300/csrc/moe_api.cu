@@ -111,6 +111,11 @@ struct moe_ctx {
   long long wait_limit_us = 20000000;
   bool pdl = true;
   std::map<std::tuple<int, int, int>, cudaGraphExec_t> graphs;
+  // tcgen05-path graphs for small batches: key (T, l0, l1, with bias, with y_last)
+  std::map<std::tuple<int, int, int, int, int>, cudaGraphExec_t> pf_graphs;
+  uint16_t *pf_gin = nullptr, *pf_gout = nullptr;   // graph-owned copies of h in / h out [max_tokens][d]
+  float* pf_gbias = nullptr;                        // [n_layers][max_tokens][E], made on first use
+  float* pf_gy = nullptr;                           // [max_tokens][d]
   // persistent decode kernel (resident, B = 1)
   bool use_persistent = true;
   bool p_ok = false;                   // one CTA per SM fits
@@ -711,6 +716,7 @@ void moe_destroy(moe_ctx* ctx) {
   cudaSetDevice(ctx->device);
   cudaDeviceSynchronize();
   for (auto& kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : ctx->pf_graphs) cudaGraphExecDestroy(kv.second);
   for (auto& Ls : ctx->L) {
     cudaFree(Ls.router_w);
     cudaFree(Ls.router_stats);
@@ -929,7 +935,7 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
     return st;
   }
   if (B == 1 && ctx->use_persistent && ctx->p_ok) return persistent_run(ctx, layer_begin, layer_end, s);
-  // from about 20 tokens on, the grouped tcgen05 path beats the mma.sync GEMVs (measured crossover)
+  // from about 16 tokens on, the grouped tcgen05 path beats the mma.sync GEMVs (measured crossover)
   if (B >= kPfMinDecodeB && ctx->pf_ok && ctx->use_pf) return pf_run(ctx, h_in, B, layer_begin, layer_end, logit_bias,
                                                                   h_out, y_last, s);
   return resident_run(ctx, B, layer_begin, layer_end, s);
@@ -1088,18 +1094,74 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
 }
 
 // The tcgen05 path over [l0, l1) for T tokens.
-moe_status pf_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const float* logit_bias, void* h_out,
-                  float* y_last, cudaStream_t s) {
-  moe_status st = pf_alloc(ctx);
-  if (st != MOE_OK) return st;
+moe_status pf_enqueue(moe_ctx* ctx, const void* h, int T, int l0, int l1, const float* logit_bias, void* h_out,
+                      float* y_last, cudaStream_t s) {
   const int n_rel = l1 - l0;
   for (int rel = 0; rel < n_rel; ++rel) {
     const uint16_t* hin = rel == 0 ? static_cast<const uint16_t*>(h) : ctx->pf_h[(rel - 1) & 1];
     uint16_t* hout = rel == n_rel - 1 ? static_cast<uint16_t*>(h_out) : ctx->pf_h[rel & 1];
-    st = pf_layer(ctx, l0 + rel, rel, n_rel, hin, hout, T, logit_bias, y_last, s);
+    moe_status st = pf_layer(ctx, l0 + rel, rel, n_rel, hin, hout, T, logit_bias, y_last, s);
     if (st != MOE_OK) return st;
   }
-  return prof_collect(ctx, s);
+  return MOE_OK;
+}
+
+moe_status pf_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const float* logit_bias, void* h_out,
+                  float* y_last, cudaStream_t s) {
+  moe_status st = pf_alloc(ctx);
+  if (st != MOE_OK) return st;
+  const moe_config& c = ctx->cfg;
+  const bool dbg = ctx->dbg_x || ctx->dbg_ids || ctx->dbg_gates || ctx->dbg_y;
+  if (ctx->profiling || dbg || T > kPfGraphMaxT || ctx->pf_timeline) {
+    st = pf_enqueue(ctx, h, T, l0, l1, logit_bias, h_out, y_last, s);
+    if (st != MOE_OK) return st;
+    return prof_collect(ctx, s);
+  }
+  // small batches: one graph launch for all layers (the ~10 short kernels per layer would
+  // otherwise cost more in launch gaps than in work); the caller's buffers are copied in and out
+  const int n_rel = l1 - l0;
+  if (!ctx->pf_gin) {
+    size_t nb = 0;
+    ctx->pf_gin = dalloc<uint16_t>(static_cast<size_t>(c.max_tokens) * c.d, ctx->pf_owned, nb);
+    ctx->pf_gout = dalloc<uint16_t>(static_cast<size_t>(c.max_tokens) * c.d, ctx->pf_owned, nb);
+    ctx->pf_gy = dalloc<float>(static_cast<size_t>(c.max_tokens) * c.d, ctx->pf_owned, nb);
+    if (!ctx->pf_gin || !ctx->pf_gout || !ctx->pf_gy) return fail(ctx, MOE_ENOMEM, "graph staging buffers");
+    ctx->device_bytes += nb;
+  }
+  if (logit_bias && !ctx->pf_gbias) {
+    size_t nb = 0;
+    ctx->pf_gbias = dalloc<float>(static_cast<size_t>(c.n_layers) * c.max_tokens * c.n_experts, ctx->pf_owned, nb);
+    if (!ctx->pf_gbias) return fail(ctx, MOE_ENOMEM, "graph bias buffer");
+    ctx->device_bytes += nb;
+  }
+  const size_t hb = static_cast<size_t>(T) * c.d * 2;
+  CK(cudaMemcpyAsync(ctx->pf_gin, h, hb, cudaMemcpyDeviceToDevice, s));
+  if (logit_bias)
+    CK(cudaMemcpyAsync(ctx->pf_gbias, logit_bias, static_cast<size_t>(n_rel) * T * c.n_experts * 4,
+                       cudaMemcpyDeviceToDevice, s));
+  const auto key = std::make_tuple(T, l0, l1, logit_bias ? 1 : 0, y_last ? 1 : 0);
+  auto it = ctx->pf_graphs.find(key);
+  if (it == ctx->pf_graphs.end()) {
+    cudaGraph_t g = nullptr;
+    CK(cudaStreamBeginCapture(ctx->cap, cudaStreamCaptureModeThreadLocal));
+    st = pf_enqueue(ctx, ctx->pf_gin, T, l0, l1, logit_bias ? ctx->pf_gbias : nullptr, ctx->pf_gout,
+                    y_last ? ctx->pf_gy : nullptr, ctx->cap);
+    cudaError_t e = cudaStreamEndCapture(ctx->cap, &g);
+    if (st != MOE_OK) {
+      if (g) cudaGraphDestroy(g);
+      return st;
+    }
+    CK(e);
+    cudaGraphExec_t ex = nullptr;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    CK(e);
+    it = ctx->pf_graphs.emplace(key, ex).first;
+  }
+  CK(cudaGraphLaunch(it->second, s));
+  CK(cudaMemcpyAsync(h_out, ctx->pf_gout, hb, cudaMemcpyDeviceToDevice, s));
+  if (y_last) CK(cudaMemcpyAsync(y_last, ctx->pf_gy, static_cast<size_t>(T) * c.d * 4, cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
 }
 
 }  // namespace
@@ -1235,6 +1297,8 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
       if (want != ctx->pdl) {
         for (auto& kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
         ctx->graphs.clear();
+        for (auto& kv : ctx->pf_graphs) cudaGraphExecDestroy(kv.second);
+        ctx->pf_graphs.clear();
         ctx->pdl = want;
       }
       return MOE_OK;

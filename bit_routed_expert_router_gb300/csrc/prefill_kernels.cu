@@ -786,19 +786,32 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
     if (e == E - 1) *n_items = it + (n_e + tile - 1) / tile;
   }
   __syncthreads();
+  // 2048 pairs per pass, eight consecutive ones per thread, placed in pair order
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  for (int c0 = 0; c0 < P; c0 += 256) {
-    const int i = c0 + threadIdx.x;
-    const bool mine = i < P && ids[i] == e;
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, mine);
-    if (lane == 0) wsum[w] = __popc(bal);
+  for (int c0 = 0; c0 < P; c0 += 2048) {
+    const int i0 = c0 + 8 * threadIdx.x;
+    unsigned mask = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (i0 + u < P && ids[i0 + u] == e) mask |= 1u << u;
+    const int n = __popc(mask);
+    int incl = n;   // inclusive scan over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[w] = incl;
     __syncthreads();
-    int before = 0, total = 0;
+    int before = incl - n, total = 0;
     for (int w2 = 0; w2 < 8; ++w2) {
       if (w2 < w) before += wsum[w2];
       total += wsum[w2];
     }
-    if (mine) row_pair[s_off + s_base + before + __popc(bal & ((1u << lane) - 1u))] = i;
+    int pos = s_off + s_base + before;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (mask & (1u << u)) row_pair[pos++] = i0 + u;
     __syncthreads();
     if (threadIdx.x == 0) s_base += total;
     __syncthreads();

@@ -156,7 +156,7 @@ moe_status moe_set_slots(moe_ctx *ctx, int n_slots);
  *          receives (layer_end - layer_begin) * top_k records, or NULL
  *   stream: cudaStream_t to run on (NULL = legacy default stream)
  * Resident contexts accept 1 <= B <= min(max_tokens, 32) and return without
- * synchronising; from 20 tokens on (when the shape allows it) a step runs
+ * synchronising; from 16 tokens on (when the shape allows it) a step runs
  * through the same grouped tcgen05 path as moe_prefill, with the same exact
  * routing.  Host-pool contexts need B == 1 and slots set; every call is
  * one LRU step (the step counter increments per call) and the call returns
@@ -289,7 +289,7 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
  * it also gets per-CTA event times of the step's third layer; 0 stops it.
  * hook 4 or 7 with a non-zero value on a configuration where that kernel path
  * cannot run returns MOE_ESTATE.  hook 7: the tcgen05 path for prefill and for
- * decode steps of 20 or more tokens on (value != 0, the default when the
+ * decode steps of 16 or more tokens on (value != 0, the default when the
  * shape allows it) or off (batched decode kernels).
  * hook 8: `value` is a caller device buffer of 4 * 16 uint64 receiving event
  * times of CTA (0, 0) of each prefill GEMM of the first layer of a call, or

@@ -214,3 +214,33 @@ def test_prefill_router_exact_ties_and_zero_rows():
         bias = bias.cuda()
         h_out, y, xs, ids, gs, ys = _run_prefill(ctx, H, bias=bias)
         _check_tokens(lay, H, xs[0], ids[0], gs[0], ys[0], h_out, range(T), bias=bias[0])
+
+
+def test_small_batch_graph_replay_equals_direct_launches():
+    """Calls of at most 512 tokens without debug capture replay a CUDA graph with
+    the caller's buffers copied in and out; results equal the direct launches."""
+    L = 2
+    ctx, _ = _ctx(TINY, n_layers=L, prenorm=1, seed=23)
+    with ctx:
+        for T in (24, 100):
+            H = gen_hidden(T, TINY.d, seed=23 + T).cuda()
+            bias = torch.zeros(L, T, TINY.n_experts, dtype=torch.float32)
+            bias[:, :, 1] = 16.0
+            bias = bias.cuda()
+            outs = []
+            for rep in range(3):   # first call captures, later calls replay
+                h_out = torch.empty_like(H)
+                y = torch.empty(T, TINY.d, dtype=torch.float32, device="cuda")
+                moe.check(moe.moe_prefill(ctx.h, H, T, 0, L, bias, h_out, y), ctx.h)
+                ctx.sync()
+                outs.append((h_out.clone(), y.clone()))
+            ref = _run_prefill(ctx, H, n_layers=L, bias=bias)   # debug capture: direct launches
+            for h_out, y in outs:
+                assert torch.equal(h_out.view(torch.int16), ref[0].view(torch.int16))
+                assert torch.equal(y, ref[1])
+        # decode steps of 20+ tokens take the same path
+        H = gen_hidden(24, TINY.d, seed=29).cuda()
+        h1, y1, _ = ctx.decode(H, 0, L)
+        ctx.sync()
+        ref = _run_prefill(ctx, H, n_layers=L)
+        assert torch.equal(y1, ref[1])
