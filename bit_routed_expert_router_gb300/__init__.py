@@ -21,6 +21,7 @@ MOE_CACHE_LRU, MOE_CACHE_LFU = 0, 1
 MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
 HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6
 HOOK_PREFILL_TC = 7
+HOOK_CLUSTER = 9
 
 
 class MoeConfig(C.Structure):

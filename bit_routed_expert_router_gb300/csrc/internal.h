@@ -35,6 +35,7 @@ enum : uint32_t {
   ERR_WAIT_TIMEOUT = 1u << 1,    // a bounded wait ran out
   ERR_PLAN = 1u << 2,            // plan capacity exceeded (should be unreachable)
   ERR_PF_RANGE = 1u << 3,        // prefill: an fp16 matrix operand would overflow (|v| >= 65504)
+  ERR_Y_RANGE = 1u << 4,         // decode: a CTA's partial layer output beyond 2^24 (fixed-point sum range)
 };
 
 constexpr int kGroup = 64;

@@ -62,6 +62,45 @@ cudaError_t persistent_attrs();
 cudaError_t persistent_occupancy(int* blocks_per_sm);
 cudaError_t launch_persistent(PParams& p, int grid, cudaStream_t s);
 
+// Clustered persistent decode kernel (B = 1, resident, every layer in one
+// launch on clusters of kCCluster CTAs, one CTA per SM).
+constexpr int kCCluster = 4;           // CTAs per cluster
+constexpr int kCStages = 6;            // shared-memory ring slots (one gate/up tile or down slice each)
+constexpr int kCMaxUnits = 6;          // (source, group) units per cluster and layer
+constexpr int kCThreads = 32 * 18;     // producer warp, 16 consumer warps, top-k warp
+
+struct CLayer {                        // one layer, device memory (the tensor maps keep it 64-byte aligned)
+  CUtensorMap dn_shared;               // shared expert's down region as u32 [1][d/16][f_s/64 * 144], box 144 x d/64
+  CUtensorMap dn_routed;               // the experts' down regions as u32 [E][d/16][f/64 * 144], same box
+  const uint16_t* router_w;            // fp16 [E][d]
+  const uint8_t* shared;               // shared expert, device layout (gate/up region first)
+  const uint8_t* experts;              // expert 0, device layout
+};
+
+struct CParams {
+  int d, f, fs, E, k, prenorm, gelu;
+  float eps;
+  int l0, l1;                          // layers of this call
+  long long expert_stride;
+  const CLayer* layers;                // [n_layers]
+  const DevCallArgs* args;
+  unsigned long long* tlog;            // [n_layers][E][2]: logit low / high word, each | tag << 32
+  unsigned tag;                        // this launch's tag (never 0)
+  long long* ybuf;                     // [3][d] layer outputs on the 2^-32 grid; zero between launches
+  unsigned* y_cnt;                     // [n_counters] CTAs done with the call's layer rel
+  int n_counters;
+  unsigned* exit_cnt;
+  unsigned* abort_flag;
+  uint32_t* err;
+  unsigned long long* timeline;        // optional [grid][16] event times (ns) of one layer, null = off
+};
+
+size_t cluster_smem();
+int cluster_max_units();
+cudaError_t cluster_attrs();
+cudaError_t cluster_max_active(int* n_clusters);
+cudaError_t launch_cluster(CParams& p, int grid, cudaStream_t s);
+
 // Prefill (tcgen05 grouped GEMM over int4 weights).
 constexpr int kPfTileN = 128;          // token rows per GEMM tile (large groups)
 constexpr int kPfTileNSmall = 32;      // token rows per GEMM tile when every expert has only a few rows

@@ -128,6 +128,15 @@ struct moe_ctx {
   float *p_asum_s = nullptr, *p_asum_r = nullptr, *p_part = nullptr;
   int p_n_sc = 1;
   float* p_gates = nullptr;            // [n_layers][k]
+  // clustered persistent decode kernel (resident, B = 1; preferred when available)
+  bool c_ok = false;                   // shapes and device allow it
+  bool use_cluster = true;             // test hook 9
+  int c_grid = 0;                      // CTAs: resident clusters x kCCluster
+  CLayer* c_layers = nullptr;          // device [n_layers]
+  unsigned long long* c_tlog = nullptr;  // [n_layers][E][2] tagged logits
+  long long* c_ybuf = nullptr;         // [3][d] fixed-point layer outputs
+  unsigned* c_counters = nullptr;      // [n_layers] layer counters, exit counter, abort flag
+  unsigned c_tag = 0;                  // tag of the last launch
   // batched prefill on tcgen05 (resident contexts): scratch for max_tokens tokens, made on first use
   bool pf_ok = false;                  // shapes and device allow it
   bool use_pf = true;                  // test hook 7
@@ -395,6 +404,76 @@ moe_status check_ready(moe_ctx* ctx, int l0, int l1) {
   return MOE_OK;
 }
 
+// cuTensorMapEncodeTiled, looked up through the runtime so that the library
+// does not link libcuda itself (it loads on machines without a driver).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q{};
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return encode;
+}
+
+// 3-D tensor map over the down regions of n_mat matrices seen as 32-bit words:
+// x = the nG * 144 words of one 16-row tile (nG groups of 576 bytes), y = the
+// nT tiles, z = the matrices (mat_stride bytes apart).  A box is one group of
+// nT / 4 consecutive tiles: the down slice of one cluster rank for one unit.
+bool encode_down(CUtensorMap* m, const void* base, int nG, int nT, int n_mat, long long mat_stride) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t row = static_cast<cuuint64_t>(nG) * kGroupBytes;
+  cuuint64_t gdim[3] = {static_cast<cuuint64_t>(nG) * (kGroupBytes / 4), static_cast<cuuint64_t>(nT),
+                        static_cast<cuuint64_t>(n_mat)};
+  cuuint64_t gstride[2] = {row, n_mat > 1 ? static_cast<cuuint64_t>(mat_stride) : row * nT};
+  cuuint32_t box[3] = {kGroupBytes / 4, static_cast<cuuint32_t>(nT / kCCluster), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), gdim, gstride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Resident decode of one token through [l0, l1) with the clustered kernel.
+moe_status cluster_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
+  CParams p{};
+  p.d = c.d;
+  p.f = c.f;
+  p.fs = c.f_shared;
+  p.E = c.n_experts;
+  p.k = c.top_k;
+  p.prenorm = c.prenorm;
+  p.gelu = c.gelu_variant;
+  p.eps = c.norm_eps;
+  p.l0 = l0;
+  p.l1 = l1;
+  p.expert_stride = ctx->stride;
+  p.layers = ctx->c_layers;
+  p.args = ctx->dargs;
+  if (++ctx->c_tag == 0) {   // tags wrapped: no stale entry may carry the new one
+    CK(cudaMemsetAsync(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * c.n_experts * 16, s));
+    ctx->c_tag = 1;
+  }
+  p.tlog = ctx->c_tlog;
+  p.tag = ctx->c_tag;
+  p.ybuf = ctx->c_ybuf;
+  p.y_cnt = ctx->c_counters;
+  p.n_counters = c.n_layers;
+  p.exit_cnt = ctx->c_counters + c.n_layers;
+  p.abort_flag = p.exit_cnt + 1;
+  p.err = ctx->err_word;
+  p.timeline = ctx->p_timeline;
+  PROF(3, s);
+  CK(launch_cluster(p, ctx->c_grid, s));
+  PROF(-1, s);
+  return prof_collect(ctx, s);
+}
+
 // Resident decode of one token through [l0, l1) with the persistent kernel.
 moe_status persistent_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   const moe_config& c = ctx->cfg;
@@ -649,6 +728,10 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->p_asum_r = dalloc<float>(static_cast<size_t>(c.top_k) * (c.f / 8) * 2, o, nb);
   ctx->p_part = dalloc<float>(static_cast<size_t>(2) * pparts * c.d, o, nb);
   ctx->p_gates = dalloc<float>(static_cast<size_t>(c.n_layers) * c.top_k, o, nb);
+  ctx->c_layers = dalloc<CLayer>(c.n_layers, o, nb);
+  ctx->c_tlog = dalloc<unsigned long long>(static_cast<size_t>(c.n_layers) * c.n_experts * 2, o, nb);
+  ctx->c_ybuf = dalloc<long long>(static_cast<size_t>(3) * c.d, o, nb);
+  ctx->c_counters = dalloc<unsigned>(static_cast<size_t>(c.n_layers) + 2, o, nb);
   for (void* ptr : o)
     if (!ptr) return bail(MOE_ENOMEM);
   if (!ctx->hbuf[0] || !ctx->hbuf[1] || !ctx->x_perm || !ctx->dargs || !ctx->y_r || !ctx->part_s || !ctx->a_r)
@@ -660,7 +743,11 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       cudaMemset(ctx->lru_counts, 0, static_cast<size_t>(c.n_layers) * 16) != cudaSuccess ||
       cudaMemset(ctx->p_counters, 0, static_cast<size_t>(ctx->p_n_counters) * 4) != cudaSuccess ||
       cudaMemset(ctx->p_exit, 0, 8) != cudaSuccess ||
-      cudaMemset(ctx->p_layers, 0, sizeof(PLayer) * c.n_layers) != cudaSuccess)
+      cudaMemset(ctx->p_layers, 0, sizeof(PLayer) * c.n_layers) != cudaSuccess ||
+      cudaMemset(ctx->c_layers, 0, sizeof(CLayer) * c.n_layers) != cudaSuccess ||
+      cudaMemset(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * c.n_experts * 16) != cudaSuccess ||
+      cudaMemset(ctx->c_ybuf, 0, static_cast<size_t>(3) * c.d * 8) != cudaSuccess ||
+      cudaMemset(ctx->c_counters, 0, (static_cast<size_t>(c.n_layers) + 2) * 4) != cudaSuccess)
     return bail(MOE_ECUDA);
   if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->args_ring), sizeof(DevCallArgs) * kArgRing, cudaHostAllocDefault) !=
       cudaSuccess)
@@ -696,6 +783,20 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     int per_sm = 0;
     if (persistent_attrs() == cudaSuccess && persistent_occupancy(&per_sm) == cudaSuccess && per_sm >= 1)
       ctx->p_ok = true;
+    cudaGetLastError();
+  }
+  // the clustered decode kernel: one router row per CTA, at most kCMaxUnits
+  // (source, group) units per cluster and layer, its shared memory, and a
+  // cooperative launch of every resident cluster
+  {
+    int n_cl = 0;
+    const int units = c.f_shared / 64 + c.top_k * (c.f / 64);
+    if (c.top_k <= 32 && cluster_smem() + 2048 <= static_cast<size_t>(max_smem) && cluster_attrs() == cudaSuccess &&
+        cluster_max_active(&n_cl) == cudaSuccess && n_cl >= 1 && c.n_experts <= n_cl * kCCluster &&
+        (units + n_cl - 1) / n_cl <= cluster_max_units()) {
+      ctx->c_ok = true;
+      ctx->c_grid = n_cl * kCCluster;
+    }
     cudaGetLastError();
   }
   // the tcgen05 prefill: 128-row weight tiles of the down projection, one router
@@ -836,6 +937,18 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
   if (pool && ctx->n_slots > 0 && Ls.slot_of_expert) CK(cudaMemset(Ls.slot_of_expert, 0xFF, c.n_experts * 4));
   PLayer pl{Ls.router_w, Ls.shared, Ls.experts};
   CK(cudaMemcpy(ctx->p_layers + layer, &pl, sizeof(PLayer), cudaMemcpyHostToDevice));
+  if (ctx->c_ok && !pool) {
+    CLayer cl{};
+    const size_t gu_s = static_cast<size_t>(c.f_shared / 8) * (c.d / 64) * kGroupBytes;
+    const size_t gu_r = static_cast<size_t>(c.f / 8) * (c.d / 64) * kGroupBytes;
+    if (!encode_down(&cl.dn_shared, Ls.shared + gu_s, c.f_shared / 64, c.d / 16, 1, 0) ||
+        !encode_down(&cl.dn_routed, Ls.experts + gu_r, c.f / 64, c.d / 16, c.n_experts, ctx->stride))
+      return fail(ctx, MOE_ECUDA, "init_layer %d: cuTensorMapEncodeTiled failed for the down regions", layer);
+    cl.router_w = Ls.router_w;
+    cl.shared = Ls.shared;
+    cl.experts = Ls.experts;
+    CK(cudaMemcpy(ctx->c_layers + layer, &cl, sizeof(CLayer), cudaMemcpyHostToDevice));
+  }
   Ls.ready = true;
   return MOE_OK;
 }
@@ -934,7 +1047,10 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
     ++ctx->steps;
     return st;
   }
-  if (B == 1 && ctx->use_persistent && ctx->p_ok) return persistent_run(ctx, layer_begin, layer_end, s);
+  if (B == 1 && ctx->use_persistent) {
+    if (ctx->c_ok && ctx->use_cluster) return cluster_run(ctx, layer_begin, layer_end, s);
+    if (ctx->p_ok) return persistent_run(ctx, layer_begin, layer_end, s);
+  }
   // from about 16 tokens on, the grouped tcgen05 path beats the mma.sync GEMVs (measured crossover)
   if (B >= kPfMinDecodeB && ctx->pf_ok && ctx->use_pf) return pf_run(ctx, h_in, B, layer_begin, layer_end, logit_bias,
                                                                   h_out, y_last, s);
@@ -945,19 +1061,9 @@ namespace {
 
 // 2-D tensor map over a row-major fp16 matrix [rows][K]: boxes of 64 columns x
 // box_rows rows with the 128-byte swizzle the GEMM's operand tiles use.
-// The driver entry point is looked up through the runtime, so the library does
-// not link libcuda itself (it loads on machines without a driver).
 bool encode_rows(CUtensorMap* m, void* base, int K, long long rows, int box_rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
-    cudaDriverEntryPointQueryResult q{};
-    void* fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return false;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
   cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
@@ -1218,6 +1324,7 @@ moe_status moe_sync(moe_ctx* ctx, void* stream) {
   if (w & ERR_PLAN) return fail(ctx, MOE_ECUDA, "device plan overflow (error word 0x%x)", w);
   if (w & ERR_ROUTER_DOMAIN) return fail(ctx, MOE_EDOMAIN, "router input outside the exact fixed-point domain");
   if (w & ERR_PF_RANGE) return fail(ctx, MOE_EDOMAIN, "prefill: an fp16 matrix operand is outside [-65504, 65504]");
+  if (w & ERR_Y_RANGE) return fail(ctx, MOE_EDOMAIN, "decode: a partial FFN output is outside (-2^24, 2^24)");
   return MOE_OK;
 }
 
@@ -1311,8 +1418,13 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
         return fail(ctx, MOE_ESTATE, "tcgen05 prefill unavailable for this configuration or device");
       ctx->use_pf = value != 0;
       return MOE_OK;
+    case 9:  // clustered (1) or per-SM (0) persistent decode kernel; asking for one that cannot run is an error
+      if ((value != 0 && !ctx->c_ok) || (value == 0 && !ctx->p_ok))
+        return fail(ctx, MOE_ESTATE, "that persistent decode kernel is unavailable for this configuration or device");
+      ctx->use_cluster = value != 0;
+      return MOE_OK;
     case 4:  // persistent B = 1 decode kernel on/off; asking for it where it cannot run is an error
-      if (value != 0 && !ctx->p_ok)
+      if (value != 0 && !ctx->p_ok && !ctx->c_ok)
         return fail(ctx, MOE_ESTATE, "persistent decode kernel unavailable for this configuration or device");
       ctx->use_persistent = value != 0;
       return MOE_OK;

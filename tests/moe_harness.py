@@ -75,6 +75,19 @@ class Ctx:
         self.close()
 
 
+# B = 1 decode kernels a test can pin: the clustered persistent kernel, the
+# per-SM persistent kernel, or the per-layer kernels.
+DECODE_KERNELS = ("cluster", "per_sm", "layers")
+
+
+def use_decode_kernel(ctx: "Ctx", which: str) -> None:
+    if which == "layers":
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PERSISTENT, 0), ctx.h)
+        return
+    moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PERSISTENT, 1), ctx.h)
+    moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_CLUSTER, 1 if which == "cluster" else 0), ctx.h)
+
+
 def assert_ffn_close(y_gpu, y_ref, what=""):
     y_gpu = np.asarray(y_gpu, dtype=np.float64)
     y_ref = np.asarray(y_ref, dtype=np.float64)

@@ -9,7 +9,7 @@ import bit_routed_expert_router_gb300 as moe
 import oracle
 from workload import FULL, TINY, Shape, gen_hidden, gen_layer
 
-from moe_harness import GATE_RTOL, Ctx, assert_ffn_close, bf16_to_f64, to_device
+from moe_harness import DECODE_KERNELS, GATE_RTOL, Ctx, assert_ffn_close, bf16_to_f64, to_device, use_decode_kernel
 
 pytestmark = pytest.mark.gpu
 
@@ -53,11 +53,11 @@ def _tiny_ctx(shape=TINY, prenorm=0, seed=0, gelu=0):
     return ctx, oracle.Layer(w, shape.top_k, gelu_variant=gelu)
 
 
-@pytest.mark.parametrize("persistent", [1, 0])
-def test_tiny_layer_single_tokens(persistent):
+@pytest.mark.parametrize("kernel", DECODE_KERNELS)
+def test_tiny_layer_single_tokens(kernel):
     ctx, lay = _tiny_ctx()
     with ctx:
-        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PERSISTENT, persistent), ctx.h)
+        use_decode_kernel(ctx, kernel)
         H = gen_hidden(16, TINY.d, seed=0).cuda()
         for t in range(16):
             _check_layer_outputs(ctx, lay, H[t:t + 1])
