@@ -21,11 +21,14 @@
 // row per CTA, published with a per-launch tag inside each 64-bit word, so a
 // reader polls the data itself) and the layer output: each CTA sums its units'
 // down partials (gate-weighted, fixed order) for its d/4 rows, rounds them onto
-// a 2^-32 fixed-point grid and adds them into the layer's int64 output vector
-// with one bulk reduction (TMA engine, integer adds in L2, so the result does
-// not depend on the order in which CTAs arrive), then bumps the layer's
-// counter.  Every CTA then reads the vector, adds it to its own copy of the
-// residual stream and normalises it for the next layer.
+// a 2^-32 fixed-point grid and adds (v << 8) + 1 per row into the layer's int64
+// output vector with one bulk reduction (TMA engine, integer adds in L2, so the
+// result does not depend on the order in which CTAs arrive).  The low byte of
+// a row counts its contributions, so a reader polls the rows themselves: each
+// CTA waits for its rank's quarter of the vector, adds it to the residual
+// stream and writes the result into the shared memory of all four CTAs of its
+// cluster, which then all hold the whole residual and normalise it for the
+// next layer.
 //
 // Roles per CTA (18 warps):
 //   warp 0, lane 0 (producer): the router row, then every stage of the CTA's
@@ -34,13 +37,16 @@
 //     six shared-memory slots; routing-independent units (shared expert) come
 //     first, routed units after the top-k is known.
 //   warps 1..16 (consumers): four quads of four warps; stage u of the CTA goes
-//     to quad u mod 4 (gate/up: 11-group chunks per warp, the last warp of the
-//     quad runs the epilogue and the push; down: row tiles split by warp).
+//     to quad u mod 4 (gate/up: a quarter of the groups per warp, the last
+//     warp of the quad to finish sums the partials in warp order and runs the
+//     epilogue and the push; down: row tiles strided by warp).  A unit's down
+//     stage is queued after the next unit's gate/up stages, so its 64 values
+//     of a have normally arrived from the other CTAs of the cluster by then.
 //   warp 17 (top-k): polls the layer's tagged logits, takes the top-k and the
 //     softmax gates and releases the producer.
 // Every wait is bounded and gives up through an abort flag and the device
-// error word (MOE_ETIMEOUT from moe_sync); the last CTA to leave zeroes the
-// counters for the next launch.
+// error word (MOE_ETIMEOUT from moe_sync).  Output vectors rotate over three
+// buffers, each zeroed (in shares, by every CTA) once everyone has read it.
 #include "common.cuh"
 #include "internal.h"
 #include "kernels.h"
@@ -53,7 +59,7 @@ namespace {
 
 constexpr int kCl = kCCluster;                    // CTAs per cluster
 constexpr int kNC = 16;                           // consumer warps
-constexpr int kQW = 4;                            // warps per quad (one stage each)
+constexpr int kQW = 4;                            // warps per quad (one work item each)
 constexpr int kNQ = kNC / kQW;                    // quads
 constexpr int kNS = kCStages;                     // ring slots
 constexpr int kMaxG = kPMaxD / 64;                // int4 groups along d
@@ -62,6 +68,7 @@ constexpr int kMaxU = kCMaxUnits;                 // units per cluster and layer
 constexpr int kMaxRows = kPMaxD / kCl;            // down output rows per CTA
 constexpr int kMaxTasks = 3 * kMaxU + 1;
 constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr unsigned kPollSleepNs = 200;             // back-off between polls of data every CTA reads
 
 static_assert(kCThreads == 32 * (kNC + 2), "producer warp, 16 consumer warps, top-k warp");
 static_assert(kCl == 4, "the a push maps 32 lanes onto 4 ranks x 8 fragment words; 8 tiles = 4 ranks x 2");
@@ -80,15 +87,15 @@ struct CTask {
 struct Smem {
   alignas(128) uint8_t ring[kNS][kSlotBytes];     // bulk / TMA targets
   alignas(16) uint16_t rrow[kPMaxD];               // this CTA's router row (fp16)
-  alignas(16) uint16_t h[kPMaxD];                  // residual stream (bf16), the same in every CTA
+  alignas(16) uint16_t h[2][kPMaxD];               // residual stream (bf16) by layer parity, the same in every CTA
   alignas(16) uint16_t xs[kPMaxD];                 // FFN input x (bf16)
-  alignas(16) uint16_t xp[kPMaxD];                 // x as mma B fragments
-  alignas(16) float xg[kMaxG];                     // per-group sums of x
+  alignas(16) uint16_t xp[kPMaxD];                 // x as fp16 mma B fragments
+  alignas(16) float xg[kMaxG];                     // per-group sums of the fp16 x
   alignas(16) uint32_t abuf[2 * kMaxU][64];        // per unit: a as down B fragments (hi/lo), pushed by the cluster
   alignas(16) float tsum[2 * kMaxU][8];            // per unit: sum of a (hi + lo) of each of the 8 gate/up tiles
   alignas(16) float dn_part[kMaxU][kMaxRows];      // per unit: down partials of this CTA's rows
   alignas(16) long long yq[kMaxRows];              // fixed-point layer output rows, bulk-reduce source
-  alignas(16) float gu_part[kNS][kQW][8][2];       // gate/up chunk partials [slot][warp][row][gate/up]
+  alignas(16) float gu_part[kNS][kQW][8][2];       // gate/up partials [slot][warp of the quad][row][gate/up]
   alignas(8) uint64_t full[kNS];
   alignas(8) uint64_t empty[kNS];
   alignas(8) uint64_t a_full[2 * kMaxU];           // 8 remote arrivals per use (4 ranks x 2 tiles)
@@ -96,13 +103,15 @@ struct Smem {
   alignas(8) uint64_t rrow_empty;
   alignas(8) uint64_t topk_bar;                    // one phase per layer
   alignas(8) uint64_t cbar;                        // consumer-warp barrier
+  alignas(8) uint64_t clbar;                       // consumer warps of the whole cluster (remote arrivals)
   alignas(16) DevCallArgs args;
   CTask tasks[kMaxTasks];
   int n_tasks, n_units, n_stages;
   int unit_src[kMaxU];
+  int unit_G[kMaxU];
   int gu_cnt[kNS];
-  int finisher;
   float red[kNC];
+  float ssq[2][kCl][kNC];                          // by layer parity, per rank and warp: sums of squares
   long long rlog[kNC];
   int32_t ids[2][32];
   float gates[2][32];
@@ -122,6 +131,11 @@ __device__ __forceinline__ unsigned cluster_rank() {
 __device__ __forceinline__ unsigned cluster_idx() {
   unsigned r;
   asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ unsigned cluster_size() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 __device__ __forceinline__ unsigned cluster_count() {
@@ -180,15 +194,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// dst[i] += src[i] (int64, in L2) for bytes / 8 elements; waits until done.
-__device__ __forceinline__ void bulk_reduce_add_s64(long long* dst, const long long* src, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u64 [%0], [%1], %2;" ::"l"(dst),
-               "r"(smem_u32(src)), "r"(bytes)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 __device__ __forceinline__ ulonglong2 ld_volatile_u64x2(const unsigned long long* p) {
   ulonglong2 v;
   asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
@@ -198,18 +203,6 @@ __device__ __forceinline__ void st_volatile_u64x2(unsigned long long* p, unsigne
   asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
 __device__ __forceinline__ bool aborted(const CParams& p) {
   return *reinterpret_cast<volatile unsigned*>(p.abort_flag) != 0;
 }
@@ -217,25 +210,6 @@ __device__ __forceinline__ bool aborted(const CParams& p) {
 __device__ __forceinline__ void raise_abort(const CParams& p) {
   atomicOr(p.err, ERR_WAIT_TIMEOUT);
   atomicExch(p.abort_flag, 1u);
-}
-
-// The whole warp waits until *ctr >= target (acquire); warp-uniform polling
-// (a loop run by one lane while the others wait leaves the warp diverged and
-// slows every later warp-wide instruction).  False on abort or timeout.
-__device__ bool warp_wait_counter(const CParams& p, const unsigned* ctr, unsigned target) {
-  if (__all_sync(kFull, ld_acquire(ctr) >= target)) return true;
-  const long long t0 = clock64();
-  for (unsigned it = 1;; ++it) {
-    __nanosleep(32);
-    if (__all_sync(kFull, ld_acquire(ctr) >= target)) return true;
-    if ((it & 255) == 0) {
-      if (__any_sync(kFull, aborted(p))) return false;
-      if (__any_sync(kFull, clock64() - t0 > kSpinLimitCycles)) {
-        if ((threadIdx.x & 31) == 0) raise_abort(p);
-        return false;
-      }
-    }
-  }
 }
 
 // Consumer-warp barrier: one arrival per consumer warp; round r (from 1)
@@ -249,6 +223,50 @@ __device__ bool consumer_barrier(const CParams& p, Smem& S, int round) {
   return ok;
 }
 
+// Barrier of the consumer warps of every CTA of the cluster: each warp makes
+// its earlier shared-memory writes (local and remote) visible cluster-wide,
+// then arrives on every CTA's clbar; phase n of a launch has parity n & 1.
+__device__ bool cluster_consumer_barrier(const CParams& p, Smem& S, uint32_t parity) {
+  const int lane = threadIdx.x & 31;
+  fence_acq_rel_cluster();
+  __syncwarp();
+  if (lane < kCl) arrive_peer(peer_addr(&S.clbar, static_cast<unsigned>(lane)));
+  const bool ok = mbar_wait_cluster(&S.clbar, parity, p.err);
+  if (!ok) raise_abort(p);
+  __syncwarp();
+  return ok;
+}
+
+// Layer outputs carry their completeness: every CTA adds (v << 8) + 1 into
+// each of its rows (v = the row's partial on the 2^-32 grid), so a row is final
+// once its low byte equals the number of clusters (one CTA of each cluster
+// adds into every row).  The warp polls the two rows each lane holds (bounded)
+// and returns their values.  False on abort or timeout.
+// Lanes with valid == false take part in the warp-wide votes only.
+__device__ bool poll_rows(const CParams& p, const long long* rows2, bool valid, float& y0, float& y1) {
+  const unsigned n_cl = gridDim.x / kCl;
+  const unsigned long long* src = reinterpret_cast<const unsigned long long*>(rows2);
+  const long long t0 = clock64();
+  y0 = y1 = 0.f;
+  for (unsigned it = 0;; ++it) {
+    const ulonglong2 v = valid ? ld_volatile_u64x2(src) : make_ulonglong2(n_cl, n_cl);
+    const bool ok = (v.x & 0xFFull) == n_cl && (v.y & 0xFFull) == n_cl;
+    if (__all_sync(kFull, ok)) {
+      y0 = __ll2float_rn(static_cast<long long>(v.x) >> 8) * 2.3283064365386963e-10f;   // 2^-32
+      y1 = __ll2float_rn(static_cast<long long>(v.y) >> 8) * 2.3283064365386963e-10f;
+      return true;
+    }
+    __nanosleep(64);
+    if ((it & 255) == 255) {
+      if (__any_sync(kFull, aborted(p))) return false;
+      if (__any_sync(kFull, clock64() - t0 > kSpinLimitCycles)) {
+        if ((threadIdx.x & 31) == 0) raise_abort(p);
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float gelu_p(float v, int variant) {
   if (variant == 1) return 0.5f * v * (1.f + tanhf(0.7978845608028654f * (v + 0.044715f * v * v * v)));
   return 0.5f * v * (1.f + erff(v * 0.7071067811865476f));
@@ -257,11 +275,13 @@ __device__ __forceinline__ float gelu_p(float v, int variant) {
 // ------------------------------------------------------------------ timeline (optional)
 
 // Event times (%globaltimer, ns) of the call's third layer (the last one if
-// fewer), row blockIdx.x of the caller's buffer: first occurrence, or latest
-// for the *_LAST events.
+// fewer), row blockIdx.x (32 columns) of the caller's buffer: first
+// occurrence, or latest for the *_LAST events.
 enum : int { EV_Y_SEEN, EV_X_READY, EV_LOGIT_OUT, EV_LOGITS_IN, EV_TOPK_DONE, EV_ROUTED_ISSUE, EV_SHARED_DATA,
              EV_ROUTED_DATA, EV_PUSH_LAST, EV_DN_LAST, EV_STAGES_DONE, EV_REDUCED, EV_ISSUE_LAST, EV_DATA_LAST,
-             EV_DN_A_FIRST, EV_A_WAIT_LAST };
+             EV_DN_A_FIRST, EV_A_WAIT_LAST, EV_PREP_B1, EV_PREP_Y, EV_PREP_B2, EV_ROUTER_B, EV_TOPK_SORTED,
+             EV_BULK_ISSUED };
+constexpr int kTlCols = 32;            // timeline row: events 0..23, accumulators 24..31
 
 __device__ __forceinline__ void stamp(const CParams& p, int rel, int ev, bool latest = false) {
   if (!p.timeline) return;
@@ -269,9 +289,25 @@ __device__ __forceinline__ void stamp(const CParams& p, int rel, int ev, bool la
   if (rel != (n_rel > 2 ? 2 : n_rel - 1)) return;
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  unsigned long long* q = p.timeline + static_cast<size_t>(blockIdx.x) * 16 + ev;
+  unsigned long long* q = p.timeline + static_cast<size_t>(blockIdx.x) * kTlCols + ev;
   if (latest) atomicMax(q, t);
   else atomicCAS(q, 0ull, t);
+}
+
+// Accumulated times of the stamped layer at columns 24.. of row blockIdx.x:
+// [0] gate/up compute, [1] down compute, [2] down wait for a, [3] data wait
+// (routed stages), [4] gate/up stages, [5] down stages, [6] data wait
+// (shared stages), all in ns summed over the CTA's consumer warps.
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void acc(const CParams& p, int rel, int slot, unsigned long long v) {
+  if (!p.timeline) return;
+  const int n_rel = p.l1 - p.l0;
+  if (rel != (n_rel > 2 ? 2 : n_rel - 1)) return;
+  atomicAdd(p.timeline + static_cast<size_t>(blockIdx.x) * kTlCols + 24 + slot, v);
 }
 
 // ------------------------------------------------------------------ units and stages
@@ -281,35 +317,44 @@ __device__ __forceinline__ void stamp(const CParams& p, int rel, int ev, bool la
 // (position j, group G -> j * f/64 + G), then shared (k * f/64 + G), and dealt
 // round-robin over the clusters, so a cluster with one routed unit more than
 // another gets one shared unit fewer; a cluster runs its shared units first.
-// Returns the number of units (> kMaxU: does not fit).
+// Within each list a unit's down stage follows the next unit's two gate/up
+// stages.  Returns the number of units (> kMaxU: does not fit).
 __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
   const int nGf = p.f / 64, nGs = p.fs / 64, Ur = p.k * nGf;
   int n = 0, t = 0;
+  int pend = -1;            // unit whose down stage is still to be queued
+  auto push = [&](int kind, int tt, int ui) {
+    CTask e;
+    e.kind = static_cast<int8_t>(kind);
+    e.tt = static_cast<int8_t>(tt);
+    e.ui = static_cast<int8_t>(ui);
+    e.pad = 0;
+    e.src = static_cast<int16_t>(ui >= 0 ? S.unit_src[ui] : 0);
+    e.G = static_cast<int16_t>(ui >= 0 ? S.unit_G[ui] : 0);
+    S.tasks[t++] = e;
+  };
   auto add_unit = [&](int src, int G) {
     if (n < kMaxU) {
       S.unit_src[n] = src;
-      for (int s = 0; s < 3; ++s) {
-        CTask e;
-        e.kind = static_cast<int8_t>(s < 2 ? K_GU : K_DN);
-        e.tt = static_cast<int8_t>(s < 2 ? s : 0);
-        e.ui = static_cast<int8_t>(n);
-        e.pad = 0;
-        e.src = static_cast<int16_t>(src);
-        e.G = static_cast<int16_t>(G);
-        S.tasks[t++] = e;
-      }
+      S.unit_G[n] = G;
+      push(K_GU, 0, n);
+      push(K_GU, 1, n);
+      if (pend >= 0) push(K_DN, 0, pend);
+      pend = n;
     }
     ++n;
   };
+  auto flush = [&]() {
+    if (pend >= 0 && n <= kMaxU) push(K_DN, 0, pend);
+    pend = -1;
+  };
   for (int G = 0; G < nGs; ++G)
     if ((Ur + G) % n_cl == cl) add_unit(-1, G);
-  if (n <= kMaxU) {
-    CTask m{};
-    m.kind = K_TOPK;
-    S.tasks[t++] = m;
-  }
+  flush();
+  if (n <= kMaxU) push(K_TOPK, 0, -1);
   for (int i = 0; i < Ur; ++i)
     if (i % n_cl == cl) add_unit(i / nGf, i % nGf);
+  flush();
   S.n_tasks = t;
   S.n_units = n < kMaxU ? n : kMaxU;
   S.n_stages = 3 * S.n_units;
@@ -323,7 +368,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
   const uint32_t tile_bytes = static_cast<uint32_t>(p.d / 64) * kGroupBytes;   // gate/up tile = down slice
   const int R = p.d / 64;                                                     // 16-row down tiles per CTA
   uint32_t u_issued = 0;
-  bool rrow_issued = false;
+  int rrow_last = -1;      // layer of the last router-row copy
   bool stop = false;
   for (int rel = 0; rel < n_rel && !stop; ++rel) {
     const CLayer* L = p.layers + (p.l0 + rel);
@@ -335,7 +380,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
       const uint16_t* rw = L->router_w;
       mbar_arrive_expect_tx(&S.rrow_full, static_cast<uint32_t>(p.d) * 2u);
       bulk_g2s(S.rrow, rw + static_cast<size_t>(blockIdx.x) * p.d, static_cast<uint32_t>(p.d) * 2u, &S.rrow_full);
-      rrow_issued = true;
+      rrow_last = rel;
     }
     int s = 0;
     for (int i = 0; i < S.n_tasks; ++i) {
@@ -376,11 +421,9 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
   if (aborted(p)) {
     for (uint32_t v = (u_issued > static_cast<uint32_t>(kNS) ? u_issued - kNS : 0); v < u_issued; ++v)
       mbar_wait_bounded(&S.full[v % kNS], (v / kNS) & 1u, p.err);
-    if (rrow_issued) {
-      // the newest router-row phase: consumers may not have waited for it
-      for (uint32_t par = 0; par < 2; ++par)
-        if (mbar_try_wait(&S.rrow_full, par)) break;
-    }
+    // the last router-row copy completes phase rrow_last of rrow_full (its
+    // consumers may have given up before waiting for it)
+    if (rrow_last >= 0) mbar_wait_bounded(&S.rrow_full, static_cast<uint32_t>(rrow_last) & 1u, p.err);
   }
 }
 
@@ -388,21 +431,23 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
 
 // Polls layer l's tagged logits until every entry carries this launch's tag,
 // then takes the top-k (ties to the lower index) and the softmax gates.  Each
-// lane holds up to 8 logits sorted by (value desc, index asc); a round picks
+// lane holds up to NPL logits (4 for at most 128 experts, else 8) sorted by
+// (value desc, index asc); a round picks
 // the warp-wide best head with three warp reductions on the order-preserving
 // unsigned image of the int64 logit and on the index.
+template <int NPL>
 __device__ bool topk_layer(const CParams& p, int l, int32_t* ids, float* gates) {
   const int lane = threadIdx.x & 31;
   const unsigned long long* lg = p.tlog + static_cast<size_t>(l) * p.E * 2;
-  unsigned long long key[8];
-  int idx[8];
+  unsigned long long key[NPL];
+  int idx[NPL];
   int n = 0;
   const long long t0 = clock64();
   for (unsigned it = 0;; ++it) {
     bool ok = true;
     n = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < NPL; ++i) {
       const int e = lane + 32 * i;
       key[i] = 0ull;
       idx[i] = 0x7fffffff;
@@ -418,7 +463,9 @@ __device__ bool topk_layer(const CParams& p, int l, int32_t* ids, float* gates) 
       if (lane == 0) stamp(p, l - p.l0, EV_LOGITS_IN);
       break;
     }
-    __nanosleep(32);
+    // every CTA polls the same 16 lines: back off so the pollers do not
+    // crowd out the stores they wait for
+    __nanosleep(kPollSleepNs);
     if ((it & 255) == 255) {
       if (__any_sync(kFull, aborted(p))) return false;
       if (__any_sync(kFull, clock64() - t0 > kSpinLimitCycles)) {
@@ -428,7 +475,7 @@ __device__ bool topk_layer(const CParams& p, int l, int32_t* ids, float* gates) 
     }
   }
 #pragma unroll
-  for (int i = 1; i < 8; ++i) {
+  for (int i = 1; i < NPL; ++i) {
 #pragma unroll
     for (int j = i; j > 0; --j) {
       if (key[j] > key[j - 1]) {
@@ -441,13 +488,14 @@ __device__ bool topk_layer(const CParams& p, int l, int32_t* ids, float* gates) 
       }
     }
   }
+  if (lane == 0) stamp(p, l - p.l0, EV_TOPK_SORTED);
   int head = 0, my_id = 0;
   long long my_v = 0;
   for (int j = 0; j < p.k; ++j) {
     unsigned long long hk = 0ull;
     int he = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < NPL; ++i)
       if (i == head) {
         hk = key[i];
         he = idx[i];
@@ -485,7 +533,8 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
   for (int rel = 0; rel < n_rel; ++rel) {
     int32_t* sid = S.ids[rel & 1];
     float* sg = S.gates[rel & 1];
-    if (!topk_layer(p, p.l0 + rel, sid, sg)) return;
+    const bool ok = p.E <= 128 ? topk_layer<4>(p, p.l0 + rel, sid, sg) : topk_layer<8>(p, p.l0 + rel, sid, sg);
+    if (!ok) return;
     if (lane == 0) stamp(p, rel, EV_TOPK_DONE);
     if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
       const DevCallArgs* A = &S.args;
@@ -503,79 +552,118 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
 // Layer input: wait for the previous layer's output vector, add it to this
 // CTA's copy of the residual stream, RMS norm in a fixed order (every CTA gets
 // the same x), x as plain bf16, as mma B fragments and as per-group sums.
-__device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round) {
+__device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, unsigned rank) {
   const int lane = threadIdx.x & 31;
   const int d = p.d, nGd = d / 64;
   const DevCallArgs* A = &S.args;
-  const long long* yin = nullptr;
-  if (rel > 0) {
-    if (cw == 0 && !warp_wait_counter(p, p.y_cnt + (rel - 1), gridDim.x)) return false;
-    if (cw == 0 && lane == 0) stamp(p, rel, EV_Y_SEEN);
-    if (!consumer_barrier(p, S, ++round)) return false;
-    yin = p.ybuf + static_cast<size_t>((rel - 1) % 3) * d;
-    // this CTA's share of the vector layer rel + 1 adds into: its last reader
-    // was the input step of layer rel - 1, which every CTA finished before the
-    // counter just waited for
-    long long* yz = p.ybuf + static_cast<size_t>((rel + 1) % 3) * d;
-    const int share = (d + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-    const int j = cw * 32 + lane, i = static_cast<int>(blockIdx.x) * share + j;
-    if (j < share && i < d) yz[i] = 0;
-  }
-  // warp cw takes groups G = cw, cw + kNC, ...; lane holds elements 64G + 2*lane, +1
-  uint32_t hv[(kMaxG + kNC - 1) / kNC];
-  float ss = 0.f;
-  int ng = 0;
-  const bool dbg_y = blockIdx.x == 0 && rel > 0 && A->dbg_y && rel - 1 < A->dbg_layers;
-  for (int G = cw; G < nGd; G += kNC, ++ng) {
-    uint32_t v;
-    if (rel == 0) {
-      v = __ldcg(reinterpret_cast<const unsigned*>(A->h_in + 64 * G) + lane);
-    } else {
-      v = reinterpret_cast<const uint32_t*>(S.h)[32 * G + lane];
-      const longlong2 yy = __ldcg(reinterpret_cast<const longlong2*>(yin + 64 * G + 2 * lane));
-      const float y0 = __ll2float_rn(yy.x) * 2.3283064365386963e-10f;   // 2^-32
-      const float y1 = __ll2float_rn(yy.y) * 2.3283064365386963e-10f;
-      const float a = bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu)) + y0;
-      const float b = bf16_bits_to_float(static_cast<uint16_t>(v >> 16)) + y1;
-      v = static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
-      if (dbg_y) {
-        float* dy = A->dbg_y + (static_cast<size_t>(rel - 1) * A->tok_total + A->tok_off) * d + 64 * G + 2 * lane;
-        dy[0] = y0;
-        dy[1] = y1;
+  constexpr int kGW = (kMaxG + kNC - 1) / kNC;   // groups per warp at most
+  float r = 1.f;
+  if (rel == 0) {
+    // the call's input: every CTA reads all of h_in; warp cw takes groups cw,
+    // cw + kNC, ...; lane holds elements 64G + 2*lane, +1
+    uint32_t hv[kGW];
+#pragma unroll
+    for (int i = 0; i < kGW; ++i) {
+      const int G = cw + kNC * i;
+      hv[i] = G < nGd ? __ldcg(reinterpret_cast<const unsigned*>(A->h_in + 64 * G) + lane) : 0u;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kGW; ++i) {
+      const int G = cw + kNC * i;
+      if (G < nGd) {
+        reinterpret_cast<uint32_t*>(S.h[0])[32 * G + lane] = hv[i];
+        const float a = bf16_bits_to_float(static_cast<uint16_t>(hv[i] & 0xFFFFu));
+        const float b = bf16_bits_to_float(static_cast<uint16_t>(hv[i] >> 16));
+        ss += a * a;
+        ss += b * b;
       }
     }
-    reinterpret_cast<uint32_t*>(S.h)[32 * G + lane] = v;
-    hv[ng] = v;
-    const float a = bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu));
-    const float b = bf16_bits_to_float(static_cast<uint16_t>(v >> 16));
-    ss += a * a;
-    ss += b * b;
-  }
 #pragma unroll
-  for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(kFull, ss, m);
-  if (lane == 0) S.red[cw] = ss;
-  if (!consumer_barrier(p, S, ++round)) return false;   // red[] complete, the previous layer's stages all done
-  float r = 1.f;
-  if (p.prenorm) {
-    float tot = 0.f;
-    for (int w = 0; w < kNC; ++w) tot += S.red[w];
-    r = 1.0f / sqrtf(tot / static_cast<float>(d) + p.eps);
+    for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(kFull, ss, m);
+    if (lane == 0) S.red[cw] = ss;
+    if (!consumer_barrier(p, S, ++round)) return false;   // red[] and S.h complete
+    if (p.prenorm) {
+      float tot = 0.f;
+      for (int w = 0; w < kNC; ++w) tot += S.red[w];
+      r = 1.0f / sqrtf(tot / static_cast<float>(d) + p.eps);
+    }
+  } else {
+    // the previous layer's output: this CTA polls and reads its rank's quarter
+    // (element pairs spread over the warps), adds it to the residual and
+    // writes the result into every CTA of the cluster, with the quarter's sums
+    // of squares; after the cluster barrier every CTA holds the whole h.  The
+    // residual and the sums are double-buffered by layer parity: a peer may
+    // still be reading the previous layer's copy (its x step), never the one
+    // before (it has passed this layer's cluster barrier since).
+    const long long* yin = p.ybuf + static_cast<size_t>((rel - 1) % 3) * d;
+    const int npair = d / 8;                          // element pairs per quarter
+    const int j = cw * 32 + lane, e = static_cast<int>(rank) * (d / 4) + 2 * j;   // pair j of this quarter
+    float ss = 0.f;
+    if (cw * 32 < npair) {
+      const bool valid = j < npair;
+      float y0, y1;
+      if (!poll_rows(p, yin + e, valid, y0, y1)) return false;
+      if (cw == 0 && lane == 0) stamp(p, rel, EV_Y_SEEN);
+      if (valid) {
+        const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h[(rel - 1) & 1])[e / 2];
+        const float a = bf16_bits_to_float(static_cast<uint16_t>(hv & 0xFFFFu)) + y0;
+        const float b = bf16_bits_to_float(static_cast<uint16_t>(hv >> 16)) + y1;
+        const uint32_t v =
+            static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
+#pragma unroll
+        for (int r2 = 0; r2 < kCl; ++r2)
+          st_peer_u32(peer_addr(reinterpret_cast<uint32_t*>(S.h[rel & 1]) + e / 2, static_cast<unsigned>(r2)), v);
+        const float ha = bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu));
+        const float hb = bf16_bits_to_float(static_cast<uint16_t>(v >> 16));
+        ss = ha * ha + hb * hb;
+        if (blockIdx.x < static_cast<unsigned>(kCl) && A->dbg_y && rel - 1 < A->dbg_layers) {   // cluster 0
+          float* dy = A->dbg_y + (static_cast<size_t>(rel - 1) * A->tok_total + A->tok_off) * d + e;
+          dy[0] = y0;
+          dy[1] = y1;
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(kFull, ss, m);
+    if (lane < kCl) st_peer_f32(peer_addr(&S.ssq[rel & 1][rank][cw], static_cast<unsigned>(lane)), ss);
+    if (!cluster_consumer_barrier(p, S, static_cast<uint32_t>(rel - 1) & 1u)) return false;
+    if (cw == 0 && lane == 0) stamp(p, rel, EV_PREP_B1);
+    // every CTA has added into the previous layer's vector, so every CTA is
+    // done reading the one before it: zero this CTA's share of it for layer rel + 1
+    long long* yz = p.ybuf + static_cast<size_t>((rel + 1) % 3) * d;
+    const int share = (d + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+    const int zi = static_cast<int>(blockIdx.x) * share + j;
+    if (j < share && zi < d) yz[zi] = 0;
+    if (p.prenorm) {
+      float tot = 0.f;
+      for (int q = 0; q < kCl; ++q)
+        for (int w = 0; w < kNC; ++w) tot += S.ssq[rel & 1][q][w];
+      r = 1.0f / sqrtf(tot / static_cast<float>(d) + p.eps);
+    }
   }
-  ng = 0;
-  for (int G = cw; G < nGd; G += kNC, ++ng) {
-    uint32_t xv = hv[ng];
+  if (cw == 0 && lane == 0) stamp(p, rel, EV_PREP_B2);
+#pragma unroll
+  for (int i = 0; i < kGW; ++i) {
+    const int G = cw + kNC * i;
+    if (G >= nGd) continue;
+    uint32_t xv = reinterpret_cast<const uint32_t*>(S.h[rel & 1])[32 * G + lane];
     if (p.prenorm) {
       const float a = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu)) * r;
       const float b = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16)) * r;
       xv = static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
     }
     reinterpret_cast<uint32_t*>(S.xs)[32 * G + lane] = xv;
-    // B fragments: element e = 2*lane of the group lands in (t4, st, pos)
+    // fp16 B fragments: element e = 2*lane of the group lands in (t4, st, pos)
+    const float xa = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu));
+    const float xb = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16));
+    const __half ha = __float2half_rn(xa), hb = __float2half_rn(xb);
+    if (__any_sync(kFull, !(fabsf(xa) < 65504.f && fabsf(xb) < 65504.f)) && lane == 0) atomicOr(p.err, ERR_PF_RANGE);
     const int e = 2 * lane, st = e >> 4, w = e & 15;
     const int t4 = (w & 7) >> 1, hi = w >> 3;
-    reinterpret_cast<uint32_t*>(S.xp)[((G * 4 + t4) * 4 + st) * 2 + hi] = xv;
-    float gs = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu)) +
-               bf16_bits_to_float(static_cast<uint16_t>(xv >> 16));
+    reinterpret_cast<uint32_t*>(S.xp)[((G * 4 + t4) * 4 + st) * 2 + hi] =
+        static_cast<uint32_t>(__half_as_ushort(ha)) | (static_cast<uint32_t>(__half_as_ushort(hb)) << 16);
+    float gs = __half2float(ha) + __half2float(hb);
 #pragma unroll
     for (int m = 16; m; m >>= 1) gs += __shfl_xor_sync(kFull, gs, m);
     if (lane == 0) S.xg[G] = gs;
@@ -628,6 +716,7 @@ __device__ bool router(const CParams& p, Smem& S, int cw, int rel, int& round) {
   if (lane == 0) S.rlog[cw] = acc;
   if (!consumer_barrier(p, S, ++round)) return false;   // every warp is done with the row and rlog[] is complete
   if (cw != 0) return true;
+  if (lane == 0) stamp(p, rel, EV_ROUTER_B);
   acc = 0;
   for (int w = 0; w < kNC; ++w) acc += S.rlog[w];
   if (lane == 0) {
@@ -647,44 +736,73 @@ __device__ bool router(const CParams& p, Smem& S, int cw, int rel, int& round) {
   return true;
 }
 
-// One chunk (<= 11 groups) of a gate/up tile: partial gate and up sums of row g.
-__device__ void gu_chunk(Smem& S, const uint8_t* chunk, int g0, int ng, float& ga, float& ua) {
+// Eight packed nibbles -> four f16x2 A-fragment registers with four logic ops
+// and one shift: register r takes nibbles r (low half) and r + 4 (high half)
+// where they sit, under the fp16 exponent of 1024 (unit in the last place 1).
+// Registers 0 and 2 (fragment rows g) hold 1024 + q; registers 1 and 3 (rows
+// g + 8) keep their nibbles four bits up and hold 1024 + 16 q, which the
+// epilogue undoes per row.  (bf16 has too few mantissa bits for the second
+// form, which is why the activations of this kernel's MMAs are fp16.)
+__device__ __forceinline__ void nibbles_to_f16x2(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t w8 = w >> 8;
+  a[0] = (w & 0x000F000Fu) | 0x64006400u;
+  a[1] = (w & 0x00F000F0u) | 0x64006400u;
+  a[2] = (w8 & 0x000F000Fu) | 0x64006400u;
+  a[3] = (w8 & 0x00F000F0u) | 0x64006400u;
+}
+
+// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators, A/B from registers.
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Groups [G0, G1) of a gate/up tile: partial gate and up sums of row g.  With
+// P = sum_k x_k (1024 + q_k) (gate rows) and sum_k x_k (1024 + 16 q_k) (up
+// rows), sum_k x_k (s q_k + b) = s P + (b - 1024 s) X for the gate rows and
+// (s / 16) P + (b - 64 s) X for the up rows, X = the group's sum of x.
+__device__ void gu_groups(Smem& S, const uint8_t* tile, int G0, int G1, float& ga, float& ua) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-  for (int i = 0; i < ng; ++i) {
-    const int G = g0 + i;
-    const uint8_t* blk = chunk + i * kGroupBytes;
+#pragma unroll 2
+  for (int G = G0; G < G1; ++G) {
+    const uint8_t* blk = tile + static_cast<size_t>(G) * kGroupBytes;
     const uint4 q = *reinterpret_cast<const uint4*>(blk + lane * 16);
     const uint2 sbv = *reinterpret_cast<const uint2*>(blk + kFragBytes + g * 8);
     const uint4* xf = reinterpret_cast<const uint4*>(S.xp) + (G * 4 + t4) * 2;
     const uint4 x01 = xf[0], x23 = xf[1];
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
     uint32_t a[4];
-    nibbles_to_bf16x2(q.x, a);
-    mma_bf16(c0, a, x01.x, x01.y);
-    nibbles_to_bf16x2(q.y, a);
-    mma_bf16(c1, a, x01.z, x01.w);
-    nibbles_to_bf16x2(q.z, a);
-    mma_bf16(c0, a, x23.x, x23.y);
-    nibbles_to_bf16x2(q.w, a);
-    mma_bf16(c1, a, x23.z, x23.w);
+    nibbles_to_f16x2(q.x, a);
+    mma_f16(c0, a, x01.x, x01.y);
+    nibbles_to_f16x2(q.y, a);
+    mma_f16(c1, a, x01.z, x01.w);
+    nibbles_to_f16x2(q.z, a);
+    mma_f16(c0, a, x23.x, x23.y);
+    nibbles_to_f16x2(q.w, a);
+    mma_f16(c1, a, x23.z, x23.w);
     const float X = S.xg[G];
     const float sg = half_lo(sbv.x), bg = half_hi(sbv.x), su = half_lo(sbv.y), bu = half_hi(sbv.y);
-    ga += sg * (c0[0] + c1[0]) + fmaf(-128.f, sg, bg) * X;
-    ua += su * (c0[2] + c1[2]) + fmaf(-128.f, su, bu) * X;
+    ga += sg * (c0[0] + c1[0]) + fmaf(-1024.f, sg, bg) * X;
+    ua += (su * 0.0625f) * (c0[2] + c1[2]) + fmaf(-64.f, su, bu) * X;
   }
 }
 
 // Epilogue of gate/up tile tt of a unit: a = GELU(gate) * up for its 8 rows,
-// split into bf16 hi + lo, written as down B fragments into the unit's a-slot
+// split into fp16 hi + lo, written as down B fragments into the unit's a-slot
 // of every CTA of the cluster, with the tile's sum of a; then one remote
 // arrival on each CTA's a_full barrier.  Tile tt of rank r holds the unit's
 // intermediate rows 16r + 8tt + g, i.e. k16 step r, in-step rows 8tt + g.
 __device__ void gu_push(const CParams& p, Smem& S, int rel, const CTask& t, unsigned rank, float ga, float ua) {
   const int lane = threadIdx.x & 31;
   const float av = gelu_p(ga, p.gelu) * ua;
-  const uint32_t hi = float_to_bf16_bits(av);
-  const uint32_t lo = float_to_bf16_bits(av - bf16_bits_to_float(static_cast<uint16_t>(hi)));
-  float sh = bf16_bits_to_float(static_cast<uint16_t>(hi)), sl = bf16_bits_to_float(static_cast<uint16_t>(lo));
+  if (__any_sync(kFull, !(fabsf(av) < 65504.f)) && lane == 0) atomicOr(p.err, ERR_PF_RANGE);
+  const __half hh = __float2half_rn(av);
+  const __half hl = __float2half_rn(av - __half2float(hh));
+  const uint32_t hi = __half_as_ushort(hh), lo = __half_as_ushort(hl);
+  float sh = __half2float(hh), sl = __half2float(hl);
 #pragma unroll
   for (int m = 4; m < 32; m <<= 1) {
     sh += __shfl_xor_sync(kFull, sh, m);
@@ -706,14 +824,15 @@ __device__ void gu_push(const CParams& p, Smem& S, int rel, const CTask& t, unsi
   if (lane == 0) stamp(p, rel, EV_PUSH_LAST, true);
 }
 
-// Gate/up stage: warp qw of the quad takes groups [qw * cgu, ...); the last
-// warp of the quad to finish sums the four partials in warp order and pushes a.
+// Gate/up stage: warp qw of the quad takes groups [qw * cgu, (qw + 1) * cgu);
+// the last warp of the quad to finish sums the four partials in warp order and
+// pushes a.
 __device__ void stage_gu(const CParams& p, Smem& S, int qw, int rel, int slot, const CTask& t, unsigned rank) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int nGd = p.d / 64, cgu = (nGd + kQW - 1) / kQW;
-  const int g0 = qw * cgu, ng = min(cgu, nGd - g0);
+  const int g0 = qw * cgu, g1 = min(nGd, g0 + cgu);
   float ga = 0.f, ua = 0.f;
-  if (ng > 0) gu_chunk(S, S.ring[slot] + static_cast<size_t>(g0) * kGroupBytes, g0, ng, ga, ua);
+  gu_groups(S, S.ring[slot], g0, g1, ga, ua);
   if (t4 == 0) {
     S.gu_part[slot][qw][g][0] = ga;
     S.gu_part[slot][qw][g][1] = ua;
@@ -736,9 +855,12 @@ __device__ void stage_gu(const CParams& p, Smem& S, int qw, int rel, int slot, c
   gu_push(p, S, rel, t, rank, ga, ua);
 }
 
-// Down stage: this CTA's d/64 row tiles of the unit's group, warp qw taking
-// tiles qw, qw + 4, ...; every tile uses the same 64 values of a.
-__device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, const CTask& t) {
+// Down stage: this CTA's d/64 row tiles of the unit's group, warp qw of the
+// quad taking tiles qw, qw + 4, ...; every tile uses the same 64 values of a
+// (fp16 hi + lo in two B columns).  Rows g and g + 8 of a tile follow the
+// gate/up epilogue's two forms (1024 + q and 1024 + 16 q).
+__device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, const CTask& t,
+                         unsigned long long* t_ready) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int aslot = (rel & 1) * kMaxU + t.ui;
   if (!mbar_wait_cluster(&S.a_full[aslot], (static_cast<uint32_t>(rel) >> 1) & 1u, p.err)) return false;
@@ -746,6 +868,7 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
     stamp(p, rel, EV_DN_A_FIRST);
     stamp(p, rel, EV_A_WAIT_LAST, true);
   }
+  if (p.timeline) *t_ready = now_ns();
   float As = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) As += S.tsum[aslot][i];
@@ -754,23 +877,24 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
   const uint4 b01 = bf[0], b23 = bf[1];
   const int R = p.d / 64;
   float* out = S.dn_part[t.ui];
+#pragma unroll 2
   for (int T = qw; T < R; T += kQW) {
     const uint8_t* blk = S.ring[slot] + static_cast<size_t>(T) * kGroupBytes;
     const uint4 q = *reinterpret_cast<const uint4*>(blk + lane * 16);
     const uint2 sbv = *reinterpret_cast<const uint2*>(blk + kFragBytes + g * 8);
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
     uint32_t a[4];
-    nibbles_to_bf16x2(q.x, a);
-    mma_bf16(c0, a, b01.x, b01.y);
-    nibbles_to_bf16x2(q.y, a);
-    mma_bf16(c1, a, b01.z, b01.w);
-    nibbles_to_bf16x2(q.z, a);
-    mma_bf16(c0, a, b23.x, b23.y);
-    nibbles_to_bf16x2(q.w, a);
-    mma_bf16(c1, a, b23.z, b23.w);
+    nibbles_to_f16x2(q.x, a);
+    mma_f16(c0, a, b01.x, b01.y);
+    nibbles_to_f16x2(q.y, a);
+    mma_f16(c1, a, b01.z, b01.w);
+    nibbles_to_f16x2(q.z, a);
+    mma_f16(c0, a, b23.x, b23.y);
+    nibbles_to_f16x2(q.w, a);
+    mma_f16(c1, a, b23.z, b23.w);
     const float s0 = half_lo(sbv.x), o0 = half_hi(sbv.x), s1 = half_lo(sbv.y), o1 = half_hi(sbv.y);
-    const float y0 = s0 * ((c0[0] + c1[0]) + (c0[1] + c1[1])) + fmaf(-128.f, s0, o0) * As;
-    const float y1 = s1 * ((c0[2] + c1[2]) + (c0[3] + c1[3])) + fmaf(-128.f, s1, o1) * As;
+    const float y0 = s0 * ((c0[0] + c1[0]) + (c0[1] + c1[1])) + fmaf(-1024.f, s0, o0) * As;
+    const float y1 = (s1 * 0.0625f) * ((c0[2] + c1[2]) + (c0[3] + c1[3])) + fmaf(-64.f, s1, o1) * As;
     if (t4 == 0) {
       out[T * 16 + g] = y0;
       out[T * 16 + g + 8] = y1;
@@ -780,15 +904,17 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
 }
 
 // End of layer rel: gate-weighted sum of the units' partials in unit order,
-// onto the 2^-32 grid, one bulk reduction into the layer's output vector, and
-// the layer counter.  The CTA whose increment completes the last layer reads
-// the final vector (finish()).
+// onto the 2^-32 grid with this CTA's count in the low byte, and one bulk
+// reduction into the layer's output vector (not waited for: readers poll the
+// counts).
 __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round, unsigned rank) {
   const int lane = threadIdx.x & 31;
   if (!mbar_wait_bounded(&S.topk_bar, static_cast<uint32_t>(rel) & 1u, p.err)) {   // gates of this layer
     raise_abort(p);
     return false;
   }
+  // the previous layer's bulk reduction must have read yq before it is rewritten
+  if (cw == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   if (!consumer_barrier(p, S, ++round)) return false;   // every down partial of the layer written
   if (cw == 0 && lane == 0) stamp(p, rel, EV_STAGES_DONE);
   const int rows = p.d / kCl;
@@ -802,69 +928,66 @@ __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round
         const int src = S.unit_src[u];
         y = fmaf(src < 0 ? 1.f : gts[src], S.dn_part[u][i], y);
       }
-      const bool ok = fabsf(y) < 16777216.f;   // |y| < 2^24: the int64 sum over all CTAs cannot overflow
+      // |y| < 2^17: (v << 8) summed over up to 255 clusters stays inside int64
+      const bool ok = fabsf(y) < 131072.f;
       bad |= !ok;
-      S.yq[i] = ok ? __float2ll_rn(y * 4294967296.f) : 0ll;
+      S.yq[i] = (ok ? (__float2ll_rn(y * 4294967296.f) << 8) : 0ll) + 1;   // + 1: this CTA's count
     }
   }
   if (__any_sync(kFull, bad) && lane == 0) atomicOr(p.err, ERR_Y_RANGE);
   fence_proxy_async_smem();   // yq is read by the bulk reduction (async proxy)
   if (!consumer_barrier(p, S, ++round)) return false;
   if (cw != 0) return true;
-  unsigned old = 0;
   if (lane == 0) {
-    if (S.n_units > 0) {
-      fence_proxy_async_global();   // the zeroing of this vector (generic stores, other CTAs) came first
-      bulk_reduce_add_s64(p.ybuf + static_cast<size_t>(rel % 3) * p.d + static_cast<size_t>(rank) * rows, S.yq,
-                          static_cast<uint32_t>(rows) * 8u);
-      fence_proxy_async_global();
-    }
-    stamp(p, rel, EV_REDUCED);
+    // this CTA's zeroing (generic stores) before its reduction becomes
+    // visible; the other CTAs zeroed this vector before adding their rows of
+    // the previous one, which this CTA has read complete
     __threadfence();
-    old = atom_add_acq_rel(p.y_cnt + rel, 1u);
+    fence_proxy_async_global();
+    stamp(p, rel, EV_BULK_ISSUED);
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u64 [%0], [%1], %2;" ::"l"(
+                     p.ybuf + static_cast<size_t>(rel % 3) * p.d + static_cast<size_t>(rank) * rows),
+                 "r"(smem_u32(S.yq)), "r"(static_cast<uint32_t>(rows) * 8u)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    stamp(p, rel, EV_REDUCED);
   }
-  old = __shfl_sync(kFull, old, 0);
-  if (lane == 0) S.finisher = old == gridDim.x - 1 ? 1 : 0;
+  __syncwarp();
   return true;
 }
 
-// Run by the CTA that completed the last layer: h_out = bf16(h + y), y_last,
-// the last layer's debug y, and the output vectors zeroed for the next launch.
-__device__ void finish(const CParams& p, Smem& S, int cw, int rel, int& round) {
+// After the last layer, cluster 0's four CTAs poll their quarters of the
+// final vector: h_out = bf16(h + y), y_last, the last layer's debug y, and the
+// last two vectors zeroed for the next launch (every CTA has added into the
+// last one, so every CTA is done reading the one before it).
+__device__ void finish(const CParams& p, Smem& S, int cw, int rel, unsigned rank) {
   const int lane = threadIdx.x & 31;
-  if (!consumer_barrier(p, S, ++round)) return;
-  if (!S.finisher) return;
+  if (blockIdx.x >= static_cast<unsigned>(kCl)) return;
   const DevCallArgs* A = &S.args;
-  const int d = p.d;
-  long long* yv = p.ybuf + static_cast<size_t>(rel % 3) * d;
-  const bool dbg_y = A->dbg_y && rel < A->dbg_layers;
-  for (int j0 = 0; j0 < d / 2; j0 += kNC * 32) {
-    const int j = j0 + cw * 32 + lane;
-    if (j < d / 2) {
-      const longlong2 yy = __ldcg(reinterpret_cast<const longlong2*>(yv + 2 * j));
-      const float y0 = __ll2float_rn(yy.x) * 2.3283064365386963e-10f;
-      const float y1 = __ll2float_rn(yy.y) * 2.3283064365386963e-10f;
-      const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h)[j];
-      const float a = bf16_bits_to_float(static_cast<uint16_t>(hv & 0xFFFFu)) + y0;
-      const float b = bf16_bits_to_float(static_cast<uint16_t>(hv >> 16)) + y1;
-      reinterpret_cast<uint32_t*>(A->h_out)[j] =
-          static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
-      if (A->y_last) {
-        A->y_last[2 * j] = y0;
-        A->y_last[2 * j + 1] = y1;
-      }
-      if (dbg_y) {
-        float* dy = A->dbg_y + (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * d + 2 * j;
-        dy[0] = y0;
-        dy[1] = y1;
-      }
-      *reinterpret_cast<longlong2*>(yv + 2 * j) = make_longlong2(0, 0);
-      if (rel > 0) {
-        long long* yp = p.ybuf + static_cast<size_t>((rel - 1) % 3) * d;
-        *reinterpret_cast<longlong2*>(yp + 2 * j) = make_longlong2(0, 0);
-      }
-    }
+  const int d = p.d, npair = d / 8;
+  if (cw * 32 >= npair) return;
+  const int j = cw * 32 + lane, e = static_cast<int>(rank) * (d / 4) + 2 * j;
+  const bool valid = j < npair;
+  long long* yv = p.ybuf + static_cast<size_t>(rel % 3) * d + e;
+  float y0, y1;
+  if (!poll_rows(p, yv, valid, y0, y1) || !valid) return;
+  const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h[rel & 1])[e / 2];
+  const float a = bf16_bits_to_float(static_cast<uint16_t>(hv & 0xFFFFu)) + y0;
+  const float b = bf16_bits_to_float(static_cast<uint16_t>(hv >> 16)) + y1;
+  reinterpret_cast<uint32_t*>(A->h_out)[e / 2] =
+      static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
+  if (A->y_last) {
+    A->y_last[e] = y0;
+    A->y_last[e + 1] = y1;
   }
+  if (A->dbg_y && rel < A->dbg_layers) {
+    float* dy = A->dbg_y + (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * d + e;
+    dy[0] = y0;
+    dy[1] = y1;
+  }
+  *reinterpret_cast<longlong2*>(yv) = make_longlong2(0, 0);
+  if (rel > 0)
+    *reinterpret_cast<longlong2*>(p.ybuf + static_cast<size_t>((rel - 1) % 3) * d + e) = make_longlong2(0, 0);
 }
 
 __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
@@ -873,8 +996,9 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
   const int n_rel = p.l1 - p.l0;
   int round = 0;
   for (int rel = 0; rel < n_rel; ++rel) {
-    if (!prep(p, S, cw, rel, round)) return;
+    if (!prep(p, S, cw, rel, round, rank)) return;
     if (!router(p, S, cw, rel, round)) return;
+    // stage u of the CTA goes to quad u mod 4
     int s = 0;
     for (int i = 0; i < S.n_tasks; ++i) {
       const CTask t = S.tasks[i];
@@ -882,26 +1006,36 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
       const uint32_t u = static_cast<uint32_t>(rel) * S.n_stages + s++;
       if (static_cast<int>(u % kNQ) != quad) continue;
       const int slot = u % kNS;
+      const unsigned long long t0 = p.timeline ? now_ns() : 0ull;
       if (!mbar_wait_bounded(&S.full[slot], (u / kNS) & 1u, p.err)) {
         raise_abort(p);
         return;
       }
+      const unsigned long long t1 = p.timeline ? now_ns() : 0ull;
       if (lane == 0) {
         stamp(p, rel, t.src < 0 ? EV_SHARED_DATA : EV_ROUTED_DATA);
         stamp(p, rel, EV_DATA_LAST, true);
+        acc(p, rel, t.src < 0 ? 6 : 3, t1 - t0);
       }
+      unsigned long long ta = t1;
       if (t.kind == K_GU) {
         stage_gu(p, S, qw, rel, slot, t, rank);
-      } else if (!stage_dn(p, S, qw, rel, slot, t)) {
+      } else if (!stage_dn(p, S, qw, rel, slot, t, &ta)) {
         raise_abort(p);
         return;
+      }
+      if (lane == 0 && p.timeline) {
+        const unsigned long long t2 = now_ns();
+        acc(p, rel, t.kind == K_GU ? 0 : 1, t2 - ta);
+        acc(p, rel, t.kind == K_GU ? 4 : 5, 1);
+        if (t.kind == K_DN) acc(p, rel, 2, ta - t1);
       }
       __syncwarp();
       if (lane == 0) mbarrier_arrive(&S.empty[slot]);
     }
     if (!layer_end(p, S, cw, rel, round, rank)) return;
   }
-  finish(p, S, cw, n_rel - 1, round);
+  finish(p, S, cw, n_rel - 1, rank);
 }
 
 // 18 warps put five on two of the SM's four schedulers; each scheduler has 16 K
@@ -911,6 +1045,12 @@ __global__ void __launch_bounds__(kCThreads, 1) k_decode_cluster(CParams p) {
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const unsigned rank = cluster_rank();
+  // every distributed-shared-memory address below assumes clusters of kCl
+  // CTAs covering the grid: anything else returns before touching a peer
+  if (cluster_size() != static_cast<unsigned>(kCl) || cluster_count() * kCl != gridDim.x) {
+    if (threadIdx.x == 0) atomicOr(p.err, ERR_LAUNCH_SHAPE);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNS; ++i) {
       mbar_init(&S.full[i], 1);
@@ -921,9 +1061,9 @@ __global__ void __launch_bounds__(kCThreads, 1) k_decode_cluster(CParams p) {
     mbar_init(&S.rrow_empty, 1);
     mbar_init(&S.topk_bar, 1);
     mbar_init(&S.cbar, kNC);
+    mbar_init(&S.clbar, kCl * kNC);
     fence_mbar_init();
     S.args = *p.args;
-    S.finisher = 0;
     if (build_tasks(p, S, static_cast<int>(cluster_idx()), static_cast<int>(cluster_count())) > kMaxU)
       raise_abort(p);
   }
@@ -939,9 +1079,11 @@ __global__ void __launch_bounds__(kCThreads, 1) k_decode_cluster(CParams p) {
       topk_warp(p, S);
     }
   }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // this thread's bulk reductions are done
   __syncthreads();
   cluster_sync_all();   // no CTA leaves while a peer may still write into its shared memory
-  // the last CTA out zeroes the counters (and, after an abort, the output vectors)
+  // the last CTA out resets the exit counter and the abort flag (and, after an
+  // abort, zeroes the output vectors, whose counts would otherwise be stale)
   __shared__ int s_last;
   if (threadIdx.x == 0) {
     __threadfence();
@@ -950,7 +1092,6 @@ __global__ void __launch_bounds__(kCThreads, 1) k_decode_cluster(CParams p) {
   __syncthreads();
   if (s_last) {
     __threadfence();
-    for (int i = threadIdx.x; i < p.n_counters; i += blockDim.x) p.y_cnt[i] = 0;
     if (aborted(p))
       for (int i = threadIdx.x; i < 3 * p.d; i += blockDim.x) p.ybuf[i] = 0;
     __syncthreads();

@@ -34,8 +34,9 @@ enum : uint32_t {
   ERR_ROUTER_DOMAIN = 1u << 0,   // |W_r * x| >= 2^11 or a non-finite router input
   ERR_WAIT_TIMEOUT = 1u << 1,    // a bounded wait ran out
   ERR_PLAN = 1u << 2,            // plan capacity exceeded (should be unreachable)
-  ERR_PF_RANGE = 1u << 3,        // prefill: an fp16 matrix operand would overflow (|v| >= 65504)
+  ERR_PF_RANGE = 1u << 3,        // an fp16 matrix operand would overflow (|v| >= 65504)
   ERR_Y_RANGE = 1u << 4,         // decode: a CTA's partial layer output beyond 2^24 (fixed-point sum range)
+  ERR_LAUNCH_SHAPE = 1u << 5,    // the clustered kernel ran without its cluster shape (it returned at once)
 };
 
 constexpr int kGroup = 64;

@@ -86,9 +86,8 @@ struct CParams {
   const DevCallArgs* args;
   unsigned long long* tlog;            // [n_layers][E][2]: logit low / high word, each | tag << 32
   unsigned tag;                        // this launch's tag (never 0)
-  long long* ybuf;                     // [3][d] layer outputs on the 2^-32 grid; zero between launches
-  unsigned* y_cnt;                     // [n_counters] CTAs done with the call's layer rel
-  int n_counters;
+  long long* ybuf;                     // [3][d] layer outputs: sum over CTAs of (v << 8) + 1, v on the 2^-32 grid;
+                                       // zero between launches
   unsigned* exit_cnt;
   unsigned* abort_flag;
   uint32_t* err;

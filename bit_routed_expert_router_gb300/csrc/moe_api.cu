@@ -135,7 +135,7 @@ struct moe_ctx {
   CLayer* c_layers = nullptr;          // device [n_layers]
   unsigned long long* c_tlog = nullptr;  // [n_layers][E][2] tagged logits
   long long* c_ybuf = nullptr;         // [3][d] fixed-point layer outputs
-  unsigned* c_counters = nullptr;      // [n_layers] layer counters, exit counter, abort flag
+  unsigned* c_counters = nullptr;      // exit counter, abort flag
   unsigned c_tag = 0;                  // tag of the last launch
   // batched prefill on tcgen05 (resident contexts): scratch for max_tokens tokens, made on first use
   bool pf_ok = false;                  // shapes and device allow it
@@ -462,10 +462,8 @@ moe_status cluster_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   p.tlog = ctx->c_tlog;
   p.tag = ctx->c_tag;
   p.ybuf = ctx->c_ybuf;
-  p.y_cnt = ctx->c_counters;
-  p.n_counters = c.n_layers;
-  p.exit_cnt = ctx->c_counters + c.n_layers;
-  p.abort_flag = p.exit_cnt + 1;
+  p.exit_cnt = ctx->c_counters;
+  p.abort_flag = ctx->c_counters + 1;
   p.err = ctx->err_word;
   p.timeline = ctx->p_timeline;
   PROF(3, s);
@@ -731,7 +729,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->c_layers = dalloc<CLayer>(c.n_layers, o, nb);
   ctx->c_tlog = dalloc<unsigned long long>(static_cast<size_t>(c.n_layers) * c.n_experts * 2, o, nb);
   ctx->c_ybuf = dalloc<long long>(static_cast<size_t>(3) * c.d, o, nb);
-  ctx->c_counters = dalloc<unsigned>(static_cast<size_t>(c.n_layers) + 2, o, nb);
+  ctx->c_counters = dalloc<unsigned>(2, o, nb);
   for (void* ptr : o)
     if (!ptr) return bail(MOE_ENOMEM);
   if (!ctx->hbuf[0] || !ctx->hbuf[1] || !ctx->x_perm || !ctx->dargs || !ctx->y_r || !ctx->part_s || !ctx->a_r)
@@ -747,7 +745,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       cudaMemset(ctx->c_layers, 0, sizeof(CLayer) * c.n_layers) != cudaSuccess ||
       cudaMemset(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * c.n_experts * 16) != cudaSuccess ||
       cudaMemset(ctx->c_ybuf, 0, static_cast<size_t>(3) * c.d * 8) != cudaSuccess ||
-      cudaMemset(ctx->c_counters, 0, (static_cast<size_t>(c.n_layers) + 2) * 4) != cudaSuccess)
+      cudaMemset(ctx->c_counters, 0, 8) != cudaSuccess)
     return bail(MOE_ECUDA);
   if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->args_ring), sizeof(DevCallArgs) * kArgRing, cudaHostAllocDefault) !=
       cudaSuccess)
@@ -1323,7 +1321,9 @@ moe_status moe_sync(moe_ctx* ctx, void* stream) {
   if (w & ERR_WAIT_TIMEOUT) return fail(ctx, MOE_ETIMEOUT, "a device wait ran out (error word 0x%x)", w);
   if (w & ERR_PLAN) return fail(ctx, MOE_ECUDA, "device plan overflow (error word 0x%x)", w);
   if (w & ERR_ROUTER_DOMAIN) return fail(ctx, MOE_EDOMAIN, "router input outside the exact fixed-point domain");
-  if (w & ERR_PF_RANGE) return fail(ctx, MOE_EDOMAIN, "prefill: an fp16 matrix operand is outside [-65504, 65504]");
+  if (w & ERR_PF_RANGE) return fail(ctx, MOE_EDOMAIN, "an fp16 matrix operand (prefill, or the clustered decode kernel) is outside [-65504, 65504]");
+  if (w & ERR_LAUNCH_SHAPE)
+    return fail(ctx, MOE_ECUDA, "clustered decode kernel ran without clusters of %d CTAs (error word 0x%x)", kCCluster, w);
   if (w & ERR_Y_RANGE) return fail(ctx, MOE_EDOMAIN, "decode: a partial FFN output is outside (-2^24, 2^24)");
   return MOE_OK;
 }
