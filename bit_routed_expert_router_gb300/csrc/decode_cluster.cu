@@ -313,10 +313,11 @@ __device__ __forceinline__ void acc(const CParams& p, int rel, int slot, unsigne
 // ------------------------------------------------------------------ units and stages
 
 // The cluster's units of a layer (the same for every layer: only the experts
-// behind the top-k positions change).  Units are numbered routed first
-// (position j, group G -> j * f/64 + G), then shared (k * f/64 + G), and dealt
-// round-robin over the clusters, so a cluster with one routed unit more than
-// another gets one shared unit fewer; a cluster runs its shared units first.
+// behind the top-k positions change).  Routed unit i (position j, group G,
+// i = j * f/64 + G) goes to cluster i mod n_cl; shared units go round-robin
+// to the clusters with the fewer routed units (all clusters if the routed
+// units divide evenly): routed work waits for the top-k and sets the layer's
+// length, shared work fills the wait.  A cluster runs its shared units first.
 // Within each list a unit's down stage follows the next unit's two gate/up
 // stages.  Returns the number of units (> kMaxU: does not fit).
 __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
@@ -349,7 +350,7 @@ __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
     pend = -1;
   };
   for (int G = 0; G < nGs; ++G)
-    if ((Ur + G) % n_cl == cl) add_unit(-1, G);
+    if (cluster_unit_owner_shared(G, Ur, n_cl) == cl) add_unit(-1, G);
   flush();
   if (n <= kMaxU) push(K_TOPK, 0, -1);
   for (int i = 0; i < Ur; ++i)
@@ -643,6 +644,16 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     }
   }
   if (cw == 0 && lane == 0) stamp(p, rel, EV_PREP_B2);
+  // the router row of this CTA's expert is dotted with x as x is formed: each
+  // warp adds its elements' exact products (RNE onto the 2^-40 grid, integer
+  // sums, so the split does not change the logit) and leaves one partial
+  const bool routes = static_cast<int>(blockIdx.x) < p.E;
+  if (routes && !mbar_wait_bounded(&S.rrow_full, static_cast<uint32_t>(rel) & 1u, p.err)) {
+    raise_abort(p);
+    return false;
+  }
+  Fix40 fx;
+  bool bad = false;
 #pragma unroll
   for (int i = 0; i < kGW; ++i) {
     const int G = cw + kNC * i;
@@ -654,6 +665,18 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
       xv = static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
     }
     reinterpret_cast<uint32_t*>(S.xs)[32 * G + lane] = xv;
+    if (routes) {
+      const uint32_t wv = reinterpret_cast<const uint32_t*>(S.rrow)[32 * G + lane];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float pw = hh ? half_hi(wv) : half_lo(wv);
+        const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xv >> 16) : (xv & 0xFFFFu)));
+        const float prod = pw * px;   // exact: 11-bit x 8-bit significands
+        const bool okp = fabsf(prod) < 2048.f;
+        bad |= !okp;
+        fix40_add(fx, okp ? prod * 1099511627776.0f : 0.f);
+      }
+    }
     // fp16 B fragments: element e = 2*lane of the group lands in (t4, st, pos)
     const float xa = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu));
     const float xb = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16));
@@ -670,57 +693,29 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     if (blockIdx.x == 0 && A->dbg_x && rel < A->dbg_layers)
       reinterpret_cast<uint32_t*>(A->dbg_x + (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * d)[32 * G + lane] = xv;
   }
-  const bool ok = consumer_barrier(p, S, ++round);   // x complete
+  if (routes) {
+    long long acc = fix40_value(fx);
+#pragma unroll
+    for (int m = 16; m; m >>= 1) acc += shfl_xor_i64(acc, m);
+    if (__any_sync(kFull, bad) && lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);
+    if (lane == 0) S.rlog[cw] = acc;
+  }
+  const bool ok = consumer_barrier(p, S, ++round);   // x and the router partials complete
   if (cw == 0 && lane == 0) stamp(p, rel, EV_X_READY);
   return ok;
 }
 
-// Router row blockIdx.x of layer rel (exact fixed-point logit, all consumer
-// warps), published with this launch's tag in both 64-bit words.
-__device__ bool router(const CParams& p, Smem& S, int cw, int rel, int& round) {
-  if (static_cast<int>(blockIdx.x) >= p.E) return true;
+// Logit of router row blockIdx.x of layer rel: the warps' exact partials
+// (formed with x in prep) summed, plus the bias, published with this launch's
+// tag in both 64-bit words.  Run by consumer warp 0 after the x barrier.
+__device__ void router_publish(const CParams& p, Smem& S, int cw, int rel) {
+  if (static_cast<int>(blockIdx.x) >= p.E || cw != 0) return;
   const int lane = threadIdx.x & 31;
-  if (!mbar_wait_bounded(&S.rrow_full, static_cast<uint32_t>(rel) & 1u, p.err)) {
-    raise_abort(p);
-    return false;
-  }
-  const uint4* wr = reinterpret_cast<const uint4*>(S.rrow);
-  const uint4* xv4 = reinterpret_cast<const uint4*>(S.xs);
-  Fix40 fx;
-  bool bad = false;
-  for (int c0 = cw * 32; c0 < p.d / 8; c0 += 32 * kNC) {
-    const int c = min(c0 + lane, p.d / 8 - 1);
-    const bool live = c0 + lane < p.d / 8;   // the clamped lanes of a ragged tail add nothing
-    uint4 wv = wr[c];
-    const uint4 xv = xv4[c];
-    if (!live) wv = make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
-    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float pw = hh ? half_hi(wa[i]) : half_lo(wa[i]);
-        const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xa[i] >> 16) : (xa[i] & 0xFFFFu)));
-        const float prod = pw * px;  // exact: 11-bit x 8-bit significands
-        const bool ok = fabsf(prod) < 2048.f;
-        bad |= !ok;
-        fix40_add(fx, ok ? prod * 1099511627776.0f : 0.f);  // RNE onto the 2^-40 grid, summed exactly
-      }
-    }
-  }
-  long long acc = fix40_value(fx);
-#pragma unroll
-  for (int m = 16; m; m >>= 1) acc += shfl_xor_i64(acc, m);
-  if (__any_sync(kFull, bad) && lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);
-  if (lane == 0) S.rlog[cw] = acc;
-  if (!consumer_barrier(p, S, ++round)) return false;   // every warp is done with the row and rlog[] is complete
-  if (cw != 0) return true;
   if (lane == 0) stamp(p, rel, EV_ROUTER_B);
-  acc = 0;
+  long long acc = 0;
   for (int w = 0; w < kNC; ++w) acc += S.rlog[w];
   if (lane == 0) {
-    mbarrier_arrive(&S.rrow_empty);
+    mbarrier_arrive(&S.rrow_empty);   // every warp read the row before the barrier
     const DevCallArgs* A = &S.args;
     if (A->bias) {
       const float bv = A->bias[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.E + blockIdx.x];
@@ -733,7 +728,7 @@ __device__ bool router(const CParams& p, Smem& S, int cw, int rel, int& round) {
                       (ua >> 32) | tg);
     stamp(p, rel, EV_LOGIT_OUT);
   }
-  return true;
+  __syncwarp();
 }
 
 // Eight packed nibbles -> four f16x2 A-fragment registers with four logic ops
@@ -997,7 +992,7 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
   int round = 0;
   for (int rel = 0; rel < n_rel; ++rel) {
     if (!prep(p, S, cw, rel, round, rank)) return;
-    if (!router(p, S, cw, rel, round)) return;
+    router_publish(p, S, cw, rel);
     // stage u of the CTA goes to quad u mod 4
     int s = 0;
     for (int i = 0; i < S.n_tasks; ++i) {

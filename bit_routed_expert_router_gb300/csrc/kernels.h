@@ -94,6 +94,13 @@ struct CParams {
   unsigned long long* timeline;        // optional [grid][16] event times (ns) of one layer, null = off
 };
 
+// Cluster of shared unit G (of the shared expert's f_s/64 groups) when the
+// Ur routed units are dealt round-robin over n_cl clusters.
+__host__ __device__ inline int cluster_unit_owner_shared(int G, int Ur, int n_cl) {
+  const int extra = Ur % n_cl;
+  return extra == 0 ? G % n_cl : extra + G % (n_cl - extra);
+}
+
 size_t cluster_smem();
 int cluster_max_units();
 cudaError_t cluster_attrs();

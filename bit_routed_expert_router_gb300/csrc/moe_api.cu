@@ -438,6 +438,19 @@ bool encode_down(CUtensorMap* m, const void* base, int nG, int nT, int n_mat, lo
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Largest number of (source, group) units any cluster gets per layer (the
+// kernel's dealing rule: routed unit i -> cluster i mod n_cl, shared units by
+// cluster_unit_owner_shared).
+int cluster_units_max(const moe_config& c, int n_cl) {
+  const int Ur = c.top_k * (c.f / 64);
+  std::vector<int> n(static_cast<size_t>(n_cl), 0);
+  for (int i = 0; i < Ur; ++i) ++n[static_cast<size_t>(i % n_cl)];
+  for (int G = 0; G < c.f_shared / 64; ++G) ++n[static_cast<size_t>(cluster_unit_owner_shared(G, Ur, n_cl))];
+  int m = 0;
+  for (int v : n) m = v > m ? v : m;
+  return m;
+}
+
 // Resident decode of one token through [l0, l1) with the clustered kernel.
 moe_status cluster_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   const moe_config& c = ctx->cfg;
@@ -788,10 +801,9 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // cooperative launch of every resident cluster
   {
     int n_cl = 0;
-    const int units = c.f_shared / 64 + c.top_k * (c.f / 64);
     if (c.top_k <= 32 && cluster_smem() + 2048 <= static_cast<size_t>(max_smem) && cluster_attrs() == cudaSuccess &&
         cluster_max_active(&n_cl) == cudaSuccess && n_cl >= 1 && c.n_experts <= n_cl * kCCluster &&
-        (units + n_cl - 1) / n_cl <= cluster_max_units()) {
+        cluster_units_max(c, n_cl) <= cluster_max_units()) {
       ctx->c_ok = true;
       ctx->c_grid = n_cl * kCCluster;
     }
