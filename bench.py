@@ -295,6 +295,8 @@ def run_ours(args):
     for i in range(args.warmup):
         step(i)
     moe.check(moe.moe_sync(ctx, stream), ctx)
+    if args.timeline:
+        return print_timeline(moe, ctx, step, args.warmup)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -377,7 +379,7 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16xint4->f32 (router int64)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16xint4->f32 (router int64)",
             "data": "synthetic", "config": config_dict(sh),
             "hbm_roofline_frac_8tbs": value / ws * ffn_bytes / NOMINAL_HBM,
             "bytes_per_token": ffn_bytes,
@@ -403,6 +405,47 @@ def run_ours(args):
 
 PF_TOKENS = 4096
 PF_SEED = 4
+
+
+# Event columns of the clustered decode kernel's per-CTA timeline (hook 5),
+# in the kernel's order; columns 24.. hold summed stage times (ns).
+TIMELINE_EVENTS = ["y_seen", "x_ready", "logit_out", "logits_in", "topk_done", "routed_issue", "shared_data",
+                   "routed_data", "push_last", "dn_last", "stages_done", "reduced", "issue_last", "data_last",
+                   "dn_a_first", "a_wait_last", "prep_cluster_barrier", "prep_y", "prep_norm", "router_publish",
+                   "topk_sorted", "bulk_issued"]
+TIMELINE_SUMS = ["gateup_compute", "down_compute", "down_wait_for_a", "routed_data_wait", "gateup_stages",
+                 "down_stages", "shared_data_wait"]
+
+
+def print_timeline(moe, ctx, step, first, reps=3):
+    """Stamp one layer (the call's third) in every CTA with %globaltimer and
+    print the per-event distribution (us from the first CTA's y_seen), one
+    JSON line per repetition.  Diagnostic only: the stamps cost time."""
+    import numpy as np
+    import torch
+
+    for rep in range(reps):
+        tl = torch.zeros(152, 32, dtype=torch.int64, device="cuda")
+        moe.check(moe.moe_test_hook(ctx, moe.HOOK_TIMELINE, tl.data_ptr()), ctx)
+        step(first + rep)
+        moe.check(moe.moe_sync(ctx), ctx)
+        moe.check(moe.moe_test_hook(ctx, moe.HOOK_TIMELINE, 0), ctx)
+        t = tl.cpu().numpy().astype(np.float64)
+        rows = t[t[:, 0] > 1e12]
+        ref = rows[:, 0].min()
+        ev = {}
+        for k, name in enumerate(TIMELINE_EVENTS):
+            v = rows[:, k]
+            v = v[v > 0]
+            if len(v):
+                v = (v - ref) / 1000.0
+                ev[name] = {"n": int(len(v)), "min": round(float(v.min()), 2),
+                            "med": round(float(np.median(v)), 2), "max": round(float(v.max()), 2)}
+        sums = {name: round(float(np.median(rows[:, 24 + k])) / (1.0 if "stages" in name else 1000.0), 2)
+                for k, name in enumerate(TIMELINE_SUMS)}
+        print(json.dumps({"timeline_rep": rep, "ctas": int(len(rows)), "events_us": ev,
+                          "per_cta_median_sums_us_or_count": sums}), flush=True)
+    return 0
 
 
 def prefill_flops_per_layer(sh, T):
@@ -671,7 +714,7 @@ def run_ours_batched(args):
             "metric": "MoE batched decode tokens/s (30-layer routed+shared FFN, B=32)", "value": value,
             "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16xint4->f32 (router int64)", "data": "synthetic",
+            "vs_baseline": None, "dtype": "fp16xint4->f32 (router int64)", "data": "synthetic",
             "config": {"workload": f"batched{BATCH}_decode{N_LAYERS}_resident", "layers": N_LAYERS, "B": BATCH,
                        "d": sh.d, "f": sh.f, "f_shared": sh.f_shared, "experts": sh.n_experts, "top_k": sh.top_k,
                        "unique_experts_per_layer_mean": float(np.mean(U)), "bytes_per_step": step_bytes,
@@ -782,6 +825,8 @@ def main(argv=None):
                          "step; batched: B=32 tokens per step; pool: host expert pool + LRU slot sweep")
     ap.add_argument("--layers", type=int, default=30,
                     help="layers in the stack (30 is the benchmark; fewer only for small profiler captures)")
+    ap.add_argument("--timeline", action="store_true",
+                    help="decode: print the clustered kernel's per-CTA event timeline of one layer instead of timing")
     args = ap.parse_args(argv)
     global N_LAYERS
     N_LAYERS = args.layers

@@ -62,10 +62,11 @@ constexpr int kNC = 16;                           // consumer warps
 constexpr int kQW = 4;                            // warps per quad (one work item each)
 constexpr int kNQ = kNC / kQW;                    // quads
 constexpr int kNS = kCStages;                     // ring slots
-constexpr int kMaxG = kPMaxD / 64;                // int4 groups along d
+constexpr int kMaxD = kCMaxD;                     // largest d this kernel's buffers hold
+constexpr int kMaxG = kMaxD / 64;                 // int4 groups along d
 constexpr int kSlotBytes = kMaxG * kGroupBytes;   // one gate/up tile or one down slice
 constexpr int kMaxU = kCMaxUnits;                 // units per cluster and layer
-constexpr int kMaxRows = kPMaxD / kCl;            // down output rows per CTA
+constexpr int kMaxRows = kMaxD / kCl;             // down output rows per CTA
 constexpr int kMaxTasks = 3 * kMaxU + 1;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr unsigned kPollSleepNs = 200;             // back-off between polls of data every CTA reads
@@ -86,10 +87,9 @@ struct CTask {
 
 struct Smem {
   alignas(128) uint8_t ring[kNS][kSlotBytes];     // bulk / TMA targets
-  alignas(16) uint16_t rrow[kPMaxD];               // this CTA's router row (fp16)
-  alignas(16) uint16_t h[2][kPMaxD];               // residual stream (bf16) by layer parity, the same in every CTA
-  alignas(16) uint16_t xs[kPMaxD];                 // FFN input x (bf16)
-  alignas(16) uint16_t xp[kPMaxD];                 // x as fp16 mma B fragments
+  alignas(16) uint16_t rrow[kMaxD];                // this CTA's router row (fp16)
+  alignas(16) uint16_t h[2][kMaxD];                // residual stream (bf16) by layer parity, the same in every CTA
+  alignas(16) uint16_t xp[kMaxD];                  // x as fp16 mma B fragments
   alignas(16) float xg[kMaxG];                     // per-group sums of the fp16 x
   alignas(16) uint32_t abuf[2 * kMaxU][64];        // per unit: a as down B fragments (hi/lo), pushed by the cluster
   alignas(16) float tsum[2 * kMaxU][8];            // per unit: sum of a (hi + lo) of each of the 8 gate/up tiles
@@ -194,13 +194,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Relaxed (gpu scope) 2 x 64-bit accesses; each 64-bit element is single-copy
+// atomic, which is what the tagged and counted words rely on.
 __device__ __forceinline__ ulonglong2 ld_volatile_u64x2(const unsigned long long* p) {
   ulonglong2 v;
-  asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_volatile_u64x2(unsigned long long* p, unsigned long long a, unsigned long long b) {
-  asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 
 __device__ __forceinline__ bool aborted(const CParams& p) {
@@ -664,7 +666,6 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
       const float b = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16)) * r;
       xv = static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
     }
-    reinterpret_cast<uint32_t*>(S.xs)[32 * G + lane] = xv;
     if (routes) {
       const uint32_t wv = reinterpret_cast<const uint32_t*>(S.rrow)[32 * G + lane];
 #pragma unroll

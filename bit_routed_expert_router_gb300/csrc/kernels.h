@@ -67,6 +67,7 @@ cudaError_t launch_persistent(PParams& p, int grid, cudaStream_t s);
 constexpr int kCCluster = 4;           // CTAs per cluster
 constexpr int kCStages = 6;            // shared-memory ring slots (one gate/up tile or down slice each)
 constexpr int kCMaxUnits = 6;          // (source, group) units per cluster and layer
+constexpr int kCMaxD = kPMaxD;         // largest d of the clustered kernel
 constexpr int kCThreads = 32 * 18;     // producer warp, 16 consumer warps, top-k warp
 
 struct CLayer {                        // one layer, device memory (the tensor maps keep it 64-byte aligned)

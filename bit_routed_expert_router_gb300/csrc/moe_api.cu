@@ -801,7 +801,8 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // cooperative launch of every resident cluster
   {
     int n_cl = 0;
-    if (c.top_k <= 32 && cluster_smem() + 2048 <= static_cast<size_t>(max_smem) && cluster_attrs() == cudaSuccess &&
+    if (c.top_k <= 32 && c.d <= kCMaxD && cluster_smem() + 2048 <= static_cast<size_t>(max_smem) &&
+        cluster_attrs() == cudaSuccess &&
         cluster_max_active(&n_cl) == cudaSuccess && n_cl >= 1 && c.n_experts <= n_cl * kCCluster &&
         cluster_units_max(c, n_cl) <= cluster_max_units()) {
       ctx->c_ok = true;

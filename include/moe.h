@@ -51,8 +51,11 @@ typedef enum {
     MOE_ESTATE = 4,   /* poisoned context, or a call in the wrong state (layer not initialised,
                          slots not set) */
     MOE_ETIMEOUT = 5, /* a bounded wait expired; the context is now poisoned */
-    MOE_EDOMAIN = 6   /* the device saw a router input outside the exact fixed-point domain
-                         (|W_r[e,i] * x[i]| >= 2^11 or non-finite); reported by moe_sync */
+    MOE_EDOMAIN = 6   /* the device saw a value outside a documented domain: a router input
+                         outside the exact fixed-point domain (|W_r[e,i] * x[i]| >= 2^11 or
+                         non-finite), an fp16 matrix operand outside [-65504, 65504] (prefill
+                         and the clustered one-token kernel), or a clustered-kernel partial
+                         layer output with |y| >= 2^17; reported by moe_sync */
 } moe_status;
 
 enum { MOE_RESIDENT_HBM = 0, MOE_HOST_POOL = 1 };
@@ -156,9 +159,16 @@ moe_status moe_set_slots(moe_ctx *ctx, int n_slots);
  *          receives (layer_end - layer_begin) * top_k records, or NULL
  *   stream: cudaStream_t to run on (NULL = legacy default stream)
  * Resident contexts accept 1 <= B <= min(max_tokens, 32) and return without
- * synchronising; from 16 tokens on (when the shape allows it) a step runs
- * through the same grouped tcgen05 path as moe_prefill, with the same exact
- * routing.  Host-pool contexts need B == 1 and slots set; every call is
+ * synchronising.  B == 1 runs every layer in one cooperative launch: the
+ * clustered kernel (clusters of four CTAs, one per SM, when the device and
+ * the shape allow it: at most 6 (shared or top-k position, int4 group) units
+ * per cluster and layer, n_experts <= CTAs), else the per-SM persistent
+ * kernel.  The clustered kernel multiplies fp16 activations (x and the GELU
+ * product, the latter as an fp16 hi + lo pair), sums the layer output as
+ * integers on a 2^-32 grid (deterministic), and reports a launch without its
+ * cluster shape as MOE_ECUDA from moe_sync.  From 16 tokens on (when the
+ * shape allows it) a step runs through the same grouped tcgen05 path as
+ * moe_prefill, with the same exact routing.  Host-pool contexts need B == 1 and slots set; every call is
  * one LRU step (the step counter increments per call) and the call returns
  * after the last layer's staging decision, with the compute still enqueued.
  * Waits inside the call are bounded (MOE_ETIMEOUT). */
@@ -195,8 +205,10 @@ moe_status moe_set_debug(moe_ctx *ctx, uint16_t *x_layers, int32_t *ids, float *
                          float *y_layers, int max_layers);
 
 /* Synchronise `stream`, then report device-side conditions raised since the
- * last moe_sync: MOE_EDOMAIN (router input domain), MOE_ETIMEOUT (a device
- * wait ran out; poisons).  Clears the reported conditions. */
+ * last moe_sync: MOE_EDOMAIN (a value outside a documented domain, see
+ * moe_status), MOE_ETIMEOUT (a device wait ran out; poisons), MOE_ECUDA (the
+ * clustered kernel ran without its cluster shape and did nothing; poisons).
+ * Clears the reported conditions. */
 moe_status moe_sync(moe_ctx *ctx, void *stream);
 
 moe_status moe_get_stats(moe_ctx *ctx, moe_stats *out);
@@ -280,15 +292,19 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
  * checks see `value` bytes of free device memory (-1 restores the real
  * figure).  hook 3: programmatic dependent launch
  * between consecutive kernels on (value != 0, the default) or off.  hook 4:
- * the single-launch persistent kernel for resident one-token decode on
- * (value != 0, the default) or off (per-layer kernels).  hook 5: `value` is
- * the address of a caller device buffer of 2 * n_layers * 16 uint64 into
- * which the persistent kernel records event times (%globaltimer ns): rows
- * [0, n_layers) min or max over CTAs, rows [n_layers, 2 n_layers) steps of
- * the first routed CTA (see persistent.cu); with 2 * n_layers + gridDim.x rows
- * it also gets per-CTA event times of the step's third layer; 0 stops it.
- * hook 4 or 7 with a non-zero value on a configuration where that kernel path
- * cannot run returns MOE_ESTATE.  hook 7: the tcgen05 path for prefill and for
+ * the single-launch kernels for resident one-token decode on (value != 0, the
+ * default) or off (per-layer kernels).  hook 9: among those, the clustered
+ * kernel (value != 0, the default when available) or the per-SM persistent
+ * kernel (0).  hook 5: `value` is the address of a caller device buffer of
+ * event times (%globaltimer ns), 0 stops it.  Clustered kernel: 152 rows of
+ * 32 uint64, row = CTA, columns 0..21 the first (or, for the "last" events,
+ * the latest) time of each event of the call's third layer, columns 24..30
+ * summed stage times (see decode_cluster.cu).  Per-SM kernel: 2 * n_layers *
+ * 16 uint64, rows [0, n_layers) min or max over CTAs, rows [n_layers,
+ * 2 n_layers) steps of the first routed CTA; with 2 * n_layers + gridDim.x
+ * rows also per-CTA times of the third layer (see persistent.cu).
+ * hook 4, 7 or 9 with a value selecting a kernel path that cannot run on the
+ * configuration returns MOE_ESTATE.  hook 7: the tcgen05 path for prefill and for
  * decode steps of 16 or more tokens on (value != 0, the default when the
  * shape allows it) or off (batched decode kernels).
  * hook 8: `value` is a caller device buffer of 4 * 16 uint64 receiving event
