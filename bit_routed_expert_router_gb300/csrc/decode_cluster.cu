@@ -1036,7 +1036,9 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
 
 // 18 warps put five on two of the SM's four schedulers; each scheduler has 16 K
 // registers, so a thread may hold at most 96 (launch bounds give exactly that).
-__global__ void __launch_bounds__(kCThreads, 1) k_decode_cluster(CParams p) {
+// The cluster shape is a property of the kernel (not only of the launch), so
+// every launch path, a profiler's replay included, runs it in 4-CTA clusters.
+__global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1) k_decode_cluster(CParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int warp = threadIdx.x >> 5;
@@ -1116,13 +1118,6 @@ cudaError_t cluster_max_active(int* n_clusters) {
   cfg.gridDim = dim3(kCCluster);
   cfg.blockDim = dim3(kCThreads);
   cfg.dynamicSmemBytes = sizeof(Smem);
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCCluster;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
   return cudaOccupancyMaxActiveClusters(n_clusters, (const void*)k_decode_cluster, &cfg);
 }
 
@@ -1132,15 +1127,11 @@ cudaError_t launch_cluster(CParams& p, int grid, cudaStream_t s) {
   cfg.blockDim = dim3(kCThreads);
   cfg.dynamicSmemBytes = sizeof(Smem);
   cfg.stream = s;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCCluster;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeCooperative;
-  at[1].val.cooperative = 1;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_decode_cluster, p);
 }
 
