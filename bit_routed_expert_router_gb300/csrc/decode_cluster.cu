@@ -91,7 +91,8 @@ struct Smem {
   alignas(16) uint16_t h[2][kMaxD];                // residual stream (bf16) by layer parity, the same in every CTA
   alignas(16) uint16_t xp[kMaxD];                  // x as fp16 mma B fragments
   alignas(16) float xg[kMaxG];                     // per-group sums of the fp16 x
-  alignas(16) uint32_t abuf[2 * kMaxU][64];        // per unit: a as down B fragments (hi/lo), pushed by the cluster
+  alignas(16) uint32_t abuf[2 * kMaxU][64];        // per unit: a as B-fragment words, block (2 rank + tile) of 8
+                                                   // words (4 * hi/lo column + t4) per sending tile
   alignas(16) float tsum[2 * kMaxU][8];            // per unit: sum of a (hi + lo) of each of the 8 gate/up tiles
   alignas(16) float dn_part[kMaxU][kMaxRows];      // per unit: down partials of this CTA's rows
   alignas(16) long long yq[kMaxRows];              // fixed-point layer output rows, bulk-reduce source
@@ -152,16 +153,12 @@ __device__ __forceinline__ uint32_t peer_addr(const void* local, unsigned rank) 
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 __device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 __device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // Bounded wait for an mbarrier phase completed by arrivals from other CTAs of
@@ -220,20 +217,6 @@ __device__ bool consumer_barrier(const CParams& p, Smem& S, int round) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbarrier_arrive(&S.cbar);
   const bool ok = mbar_wait_bounded(&S.cbar, static_cast<uint32_t>(round - 1) & 1u, p.err);
-  if (!ok) raise_abort(p);
-  __syncwarp();
-  return ok;
-}
-
-// Barrier of the consumer warps of every CTA of the cluster: each warp makes
-// its earlier shared-memory writes (local and remote) visible cluster-wide,
-// then arrives on every CTA's clbar; phase n of a launch has parity n & 1.
-__device__ bool cluster_consumer_barrier(const CParams& p, Smem& S, uint32_t parity) {
-  const int lane = threadIdx.x & 31;
-  fence_acq_rel_cluster();
-  __syncwarp();
-  if (lane < kCl) arrive_peer(peer_addr(&S.clbar, static_cast<unsigned>(lane)));
-  const bool ok = mbar_wait_cluster(&S.clbar, parity, p.err);
   if (!ok) raise_abort(p);
   __syncwarp();
   return ok;
@@ -614,9 +597,7 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
         const float b = bf16_bits_to_float(static_cast<uint16_t>(hv >> 16)) + y1;
         const uint32_t v =
             static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
-#pragma unroll
-        for (int r2 = 0; r2 < kCl; ++r2)
-          st_peer_u32(peer_addr(reinterpret_cast<uint32_t*>(S.h[rel & 1]) + e / 2, static_cast<unsigned>(r2)), v);
+        reinterpret_cast<uint32_t*>(S.h[rel & 1])[e / 2] = v;   // copied to the peers below
         const float ha = bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu));
         const float hb = bf16_bits_to_float(static_cast<uint16_t>(v >> 16));
         ss = ha * ha + hb * hb;
@@ -629,8 +610,32 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     }
 #pragma unroll
     for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(kFull, ss, m);
-    if (lane < kCl) st_peer_f32(peer_addr(&S.ssq[rel & 1][rank][cw], static_cast<unsigned>(lane)), ss);
-    if (!cluster_consumer_barrier(p, S, static_cast<uint32_t>(rel - 1) & 1u)) return false;
+    if (lane == 0) S.ssq[rel & 1][rank][cw] = ss;
+    __syncwarp();
+    // lane r < 4 copies this warp's block of the new residual (up to 32 words,
+    // 16-byte aligned) and its sum of squares into CTA r of the cluster, then
+    // arrives there with release semantics (ordering its own stores: no fence)
+    if (lane < kCl) {
+      const unsigned r = static_cast<unsigned>(lane);
+      if (r != rank) {
+        const int w0 = cw * 32, nw = min(32, npair - w0);
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(S.h[rel & 1]) + static_cast<int>(rank) * (d / 8) + w0;
+        const uint32_t dst = peer_addr(src, r);
+        for (int i = 0; i < nw; i += 4) {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(src + i);
+          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 4 * i), "r"(v4.x), "r"(v4.y),
+                       "r"(v4.z), "r"(v4.w)
+                       : "memory");
+        }
+        st_peer_f32(peer_addr(&S.ssq[rel & 1][rank][cw], r), ss);
+      }
+      arrive_peer(peer_addr(&S.clbar, r));
+    }
+    __syncwarp();
+    if (!mbar_wait_cluster(&S.clbar, static_cast<uint32_t>(rel - 1) & 1u, p.err)) {
+      raise_abort(p);
+      return false;
+    }
     if (cw == 0 && lane == 0) stamp(p, rel, EV_PREP_B1);
     // every CTA has added into the previous layer's vector, so every CTA is
     // done reading the one before it: zero this CTA's share of it for layer rel + 1
@@ -804,19 +809,32 @@ __device__ void gu_push(const CParams& p, Smem& S, int rel, const CTask& t, unsi
     sh += __shfl_xor_sync(kFull, sh, m);
     sl += __shfl_xor_sync(kFull, sl, m);
   }
-  // lane = (destination rank, hi/lo column, t4): fragment word t4 of that
-  // column packs rows 2*t4 and 2*t4 + 1 (held by lanes 8*t4 and 8*t4 + 4)
-  const int dr = lane >> 3, par = (lane >> 2) & 1, t4w = lane & 3;
+  // word w = (hi/lo column, t4) = 4 * column + t4 packs rows 2*t4 and 2*t4 + 1
+  // of that column (held by lanes 8*t4 and 8*t4 + 4); lane w & 7 forms it
+  const int par = (lane >> 2) & 1, t4w = lane & 3;
   const uint32_t h0 = __shfl_sync(kFull, hi, 8 * t4w), h1 = __shfl_sync(kFull, hi, 8 * t4w + 4);
   const uint32_t l0 = __shfl_sync(kFull, lo, 8 * t4w), l1 = __shfl_sync(kFull, lo, 8 * t4w + 4);
   const uint32_t word = par ? (l0 | (l1 << 16)) : (h0 | (h1 << 16));
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = __shfl_sync(kFull, word, i);
+  // lane r < 4 writes this tile's eight words (one 32-byte block) and its sum
+  // into CTA r of the cluster, then arrives there with release semantics,
+  // which orders its own two stores before the arrival (no fence needed)
   const int aslot = (rel & 1) * kMaxU + t.ui;
-  const int wpos = ((par * 4 + t4w) * 4 + static_cast<int>(rank)) * 2 + t.tt;
-  st_peer_u32(peer_addr(&S.abuf[aslot][wpos], static_cast<unsigned>(dr)), word);
-  if (lane < kCl) st_peer_f32(peer_addr(&S.tsum[aslot][2 * rank + t.tt], static_cast<unsigned>(lane)), sh + sl);
-  fence_acq_rel_cluster();
+  if (lane < kCl) {
+    const unsigned r = static_cast<unsigned>(lane);
+    const uint32_t a = peer_addr(&S.abuf[aslot][(2 * rank + t.tt) * 8], r);
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3])
+                 : "memory");
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 16), "r"(w[4]), "r"(w[5]),
+                 "r"(w[6]), "r"(w[7])
+                 : "memory");
+    st_peer_f32(peer_addr(&S.tsum[aslot][2 * rank + t.tt], r), sh + sl);
+    arrive_peer(peer_addr(&S.a_full[aslot], r));
+  }
   __syncwarp();
-  if (lane < kCl) arrive_peer(peer_addr(&S.a_full[aslot], static_cast<unsigned>(lane)));
   if (lane == 0) stamp(p, rel, EV_PUSH_LAST, true);
 }
 
@@ -868,9 +886,11 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
   float As = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) As += S.tsum[aslot][i];
-  const uint4* bf = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(S.abuf[aslot]) +
-                                                   ((g & 1) * 4 + t4) * 32);
-  const uint4 b01 = bf[0], b23 = bf[1];
+  // B fragments of lane (g, t4): column g & 1 (hi / lo), k16 step st = sending
+  // rank, b0 / b1 = the rank's tiles 0 / 1
+  const uint32_t* ab = S.abuf[aslot] + (g & 1) * 4 + t4;
+  const uint4 b01 = make_uint4(ab[0], ab[8], ab[16], ab[24]);
+  const uint4 b23 = make_uint4(ab[32], ab[40], ab[48], ab[56]);
   const int R = p.d / 64;
   float* out = S.dn_part[t.ui];
 #pragma unroll 2
