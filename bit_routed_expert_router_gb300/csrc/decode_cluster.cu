@@ -358,6 +358,12 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
   bool stop = false;
   for (int rel = 0; rel < n_rel && !stop; ++rel) {
     const CLayer* L = p.layers + (p.l0 + rel);
+    // the layer's addresses once, before any wait, and its down tensor maps
+    // into the TMA unit's descriptor cache
+    const uint8_t* const Lsh = L->shared;
+    const uint8_t* const Lex = L->experts;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L->dn_shared)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L->dn_routed)) : "memory");
     if (static_cast<int>(blockIdx.x) < p.E) {
       if (!mbar_wait_bounded(&S.rrow_empty, (static_cast<uint32_t>(rel) & 1u) ^ 1u, p.err)) {
         raise_abort(p);
@@ -390,7 +396,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&S.full[slot], tile_bytes);
       if (t.kind == K_GU) {
-        const uint8_t* base = t.src < 0 ? L->shared : L->experts + static_cast<long long>(e) * p.expert_stride;
+        const uint8_t* base = t.src < 0 ? Lsh : Lex + static_cast<long long>(e) * p.expert_stride;
         const size_t tile = static_cast<size_t>(8 * t.G + 2 * static_cast<int>(rank) + t.tt);
         bulk_g2s(S.ring[slot], base + tile * tile_bytes, tile_bytes, &S.full[slot]);
       } else {
