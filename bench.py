@@ -793,6 +793,12 @@ def run_ours_pool(args):
                                    "misses_per_token": misses / n_tok, "staged_bytes_per_token": staged / n_tok,
                                    "host_link_gbs": staged / dt / 1e9}
     moe.moe_destroy(ctx)
+    file_tier = None
+    if args.file_dir:
+        try:
+            file_tier = file_tier_run(args, H, bias, out, stream)
+        except moe.MoeError as e:
+            file_tier = {"error": str(e), "dir": args.file_dir, "o_direct": bool(args.file_direct)}
     best = sweeps["lru"]["64"]
     line = {
         "metric": "MoE decode tokens/s with a per-layer LRU slot cache over a pinned host expert pool (30 layers)",
@@ -802,7 +808,7 @@ def run_ours_pool(args):
         "config": {"workload": "decode30_hostpool_lru_zipf", "layers": N_LAYERS, "B": 1, "slots_reported": 64,
                    "routing": "router logits + Zipf(1.1)/reuse-0.6 bias trace",
                    "timing": "host wall clock around the synchronised token loop (the host drives the staging)"},
-        "sweep_by_slots": sweeps["lru"], "sweep_by_slots_lfu": sweeps["lfu"],
+        "sweep_by_slots": sweeps["lru"], "sweep_by_slots_lfu": sweeps["lfu"], "file_tier": file_tier,
         "roofline": {"bound": "host link", "achieved": best["host_link_gbs"], "peak": None, "unit": "GB/s",
                      "frac": None, "traffic": None},
         "gpu_launches": None, "cpu_baseline": None,
@@ -810,6 +816,62 @@ def run_ours_pool(args):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def file_tier_run(args, H, bias, out, stream, n_slots=64):
+    """The same decode with the routed experts in an expert file instead of the
+    pinned pool (MOE_FILE_POOL: a miss is read by parallel pread into pinned
+    staging): tokens/s over --file-layers layers, the file reads' rate."""
+    import torch
+
+    import bit_routed_expert_router_gb300 as moe
+    from workload import gen_layer
+
+    sh = _shape()
+    L = args.file_layers
+    cfg = moe.make_config(sh.d, sh.f, sh.f_shared, sh.n_experts, sh.top_k, n_layers=L, prenorm=1, max_tokens=1)
+    st, ctx = moe.moe_create(cfg, torch.cuda.current_device())
+    if st != moe.MOE_OK:
+        raise moe.MoeError(st, moe.moe_last_error(None))
+    path = os.path.join(args.file_dir, f"moe_experts_{os.getpid()}.bin")
+    flags = moe.MOE_FILE_DIRECT if args.file_direct else 0
+    try:
+        moe.check(moe.moe_set_expert_file(ctx, path, args.file_threads, 0, flags), ctx)
+        t0 = time.perf_counter()
+        for layer in range(L):
+            w = gen_layer(sh, seed=SEED, layer=layer, device="cuda")
+            moe.check(moe.moe_init_layer(ctx, layer, w["router_w"], w["experts"], w["shared"], moe.MOE_FILE_POOL),
+                      ctx)
+            del w
+        init_s = time.perf_counter() - t0
+        moe.check(moe.moe_set_slots(ctx, n_slots), ctx)
+        for t in range(args.warmup):
+            moe.check(moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, L, bias[t, :L].contiguous(), out, None, None,
+                                          stream)[0], ctx)
+        moe.check(moe.moe_sync(ctx, stream), ctx)
+        _, s0 = moe.moe_get_stats(ctx)
+        n_tok = min(N_TOKENS, max(args.steps, 16))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n_tok):
+            t = (args.warmup + i) % N_TOKENS
+            moe.check(moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, L, bias[t, :L].contiguous(), out, None, None,
+                                          stream)[0], ctx)
+        moe.check(moe.moe_sync(ctx, stream), ctx)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        _, s1 = moe.moe_get_stats(ctx)
+        misses = s1.misses - s0.misses
+        read = (s1.staged_bytes - s0.staged_bytes)
+        return {"layers": L, "slots": n_slots, "tokens_per_s": n_tok / dt, "us_per_layer": dt / n_tok / L * 1e6,
+                "misses_per_token": misses / n_tok, "file_read_gbs": read / dt / 1e9,
+                "threads": args.file_threads, "o_direct": bool(args.file_direct), "dir": args.file_dir,
+                "file_bytes": L * sh.n_experts * ((s1.expert_bytes + 4095) // 4096 * 4096),
+                "init_write_s": init_s}
+    finally:
+        moe.moe_destroy(ctx)
+        if os.path.exists(path):
+            os.remove(path)
 
 
 def main(argv=None):
@@ -825,6 +887,11 @@ def main(argv=None):
                          "step; batched: B=32 tokens per step; pool: host expert pool + LRU slot sweep")
     ap.add_argument("--layers", type=int, default=30,
                     help="layers in the stack (30 is the benchmark; fewer only for small profiler captures)")
+    ap.add_argument("--file-dir", default=None,
+                    help="pool: also time the expert file tier with its file in this directory")
+    ap.add_argument("--file-layers", type=int, default=30, help="pool: layers of the file-tier run")
+    ap.add_argument("--file-threads", type=int, default=8, help="pool: pread threads of the file-tier run")
+    ap.add_argument("--file-direct", action="store_true", help="pool: file-tier reads with O_DIRECT")
     ap.add_argument("--timeline", action="store_true",
                     help="decode: print the clustered kernel's per-CTA event timeline of one layer instead of timing")
     args = ap.parse_args(argv)

@@ -15,8 +15,9 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
 
-MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTATE, MOE_ETIMEOUT, MOE_EDOMAIN = range(7)
-MOE_RESIDENT_HBM, MOE_HOST_POOL = 0, 1
+MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTATE, MOE_ETIMEOUT, MOE_EDOMAIN, MOE_EIO = range(8)
+MOE_RESIDENT_HBM, MOE_HOST_POOL, MOE_FILE_POOL = 0, 1, 2
+MOE_FILE_DIRECT = 1
 MOE_CACHE_LRU, MOE_CACHE_LFU = 0, 1
 MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
 HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6
@@ -71,6 +72,8 @@ _SIGS = {
                                  C.POINTER(MoeExpertWeights), C.c_int]),
     "moe_set_slots": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_set_cache_policy": (C.c_int, [C.c_void_p, C.c_int]),
+    "moe_set_expert_file": (C.c_int, [C.c_void_p, C.c_char_p, C.c_int, C.c_uint64, C.c_int]),
+    "moe_pread_parallel": (C.c_int, [C.c_char_p, C.c_uint64, C.c_uint64, C.c_void_p, C.c_int, C.c_uint64]),
     "moe_decode_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                                   C.c_void_p, C.POINTER(MoeTraceRec), C.c_int, C.POINTER(C.c_int),
                                   C.c_void_p]),
@@ -183,6 +186,18 @@ def moe_set_slots(ctx, n_slots: int) -> int:
 
 def moe_set_cache_policy(ctx, policy: int) -> int:
     return lib().moe_set_cache_policy(ctx, policy)
+
+
+def moe_set_expert_file(ctx, path, n_threads: int = 8, chunk_bytes: int = 0, flags: int = 0) -> int:
+    return lib().moe_set_expert_file(ctx, None if path is None else os.fsencode(path), n_threads, chunk_bytes,
+                                     flags)
+
+
+def moe_pread_parallel(path, offset: int, nbytes: int, dst, n_threads: int = 8, chunk_bytes: int = 0) -> int:
+    """Read [offset, offset + nbytes) of `path` into `dst` (a writable buffer:
+    a numpy array or a pinned host tensor)."""
+    return lib().moe_pread_parallel(None if path is None else os.fsencode(path), offset, nbytes, _ptr(dst),
+                                    n_threads, chunk_bytes)
 
 
 def moe_decode_step(ctx, h_in, B: int, layer_begin: int, layer_end: int, logit_bias=None, h_out=None,

@@ -7,6 +7,7 @@
 #include "moe.h"
 
 #include <chrono>
+#include <cerrno>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -15,6 +16,14 @@
 #include <thread>
 #include <tuple>
 #include <vector>
+
+#ifndef _GNU_SOURCE
+#define _GNU_SOURCE
+#endif
+#include <fcntl.h>
+#include <unistd.h>
+
+#include "expert_file.h"
 
 #include <cudaTypedefs.h>
 
@@ -64,6 +73,16 @@ struct moe_ctx {
   std::vector<LayerStore> L;
   uint8_t* pool = nullptr;
   size_t pool_bytes = 0;
+  // expert file tier (MOE_FILE_POOL contexts)
+  int file_fd = -1;
+  int file_rfd = -1;                     // O_DIRECT read descriptor (MOE_FILE_DIRECT), else -1
+  FilePool* fpool = nullptr;
+  uint64_t file_chunk = 512u << 10;
+  size_t file_stride = 0;                // bytes between records (expert device bytes rounded up to 4096)
+  uint8_t* fstage = nullptr;             // pinned [2][top_k][file_stride] staging records
+  cudaEvent_t fev[2] = {nullptr, nullptr};   // copies out of each staging half done
+  int fhalf = 0;
+  long long file_read_bytes = 0, file_read_us = 0;
   std::vector<void*> owned;           // scratch allocations
   size_t device_bytes = 0;
   // scratch
@@ -171,7 +190,7 @@ moe_status fail(moe_ctx* c, moe_status s, const char* fmt, ...) {
   va_end(ap);
   if (c) {
     c->err = buf;
-    if (s == MOE_ECUDA || s == MOE_ETIMEOUT) c->poisoned = true;
+    if (s == MOE_ECUDA || s == MOE_ETIMEOUT || s == MOE_EIO) c->poisoned = true;
   }
   return s;
 }
@@ -253,7 +272,7 @@ KParams base_params(moe_ctx* ctx, int layer, int rel, int first, int last, int B
   p.rel_layer = rel;
   p.first = first;
   p.last = last;
-  p.pool = ctx->residency == MOE_HOST_POOL;
+  p.pool = ctx->residency == MOE_HOST_POOL || ctx->residency == MOE_FILE_POOL;
   p.pass = -1;
   p.n_slots = ctx->n_slots;
   const LayerStore& Ls = ctx->L[layer];
@@ -584,6 +603,12 @@ moe_status pool_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec*
     const int n_miss = rec[0];
     if (n_miss < 0 || n_miss > k) return fail(ctx, MOE_ECUDA, "corrupt miss record (%d)", n_miss);
     const LayerStore& Ls = ctx->L[l];
+    const bool from_file = ctx->file_fd >= 0;
+    const int half = ctx->fhalf;
+    if (from_file && n_miss > 0) {
+      // the copies out of this staging half two layers ago must be done before it is refilled
+      CK(cudaEventSynchronize(ctx->fev[half]));
+    }
     for (int m = 0; m < n_miss; ++m) {
       const int ex = rec[1 + 2 * m], slot = rec[2 + 2 * m];
       if (ex < 0 || ex >= ctx->cfg.n_experts || slot < 0 || slot >= ctx->n_slots)
@@ -592,10 +617,29 @@ moe_status pool_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec*
         ctx->hook_fail_copy = false;
         return fail(ctx, MOE_ECUDA, "staging copy failed (injected by test hook)");
       }
-      const uint8_t* src = ctx->pool + (static_cast<size_t>(l) * ctx->cfg.n_experts + ex) * ctx->stride;
+      const uint8_t* src;
+      if (from_file) {
+        uint8_t* dst = ctx->fstage + (static_cast<size_t>(half) * k + m) * ctx->file_stride;
+        const uint64_t off = (static_cast<uint64_t>(l) * ctx->cfg.n_experts + ex) * ctx->file_stride;
+        const long long t0 = now_us();
+        // O_DIRECT reads whole 4096-byte-aligned records into the page-aligned staging
+        const bool direct = ctx->file_rfd >= 0;
+        const int e = file_pool_transfer(ctx->fpool, direct ? ctx->file_rfd : ctx->file_fd, false, off, dst,
+                                         direct ? ctx->file_stride : ctx->expert_bytes, ctx->file_chunk);
+        ctx->file_read_us += now_us() - t0;
+        if (e != 0) return fail(ctx, MOE_EIO, "expert file read (layer %d, expert %d): %s", l, ex, strerror(e));
+        ctx->file_read_bytes += ctx->expert_bytes;
+        src = dst;
+      } else {
+        src = ctx->pool + (static_cast<size_t>(l) * ctx->cfg.n_experts + ex) * ctx->stride;
+      }
       CK(cudaMemcpyAsync(Ls.slots + static_cast<size_t>(slot) * ctx->stride, src, ctx->expert_bytes,
                          cudaMemcpyHostToDevice, ctx->side));
       ctx->staged += ctx->expert_bytes;
+    }
+    if (from_file && n_miss > 0) {
+      CK(cudaEventRecord(ctx->fev[half], ctx->side));
+      ctx->fhalf ^= 1;
     }
     CK(cudaEventRecord(ctx->ev_copy, ctx->side));
     CK(cudaStreamWaitEvent(s, ctx->ev_copy, 0));
@@ -637,6 +681,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ESTATE: return "MOE_ESTATE";
     case MOE_ETIMEOUT: return "MOE_ETIMEOUT";
     case MOE_EDOMAIN: return "MOE_EDOMAIN";
+    case MOE_EIO: return "MOE_EIO";
   }
   return "unknown";
 }
@@ -843,6 +888,12 @@ void moe_destroy(moe_ctx* ctx) {
   for (void* p : ctx->owned) cudaFree(p);
   for (void* p : ctx->pf_owned) cudaFree(p);
   if (ctx->pool) cudaFreeHost(ctx->pool);
+  if (ctx->fpool) file_pool_destroy(ctx->fpool);
+  if (ctx->file_fd >= 0) ::close(ctx->file_fd);
+  if (ctx->file_rfd >= 0) ::close(ctx->file_rfd);
+  if (ctx->fstage) cudaFreeHost(ctx->fstage);
+  for (auto& e : ctx->fev)
+    if (e) cudaEventDestroy(e);
   if (ctx->args_ring) cudaFreeHost(ctx->args_ring);
   if (ctx->host_rec) cudaFreeHost(ctx->host_rec);
   for (auto& e : ctx->ring_ev)
@@ -861,8 +912,10 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
   if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
   const moe_config& c = ctx->cfg;
   if (layer < 0 || layer >= c.n_layers) return fail(ctx, MOE_EINVAL, "layer %d out of range", layer);
-  if (residency != MOE_RESIDENT_HBM && residency != MOE_HOST_POOL)
+  if (residency != MOE_RESIDENT_HBM && residency != MOE_HOST_POOL && residency != MOE_FILE_POOL)
     return fail(ctx, MOE_EINVAL, "unknown residency %d", residency);
+  if (residency == MOE_FILE_POOL && ctx->file_fd < 0)
+    return fail(ctx, MOE_ESTATE, "MOE_FILE_POOL needs moe_set_expert_file first");
   if (ctx->residency >= 0 && residency != ctx->residency)
     return fail(ctx, MOE_EINVAL, "all layers of a context must use the same residency");
   if (!router_w || !experts || !shared) return fail(ctx, MOE_EINVAL, "NULL weights");
@@ -873,7 +926,8 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
   }
   CK(cudaSetDevice(ctx->device));
   LayerStore& Ls = ctx->L[layer];
-  const bool pool = residency == MOE_HOST_POOL;
+  const bool pool = residency == MOE_HOST_POOL || residency == MOE_FILE_POOL;
+  const bool file = residency == MOE_FILE_POOL;
   // memory budget before allocating
   size_t free_b = 0;
   CK(free_device_bytes(ctx, &free_b));
@@ -882,7 +936,7 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
   need += static_cast<size_t>(c.n_experts) * ctx->stride;  // resident experts or the staging buffer
   if (!Ls.ready && need + (256u << 20) > free_b)
     return fail(ctx, MOE_ENOMEM, "layer needs %zu bytes, %zu free", need, free_b);
-  if (pool && !ctx->pool) {
+  if (pool && !file && !ctx->pool) {
     const size_t pb = static_cast<size_t>(c.n_layers) * c.n_experts * ctx->stride;
     if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->pool), pb, cudaHostAllocDefault) != cudaSuccess) {
       ctx->pool = nullptr;
@@ -939,12 +993,24 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
     e = stage(experts[ex], c.f, dst);
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  if (e == cudaSuccess && pool)
+  if (e == cudaSuccess && pool && !file)
     e = cudaMemcpy(ctx->pool + static_cast<size_t>(layer) * c.n_experts * ctx->stride, tmp,
                    static_cast<size_t>(c.n_experts) * ctx->stride, cudaMemcpyDeviceToHost);
+  int io_err = 0;
+  if (e == cudaSuccess && file) {
+    // the layer's records, through a host bounce buffer, written in parallel chunks
+    std::vector<uint8_t> host(static_cast<size_t>(c.n_experts) * ctx->stride);
+    e = cudaMemcpy(host.data(), tmp, host.size(), cudaMemcpyDeviceToHost);
+    for (int ex = 0; ex < c.n_experts && e == cudaSuccess && io_err == 0; ++ex)
+      io_err = file_pool_transfer(ctx->fpool, ctx->file_fd, true,
+                                  (static_cast<uint64_t>(layer) * c.n_experts + ex) * ctx->file_stride,
+                                  host.data() + static_cast<size_t>(ex) * ctx->stride, ctx->expert_bytes,
+                                  ctx->file_chunk);
+  }
   cudaFree(can);
   if (tmp) cudaFree(tmp);
   if (e != cudaSuccess) return fail(ctx, MOE_ECUDA, "init_layer %d: %s", layer, cudaGetErrorString(e));
+  if (io_err != 0) return fail(ctx, MOE_EIO, "init_layer %d: expert file write: %s", layer, strerror(io_err));
   if (pool && ctx->n_slots > 0 && Ls.slot_of_expert) CK(cudaMemset(Ls.slot_of_expert, 0xFF, c.n_experts * 4));
   PLayer pl{Ls.router_w, Ls.shared, Ls.experts};
   CK(cudaMemcpy(ctx->p_layers + layer, &pl, sizeof(PLayer), cudaMemcpyHostToDevice));
@@ -968,7 +1034,8 @@ moe_status moe_set_slots(moe_ctx* ctx, int n_slots) {
   if (!ctx) return MOE_EINVAL;
   if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
   const moe_config& c = ctx->cfg;
-  if (ctx->residency != MOE_HOST_POOL) return fail(ctx, MOE_ESTATE, "slots need a host-pool context");
+  if (ctx->residency != MOE_HOST_POOL && ctx->residency != MOE_FILE_POOL)
+    return fail(ctx, MOE_ESTATE, "slots need a host-pool or file-pool context");
   if (n_slots < c.top_k || n_slots > c.n_experts)
     return fail(ctx, MOE_EINVAL, "n_slots %d outside [top_k=%d, n_experts=%d]", n_slots, c.top_k, c.n_experts);
   CK(cudaSetDevice(ctx->device));
@@ -1007,9 +1074,57 @@ moe_status moe_set_cache_policy(moe_ctx* ctx, int policy) {
   if (!ctx) return MOE_EINVAL;
   if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
   if (policy != MOE_CACHE_LRU && policy != MOE_CACHE_LFU) return fail(ctx, MOE_EINVAL, "unknown policy %d", policy);
-  if (ctx->residency != MOE_HOST_POOL) return fail(ctx, MOE_ESTATE, "cache policy needs a host-pool context");
+  if (ctx->residency != MOE_HOST_POOL && ctx->residency != MOE_FILE_POOL)
+    return fail(ctx, MOE_ESTATE, "cache policy needs a host-pool or file-pool context");
   ctx->policy = policy;
   return moe_reset_cache(ctx);
+}
+
+moe_status moe_set_expert_file(moe_ctx* ctx, const char* path, int n_threads, uint64_t chunk_bytes, int flags) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  if (!path || n_threads < 1 || n_threads > 64 || chunk_bytes % 4096 != 0 || (flags & ~MOE_FILE_DIRECT))
+    return fail(ctx, MOE_EINVAL, "bad expert file arguments");
+  if (ctx->residency >= 0 || ctx->file_fd >= 0)
+    return fail(ctx, MOE_EINVAL, "the expert file must be set before any layer is initialised, once");
+  const int fd = ::open(path, O_RDWR | O_CREAT | O_TRUNC, 0644);
+  if (fd < 0) return fail(ctx, MOE_EINVAL, "cannot create expert file %s: %s", path, strerror(errno));
+  int rfd = -1;
+  const size_t fstride_all = (ctx->expert_bytes + 4095) / 4096 * 4096;
+  if (flags & MOE_FILE_DIRECT) {
+    // whole records are read: the file spans every record in full (sparse tails)
+    rfd = ::open(path, O_RDONLY | O_DIRECT);
+    const off_t full = static_cast<off_t>(ctx->cfg.n_layers) * ctx->cfg.n_experts * static_cast<off_t>(fstride_all);
+    if (rfd < 0 || ::ftruncate(fd, full) != 0) {
+      const int e = errno;
+      if (rfd >= 0) ::close(rfd);
+      ::close(fd);
+      return fail(ctx, MOE_EINVAL, "O_DIRECT reads of %s refused: %s", path, strerror(e));
+    }
+  }
+  const size_t fstride = (ctx->expert_bytes + 4095) / 4096 * 4096;
+  uint8_t* stage = nullptr;
+  if (cudaHostAlloc(reinterpret_cast<void**>(&stage), 2 * static_cast<size_t>(ctx->cfg.top_k) * fstride,
+                    cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    ::close(fd);
+    if (rfd >= 0) ::close(rfd);
+    return fail(ctx, MOE_ENOMEM, "pinned staging for the expert file");
+  }
+  for (auto& ev : ctx->fev)
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+      cudaFreeHost(stage);
+      ::close(fd);
+      if (rfd >= 0) ::close(rfd);
+      return fail(ctx, MOE_ECUDA, "events for the expert file");
+    }
+  ctx->file_fd = fd;
+  ctx->file_rfd = rfd;
+  ctx->file_stride = fstride;
+  ctx->fstage = stage;
+  ctx->file_chunk = chunk_bytes == 0 ? (512u << 10) : chunk_bytes;
+  ctx->fpool = file_pool_create(n_threads);
+  return MOE_OK;
 }
 
 moe_status moe_reset_cache(moe_ctx* ctx) {
@@ -1042,7 +1157,7 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
   moe_status st = check_ready(ctx, layer_begin, layer_end);
   if (st != MOE_OK) return st;
   if (!h_in || !h_out) return fail(ctx, MOE_EINVAL, "NULL h_in / h_out");
-  const bool pool = ctx->residency == MOE_HOST_POOL;
+  const bool pool = ctx->residency == MOE_HOST_POOL || ctx->residency == MOE_FILE_POOL;
   if (B < 1 || B > ctx->Bd) return fail(ctx, MOE_EINVAL, "B=%d outside [1, %d]", B, ctx->Bd);
   if (pool && B != 1) return fail(ctx, MOE_EINVAL, "host-pool decode takes one token per call");
   if (pool && ctx->n_slots < ctx->cfg.top_k) return fail(ctx, MOE_ESTATE, "slots are not set");
@@ -1374,7 +1489,8 @@ moe_status moe_get_cache_state(moe_ctx* ctx, int layer, int32_t* expert_of_slot,
   if (!ctx) return MOE_EINVAL;
   if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
   if (layer < 0 || layer >= ctx->cfg.n_layers) return fail(ctx, MOE_EINVAL, "layer %d out of range", layer);
-  if (ctx->residency != MOE_HOST_POOL || ctx->n_slots == 0) return fail(ctx, MOE_ESTATE, "no slot cache");
+  if ((ctx->residency != MOE_HOST_POOL && ctx->residency != MOE_FILE_POOL) || ctx->n_slots == 0)
+    return fail(ctx, MOE_ESTATE, "no slot cache");
   CK(cudaSetDevice(ctx->device));
   CK(cudaDeviceSynchronize());
   if (expert_of_slot)

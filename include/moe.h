@@ -51,14 +51,17 @@ typedef enum {
     MOE_ESTATE = 4,   /* poisoned context, or a call in the wrong state (layer not initialised,
                          slots not set) */
     MOE_ETIMEOUT = 5, /* a bounded wait expired; the context is now poisoned */
-    MOE_EDOMAIN = 6   /* the device saw a value outside a documented domain: a router input
+    MOE_EDOMAIN = 6,  /* the device saw a value outside a documented domain: a router input
                          outside the exact fixed-point domain (|W_r[e,i] * x[i]| >= 2^11 or
                          non-finite), an fp16 matrix operand outside [-65504, 65504] (prefill
                          and the clustered one-token kernel), or a clustered-kernel partial
                          layer output with |y| >= 2^17; reported by moe_sync */
+    MOE_EIO = 7       /* a read or write of the expert file failed or came up short; the
+                         context (if any) is now poisoned */
 } moe_status;
 
-enum { MOE_RESIDENT_HBM = 0, MOE_HOST_POOL = 1 };
+enum { MOE_RESIDENT_HBM = 0, MOE_HOST_POOL = 1, MOE_FILE_POOL = 2 };
+enum { MOE_FILE_DIRECT = 1 };   /* moe_set_expert_file flag: read misses with O_DIRECT */
 enum { MOE_CACHE_LRU = 0, MOE_CACHE_LFU = 1 };
 enum { MOE_GELU_ERF = 0, MOE_GELU_TANH = 1 };
 
@@ -231,6 +234,38 @@ moe_status moe_reset_cache(moe_ctx *ctx);
  * touched.  MOE_EINVAL for an unknown policy, MOE_ESTATE for a resident
  * context. */
 moe_status moe_set_cache_policy(moe_ctx *ctx, int policy);
+
+/* Expert file tier ("Optimizing a 14.3 GB model for an 8 GB machine", section
+ * "Explicit reads made expert streaming work": routed experts are read from
+ * the model file on a miss with a bounded number of parallel pread calls into
+ * per-layer slots, instead of being mapped and paged in).  Call before the
+ * first moe_init_layer of a context whose layers use residency
+ * MOE_FILE_POOL: `path` is created (or truncated); moe_init_layer then writes
+ * each routed expert of the layer, in the device layout, to the record at
+ * byte offset (layer * n_experts + expert) * record_stride (record_stride =
+ * the expert's device bytes rounded up to 4096) instead of keeping it in a
+ * pinned host pool.  Such a context behaves like a MOE_HOST_POOL context
+ * (moe_set_slots, moe_set_cache_policy, traces, one token per decode call)
+ * except that a miss is read from the file by `n_threads` (1..64) host
+ * threads in chunks of `chunk_bytes` (0 = 512 KiB; multiple of 4096) into
+ * pinned staging memory (2 * top_k records, owned by the library), from which
+ * the staging copy to the slot is issued.  The host pool's bytes are 0.
+ * flags: MOE_FILE_DIRECT reads whole records through a second descriptor
+ * opened with O_DIRECT (past the page cache; MOE_EINVAL where the file system
+ * refuses it), else 0.
+ * Errors: MOE_EINVAL (NULL path, bad counts, layers already initialised, or
+ * the file cannot be created), MOE_ENOMEM (staging memory), MOE_EIO later
+ * (a record read or write that fails or comes up short). */
+moe_status moe_set_expert_file(moe_ctx *ctx, const char *path, int n_threads, uint64_t chunk_bytes, int flags);
+
+/* Reads bytes [offset, offset + bytes) of the file at `path` into host
+ * memory `dst` with `n_threads` (1..64) threads taking chunks of
+ * `chunk_bytes` (0 = one chunk), restarting short reads: the expert file
+ * tier's read engine on its own.  No context, no GPU.  MOE_EINVAL for bad
+ * arguments or a file that cannot be opened, MOE_EIO for a failed or short
+ * read (past the end of the file). */
+moe_status moe_pread_parallel(const char *path, uint64_t offset, uint64_t bytes, void *dst, int n_threads,
+                              uint64_t chunk_bytes);
 
 /* Bytes of one routed expert / of the shared expert for a config (0 on a bad config). */
 int64_t moe_expert_bytes(const moe_config *cfg);
