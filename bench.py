@@ -76,23 +76,35 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def load_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if still current."""
+# The sources that decide each captured kernel's DRAM traffic: its translation
+# unit and the headers it includes (the launch shape lives in kernels.h).
+TRAFFIC_SOURCES = {
+    "decode_persistent": ("decode_cluster.cu", "common.cuh", "internal.h", "kernels.h"),
+}
+
+
+def traffic_digest(names):
     import hashlib
+    src = os.path.join(ROOT, "bit_routed_expert_router_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(names):
+        with open(os.path.join(src, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, for each kernel whose
+    sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     out = {}
     if not os.path.exists(path):
         return out
-    src = os.path.join(ROOT, "bit_routed_expert_router_gb300", "csrc")
-    h = hashlib.sha256()
-    for name in sorted(os.listdir(src)):
-        with open(os.path.join(src, name), "rb") as fh:
-            h.update(fh.read())
-    digest = h.hexdigest()[:16]
     with open(path) as fh:
         for line in fh:
             parts = line.split()
-            if len(parts) == 3 and not line.startswith("#") and parts[2] == digest:
+            if len(parts) == 3 and not line.startswith("#") and parts[0] in TRAFFIC_SOURCES \
+                    and parts[2] == traffic_digest(TRAFFIC_SOURCES[parts[0]]):
                 out[parts[0]] = float(parts[1])
     return out
 
@@ -795,10 +807,13 @@ def run_ours_pool(args):
     moe.moe_destroy(ctx)
     file_tier = None
     if args.file_dir:
-        try:
-            file_tier = file_tier_run(args, H, bias, out, stream)
-        except moe.MoeError as e:
-            file_tier = {"error": str(e), "dir": args.file_dir, "o_direct": bool(args.file_direct)}
+        file_tier = {}
+        for direct in ((False, True) if args.file_direct else (False,)):
+            try:
+                r = file_tier_run(args, H, bias, out, stream, direct)
+            except moe.MoeError as e:
+                r = {"error": str(e), "dir": args.file_dir}
+            file_tier["o_direct" if direct else "buffered"] = r
     best = sweeps["lru"]["64"]
     line = {
         "metric": "MoE decode tokens/s with a per-layer LRU slot cache over a pinned host expert pool (30 layers)",
@@ -818,10 +833,12 @@ def run_ours_pool(args):
     return 0
 
 
-def file_tier_run(args, H, bias, out, stream, n_slots=64):
+def file_tier_run(args, H, bias, out, stream, direct, n_slots=64):
     """The same decode with the routed experts in an expert file instead of the
     pinned pool (MOE_FILE_POOL: a miss is read by parallel pread into pinned
-    staging): tokens/s over --file-layers layers, the file reads' rate."""
+    staging): tokens/s over --file-layers layers, the file reads' rate.  Without
+    O_DIRECT the reads are served from the page cache the file was just written
+    through; with it they go to the device under the file."""
     import torch
 
     import bit_routed_expert_router_gb300 as moe
@@ -834,7 +851,7 @@ def file_tier_run(args, H, bias, out, stream, n_slots=64):
     if st != moe.MOE_OK:
         raise moe.MoeError(st, moe.moe_last_error(None))
     path = os.path.join(args.file_dir, f"moe_experts_{os.getpid()}.bin")
-    flags = moe.MOE_FILE_DIRECT if args.file_direct else 0
+    flags = moe.MOE_FILE_DIRECT if direct else 0
     try:
         moe.check(moe.moe_set_expert_file(ctx, path, args.file_threads, 0, flags), ctx)
         t0 = time.perf_counter()
@@ -865,7 +882,7 @@ def file_tier_run(args, H, bias, out, stream, n_slots=64):
         read = (s1.staged_bytes - s0.staged_bytes)
         return {"layers": L, "slots": n_slots, "tokens_per_s": n_tok / dt, "us_per_layer": dt / n_tok / L * 1e6,
                 "misses_per_token": misses / n_tok, "file_read_gbs": read / dt / 1e9,
-                "threads": args.file_threads, "o_direct": bool(args.file_direct), "dir": args.file_dir,
+                "threads": args.file_threads, "dir": args.file_dir,
                 "file_bytes": L * sh.n_experts * ((s1.expert_bytes + 4095) // 4096 * 4096),
                 "init_write_s": init_s}
     finally:
@@ -891,7 +908,7 @@ def main(argv=None):
                     help="pool: also time the expert file tier with its file in this directory")
     ap.add_argument("--file-layers", type=int, default=30, help="pool: layers of the file-tier run")
     ap.add_argument("--file-threads", type=int, default=8, help="pool: pread threads of the file-tier run")
-    ap.add_argument("--file-direct", action="store_true", help="pool: file-tier reads with O_DIRECT")
+    ap.add_argument("--file-direct", action="store_true", help="pool: time the file tier with O_DIRECT reads too")
     ap.add_argument("--timeline", action="store_true",
                     help="decode: print the clustered kernel's per-CTA event timeline of one layer instead of timing")
     args = ap.parse_args(argv)

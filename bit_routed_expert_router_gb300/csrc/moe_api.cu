@@ -1090,11 +1090,11 @@ moe_status moe_set_expert_file(moe_ctx* ctx, const char* path, int n_threads, ui
   const int fd = ::open(path, O_RDWR | O_CREAT | O_TRUNC, 0644);
   if (fd < 0) return fail(ctx, MOE_EINVAL, "cannot create expert file %s: %s", path, strerror(errno));
   int rfd = -1;
-  const size_t fstride_all = (ctx->expert_bytes + 4095) / 4096 * 4096;
+  const size_t fstride = (ctx->expert_bytes + 4095) / 4096 * 4096;
   if (flags & MOE_FILE_DIRECT) {
     // whole records are read: the file spans every record in full (sparse tails)
     rfd = ::open(path, O_RDONLY | O_DIRECT);
-    const off_t full = static_cast<off_t>(ctx->cfg.n_layers) * ctx->cfg.n_experts * static_cast<off_t>(fstride_all);
+    const off_t full = static_cast<off_t>(ctx->cfg.n_layers) * ctx->cfg.n_experts * static_cast<off_t>(fstride);
     if (rfd < 0 || ::ftruncate(fd, full) != 0) {
       const int e = errno;
       if (rfd >= 0) ::close(rfd);
@@ -1102,7 +1102,6 @@ moe_status moe_set_expert_file(moe_ctx* ctx, const char* path, int n_threads, ui
       return fail(ctx, MOE_EINVAL, "O_DIRECT reads of %s refused: %s", path, strerror(e));
     }
   }
-  const size_t fstride = (ctx->expert_bytes + 4095) / 4096 * 4096;
   uint8_t* stage = nullptr;
   if (cudaHostAlloc(reinterpret_cast<void**>(&stage), 2 * static_cast<size_t>(ctx->cfg.top_k) * fstride,
                     cudaHostAllocDefault) != cudaSuccess) {

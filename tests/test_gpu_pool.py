@@ -7,7 +7,6 @@ misses are staged from the pinned pool; outputs do not depend on the slot
 count; host-side failures (argument errors, budget, a failed staging copy, a
 timed-out wait) are reported and poison the context as documented."""
 
-import ctypes as C
 import json
 import os
 
@@ -319,8 +318,8 @@ def _file_run(shape, L, ws, H, n_slots, path=None):
             ys.append(y.clone())
             trs.append(tr)
         ctx.sync()
-        st = moe.MoeStats()
-        moe.check(moe.moe_get_stats(ctx.h, C.byref(st)), ctx.h)
+        status, st = moe.moe_get_stats(ctx.h)
+        moe.check(status, ctx.h)
         return torch.cat(ys), trs, st
 
 
