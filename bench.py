@@ -808,12 +808,16 @@ def run_ours_pool(args):
     file_tier = None
     if args.file_dir:
         file_tier = {}
-        for direct in ((False, True) if args.file_direct else (False,)):
+        runs = [("buffered", False, 64, 0)]
+        if args.file_direct:
+            runs += [("o_direct", True, 64, 0), ("o_direct_slots16", True, 16, 0),
+                     ("o_direct_slots16_host64", True, 16, 64)]
+        for name, direct, n_slots, n_host in runs:
             try:
-                r = file_tier_run(args, H, bias, out, stream, direct)
+                r = file_tier_run(args, H, bias, out, stream, direct, n_slots, n_host)
             except moe.MoeError as e:
                 r = {"error": str(e), "dir": args.file_dir}
-            file_tier["o_direct" if direct else "buffered"] = r
+            file_tier[name] = r
     best = sweeps["lru"]["64"]
     line = {
         "metric": "MoE decode tokens/s with a per-layer LRU slot cache over a pinned host expert pool (30 layers)",
@@ -833,12 +837,13 @@ def run_ours_pool(args):
     return 0
 
 
-def file_tier_run(args, H, bias, out, stream, direct, n_slots=64):
+def file_tier_run(args, H, bias, out, stream, direct, n_slots, n_host):
     """The same decode with the routed experts in an expert file instead of the
     pinned pool (MOE_FILE_POOL: a miss is read by parallel pread into pinned
-    staging): tokens/s over --file-layers layers, the file reads' rate.  Without
-    O_DIRECT the reads are served from the page cache the file was just written
-    through; with it they go to the device under the file."""
+    staging, or, with n_host > 0, served from / read into a pinned host tier of
+    n_host records per layer): tokens/s over --file-layers layers, the file
+    reads' rate.  Without O_DIRECT the reads are served from the page cache the
+    file was just written through; with it they go to the device under the file."""
     import torch
 
     import bit_routed_expert_router_gb300 as moe
@@ -861,6 +866,8 @@ def file_tier_run(args, H, bias, out, stream, direct, n_slots=64):
                       ctx)
             del w
         init_s = time.perf_counter() - t0
+        if n_host:
+            moe.check(moe.moe_set_file_cache(ctx, n_host), ctx)
         moe.check(moe.moe_set_slots(ctx, n_slots), ctx)
         for t in range(args.warmup):
             moe.check(moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, L, bias[t, :L].contiguous(), out, None, None,
@@ -879,9 +886,11 @@ def file_tier_run(args, H, bias, out, stream, direct, n_slots=64):
         dt = time.perf_counter() - t0
         _, s1 = moe.moe_get_stats(ctx)
         misses = s1.misses - s0.misses
-        read = (s1.staged_bytes - s0.staged_bytes)
-        return {"layers": L, "slots": n_slots, "tokens_per_s": n_tok / dt, "us_per_layer": dt / n_tok / L * 1e6,
-                "misses_per_token": misses / n_tok, "file_read_gbs": read / dt / 1e9,
+        read = s1.file_read_bytes - s0.file_read_bytes
+        return {"layers": L, "slots": n_slots, "host_records": n_host, "tokens_per_s": n_tok / dt,
+                "us_per_layer": dt / n_tok / L * 1e6, "misses_per_token": misses / n_tok,
+                "host_tier_hits_per_token": (s1.host_tier_hits - s0.host_tier_hits) / n_tok,
+                "file_reads_per_token": read / s1.expert_bytes / n_tok, "file_read_gbs": read / dt / 1e9,
                 "threads": args.file_threads, "dir": args.file_dir,
                 "file_bytes": L * sh.n_experts * ((s1.expert_bytes + 4095) // 4096 * 4096),
                 "init_write_s": init_s}

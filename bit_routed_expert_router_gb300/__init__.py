@@ -45,7 +45,8 @@ class MoeTraceRec(C.Structure):
 class MoeStats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("steps", "hits", "misses", "staged_bytes", "n_slots",
                                           "expert_bytes", "shared_bytes", "device_bytes",
-                                          "host_pool_bytes")]
+                                          "host_pool_bytes", "file_read_bytes", "host_tier_hits",
+                                          "host_tier_bytes")]
 
 
 class MoeKernelTime(C.Structure):
@@ -73,6 +74,7 @@ _SIGS = {
     "moe_set_slots": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_set_cache_policy": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_set_expert_file": (C.c_int, [C.c_void_p, C.c_char_p, C.c_int, C.c_uint64, C.c_int]),
+    "moe_set_file_cache": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_pread_parallel": (C.c_int, [C.c_char_p, C.c_uint64, C.c_uint64, C.c_void_p, C.c_int, C.c_uint64]),
     "moe_decode_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                                   C.c_void_p, C.POINTER(MoeTraceRec), C.c_int, C.POINTER(C.c_int),
@@ -191,6 +193,10 @@ def moe_set_cache_policy(ctx, policy: int) -> int:
 def moe_set_expert_file(ctx, path, n_threads: int = 8, chunk_bytes: int = 0, flags: int = 0) -> int:
     return lib().moe_set_expert_file(ctx, None if path is None else os.fsencode(path), n_threads, chunk_bytes,
                                      flags)
+
+
+def moe_set_file_cache(ctx, n_host: int) -> int:
+    return lib().moe_set_file_cache(ctx, n_host)
 
 
 def moe_pread_parallel(path, offset: int, nbytes: int, dst, n_threads: int = 8, chunk_bytes: int = 0) -> int:

@@ -83,6 +83,18 @@ struct moe_ctx {
   cudaEvent_t fev[2] = {nullptr, nullptr};   // copies out of each staging half done
   int fhalf = 0;
   long long file_read_bytes = 0, file_read_us = 0;
+  // host tier in front of the expert file (moe_set_file_cache): per layer n_host
+  // pinned records with an LRU table; a miss of the slot cache that the host
+  // tier holds is copied from it, any other is read from the file into it
+  int n_host = 0;
+  uint8_t* hcache = nullptr;             // pinned [n_layers][n_host][file_stride]
+  std::vector<int32_t> h_expert_of_slot; // [n_layers][n_host], -1 = empty
+  std::vector<long long> h_last_use;     // [n_layers][n_host], -1 = empty
+  std::vector<int32_t> h_slot_of_expert; // [n_layers][n_experts], -1 = not held
+  std::vector<char> h_touched;           // [n_host] scratch of one step
+  const uint8_t* h_src[32] = {};         // source record of each miss of the current layer
+  cudaEvent_t hev = nullptr;             // every copy out of the host tier issued so far is done
+  long long host_hits = 0;
   std::vector<void*> owned;           // scratch allocations
   size_t device_bytes = 0;
   // scratch
@@ -582,6 +594,80 @@ moe_status resident_run(moe_ctx* ctx, int B, int l0, int l1, cudaStream_t s) {
   return MOE_OK;
 }
 
+// One read of expert `ex` of layer `l` from the expert file into `dst` (pinned,
+// 4096-byte aligned, file_stride bytes).
+moe_status file_read_record(moe_ctx* ctx, int l, int ex, uint8_t* dst) {
+  const uint64_t off = (static_cast<uint64_t>(l) * ctx->cfg.n_experts + ex) * ctx->file_stride;
+  const long long t0 = now_us();
+  // O_DIRECT reads whole 4096-byte-aligned records
+  const bool direct = ctx->file_rfd >= 0;
+  const int e = file_pool_transfer(ctx->fpool, direct ? ctx->file_rfd : ctx->file_fd, false, off, dst,
+                                   direct ? ctx->file_stride : ctx->expert_bytes, ctx->file_chunk);
+  ctx->file_read_us += now_us() - t0;
+  if (e != 0) return fail(ctx, MOE_EIO, "expert file read (layer %d, expert %d): %s", l, ex, strerror(e));
+  ctx->file_read_bytes += ctx->expert_bytes;
+  return MOE_OK;
+}
+
+// The host tier's step for the slot-cache misses of layer `l` (rec: the miss
+// record, n_miss >= 1), with the slot cache's LRU rules one level down: the
+// misses it holds refresh their record (last use = the step counter); the
+// others, in top-k order, each take the record with the smallest (last use,
+// index) among those this step has not touched (empty ones first) and are read
+// from the file into it.  Sets h_src[m] to each miss's source record.
+moe_status host_tier_step(moe_ctx* ctx, int l, const volatile int32_t* rec, int n_miss) {
+  const int H = ctx->n_host;
+  int32_t* eos = ctx->h_expert_of_slot.data() + static_cast<size_t>(l) * H;
+  long long* lu = ctx->h_last_use.data() + static_cast<size_t>(l) * H;
+  int32_t* soe = ctx->h_slot_of_expert.data() + static_cast<size_t>(l) * ctx->cfg.n_experts;
+  uint8_t* base = ctx->hcache + static_cast<size_t>(l) * H * ctx->file_stride;
+  const long long t = ctx->step;
+  std::fill(ctx->h_touched.begin(), ctx->h_touched.end(), 0);
+  bool need_read = false;
+  for (int m = 0; m < n_miss; ++m) {
+    const int hs = soe[rec[1 + 2 * m]];
+    ctx->h_src[m] = nullptr;
+    if (hs >= 0) {
+      lu[hs] = t;
+      ctx->h_touched[hs] = 1;
+      ctx->h_src[m] = base + static_cast<size_t>(hs) * ctx->file_stride;
+      ++ctx->host_hits;
+    } else {
+      need_read = true;
+    }
+  }
+  // a record is rewritten only once the copies issued out of it earlier are done
+  if (need_read) CK(cudaEventSynchronize(ctx->hev));
+  for (int m = 0; m < n_miss; ++m) {
+    if (ctx->h_src[m]) continue;
+    const int ex = rec[1 + 2 * m];
+    int v = -1;
+    for (int i = 0; i < H; ++i)
+      if (!ctx->h_touched[i] && (v < 0 || lu[i] < lu[v])) v = i;
+    if (v < 0) return fail(ctx, MOE_ECUDA, "host tier has no free record (%d records, %d misses)", H, n_miss);
+    if (eos[v] >= 0) soe[eos[v]] = -1;
+    eos[v] = -1;
+    uint8_t* dst = base + static_cast<size_t>(v) * ctx->file_stride;
+    moe_status st = file_read_record(ctx, l, ex, dst);
+    if (st != MOE_OK) return st;
+    eos[v] = ex;
+    soe[ex] = v;
+    lu[v] = t;
+    ctx->h_touched[v] = 1;
+    ctx->h_src[m] = dst;
+  }
+  return MOE_OK;
+}
+
+void host_tier_clear(moe_ctx* ctx) {
+  std::fill(ctx->h_expert_of_slot.begin(), ctx->h_expert_of_slot.end(), -1);
+  std::fill(ctx->h_last_use.begin(), ctx->h_last_use.end(), -1);
+  std::fill(ctx->h_slot_of_expert.begin(), ctx->h_slot_of_expert.end(), -1);
+  ctx->host_hits = 0;
+  ctx->file_read_bytes = 0;
+  ctx->file_read_us = 0;
+}
+
 // Host-pool decode of one token through [l0, l1): per layer, route + LRU,
 // shared and hit experts while the misses are staged, then the misses, then down.
 moe_status pool_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec* trace, int trace_cap,
@@ -604,31 +690,33 @@ moe_status pool_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec*
     if (n_miss < 0 || n_miss > k) return fail(ctx, MOE_ECUDA, "corrupt miss record (%d)", n_miss);
     const LayerStore& Ls = ctx->L[l];
     const bool from_file = ctx->file_fd >= 0;
+    const bool tiered = from_file && ctx->n_host > 0;
     const int half = ctx->fhalf;
-    if (from_file && n_miss > 0) {
+    for (int m = 0; m < n_miss; ++m) {
+      const int ex = rec[1 + 2 * m], slot = rec[2 + 2 * m];
+      if (ex < 0 || ex >= ctx->cfg.n_experts || slot < 0 || slot >= ctx->n_slots)
+        return fail(ctx, MOE_ECUDA, "corrupt miss record (expert %d, slot %d)", ex, slot);
+    }
+    if (tiered && n_miss > 0) {
+      st = host_tier_step(ctx, l, rec, n_miss);
+      if (st != MOE_OK) return st;
+    } else if (from_file && n_miss > 0) {
       // the copies out of this staging half two layers ago must be done before it is refilled
       CK(cudaEventSynchronize(ctx->fev[half]));
     }
     for (int m = 0; m < n_miss; ++m) {
       const int ex = rec[1 + 2 * m], slot = rec[2 + 2 * m];
-      if (ex < 0 || ex >= ctx->cfg.n_experts || slot < 0 || slot >= ctx->n_slots)
-        return fail(ctx, MOE_ECUDA, "corrupt miss record (expert %d, slot %d)", ex, slot);
       if (ctx->hook_fail_copy) {
         ctx->hook_fail_copy = false;
         return fail(ctx, MOE_ECUDA, "staging copy failed (injected by test hook)");
       }
       const uint8_t* src;
-      if (from_file) {
+      if (tiered) {
+        src = ctx->h_src[m];
+      } else if (from_file) {
         uint8_t* dst = ctx->fstage + (static_cast<size_t>(half) * k + m) * ctx->file_stride;
-        const uint64_t off = (static_cast<uint64_t>(l) * ctx->cfg.n_experts + ex) * ctx->file_stride;
-        const long long t0 = now_us();
-        // O_DIRECT reads whole 4096-byte-aligned records into the page-aligned staging
-        const bool direct = ctx->file_rfd >= 0;
-        const int e = file_pool_transfer(ctx->fpool, direct ? ctx->file_rfd : ctx->file_fd, false, off, dst,
-                                         direct ? ctx->file_stride : ctx->expert_bytes, ctx->file_chunk);
-        ctx->file_read_us += now_us() - t0;
-        if (e != 0) return fail(ctx, MOE_EIO, "expert file read (layer %d, expert %d): %s", l, ex, strerror(e));
-        ctx->file_read_bytes += ctx->expert_bytes;
+        st = file_read_record(ctx, l, ex, dst);
+        if (st != MOE_OK) return st;
         src = dst;
       } else {
         src = ctx->pool + (static_cast<size_t>(l) * ctx->cfg.n_experts + ex) * ctx->stride;
@@ -637,7 +725,9 @@ moe_status pool_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec*
                          cudaMemcpyHostToDevice, ctx->side));
       ctx->staged += ctx->expert_bytes;
     }
-    if (from_file && n_miss > 0) {
+    if (tiered && n_miss > 0) {
+      CK(cudaEventRecord(ctx->hev, ctx->side));
+    } else if (from_file && n_miss > 0) {
       CK(cudaEventRecord(ctx->fev[half], ctx->side));
       ctx->fhalf ^= 1;
     }
@@ -892,6 +982,8 @@ void moe_destroy(moe_ctx* ctx) {
   if (ctx->file_fd >= 0) ::close(ctx->file_fd);
   if (ctx->file_rfd >= 0) ::close(ctx->file_rfd);
   if (ctx->fstage) cudaFreeHost(ctx->fstage);
+  if (ctx->hcache) cudaFreeHost(ctx->hcache);
+  if (ctx->hev) cudaEventDestroy(ctx->hev);
   for (auto& e : ctx->fev)
     if (e) cudaEventDestroy(e);
   if (ctx->args_ring) cudaFreeHost(ctx->args_ring);
@@ -1126,6 +1218,37 @@ moe_status moe_set_expert_file(moe_ctx* ctx, const char* path, int n_threads, ui
   return MOE_OK;
 }
 
+moe_status moe_set_file_cache(moe_ctx* ctx, int n_host) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  if (ctx->file_fd < 0) return fail(ctx, MOE_ESTATE, "the host tier needs an expert file (moe_set_expert_file)");
+  const moe_config& c = ctx->cfg;
+  if (n_host != 0 && (n_host < c.top_k || n_host > c.n_experts))
+    return fail(ctx, MOE_EINVAL, "host records per layer %d outside {0} + [top_k=%d, n_experts=%d]", n_host, c.top_k,
+                c.n_experts);
+  CK(cudaSetDevice(ctx->device));
+  CK(cudaDeviceSynchronize());   // no copy out of the old records is in flight
+  if (ctx->hcache) cudaFreeHost(ctx->hcache);
+  ctx->hcache = nullptr;
+  ctx->n_host = 0;
+  if (n_host > 0) {
+    const size_t bytes = static_cast<size_t>(c.n_layers) * n_host * ctx->file_stride;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->hcache), bytes, cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      ctx->hcache = nullptr;
+      return fail(ctx, MOE_ENOMEM, "pinned host tier (%zu bytes)", bytes);
+    }
+    if (!ctx->hev) CK(cudaEventCreateWithFlags(&ctx->hev, cudaEventDisableTiming));
+    ctx->n_host = n_host;
+  }
+  ctx->h_expert_of_slot.assign(static_cast<size_t>(c.n_layers) * n_host, -1);
+  ctx->h_last_use.assign(static_cast<size_t>(c.n_layers) * n_host, -1);
+  ctx->h_slot_of_expert.assign(static_cast<size_t>(c.n_layers) * c.n_experts, -1);
+  ctx->h_touched.assign(static_cast<size_t>(n_host), 0);
+  host_tier_clear(ctx);
+  return MOE_OK;
+}
+
 moe_status moe_reset_cache(moe_ctx* ctx) {
   if (!ctx) return MOE_EINVAL;
   if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
@@ -1142,6 +1265,7 @@ moe_status moe_reset_cache(moe_ctx* ctx) {
   ctx->step = 0;
   ctx->steps = 0;
   ctx->staged = 0;
+  host_tier_clear(ctx);
   return MOE_OK;
 }
 
@@ -1469,6 +1593,9 @@ moe_status moe_get_stats(moe_ctx* ctx, moe_stats* out) {
   }
   out->steps = ctx->steps;
   out->staged_bytes = ctx->staged;
+  out->file_read_bytes = ctx->file_read_bytes;
+  out->host_tier_hits = ctx->host_hits;
+  out->host_tier_bytes = ctx->hcache ? static_cast<int64_t>(ctx->cfg.n_layers) * ctx->n_host * ctx->file_stride : 0;
   out->n_slots = ctx->n_slots;
   out->expert_bytes = ctx->expert_bytes;
   out->shared_bytes = ctx->shared_bytes;

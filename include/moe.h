@@ -123,6 +123,9 @@ typedef struct {
     int64_t shared_bytes;
     int64_t device_bytes;  /* device memory held by the context */
     int64_t host_pool_bytes;
+    int64_t file_read_bytes;  /* expert-file contexts: routed-expert bytes read from the file */
+    int64_t host_tier_hits;   /* expert-file contexts: slot-cache misses served by the host tier */
+    int64_t host_tier_bytes;  /* pinned bytes of the host tier (moe_set_file_cache) */
 } moe_stats;
 
 /* Create a context on CUDA device `device`.  Allocates the per-call scratch
@@ -257,6 +260,25 @@ moe_status moe_set_cache_policy(moe_ctx *ctx, int policy);
  * the file cannot be created), MOE_ENOMEM (staging memory), MOE_EIO later
  * (a record read or write that fails or comes up short). */
 moe_status moe_set_expert_file(moe_ctx *ctx, const char *path, int n_threads, uint64_t chunk_bytes, int flags);
+
+/* Two-tier cache (expert file -> pinned host records -> HBM slots): keeps
+ * `n_host` records per layer of an expert-file context in pinned host memory
+ * in front of the file, so the slot cache's misses come from the file only
+ * when the host tier misses too (the goinfer chapter "When the model doesn't
+ * fit" and the TurboFieldfare write-up keep recently used experts in memory
+ * in front of the model file; here that level is explicit, pinned and
+ * bounded).  The host tier follows the slot cache's LRU rules one level down:
+ * per layer and step, the misses it holds refresh their record's last use
+ * (the step counter); the others, in top-k order, take the record with the
+ * smallest (last use, record index) among those the step has not touched
+ * (empty records, last use -1, first) and are read from the file into it; the
+ * staging copy to the slot then comes from that record.  n_host = 0 removes
+ * the tier (misses go through the two staging halves again).  Any call empties
+ * the tier; moe_reset_cache, moe_set_slots and moe_set_cache_policy do too.
+ * Call between steps.  Errors: MOE_ESTATE (no expert file), MOE_EINVAL
+ * (n_host outside {0} + [top_k, n_experts]), MOE_ENOMEM (n_layers * n_host
+ * records of pinned memory). */
+moe_status moe_set_file_cache(moe_ctx *ctx, int n_host);
 
 /* Reads bytes [offset, offset + bytes) of the file at `path` into host
  * memory `dst` with `n_threads` (1..64) threads taking chunks of

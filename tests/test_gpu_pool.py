@@ -304,13 +304,15 @@ def test_cache_policy_argument_errors():
         assert moe.moe_set_cache_policy(res.h, moe.MOE_CACHE_LFU) == moe.MOE_ESTATE
 
 
-def _file_run(shape, L, ws, H, n_slots, path=None):
+def _file_run(shape, L, ws, H, n_slots, path=None, n_host=0):
     ctx = Ctx(shape, n_layers=L, prenorm=1)
     with ctx:
         if path is not None:
             moe.check(moe.moe_set_expert_file(ctx.h, str(path), 4, 65536), ctx.h)
         for l in range(L):
             ctx.init_layer(l, ws[l], residency=moe.MOE_FILE_POOL if path is not None else moe.MOE_HOST_POOL)
+        if n_host:
+            moe.check(moe.moe_set_file_cache(ctx.h, n_host), ctx.h)
         moe.check(moe.moe_set_slots(ctx.h, n_slots), ctx.h)
         ys, trs = [], []
         for t in range(H.shape[0]):
@@ -363,3 +365,50 @@ def test_file_pool_state_and_io_errors(tmp_path):
         st, _ = moe.moe_decode_step(ctx.h, H, 1, 0, 1, None, h_out, None, None, None)
         assert st == moe.MOE_EIO
         assert moe.moe_set_slots(ctx.h, 2) == moe.MOE_ESTATE      # poisoned
+
+
+def test_file_host_tier_follows_oracle_lru(tmp_path):
+    # two-tier cache (file -> pinned host records -> HBM slots): a slot-cache
+    # miss that the host tier holds is copied from it, any other is read from
+    # the file; the host tier runs the oracle's LRU rules over each step's miss
+    # list (top-k order).  Slot traces and outputs stay those of the host pool.
+    sh = Shape(d=256, f=128, f_shared=128, n_experts=16, top_k=2)
+    L, N, NH = 3, 3, 6
+    ws = [to_device(gen_layer(sh, seed=152, layer=l)) for l in range(L)]
+    H = gen_hidden(16, sh.d, seed=152).cuda()
+    y_h, tr_h, st_h = _file_run(sh, L, ws, H, N)
+    y_f, tr_f, st_f = _file_run(sh, L, ws, H, N, tmp_path / "experts.bin", n_host=NH)
+    assert tr_h == tr_f
+    assert torch.equal(y_h, y_f)
+    host = [oracle.LRU(NH) for _ in range(L)]
+    hits = reads = 0
+    for t, tr in enumerate(tr_f):
+        for l in range(L):
+            miss = [r[2] for r in sorted(r for r in tr if r[0] == l) if not r[3]]
+            if miss:
+                h, _, _ = host[l].step(miss, t)
+                hits += int(h.sum())
+                reads += len(miss) - int(h.sum())
+    assert st_f.misses == st_h.misses == hits + reads
+    assert st_f.host_tier_hits == hits > 0 and reads > 0
+    assert st_f.file_read_bytes == reads * st_f.expert_bytes
+    rec = (st_f.expert_bytes + 4095) // 4096 * 4096
+    assert st_f.host_tier_bytes == L * NH * rec
+
+
+def test_file_host_tier_argument_errors(tmp_path):
+    sh = Shape(d=256, f=128, f_shared=128, n_experts=8, top_k=2)
+    w = to_device(gen_layer(sh, seed=153, layer=0))
+    with _pool_ctx(sh, 1, 4, [w]) as ctx:
+        assert moe.moe_set_file_cache(ctx.h, 4) == moe.MOE_ESTATE      # host pool: no expert file
+    ctx = Ctx(sh, n_layers=1, prenorm=1)
+    with ctx:
+        moe.check(moe.moe_set_expert_file(ctx.h, str(tmp_path / "e.bin"), 2, 0), ctx.h)
+        ctx.init_layer(0, w, residency=moe.MOE_FILE_POOL)
+        assert moe.moe_set_file_cache(ctx.h, 1) == moe.MOE_EINVAL       # below top_k
+        assert moe.moe_set_file_cache(ctx.h, 9) == moe.MOE_EINVAL       # above n_experts
+        moe.check(moe.moe_set_file_cache(ctx.h, 8), ctx.h)
+        moe.check(moe.moe_set_file_cache(ctx.h, 0), ctx.h)              # removed again
+        moe.check(moe.moe_set_slots(ctx.h, 2), ctx.h)
+        _, st = moe.moe_get_stats(ctx.h)
+        assert st.host_tier_bytes == 0
