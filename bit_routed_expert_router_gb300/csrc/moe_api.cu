@@ -180,6 +180,12 @@ struct moe_ctx {
   float *pf_approx = nullptr, *pf_xn2 = nullptr, *pf_xmax = nullptr;
   float* pf_ys = nullptr;
   unsigned long long* pf_timeline = nullptr;   // test hook 8: [4][16] GEMM event times of the first layer
+  // chunked prefill of host-pool / expert-file contexts: the union of a chunk's
+  // experts of one layer, staged into an arena (expert e at e * stride)
+  uint8_t* pf_arena = nullptr;
+  int32_t* pf_cnt_host = nullptr;              // pinned [n_experts]: pairs per expert of the layer
+  cudaEvent_t pf_ev_cnt = nullptr;             // pf_cnt_host filled
+  cudaEvent_t pf_ev_read = nullptr;            // the GEMMs that read the arena last are done
   CUtensorMap pf_map_xp[2]{}, pf_map_x16[2]{}, pf_map_ar[2]{}, pf_map_as[2]{};   // [0]: 128-row boxes, [1]: 32
   unsigned long long* p_timeline = nullptr;   // caller device buffer [n_layers][16], test hook 5
   // per-kernel timing
@@ -984,6 +990,9 @@ void moe_destroy(moe_ctx* ctx) {
   if (ctx->fstage) cudaFreeHost(ctx->fstage);
   if (ctx->hcache) cudaFreeHost(ctx->hcache);
   if (ctx->hev) cudaEventDestroy(ctx->hev);
+  if (ctx->pf_cnt_host) cudaFreeHost(ctx->pf_cnt_host);
+  if (ctx->pf_ev_cnt) cudaEventDestroy(ctx->pf_ev_cnt);
+  if (ctx->pf_ev_read) cudaEventDestroy(ctx->pf_ev_read);
   for (auto& e : ctx->fev)
     if (e) cudaEventDestroy(e);
   if (ctx->args_ring) cudaFreeHost(ctx->args_ring);
@@ -1365,8 +1374,14 @@ moe_status pf_alloc(moe_ctx* ctx) {
 }
 
 // One layer of the batched prefill: route, group by expert, four grouped GEMMs.
-moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin, uint16_t* hout, int T,
-                    const float* bias, float* y_last, cudaStream_t s) {
+// Token tiles of 32 rows when the experts' groups are small (a few rows each), else 128.
+int pf_tile_routed(const moe_config& c, int T) { return T * c.top_k <= 16 * c.n_experts ? kPfTileNSmall : kPfTileN; }
+int pf_tile_shared(int T) { return T <= 48 ? kPfTileNSmall : kPfTileN; }
+
+// One prefill layer, first part: RMS norm, router, the expert-ordered pair list
+// and the gathered token rows (pf_cnt then holds the pairs per expert).
+moe_status pf_layer_route(moe_ctx* ctx, int l, int rel, const uint16_t* hin, int T, const float* bias,
+                          cudaStream_t s) {
   const moe_config& c = ctx->cfg;
   const LayerStore& L = ctx->L[l];
   const int d = c.d, E = c.n_experts, k = c.top_k, P = T * k;
@@ -1378,26 +1393,59 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_approx,
                       ctx->pf_xn2, L.router_stats, ctx->pf_xmax, L.router_stats + E, ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
                       dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr, ctx->err_word, ctx->n_sm, s));
-  // token tiles of 32 rows when the experts' groups are small (a few rows each), else 128
-  const int nr = P <= 16 * E ? kPfTileNSmall : kPfTileN, ns = T <= 48 ? kPfTileNSmall : kPfTileN;
-  const int mr = nr == kPfTileN ? 0 : 1, ms = ns == kPfTileN ? 0 : 1;
-  CK(launch_pf_plan(ctx->pf_ids, P, E, nr, ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items, ctx->pf_nitems, s));
+  CK(launch_pf_plan(ctx->pf_ids, P, E, pf_tile_routed(c, T), ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items,
+                    ctx->pf_nitems, s));
   CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
   PROF(-1, s);
+  return MOE_OK;
+}
+
+PfGemm pf_gemm_base(moe_ctx* ctx) {
+  PfGemm g{};
+  g.tl = nullptr;
+  g.d = ctx->cfg.d;
+  g.k = ctx->cfg.top_k;
+  g.gelu = ctx->cfg.gelu_variant;
+  g.err = ctx->err_word;
+  return g;
+}
+
+// Shared expert gate/up over every token (needs no routed expert).
+moe_status pf_layer_shared_gu(moe_ctx* ctx, int l, int rel, int T, cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
+  const int ns = pf_tile_shared(T), ms = ns == kPfTileN ? 0 : 1;
+  const int t_items = (T + ns - 1) / ns;
+  PfGemm b = pf_gemm_base(ctx);
+  b.w = ctx->L[l].shared;
+  b.nG = c.d / 64;
+  b.n_items = t_items;
+  b.rows_total = T;
+  b.mode = PF_GU;
+  b.out16 = ctx->pf_as;
+  b.f_out = c.f_shared;
+  if (ctx->pf_timeline && rel == 0) b.tl = ctx->pf_timeline + 16;
+  CK(launch_pf_gemm(ns, ctx->pf_map_x16[ms], b, c.f_shared / 64, t_items, s));
+  return MOE_OK;
+}
+
+// The rest of the layer: routed gate/up and down over `experts` (expert e's
+// device record at e * stride), shared down, combine (+ residual).
+moe_status pf_layer_rest(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin, uint16_t* hout, int T,
+                         float* y_last, const uint8_t* experts, cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
+  const LayerStore& L = ctx->L[l];
+  const int d = c.d, E = c.n_experts, k = c.top_k, P = T * k;
+  const bool dbg = rel < ctx->dbg_layers;
+  const size_t xo = static_cast<size_t>(rel) * T;
+  const int nr = pf_tile_routed(c, T), ns = pf_tile_shared(T);
+  const int mr = nr == kPfTileN ? 0 : 1, ms = ns == kPfTileN ? 0 : 1;
   const size_t gu_r = static_cast<size_t>(c.f / 8) * (d / 64) * kGroupBytes;
   const size_t gu_s = static_cast<size_t>(c.f_shared / 8) * (d / 64) * kGroupBytes;
   const int max_items = P / nr + E + 1;
   const int t_items = (T + ns - 1) / ns;
-  PfGemm g{};
-  g.tl = nullptr;
-  g.d = d;
-  g.k = k;
-  g.gelu = c.gelu_variant;
-  g.err = ctx->err_word;
-  PROF(5, s);
   // routed gate/up: expert-ordered rows -> GELU(gate) * up, fp16 [P][f]
-  PfGemm a = g;
-  a.w = L.experts;
+  PfGemm a = pf_gemm_base(ctx);
+  a.w = experts;
   a.w_stride = ctx->stride;
   a.nG = d / 64;
   a.items = ctx->pf_items;
@@ -1407,20 +1455,9 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   a.f_out = c.f;
   if (ctx->pf_timeline && rel == 0) a.tl = ctx->pf_timeline;
   CK(launch_pf_gemm(nr, ctx->pf_map_xp[mr], a, c.f / 64, max_items, s));
-  // shared gate/up over every token
-  PfGemm b = g;
-  b.w = L.shared;
-  b.nG = d / 64;
-  b.n_items = t_items;
-  b.rows_total = T;
-  b.mode = PF_GU;
-  b.out16 = ctx->pf_as;
-  b.f_out = c.f_shared;
-  if (ctx->pf_timeline && rel == 0) b.tl = ctx->pf_timeline + 16;
-  CK(launch_pf_gemm(ns, ctx->pf_map_x16[ms], b, c.f_shared / 64, t_items, s));
   // routed down: per pair, fp32 [T*k][d]
-  PfGemm r = g;
-  r.w = L.experts + gu_r;
+  PfGemm r = pf_gemm_base(ctx);
+  r.w = experts + gu_r;
   r.w_stride = ctx->stride;
   r.nG = c.f / 64;
   r.items = ctx->pf_items;
@@ -1431,7 +1468,7 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   if (ctx->pf_timeline && rel == 0) r.tl = ctx->pf_timeline + 32;
   CK(launch_pf_gemm(nr, ctx->pf_map_ar[mr], r, d / 128, max_items, s));
   // shared down, then the combine: shared + routed in top-k order + residual
-  PfGemm q = g;
+  PfGemm q = pf_gemm_base(ctx);
   q.w = L.shared + gu_s;
   q.nG = c.f_shared / 64;
   q.n_items = t_items;
@@ -1448,6 +1485,16 @@ moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin
   return MOE_OK;
 }
 
+moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin, uint16_t* hout, int T,
+                    const float* bias, float* y_last, cudaStream_t s) {
+  moe_status st = pf_layer_route(ctx, l, rel, hin, T, bias, s);
+  if (st != MOE_OK) return st;
+  PROF(5, s);
+  st = pf_layer_shared_gu(ctx, l, rel, T, s);
+  if (st != MOE_OK) return st;
+  return pf_layer_rest(ctx, l, rel, n_rel, hin, hout, T, y_last, ctx->L[l].experts, s);
+}
+
 // The tcgen05 path over [l0, l1) for T tokens.
 moe_status pf_enqueue(moe_ctx* ctx, const void* h, int T, int l0, int l1, const float* logit_bias, void* h_out,
                       float* y_last, cudaStream_t s) {
@@ -1459,6 +1506,97 @@ moe_status pf_enqueue(moe_ctx* ctx, const void* h, int T, int l0, int l1, const 
     if (st != MOE_OK) return st;
   }
   return MOE_OK;
+}
+
+// Stages the union of layer l's experts picked by the chunk (pf_cnt_host[e] >
+// 0) into the arena on the side stream: from the pinned host pool, or read from
+// the expert file into the staging halves, k records at a time.
+moe_status pf_stage_union(moe_ctx* ctx, int l, int T) {
+  const int E = ctx->cfg.n_experts, k = ctx->cfg.top_k;
+  const bool from_file = ctx->file_fd >= 0;
+  const volatile int32_t* cnt = ctx->pf_cnt_host;
+  int n = 0;
+  for (int e = 0; e < E; ++e) {
+    const int ne = cnt[e];
+    if (ne < 0 || ne > T) return fail(ctx, MOE_ECUDA, "corrupt prefill pair count (%d for expert %d)", ne, e);
+    if (ne == 0) continue;
+    const uint8_t* src;
+    if (from_file) {
+      const int half = ctx->fhalf, m = n % k;
+      // the copies out of this staging half are done before it is refilled
+      if (m == 0) CK(cudaEventSynchronize(ctx->fev[half]));
+      uint8_t* dst = ctx->fstage + (static_cast<size_t>(half) * k + m) * ctx->file_stride;
+      moe_status st = file_read_record(ctx, l, e, dst);
+      if (st != MOE_OK) return st;
+      src = dst;
+    } else {
+      src = ctx->pool + (static_cast<size_t>(l) * E + e) * ctx->stride;
+    }
+    CK(cudaMemcpyAsync(ctx->pf_arena + static_cast<size_t>(e) * ctx->stride, src, ctx->expert_bytes,
+                       cudaMemcpyHostToDevice, ctx->side));
+    ctx->staged += ctx->expert_bytes;
+    ++n;
+    if (from_file && n % k == 0) {
+      CK(cudaEventRecord(ctx->fev[ctx->fhalf], ctx->side));
+      ctx->fhalf ^= 1;
+    }
+  }
+  if (from_file && n % k != 0) {
+    CK(cudaEventRecord(ctx->fev[ctx->fhalf], ctx->side));
+    ctx->fhalf ^= 1;
+  }
+  return MOE_OK;
+}
+
+// Chunked prefill of a host-pool or expert-file context over [l0, l1): per
+// layer, the chunk's T tokens are routed, the union of their experts is staged
+// once into the arena, and the layer's grouped GEMMs run over it; the shared
+// expert's gate/up runs while the union is staged.
+moe_status pf_pool_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const float* logit_bias, void* h_out,
+                       float* y_last, cudaStream_t s) {
+  moe_status st = pf_alloc(ctx);
+  if (st != MOE_OK) return st;
+  const int E = ctx->cfg.n_experts;
+  if (!ctx->pf_arena) {
+    size_t nb = 0;
+    uint8_t* arena = dalloc<uint8_t>(static_cast<size_t>(E) * ctx->stride, ctx->pf_owned, nb);
+    if (!arena) return fail(ctx, MOE_ENOMEM, "prefill expert arena (%zu bytes)", static_cast<size_t>(E) * ctx->stride);
+    if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->pf_cnt_host), static_cast<size_t>(E) * 4,
+                      cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      ctx->pf_cnt_host = nullptr;
+      return fail(ctx, MOE_ENOMEM, "pinned prefill counts");
+    }
+    CK(cudaEventCreateWithFlags(&ctx->pf_ev_cnt, cudaEventDisableTiming));
+    CK(cudaEventCreateWithFlags(&ctx->pf_ev_read, cudaEventDisableTiming));
+    ctx->device_bytes += nb;
+    ctx->pf_arena = arena;
+  }
+  const int n_rel = l1 - l0;
+  for (int rel = 0; rel < n_rel; ++rel) {
+    const int l = l0 + rel;
+    const uint16_t* hin = rel == 0 ? static_cast<const uint16_t*>(h) : ctx->pf_h[(rel - 1) & 1];
+    uint16_t* hout = rel == n_rel - 1 ? static_cast<uint16_t*>(h_out) : ctx->pf_h[rel & 1];
+    st = pf_layer_route(ctx, l, rel, hin, T, logit_bias, s);
+    if (st != MOE_OK) return st;
+    CK(cudaMemcpyAsync(ctx->pf_cnt_host, ctx->pf_cnt, static_cast<size_t>(E) * 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaEventRecord(ctx->pf_ev_cnt, s));
+    PROF(5, s);
+    st = pf_layer_shared_gu(ctx, l, rel, T, s);
+    if (st != MOE_OK) return st;
+    st = wait_event(ctx, ctx->pf_ev_cnt, "prefill routing");
+    if (st != MOE_OK) return st;
+    // the arena is rewritten only after the GEMMs that read it last are done
+    CK(cudaStreamWaitEvent(ctx->side, ctx->pf_ev_read, 0));
+    st = pf_stage_union(ctx, l, T);
+    if (st != MOE_OK) return st;
+    CK(cudaEventRecord(ctx->ev_copy, ctx->side));
+    CK(cudaStreamWaitEvent(s, ctx->ev_copy, 0));
+    st = pf_layer_rest(ctx, l, rel, n_rel, hin, hout, T, y_last, ctx->pf_arena, s);
+    if (st != MOE_OK) return st;
+    CK(cudaEventRecord(ctx->pf_ev_read, s));
+  }
+  return prof_collect(ctx, s);
 }
 
 moe_status pf_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const float* logit_bias, void* h_out,
@@ -1526,10 +1664,15 @@ moe_status moe_prefill(moe_ctx* ctx, const void* h, int T, int layer_begin, int 
   moe_status st = check_ready(ctx, layer_begin, layer_end);
   if (st != MOE_OK) return st;
   if (!h || !h_out) return fail(ctx, MOE_EINVAL, "NULL h / h_out");
-  if (ctx->residency != MOE_RESIDENT_HBM) return fail(ctx, MOE_EINVAL, "prefill needs a resident context");
   if (T < 1 || T > ctx->cfg.max_tokens) return fail(ctx, MOE_EINVAL, "T=%d outside [1, %d]", T, ctx->cfg.max_tokens);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CK(cudaSetDevice(ctx->device));
+  if (ctx->residency == MOE_HOST_POOL || ctx->residency == MOE_FILE_POOL) {
+    if (!(ctx->pf_ok && ctx->use_pf))
+      return fail(ctx, MOE_EINVAL, "prefill of a host-pool context needs the tcgen05 path (d %% 128 == 0, "
+                                   "n_experts <= 128)");
+    return pf_pool_run(ctx, h, T, layer_begin, layer_end, logit_bias, h_out, y_last, s);
+  }
   const int d = ctx->cfg.d;
   if (ctx->pf_ok && ctx->use_pf) return pf_run(ctx, h, T, layer_begin, layer_end, logit_bias, h_out, y_last, s);
   // otherwise: the batched decode kernels, kMaxDecodeB tokens at a time

@@ -185,8 +185,8 @@ moe_status moe_decode_step(moe_ctx *ctx, const void *h_in, int B, int layer_begi
 /* Prefill: T tokens at once through layers [layer_begin, layer_end)
  * ("Optimizing a 14.3 GB model for an 8 GB machine", section "Splitting the
  * work improved attention and prefill": dequantise a small 16-bit tile, run
- * the matrix primitive, discard the tile).  Resident contexts only,
- * 1 <= T <= max_tokens; h, h_out bf16 [T][d] and y_last fp32 [T][d] (nullable)
+ * the matrix primitive, discard the tile).  1 <= T <= max_tokens; h, h_out
+ * bf16 [T][d] and y_last fp32 [T][d] (nullable)
  * on the device; logit_bias (nullable) fp32 [layer_end - layer_begin][T][E].
  * When d % 128 == 0 and n_experts <= 128 (else the batched decode kernels run,
  * 32 tokens at a time): the routing is exact (the same ids and gates as
@@ -196,7 +196,20 @@ moe_status moe_decode_step(moe_ctx *ctx, const void *h_in, int B, int layer_begi
  * are combined per token as shared + routed outputs in top-k order; an fp16
  * operand outside [-65504, 65504] is reported by moe_sync as MOE_EDOMAIN.  The
  * first call allocates scratch for max_tokens tokens (about 180 KB per token at
- * the full shape).  Returns without synchronising. */
+ * the full shape).  Returns without synchronising.
+ * Host-pool and expert-file contexts (chunked prefill, same write-up and
+ * section: the prompt goes through in bounded batches instead of one token at
+ * a time, here with only the experts a batch picks in device memory): the
+ * call is one chunk.  Per layer the T tokens
+ * are routed, the union of the experts they pick is staged once (from the
+ * pinned pool, or read from the expert file) into a one-layer arena of
+ * n_experts device records (made on the first call), and the same grouped
+ * GEMMs run over it, so the outputs are bit-identical to a resident context's;
+ * the shared expert's gate/up runs while the union is staged.  The host waits
+ * for each layer's routing (bounded: MOE_ETIMEOUT), so the call returns after
+ * the last layer's staging.  The decode slot cache is neither read nor
+ * changed; staged bytes count in moe_stats.  Needs the tensor-core path
+ * (d % 128 == 0, n_experts <= 128), else MOE_EINVAL. */
 moe_status moe_prefill(moe_ctx *ctx, const void *h, int T, int layer_begin, int layer_end,
                        const float *logit_bias, void *h_out, float *y_last, void *stream);
 

@@ -244,3 +244,55 @@ def test_small_batch_graph_replay_equals_direct_launches():
         ctx.sync()
         ref = _run_prefill(ctx, H, n_layers=L)
         assert torch.equal(y1, ref[1])
+
+
+def _pool_prefill_ctx(shape, n_layers, residency, path, max_tokens, seed):
+    ctx = Ctx(shape, n_layers=n_layers, prenorm=1, max_tokens=max_tokens)
+    if residency == moe.MOE_FILE_POOL:
+        moe.check(moe.moe_set_expert_file(ctx.h, str(path), 4, 0), ctx.h)
+    for l in range(n_layers):
+        ctx.init_layer(l, to_device(gen_layer(shape, seed=seed, layer=l)), residency=residency)
+    return ctx
+
+
+@pytest.mark.parametrize("residency", [moe.MOE_HOST_POOL, moe.MOE_FILE_POOL])
+@pytest.mark.parametrize("T", [3, 300])
+def test_chunked_prefill_through_the_pool(residency, T, tmp_path):
+    # a host-pool (or expert-file) context prefills a chunk of T tokens layer by
+    # layer: route, stage the union of the picked experts once, grouped GEMMs
+    # over it.  Same kernels and bytes as the resident prefill, so every output
+    # is bit-identical; the staged bytes are the per-layer unions' and the
+    # decode slot cache is left alone.
+    L = 3
+    ref, _ = _ctx(MEDIUM, n_layers=L, prenorm=1, max_tokens=T, seed=31)
+    pool = _pool_prefill_ctx(MEDIUM, L, residency, tmp_path / "experts.bin", T, seed=31)
+    with ref, pool:
+        H = gen_hidden(T, MEDIUM.d, seed=310 + T).cuda()
+        r = _run_prefill(ref, H, n_layers=L)
+        p = _run_prefill(pool, H, n_layers=L)
+        for a, b, name in zip(r, p, ("h_out", "y_last", "x", "ids", "gates", "y")):
+            assert torch.equal(a, b), name
+        _, st = moe.moe_get_stats(pool.h)
+        unions = [len(np.unique(r[3][l].cpu().numpy())) for l in range(L)]
+        if T == 3:
+            assert max(unions) < MEDIUM.n_experts      # a partial union is staged
+        assert st.staged_bytes == sum(unions) * st.expert_bytes
+        assert st.hits == 0 and st.misses == 0
+        if residency == moe.MOE_FILE_POOL:
+            assert st.file_read_bytes == st.staged_bytes
+        # a second chunk through the same arena
+        H2 = gen_hidden(T, MEDIUM.d, seed=320 + T).cuda()
+        r2 = _run_prefill(ref, H2, n_layers=L)
+        p2 = _run_prefill(pool, H2, n_layers=L)
+        for a, b in zip(r2, p2):
+            assert torch.equal(a, b)
+
+
+def test_chunked_prefill_needs_the_tensor_core_path():
+    pool = _pool_prefill_ctx(MEDIUM, 1, moe.MOE_HOST_POOL, None, 8, seed=32)
+    with pool:
+        moe.check(moe.moe_test_hook(pool.h, moe.HOOK_PREFILL_TC, 0), pool.h)
+        H = gen_hidden(8, MEDIUM.d, seed=32).cuda()
+        h_out = torch.empty_like(H)
+        assert moe.moe_prefill(pool.h, H, 8, 0, 1, None, h_out, None) == moe.MOE_EINVAL
+        assert moe.moe_prefill(pool.h, H, 9, 0, 1, None, h_out, None) == moe.MOE_EINVAL   # T > max_tokens
