@@ -764,7 +764,7 @@ def run_ours_pool(args):
     dev = torch.device("cuda", local)
     sh = _shape()
     cfg = moe.make_config(sh.d, sh.f, sh.f_shared, sh.n_experts, sh.top_k, n_layers=N_LAYERS, prenorm=1,
-                          max_tokens=1)
+                          max_tokens=POOL_PREFILL_CHUNK)
     st, ctx = moe.moe_create(cfg, local)
     if st != moe.MOE_OK:
         raise moe.MoeError(st, moe.moe_last_error(None))
@@ -804,6 +804,7 @@ def run_ours_pool(args):
             sweep[str(n_slots)] = {"tokens_per_s": n_tok / dt, "hit_rate": hits / max(hits + misses, 1),
                                    "misses_per_token": misses / n_tok, "staged_bytes_per_token": staged / n_tok,
                                    "host_link_gbs": staged / dt / 1e9}
+    chunked = pool_prefill_run(args, ctx, dev, stream)
     moe.moe_destroy(ctx)
     file_tier = None
     if args.file_dir:
@@ -828,6 +829,7 @@ def run_ours_pool(args):
                    "routing": "router logits + Zipf(1.1)/reuse-0.6 bias trace",
                    "timing": "host wall clock around the synchronised token loop (the host drives the staging)"},
         "sweep_by_slots": sweeps["lru"], "sweep_by_slots_lfu": sweeps["lfu"], "file_tier": file_tier,
+        "chunked_prefill": chunked,
         "roofline": {"bound": "host link", "achieved": best["host_link_gbs"], "peak": None, "unit": "GB/s",
                      "frac": None, "traffic": None},
         "gpu_launches": None, "cpu_baseline": None,
@@ -835,6 +837,42 @@ def run_ours_pool(args):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+POOL_PREFILL_CHUNK = 512
+
+
+def pool_prefill_run(args, ctx, dev, stream):
+    """Chunked prefill through the host pool: chunks of POOL_PREFILL_CHUNK
+    tokens through the 30 layers, each layer staging the union of the chunk's
+    experts once from the pinned pool (host wall clock around synchronised
+    calls: the host drives the staging)."""
+    import torch
+
+    import bit_routed_expert_router_gb300 as moe
+    from workload import gen_hidden
+
+    sh = _shape()
+    T = POOL_PREFILL_CHUNK
+    H = gen_hidden(T, sh.d, seed=SEED + 7).to(dev)
+    h_out = torch.empty_like(H)
+    for _ in range(args.warmup):
+        moe.check(moe.moe_prefill(ctx, H, T, 0, N_LAYERS, None, h_out, None, stream), ctx)
+    moe.check(moe.moe_sync(ctx, stream), ctx)
+    _, s0 = moe.moe_get_stats(ctx)
+    n = 4
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        moe.check(moe.moe_prefill(ctx, H, T, 0, N_LAYERS, None, h_out, None, stream), ctx)
+    moe.check(moe.moe_sync(ctx, stream), ctx)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    _, s1 = moe.moe_get_stats(ctx)
+    staged = s1.staged_bytes - s0.staged_bytes
+    return {"chunk_tokens": T, "layers": N_LAYERS, "chunks": n, "tokens_per_s": n * T / dt,
+            "ms_per_chunk": dt / n * 1e3, "experts_staged_per_layer": staged / s1.expert_bytes / n / N_LAYERS,
+            "host_link_gbs": staged / dt / 1e9}
 
 
 def file_tier_run(args, H, bias, out, stream, direct, n_slots, n_host):
