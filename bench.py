@@ -250,16 +250,16 @@ def run_reference(args):
     sh = _shape()
     H, bias = host_inputs()
     layers = gen_cpu_layers(2)
-    # one untimed evaluation warms the oracle; the timed sample is bounded by
+    # W untimed evaluations warm the oracle; the timed sample is bounded by
     # --cpu-budget seconds so the run ends within a few minutes whatever K is
-    oracle_token_layer_seconds(layers, H, bias, 1, 1e9)
+    oracle_token_layer_seconds(layers, H, bias, max(args.warmup, 1), 1e9)
     t0 = time.perf_counter()
     mean_s, n, cores = oracle_token_layer_seconds(layers, H, bias, args.steps, args.cpu_budget * 4)
     wall = time.perf_counter() - t0
     tok_s = 1.0 / (N_LAYERS * mean_s)
     sample = f"{n} (token, layer) oracle evaluations on layers 0-1, extrapolated x{N_LAYERS} layers per token"
     line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": ws,
-            "steps": n, "warmup": 1, "ms_per_step": wall / max(n, 1) * 1e3,
+            "steps": n, "warmup": max(args.warmup, 1), "ms_per_step": wall / max(n, 1) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_dict(sh),
             "cpu_baseline": {"value": tok_s, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},

@@ -117,7 +117,8 @@ typedef struct {
     int64_t steps;         /* decode calls on a host-pool context since create/reset */
     int64_t hits;          /* summed over layers */
     int64_t misses;
-    int64_t staged_bytes;  /* host-pool -> slot bytes copied */
+    int64_t staged_bytes;  /* routed-expert bytes copied to the device: decode misses into
+                              slots, and chunked-prefill unions into the prefill arena */
     int64_t n_slots;
     int64_t expert_bytes;  /* bytes of one routed expert (device layout == canonical size) */
     int64_t shared_bytes;
