@@ -779,10 +779,13 @@ def run_ours_pool(args):
     stream = torch.cuda.current_stream()
     n_tok = min(N_TOKENS, max(args.steps, 16))
     sweeps = {}
-    for policy in (moe.MOE_CACHE_LRU, moe.MOE_CACHE_LFU):
-        sweep = sweeps.setdefault("lru" if policy == moe.MOE_CACHE_LRU else "lfu", {})
+    for name, policy, staging in (("lru", moe.MOE_CACHE_LRU, moe.MOE_STAGING_HOST),
+                                  ("lfu", moe.MOE_CACHE_LFU, moe.MOE_STAGING_HOST),
+                                  ("lru_device", moe.MOE_CACHE_LRU, moe.MOE_STAGING_DEVICE)):
+        sweep = sweeps.setdefault(name, {})
         for n_slots in (8, 16, 32, 64):
             moe.check(moe.moe_set_slots(ctx, n_slots), ctx)
+            moe.check(moe.moe_set_staging(ctx, staging), ctx)
             moe.check(moe.moe_set_cache_policy(ctx, policy), ctx)
             for t in range(args.warmup):
                 moe.check(moe.moe_decode_step(ctx, H[t:t + 1], 1, 0, N_LAYERS, bias[t], out, None, None,
@@ -828,7 +831,8 @@ def run_ours_pool(args):
         "config": {"workload": "decode30_hostpool_lru_zipf", "layers": N_LAYERS, "B": 1, "slots_reported": 64,
                    "routing": "router logits + Zipf(1.1)/reuse-0.6 bias trace",
                    "timing": "host wall clock around the synchronised token loop (the host drives the staging)"},
-        "sweep_by_slots": sweeps["lru"], "sweep_by_slots_lfu": sweeps["lfu"], "file_tier": file_tier,
+        "sweep_by_slots": sweeps["lru"], "sweep_by_slots_lfu": sweeps["lfu"],
+        "sweep_by_slots_device_staging": sweeps["lru_device"], "file_tier": file_tier,
         "chunked_prefill": chunked,
         "roofline": {"bound": "host link", "achieved": best["host_link_gbs"], "peak": None, "unit": "GB/s",
                      "frac": None, "traffic": None},

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTATE, MOE_ETIMEOUT, MOE_EDOMAIN, MOE_EIO = range(8)
 MOE_RESIDENT_HBM, MOE_HOST_POOL, MOE_FILE_POOL = 0, 1, 2
 MOE_FILE_DIRECT = 1
+MOE_STAGING_HOST, MOE_STAGING_DEVICE = 0, 1
 MOE_CACHE_LRU, MOE_CACHE_LFU = 0, 1
 MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
 HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6
@@ -75,6 +76,7 @@ _SIGS = {
     "moe_set_cache_policy": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_set_expert_file": (C.c_int, [C.c_void_p, C.c_char_p, C.c_int, C.c_uint64, C.c_int]),
     "moe_set_file_cache": (C.c_int, [C.c_void_p, C.c_int]),
+    "moe_set_staging": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_pread_parallel": (C.c_int, [C.c_char_p, C.c_uint64, C.c_uint64, C.c_void_p, C.c_int, C.c_uint64]),
     "moe_decode_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                                   C.c_void_p, C.POINTER(MoeTraceRec), C.c_int, C.POINTER(C.c_int),
@@ -193,6 +195,10 @@ def moe_set_cache_policy(ctx, policy: int) -> int:
 def moe_set_expert_file(ctx, path, n_threads: int = 8, chunk_bytes: int = 0, flags: int = 0) -> int:
     return lib().moe_set_expert_file(ctx, None if path is None else os.fsencode(path), n_threads, chunk_bytes,
                                      flags)
+
+
+def moe_set_staging(ctx, mode: int) -> int:
+    return lib().moe_set_staging(ctx, mode)
 
 
 def moe_set_file_cache(ctx, n_host: int) -> int:

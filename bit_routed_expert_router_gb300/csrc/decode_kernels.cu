@@ -873,6 +873,54 @@ cudaError_t launch_down(KParams& p, int B, int max_items, int n_sm, cudaStream_t
   return launch(fn, dim3(grid > 0 ? grid : 1), dim3(kDnWarps * 32), down_smem(p.cg, nb4), s, pdl, &p);
 }
 
+namespace {
+
+// Device-driven staging of a layer's misses (no host round trip): block row y
+// copies the record of miss y from the pinned host pool, read through the host
+// link as mapped memory, into its slot, four 16-byte loads in flight per
+// thread to cover the link's latency.  A malformed record sets ERR_PLAN and
+// is skipped.
+__global__ void __launch_bounds__(256) k_stage_misses(const int32_t* rec, const uint8_t* pool_layer, uint8_t* slots,
+                                                      long long stride, long long n16, int E, int n_slots, int k,
+                                                      uint32_t* err) {
+  const int m = blockIdx.y;
+  const int n_miss = rec[0];
+  const bool lead = blockIdx.x == 0 && threadIdx.x == 0;
+  if (n_miss < 0 || n_miss > k) {
+    if (lead && m == 0) atomicOr(err, ERR_PLAN);
+    return;
+  }
+  if (m >= n_miss) return;
+  const int ex = rec[1 + 2 * m], slot = rec[2 + 2 * m];
+  if (ex < 0 || ex >= E || slot < 0 || slot >= n_slots) {
+    if (lead) atomicOr(err, ERR_PLAN);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(pool_layer + static_cast<long long>(ex) * stride);
+  uint4* dst = reinterpret_cast<uint4*>(slots + static_cast<long long>(slot) * stride);
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * step < n16; i += 4 * step) {
+    const uint4 a = src[i], b = src[i + step], c = src[i + 2 * step], e = src[i + 3 * step];
+    dst[i] = a;
+    dst[i + step] = b;
+    dst[i + 2 * step] = c;
+    dst[i + 3 * step] = e;
+  }
+  for (; i < n16; i += step) dst[i] = src[i];
+}
+
+}  // namespace
+
+cudaError_t launch_stage_misses(const int32_t* rec, const uint8_t* pool_layer, uint8_t* slots, long long stride,
+                                long long bytes, int E, int n_slots, int k, uint32_t* err, int n_sm, cudaStream_t s) {
+  if (bytes % 16 != 0 || stride % 16 != 0) return cudaErrorInvalidValue;
+  int per_miss = 2 * n_sm / k;
+  per_miss = per_miss < 1 ? 1 : (per_miss > 64 ? 64 : per_miss);
+  k_stage_misses<<<dim3(per_miss, k), 256, 0, s>>>(rec, pool_layer, slots, stride, bytes / 16, E, n_slots, k, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_repack(const uint8_t* gq, const uint16_t* gsb, const uint8_t* uq, const uint16_t* usb,
                           const uint8_t* dq, const uint16_t* dsb, int d, int f, uint8_t* dst, cudaStream_t s) {
   const size_t gu_bytes = static_cast<size_t>(f / 8) * (d / 64) * kGroupBytes;

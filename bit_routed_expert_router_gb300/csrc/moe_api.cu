@@ -72,6 +72,8 @@ struct moe_ctx {
   int n_sc = 1, cg = 1, Bd = 1;
   std::vector<LayerStore> L;
   uint8_t* pool = nullptr;
+  const uint8_t* pool_dev = nullptr;     // the pool's device address (mapped), or null
+  bool stage_device = false;             // moe_set_staging(MOE_STAGING_DEVICE)
   size_t pool_bytes = 0;
   // expert file tier (MOE_FILE_POOL contexts)
   int file_fd = -1;
@@ -764,6 +766,60 @@ moe_status pool_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec*
   return MOE_OK;
 }
 
+// Device-driven variant of pool_run (moe_set_staging MOE_STAGING_DEVICE): per
+// layer, a staging kernel on the side stream, ordered after the router kernel,
+// reads the router's miss record and copies the missed experts from the
+// mapped host pool into their slots; the host enqueues every layer without
+// waiting and fills the trace, if asked for, once the step is done.
+moe_status pool_run_device(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec* trace, int trace_cap,
+                           int* trace_len) {
+  const int k = ctx->cfg.top_k, E = ctx->cfg.n_experts;
+  const int n_rel = l1 - l0;
+  for (int l = l0; l < l1; ++l) {
+    const int rel = l - l0;
+    KParams p = base_params(ctx, l, rel, rel == 0, rel == n_rel - 1, 1);
+    p.h_src = rel == 0 ? nullptr : ctx->hbuf[(rel - 1) & 1];
+    p.h_dst = rel == n_rel - 1 ? nullptr : ctx->hbuf[rel & 1];
+    CK(launch_router(p, 1, s, false));
+    CK(cudaEventRecord(ctx->ev_route, s));
+    CK(cudaStreamWaitEvent(ctx->side, ctx->ev_route, 0));
+    CK(launch_stage_misses(ctx->host_rec_dev + static_cast<size_t>(rel) * (1 + 6 * k),
+                           ctx->pool_dev + static_cast<size_t>(l) * E * ctx->stride, ctx->L[l].slots, ctx->stride,
+                           ctx->expert_bytes, E, ctx->n_slots, k, ctx->err_word, ctx->n_sm, ctx->side));
+    CK(cudaEventRecord(ctx->ev_copy, ctx->side));
+    p.pass = 0;
+    CK(launch_gateup(p, 1, gu_max_items(ctx, 1), ctx->n_sm, s, false));
+    CK(cudaStreamWaitEvent(s, ctx->ev_copy, 0));
+    p.pass = 1;
+    CK(launch_gateup(p, 1, gu_max_items(ctx, 1), ctx->n_sm, s, false));
+    p.pass = -1;
+    CK(launch_down(p, 1, dn_max_items(ctx, 1), ctx->n_sm, s, false));
+  }
+  int n_rec = 0;
+  if (trace) {
+    CK(cudaEventRecord(ctx->ev_route, s));
+    moe_status st = wait_event(ctx, ctx->ev_route, "decode step (trace)");
+    if (st != MOE_OK) return st;
+    for (int rel = 0; rel < n_rel; ++rel) {
+      const volatile int32_t* rec = ctx->host_rec + static_cast<size_t>(rel) * (1 + 6 * k);
+      for (int j = 0; j < k && n_rec < trace_cap; ++j) {
+        const volatile int32_t* tr = rec + 1 + 2 * k + 4 * j;
+        moe_trace_rec r;
+        r.token = static_cast<int32_t>(ctx->step);
+        r.layer = l0 + rel;
+        r.k_pos = j;
+        r.expert = tr[0];
+        r.hit = tr[1];
+        r.slot = tr[2];
+        r.evicted = tr[3];
+        trace[n_rec++] = r;
+      }
+    }
+  }
+  if (trace_len) *trace_len = n_rec;
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1039,12 +1095,15 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
     return fail(ctx, MOE_ENOMEM, "layer needs %zu bytes, %zu free", need, free_b);
   if (pool && !file && !ctx->pool) {
     const size_t pb = static_cast<size_t>(c.n_layers) * c.n_experts * ctx->stride;
-    if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->pool), pb, cudaHostAllocDefault) != cudaSuccess) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->pool), pb, cudaHostAllocMapped) != cudaSuccess) {
       ctx->pool = nullptr;
       cudaGetLastError();
       return fail(ctx, MOE_ENOMEM, "pinned host pool of %zu bytes", pb);
     }
     ctx->pool_bytes = pb;
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, ctx->pool, 0) == cudaSuccess) ctx->pool_dev = static_cast<const uint8_t*>(dp);
+    cudaGetLastError();
   }
   ctx->residency = residency;
   if (!Ls.router_w) CK(cudaMalloc(&Ls.router_w, static_cast<size_t>(c.n_experts) * c.d * 2));
@@ -1227,6 +1286,19 @@ moe_status moe_set_expert_file(moe_ctx* ctx, const char* path, int n_threads, ui
   return MOE_OK;
 }
 
+moe_status moe_set_staging(moe_ctx* ctx, int mode) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  if (mode != MOE_STAGING_HOST && mode != MOE_STAGING_DEVICE) return fail(ctx, MOE_EINVAL, "unknown staging mode %d", mode);
+  if (ctx->residency != MOE_HOST_POOL) return fail(ctx, MOE_ESTATE, "staging modes apply to host-pool contexts");
+  if (mode == MOE_STAGING_DEVICE && !ctx->pool_dev)
+    return fail(ctx, MOE_ESTATE, "the host pool is not mapped into the device address space");
+  CK(cudaSetDevice(ctx->device));
+  CK(cudaDeviceSynchronize());
+  ctx->stage_device = mode == MOE_STAGING_DEVICE;
+  return moe_reset_cache(ctx);
+}
+
 moe_status moe_set_file_cache(moe_ctx* ctx, int n_host) {
   if (!ctx) return MOE_EINVAL;
   if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
@@ -1300,7 +1372,8 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
   st = put_args(ctx, make_args(ctx, h_in, h_out, y_last, logit_bias, B, B, 0), s);
   if (st != MOE_OK) return st;
   if (pool) {
-    st = pool_run(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len);
+    st = ctx->stage_device ? pool_run_device(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len)
+                           : pool_run(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len);
     ++ctx->step;
     ++ctx->steps;
     return st;
@@ -1735,12 +1808,14 @@ moe_status moe_get_stats(moe_ctx* ctx, moe_stats* out) {
     out->misses += cnt[2 * l + 1];
   }
   out->steps = ctx->steps;
+  // device-driven staging copies every miss once (the mode switch zeroed the counters)
   out->staged_bytes = ctx->staged;
   out->file_read_bytes = ctx->file_read_bytes;
   out->host_tier_hits = ctx->host_hits;
   out->host_tier_bytes = ctx->hcache ? static_cast<int64_t>(ctx->cfg.n_layers) * ctx->n_host * ctx->file_stride : 0;
   out->n_slots = ctx->n_slots;
   out->expert_bytes = ctx->expert_bytes;
+  if (ctx->stage_device) out->staged_bytes += out->misses * ctx->expert_bytes;
   out->shared_bytes = ctx->shared_bytes;
   size_t dev = ctx->device_bytes;
   for (auto& Ls : ctx->L) {

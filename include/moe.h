@@ -62,6 +62,7 @@ typedef enum {
 
 enum { MOE_RESIDENT_HBM = 0, MOE_HOST_POOL = 1, MOE_FILE_POOL = 2 };
 enum { MOE_FILE_DIRECT = 1 };   /* moe_set_expert_file flag: read misses with O_DIRECT */
+enum { MOE_STAGING_HOST = 0, MOE_STAGING_DEVICE = 1 };   /* moe_set_staging modes */
 enum { MOE_CACHE_LRU = 0, MOE_CACHE_LFU = 1 };
 enum { MOE_GELU_ERF = 0, MOE_GELU_TANH = 1 };
 
@@ -274,6 +275,21 @@ moe_status moe_set_cache_policy(moe_ctx *ctx, int policy);
  * the file cannot be created), MOE_ENOMEM (staging memory), MOE_EIO later
  * (a record read or write that fails or comes up short). */
 moe_status moe_set_expert_file(moe_ctx *ctx, const char *path, int n_threads, uint64_t chunk_bytes, int flags);
+
+/* Host-pool contexts: who stages the slot cache's misses.  MOE_STAGING_HOST
+ * (the default; the TurboFieldfare write-up's "coarse overlap": the host
+ * waits for each layer's routing, then issues the copies on a side stream
+ * while the shared expert and the hits are computed).  MOE_STAGING_DEVICE:
+ * no host round trip per layer; a staging kernel on the side stream, ordered
+ * after the layer's router kernel, reads the miss record and copies the
+ * missed experts from the pinned pool (mapped into the device address space,
+ * read through the host link) into their slots, so moe_decode_step enqueues
+ * all layers and returns at once (after the step completes when a trace is
+ * asked for, to fill it).  Both modes give the same cache decisions, traces
+ * and outputs.  Empties the cache as moe_reset_cache.  Errors: MOE_EINVAL
+ * (unknown mode), MOE_ESTATE (not a host-pool context, or a pool the device
+ * cannot address). */
+moe_status moe_set_staging(moe_ctx *ctx, int mode);
 
 /* Two-tier cache (expert file -> pinned host records -> HBM slots): keeps
  * `n_host` records per layer of an expert-file context in pinned host memory

@@ -131,13 +131,15 @@ def test_outputs_do_not_depend_on_slot_count():
             assert torch.equal(outs[n_slots][t][1], outs[4][t][1]), f"y differs, N={n_slots} t={t}"
 
 
-def test_full_shape_pool_three_layers():
+@pytest.mark.parametrize("staging", [moe.MOE_STAGING_HOST, moe.MOE_STAGING_DEVICE])
+def test_full_shape_pool_three_layers(staging):
     sh = FULL
     L, N, T = 3, 16, 6
     wd = [gen_layer(sh, seed=130, layer=l, device="cuda") for l in range(L)]
     tg = zipf_reuse_targets(T, L, sh.n_experts, sh.top_k, seed=130)
     bias = torch.from_numpy(bias_from_targets(tg, sh.n_experts))
     with _pool_ctx(sh, L, N, wd) as ctx:
+        moe.check(moe.moe_set_staging(ctx.h, staging), ctx.h)
         hosts = [to_host(w) for w in wd]
         del wd
         H = gen_hidden(T, sh.d, seed=130, device="cuda")
@@ -304,7 +306,7 @@ def test_cache_policy_argument_errors():
         assert moe.moe_set_cache_policy(res.h, moe.MOE_CACHE_LFU) == moe.MOE_ESTATE
 
 
-def _file_run(shape, L, ws, H, n_slots, path=None, n_host=0):
+def _file_run(shape, L, ws, H, n_slots, path=None, n_host=0, staging=None):
     ctx = Ctx(shape, n_layers=L, prenorm=1)
     with ctx:
         if path is not None:
@@ -314,6 +316,8 @@ def _file_run(shape, L, ws, H, n_slots, path=None, n_host=0):
         if n_host:
             moe.check(moe.moe_set_file_cache(ctx.h, n_host), ctx.h)
         moe.check(moe.moe_set_slots(ctx.h, n_slots), ctx.h)
+        if staging is not None:
+            moe.check(moe.moe_set_staging(ctx.h, staging), ctx.h)
         ys, trs = [], []
         for t in range(H.shape[0]):
             y, tr = _decode_trace(ctx, H[t:t + 1], L, None)
@@ -412,3 +416,42 @@ def test_file_host_tier_argument_errors(tmp_path):
         moe.check(moe.moe_set_slots(ctx.h, 2), ctx.h)
         _, st = moe.moe_get_stats(ctx.h)
         assert st.host_tier_bytes == 0
+
+
+def test_device_staging_matches_host_staging():
+    # device-driven staging (a kernel copies the misses from the mapped host
+    # pool, no host round trip per layer) makes the same cache decisions and
+    # outputs as the host-driven copies, bit for bit
+    sh = Shape(d=256, f=128, f_shared=128, n_experts=16, top_k=2)
+    L = 3
+    ws = [to_device(gen_layer(sh, seed=154, layer=l)) for l in range(L)]
+    H = gen_hidden(16, sh.d, seed=154).cuda()
+    y_h, tr_h, st_h = _file_run(sh, L, ws, H, 3)
+    y_d, tr_d, st_d = _file_run(sh, L, ws, H, 3, staging=moe.MOE_STAGING_DEVICE)
+    assert tr_h == tr_d
+    assert torch.equal(y_h, y_d)
+    assert st_d.hits == st_h.hits and st_d.misses == st_h.misses > 0
+    assert st_d.staged_bytes == st_h.staged_bytes == st_h.misses * st_h.expert_bytes
+
+
+def test_device_staging_without_trace_and_errors(tmp_path):
+    sh = Shape(d=256, f=128, f_shared=128, n_experts=8, top_k=2)
+    w = to_device(gen_layer(sh, seed=155, layer=0))
+    H = gen_hidden(4, sh.d, seed=155).cuda()
+    with _pool_ctx(sh, 1, 2, [w]) as ctx:
+        assert moe.moe_set_staging(ctx.h, 2) == moe.MOE_EINVAL
+        moe.check(moe.moe_set_staging(ctx.h, moe.MOE_STAGING_DEVICE), ctx.h)
+        ys = [ctx.decode(H[t:t + 1], 0, 1)[1].clone() for t in range(4)]   # no trace: returns at once
+        ctx.sync()
+        moe.check(moe.moe_set_staging(ctx.h, moe.MOE_STAGING_HOST), ctx.h)
+        for t in range(4):
+            assert torch.equal(ctx.decode(H[t:t + 1], 0, 1)[1], ys[t])
+    res = Ctx(sh, n_layers=1)
+    with res:
+        res.init_layer(0, w)
+        assert moe.moe_set_staging(res.h, moe.MOE_STAGING_DEVICE) == moe.MOE_ESTATE   # resident context
+    fctx = Ctx(sh, n_layers=1, prenorm=1)
+    with fctx:
+        moe.check(moe.moe_set_expert_file(fctx.h, str(tmp_path / "e.bin"), 2, 0), fctx.h)
+        fctx.init_layer(0, w, residency=moe.MOE_FILE_POOL)
+        assert moe.moe_set_staging(fctx.h, moe.MOE_STAGING_DEVICE) == moe.MOE_ESTATE  # file reads are host I/O
