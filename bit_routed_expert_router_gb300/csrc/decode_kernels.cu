@@ -877,7 +877,7 @@ namespace {
 
 // Device-driven staging of a layer's misses (no host round trip): block row y
 // copies the record of miss y from the pinned host pool, read through the host
-// link as mapped memory, into its slot, four 16-byte loads in flight per
+// link as mapped memory, into its slot, eight 16-byte loads in flight per
 // thread to cover the link's latency.  A malformed record sets ERR_PLAN and
 // is skipped.
 __global__ void __launch_bounds__(256) k_stage_misses(const int32_t* rec, const uint8_t* pool_layer, uint8_t* slots,
@@ -900,12 +900,12 @@ __global__ void __launch_bounds__(256) k_stage_misses(const int32_t* rec, const 
   uint4* dst = reinterpret_cast<uint4*>(slots + static_cast<long long>(slot) * stride);
   const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
   long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + 3 * step < n16; i += 4 * step) {
-    const uint4 a = src[i], b = src[i + step], c = src[i + 2 * step], e = src[i + 3 * step];
-    dst[i] = a;
-    dst[i + step] = b;
-    dst[i + 2 * step] = c;
-    dst[i + 3 * step] = e;
+  for (; i + 7 * step < n16; i += 8 * step) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = src[i + u * step];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) dst[i + u * step] = v[u];
   }
   for (; i < n16; i += step) dst[i] = src[i];
 }
@@ -915,8 +915,8 @@ __global__ void __launch_bounds__(256) k_stage_misses(const int32_t* rec, const 
 cudaError_t launch_stage_misses(const int32_t* rec, const uint8_t* pool_layer, uint8_t* slots, long long stride,
                                 long long bytes, int E, int n_slots, int k, uint32_t* err, int n_sm, cudaStream_t s) {
   if (bytes % 16 != 0 || stride % 16 != 0) return cudaErrorInvalidValue;
-  int per_miss = 2 * n_sm / k;
-  per_miss = per_miss < 1 ? 1 : (per_miss > 64 ? 64 : per_miss);
+  int per_miss = 4 * n_sm / k;
+  per_miss = per_miss < 1 ? 1 : (per_miss > 128 ? 128 : per_miss);
   k_stage_misses<<<dim3(per_miss, k), 256, 0, s>>>(rec, pool_layer, slots, stride, bytes / 16, E, n_slots, k, err);
   return cudaGetLastError();
 }
