@@ -1808,13 +1808,13 @@ moe_status moe_get_stats(moe_ctx* ctx, moe_stats* out) {
     out->misses += cnt[2 * l + 1];
   }
   out->steps = ctx->steps;
-  // device-driven staging copies every miss once (the mode switch zeroed the counters)
   out->staged_bytes = ctx->staged;
   out->file_read_bytes = ctx->file_read_bytes;
   out->host_tier_hits = ctx->host_hits;
   out->host_tier_bytes = ctx->hcache ? static_cast<int64_t>(ctx->cfg.n_layers) * ctx->n_host * ctx->file_stride : 0;
   out->n_slots = ctx->n_slots;
   out->expert_bytes = ctx->expert_bytes;
+  // device-driven staging copies every miss once (the mode switch zeroed the counters)
   if (ctx->stage_device) out->staged_bytes += out->misses * ctx->expert_bytes;
   out->shared_bytes = ctx->shared_bytes;
   size_t dev = ctx->device_bytes;
