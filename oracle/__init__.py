@@ -33,8 +33,12 @@ def build(force: bool = False) -> str:
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-ffp-contract=off",
-                               "-fno-fast-math", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
+        base = ["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                "-shared", _SRC, "-o", tmp, "-lm"]
+        try:   # threads over matrix rows where the compiler has OpenMP, else one thread
+            subprocess.check_call(base[:1] + ["-fopenmp"] + base[1:], stderr=subprocess.DEVNULL)
+        except subprocess.CalledProcessError:
+            subprocess.check_call(base)
         os.replace(tmp, _SO)
     return _SO
 
@@ -85,8 +89,16 @@ def lib():
             L.or_lru_step.argtypes = [i32, vp, vp, vp, i32, i64, vp, vp, vp]
             L.or_lfu_step.restype = i32
             L.or_lfu_step.argtypes = [i32, vp, vp, vp, vp, i32, i64, vp, vp, vp]
+            L.or_set_threads.restype = i32
+            L.or_set_threads.argtypes = [i32]
             _lib = L
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Host threads over the rows of each matrix-vector product (results do not
+    depend on it); returns the count in effect."""
+    return lib().or_set_threads(n)
 
 
 def _p(a: np.ndarray):

@@ -37,11 +37,19 @@
  *  - LRU: hits refresh their slot; misses, in top-k order, take the slot with
  *    the smallest (last_use, slot index) among slots neither hit nor filled
  *    in this step; empty slots carry last_use = -1.
+ *
+ * The rows of a matrix-vector product may be spread over host threads
+ * (or_set_threads, OpenMP when the compiler has it; one thread by default):
+ * each row is still summed by one thread in index order, so no result depends
+ * on the thread count.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_OK 0
 #define OR_EDOMAIN 1   /* router product outside |p| < 2^11, or non-finite input */
@@ -128,10 +136,27 @@ double or_weight(const uint8_t *q, const uint16_t *sb, int cols, int group, int 
     return s * (double)nib + b;
 }
 
+static int or_threads = 1;
+
+/* Host threads for the rows of or_matvec; returns the count in effect (1
+ * without OpenMP). */
+int or_set_threads(int n)
+{
+    or_threads = n < 1 ? 1 : n;
+#ifdef _OPENMP
+    return or_threads;
+#else
+    return 1;
+#endif
+}
+
 /* y[rows] = W x, fp64 accumulation in index order. */
 void or_matvec(const uint8_t *q, const uint16_t *sb, int rows, int cols, int group,
                const double *x, double *y)
 {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(or_threads) if (or_threads > 1)
+#endif
     for (int r = 0; r < rows; ++r) {
         double acc = 0.0;
         for (int c = 0; c < cols; ++c)

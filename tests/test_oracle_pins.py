@@ -430,3 +430,21 @@ def test_lfu_keeps_a_hot_expert_through_a_scan():
         t += 1
     assert 7 in list(lfu.expert_of_slot)
     assert 7 not in list(lru.expert_of_slot)
+
+
+def test_thread_count_does_not_change_results():
+    # the rows of each matrix-vector product may run on several threads; every
+    # row is still summed in index order by one thread, so results are bitwise
+    # the same at any thread count
+    sh = Shape(d=256, f=128, f_shared=192, n_experts=8, top_k=2)
+    lay = oracle.Layer(gen_layer(sh, seed=77, layer=0), sh.top_k)
+    x = oracle.rmsnorm_bf16(oracle.as_bits(gen_hidden(1, sh.d, seed=77)[0]), 1e-6)
+    try:
+        oracle.set_threads(1)
+        ref = lay.forward(x, None)
+        assert oracle.set_threads(4) in (1, 4)
+        got = lay.forward(x, None)
+    finally:
+        oracle.set_threads(1)
+    assert list(ref[0]) == list(got[0])
+    assert np.array_equal(ref[3], got[3])
