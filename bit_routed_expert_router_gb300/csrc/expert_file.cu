@@ -125,7 +125,14 @@ struct FilePool {
   int err = 0;
 };
 
-FilePool* file_pool_create(int n_threads) { return new FilePool(n_threads < 1 ? 1 : n_threads); }
+// Null when the threads cannot be started (no exception leaves the library).
+FilePool* file_pool_create(int n_threads) {
+  try {
+    return new FilePool(n_threads < 1 ? 1 : n_threads);
+  } catch (...) {
+    return nullptr;
+  }
+}
 void file_pool_destroy(FilePool* fp) { delete fp; }
 int file_pool_transfer(FilePool* fp, int fd, bool write, uint64_t offset, void* buf, uint64_t bytes, uint64_t chunk) {
   return fp->run(fd, write, offset, buf, bytes, chunk);
@@ -138,8 +145,13 @@ extern "C" moe_status moe_pread_parallel(const char* path, uint64_t offset, uint
   if (!path || (!dst && bytes > 0) || n_threads < 1 || n_threads > 64) return MOE_EINVAL;
   const int fd = ::open(path, O_RDONLY);
   if (fd < 0) return MOE_EINVAL;
-  moe::FilePool pool(n_threads);
-  const int e = pool.run(fd, false, offset, dst, bytes, chunk_bytes);
+  moe::FilePool* pool = moe::file_pool_create(n_threads);
+  if (!pool) {
+    ::close(fd);
+    return MOE_ENOMEM;
+  }
+  const int e = pool->run(fd, false, offset, dst, bytes, chunk_bytes);
+  moe::file_pool_destroy(pool);
   ::close(fd);
   return e == 0 ? MOE_OK : MOE_EIO;
 }

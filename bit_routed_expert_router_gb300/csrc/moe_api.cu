@@ -1283,6 +1283,14 @@ moe_status moe_set_expert_file(moe_ctx* ctx, const char* path, int n_threads, ui
   ctx->fstage = stage;
   ctx->file_chunk = chunk_bytes == 0 ? (512u << 10) : chunk_bytes;
   ctx->fpool = file_pool_create(n_threads);
+  if (!ctx->fpool) {
+    ::close(ctx->file_fd);
+    if (ctx->file_rfd >= 0) ::close(ctx->file_rfd);
+    ctx->file_fd = ctx->file_rfd = -1;
+    cudaFreeHost(ctx->fstage);
+    ctx->fstage = nullptr;
+    return fail(ctx, MOE_ENOMEM, "expert file reader threads");
+  }
   return MOE_OK;
 }
 

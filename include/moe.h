@@ -272,7 +272,8 @@ moe_status moe_set_cache_policy(moe_ctx *ctx, int policy);
  * opened with O_DIRECT (past the page cache; MOE_EINVAL where the file system
  * refuses it), else 0.
  * Errors: MOE_EINVAL (NULL path, bad counts, layers already initialised, or
- * the file cannot be created), MOE_ENOMEM (staging memory), MOE_EIO later
+ * the file cannot be created), MOE_ENOMEM (staging memory, or the reader
+ * threads cannot be started), MOE_EIO later
  * (a record read or write that fails or comes up short). */
 moe_status moe_set_expert_file(moe_ctx *ctx, const char *path, int n_threads, uint64_t chunk_bytes, int flags);
 
@@ -314,8 +315,8 @@ moe_status moe_set_file_cache(moe_ctx *ctx, int n_host);
  * memory `dst` with `n_threads` (1..64) threads taking chunks of
  * `chunk_bytes` (0 = one chunk), restarting short reads: the expert file
  * tier's read engine on its own.  No context, no GPU.  MOE_EINVAL for bad
- * arguments or a file that cannot be opened, MOE_EIO for a failed or short
- * read (past the end of the file). */
+ * arguments or a file that cannot be opened, MOE_ENOMEM if the threads cannot
+ * be started, MOE_EIO for a failed or short read (past the end of the file). */
 moe_status moe_pread_parallel(const char *path, uint64_t offset, uint64_t bytes, void *dst, int n_threads,
                               uint64_t chunk_bytes);
 
