@@ -15,6 +15,7 @@
 #include <string>
 #include <thread>
 #include <tuple>
+#include <new>
 #include <vector>
 
 #ifndef _GNU_SOURCE
@@ -1159,7 +1160,14 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
   int io_err = 0;
   if (e == cudaSuccess && file) {
     // the layer's records, through a host bounce buffer, written in parallel chunks
-    std::vector<uint8_t> host(static_cast<size_t>(c.n_experts) * ctx->stride);
+    std::vector<uint8_t> host;
+    try {
+      host.resize(static_cast<size_t>(c.n_experts) * ctx->stride);
+    } catch (const std::bad_alloc&) {
+      cudaFree(can);
+      cudaFree(tmp);
+      return fail(ctx, MOE_ENOMEM, "init_layer %d: host bounce buffer", layer);
+    }
     e = cudaMemcpy(host.data(), tmp, host.size(), cudaMemcpyDeviceToHost);
     for (int ex = 0; ex < c.n_experts && e == cudaSuccess && io_err == 0; ++ex)
       io_err = file_pool_transfer(ctx->fpool, ctx->file_fd, true,
