@@ -25,6 +25,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "kernels.h"
+#include "staging.h"
 
 #include <climits>
 

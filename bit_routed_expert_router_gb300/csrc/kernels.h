@@ -166,10 +166,5 @@ cudaError_t launch_gateup(KParams& p, int B, int max_items, int n_sm, cudaStream
 cudaError_t launch_down(KParams& p, int B, int max_items, int n_sm, cudaStream_t s, bool pdl);
 cudaError_t launch_repack(const uint8_t* gq, const uint16_t* gsb, const uint8_t* uq, const uint16_t* usb,
                           const uint8_t* dq, const uint16_t* dsb, int d, int f, uint8_t* dst, cudaStream_t s);
-// Device-driven miss staging of one layer: rec is the layer's miss record
-// ([0] = n_miss, then (expert, slot) pairs, written by the router kernel),
-// pool_layer the layer's records in mapped pinned host memory; bytes % 16 == 0.
-cudaError_t launch_stage_misses(const int32_t* rec, const uint8_t* pool_layer, uint8_t* slots, long long stride,
-                                long long bytes, int E, int n_slots, int k, uint32_t* err, int n_sm, cudaStream_t s);
 
 }  // namespace moe

@@ -30,6 +30,7 @@
 
 #include "internal.h"
 #include "kernels.h"
+#include "staging.h"
 
 using namespace moe;
 
