@@ -78,6 +78,9 @@ def test_null_context_is_rejected(lib):
     assert lib.moe_profile(None, 1) == moe.MOE_EINVAL
     assert lib.moe_test_hook(None, 1, 0) == moe.MOE_EINVAL
     assert lib.moe_set_debug(None, None, None, None, None, 0) == moe.MOE_EINVAL
+    assert lib.moe_set_expert_file(None, b"/nonexistent/e.bin", 4, 0, 0) == moe.MOE_EINVAL
+    assert lib.moe_set_file_cache(None, 8) == moe.MOE_EINVAL
+    assert lib.moe_set_staging(None, moe.MOE_STAGING_DEVICE) == moe.MOE_EINVAL
     assert lib.moe_decode_step(None, None, 1, 0, 1, None, None, None, None, 0, None, None) == moe.MOE_EINVAL
     assert lib.moe_prefill(None, None, 1, 0, 1, None, None, None, None) == moe.MOE_EINVAL
     st = moe.MoeStats()
