@@ -49,3 +49,28 @@ def test_two_gloo_ranks_aggregate_max_time_and_summed_units():
 def test_single_process_aggregate_is_identity():
     import bench
     assert bench.aggregate(None, 1.5, 7.0) == (1.5, 7.0)
+
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    # the reference arm is the oracle on the host cores: one JSON line with the
+    # base contract's keys, its cpu_baseline (one thread, plus every core) and
+    # an e2e entry with no host/device traffic (a small shape keeps it short)
+    import json
+
+    import bench
+    from workload import Shape
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    monkeypatch.setattr(bench, "_shape", lambda: Shape(d=256, f=128, f_shared=128, n_experts=8, top_k=2))
+    assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3", "--cpu-budget", "1"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["warmup"] == 3 and line["value"] > 0
+    for key in ("metric", "unit", "n_gpus", "steps", "ms_per_step", "higher_is_better", "scaling", "dtype",
+                "data", "config"):
+        assert key in line
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"]
+    assert cb["all_cores"]["value"] > 0 and cb["all_cores"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
