@@ -125,6 +125,39 @@ struct FilePool {
   int err = 0;
 };
 
+int host_tier_lru_step(int n_rec, int32_t* expert_of_rec, long long* last_use, int32_t* rec_of_expert,
+                       const int32_t* ids, int n, long long t, int32_t* rec, int32_t* hit, int32_t* evicted,
+                       char* touched) {
+  if (n > n_rec) return -1;
+  for (int i = 0; i < n_rec; ++i) touched[i] = 0;
+  for (int m = 0; m < n; ++m) {
+    const int r = rec_of_expert[ids[m]];
+    hit[m] = r >= 0;
+    evicted[m] = -1;
+    rec[m] = r;
+    if (r >= 0) {
+      last_use[r] = t;
+      touched[r] = 1;
+    }
+  }
+  int n_new = 0;
+  for (int m = 0; m < n; ++m) {
+    if (hit[m]) continue;
+    int v = -1;
+    for (int i = 0; i < n_rec; ++i)
+      if (!touched[i] && (v < 0 || last_use[i] < last_use[v])) v = i;
+    evicted[m] = expert_of_rec[v];
+    if (expert_of_rec[v] >= 0) rec_of_expert[expert_of_rec[v]] = -1;
+    expert_of_rec[v] = ids[m];
+    rec_of_expert[ids[m]] = v;
+    last_use[v] = t;
+    touched[v] = 1;
+    rec[m] = v;
+    ++n_new;
+  }
+  return n_new;
+}
+
 // Null when the threads cannot be started (no exception leaves the library).
 FilePool* file_pool_create(int n_threads) {
   try {

@@ -627,43 +627,24 @@ moe_status file_read_record(moe_ctx* ctx, int l, int ex, uint8_t* dst) {
 // from the file into it.  Sets h_src[m] to each miss's source record.
 moe_status host_tier_step(moe_ctx* ctx, int l, const volatile int32_t* rec, int n_miss) {
   const int H = ctx->n_host;
-  int32_t* eos = ctx->h_expert_of_slot.data() + static_cast<size_t>(l) * H;
-  long long* lu = ctx->h_last_use.data() + static_cast<size_t>(l) * H;
-  int32_t* soe = ctx->h_slot_of_expert.data() + static_cast<size_t>(l) * ctx->cfg.n_experts;
   uint8_t* base = ctx->hcache + static_cast<size_t>(l) * H * ctx->file_stride;
-  const long long t = ctx->step;
-  std::fill(ctx->h_touched.begin(), ctx->h_touched.end(), 0);
-  bool need_read = false;
+  int32_t ids[32], where[32], hit[32], evicted[32];
+  for (int m = 0; m < n_miss; ++m) ids[m] = rec[1 + 2 * m];
+  const int n_read = host_tier_lru_step(H, ctx->h_expert_of_slot.data() + static_cast<size_t>(l) * H,
+                                        ctx->h_last_use.data() + static_cast<size_t>(l) * H,
+                                        ctx->h_slot_of_expert.data() + static_cast<size_t>(l) * ctx->cfg.n_experts,
+                                        ids, n_miss, ctx->step, where, hit, evicted, ctx->h_touched.data());
+  if (n_read < 0) return fail(ctx, MOE_ECUDA, "host tier has no free record (%d records, %d misses)", H, n_miss);
+  // a record is rewritten only once the copies issued out of it earlier are done
+  if (n_read > 0) CK(cudaEventSynchronize(ctx->hev));
   for (int m = 0; m < n_miss; ++m) {
-    const int hs = soe[rec[1 + 2 * m]];
-    ctx->h_src[m] = nullptr;
-    if (hs >= 0) {
-      lu[hs] = t;
-      ctx->h_touched[hs] = 1;
-      ctx->h_src[m] = base + static_cast<size_t>(hs) * ctx->file_stride;
+    uint8_t* dst = base + static_cast<size_t>(where[m]) * ctx->file_stride;
+    if (hit[m]) {
       ++ctx->host_hits;
     } else {
-      need_read = true;
+      moe_status st = file_read_record(ctx, l, ids[m], dst);
+      if (st != MOE_OK) return st;
     }
-  }
-  // a record is rewritten only once the copies issued out of it earlier are done
-  if (need_read) CK(cudaEventSynchronize(ctx->hev));
-  for (int m = 0; m < n_miss; ++m) {
-    if (ctx->h_src[m]) continue;
-    const int ex = rec[1 + 2 * m];
-    int v = -1;
-    for (int i = 0; i < H; ++i)
-      if (!ctx->h_touched[i] && (v < 0 || lu[i] < lu[v])) v = i;
-    if (v < 0) return fail(ctx, MOE_ECUDA, "host tier has no free record (%d records, %d misses)", H, n_miss);
-    if (eos[v] >= 0) soe[eos[v]] = -1;
-    eos[v] = -1;
-    uint8_t* dst = base + static_cast<size_t>(v) * ctx->file_stride;
-    moe_status st = file_read_record(ctx, l, ex, dst);
-    if (st != MOE_OK) return st;
-    eos[v] = ex;
-    soe[ex] = v;
-    lu[v] = t;
-    ctx->h_touched[v] = 1;
     ctx->h_src[m] = dst;
   }
   return MOE_OK;
