@@ -18,6 +18,12 @@
  *     that stages missing experts into fixed device slots (section "MoE
  *     needed parallel work, reuse, and coarse overlap"; goinfer, "When the
  *     model doesn't fit"), the copies overlapped with the shared expert.
+ *     The cache can evict by LFU instead, and the staging can be done by a
+ *     device kernel instead of host-issued copies.  The experts can also
+ *     live in a file read by bounded parallel pread (section "Explicit reads
+ *     made expert streaming work"), optionally behind a pinned host tier.
+ *     Prefill on such a context goes a chunk at a time, each layer staging
+ *     the union of the chunk's experts once.
  *
  * Conventions for every entry point:
  *   - Every call returns a moe_status and never aborts, throws or exits.
