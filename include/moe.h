@@ -148,15 +148,17 @@ moe_status moe_create(const moe_config *cfg, int device, moe_ctx **out);
  *   shared:   the shared expert (intermediate size f_shared)
  *   residency: MOE_RESIDENT_HBM keeps every expert in device memory;
  *              MOE_HOST_POOL keeps routed experts in a pinned host pool and
- *              serves them from per-layer device slots (see moe_set_slots).
- *              All layers of a context use the same residency.
+ *              serves them from per-layer device slots (see moe_set_slots);
+ *              MOE_FILE_POOL writes them to the expert file instead (see
+ *              moe_set_expert_file, which must come first) and serves them
+ *              the same way.  All layers of a context use the same residency.
  * The library repacks the weights into its own device layout: a permutation
  * of the same bytes (nibbles and (scale, bias) pairs), never a re-encoding. */
 moe_status moe_init_layer(moe_ctx *ctx, int layer, const uint16_t *router_w,
                           const moe_expert_weights *experts, const moe_expert_weights *shared,
                           int residency);
 
-/* Host-pool contexts: give every layer n_slots device slots (top_k <= n_slots
+/* Host-pool and expert-file contexts: give every layer n_slots device slots (top_k <= n_slots
  * <= n_experts) and empty the LRU tables.  The byte budget
  * n_layers * n_slots * expert_bytes is checked against free device memory
  * before anything is allocated (MOE_ENOMEM, context unchanged). */
@@ -182,10 +184,14 @@ moe_status moe_set_slots(moe_ctx *ctx, int n_slots);
  * integers on a 2^-32 grid (deterministic), and reports a launch without its
  * cluster shape as MOE_ECUDA from moe_sync.  From 16 tokens on (when the
  * shape allows it) a step runs through the same grouped tcgen05 path as
- * moe_prefill, with the same exact routing.  Host-pool contexts need B == 1 and slots set; every call is
- * one LRU step (the step counter increments per call) and the call returns
- * after the last layer's staging decision, with the compute still enqueued.
- * Waits inside the call are bounded (MOE_ETIMEOUT). */
+ * moe_prefill, with the same exact routing.  Host-pool and expert-file
+ * contexts need B == 1 and slots set; every call is one cache step (the step
+ * counter increments per call).  With host staging (the default) the call
+ * returns after the last layer's staging decision, with the compute still
+ * enqueued; an expert-file context reads its misses on the calling thread
+ * meanwhile.  With MOE_STAGING_DEVICE (moe_set_staging) it returns once every
+ * layer is enqueued, or after the step when a trace is asked for.  Waits
+ * inside the call are bounded (MOE_ETIMEOUT). */
 moe_status moe_decode_step(moe_ctx *ctx, const void *h_in, int B, int layer_begin, int layer_end,
                            const float *logit_bias, void *h_out, float *y_last, moe_trace_rec *trace,
                            int trace_cap, int *trace_len, void *stream);
