@@ -307,10 +307,13 @@ moe_status moe_set_staging(moe_ctx *ctx, int mode);
 /* Two-tier cache (expert file -> pinned host records -> HBM slots): keeps
  * `n_host` records per layer of an expert-file context in pinned host memory
  * in front of the file, so the slot cache's misses come from the file only
- * when the host tier misses too (the goinfer chapter "When the model doesn't
- * fit" and the TurboFieldfare write-up keep recently used experts in memory
- * in front of the model file; here that level is explicit, pinned and
- * bounded).  The host tier follows the slot cache's LRU rules one level down:
+ * when the host tier misses too.  The pages keep a bounded set of experts in
+ * memory in front of the SSD (the TurboFieldfare video walkthrough: 16 per
+ * layer; the goinfer chapter "When the model doesn't fit": weights on disk or
+ * in host memory, streamed as needed); with device memory apart from host
+ * memory, that level sits between the file and the device slots, here
+ * explicit, pinned and bounded.  The host tier follows the slot cache's LRU
+ * rules one level down:
  * per layer and step, the misses it holds refresh their record's last use
  * (the step counter); the others, in top-k order, take the record with the
  * smallest (last use, record index) among those the step has not touched
