@@ -25,7 +25,8 @@ def np_fp16(bits):
 
 
 def np_bf16(bits):
-    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):   # signalling-NaN patterns widen to NaN
+        return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def dense_dequant(q, sb, group=64):

@@ -36,7 +36,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks_aggregate_max_time_and_summed_units():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:   # no fork of this multi-threaded process
         out = m.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         for rank in range(world):
