@@ -54,8 +54,23 @@ def bytes_per_token_layer(sh) -> dict:
             "gateup_gelu_gemv": gu_s + sh.top_k * gu_r,
             "down_combine_gemv": dn_s + sh.top_k * dn_r,
             "ffn_total": ffn,
-            # one launch of the persistent kernel runs the token through every layer
+            # one launch of the single-launch kernel runs the token through every layer
             "decode_persistent": N_LAYERS * (router + ffn)}
+
+
+# The kernel function a profiled kind times at the benchmark's shape (the
+# clustered persistent kernel is the default single-launch decode kernel).
+KERNEL_FUNCTION = {"decode_persistent": "k_decode_cluster"}
+
+
+def algorithmic_bytes(bpl: dict, kind: str):
+    """(FFN bytes, router bytes) of one launch of kind: the FFN bytes are the
+    selected experts plus the shared expert, the router rows apart."""
+    if kind == "decode_persistent":
+        return N_LAYERS * bpl["ffn_total"], N_LAYERS * bpl["router_topk_plan"]
+    if kind == "router_topk_plan":
+        return 0, bpl[kind]
+    return bpl[kind], 0
 
 
 def config_dict(sh):
@@ -114,12 +129,13 @@ class ClockSampler:
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.file = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -127,9 +143,22 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
+            # the timed region starts only once the sampler is writing rows
+            deadline = time.time() + 10.0
+            while time.time() < deadline:
+                if os.path.getsize(self.file.name) > 0:
+                    break
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
+
+    def mark(self, start: bool):
+        """Host wall-clock bounds of the timed region (rows outside it are not counted)."""
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -148,22 +177,76 @@ class ClockSampler:
             os.unlink(self.file.name)
         except Exception:
             return None
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
-            try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-            except (ValueError, IndexError):
-                continue
-            for i, n in enumerate(names):
-                if len(r) > 5 + i and r[5 + i].lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return clock_summary(rows, self.t0, self.t1)
+
+
+def _smi_time(ts: str):
+    import datetime
+    for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+        try:
+            return datetime.datetime.strptime(ts.strip(), fmt).timestamp()
+        except ValueError:
+            continue
+    return None
+
+
+def clock_summary(rows, t0=None, t1=None):
+    """Median SM clock, max clock and active throttle reasons of the nvidia-smi
+    rows whose timestamp lies in the timed region [t0, t1] (all rows when the
+    bounds or the timestamps are missing)."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    total = 0
+    for r in rows:
+        r = [x.strip() for x in r]
+        try:
+            smv, mxv = float(r[1]), float(r[2])
+        except (ValueError, IndexError):
+            continue
+        total += 1
+        ts = _smi_time(r[9]) if len(r) > 9 else None
+        if t0 is not None and t1 is not None and ts is not None and not (t0 - 0.025 <= ts <= t1 + 0.025):
+            continue
+        sm.append(smv)
+        mx.append(mxv)
+        for i, n in enumerate(names):
+            if len(r) > 5 + i and r[5 + i].lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+           "samples": len(sm), "samples_total": total}
+    if t0 is not None and t1 is not None:
+        out["region_s"] = round(t1 - t0, 4)
+        out["sm_mhz_x_s"] = round(statistics.median(sm) * (t1 - t0), 2)
+    return out
+
+
+def time_k_steps(run_k, stream, clk, min_seconds: float = 1.0, max_reps: int = 400):
+    """Time regions of exactly K steps (run_k(rep) enqueues one region), each
+    bracketed by CUDA events on the launch stream, back to back until at least
+    min_seconds have passed, so the clock sampler sees the timed work.  Returns
+    (seconds over all regions, regions)."""
+    import math
+
+    import torch
+
+    def region(rep):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run_k(rep)
+        e1.record(stream)
+        return e0, e1
+
+    clk.mark(True)
+    first = region(0)
+    first[1].synchronize()
+    t_first = first[0].elapsed_time(first[1]) / 1e3
+    reps = max(1, min(max_reps, int(math.ceil(min_seconds / max(t_first, 1e-6)))))
+    pairs = [first] + [region(r) for r in range(1, reps)]
+    pairs[-1][1].synchronize()
+    clk.mark(False)
+    return sum(a.elapsed_time(b) for a, b in pairs) / 1e3, reps
 
 
 def dist_env():
@@ -335,20 +418,20 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
 
-    # timed region: K graph-replayed decode steps, CUDA events on the launch stream
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        e0.record(stream)
+    # timed regions of exactly K decode steps each (CUDA events on the launch
+    # stream), repeated back to back for at least a second so that the clock
+    # record covers them
+    def run_k(rep):
         for i in range(args.steps):
-            step(args.warmup + i)
-        e1.record(stream)
-        e1.synchronize()
+            step(args.warmup + rep * args.steps + i)
+
+    with ClockSampler(local) as clk:
+        elapsed, reps = time_k_steps(run_k, stream, clk, args.min_seconds)
     moe.check(moe.moe_sync(ctx, stream), ctx)
-    elapsed = e0.elapsed_time(e1) / 1e3
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    t_max, units = aggregate(dist, elapsed, float(args.steps))
+    t_max, units = aggregate(dist, elapsed, float(args.steps * reps))
     value = units / t_max
     clocks = clk.result()
 
@@ -366,7 +449,10 @@ def run_ours(args):
     dur = kinds[dom]["ms"] / kinds[dom]["launches"] / 1e3
     launches_per_step = sum(v["launches"] for v in kinds.values()) / n_prof
     peak, peak_kind = load_peaks()
-    achieved = bpl[dom] / dur / 1e9
+    # the roofline counts the FFN bytes (selected experts + shared expert); the
+    # router rows are listed apart
+    ffn_launch, router_launch = algorithmic_bytes(bpl, dom)
+    achieved = ffn_launch / dur / 1e9
     traffic = load_traffic().get(dom)
     shares = {k: round(v["ms"] / sum(x["ms"] for x in kinds.values()), 4) for k, v in kinds.items()}
 
@@ -408,19 +494,20 @@ def run_ours(args):
         ffn_bytes = bpl["ffn_total"] * N_LAYERS
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp16xint4->f32 (router int64)",
+            "timed_repeats": reps, "warmup": args.warmup, "ms_per_step": t_max / (args.steps * reps) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp16xint4->f32 (router int64)",
             "data": "synthetic", "config": config_dict(sh),
             "hbm_roofline_frac_8tbs": value / ws * ffn_bytes / NOMINAL_HBM,
             "bytes_per_token": ffn_bytes,
-            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": traffic, "bytes_per_launch": bpl[dom],
-                         "avg_launch_us": dur * 1e6},
+            "roofline": {"bound": "hbm", "kernel": KERNEL_FUNCTION.get(dom, dom), "achieved": achieved,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "bytes_per_launch": ffn_launch,
+                         "router_bytes_per_launch": router_launch, "avg_launch_us": dur * 1e6},
             "kernel_shares": shares,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": sh.d * 2 + N_LAYERS * sh.n_experts * 4,
                     "d2h_bytes_per_step": sh.d * 2},
-            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "gpu_launches": int(round(launches_per_step * args.steps * reps)),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
@@ -546,11 +633,13 @@ def run_ours_prefill(args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        clk.mark(True)
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         e1.synchronize()
+        clk.mark(False)
     moe.check(moe.moe_sync(ctx, stream), ctx)
     elapsed = e0.elapsed_time(e1) / 1e3
     if dist is not None:
@@ -683,11 +772,13 @@ def run_ours_batched(args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        clk.mark(True)
         e0.record(stream)
         for i in range(args.steps):
             step(i)
         e1.record(stream)
         e1.synchronize()
+        clk.mark(False)
     moe.check(moe.moe_sync(ctx, stream), ctx)
     t_max, units = aggregate(dist, e0.elapsed_time(e1) / 1e3, float(args.steps * BATCH))
     value = units / t_max
@@ -985,6 +1076,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the K-step timed region until this much device time has passed")
     ap.add_argument("--workload", choices=["decode", "prefill", "batched", "pool"], default="decode",
                     help="decode: the B=1 30-layer decode stack (the headline); prefill: T=4096 tokens per "
                          "step; batched: B=32 tokens per step; pool: host expert pool + LRU slot sweep")
