@@ -24,6 +24,7 @@ MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
 HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6
 HOOK_PREFILL_TC = 7
 HOOK_CLUSTER = 9
+HOOK_SPIN_LIMIT = 10      # bounded waits of the clustered decode kernel: cycles (<= 0: the default)
 
 
 class MoeConfig(C.Structure):

@@ -18,8 +18,9 @@
 //   the unit's down block by the 64 values once all eight tiles have arrived.
 //
 // The grid-wide exchanges left per layer are the router logits (one router
-// row per CTA, published with a per-launch tag inside each 64-bit word, so a
-// reader polls the data itself) and the layer output: each CTA sums its units'
+// row per CTA, published with a per-launch tag inside each 64-bit word into
+// one replica per cluster, so a cluster's top-k warps poll their own copy
+// and the readers do not crowd a single set of lines) and the layer output: each CTA sums its units'
 // down partials (gate-weighted, fixed order) for its d/4 rows, rounds them onto
 // a 2^-32 fixed-point grid and adds (v << 8) + 1 per row into the layer's int64
 // output vector with one bulk reduction (TMA engine, integer adds in L2, so the
@@ -69,7 +70,7 @@ constexpr int kMaxU = kCMaxUnits;                 // units per cluster and layer
 constexpr int kMaxRows = kMaxD / kCl;             // down output rows per CTA
 constexpr int kMaxTasks = 3 * kMaxU + 1;
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr unsigned kPollSleepNs = 200;             // back-off between polls of data every CTA reads
+constexpr unsigned kPollSleepNs = 32;              // back-off between polls of the cluster's logit replica
 
 static_assert(kCThreads == 32 * (kNC + 2), "producer warp, 16 consumer warps, top-k warp");
 static_assert(kCl == 4, "the a push maps 32 lanes onto 4 ranks x 8 fragment words; 8 tiles = 4 ranks x 2");
@@ -116,6 +117,7 @@ struct Smem {
   long long rlog[kNC];
   int32_t ids[2][32];
   float gates[2][32];
+  alignas(8) long long topv[32];                   // top-k logits in rank order
 };
 
 static_assert(offsetof(Smem, ring) % 128 == 0 && kSlotBytes % 128 == 0, "TMA targets 128-byte aligned");
@@ -161,22 +163,38 @@ __device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
 }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+__device__ __forceinline__ bool aborted(const CParams& p);
+
 // Bounded wait for an mbarrier phase completed by arrivals from other CTAs of
-// the cluster (acquire at cluster scope).
-__device__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* err) {
+// the cluster (acquire at cluster scope).  False after p.spin_limit cycles or
+// once another CTA has aborted.
+__device__ bool mbar_wait_cluster(const CParams& p, uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
-  for (;;) {
+  for (unsigned it = 0;; ++it) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
+        "{\n\t.reg .pred q;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 q, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
         : "memory");
     if (ok) return true;
-    if (clock64() - t0 > kSpinLimitCycles) {
-      atomicOr(err, ERR_WAIT_TIMEOUT);
+    if (clock64() - t0 > p.spin_limit || ((it & 15) == 15 && aborted(p))) {
+      atomicOr(p.err, ERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded wait on a phase of a local mbarrier (this CTA's threads or copies).
+__device__ bool wait_local(const CParams& p, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > p.spin_limit || ((it & 15) == 0 && aborted(p))) {
+      atomicOr(p.err, ERR_WAIT_TIMEOUT);
       return false;
     }
   }
@@ -216,7 +234,7 @@ __device__ __forceinline__ void raise_abort(const CParams& p) {
 __device__ bool consumer_barrier(const CParams& p, Smem& S, int round) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbarrier_arrive(&S.cbar);
-  const bool ok = mbar_wait_bounded(&S.cbar, static_cast<uint32_t>(round - 1) & 1u, p.err);
+  const bool ok = wait_local(p, &S.cbar, static_cast<uint32_t>(round - 1) & 1u);
   if (!ok) raise_abort(p);
   __syncwarp();
   return ok;
@@ -244,7 +262,7 @@ __device__ bool poll_rows(const CParams& p, const long long* rows2, bool valid, 
     __nanosleep(64);
     if ((it & 255) == 255) {
       if (__any_sync(kFull, aborted(p))) return false;
-      if (__any_sync(kFull, clock64() - t0 > kSpinLimitCycles)) {
+      if (__any_sync(kFull, clock64() - t0 > p.spin_limit)) {
         if ((threadIdx.x & 31) == 0) raise_abort(p);
         return false;
       }
@@ -365,7 +383,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L->dn_shared)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L->dn_routed)) : "memory");
     if (static_cast<int>(blockIdx.x) < p.E) {
-      if (!mbar_wait_bounded(&S.rrow_empty, (static_cast<uint32_t>(rel) & 1u) ^ 1u, p.err)) {
+      if (!wait_local(p, &S.rrow_empty, (static_cast<uint32_t>(rel) & 1u) ^ 1u)) {
         raise_abort(p);
         break;
       }
@@ -378,7 +396,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
     for (int i = 0; i < S.n_tasks; ++i) {
       const CTask t = S.tasks[i];
       if (t.kind == K_TOPK) {
-        if (!mbar_wait_bounded(&S.topk_bar, static_cast<uint32_t>(rel) & 1u, p.err)) {
+        if (!wait_local(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {
           raise_abort(p);
           stop = true;
           break;
@@ -387,7 +405,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
       }
       const uint32_t u = static_cast<uint32_t>(rel) * S.n_stages + s++;
       const int slot = u % kNS;
-      if (!mbar_wait_bounded(&S.empty[slot], ((u / kNS) & 1u) ^ 1u, p.err)) {
+      if (!wait_local(p, &S.empty[slot], ((u / kNS) & 1u) ^ 1u)) {
         raise_abort(p);
         stop = true;
         break;
@@ -421,23 +439,24 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
 
 // ------------------------------------------------------------------ top-k
 
-// Polls layer l's tagged logits until every entry carries this launch's tag,
-// then takes the top-k (ties to the lower index) and the softmax gates.  Each
-// lane holds up to NPL logits (4 for at most 128 experts, else 8) sorted by
-// (value desc, index asc); a round picks
-// the warp-wide best head with three warp reductions on the order-preserving
-// unsigned image of the int64 logit and on the index.
+// Polls the cluster's replica of layer l's tagged logits until every entry
+// carries this launch's tag, then takes the top-k (ties to the lower index)
+// and the softmax gates.  Each lane holds up to NPL logits (4 for at most 128
+// experts, else 8) sorted by (value desc, index asc); a round picks the
+// warp-wide best head with one reduction on the high 32 bits of the
+// order-preserving unsigned image of the int64 logit, and further reductions
+// (low bits, then index) only when several heads tie there; the winning lane
+// records it directly.
 template <int NPL>
-__device__ bool topk_layer(const CParams& p, int l, int32_t* ids, float* gates) {
+__device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float* gates) {
   const int lane = threadIdx.x & 31;
-  const unsigned long long* lg = p.tlog + static_cast<size_t>(l) * p.E * 2;
+  const unsigned cl = cluster_idx(), n_cl = cluster_count();
+  const unsigned long long* lg = p.tlog + (static_cast<size_t>(l) * n_cl + cl) * p.E * 2;
   unsigned long long key[NPL];
   int idx[NPL];
-  int n = 0;
   const long long t0 = clock64();
   for (unsigned it = 0;; ++it) {
     bool ok = true;
-    n = 0;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       const int e = lane + 32 * i;
@@ -448,41 +467,37 @@ __device__ bool topk_layer(const CParams& p, int l, int32_t* ids, float* gates) 
         ok = ok && static_cast<unsigned>(v.x >> 32) == p.tag && static_cast<unsigned>(v.y >> 32) == p.tag;
         key[i] = ((v.y << 32) | (v.x & 0xFFFFFFFFull)) ^ 0x8000000000000000ull;
         idx[i] = e;
-        ++n;
       }
     }
     if (__all_sync(kFull, ok)) {
       if (lane == 0) stamp(p, l - p.l0, EV_LOGITS_IN);
       break;
     }
-    // every CTA polls the same 16 lines: back off so the pollers do not
-    // crowd out the stores they wait for
     __nanosleep(kPollSleepNs);
-    if ((it & 255) == 255) {
+    if ((it & 63) == 63) {
       if (__any_sync(kFull, aborted(p))) return false;
-      if (__any_sync(kFull, clock64() - t0 > kSpinLimitCycles)) {
+      if (__any_sync(kFull, clock64() - t0 > p.spin_limit)) {
         if (lane == 0) raise_abort(p);
         return false;
       }
     }
   }
+  // absent entries (key 0, index max) sort last and are never picked (k <= E)
 #pragma unroll
   for (int i = 1; i < NPL; ++i) {
 #pragma unroll
     for (int j = i; j > 0; --j) {
-      if (key[j] > key[j - 1]) {
-        const unsigned long long tk = key[j];
-        key[j] = key[j - 1];
-        key[j - 1] = tk;
-        const int ti = idx[j];
-        idx[j] = idx[j - 1];
-        idx[j - 1] = ti;
-      }
+      const bool sw = key[j] > key[j - 1];
+      const unsigned long long tk = sw ? key[j] : key[j - 1];
+      key[j] = sw ? key[j - 1] : key[j];
+      key[j - 1] = tk;
+      const int ti = sw ? idx[j] : idx[j - 1];
+      idx[j] = sw ? idx[j - 1] : idx[j];
+      idx[j - 1] = ti;
     }
   }
   if (lane == 0) stamp(p, l - p.l0, EV_TOPK_SORTED);
-  int head = 0, my_id = 0;
-  long long my_v = 0;
+  int head = 0;
   for (int j = 0; j < p.k; ++j) {
     unsigned long long hk = 0ull;
     int he = 0x7fffffff;
@@ -492,29 +507,31 @@ __device__ bool topk_layer(const CParams& p, int l, int32_t* ids, float* gates) 
         hk = key[i];
         he = idx[i];
       }
-    const bool has = head < n;
-    const unsigned hi = has ? static_cast<unsigned>(hk >> 32) : 0u;
-    const unsigned lo = has ? static_cast<unsigned>(hk) : 0u;
+    const unsigned hi = static_cast<unsigned>(hk >> 32), lo = static_cast<unsigned>(hk);
     const unsigned mh = __reduce_max_sync(kFull, hi);
-    const bool c1 = has && hi == mh;
-    const unsigned ml = __reduce_max_sync(kFull, c1 ? lo : 0u);
-    const bool c2 = c1 && lo == ml;
-    const unsigned me = __reduce_min_sync(kFull, c2 ? static_cast<unsigned>(he) : 0xFFFFFFFFu);
-    if (c2 && static_cast<unsigned>(he) == me) ++head;
-    if (lane == j) {
-      my_id = static_cast<int>(me);
-      my_v = static_cast<long long>((static_cast<unsigned long long>(mh) << 32 | ml) ^ 0x8000000000000000ull);
+    bool c = hi == mh;
+    unsigned bal = __ballot_sync(kFull, c);
+    if (__popc(bal) > 1) {
+      const unsigned ml = __reduce_max_sync(kFull, c ? lo : 0u);
+      c = c && lo == ml;
+      bal = __ballot_sync(kFull, c);
+      if (__popc(bal) > 1) {
+        const unsigned me = __reduce_min_sync(kFull, c ? static_cast<unsigned>(he) : 0xFFFFFFFFu);
+        c = c && static_cast<unsigned>(he) == me;
+      }
+    }
+    if (c) {
+      ids[j] = he;
+      S.topv[j] = static_cast<long long>(hk ^ 0x8000000000000000ull);
+      ++head;
     }
   }
-  const long long top = __shfl_sync(kFull, my_v, 0);
+  __syncwarp();
   float ex = 0.f;
-  if (lane < p.k) ex = expf(__ll2float_rn(my_v - top) * 9.094947017729282e-13f);
+  if (lane < p.k) ex = expf(__ll2float_rn(S.topv[lane] - S.topv[0]) * 9.094947017729282e-13f);   // 2^-40
   float sum = 0.f;
   for (int j = 0; j < p.k; ++j) sum += __shfl_sync(kFull, ex, j);
-  if (lane < p.k) {
-    ids[lane] = my_id;
-    gates[lane] = ex / sum;
-  }
+  if (lane < p.k) gates[lane] = ex / sum;
   __syncwarp();
   return true;
 }
@@ -525,7 +542,8 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
   for (int rel = 0; rel < n_rel; ++rel) {
     int32_t* sid = S.ids[rel & 1];
     float* sg = S.gates[rel & 1];
-    const bool ok = p.E <= 128 ? topk_layer<4>(p, p.l0 + rel, sid, sg) : topk_layer<8>(p, p.l0 + rel, sid, sg);
+    const bool ok =
+        p.E <= 128 ? topk_layer<4>(p, S, p.l0 + rel, sid, sg) : topk_layer<8>(p, S, p.l0 + rel, sid, sg);
     if (!ok) return;
     if (lane == 0) stamp(p, rel, EV_TOPK_DONE);
     if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
@@ -638,7 +656,7 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
       arrive_peer(peer_addr(&S.clbar, r));
     }
     __syncwarp();
-    if (!mbar_wait_cluster(&S.clbar, static_cast<uint32_t>(rel - 1) & 1u, p.err)) {
+    if (!mbar_wait_cluster(p, &S.clbar, static_cast<uint32_t>(rel - 1) & 1u)) {
       raise_abort(p);
       return false;
     }
@@ -661,7 +679,7 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
   // warp adds its elements' exact products (RNE onto the 2^-40 grid, integer
   // sums, so the split does not change the logit) and leaves one partial
   const bool routes = static_cast<int>(blockIdx.x) < p.E;
-  if (routes && !mbar_wait_bounded(&S.rrow_full, static_cast<uint32_t>(rel) & 1u, p.err)) {
+  if (routes && !wait_local(p, &S.rrow_full, static_cast<uint32_t>(rel) & 1u)) {
     raise_abort(p);
     return false;
   }
@@ -724,22 +742,28 @@ __device__ void router_publish(const CParams& p, Smem& S, int cw, int rel) {
   if (static_cast<int>(blockIdx.x) >= p.E || cw != 0) return;
   const int lane = threadIdx.x & 31;
   if (lane == 0) stamp(p, rel, EV_ROUTER_B);
+  // every lane forms the same logit (the warps' parts in warp order, plus the bias)
   long long acc = 0;
   for (int w = 0; w < kNC; ++w) acc += S.rlog[w];
-  if (lane == 0) {
-    mbarrier_arrive(&S.rrow_empty);   // every warp read the row before the barrier
-    const DevCallArgs* A = &S.args;
-    if (A->bias) {
-      const float bv = A->bias[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.E + blockIdx.x];
-      if (!(fabsf(bv) < 1048576.f)) atomicOr(p.err, ERR_ROUTER_DOMAIN);
-      else acc += __float2ll_rn(bv * 1099511627776.0f);
+  const DevCallArgs* A = &S.args;
+  if (A->bias) {
+    const float bv = A->bias[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.E + blockIdx.x];
+    if (!(fabsf(bv) < 1048576.f)) {
+      if (lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);
+    } else {
+      acc += __float2ll_rn(bv * 1099511627776.0f);
     }
-    const unsigned long long tg = static_cast<unsigned long long>(p.tag) << 32;
-    const unsigned long long ua = static_cast<unsigned long long>(acc);
-    st_volatile_u64x2(p.tlog + (static_cast<size_t>(p.l0 + rel) * p.E + blockIdx.x) * 2, (ua & 0xFFFFFFFFull) | tg,
-                      (ua >> 32) | tg);
-    stamp(p, rel, EV_LOGIT_OUT);
   }
+  __syncwarp();
+  if (lane == 0) mbarrier_arrive(&S.rrow_empty);   // every warp read the row before the barrier
+  const long long logit = acc;
+  const unsigned long long tg = static_cast<unsigned long long>(p.tag) << 32;
+  const unsigned long long ua = static_cast<unsigned long long>(logit);
+  const unsigned n_cl = cluster_count();
+  for (unsigned c = lane; c < n_cl; c += 32)
+    st_volatile_u64x2(p.tlog + ((static_cast<size_t>(p.l0 + rel) * n_cl + c) * p.E + blockIdx.x) * 2,
+                      (ua & 0xFFFFFFFFull) | tg, (ua >> 32) | tg);
+  if (lane == 0) stamp(p, rel, EV_LOGIT_OUT);
   __syncwarp();
 }
 
@@ -883,7 +907,7 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
                          unsigned long long* t_ready) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int aslot = (rel & 1) * kMaxU + t.ui;
-  if (!mbar_wait_cluster(&S.a_full[aslot], (static_cast<uint32_t>(rel) >> 1) & 1u, p.err)) return false;
+  if (!mbar_wait_cluster(p, &S.a_full[aslot], (static_cast<uint32_t>(rel) >> 1) & 1u)) return false;
   if (lane == 0) {
     stamp(p, rel, EV_DN_A_FIRST);
     stamp(p, rel, EV_A_WAIT_LAST, true);
@@ -931,7 +955,7 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
 // counts).
 __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round, unsigned rank) {
   const int lane = threadIdx.x & 31;
-  if (!mbar_wait_bounded(&S.topk_bar, static_cast<uint32_t>(rel) & 1u, p.err)) {   // gates of this layer
+  if (!wait_local(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {   // gates of this layer
     raise_abort(p);
     return false;
   }
@@ -950,7 +974,8 @@ __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round
         const int src = S.unit_src[u];
         y = fmaf(src < 0 ? 1.f : gts[src], S.dn_part[u][i], y);
       }
-      // |y| < 2^17: (v << 8) summed over up to 255 clusters stays inside int64
+      // |y| < 2^17 (v < 2^49 on the 2^-32 grid): with at most 64 clusters the
+      // int64 sum of (v << 8) stays below 2^63 (the host checks the count)
       const bool ok = fabsf(y) < 131072.f;
       bad |= !ok;
       S.yq[i] = (ok ? (__float2ll_rn(y * 4294967296.f) << 8) : 0ll) + 1;   // + 1: this CTA's count
@@ -1029,7 +1054,7 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
       if (static_cast<int>(u % kNQ) != quad) continue;
       const int slot = u % kNS;
       const unsigned long long t0 = p.timeline ? now_ns() : 0ull;
-      if (!mbar_wait_bounded(&S.full[slot], (u / kNS) & 1u, p.err)) {
+      if (!wait_local(p, &S.full[slot], (u / kNS) & 1u)) {
         raise_abort(p);
         return;
       }

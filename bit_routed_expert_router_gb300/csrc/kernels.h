@@ -85,8 +85,9 @@ struct CParams {
   long long expert_stride;
   const CLayer* layers;                // [n_layers]
   const DevCallArgs* args;
-  unsigned long long* tlog;            // [n_layers][E][2]: logit low / high word, each | tag << 32
+  unsigned long long* tlog;            // [n_layers][n_cl][E][2]: per cluster, logit low / high word, each | tag << 32
   unsigned tag;                        // this launch's tag (never 0)
+  long long spin_limit;                // bounded waits give up after this many cycles
   long long* ybuf;                     // [3][d] layer outputs: sum over CTAs of (v << 8) + 1, v on the 2^-32 grid;
                                        // zero between launches
   unsigned* exit_cnt;

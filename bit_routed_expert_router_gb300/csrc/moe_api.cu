@@ -168,7 +168,8 @@ struct moe_ctx {
   bool use_cluster = true;             // test hook 9
   int c_grid = 0;                      // CTAs: resident clusters x kCCluster
   CLayer* c_layers = nullptr;          // device [n_layers]
-  unsigned long long* c_tlog = nullptr;  // [n_layers][E][2] tagged logits
+  unsigned long long* c_tlog = nullptr;  // [n_layers][n_cl][E][2] tagged logits, one replica per cluster
+  long long spin_limit = 4000000000LL; // test hook 10: wait limit (cycles) of the clustered kernel's bounded waits
   long long* c_ybuf = nullptr;         // [3][d] fixed-point layer outputs
   unsigned* c_counters = nullptr;      // exit counter, abort flag
   unsigned c_tag = 0;                  // tag of the last launch
@@ -510,7 +511,8 @@ moe_status cluster_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   p.layers = ctx->c_layers;
   p.args = ctx->dargs;
   if (++ctx->c_tag == 0) {   // tags wrapped: no stale entry may carry the new one
-    CK(cudaMemsetAsync(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * c.n_experts * 16, s));
+    CK(cudaMemsetAsync(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * (ctx->c_grid / kCCluster) * c.n_experts * 16,
+                       s));
     ctx->c_tag = 1;
   }
   p.tlog = ctx->c_tlog;
@@ -520,6 +522,7 @@ moe_status cluster_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   p.abort_flag = ctx->c_counters + 1;
   p.err = ctx->err_word;
   p.timeline = ctx->p_timeline;
+  p.spin_limit = ctx->spin_limit;
   PROF(3, s);
   CK(launch_cluster(p, ctx->c_grid, s));
   PROF(-1, s);
@@ -920,7 +923,6 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->p_part = dalloc<float>(static_cast<size_t>(2) * pparts * c.d, o, nb);
   ctx->p_gates = dalloc<float>(static_cast<size_t>(c.n_layers) * c.top_k, o, nb);
   ctx->c_layers = dalloc<CLayer>(c.n_layers, o, nb);
-  ctx->c_tlog = dalloc<unsigned long long>(static_cast<size_t>(c.n_layers) * c.n_experts * 2, o, nb);
   ctx->c_ybuf = dalloc<long long>(static_cast<size_t>(3) * c.d, o, nb);
   ctx->c_counters = dalloc<unsigned>(2, o, nb);
   for (void* ptr : o)
@@ -936,7 +938,6 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       cudaMemset(ctx->p_exit, 0, 8) != cudaSuccess ||
       cudaMemset(ctx->p_layers, 0, sizeof(PLayer) * c.n_layers) != cudaSuccess ||
       cudaMemset(ctx->c_layers, 0, sizeof(CLayer) * c.n_layers) != cudaSuccess ||
-      cudaMemset(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * c.n_experts * 16) != cudaSuccess ||
       cudaMemset(ctx->c_ybuf, 0, static_cast<size_t>(3) * c.d * 8) != cudaSuccess ||
       cudaMemset(ctx->c_counters, 0, 8) != cudaSuccess)
     return bail(MOE_ECUDA);
@@ -977,14 +978,20 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     cudaGetLastError();
   }
   // the clustered decode kernel: one router row per CTA, at most kCMaxUnits
-  // (source, group) units per cluster and layer, its shared memory, and a
-  // cooperative launch of every resident cluster
+  // (source, group) units per cluster and layer, its shared memory, a
+  // cooperative launch of every resident cluster, and at most 64 clusters (the
+  // range of its int64 layer-output sums)
   {
     int n_cl = 0;
     if (c.top_k <= 32 && c.d <= kCMaxD && cluster_smem() + 2048 <= static_cast<size_t>(max_smem) &&
         cluster_attrs() == cudaSuccess &&
-        cluster_max_active(&n_cl) == cudaSuccess && n_cl >= 1 && c.n_experts <= n_cl * kCCluster &&
+        cluster_max_active(&n_cl) == cudaSuccess && n_cl >= 1 && n_cl <= 64 && c.n_experts <= n_cl * kCCluster &&
         cluster_units_max(c, n_cl) <= cluster_max_units()) {
+      // the tagged logits, one replica per cluster of every layer
+      ctx->c_tlog = dalloc<unsigned long long>(static_cast<size_t>(c.n_layers) * n_cl * c.n_experts * 2, o, nb);
+      if (!ctx->c_tlog) return bail(MOE_ENOMEM);
+      if (cudaMemset(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * n_cl * c.n_experts * 16) != cudaSuccess)
+        return bail(MOE_ECUDA);
       ctx->c_ok = true;
       ctx->c_grid = n_cl * kCCluster;
     }
@@ -1898,6 +1905,9 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
       if (value != 0 && !ctx->p_ok && !ctx->c_ok)
         return fail(ctx, MOE_ESTATE, "persistent decode kernel unavailable for this configuration or device");
       ctx->use_persistent = value != 0;
+      return MOE_OK;
+    case 10:  // bounded waits of the clustered decode kernel give up after `value` cycles (<= 0: the default, ~2 s)
+      ctx->spin_limit = value > 0 ? value : 4000000000LL;
       return MOE_OK;
     case 6:  // budget checks see `value` bytes of free device memory (-1: the real figure)
       ctx->hook_free_bytes = value;
