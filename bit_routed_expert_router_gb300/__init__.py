@@ -24,7 +24,8 @@ MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
 HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6
 HOOK_PREFILL_TC = 7
 HOOK_CLUSTER = 9
-HOOK_SPIN_LIMIT = 10      # bounded waits of the clustered decode kernel: cycles (<= 0: the default)
+HOOK_SPIN_LIMIT = 10      # bounded waits of the persistent decode kernels: cycles (<= 0: the default)
+HOOK_AT_REST = 11         # MOE_OK when the persistent kernels' launch words are back at rest
 
 
 class MoeConfig(C.Structure):
@@ -85,6 +86,7 @@ _SIGS = {
     "moe_prefill": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                               C.c_void_p, C.c_void_p]),
     "moe_set_debug": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int]),
+    "moe_set_debug_logits": (C.c_int, [C.c_void_p, C.c_void_p]),
     "moe_sync": (C.c_int, [C.c_void_p, C.c_void_p]),
     "moe_get_stats": (C.c_int, [C.c_void_p, C.POINTER(MoeStats)]),
     "moe_get_cache_state": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]),
@@ -231,6 +233,10 @@ def moe_prefill(ctx, h, T: int, layer_begin: int, layer_end: int, logit_bias=Non
 
 def moe_set_debug(ctx, x_layers=None, ids=None, gates=None, y_layers=None, max_layers: int = 0) -> int:
     return lib().moe_set_debug(ctx, _ptr(x_layers), _ptr(ids), _ptr(gates), _ptr(y_layers), max_layers)
+
+
+def moe_set_debug_logits(ctx, logits=None) -> int:
+    return lib().moe_set_debug_logits(ctx, _ptr(logits))
 
 
 def moe_sync(ctx, stream=None) -> int:

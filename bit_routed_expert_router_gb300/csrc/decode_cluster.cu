@@ -166,8 +166,9 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 __device__ __forceinline__ bool aborted(const CParams& p);
 
 // Bounded wait for an mbarrier phase completed by arrivals from other CTAs of
-// the cluster (acquire at cluster scope).  False after p.spin_limit cycles or
-// once another CTA has aborted.
+// the cluster (acquire at cluster scope), by a whole warp: the lanes decide
+// together (a vote per poll), so a warp never splits between going on and
+// giving up.  False after p.spin_limit cycles or once another CTA has aborted.
 __device__ bool mbar_wait_cluster(const CParams& p, uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
   for (unsigned it = 0;; ++it) {
@@ -179,16 +180,30 @@ __device__ bool mbar_wait_cluster(const CParams& p, uint64_t* bar, uint32_t pari
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
         : "memory");
-    if (ok) return true;
-    if (clock64() - t0 > p.spin_limit || ((it & 15) == 15 && aborted(p))) {
-      atomicOr(p.err, ERR_WAIT_TIMEOUT);
+    if (__all_sync(kFull, ok != 0)) return true;
+    if (__any_sync(kFull, clock64() - t0 > p.spin_limit || ((it & 15) == 15 && aborted(p)))) {
+      if ((threadIdx.x & 31) == 0) atomicOr(p.err, ERR_WAIT_TIMEOUT);
       return false;
     }
   }
 }
 
-// Bounded wait on a phase of a local mbarrier (this CTA's threads or copies).
-__device__ bool wait_local(const CParams& p, uint64_t* bar, uint32_t parity) {
+// Bounded wait on a phase of a local mbarrier (this CTA's threads or copies)
+// by a whole warp, deciding together as above.
+__device__ bool wait_warp(const CParams& p, uint64_t* bar, uint32_t parity) {
+  if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(kFull, clock64() - t0 > p.spin_limit || ((it & 15) == 0 && aborted(p)))) {
+      if ((threadIdx.x & 31) == 0) atomicOr(p.err, ERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// The same wait by a single thread (the producer).
+__device__ bool wait_one(const CParams& p, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (unsigned it = 1;; ++it) {
@@ -234,7 +249,7 @@ __device__ __forceinline__ void raise_abort(const CParams& p) {
 __device__ bool consumer_barrier(const CParams& p, Smem& S, int round) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbarrier_arrive(&S.cbar);
-  const bool ok = wait_local(p, &S.cbar, static_cast<uint32_t>(round - 1) & 1u);
+  const bool ok = wait_warp(p, &S.cbar, static_cast<uint32_t>(round - 1) & 1u);
   if (!ok) raise_abort(p);
   __syncwarp();
   return ok;
@@ -383,7 +398,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L->dn_shared)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L->dn_routed)) : "memory");
     if (static_cast<int>(blockIdx.x) < p.E) {
-      if (!wait_local(p, &S.rrow_empty, (static_cast<uint32_t>(rel) & 1u) ^ 1u)) {
+      if (!wait_one(p, &S.rrow_empty, (static_cast<uint32_t>(rel) & 1u) ^ 1u)) {
         raise_abort(p);
         break;
       }
@@ -396,7 +411,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
     for (int i = 0; i < S.n_tasks; ++i) {
       const CTask t = S.tasks[i];
       if (t.kind == K_TOPK) {
-        if (!wait_local(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {
+        if (!wait_one(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {
           raise_abort(p);
           stop = true;
           break;
@@ -405,7 +420,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
       }
       const uint32_t u = static_cast<uint32_t>(rel) * S.n_stages + s++;
       const int slot = u % kNS;
-      if (!wait_local(p, &S.empty[slot], ((u / kNS) & 1u) ^ 1u)) {
+      if (!wait_one(p, &S.empty[slot], ((u / kNS) & 1u) ^ 1u)) {
         raise_abort(p);
         stop = true;
         break;
@@ -679,7 +694,7 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
   // warp adds its elements' exact products (RNE onto the 2^-40 grid, integer
   // sums, so the split does not change the logit) and leaves one partial
   const bool routes = static_cast<int>(blockIdx.x) < p.E;
-  if (routes && !wait_local(p, &S.rrow_full, static_cast<uint32_t>(rel) & 1u)) {
+  if (routes && !wait_warp(p, &S.rrow_full, static_cast<uint32_t>(rel) & 1u)) {
     raise_abort(p);
     return false;
   }
@@ -757,6 +772,8 @@ __device__ void router_publish(const CParams& p, Smem& S, int cw, int rel) {
   __syncwarp();
   if (lane == 0) mbarrier_arrive(&S.rrow_empty);   // every warp read the row before the barrier
   const long long logit = acc;
+  if (lane == 0 && A->dbg_logits && rel < A->dbg_layers)
+    A->dbg_logits[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.E + blockIdx.x] = logit;
   const unsigned long long tg = static_cast<unsigned long long>(p.tag) << 32;
   const unsigned long long ua = static_cast<unsigned long long>(logit);
   const unsigned n_cl = cluster_count();
@@ -955,7 +972,7 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
 // counts).
 __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round, unsigned rank) {
   const int lane = threadIdx.x & 31;
-  if (!wait_local(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {   // gates of this layer
+  if (!wait_warp(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {   // gates of this layer
     raise_abort(p);
     return false;
   }
@@ -1054,7 +1071,7 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
       if (static_cast<int>(u % kNQ) != quad) continue;
       const int slot = u % kNS;
       const unsigned long long t0 = p.timeline ? now_ns() : 0ull;
-      if (!wait_local(p, &S.full[slot], (u / kNS) & 1u)) {
+      if (!wait_warp(p, &S.full[slot], (u / kNS) & 1u)) {
         raise_abort(p);
         return;
       }

@@ -154,6 +154,8 @@ __global__ void __launch_bounds__(256) k_router(KParams p) {
     for (int i = 0; i < 8; ++i) {
       const int ee = lane + 32 * i;
       v[i] = (ee < E) ? __ldcg(&p.logits[static_cast<size_t>(b) * E + ee]) : LLONG_MIN;
+      if (ee < E && A->dbg_logits && p.rel_layer < A->dbg_layers)
+        A->dbg_logits[(static_cast<size_t>(p.rel_layer) * A->tok_total + A->tok_off + b) * E + ee] = v[i];
     }
     unsigned taken = 0;
 #pragma unroll

@@ -52,6 +52,7 @@ struct DevCallArgs {                   // per-call pointers, written before each
   int32_t* dbg_ids;                    // int32 [L][B][k] or null
   float* dbg_gates;                    // fp32 [L][B][k] or null
   float* dbg_y;                        // fp32 [L][B][d] or null
+  int64_t* dbg_logits;                 // int64 [L][B][E] or null: router logits (bias included), 2^-40 units
   int32_t dbg_layers;
   int32_t B;                           // tokens of this launch
   int32_t tok_total;                   // tokens per layer in bias / debug buffers

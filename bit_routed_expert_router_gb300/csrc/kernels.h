@@ -53,6 +53,7 @@ struct PParams {
   unsigned long long* timeline;        // optional [n_layers][16] event times (ns), null = off
   float* gates_g;                      // [n_layers][k] gates published before any routed work
   int n_layers_tl;                     // rows of the timeline's all-CTA part (= n_layers)
+  long long spin_limit;                // bounded waits give up after this many cycles
 };
 
 size_t persistent_smem();
@@ -129,12 +130,6 @@ struct PfGemm {
   int f_out;
   float* out32;                        // PF_DN_ROUTED: fp32 [T*k][d] by pair; PF_DN_SHARED: fp32 [T][d]
   const int32_t* pair_of_row;          // PF_DN_ROUTED: pair of each expert-ordered row
-  const float* gates;                  // PF_DN_SHARED: [T][k]
-  const float* ytok;                   // PF_DN_SHARED: [T*k][d]
-  const uint16_t* hin;                 // PF_DN_SHARED: residual in, bf16 [T][d]
-  uint16_t* hout;                      // PF_DN_SHARED: bf16 [T][d]
-  float* y_last;                       // PF_DN_SHARED: optional fp32 [T][d]
-  float* dbg_y;                        // PF_DN_SHARED: optional fp32 [T][d]
   uint32_t* err;
   unsigned long long* tl;              // optional: 16 event times (ns) of CTA (0, 0), null = off
 };
@@ -148,7 +143,7 @@ cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float e
 cudaError_t launch_pf_row_stats(const uint16_t* rows, int n, int d, float* n2, float* mx, cudaStream_t s);
 cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
                              int k, float* approx, float* xn2, float* wn2, float* xmax, float* wmax, int32_t* ids,
-                             float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err, int n_sm,
+                             float* gates, int32_t* dbg_ids, float* dbg_gates, int64_t* dbg_logits, uint32_t* err, int n_sm,
                              cudaStream_t s);
 cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int tile, int32_t* cnt, int32_t* row_pair,
                            int32_t* items, int32_t* n_items, cudaStream_t s);

@@ -136,6 +136,7 @@ struct moe_ctx {
   int32_t* dbg_ids = nullptr;
   float* dbg_gates = nullptr;
   float* dbg_y = nullptr;
+  int64_t* dbg_logits = nullptr;
   int dbg_layers = 0;
   // counters
   long long step = 0, steps = 0, staged = 0;
@@ -418,6 +419,10 @@ moe_status put_args(moe_ctx* ctx, const DevCallArgs& a, cudaStream_t s) {
   return MOE_OK;
 }
 
+bool dbg_on(const moe_ctx* ctx) {
+  return ctx->dbg_x || ctx->dbg_ids || ctx->dbg_gates || ctx->dbg_y || ctx->dbg_logits;
+}
+
 DevCallArgs make_args(moe_ctx* ctx, const void* h_in, void* h_out, float* y_last, const float* bias, int B,
                       int tok_total, int tok_off) {
   DevCallArgs a{};
@@ -429,7 +434,8 @@ DevCallArgs make_args(moe_ctx* ctx, const void* h_in, void* h_out, float* y_last
   a.dbg_ids = ctx->dbg_ids;
   a.dbg_gates = ctx->dbg_gates;
   a.dbg_y = ctx->dbg_y;
-  a.dbg_layers = (ctx->dbg_x || ctx->dbg_ids || ctx->dbg_gates || ctx->dbg_y) ? ctx->dbg_layers : 0;
+  a.dbg_logits = ctx->dbg_logits;
+  a.dbg_layers = dbg_on(ctx) ? ctx->dbg_layers : 0;
   a.B = B;
   a.tok_total = tok_total;
   a.tok_off = tok_off;
@@ -568,6 +574,7 @@ moe_status persistent_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   p.timeline = ctx->p_timeline;
   p.gates_g = ctx->p_gates;
   p.n_layers_tl = c.n_layers;
+  p.spin_limit = ctx->spin_limit;
   PROF(3, s);
   CK(launch_persistent(p, ctx->n_sm, s));
   PROF(-1, s);
@@ -1470,7 +1477,8 @@ moe_status pf_layer_route(moe_ctx* ctx, int l, int rel, const uint16_t* hin, int
                     dbg && ctx->dbg_x ? ctx->dbg_x + xo * d : nullptr, ctx->pf_xn2, ctx->pf_xmax, ctx->err_word, s));
   CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_approx,
                       ctx->pf_xn2, L.router_stats, ctx->pf_xmax, L.router_stats + E, ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
-                      dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr, ctx->err_word, ctx->n_sm, s));
+                      dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr,
+                      dbg && ctx->dbg_logits ? ctx->dbg_logits + xo * E : nullptr, ctx->err_word, ctx->n_sm, s));
   CK(launch_pf_plan(ctx->pf_ids, P, E, pf_tile_routed(c, T), ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items,
                     ctx->pf_nitems, s));
   CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
@@ -1682,7 +1690,7 @@ moe_status pf_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const floa
   moe_status st = pf_alloc(ctx);
   if (st != MOE_OK) return st;
   const moe_config& c = ctx->cfg;
-  const bool dbg = ctx->dbg_x || ctx->dbg_ids || ctx->dbg_gates || ctx->dbg_y;
+  const bool dbg = dbg_on(ctx);
   if (ctx->profiling || dbg || T > kPfGraphMaxT || ctx->pf_timeline) {
     st = pf_enqueue(ctx, h, T, l0, l1, logit_bias, h_out, y_last, s);
     if (st != MOE_OK) return st;
@@ -1778,6 +1786,13 @@ moe_status moe_set_debug(moe_ctx* ctx, uint16_t* x_layers, int32_t* ids, float* 
   ctx->dbg_gates = gates;
   ctx->dbg_y = y_layers;
   ctx->dbg_layers = max_layers;
+  return MOE_OK;
+}
+
+moe_status moe_set_debug_logits(moe_ctx* ctx, int64_t* logits) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
+  ctx->dbg_logits = logits;
   return MOE_OK;
 }
 
@@ -1906,9 +1921,32 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
         return fail(ctx, MOE_ESTATE, "persistent decode kernel unavailable for this configuration or device");
       ctx->use_persistent = value != 0;
       return MOE_OK;
-    case 10:  // bounded waits of the clustered decode kernel give up after `value` cycles (<= 0: the default, ~2 s)
+    case 10:  // bounded waits of the persistent decode kernels give up after `value` cycles (<= 0: the default, ~2 s)
       ctx->spin_limit = value > 0 ? value : 4000000000LL;
       return MOE_OK;
+    case 11: {  // MOE_OK when the persistent kernels' launch words are at rest, else MOE_ESTATE (poisoned contexts too)
+      CK(cudaDeviceSynchronize());
+      std::vector<unsigned> w;
+      std::vector<long long> yb;
+      auto take = [&](const unsigned* src, size_t n) -> cudaError_t {
+        if (!src || !n) return cudaSuccess;
+        const size_t o = w.size();
+        w.resize(o + n);
+        return cudaMemcpy(w.data() + o, src, n * 4, cudaMemcpyDeviceToHost);
+      };
+      CK(take(ctx->p_exit, ctx->p_exit ? 2 : 0));
+      CK(take(ctx->p_counters, ctx->p_counters ? static_cast<size_t>(ctx->p_n_counters) : 0));
+      CK(take(ctx->c_counters, ctx->c_counters ? 2 : 0));
+      if (ctx->c_ybuf) {
+        yb.resize(static_cast<size_t>(3) * ctx->cfg.d);
+        CK(cudaMemcpy(yb.data(), ctx->c_ybuf, yb.size() * 8, cudaMemcpyDeviceToHost));
+      }
+      for (unsigned v : w)
+        if (v) return MOE_ESTATE;
+      for (long long v : yb)
+        if (v) return MOE_ESTATE;
+      return MOE_OK;
+    }
     case 6:  // budget checks see `value` bytes of free device memory (-1: the real figure)
       ctx->hook_free_bytes = value;
       return MOE_OK;

@@ -14,6 +14,7 @@
 // RMS normalisation of h to bf16, exact fixed-point logits (every fp16 x bf16
 // product rounded half-to-even onto the 2^-40 grid and summed in int64),
 // top-k with ties to the lower expert index, softmax gates over the k picked.
+#include <cstdint>
 #include <mutex>
 
 #include "common.cuh"
@@ -173,6 +174,11 @@ extern "C" moe_status moe_route_noalloc(const moe_config* cfg, const uint16_t* r
   if (cfg->top_k < 1 || cfg->top_k > cfg->n_experts || cfg->top_k > 32) return MOE_EINVAL;
   if (cfg->prenorm != 0 && cfg->prenorm != 1) return MOE_EINVAL;
   if (B < 1 || B > kNaMaxB) return MOE_EINVAL;
+  // the kernel reads router rows and hidden rows 16 bytes at a time
+  if ((reinterpret_cast<uintptr_t>(router_w) | reinterpret_cast<uintptr_t>(h)) & 15u) return MOE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(ids) | reinterpret_cast<uintptr_t>(gates) |
+       reinterpret_cast<uintptr_t>(logit_bias)) & 3u)
+    return MOE_EINVAL;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ECUDA;
   unsigned char* scratch = nullptr;

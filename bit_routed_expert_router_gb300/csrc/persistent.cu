@@ -169,6 +169,35 @@ __device__ __forceinline__ void raise_abort(const PParams& p) {
   atomicExch(p.abort_flag, 1u);
 }
 
+// Bounded wait on a phase of a local mbarrier (this CTA's threads or copies)
+// by a whole warp: the lanes decide together (a vote per poll), so a warp never
+// splits between going on and giving up.  False after p.spin_limit cycles or
+// once another CTA has aborted.
+__device__ bool wait_warp(const PParams& p, uint64_t* bar, uint32_t parity) {
+  if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(0xFFFFFFFFu, clock64() - t0 > p.spin_limit || ((it & 15) == 0 && aborted(p)))) {
+      if ((threadIdx.x & 31) == 0) atomicOr(p.err, ERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// The same wait by a single thread (the producer).
+__device__ bool wait_one(const PParams& p, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > p.spin_limit || ((it & 15) == 0 && aborted(p))) {
+      atomicOr(p.err, ERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // The whole warp waits until *ctr >= target (acquire).  False on abort or
 // timeout.  Every lane polls (the loads of one instruction hit one address, so
 // this costs one request): a loop run by one lane while the others wait leaves
@@ -182,7 +211,7 @@ __device__ bool warp_wait_counter(const PParams& p, const unsigned* ctr, unsigne
     if (__all_sync(0xFFFFFFFFu, ld_acquire(ctr) >= target)) return true;
     if ((it & 255) == 0) {
       if (__any_sync(0xFFFFFFFFu, aborted(p))) return false;
-      if (__any_sync(0xFFFFFFFFu, clock64() - t0 > kSpinLimitCycles)) {
+      if (__any_sync(0xFFFFFFFFu, clock64() - t0 > p.spin_limit)) {
         if ((threadIdx.x & 31) == 0) raise_abort(p);
         return false;
       }
@@ -204,11 +233,11 @@ __device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
 
 // Consumer-warp barrier: an mbarrier with one arrival per consumer warp per
 // round; waiting warps sleep in try_wait.  Round r (from 1) completes phase
-// r - 1.  False on timeout (bounded wait).
+// r - 1.  False on timeout or abort (bounded wait).
 __device__ bool consumer_barrier(const PParams& p, Smem& S, int round) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbarrier_arrive(&S.cbar);
-  const bool ok = mbar_wait_bounded(&S.cbar, static_cast<uint32_t>(round - 1) & 1u, p.err);
+  const bool ok = wait_warp(p, &S.cbar, static_cast<uint32_t>(round - 1) & 1u);
   if (!ok) raise_abort(p);
   __syncwarp();
   return ok;
@@ -396,7 +425,7 @@ __device__ void producer(const PParams& p, Smem& S) {
             }
           }
         }
-        if (!mbar_wait_bounded(&S.topk_bar, static_cast<uint32_t>(rel) & 1u, p.err)) {
+        if (!wait_one(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {
           raise_abort(p);
           break;
         }
@@ -404,7 +433,7 @@ __device__ void producer(const PParams& p, Smem& S) {
       }
       const uint32_t u = static_cast<uint32_t>(rel) * spl + e.u;
       const int slot = u % kNS;
-      if (!mbar_wait_bounded(&S.empty[slot], ((u / kNS) & 1) ^ 1, p.err)) {
+      if (!wait_one(p, &S.empty[slot], ((u / kNS) & 1) ^ 1)) {
         raise_abort(p);
         break;
       }
@@ -576,6 +605,8 @@ __device__ bool task_router(const PParams& p, Smem& S, int rel, int l, int e_row
       else acc += __float2ll_rn(bv * 1099511627776.0f);
     }
     p.logits[static_cast<size_t>(l) * p.E + e_row] = acc;
+    if (A->dbg_logits && rel < A->dbg_layers)
+      A->dbg_logits[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.E + e_row] = acc;
     red_add_release(p.logit_cnt + l, 1u);
     tl_max(p, l, EV_LOGIT);
   }
@@ -799,7 +830,7 @@ __device__ void consumer(const PParams& p, Smem& S, int cw) {
       const int slot = u % kNS;
       const uint32_t par = (u / kNS) & 1;
       if (e.kind == T_R) {
-        if (!mbar_wait_bounded(&S.full[slot], par, p.err)) {
+        if (!wait_warp(p, &S.full[slot], par)) {
           raise_abort(p);
           return;
         }
@@ -818,7 +849,7 @@ __device__ void consumer(const PParams& p, Smem& S, int cw) {
       const unsigned long long t0 = p.timeline ? gtimer() : 0ull;
       bool ok = true;
       if (e.kind == T_GUS || e.kind == T_GUR) {
-        if (!mbar_wait_bounded(&S.full[slot], par, p.err)) {
+        if (!wait_warp(p, &S.full[slot], par)) {
           raise_abort(p);
           return;
         }
@@ -841,13 +872,13 @@ __device__ void consumer(const PParams& p, Smem& S, int cw) {
         const int g0 = s * kSG, ng = min(kSG, nGs - g0);
         const unsigned target = min(kSG * 8, p.fs / 8 - s * kSG * 8);
         ok = dn_operands(p, S, cw, l, false, -1, g0, ng, s, target);
-        if (ok) ok = mbar_wait_bounded(&S.full[slot], par, p.err);
+        if (ok) ok = wait_warp(p, &S.full[slot], par);
         if (ok) dn_chunk(p, S, cw, rel, l, e.a, s, S.ring[slot] + s * kChunkBytes, ng);
       } else {  // T_DNR: row tile e.b + s of routed position j = e.a
         ok = dn_operands(p, S, cw, l, true, e.a, 0, nGf, p.n_sc + e.a, p.f / 8);
         if (lane == 0 && ok) tl_max(p, l, EV_DNR_READY);
         const unsigned long long t2 = p.timeline ? gtimer() : 0ull;
-        if (ok) ok = mbar_wait_bounded(&S.full[slot], par, p.err);
+        if (ok) ok = wait_warp(p, &S.full[slot], par);
         const unsigned long long t3 = p.timeline ? gtimer() : 0ull;
         if (lane == 0 && ok) cta_stamp(p, rel, 14);
         if (ok) dn_chunk(p, S, cw, rel, l, e.b + s, p.n_sc + e.a, S.ring[slot] + s * nGf * kGroupBytes, nGf);

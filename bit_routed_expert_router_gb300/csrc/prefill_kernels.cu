@@ -4,27 +4,37 @@
 // improved attention and prefill": batched prefill dequantises a small 16-bit
 // tile of the affine int4 weights, runs the hardware matrix primitive on it and
 // throws the tile away, so the stored weights never change.  Here that
-// primitive is tcgen05 (fifth-generation tensor cores, accumulators in tensor
-// memory), and the batch is grouped by expert first:
+// primitive is tcgen05 (fifth-generation tensor cores, operands and
+// accumulators in tensor memory), and the batch is grouped by expert first:
 //
-//   k_pf_prep     RMS norm (or copy) of every token: x in bf16 (router) and
-//                 fp16 (matrix operand).
-//   k_pf_router   exact fixed-point logits of every (token, expert), top-k and
-//                 softmax gates per token.
-//   k_pf_count /  stable counting sort of the T*k (token, position) pairs by
-//   k_pf_scatter  expert, and the list of 128-row work items per expert.
-//   k_pf_gather   the pairs' x rows, in that order, as one fp16 matrix.
-//   k_pf_gemm     grouped int4 x fp16 GEMM on tcgen05.  A CTA owns 128 weight
-//                 rows and 128 token rows of one expert: a producer thread
-//                 streams the int4 blocks (bulk copies) and the token rows
-//                 (TMA tensor loads, 128-byte swizzle), four warps dequantise
-//                 each 64-wide k step into an fp16 tile in the same swizzled
-//                 layout, one thread issues the MMAs into a 128 x 128 fp32
-//                 accumulator in tensor memory, and the four warps then read
-//                 it back for the epilogue: GELU(gate) * up (gate/up pass),
-//                 the expert output per pair (routed down pass), or the
-//                 shared-expert output plus the gate-weighted routed outputs
-//                 in top-k order plus the residual (shared down pass).
+//   k_pf_prep          RMS norm (or copy) of every token: x in bf16 (router)
+//                      and fp16 (matrix operand), |x|^2 and max|x_i| per token.
+//   k_pf_row_stats     |w|^2 and max|w_i| of the router rows (once per layer).
+//   k_pf_logits_approx every (token, expert) logit in fp32 with a rigorous
+//                      error bound.
+//   k_pf_route         per token: the experts the bound cannot rule out, their
+//                      exact fixed-point logits (the same 2^-40 grid as the
+//                      decode kernels), top-k (ties to the lower index) and
+//                      softmax gates.
+//   k_pf_count /       stable counting sort of the T*k (token, position) pairs
+//   k_pf_scatter       by expert, and the list of work items per expert.
+//   k_pf_gather        the pairs' x rows, in that order, as one fp16 matrix.
+//   k_pf_gemm          grouped int4 x fp16 GEMM on tcgen05.  A CTA owns 128
+//                      weight rows and 128 (or 32) token rows of one expert.
+//                      Warp 0's lane 0 streams the int4 blocks (bulk copies)
+//                      and the token rows (TMA tensor loads, 128-byte swizzle,
+//                      into shared memory).  Eight dequantising warps turn
+//                      each 64-wide k step of the int4 blocks into fp16 and
+//                      store it straight into tensor memory (the A operand).
+//                      Warp 1 allocates tensor memory and one of its threads
+//                      issues the MMAs (A from tensor memory, B from shared
+//                      memory) into a fp32 accumulator in tensor memory; the
+//                      eight warps then read it back for the epilogue:
+//                      GELU(gate) * up (gate/up pass), the expert output per
+//                      pair (routed down pass), or the shared expert's output
+//                      per token (shared down pass).
+//   k_pf_combine       per token: the shared output plus the gate-weighted
+//                      routed outputs in top-k order, and the residual.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -561,7 +571,7 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
                                                   const float* xn2, const float* wn2, const float* xmax,
                                                   const float* wmax, const float* bias, int T, int d,
                                                   int E, int k, int32_t* ids, float* gates, int32_t* dbg_ids,
-                                                  float* dbg_gates, uint32_t* err) {
+                                                  float* dbg_gates, int64_t* dbg_logits, uint32_t* err) {
   __shared__ int cand_all[8][128];
   __shared__ long long exact_all[8][128];
   __shared__ int n_cand_all[8];
@@ -681,6 +691,13 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
   }
   if (__syncthreads_or(bad || s_bad) && tid == 0) atomicOr(err, ERR_ROUTER_DOMAIN);
   if (!live) return;
+  if (dbg_logits) {
+    // exact logits of the candidates; the experts the bound ruled out read LLONG_MIN
+    int64_t* dl = dbg_logits + static_cast<size_t>(t) * E;
+    for (int e = lane; e < E; e += 32) dl[e] = LLONG_MIN;
+    __syncwarp();
+    for (int ci = lane; ci < n_cand; ci += 32) dl[cand[ci]] = exact[ci];
+  }
   // top-k over the candidates: a lane holds candidates lane, lane + 32, ...
   unsigned long long key[4];
   int idx[4];
@@ -889,7 +906,7 @@ cudaError_t launch_pf_row_stats(const uint16_t* rows, int n, int d, float* n2, f
 
 cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
                              int k, float* approx, float* xn2, float* wn2, float* xmax, float* wmax, int32_t* ids,
-                             float* gates, int32_t* dbg_ids, float* dbg_gates, uint32_t* err, int n_sm,
+                             float* gates, int32_t* dbg_ids, float* dbg_gates, int64_t* dbg_logits, uint32_t* err, int n_sm,
                              cudaStream_t s) {
   const int tiles = ((T + kRT - 1) / kRT) * ((E + kRE - 1) / kRE);
   // slice d (in 64-wide chunks, a divisor of d/64) until the grid covers the GPU twice
@@ -907,7 +924,7 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
   k_pf_logits_approx<<<dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), 256, 0, s>>>(
       x_bf, router_w, T, d, E, d / slices, approx);
   k_pf_route<<<(T + 7) / 8, 256, 0, s>>>(x_bf, router_w, approx, xn2, wn2, xmax, wmax, bias, T, d, E, k, ids, gates, dbg_ids,
-                               dbg_gates, err);
+                               dbg_gates, dbg_logits, err);
   return cudaGetLastError();
 }
 

@@ -2,14 +2,15 @@
  * libmoe — routed mixture-of-experts FFN of a decode step, on one GB300 (sm_103a).
  *
  * Per layer and token the library computes what the TurboFieldfare write-up
- * ("Optimizing a 14.3 GB model for an 8 GB machine") and its video
- * walkthrough describe for Gemma 4 26B-A4B:
+ * ("Optimizing a 14.3 GB model for an 8 GB machine") and the video
+ * walkthrough of the same project (the yousumm.com transcript) describe for
+ * Gemma 4 26B-A4B:
  *
- *   - a router over E experts whose top k run ("the router picks the top
- *     eight [of 128] and only those eight run", video transcript), with
- *     softmax gates over the k picked logits;
- *   - for each picked expert and for the always-on shared expert ("one shared
- *     expert that always runs", same transcript): an int4-affine gate and up
+ *   - a router over E experts (128 in that model) of which only the k best
+ *     (8 there) are evaluated, as the video's account of one token step
+ *     explains, with softmax gates over the k picked logits;
+ *   - for each picked expert and for the shared expert, which the video
+ *     describes as evaluated for every token whatever the router picks: an int4-affine gate and up
  *     projection (groups of 64 inputs with a 16-bit scale and bias each,
  *     section "Vectorization helped when it respected the storage layout"),
  *     the GELU-gated product GELU(gate) * up, and the down projection;
@@ -138,7 +139,12 @@ typedef struct {
 
 /* Create a context on CUDA device `device`.  Allocates the per-call scratch
  * sized for cfg->max_tokens.  MOE_EINVAL on a bad config, MOE_ENOMEM if the
- * scratch does not fit. */
+ * scratch does not fit.  The config carries the model geometry the video
+ * walkthrough gives for Gemma 4 26B-A4B (30 layers, 128 experts per layer, 8
+ * picked, one shared expert) and the quantisation of the write-up's section
+ * "Vectorization helped when it respected the storage layout" (int4 weights,
+ * one 16-bit scale and bias per group of 64); every field can be set
+ * independently within the limits checked here. */
 moe_status moe_create(const moe_config *cfg, int device, moe_ctx **out);
 
 /* Copy one layer's weights into the context (synchronous; the caller may free
@@ -153,7 +159,11 @@ moe_status moe_create(const moe_config *cfg, int device, moe_ctx **out);
  *              moe_set_expert_file, which must come first) and serves them
  *              the same way.  All layers of a context use the same residency.
  * The library repacks the weights into its own device layout: a permutation
- * of the same bytes (nibbles and (scale, bias) pairs), never a re-encoding. */
+ * of the same bytes (nibbles and (scale, bias) pairs), never a re-encoding.
+ * This follows the write-up's section "Explicit reads made expert streaming
+ * work" and the video walkthrough's account of the file format: the weights
+ * are stored in exactly the order the kernels read them, so that staging an
+ * expert (slot copy, file read) is one contiguous copy with no conversion. */
 moe_status moe_init_layer(moe_ctx *ctx, int layer, const uint16_t *router_w,
                           const moe_expert_weights *experts, const moe_expert_weights *shared,
                           int residency);
@@ -161,11 +171,24 @@ moe_status moe_init_layer(moe_ctx *ctx, int layer, const uint16_t *router_w,
 /* Host-pool and expert-file contexts: give every layer n_slots device slots (top_k <= n_slots
  * <= n_experts) and empty the LRU tables.  The byte budget
  * n_layers * n_slots * expert_bytes is checked against free device memory
- * before anything is allocated (MOE_ENOMEM, context unchanged). */
+ * before anything is allocated (MOE_ENOMEM, context unchanged).
+ * goinfer, "When the model doesn't fit": the slot count is the lever of a
+ * paged MoE (its table sweeps 8 to 128 slots per layer), and the budget guard
+ * must be keyed on bytes the program computes itself, because a guard on the
+ * operating system's resident-set figure inverted at the failure point; the
+ * write-up's section "MoE needed parallel work, reuse, and coarse overlap"
+ * gives the per-layer bounded cache (16 of 128 experts there). */
 moe_status moe_set_slots(moe_ctx *ctx, int n_slots);
 
 /* Run layers [layer_begin, layer_end) for B tokens, each layer
  *   x = prenorm ? bf16(RMSNorm(h)) : h;  y = MoE-FFN(x);  h <- bf16(h + y).
+ * The per-layer step is the one the video walkthrough narrates for a token
+ * passing the 30 layers in order (the router names 8 of 128 experts, which
+ * run together with the shared expert) and the write-up's section "MoE needed
+ * parallel work, reuse, and coarse overlap" restructures (routed experts from
+ * the cache first, misses after; the shared expert overlapped with the
+ * reads).  The RMS pre-norm between layers stands in for the attention block
+ * the pages place there, which is outside this library.
  *   h_in:  device bf16 [B][d] residual entering layer_begin (not modified)
  *   h_out: device bf16 [B][d] residual after layer_end - 1 (may equal h_in)
  *   logit_bias: device fp32 [layer_end - layer_begin][B][n_experts] added to the
@@ -234,6 +257,14 @@ moe_status moe_prefill(moe_ctx *ctx, const void *h, int T, int layer_begin, int 
  *   gates     fp32 [max_layers][B][k]
  *   y_layers  fp32 [max_layers][B][d]   FFN output of each layer
  * Pass all NULL to stop capturing. */
+/* Capture the router logits of the next calls (bias included, units of 2^-40,
+ * layout int64 [max_layers][B][n_experts], max_layers from moe_set_debug;
+ * NULL stops).  The decode kernels write every expert's exact logit.  The
+ * prefill router evaluates exactly only the experts its error bound cannot
+ * rule out; the others read INT64_MIN.  Takes effect only while moe_set_debug
+ * has a non-zero max_layers. */
+moe_status moe_set_debug_logits(moe_ctx *ctx, int64_t *logits);
+
 moe_status moe_set_debug(moe_ctx *ctx, uint16_t *x_layers, int32_t *ids, float *gates,
                          float *y_layers, int max_layers);
 
@@ -348,12 +379,17 @@ int64_t moe_shared_bytes(const moe_config *cfg);
  * every input and output; the arithmetic is that of the router phase of
  * moe_decode_step (optional RMS norm, exact fixed-point logits, top-k with
  * lower-index ties, softmax gates over the k picked).
- *   cfg:        d, n_experts (<= 256), top_k, group, prenorm and norm_eps are used
- *   router_w:   device fp16 [n_experts][d]
- *   h:          device bf16 [B][d]
+ *   cfg:        d, n_experts, top_k, group, prenorm and norm_eps are used:
+ *               group == 64, d a multiple of 64 and at most 3072,
+ *               1 <= n_experts <= 256, 1 <= top_k <= min(n_experts, 32),
+ *               prenorm 0 or 1; anything else returns MOE_EINVAL
+ *   router_w:   device fp16 [n_experts][d], 16-byte aligned
+ *   h:          device bf16 [B][d], 16-byte aligned
  *   logit_bias: device fp32 [B][n_experts], or NULL
  *   ids:        device int32 [B][top_k] (output); gates: device fp32 [B][top_k] (output)
  *   B:          1 <= B <= MOE_ROUTE_NOALLOC_MAX_B; a larger B returns MOE_EINVAL
+ * A misaligned router_w or h (or ids, gates, logit_bias not 4-byte aligned)
+ * returns MOE_EINVAL.
  * Runs on the current CUDA device, on `stream`.  Its only scratch is a fixed
  * 131,328-byte device array that every GPU loading this library holds until
  * the process exits.  The first call on each device looks up that array's
@@ -361,7 +397,8 @@ int64_t moe_shared_bytes(const moe_config *cfg);
  * before any stream capture.  All calls share the array and it keeps the last
  * call's contents: calls that overlap on the GPU (unordered streams) race.
  * Router products outside the exact domain (|W_r[e,i] * x[i]| >= 2^11) are
- * dropped rather than reported.  Returns MOE_EINVAL or MOE_ECUDA on failure
+ * dropped rather than reported, and so is a logit_bias entry with
+ * |b| >= 2^20 or a NaN (the logit then takes no bias).  Returns MOE_EINVAL or MOE_ECUDA on failure
  * (there is no context to poison). */
 #define MOE_ROUTE_NOALLOC_MAX_B 64
 
@@ -412,7 +449,15 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
  * shape allows it) or off (batched decode kernels).
  * hook 8: `value` is a caller device buffer of 4 * 16 uint64 receiving event
  * times of CTA (0, 0) of each prefill GEMM of the first layer of a call, or
- * 0 to stop.  Other hooks: MOE_EINVAL. */
+ * 0 to stop.  hook 10: every bounded device wait of the two persistent
+ * decode kernels gives up after `value` SM cycles (<= 0 restores the default,
+ * 4e9 cycles, about two seconds); a wait that runs out sets the abort flag,
+ * every CTA drains its own copies in flight and leaves, the last one out
+ * resets the launch words, and moe_sync returns MOE_ETIMEOUT and poisons the
+ * context.  hook 11 (value ignored, allowed on a poisoned context): waits for
+ * the device, then MOE_OK if the persistent kernels' exit counters, abort
+ * flags, dependency counters and fixed-point output sums are all zero, else
+ * MOE_ESTATE.  Other hooks: MOE_EINVAL. */
 moe_status moe_test_hook(moe_ctx *ctx, int hook, int64_t value);
 
 const char *moe_status_string(moe_status s);

@@ -13,18 +13,17 @@
  *  - INT4 affine groups of 64 with a 16-bit (scale, bias) per group
  *    (TurboFieldfare, "Vectorization helped when it respected the storage
  *    layout"): weight = scale * q + bias, q in 0..15.
- *  - Router: logits over all experts, pick the top k ("the router picks the
- *    top eight experts and only those eight run", TurboFieldfare video
- *    transcript), gates = softmax over the k picked logits.
- *  - Each picked expert and the always-on shared expert ("one shared expert
- *    that always runs", same transcript) compute down( GELU(gate x) * (up x) ).
+ *  - Router: logits over all experts, pick the top k (the TurboFieldfare
+ *    video walkthrough: 8 of 128 experts are named per token and only those
+ *    are evaluated), gates = softmax over the k picked logits.
+ *  - Each picked expert and the shared expert (evaluated for every token,
+ *    same video) compute down( GELU(gate x) * (up x) ).
  *  - Combine: y = y_shared + sum_j gate_j * y_{e_j}.
  *  - Per-layer LRU slot cache (TurboFieldfare, "MoE needed parallel work,
  *    reuse, and coarse overlap": a bounded cache of 16 routed experts per
  *    layer, LRU; goinfer "When the model doesn't fit": plain LRU).
  *
- * Readings where the pages leave a step open (each is listed in the design
- * notes):
+ * Readings where the pages leave a step open:
  *  - router logits are exact fixed point on a 2^-40 grid: every fp16 x bf16
  *    product is rounded half-to-even to a multiple of 2^-40 and summed in
  *    int64, so the sum does not depend on summation order and ties are

@@ -95,3 +95,96 @@ def assert_ffn_close(y_gpu, y_ref, what=""):
     bound = FFN_RTOL * np.abs(y_ref).max()
     assert err <= bound, f"{what}: max err {err:.3e} > {bound:.3e}"
     return err / max(np.abs(y_ref).max(), 1e-30)
+
+
+INT64_MIN = np.iinfo(np.int64).min
+
+
+def check_logits(got, ref, ids, what="", candidates_only=False):
+    """Router logits (int64, 2^-40 units, bias included) bit for bit.  With
+    candidates_only (the prefill router), experts its error bound ruled out read
+    INT64_MIN; every other entry and every picked expert must be exact."""
+    got = np.asarray(got, dtype=np.int64)
+    ref = np.asarray(ref, dtype=np.int64)
+    live = got != INT64_MIN if candidates_only else np.ones(got.shape, bool)
+    assert live[np.asarray(ids)].all(), f"{what}: a picked expert has no exact logit"
+    bad = np.nonzero(live & (got != ref))[0]
+    assert bad.size == 0, f"{what}: logits differ at experts {bad[:8].tolist()}: {got[bad[:4]]} vs {ref[bad[:4]]}"
+    if candidates_only:
+        # a ruled-out expert must be strictly below the k-th largest logit
+        kth = np.sort(ref)[::-1][len(ids) - 1]
+        assert np.all(ref[~live] < kth), f"{what}: the bound ruled out an expert tied with the top-k"
+
+
+def capture(ctx, L, B, logits=False):
+    """Device buffers for the debug capture of the next call(s) over L layers, B tokens."""
+    d, k, E = ctx.shape.d, ctx.shape.top_k, ctx.shape.n_experts
+    cap = {"x": torch.zeros(L, B, d, dtype=torch.bfloat16, device="cuda"),
+           "ids": torch.zeros(L, B, k, dtype=torch.int32, device="cuda"),
+           "gates": torch.zeros(L, B, k, dtype=torch.float32, device="cuda"),
+           "y": torch.zeros(L, B, d, dtype=torch.float32, device="cuda")}
+    moe.check(moe.moe_set_debug(ctx.h, cap["x"], cap["ids"], cap["gates"], cap["y"], L), ctx.h)
+    if logits:
+        cap["logits"] = torch.full((L, B, E), 7, dtype=torch.int64, device="cuda")
+        moe.check(moe.moe_set_debug_logits(ctx.h, cap["logits"]), ctx.h)
+    return cap
+
+
+def end_capture(ctx):
+    moe.check(moe.moe_set_debug_logits(ctx.h), ctx.h)
+    moe.check(moe.moe_set_debug(ctx.h), ctx.h)
+
+
+def check_stack(weights, H, cap, h_out, top_k, ffn_layers=(), ffn_tokens=None, bias=None, prenorm=1,
+                candidates_only=False, eps=1e-6):
+    """Teacher-forced oracle check of a captured stack of L layers for every
+    token of H [B, d]: x_l within one bf16 ulp of RMSNorm(h_l) (or equal to h_l
+    without the norm), ids bit-exact, gates within GATE_RTOL, logits bit-exact
+    (if captured), y_l against oracle.Layer on ffn_layers (tokens ffn_tokens,
+    default all), and h_{l+1} = bf16(h_l + y_l) within one ulp, chained on the
+    kernels' fp32 rule.  weights[l] holds at least router_w; full host weights
+    on the FFN layers.  bias: [L, B, E] or None."""
+    xs, ids, gs, ys = (cap[n].cpu() for n in ("x", "ids", "gates", "y"))
+    lgs = cap["logits"].cpu().numpy() if "logits" in cap else None
+    L, B = ids.shape[0], ids.shape[1]
+    bias_np = None if bias is None else bias.cpu().numpy()
+    ffn_tokens = range(B) if ffn_tokens is None else ffn_tokens
+    lays = {l: oracle.Layer(weights[l], top_k) for l in ffn_layers}
+    worst = 0.0
+    for b in range(B):
+        h = oracle.as_bits(H[b])
+        for l in range(L):
+            x_gpu = oracle.as_bits(xs[l, b])
+            if prenorm:
+                x_ref = oracle.rmsnorm_bf16(h, eps)
+                dx = np.abs(bf16_to_f64(x_gpu) - bf16_to_f64(x_ref))
+                assert np.all(dx <= np.abs(bf16_to_f64(x_ref)) * 2.0 ** -7 + 1e-30), f"token {b} layer {l}: x"
+            else:
+                assert np.array_equal(x_gpu, h), f"token {b} layer {l}: x must equal h without the norm"
+            bl = None if bias_np is None else bias_np[l, b]
+            lg, st = oracle.router_logits(oracle.as_bits(weights[l]["router_w"]), x_gpu, bl)
+            assert st == 0
+            rid = oracle.topk(lg, top_k)
+            assert list(ids[l, b].numpy()) == list(rid), f"token {b} layer {l}: ids {ids[l, b].tolist()} vs {list(rid)}"
+            assert np.allclose(gs[l, b].numpy(), oracle.gates(lg, rid), rtol=GATE_RTOL, atol=1e-7), \
+                f"token {b} layer {l}: gates"
+            if lgs is not None:
+                check_logits(lgs[l, b], lg, rid, f"token {b} layer {l}", candidates_only)
+            if l in lays and b in ffn_tokens:
+                _, _, _, ry, _ = lays[l].forward(x_gpu, bl)
+                worst = max(worst, assert_ffn_close(ys[l, b].numpy(), ry, f"token {b} layer {l}"))
+            y32 = ys[l, b].numpy().astype(np.float32)
+            h_ref = oracle.residual_bf16(h, y32.astype(np.float64))
+            # the kernels form h + y in fp32 and round that to bf16; the fp64 sum
+            # can round the other way on a tie of the fp32 result (one ulp), and a
+            # one-ulp step would carry through the rest of the stack, so the chain
+            # follows the fp32 rule after checking both agree within an ulp
+            s32 = (bf16_to_f64(h).astype(np.float32) + y32).astype(np.float64)
+            h = oracle.residual_bf16(np.zeros_like(h), s32)
+            dh = np.abs(bf16_to_f64(h) - bf16_to_f64(h_ref))
+            assert np.all(dh <= np.abs(bf16_to_f64(h_ref)) * 2.0 ** -7 + 1e-30), f"token {b} layer {l}: h + y"
+        if h_out is not None:
+            got = bf16_to_f64(oracle.as_bits(h_out[b]))
+            ref = bf16_to_f64(h)
+            assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30), f"token {b}: h_out"
+    return worst

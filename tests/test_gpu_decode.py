@@ -1,5 +1,7 @@
-"""GPU parity of the decode path (router, top-k, gates, int4 gate/up/GELU,
-down, combine) against the CPU oracle, through the C ABI."""
+"""GPU parity of the decode path (router logits, top-k, gates, int4
+gate/up/GELU, down, combine) against the CPU oracle, through the C ABI."""
+
+import os
 
 import numpy as np
 import pytest
@@ -9,7 +11,8 @@ import bit_routed_expert_router_gb300 as moe
 import oracle
 from workload import FULL, TINY, Shape, gen_hidden, gen_layer
 
-from moe_harness import DECODE_KERNELS, GATE_RTOL, Ctx, assert_ffn_close, bf16_to_f64, to_device, use_decode_kernel
+from moe_harness import (DECODE_KERNELS, GATE_RTOL, Ctx, assert_ffn_close, bf16_to_f64, capture, check_logits,
+                         check_stack, end_capture, to_device, to_host, use_decode_kernel)
 
 pytestmark = pytest.mark.gpu
 
@@ -23,10 +26,13 @@ def _check_layer_outputs(ctx, lay, H, bias=None):
     ids = torch.zeros(1, B, k, dtype=torch.int32, device=dev)
     gs = torch.zeros(1, B, k, dtype=torch.float32, device=dev)
     ys = torch.zeros(1, B, d, dtype=torch.float32, device=dev)
+    lgs = torch.full((1, B, ctx.shape.n_experts), 7, dtype=torch.int64, device=dev)
     moe.check(moe.moe_set_debug(ctx.h, xs, ids, gs, ys, 1), ctx.h)
+    moe.check(moe.moe_set_debug_logits(ctx.h, lgs), ctx.h)
     h_out, y, _ = ctx.decode(H, 0, 1, bias=bias)
     ctx.sync()
-    moe.check(moe.moe_set_debug(ctx.h), ctx.h)
+    end_capture(ctx)
+    lgs = lgs[0].cpu().numpy()
     assert torch.equal(y, ys[0])
     worst = 0.0
     for b in range(B):
@@ -36,6 +42,8 @@ def _check_layer_outputs(ctx, lay, H, bias=None):
         assert st == 0
         assert list(ids[0, b].cpu().numpy()) == list(rid), f"token {b}: ids {ids[0, b].tolist()} vs {list(rid)}"
         assert np.allclose(gs[0, b].cpu().numpy(), rg, rtol=GATE_RTOL, atol=1e-7)
+        # the tensor-core path (16 tokens and up) evaluates only the candidates exactly
+        check_logits(lgs[b], rlg, rid, f"token {b}", candidates_only=B >= 16)
         worst = max(worst, assert_ffn_close(y[b].cpu().numpy(), ry, f"token {b}"))
         # residual: h_out = bf16(h + y) from the GPU's own y
         ref_h = oracle.residual_bf16(oracle.as_bits(H[b]), y[b].cpu().double().numpy())
@@ -219,3 +227,68 @@ def test_full_shape_layer_sampled_tokens():
         moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PERSISTENT, 1), ctx.h)
         # and a ragged batch
         _check_layer_outputs(ctx, lay, H[100:105])
+
+
+def test_c1_thousand_tokens_through_the_clustered_kernel():
+    """The one-token decode workload at full shape, 1024 tokens one at a time
+    through the kernel the decode benchmark times: every token's int64 logits
+    and ids bit-exact, every eighth token's FFN output (128 tokens)."""
+    sh, T = FULL, 1024
+    wd = gen_layer(sh, seed=11, layer=0, device="cuda")
+    oracle.set_threads(os.cpu_count())
+    with Ctx(sh, n_layers=1) as ctx:
+        ctx.init_layer(0, wd)
+        use_decode_kernel(ctx, "cluster")
+        w = to_host(wd)
+        del wd
+        H = gen_hidden(T, sh.d, seed=11, device="cuda")
+        k, E = sh.top_k, sh.n_experts
+        ids = torch.zeros(T, k, dtype=torch.int32, device="cuda")
+        lgs = torch.full((T, E), 7, dtype=torch.int64, device="cuda")
+        y = torch.zeros(T, sh.d, dtype=torch.float32, device="cuda")
+        h_out = torch.empty_like(H)
+        for t in range(T):
+            # each call captures into its own rows (one layer, one token)
+            moe.check(moe.moe_set_debug(ctx.h, None, ids[t:t + 1], None, None, 1), ctx.h)
+            moe.check(moe.moe_set_debug_logits(ctx.h, lgs[t:t + 1]), ctx.h)
+            st, _ = moe.moe_decode_step(ctx.h, H[t:t + 1], 1, 0, 1, None, h_out[t:t + 1], y[t:t + 1], None, None)
+            moe.check(st, ctx.h)
+        ctx.sync()
+        end_capture(ctx)
+        ids, lgs, y = ids.cpu().numpy(), lgs.cpu().numpy(), y.cpu().numpy()
+        rw = oracle.as_bits(w["router_w"])
+        Hb = oracle.as_bits(H.cpu())
+        for t in range(T):
+            lg, st = oracle.router_logits(rw, Hb[t])
+            assert st == 0
+            rid = oracle.topk(lg, k)
+            assert list(ids[t]) == list(rid), f"token {t}: ids {ids[t].tolist()} vs {list(rid)}"
+            check_logits(lgs[t], lg, rid, f"token {t}")
+        lay = oracle.Layer(w, k)
+        worst = 0.0
+        for t in range(0, T, 8):
+            _, _, _, ry, st = lay.forward(Hb[t])
+            assert st == 0
+            worst = max(worst, assert_ffn_close(y[t], ry, f"token {t}"))
+
+
+def test_full_shape_batch32_tensor_core_path():
+    """32 tokens at full shape take the tensor-core grouped GEMM path (32-row
+    token tiles over 44 k-groups): every token's ids, gates, candidate logits
+    and FFN output on two layers against the oracle."""
+    sh, L, B = FULL, 2, 32
+    oracle.set_threads(os.cpu_count())
+    with Ctx(sh, n_layers=L, prenorm=1) as ctx:
+        hosts = []
+        for l in range(L):
+            wd = gen_layer(sh, seed=12, layer=l, device="cuda")
+            ctx.init_layer(l, wd)
+            hosts.append(to_host(wd))
+            del wd
+        H = gen_hidden(B, sh.d, seed=12, device="cuda")
+        cap = capture(ctx, L, B, logits=True)
+        h_out, y_last, _ = ctx.decode(H, 0, L)
+        ctx.sync()
+        end_capture(ctx)
+        assert torch.equal(y_last, cap["y"][L - 1])
+        check_stack(hosts, H, cap, h_out, sh.top_k, ffn_layers={0, 1}, candidates_only=True)

@@ -18,7 +18,7 @@ import bit_routed_expert_router_gb300 as moe
 import oracle
 from workload import FULL, Shape, bias_from_targets, gen_hidden, gen_layer, zipf_reuse_targets
 
-from moe_harness import Ctx, assert_ffn_close, to_device, to_host
+from moe_harness import Ctx, assert_ffn_close, capture, check_stack, end_capture, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -345,6 +345,38 @@ def test_file_pool_matches_host_pool(tmp_path):
     assert st_f.host_pool_bytes == 0 and st_h.host_pool_bytes > 0
     rec = (st_h.expert_bytes + 4095) // 4096 * 4096
     assert os.path.getsize(path) == (L * sh.n_experts - 1) * rec + st_h.expert_bytes
+
+
+@pytest.mark.parametrize("tier", ["host", "file", "file+host"])
+def test_pool_outputs_match_oracle(tier, tmp_path):
+    # a slot cache smaller than the working set, misses staged from the pinned
+    # pool or read from the expert file (with or without the pinned host tier):
+    # every layer's logits, ids, gates, FFN output and residual against the oracle
+    sh = Shape(d=256, f=128, f_shared=128, n_experts=16, top_k=2)
+    L, N, NH, T = 3, 3, 6, 10
+    wh = [gen_layer(sh, seed=154, layer=l) for l in range(L)]
+    ctx = Ctx(sh, n_layers=L, prenorm=1)
+    with ctx:
+        if tier != "host":
+            moe.check(moe.moe_set_expert_file(ctx.h, str(tmp_path / "experts.bin"), 4, 65536), ctx.h)
+        for l in range(L):
+            ctx.init_layer(l, to_device(wh[l]), residency=moe.MOE_HOST_POOL if tier == "host" else moe.MOE_FILE_POOL)
+        if tier == "file+host":
+            moe.check(moe.moe_set_file_cache(ctx.h, NH), ctx.h)
+        moe.check(moe.moe_set_slots(ctx.h, N), ctx.h)
+        H = gen_hidden(T, sh.d, seed=154).cuda()
+        for t in range(T):
+            cap = capture(ctx, L, 1, logits=True)
+            h_out, _, _ = ctx.decode(H[t:t + 1], 0, L)
+            ctx.sync()
+            end_capture(ctx)
+            check_stack(wh, H[t:t + 1], cap, h_out, sh.top_k, ffn_layers=range(L))
+        _, st = moe.moe_get_stats(ctx.h)
+        assert st.misses > 0 and st.hits > 0
+        if tier == "file":
+            assert st.file_read_bytes == st.misses * st.expert_bytes
+        if tier == "file+host":
+            assert st.host_tier_hits > 0
 
 
 def test_file_pool_state_and_io_errors(tmp_path):

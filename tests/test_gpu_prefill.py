@@ -10,7 +10,7 @@ import bit_routed_expert_router_gb300 as moe
 import oracle
 from workload import FULL, TINY, Shape, bias_from_targets, gen_hidden, gen_layer, mixture_targets
 
-from moe_harness import GATE_RTOL, Ctx, assert_ffn_close, bf16_to_f64, to_device, to_host
+from moe_harness import GATE_RTOL, Ctx, assert_ffn_close, bf16_to_f64, check_stack, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -272,6 +272,10 @@ def test_chunked_prefill_through_the_pool(residency, T, tmp_path):
         p = _run_prefill(pool, H, n_layers=L)
         for a, b, name in zip(r, p, ("h_out", "y_last", "x", "ids", "gates", "y")):
             assert torch.equal(a, b), name
+        # and directly against the oracle, every token's routing, sampled tokens' FFN
+        wh = [gen_layer(MEDIUM, seed=31, layer=l) for l in range(L)]
+        check_stack(wh, H, {"x": p[2], "ids": p[3], "gates": p[4], "y": p[5]}, p[0], MEDIUM.top_k,
+                    ffn_layers=range(L), ffn_tokens=range(T) if T < 10 else (0, 1, 150, T - 1))
         _, st = moe.moe_get_stats(pool.h)
         unions = [len(np.unique(r[3][l].cpu().numpy())) for l in range(L)]
         if T == 3:

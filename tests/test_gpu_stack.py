@@ -1,69 +1,29 @@
 """Layer stacks: teacher-forced per-layer parity of the residual stream
-(x_l = bf16(RMSNorm(h_l)), y_l, h_{l+1} = bf16(h_l + y_l)) through the
-persistent one-token kernel and the per-layer kernels."""
+(x_l = bf16(RMSNorm(h_l)), logits, ids, gates, y_l, h_{l+1} = bf16(h_l + y_l))
+through the persistent one-token kernels, the per-layer kernels and, for 32
+tokens, the tensor-core grouped GEMM path."""
 
-import numpy as np
 import pytest
 import torch
 
 import bit_routed_expert_router_gb300 as moe
-import oracle
 from workload import FULL, TINY, Shape, gen_hidden, gen_layer
 
-from moe_harness import DECODE_KERNELS, GATE_RTOL, Ctx, assert_ffn_close, bf16_to_f64, to_host, use_decode_kernel
+from moe_harness import (DECODE_KERNELS, Ctx, assert_ffn_close, capture, check_stack, end_capture, to_host,
+                         use_decode_kernel)
 
 pytestmark = pytest.mark.gpu
 
 
-def _capture(ctx, H, L, bias=None):
-    B, d, k = H.shape[0], ctx.shape.d, ctx.shape.top_k
-    xs = torch.zeros(L, B, d, dtype=torch.bfloat16, device="cuda")
-    ids = torch.zeros(L, B, k, dtype=torch.int32, device="cuda")
-    gs = torch.zeros(L, B, k, dtype=torch.float32, device="cuda")
-    ys = torch.zeros(L, B, d, dtype=torch.float32, device="cuda")
-    moe.check(moe.moe_set_debug(ctx.h, xs, ids, gs, ys, L), ctx.h)
+def _check_stack(ctx, weights_host, H, L, ffn_layers, bias=None, ffn_tokens=None):
+    B = H.shape[0]
+    cap = capture(ctx, L, B, logits=True)
     h_out, y_last, _ = ctx.decode(H, 0, L, bias=bias)
     ctx.sync()
-    moe.check(moe.moe_set_debug(ctx.h), ctx.h)
-    return xs, ids, gs, ys, h_out, y_last
-
-
-def _check_stack(ctx, weights_host, H, L, ffn_layers, bias=None):
-    xs, ids, gs, ys, h_out, y_last = _capture(ctx, H, L, bias)
-    assert torch.equal(y_last, ys[L - 1])
-    B = H.shape[0]
-    for b in range(B):
-        h = oracle.as_bits(H[b])
-        for l in range(L):
-            x_gpu = oracle.as_bits(xs[l, b])
-            x_ref = oracle.rmsnorm_bf16(h, 1e-6)
-            dx = np.abs(bf16_to_f64(x_gpu) - bf16_to_f64(x_ref))
-            assert np.all(dx <= np.abs(bf16_to_f64(x_ref)) * 2.0 ** -7 + 1e-30), f"layer {l}: x off by > 1 ulp"
-            w = weights_host[l]
-            rw = oracle.as_bits(w["router_w"])
-            bl = None if bias is None else bias[l, b].cpu().numpy()
-            lg, st = oracle.router_logits(rw, x_gpu, bl)
-            assert st == 0
-            rid = oracle.topk(lg, ctx.shape.top_k)
-            assert list(ids[l, b].cpu().numpy()) == list(rid), f"token {b} layer {l}: ids"
-            assert np.allclose(gs[l, b].cpu().numpy(), oracle.gates(lg, rid), rtol=GATE_RTOL, atol=1e-7)
-            if l in ffn_layers:
-                lay = oracle.Layer(w, ctx.shape.top_k)
-                _, _, _, ry, _ = lay.forward(x_gpu, bl)
-                assert_ffn_close(ys[l, b].cpu().numpy(), ry, f"token {b} layer {l}")
-            y32 = ys[l, b].cpu().numpy().astype(np.float32)
-            h_ref = oracle.residual_bf16(h, y32.astype(np.float64))
-            # the kernels form h + y in fp32 and round that to bf16; the fp64 sum
-            # can round the other way on a tie of the fp32 result (one ulp), and a
-            # one-ulp step would carry through the rest of the stack, so the
-            # chain follows the fp32 rule after checking both agree within an ulp
-            s32 = (bf16_to_f64(h).astype(np.float32) + y32).astype(np.float64)
-            h = oracle.residual_bf16(np.zeros_like(h), s32)
-            dh = np.abs(bf16_to_f64(h) - bf16_to_f64(h_ref))
-            assert np.all(dh <= np.abs(bf16_to_f64(h_ref)) * 2.0 ** -7 + 1e-30), f"layer {l}: h + y"
-        got = bf16_to_f64(oracle.as_bits(h_out[b]))
-        ref = bf16_to_f64(h)
-        assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30)
+    end_capture(ctx)
+    assert torch.equal(y_last, cap["y"][L - 1])
+    check_stack(weights_host, H, cap, h_out, ctx.shape.top_k, ffn_layers, ffn_tokens, bias,
+                candidates_only=B >= 16)
 
 
 @pytest.mark.parametrize("kernel", DECODE_KERNELS)
@@ -126,3 +86,35 @@ def test_persistent_and_layer_kernels_agree():
             for t in range(6):
                 assert_ffn_close(outs[kernel][t].cpu().numpy(), outs["layers"][t].cpu().double().numpy(),
                                  f"{kernel} token {t}")
+
+
+def _full_stack(seed, keep):
+    """A 30-layer full-shape context (RMS pre-norm between layers) and the host
+    weights: every router, and the full weights of the layers in keep."""
+    L, sh = 30, FULL
+    ctx = Ctx(sh, n_layers=L, prenorm=1)
+    hosts = []
+    for l in range(L):
+        w = gen_layer(sh, seed=seed, layer=l, device="cuda")
+        ctx.init_layer(l, w)
+        hosts.append(to_host(w) if l in keep else {"router_w": w["router_w"].cpu()})
+        del w
+    return ctx, hosts
+
+
+def test_full_stack_thirty_layers_batch32():
+    """The batched workload (32 tokens, 30 layers, Zipf-reuse routing bias) through
+    the tensor-core path: every token's logits, ids and gates on every layer,
+    FFN outputs on sampled layers and tokens."""
+    import os
+
+    import oracle
+    from workload import bias_from_targets, zipf_reuse_targets
+    oracle.set_threads(os.cpu_count())
+    L, B, sh = 30, 32, FULL
+    ctx, hosts = _full_stack(seed=3, keep=(0, 14, 29))
+    with ctx:
+        H = gen_hidden(B, sh.d, seed=3, device="cuda")
+        tg = zipf_reuse_targets(B, L, sh.n_experts, sh.top_k, seed=3)
+        bias = torch.from_numpy(bias_from_targets(tg, sh.n_experts).transpose(1, 0, 2).copy()).cuda()  # [L, B, E]
+        _check_stack(ctx, hosts, H, L, ffn_layers={0, 14, 29}, bias=bias, ffn_tokens=(0, 9, 22, 31))
