@@ -413,7 +413,7 @@ def run_ours(args):
         step(i)
     moe.check(moe.moe_sync(ctx, stream), ctx)
     if args.timeline:
-        return print_timeline(moe, ctx, step, args.warmup)
+        return print_timeline(moe, ctx, step, args.warmup, raw_out=args.timeline_raw)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -534,7 +534,7 @@ TIMELINE_SUMS = ["gateup_compute", "down_compute", "down_wait_for_a", "routed_da
                  "down_stages", "shared_data_wait"]
 
 
-def print_timeline(moe, ctx, step, first, reps=3):
+def print_timeline(moe, ctx, step, first, reps=3, raw_out=None):
     """Stamp one layer (the call's third) in every CTA with %globaltimer and
     print the per-event distribution (us from the first CTA's y_seen), one
     JSON line per repetition.  Diagnostic only: the stamps cost time."""
@@ -548,6 +548,8 @@ def print_timeline(moe, ctx, step, first, reps=3):
         moe.check(moe.moe_sync(ctx), ctx)
         moe.check(moe.moe_test_hook(ctx, moe.HOOK_TIMELINE, 0), ctx)
         t = tl.cpu().numpy().astype(np.float64)
+        if raw_out:
+            np.save(f"{raw_out}.rep{rep}.npy", tl.cpu().numpy())
         rows = t[t[:, 0] > 1e12]
         ref = rows[:, 0].min()
         ev = {}
@@ -1088,6 +1090,8 @@ def main(argv=None):
     ap.add_argument("--file-layers", type=int, default=30, help="pool: layers of the file-tier run")
     ap.add_argument("--file-threads", type=int, default=8, help="pool: pread threads of the file-tier run")
     ap.add_argument("--file-direct", action="store_true", help="pool: time the file tier with O_DIRECT reads too")
+    ap.add_argument("--timeline-raw", default=None,
+                    help="with --timeline: also save each repetition's raw [152][32] event array to PREFIX.repN.npy")
     ap.add_argument("--timeline", action="store_true",
                     help="decode: print the clustered kernel's per-CTA event timeline of one layer instead of timing")
     args = ap.parse_args(argv)

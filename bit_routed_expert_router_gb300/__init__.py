@@ -26,6 +26,7 @@ HOOK_PREFILL_TC = 7
 HOOK_CLUSTER = 9
 HOOK_SPIN_LIMIT = 10      # bounded waits of the persistent decode kernels: cycles (<= 0: the default)
 HOOK_AT_REST = 11         # MOE_OK when the persistent kernels' launch words are back at rest
+HOOK_WAIT_DIAG = 12       # the clustered kernel's first wait that ran out (site << 16 | CTA) into a host uint32
 
 
 class MoeConfig(C.Structure):

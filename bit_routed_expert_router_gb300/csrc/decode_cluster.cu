@@ -95,7 +95,7 @@ struct Smem {
   alignas(16) uint32_t abuf[2 * kMaxU][64];        // per unit: a as B-fragment words, block (2 rank + tile) of 8
                                                    // words (4 * hi/lo column + t4) per sending tile
   alignas(16) float tsum[2 * kMaxU][8];            // per unit: sum of a (hi + lo) of each of the 8 gate/up tiles
-  alignas(16) float dn_part[kMaxU][kMaxRows];      // per unit: down partials of this CTA's rows
+  alignas(16) float dn_acc[kNQ][kMaxRows];         // per quad: its down stages' gate-weighted rows, in stage order
   alignas(16) long long yq[kMaxRows];              // fixed-point layer output rows, bulk-reduce source
   alignas(16) float gu_part[kNS][kQW][8][2];       // gate/up partials [slot][warp of the quad][row][gate/up]
   alignas(8) uint64_t full[kNS];
@@ -105,7 +105,6 @@ struct Smem {
   alignas(8) uint64_t rrow_empty;
   alignas(8) uint64_t topk_bar;                    // one phase per layer
   alignas(8) uint64_t cbar;                        // consumer-warp barrier
-  alignas(8) uint64_t clbar;                       // consumer warps of the whole cluster (remote arrivals)
   alignas(16) DevCallArgs args;
   CTask tasks[kMaxTasks];
   int n_tasks, n_units, n_stages;
@@ -113,16 +112,18 @@ struct Smem {
   int unit_G[kMaxU];
   int gu_cnt[kNS];
   float red[kNC];
-  float ssq[2][kCl][kNC];                          // by layer parity, per rank and warp: sums of squares
   long long rlog[kNC];
   int32_t ids[2][32];
   float gates[2][32];
   alignas(8) long long topv[32];                   // top-k logits in rank order
+  int last_out;                                    // this CTA is the last to leave the launch
+  unsigned topk_seq;                               // 64 * layer + ranks of the layer's top-k picked so far
 };
 
 static_assert(offsetof(Smem, ring) % 128 == 0 && kSlotBytes % 128 == 0, "TMA targets 128-byte aligned");
 static_assert(offsetof(Smem, rrow) % 16 == 0 && offsetof(Smem, yq) % 16 == 0, "bulk copy ends 16-byte aligned");
 static_assert(offsetof(Smem, abuf) % 16 == 0, "B fragments read as uint4");
+static_assert(sizeof(Smem) <= 227 * 1024, "shared memory per CTA (the kernel has no static shared memory)");
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -165,11 +166,20 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 
 __device__ __forceinline__ bool aborted(const CParams& p);
 
+// Wait sites, recorded with the CTA in p.diag by the first wait that runs out
+// (the others then see the abort flag and leave without recording).
+enum : unsigned { W_CBAR = 1, W_Y_POLL, W_RROW_EMPTY, W_P_TOPK, W_EMPTY, W_LOGITS, W_CLBAR, W_RROW_FULL, W_A_FULL,
+                  W_DN_TOPK, W_END_TOPK, W_FINISH, W_FULL };
+__device__ __forceinline__ void note_timeout(const CParams& p, unsigned site) {
+  atomicOr(p.err, ERR_WAIT_TIMEOUT);
+  if (p.diag) atomicCAS(p.diag, 0u, (site << 16) | (blockIdx.x & 0xFFFFu));
+}
+
 // Bounded wait for an mbarrier phase completed by arrivals from other CTAs of
 // the cluster (acquire at cluster scope), by a whole warp: the lanes decide
 // together (a vote per poll), so a warp never splits between going on and
 // giving up.  False after p.spin_limit cycles or once another CTA has aborted.
-__device__ bool mbar_wait_cluster(const CParams& p, uint64_t* bar, uint32_t parity) {
+__device__ bool mbar_wait_cluster(const CParams& p, uint64_t* bar, uint32_t parity, unsigned site) {
   const long long t0 = clock64();
   for (unsigned it = 0;; ++it) {
     uint32_t ok;
@@ -181,37 +191,40 @@ __device__ bool mbar_wait_cluster(const CParams& p, uint64_t* bar, uint32_t pari
         : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
         : "memory");
     if (__all_sync(kFull, ok != 0)) return true;
-    if (__any_sync(kFull, clock64() - t0 > p.spin_limit || ((it & 15) == 15 && aborted(p)))) {
-      if ((threadIdx.x & 31) == 0) atomicOr(p.err, ERR_WAIT_TIMEOUT);
+    if (__any_sync(kFull, clock64() - t0 > p.spin_limit)) {
+      if ((threadIdx.x & 31) == 0) note_timeout(p, site);
       return false;
     }
+    if ((it & 15) == 15 && __any_sync(kFull, aborted(p))) return false;
   }
 }
 
 // Bounded wait on a phase of a local mbarrier (this CTA's threads or copies)
 // by a whole warp, deciding together as above.
-__device__ bool wait_warp(const CParams& p, uint64_t* bar, uint32_t parity) {
+__device__ bool wait_warp(const CParams& p, uint64_t* bar, uint32_t parity, unsigned site) {
   if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
   const long long t0 = clock64();
   for (unsigned it = 1;; ++it) {
     if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
-    if (__any_sync(kFull, clock64() - t0 > p.spin_limit || ((it & 15) == 0 && aborted(p)))) {
-      if ((threadIdx.x & 31) == 0) atomicOr(p.err, ERR_WAIT_TIMEOUT);
+    if (__any_sync(kFull, clock64() - t0 > p.spin_limit)) {
+      if ((threadIdx.x & 31) == 0) note_timeout(p, site);
       return false;
     }
+    if ((it & 15) == 0 && __any_sync(kFull, aborted(p))) return false;
   }
 }
 
 // The same wait by a single thread (the producer).
-__device__ bool wait_one(const CParams& p, uint64_t* bar, uint32_t parity) {
+__device__ bool wait_one(const CParams& p, uint64_t* bar, uint32_t parity, unsigned site) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (unsigned it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > p.spin_limit || ((it & 15) == 0 && aborted(p))) {
-      atomicOr(p.err, ERR_WAIT_TIMEOUT);
+    if (clock64() - t0 > p.spin_limit) {
+      note_timeout(p, site);
       return false;
     }
+    if ((it & 15) == 0 && aborted(p)) return false;
   }
 }
 
@@ -249,10 +262,23 @@ __device__ __forceinline__ void raise_abort(const CParams& p) {
 __device__ bool consumer_barrier(const CParams& p, Smem& S, int round) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbarrier_arrive(&S.cbar);
-  const bool ok = wait_warp(p, &S.cbar, static_cast<uint32_t>(round - 1) & 1u);
+  const bool ok = wait_warp(p, &S.cbar, static_cast<uint32_t>(round - 1) & 1u, W_CBAR);
   if (!ok) raise_abort(p);
   __syncwarp();
   return ok;
+}
+
+// v * 2^-32 rounded to fp32 (the same value as a 64-bit integer conversion
+// scaled by 2^-32) with 32-bit conversions only: conversions from and to
+// 64-bit integers run on this part's narrow FP64 path, which measured slow
+// enough to matter in the layer's hot loops.  For |v| < 2^48 both halves are
+// exact in fp32 and the one rounding of their sum is the correct one.
+__device__ __forceinline__ float grid_to_float(long long v) {
+  const long long q = v >> 24;
+  if (q > -(1ll << 24) && q < (1ll << 24))
+    return fmaf(static_cast<float>(static_cast<int>(q)), 0.00390625f,                       // 2^-8
+                static_cast<float>(static_cast<unsigned>(v & 0xFFFFFF)) * 5.9604644775390625e-08f * 3.90625e-3f);
+  return __ll2float_rn(v) * 2.3283064365386963e-10f;                                         // 2^-32
 }
 
 // Layer outputs carry their completeness: every CTA adds (v << 8) + 1 into
@@ -261,7 +287,7 @@ __device__ bool consumer_barrier(const CParams& p, Smem& S, int round) {
 // adds into every row).  The warp polls the two rows each lane holds (bounded)
 // and returns their values.  False on abort or timeout.
 // Lanes with valid == false take part in the warp-wide votes only.
-__device__ bool poll_rows(const CParams& p, const long long* rows2, bool valid, float& y0, float& y1) {
+__device__ bool poll_rows(const CParams& p, const long long* rows2, bool valid, float& y0, float& y1, unsigned site) {
   const unsigned n_cl = gridDim.x / kCl;
   const unsigned long long* src = reinterpret_cast<const unsigned long long*>(rows2);
   const long long t0 = clock64();
@@ -270,15 +296,18 @@ __device__ bool poll_rows(const CParams& p, const long long* rows2, bool valid, 
     const ulonglong2 v = valid ? ld_volatile_u64x2(src) : make_ulonglong2(n_cl, n_cl);
     const bool ok = (v.x & 0xFFull) == n_cl && (v.y & 0xFFull) == n_cl;
     if (__all_sync(kFull, ok)) {
-      y0 = __ll2float_rn(static_cast<long long>(v.x) >> 8) * 2.3283064365386963e-10f;   // 2^-32
-      y1 = __ll2float_rn(static_cast<long long>(v.y) >> 8) * 2.3283064365386963e-10f;
+      y0 = grid_to_float(static_cast<long long>(v.x) >> 8);
+      y1 = grid_to_float(static_cast<long long>(v.y) >> 8);
       return true;
     }
     __nanosleep(64);
     if ((it & 255) == 255) {
       if (__any_sync(kFull, aborted(p))) return false;
       if (__any_sync(kFull, clock64() - t0 > p.spin_limit)) {
-        if ((threadIdx.x & 31) == 0) raise_abort(p);
+        if ((threadIdx.x & 31) == 0) {
+          note_timeout(p, site);
+          raise_abort(p);
+        }
         return false;
       }
     }
@@ -333,9 +362,10 @@ __device__ __forceinline__ void acc(const CParams& p, int rel, int slot, unsigne
 // The cluster's units of a layer (the same for every layer: only the experts
 // behind the top-k positions change).  Routed unit i (position j, group G,
 // i = j * f/64 + G) goes to cluster i mod n_cl; shared units go round-robin
-// to the clusters with the fewer routed units (all clusters if the routed
-// units divide evenly): routed work waits for the top-k and sets the layer's
-// length, shared work fills the wait.  A cluster runs its shared units first.
+// over every cluster, those with fewer routed units first
+// (cluster_unit_owner_shared): routed work waits for the top-k and sets the
+// layer's length, shared work fills the wait, which holds one or two units.
+// A cluster runs its shared units first.
 // Within each list a unit's down stage follows the next unit's two gate/up
 // stages.  Returns the number of units (> kMaxU: does not fit).
 __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
@@ -382,6 +412,23 @@ __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
 
 // ------------------------------------------------------------------ producer
 
+// The producer's bounded wait until the top-k warp has published rank
+// target - 64 * layer - 1 (acquire: its id is then visible).
+__device__ bool wait_rank(const CParams& p, const Smem& S, unsigned target) {
+  const long long t0 = clock64();
+  for (unsigned it = 0;; ++it) {
+    unsigned v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(&S.topk_seq)) : "memory");
+    if (v >= target) return true;
+    if (clock64() - t0 > p.spin_limit) {
+      note_timeout(p, W_P_TOPK);
+      return false;
+    }
+    if ((it & 15) == 15 && aborted(p)) return false;
+    __nanosleep(32);
+  }
+}
+
 __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
   const int n_rel = p.l1 - p.l0;
   const uint32_t tile_bytes = static_cast<uint32_t>(p.d / 64) * kGroupBytes;   // gate/up tile = down slice
@@ -398,7 +445,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L->dn_shared)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L->dn_routed)) : "memory");
     if (static_cast<int>(blockIdx.x) < p.E) {
-      if (!wait_one(p, &S.rrow_empty, (static_cast<uint32_t>(rel) & 1u) ^ 1u)) {
+      if (!wait_one(p, &S.rrow_empty, (static_cast<uint32_t>(rel) & 1u) ^ 1u, W_RROW_EMPTY)) {
         raise_abort(p);
         break;
       }
@@ -410,17 +457,16 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
     int s = 0;
     for (int i = 0; i < S.n_tasks; ++i) {
       const CTask t = S.tasks[i];
-      if (t.kind == K_TOPK) {
-        if (!wait_one(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {
-          raise_abort(p);
-          stop = true;
-          break;
-        }
-        continue;
+      if (t.kind == K_TOPK) continue;
+      // a routed stage needs only its own rank of the top-k
+      if (t.src >= 0 && !wait_rank(p, S, 64u * static_cast<unsigned>(rel) + static_cast<unsigned>(t.src) + 1u)) {
+        raise_abort(p);
+        stop = true;
+        break;
       }
       const uint32_t u = static_cast<uint32_t>(rel) * S.n_stages + s++;
       const int slot = u % kNS;
-      if (!wait_one(p, &S.empty[slot], ((u / kNS) & 1u) ^ 1u)) {
+      if (!wait_one(p, &S.empty[slot], ((u / kNS) & 1u) ^ 1u, W_EMPTY)) {
         raise_abort(p);
         stop = true;
         break;
@@ -463,7 +509,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
 // (low bits, then index) only when several heads tie there; the winning lane
 // records it directly.
 template <int NPL>
-__device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float* gates) {
+__device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float* gates, unsigned seq_base) {
   const int lane = threadIdx.x & 31;
   const unsigned cl = cluster_idx(), n_cl = cluster_count();
   const unsigned long long* lg = p.tlog + (static_cast<size_t>(l) * n_cl + cl) * p.E * 2;
@@ -492,7 +538,10 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
     if ((it & 63) == 63) {
       if (__any_sync(kFull, aborted(p))) return false;
       if (__any_sync(kFull, clock64() - t0 > p.spin_limit)) {
-        if (lane == 0) raise_abort(p);
+        if (lane == 0) {
+          note_timeout(p, W_LOGITS);
+          raise_abort(p);
+        }
         return false;
       }
     }
@@ -540,8 +589,12 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
       S.topv[j] = static_cast<long long>(hk ^ 0x8000000000000000ull);
       ++head;
     }
+    // rank j is known: the producer may load its expert while the warp picks the rest
+    __syncwarp();
+    if (lane == 0)
+      asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(&S.topk_seq)), "r"(seq_base + j + 1)
+                   : "memory");
   }
-  __syncwarp();
   float ex = 0.f;
   if (lane < p.k) ex = expf(__ll2float_rn(S.topv[lane] - S.topv[0]) * 9.094947017729282e-13f);   // 2^-40
   float sum = 0.f;
@@ -557,8 +610,9 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
   for (int rel = 0; rel < n_rel; ++rel) {
     int32_t* sid = S.ids[rel & 1];
     float* sg = S.gates[rel & 1];
-    const bool ok =
-        p.E <= 128 ? topk_layer<4>(p, S, p.l0 + rel, sid, sg) : topk_layer<8>(p, S, p.l0 + rel, sid, sg);
+    const unsigned base = 64u * static_cast<unsigned>(rel);
+    const bool ok = p.E <= 128 ? topk_layer<4>(p, S, p.l0 + rel, sid, sg, base)
+                               : topk_layer<8>(p, S, p.l0 + rel, sid, sg, base);
     if (!ok) return;
     if (lane == 0) stamp(p, rel, EV_TOPK_DONE);
     if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
@@ -574,10 +628,44 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
 
 // ------------------------------------------------------------------ consumers
 
+// Logit of router row blockIdx.x of layer rel: the warps' exact partials
+// (formed with x in prep) summed, plus the bias, published with this launch's
+// tag in both 64-bit words.  Run by consumer warp 0 in prep, right after the
+// barrier that completes the partials (the operands of x come after).
+__device__ void router_publish(const CParams& p, Smem& S, int cw, int rel, float bv) {
+  if (static_cast<int>(blockIdx.x) >= p.E || cw != 0) return;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) stamp(p, rel, EV_ROUTER_B);
+  // every lane forms the same logit (the warps' parts in warp order, plus the bias)
+  long long acc = 0;
+  for (int w = 0; w < kNC; ++w) acc += S.rlog[w];
+  const DevCallArgs* A = &S.args;
+  if (A->bias) {   // bv: this CTA's bias entry, loaded at the start of the layer
+    if (!(fabsf(bv) < 1048576.f)) {
+      if (lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);
+    } else {
+      acc += __float2ll_rn(bv * 1099511627776.0f);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbarrier_arrive(&S.rrow_empty);   // every warp read the row before the barrier
+  const long long logit = acc;
+  if (lane == 0 && A->dbg_logits && rel < A->dbg_layers)
+    A->dbg_logits[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.E + blockIdx.x] = logit;
+  const unsigned long long tg = static_cast<unsigned long long>(p.tag) << 32;
+  const unsigned long long ua = static_cast<unsigned long long>(logit);
+  const unsigned n_cl = cluster_count();
+  for (unsigned c = lane; c < n_cl; c += 32)
+    st_volatile_u64x2(p.tlog + ((static_cast<size_t>(p.l0 + rel) * n_cl + c) * p.E + blockIdx.x) * 2,
+                      (ua & 0xFFFFFFFFull) | tg, (ua >> 32) | tg);
+  if (lane == 0) stamp(p, rel, EV_LOGIT_OUT);
+  __syncwarp();
+}
+
 // Layer input: wait for the previous layer's output vector, add it to this
 // CTA's copy of the residual stream, RMS norm in a fixed order (every CTA gets
 // the same x), x as plain bf16, as mma B fragments and as per-group sums.
-__device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, unsigned rank) {
+__device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, unsigned rank, float bias_v) {
   const int lane = threadIdx.x & 31;
   const int d = p.d, nGd = d / 64;
   const DevCallArgs* A = &S.args;
@@ -614,95 +702,73 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
       r = 1.0f / sqrtf(tot / static_cast<float>(d) + p.eps);
     }
   } else {
-    // the previous layer's output: this CTA polls and reads its rank's quarter
-    // (element pairs spread over the warps), adds it to the residual and
-    // writes the result into every CTA of the cluster, with the quarter's sums
-    // of squares; after the cluster barrier every CTA holds the whole h.  The
-    // residual and the sums are double-buffered by layer parity: a peer may
-    // still be reading the previous layer's copy (its x step), never the one
-    // before (it has passed this layer's cluster barrier since).
+    // the previous layer's output: every CTA polls the whole vector (element
+    // pairs spread over the warps; all rows complete also means every CTA of
+    // the grid has finished the previous layer's input step), adds it to its
+    // residual copy and sums the squares; one CTA barrier then completes h.
+    // The residual is double-buffered by layer parity (the finishing CTAs of
+    // the last layer read the copy the layer started from).
     const long long* yin = p.ybuf + static_cast<size_t>((rel - 1) % 3) * d;
-    const int npair = d / 8;                          // element pairs per quarter
-    const int j = cw * 32 + lane, e = static_cast<int>(rank) * (d / 4) + 2 * j;   // pair j of this quarter
+    const int npair = d / 2;                          // element pairs of the vector
     float ss = 0.f;
-    if (cw * 32 < npair) {
+    for (int j0 = cw * 32; j0 < npair; j0 += kNC * 32) {
+      const int j = j0 + lane, e = 2 * j;
       const bool valid = j < npair;
       float y0, y1;
-      if (!poll_rows(p, yin + e, valid, y0, y1)) return false;
-      if (cw == 0 && lane == 0) stamp(p, rel, EV_Y_SEEN);
+      if (!poll_rows(p, yin + e, valid, y0, y1, W_Y_POLL)) return false;
       if (valid) {
-        const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h[(rel - 1) & 1])[e / 2];
+        const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h[(rel - 1) & 1])[j];
         const float a = bf16_bits_to_float(static_cast<uint16_t>(hv & 0xFFFFu)) + y0;
         const float b = bf16_bits_to_float(static_cast<uint16_t>(hv >> 16)) + y1;
         const uint32_t v =
             static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
-        reinterpret_cast<uint32_t*>(S.h[rel & 1])[e / 2] = v;   // copied to the peers below
+        reinterpret_cast<uint32_t*>(S.h[rel & 1])[j] = v;
         const float ha = bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu));
         const float hb = bf16_bits_to_float(static_cast<uint16_t>(v >> 16));
-        ss = ha * ha + hb * hb;
-        if (blockIdx.x < static_cast<unsigned>(kCl) && A->dbg_y && rel - 1 < A->dbg_layers) {   // cluster 0
+        ss += ha * ha + hb * hb;
+        if (blockIdx.x == 0 && A->dbg_y && rel - 1 < A->dbg_layers) {
           float* dy = A->dbg_y + (static_cast<size_t>(rel - 1) * A->tok_total + A->tok_off) * d + e;
           dy[0] = y0;
           dy[1] = y1;
         }
       }
     }
+    if (cw == 0 && lane == 0) stamp(p, rel, EV_Y_SEEN);
 #pragma unroll
     for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(kFull, ss, m);
-    if (lane == 0) S.ssq[rel & 1][rank][cw] = ss;
-    __syncwarp();
-    // lane r < 4 copies this warp's block of the new residual (up to 32 words,
-    // 16-byte aligned) and its sum of squares into CTA r of the cluster, then
-    // arrives there with release semantics (ordering its own stores: no fence)
-    if (lane < kCl) {
-      const unsigned r = static_cast<unsigned>(lane);
-      if (r != rank) {
-        const int w0 = cw * 32, nw = min(32, npair - w0);
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(S.h[rel & 1]) + static_cast<int>(rank) * (d / 8) + w0;
-        const uint32_t dst = peer_addr(src, r);
-        for (int i = 0; i < nw; i += 4) {
-          const uint4 v4 = *reinterpret_cast<const uint4*>(src + i);
-          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 4 * i), "r"(v4.x), "r"(v4.y),
-                       "r"(v4.z), "r"(v4.w)
-                       : "memory");
-        }
-        st_peer_f32(peer_addr(&S.ssq[rel & 1][rank][cw], r), ss);
-      }
-      arrive_peer(peer_addr(&S.clbar, r));
-    }
-    __syncwarp();
-    if (!mbar_wait_cluster(p, &S.clbar, static_cast<uint32_t>(rel - 1) & 1u)) {
-      raise_abort(p);
-      return false;
-    }
+    if (lane == 0) S.red[cw] = ss;
+    if (!consumer_barrier(p, S, ++round)) return false;   // red[] and S.h complete
     if (cw == 0 && lane == 0) stamp(p, rel, EV_PREP_B1);
     // every CTA has added into the previous layer's vector, so every CTA is
     // done reading the one before it: zero this CTA's share of it for layer rel + 1
     long long* yz = p.ybuf + static_cast<size_t>((rel + 1) % 3) * d;
     const int share = (d + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-    const int zi = static_cast<int>(blockIdx.x) * share + j;
-    if (j < share && zi < d) yz[zi] = 0;
+    const int zj = cw * 32 + lane, zi = static_cast<int>(blockIdx.x) * share + zj;
+    if (zj < share && zi < d) yz[zi] = 0;
     if (p.prenorm) {
       float tot = 0.f;
-      for (int q = 0; q < kCl; ++q)
-        for (int w = 0; w < kNC; ++w) tot += S.ssq[rel & 1][q][w];
+      for (int w = 0; w < kNC; ++w) tot += S.red[w];
       r = 1.0f / sqrtf(tot / static_cast<float>(d) + p.eps);
     }
   }
   if (cw == 0 && lane == 0) stamp(p, rel, EV_PREP_B2);
-  // the router row of this CTA's expert is dotted with x as x is formed: each
-  // warp adds its elements' exact products (RNE onto the 2^-40 grid, integer
-  // sums, so the split does not change the logit) and leaves one partial
+  // x first, with the router row of this CTA's expert dotted into it (each
+  // warp adds its elements' exact products: RNE onto the 2^-40 grid, integer
+  // sums, so the split does not change the logit); the warps' partials are
+  // complete at the next barrier, after which warp 0 publishes the logit while
+  // the others build the matrix operands of x
   const bool routes = static_cast<int>(blockIdx.x) < p.E;
-  if (routes && !wait_warp(p, &S.rrow_full, static_cast<uint32_t>(rel) & 1u)) {
+  if (routes && !wait_warp(p, &S.rrow_full, static_cast<uint32_t>(rel) & 1u, W_RROW_FULL)) {
     raise_abort(p);
     return false;
   }
   Fix40 fx;
   bool bad = false;
+  uint32_t xw[kGW];
 #pragma unroll
   for (int i = 0; i < kGW; ++i) {
     const int G = cw + kNC * i;
+    xw[i] = 0u;
     if (G >= nGd) continue;
     uint32_t xv = reinterpret_cast<const uint32_t*>(S.h[rel & 1])[32 * G + lane];
     if (p.prenorm) {
@@ -710,6 +776,7 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
       const float b = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16)) * r;
       xv = static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
     }
+    xw[i] = xv;
     if (routes) {
       const uint32_t wv = reinterpret_cast<const uint32_t*>(S.rrow)[32 * G + lane];
 #pragma unroll
@@ -722,6 +789,23 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
         fix40_add(fx, okp ? prod * 1099511627776.0f : 0.f);
       }
     }
+  }
+  if (routes) {
+    long long acc = fix40_value(fx);
+#pragma unroll
+    for (int m = 16; m; m >>= 1) acc += shfl_xor_i64(acc, m);
+    if (__any_sync(kFull, bad) && lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);
+    if (lane == 0) S.rlog[cw] = acc;
+  }
+  if (!consumer_barrier(p, S, ++round)) return false;   // the router partials complete
+  if (cw == 0 && lane == 0) stamp(p, rel, EV_X_READY);
+  router_publish(p, S, cw, rel, bias_v);
+  // the matrix operands: x as fp16 mma B fragments and its per-group sums
+#pragma unroll
+  for (int i = 0; i < kGW; ++i) {
+    const int G = cw + kNC * i;
+    if (G >= nGd) continue;
+    const uint32_t xv = xw[i];
     // fp16 B fragments: element e = 2*lane of the group lands in (t4, st, pos)
     const float xa = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu));
     const float xb = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16));
@@ -738,50 +822,7 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     if (blockIdx.x == 0 && A->dbg_x && rel < A->dbg_layers)
       reinterpret_cast<uint32_t*>(A->dbg_x + (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * d)[32 * G + lane] = xv;
   }
-  if (routes) {
-    long long acc = fix40_value(fx);
-#pragma unroll
-    for (int m = 16; m; m >>= 1) acc += shfl_xor_i64(acc, m);
-    if (__any_sync(kFull, bad) && lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);
-    if (lane == 0) S.rlog[cw] = acc;
-  }
-  const bool ok = consumer_barrier(p, S, ++round);   // x and the router partials complete
-  if (cw == 0 && lane == 0) stamp(p, rel, EV_X_READY);
-  return ok;
-}
-
-// Logit of router row blockIdx.x of layer rel: the warps' exact partials
-// (formed with x in prep) summed, plus the bias, published with this launch's
-// tag in both 64-bit words.  Run by consumer warp 0 after the x barrier.
-__device__ void router_publish(const CParams& p, Smem& S, int cw, int rel) {
-  if (static_cast<int>(blockIdx.x) >= p.E || cw != 0) return;
-  const int lane = threadIdx.x & 31;
-  if (lane == 0) stamp(p, rel, EV_ROUTER_B);
-  // every lane forms the same logit (the warps' parts in warp order, plus the bias)
-  long long acc = 0;
-  for (int w = 0; w < kNC; ++w) acc += S.rlog[w];
-  const DevCallArgs* A = &S.args;
-  if (A->bias) {
-    const float bv = A->bias[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.E + blockIdx.x];
-    if (!(fabsf(bv) < 1048576.f)) {
-      if (lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);
-    } else {
-      acc += __float2ll_rn(bv * 1099511627776.0f);
-    }
-  }
-  __syncwarp();
-  if (lane == 0) mbarrier_arrive(&S.rrow_empty);   // every warp read the row before the barrier
-  const long long logit = acc;
-  if (lane == 0 && A->dbg_logits && rel < A->dbg_layers)
-    A->dbg_logits[(static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.E + blockIdx.x] = logit;
-  const unsigned long long tg = static_cast<unsigned long long>(p.tag) << 32;
-  const unsigned long long ua = static_cast<unsigned long long>(logit);
-  const unsigned n_cl = cluster_count();
-  for (unsigned c = lane; c < n_cl; c += 32)
-    st_volatile_u64x2(p.tlog + ((static_cast<size_t>(p.l0 + rel) * n_cl + c) * p.E + blockIdx.x) * 2,
-                      (ua & 0xFFFFFFFFull) | tg, (ua >> 32) | tg);
-  if (lane == 0) stamp(p, rel, EV_LOGIT_OUT);
-  __syncwarp();
+  return consumer_barrier(p, S, ++round);   // x's operands complete
 }
 
 // Eight packed nibbles -> four f16x2 A-fragment registers with four logic ops
@@ -916,15 +957,27 @@ __device__ void stage_gu(const CParams& p, Smem& S, int qw, int rel, int slot, c
   gu_push(p, S, rel, t, rank, ga, ua);
 }
 
+// RNE(v * 2^32) for |v| < 2^17 with 32-bit conversions only (conversions to
+// 64-bit integers run on this part's narrow FP64 path: see grid_to_float):
+// for a = |v| * 2^8, floor(a) and a - floor(a) are exact in fp32, so
+// RNE(|v| 2^32) = floor(a) 2^24 + RNE((a - floor(a)) 2^24).
+__device__ __forceinline__ long long grid_from_float(float v) {
+  const float a = fabsf(v) * 256.f;
+  const float fa = floorf(a);
+  const long long m = static_cast<long long>(static_cast<int>(fa)) * 16777216ll +
+                      static_cast<long long>(__float2uint_rn((a - fa) * 16777216.f));
+  return v < 0.f ? -m : m;
+}
+
 // Down stage: this CTA's d/64 row tiles of the unit's group, warp qw of the
 // quad taking tiles qw, qw + 4, ...; every tile uses the same 64 values of a
 // (fp16 hi + lo in two B columns).  Rows g and g + 8 of a tile follow the
 // gate/up epilogue's two forms (1024 + q and 1024 + 16 q).
-__device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, const CTask& t,
+__device__ bool stage_dn(const CParams& p, Smem& S, int quad, int qw, int rel, int slot, const CTask& t,
                          unsigned long long* t_ready) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int aslot = (rel & 1) * kMaxU + t.ui;
-  if (!mbar_wait_cluster(p, &S.a_full[aslot], (static_cast<uint32_t>(rel) >> 1) & 1u)) return false;
+  if (!mbar_wait_cluster(p, &S.a_full[aslot], (static_cast<uint32_t>(rel) >> 1) & 1u, W_A_FULL)) return false;
   if (lane == 0) {
     stamp(p, rel, EV_DN_A_FIRST);
     stamp(p, rel, EV_A_WAIT_LAST, true);
@@ -939,7 +992,11 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
   const uint4 b01 = make_uint4(ab[0], ab[8], ab[16], ab[24]);
   const uint4 b23 = make_uint4(ab[32], ab[40], ab[48], ab[56]);
   const int R = p.d / 64;
-  float* out = S.dn_part[t.ui];
+  // the unit's weight in the combine: 1 for the shared expert, else its gate
+  // (published with the top-k before any routed stage was issued)
+  if (t.src >= 0 && !wait_warp(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u, W_DN_TOPK)) return false;
+  const float wgt = t.src < 0 ? 1.f : S.gates[rel & 1][t.src];
+  float* acc = S.dn_acc[quad];   // this quad's rows; the warp owns row tiles qw, qw + 4, ...
 #pragma unroll 2
   for (int T = qw; T < R; T += kQW) {
     const uint8_t* blk = S.ring[slot] + static_cast<size_t>(T) * kGroupBytes;
@@ -959,43 +1016,40 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int qw, int rel, int slot, c
     const float y0 = s0 * ((c0[0] + c1[0]) + (c0[1] + c1[1])) + fmaf(-1024.f, s0, o0) * As;
     const float y1 = (s1 * 0.0625f) * ((c0[2] + c1[2]) + (c0[3] + c1[3])) + fmaf(-64.f, s1, o1) * As;
     if (t4 == 0) {
-      out[T * 16 + g] = y0;
-      out[T * 16 + g + 8] = y1;
+      acc[T * 16 + g] += wgt * y0;
+      acc[T * 16 + g + 8] += wgt * y1;
     }
   }
   return true;
 }
 
-// End of layer rel: gate-weighted sum of the units' partials in unit order,
-// onto the 2^-32 grid with this CTA's count in the low byte, and one bulk
-// reduction into the layer's output vector (not waited for: readers poll the
-// counts).
+// End of layer rel: the CTA's rows (the quads' sums of their down stages,
+// added in quad order: deterministic) onto the 2^-32 grid with this CTA's
+// count in the low byte, and one bulk reduction into the layer's output
+// vector (not waited for: readers poll the counts).
 __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round, unsigned rank) {
   const int lane = threadIdx.x & 31;
-  if (!wait_warp(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u)) {   // gates of this layer
+  if (!wait_warp(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u, W_END_TOPK)) {   // gates of this layer
     raise_abort(p);
     return false;
   }
   // the previous layer's bulk reduction must have read yq before it is rewritten
   if (cw == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-  if (!consumer_barrier(p, S, ++round)) return false;   // every down partial of the layer written
+  if (!consumer_barrier(p, S, ++round)) return false;   // every down stage of the layer added in
   if (cw == 0 && lane == 0) stamp(p, rel, EV_STAGES_DONE);
   const int rows = p.d / kCl;
-  const float* gts = S.gates[rel & 1];
   bool bad = false;
   for (int i0 = 0; i0 < rows; i0 += kNC * 32) {
     const int i = i0 + cw * 32 + lane;
     if (i < rows) {
-      float y = 0.f;
-      for (int u = 0; u < S.n_units; ++u) {
-        const int src = S.unit_src[u];
-        y = fmaf(src < 0 ? 1.f : gts[src], S.dn_part[u][i], y);
-      }
+      const float y = ((S.dn_acc[0][i] + S.dn_acc[1][i]) + S.dn_acc[2][i]) + S.dn_acc[3][i];
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q) S.dn_acc[q][i] = 0.f;
       // |y| < 2^17 (v < 2^49 on the 2^-32 grid): with at most 64 clusters the
       // int64 sum of (v << 8) stays below 2^63 (the host checks the count)
       const bool ok = fabsf(y) < 131072.f;
       bad |= !ok;
-      S.yq[i] = (ok ? (__float2ll_rn(y * 4294967296.f) << 8) : 0ll) + 1;   // + 1: this CTA's count
+      S.yq[i] = (ok ? (grid_from_float(y) << 8) : 0ll) + 1;   // + 1: this CTA's count
     }
   }
   if (__any_sync(kFull, bad) && lane == 0) atomicOr(p.err, ERR_Y_RANGE);
@@ -1034,7 +1088,7 @@ __device__ void finish(const CParams& p, Smem& S, int cw, int rel, unsigned rank
   const bool valid = j < npair;
   long long* yv = p.ybuf + static_cast<size_t>(rel % 3) * d + e;
   float y0, y1;
-  if (!poll_rows(p, yv, valid, y0, y1) || !valid) return;
+  if (!poll_rows(p, yv, valid, y0, y1, W_FINISH) || !valid) return;
   const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h[rel & 1])[e / 2];
   const float a = bf16_bits_to_float(static_cast<uint16_t>(hv & 0xFFFFu)) + y0;
   const float b = bf16_bits_to_float(static_cast<uint16_t>(hv >> 16)) + y1;
@@ -1060,8 +1114,11 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
   const int n_rel = p.l1 - p.l0;
   int round = 0;
   for (int rel = 0; rel < n_rel; ++rel) {
-    if (!prep(p, S, cw, rel, round, rank)) return;
-    router_publish(p, S, cw, rel);
+    // the logit bias of this CTA's expert, loaded now and used once the logit is formed
+    float bias_v = 0.f;
+    if (cw == 0 && S.args.bias && static_cast<int>(blockIdx.x) < p.E)
+      bias_v = S.args.bias[(static_cast<size_t>(rel) * S.args.tok_total + S.args.tok_off) * p.E + blockIdx.x];
+    if (!prep(p, S, cw, rel, round, rank, bias_v)) return;
     // stage u of the CTA goes to quad u mod 4
     int s = 0;
     for (int i = 0; i < S.n_tasks; ++i) {
@@ -1071,7 +1128,7 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
       if (static_cast<int>(u % kNQ) != quad) continue;
       const int slot = u % kNS;
       const unsigned long long t0 = p.timeline ? now_ns() : 0ull;
-      if (!wait_warp(p, &S.full[slot], (u / kNS) & 1u)) {
+      if (!wait_warp(p, &S.full[slot], (u / kNS) & 1u, W_FULL)) {
         raise_abort(p);
         return;
       }
@@ -1084,7 +1141,7 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
       unsigned long long ta = t1;
       if (t.kind == K_GU) {
         stage_gu(p, S, qw, rel, slot, t, rank);
-      } else if (!stage_dn(p, S, qw, rel, slot, t, &ta)) {
+      } else if (!stage_dn(p, S, quad, qw, rel, slot, t, &ta)) {
         raise_abort(p);
         return;
       }
@@ -1113,7 +1170,10 @@ __global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1
   const unsigned rank = cluster_rank();
   // every distributed-shared-memory address below assumes clusters of kCl
   // CTAs covering the grid: anything else returns before touching a peer
-  if (cluster_size() != static_cast<unsigned>(kCl) || cluster_count() * kCl != gridDim.x) {
+  // (and the bulk and TMA copies into the ring need its 128-byte alignment,
+  // the same in every CTA of the launch)
+  if (cluster_size() != static_cast<unsigned>(kCl) || cluster_count() * kCl != gridDim.x ||
+      (smem_u32(smem_raw) & 127u) != 0) {
     if (threadIdx.x == 0) atomicOr(p.err, ERR_LAUNCH_SHAPE);
     return;
   }
@@ -1126,14 +1186,15 @@ __global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1
     mbar_init(&S.rrow_full, 1);
     mbar_init(&S.rrow_empty, 1);
     mbar_init(&S.topk_bar, 1);
+    S.topk_seq = 0;
     mbar_init(&S.cbar, kNC);
-    mbar_init(&S.clbar, kCl * kNC);
     fence_mbar_init();
     S.args = *p.args;
     if (build_tasks(p, S, static_cast<int>(cluster_idx()), static_cast<int>(cluster_count())) > kMaxU)
       raise_abort(p);
   }
   if (threadIdx.x < kNS) S.gu_cnt[threadIdx.x] = 0;
+  for (int i = threadIdx.x; i < kNQ * kMaxRows; i += blockDim.x) (&S.dn_acc[0][0])[i] = 0.f;
   __syncthreads();
   cluster_sync_all();   // every CTA's barriers exist before any remote arrival
   if (!aborted(p)) {
@@ -1150,13 +1211,12 @@ __global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1
   cluster_sync_all();   // no CTA leaves while a peer may still write into its shared memory
   // the last CTA out resets the exit counter and the abort flag (and, after an
   // abort, zeroes the output vectors, whose counts would otherwise be stale)
-  __shared__ int s_last;
   if (threadIdx.x == 0) {
     __threadfence();
-    s_last = atomicAdd(p.exit_cnt, 1u) == gridDim.x - 1;
+    S.last_out = atomicAdd(p.exit_cnt, 1u) == gridDim.x - 1;
   }
   __syncthreads();
-  if (s_last) {
+  if (S.last_out) {
     __threadfence();
     if (aborted(p))
       for (int i = threadIdx.x; i < 3 * p.d; i += blockDim.x) p.ybuf[i] = 0;

@@ -89,6 +89,7 @@ struct CParams {
   unsigned long long* tlog;            // [n_layers][n_cl][E][2]: per cluster, logit low / high word, each | tag << 32
   unsigned tag;                        // this launch's tag (never 0)
   long long spin_limit;                // bounded waits give up after this many cycles
+  unsigned* diag;                      // first wait that ran out: site << 16 | CTA (0: none)
   long long* ybuf;                     // [3][d] layer outputs: sum over CTAs of (v << 8) + 1, v on the 2^-32 grid;
                                        // zero between launches
   unsigned* exit_cnt;
@@ -98,10 +99,13 @@ struct CParams {
 };
 
 // Cluster of shared unit G (of the shared expert's f_s/64 groups) when the
-// Ur routed units are dealt round-robin over n_cl clusters.
+// Ur routed units are dealt round-robin over n_cl clusters (clusters below
+// Ur mod n_cl get one more).  Shared units run while the routing is not yet
+// known, so every cluster takes one before any takes two; the clusters with
+// fewer routed units come first in that round-robin.
 __host__ __device__ inline int cluster_unit_owner_shared(int G, int Ur, int n_cl) {
-  const int extra = Ur % n_cl;
-  return extra == 0 ? G % n_cl : extra + G % (n_cl - extra);
+  const int extra = Ur % n_cl, i = G % n_cl;
+  return i < n_cl - extra ? extra + i : i - (n_cl - extra);
 }
 
 size_t cluster_smem();

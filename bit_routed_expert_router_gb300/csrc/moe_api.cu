@@ -526,6 +526,7 @@ moe_status cluster_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   p.ybuf = ctx->c_ybuf;
   p.exit_cnt = ctx->c_counters;
   p.abort_flag = ctx->c_counters + 1;
+  p.diag = ctx->c_counters + 2;
   p.err = ctx->err_word;
   p.timeline = ctx->p_timeline;
   p.spin_limit = ctx->spin_limit;
@@ -931,7 +932,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->p_gates = dalloc<float>(static_cast<size_t>(c.n_layers) * c.top_k, o, nb);
   ctx->c_layers = dalloc<CLayer>(c.n_layers, o, nb);
   ctx->c_ybuf = dalloc<long long>(static_cast<size_t>(3) * c.d, o, nb);
-  ctx->c_counters = dalloc<unsigned>(2, o, nb);
+  ctx->c_counters = dalloc<unsigned>(4, o, nb);   // exit counter, abort flag, wait diagnostic, spare
   for (void* ptr : o)
     if (!ptr) return bail(MOE_ENOMEM);
   if (!ctx->hbuf[0] || !ctx->hbuf[1] || !ctx->x_perm || !ctx->dargs || !ctx->y_r || !ctx->part_s || !ctx->a_r)
@@ -946,7 +947,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       cudaMemset(ctx->p_layers, 0, sizeof(PLayer) * c.n_layers) != cudaSuccess ||
       cudaMemset(ctx->c_layers, 0, sizeof(CLayer) * c.n_layers) != cudaSuccess ||
       cudaMemset(ctx->c_ybuf, 0, static_cast<size_t>(3) * c.d * 8) != cudaSuccess ||
-      cudaMemset(ctx->c_counters, 0, 8) != cudaSuccess)
+      cudaMemset(ctx->c_counters, 0, 16) != cudaSuccess)
     return bail(MOE_ECUDA);
   if (cudaHostAlloc(reinterpret_cast<void**>(&ctx->args_ring), sizeof(DevCallArgs) * kArgRing, cudaHostAllocDefault) !=
       cudaSuccess)
@@ -990,7 +991,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // range of its int64 layer-output sums)
   {
     int n_cl = 0;
-    if (c.top_k <= 32 && c.d <= kCMaxD && cluster_smem() + 2048 <= static_cast<size_t>(max_smem) &&
+    if (c.top_k <= 32 && c.d <= kCMaxD && cluster_smem() <= static_cast<size_t>(max_smem) &&
         cluster_attrs() == cudaSuccess &&
         cluster_max_active(&n_cl) == cudaSuccess && n_cl >= 1 && n_cl <= 64 && c.n_experts <= n_cl * kCCluster &&
         cluster_units_max(c, n_cl) <= cluster_max_units()) {
@@ -1945,6 +1946,13 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
         if (v) return MOE_ESTATE;
       for (long long v : yb)
         if (v) return MOE_ESTATE;
+      return MOE_OK;
+    }
+    case 12: {  // the clustered kernel's wait diagnostic (site << 16 | CTA, 0: none) into *(uint32_t*)value, then cleared
+      if (!value || !ctx->c_counters) return fail(ctx, MOE_EINVAL, "hook 12 needs a host address and the clustered kernel");
+      CK(cudaDeviceSynchronize());
+      CK(cudaMemcpy(reinterpret_cast<void*>(static_cast<uintptr_t>(value)), ctx->c_counters + 2, 4, cudaMemcpyDeviceToHost));
+      CK(cudaMemset(ctx->c_counters + 2, 0, 4));
       return MOE_OK;
     }
     case 6:  // budget checks see `value` bytes of free device memory (-1: the real figure)

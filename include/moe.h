@@ -457,7 +457,11 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
  * context.  hook 11 (value ignored, allowed on a poisoned context): waits for
  * the device, then MOE_OK if the persistent kernels' exit counters, abort
  * flags, dependency counters and fixed-point output sums are all zero, else
- * MOE_ESTATE.  Other hooks: MOE_EINVAL. */
+ * MOE_ESTATE.  hook 12 (allowed on a poisoned context): waits for the device,
+ * writes the clustered kernel's wait diagnostic into the host uint32 at
+ * address `value` and clears it: 0 if no wait ran out, else (site << 16) |
+ * CTA of the first wait that did (sites are listed in decode_cluster.cu).
+ * Other hooks: MOE_EINVAL. */
 moe_status moe_test_hook(moe_ctx *ctx, int hook, int64_t value);
 
 const char *moe_status_string(moe_status s);

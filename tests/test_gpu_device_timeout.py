@@ -47,6 +47,12 @@ def test_device_wait_that_runs_out_poisons_only_its_context(kernel):
         assert st == moe.MOE_ESTATE                   # poisoned
         # the aborted launch left its exit counter, abort flag, counters and sums at rest
         assert moe.moe_test_hook(ctx.h, moe.HOOK_AT_REST, 0) == moe.MOE_OK
+        if kernel == "cluster":
+            # and recorded which wait ran out first (a site and a CTA of the grid)
+            import ctypes
+            word = ctypes.c_uint32(0)
+            assert moe.moe_test_hook(ctx.h, moe.HOOK_WAIT_DIAG, ctypes.addressof(word)) == moe.MOE_OK
+            assert 1 <= word.value >> 16 <= 13, hex(word.value)
     torch.cuda.synchronize()                          # the device still answers
     with _ctx(ws, kernel) as ctx:
         for t in range(3):
