@@ -529,9 +529,9 @@ PF_SEED = 4
 TIMELINE_EVENTS = ["y_seen", "x_ready", "logit_out", "logits_in", "topk_done", "routed_issue", "shared_data",
                    "routed_data", "push_last", "dn_last", "stages_done", "reduced", "issue_last", "data_last",
                    "dn_a_first", "a_wait_last", "prep_cluster_barrier", "prep_y", "prep_norm", "router_publish",
-                   "topk_sorted", "bulk_issued"]
+                   "topk_sorted", "bulk_issued", "ops_ready"]
 TIMELINE_SUMS = ["gateup_compute", "down_compute", "down_wait_for_a", "routed_data_wait", "gateup_stages",
-                 "down_stages", "shared_data_wait"]
+                 "down_stages", "shared_data_wait", "end_barrier_wait"]
 
 
 def print_timeline(moe, ctx, step, first, reps=3, raw_out=None):

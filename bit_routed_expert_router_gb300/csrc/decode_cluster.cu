@@ -89,7 +89,7 @@ struct CTask {
 struct Smem {
   alignas(128) uint8_t ring[kNS][kSlotBytes];     // bulk / TMA targets
   alignas(16) uint16_t rrow[kMaxD];                // this CTA's router row (fp16)
-  alignas(16) uint16_t h[2][kMaxD];                // residual stream (bf16) by layer parity, the same in every CTA
+  alignas(16) uint16_t h[kMaxD];                   // residual stream (bf16), the same in every CTA
   alignas(16) uint16_t xp[kMaxD];                  // x as fp16 mma B fragments
   alignas(16) float xg[kMaxG];                     // per-group sums of the fp16 x
   alignas(16) uint32_t abuf[2 * kMaxU][64];        // per unit: a as B-fragment words, block (2 rank + tile) of 8
@@ -117,7 +117,7 @@ struct Smem {
   float gates[2][32];
   alignas(8) long long topv[32];                   // top-k logits in rank order
   int last_out;                                    // this CTA is the last to leave the launch
-  unsigned topk_seq;                               // 64 * layer + ranks of the layer's top-k picked so far
+  unsigned rank_word[32];                          // rank j of the top-k: (64 * layer + j + 1) << 8 | expert
 };
 
 static_assert(offsetof(Smem, ring) % 128 == 0 && kSlotBytes % 128 == 0, "TMA targets 128-byte aligned");
@@ -327,7 +327,7 @@ __device__ __forceinline__ float gelu_p(float v, int variant) {
 enum : int { EV_Y_SEEN, EV_X_READY, EV_LOGIT_OUT, EV_LOGITS_IN, EV_TOPK_DONE, EV_ROUTED_ISSUE, EV_SHARED_DATA,
              EV_ROUTED_DATA, EV_PUSH_LAST, EV_DN_LAST, EV_STAGES_DONE, EV_REDUCED, EV_ISSUE_LAST, EV_DATA_LAST,
              EV_DN_A_FIRST, EV_A_WAIT_LAST, EV_PREP_B1, EV_PREP_Y, EV_PREP_B2, EV_ROUTER_B, EV_TOPK_SORTED,
-             EV_BULK_ISSUED };
+             EV_BULK_ISSUED, EV_OPS_READY };
 constexpr int kTlCols = 32;            // timeline row: events 0..23, accumulators 24..31
 
 __device__ __forceinline__ void stamp(const CParams& p, int rel, int ev, bool latest = false) {
@@ -344,7 +344,8 @@ __device__ __forceinline__ void stamp(const CParams& p, int rel, int ev, bool la
 // Accumulated times of the stamped layer at columns 24.. of row blockIdx.x:
 // [0] gate/up compute, [1] down compute, [2] down wait for a, [3] data wait
 // (routed stages), [4] gate/up stages, [5] down stages, [6] data wait
-// (shared stages), all in ns summed over the CTA's consumer warps.
+// (shared stages), [7] wait at the layer's end for the other warps' stages,
+// all in ns summed over the CTA's consumer warps.
 __device__ __forceinline__ unsigned long long now_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -412,19 +413,22 @@ __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
 
 // ------------------------------------------------------------------ producer
 
-// The producer's bounded wait until the top-k warp has published rank
-// target - 64 * layer - 1 (acquire: its id is then visible).
-__device__ bool wait_rank(const CParams& p, const Smem& S, unsigned target) {
+// The producer's bounded wait for rank j of layer rel of the top-k (written
+// by the cluster's rank-0 top-k warp); returns the expert, or -1 on abort or
+// timeout.  The tag and the expert share one 32-bit word, so the word alone
+// carries its own readiness (no fence on either side).
+__device__ int wait_rank(const CParams& p, const Smem& S, int rel, int j) {
+  const unsigned tag = 64u * static_cast<unsigned>(rel) + static_cast<unsigned>(j) + 1u;
   const long long t0 = clock64();
   for (unsigned it = 0;; ++it) {
     unsigned v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(&S.topk_seq)) : "memory");
-    if (v >= target) return true;
+    asm volatile("ld.volatile.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(&S.rank_word[j])) : "memory");
+    if ((v >> 8) == tag) return static_cast<int>(v & 0xFFu);
     if (clock64() - t0 > p.spin_limit) {
       note_timeout(p, W_P_TOPK);
-      return false;
+      return -1;
     }
-    if ((it & 15) == 15 && aborted(p)) return false;
+    if ((it & 15) == 15 && aborted(p)) return -1;
     __nanosleep(32);
   }
 }
@@ -459,7 +463,8 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
       const CTask t = S.tasks[i];
       if (t.kind == K_TOPK) continue;
       // a routed stage needs only its own rank of the top-k
-      if (t.src >= 0 && !wait_rank(p, S, 64u * static_cast<unsigned>(rel) + static_cast<unsigned>(t.src) + 1u)) {
+      const int e = t.src < 0 ? 0 : wait_rank(p, S, rel, t.src);
+      if (e < 0) {
         raise_abort(p);
         stop = true;
         break;
@@ -471,7 +476,6 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
         stop = true;
         break;
       }
-      const int e = t.src < 0 ? 0 : S.ids[rel & 1][t.src];
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&S.full[slot], tile_bytes);
       if (t.kind == K_GU) {
@@ -589,22 +593,37 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
       S.topv[j] = static_cast<long long>(hk ^ 0x8000000000000000ull);
       ++head;
     }
-    // rank j is known: the producer may load its expert while the warp picks the rest
+    // rank j is known: lane r < 4 writes it, tagged with the layer and the
+    // rank, into CTA r of the cluster, so the four producers may load its
+    // expert while the warp picks the rest
     __syncwarp();
-    if (lane == 0)
-      asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(&S.topk_seq)), "r"(seq_base + j + 1)
+    if (lane < kCl) {
+      const unsigned word = (seq_base + static_cast<unsigned>(j) + 1u) << 8 | static_cast<unsigned>(ids[j]);
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_addr(&S.rank_word[j], static_cast<unsigned>(lane))),
+                   "r"(word)
                    : "memory");
+    }
   }
   float ex = 0.f;
   if (lane < p.k) ex = expf(__ll2float_rn(S.topv[lane] - S.topv[0]) * 9.094947017729282e-13f);   // 2^-40
   float sum = 0.f;
   for (int j = 0; j < p.k; ++j) sum += __shfl_sync(kFull, ex, j);
-  if (lane < p.k) gates[lane] = ex / sum;
+  const float gv = ex / sum;
+  // lane r < 4 writes the k gates into CTA r (itself included) and then arrives
+  // there on the top-k barrier (release, cluster scope: its own stores first)
+  for (int jj = 0; jj < p.k; ++jj) {
+    const float g = __shfl_sync(kFull, gv, jj);
+    if (lane < kCl) st_peer_f32(peer_addr(&gates[jj], static_cast<unsigned>(lane)), g);
+  }
+  if (lane < kCl) arrive_peer(peer_addr(&S.topk_bar, static_cast<unsigned>(lane)));
   __syncwarp();
   return true;
 }
 
+// Rank 0 of each cluster picks the cluster's top-k for its four CTAs (one
+// poller per cluster, and the four see the same ranks at the same time).
 __device__ void topk_warp(const CParams& p, Smem& S) {
+  if (cluster_rank() != 0) return;
   const int lane = threadIdx.x & 31;
   const int n_rel = p.l1 - p.l0;
   for (int rel = 0; rel < n_rel; ++rel) {
@@ -622,7 +641,6 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
       if (A->dbg_gates) A->dbg_gates[o] = sg[lane];
     }
     __syncwarp();
-    if (lane == 0) mbarrier_arrive(&S.topk_bar);
   }
 }
 
@@ -685,7 +703,7 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     for (int i = 0; i < kGW; ++i) {
       const int G = cw + kNC * i;
       if (G < nGd) {
-        reinterpret_cast<uint32_t*>(S.h[0])[32 * G + lane] = hv[i];
+        reinterpret_cast<uint32_t*>(S.h)[32 * G + lane] = hv[i];
         const float a = bf16_bits_to_float(static_cast<uint16_t>(hv[i] & 0xFFFFu));
         const float b = bf16_bits_to_float(static_cast<uint16_t>(hv[i] >> 16));
         ss += a * a;
@@ -705,9 +723,8 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     // the previous layer's output: every CTA polls the whole vector (element
     // pairs spread over the warps; all rows complete also means every CTA of
     // the grid has finished the previous layer's input step), adds it to its
-    // residual copy and sums the squares; one CTA barrier then completes h.
-    // The residual is double-buffered by layer parity (the finishing CTAs of
-    // the last layer read the copy the layer started from).
+    // residual copy in place and sums the squares; one CTA barrier then
+    // completes h (the previous layer's reads of h all precede its stages).
     const long long* yin = p.ybuf + static_cast<size_t>((rel - 1) % 3) * d;
     const int npair = d / 2;                          // element pairs of the vector
     float ss = 0.f;
@@ -717,12 +734,12 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
       float y0, y1;
       if (!poll_rows(p, yin + e, valid, y0, y1, W_Y_POLL)) return false;
       if (valid) {
-        const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h[(rel - 1) & 1])[j];
+        const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h)[j];
         const float a = bf16_bits_to_float(static_cast<uint16_t>(hv & 0xFFFFu)) + y0;
         const float b = bf16_bits_to_float(static_cast<uint16_t>(hv >> 16)) + y1;
         const uint32_t v =
             static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
-        reinterpret_cast<uint32_t*>(S.h[rel & 1])[j] = v;
+        reinterpret_cast<uint32_t*>(S.h)[j] = v;   // in place: each word by its own lane
         const float ha = bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu));
         const float hb = bf16_bits_to_float(static_cast<uint16_t>(v >> 16));
         ss += ha * ha + hb * hb;
@@ -770,7 +787,7 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     const int G = cw + kNC * i;
     xw[i] = 0u;
     if (G >= nGd) continue;
-    uint32_t xv = reinterpret_cast<const uint32_t*>(S.h[rel & 1])[32 * G + lane];
+    uint32_t xv = reinterpret_cast<const uint32_t*>(S.h)[32 * G + lane];
     if (p.prenorm) {
       const float a = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu)) * r;
       const float b = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16)) * r;
@@ -822,7 +839,9 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     if (blockIdx.x == 0 && A->dbg_x && rel < A->dbg_layers)
       reinterpret_cast<uint32_t*>(A->dbg_x + (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * d)[32 * G + lane] = xv;
   }
-  return consumer_barrier(p, S, ++round);   // x's operands complete
+  const bool ok = consumer_barrier(p, S, ++round);   // x's operands complete
+  if (cw == 0 && lane == 0) stamp(p, rel, EV_OPS_READY);
+  return ok;
 }
 
 // Eight packed nibbles -> four f16x2 A-fragment registers with four logic ops
@@ -994,7 +1013,7 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int quad, int qw, int rel, i
   const int R = p.d / 64;
   // the unit's weight in the combine: 1 for the shared expert, else its gate
   // (published with the top-k before any routed stage was issued)
-  if (t.src >= 0 && !wait_warp(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u, W_DN_TOPK)) return false;
+  if (t.src >= 0 && !mbar_wait_cluster(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u, W_DN_TOPK)) return false;
   const float wgt = t.src < 0 ? 1.f : S.gates[rel & 1][t.src];
   float* acc = S.dn_acc[quad];   // this quad's rows; the warp owns row tiles qw, qw + 4, ...
 #pragma unroll 2
@@ -1029,13 +1048,15 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int quad, int qw, int rel, i
 // vector (not waited for: readers poll the counts).
 __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round, unsigned rank) {
   const int lane = threadIdx.x & 31;
-  if (!wait_warp(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u, W_END_TOPK)) {   // gates of this layer
+  if (!mbar_wait_cluster(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u, W_END_TOPK)) {   // gates of this layer
     raise_abort(p);
     return false;
   }
   // the previous layer's bulk reduction must have read yq before it is rewritten
   if (cw == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  const unsigned long long te = p.timeline ? now_ns() : 0ull;
   if (!consumer_barrier(p, S, ++round)) return false;   // every down stage of the layer added in
+  if (lane == 0 && p.timeline) acc(p, rel, 7, now_ns() - te);
   if (cw == 0 && lane == 0) stamp(p, rel, EV_STAGES_DONE);
   const int rows = p.d / kCl;
   bool bad = false;
@@ -1089,7 +1110,7 @@ __device__ void finish(const CParams& p, Smem& S, int cw, int rel, unsigned rank
   long long* yv = p.ybuf + static_cast<size_t>(rel % 3) * d + e;
   float y0, y1;
   if (!poll_rows(p, yv, valid, y0, y1, W_FINISH) || !valid) return;
-  const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h[rel & 1])[e / 2];
+  const uint32_t hv = reinterpret_cast<const uint32_t*>(S.h)[e / 2];
   const float a = bf16_bits_to_float(static_cast<uint16_t>(hv & 0xFFFFu)) + y0;
   const float b = bf16_bits_to_float(static_cast<uint16_t>(hv >> 16)) + y1;
   reinterpret_cast<uint32_t*>(A->h_out)[e / 2] =
@@ -1186,7 +1207,7 @@ __global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1
     mbar_init(&S.rrow_full, 1);
     mbar_init(&S.rrow_empty, 1);
     mbar_init(&S.topk_bar, 1);
-    S.topk_seq = 0;
+    for (int j = 0; j < 32; ++j) S.rank_word[j] = 0;
     mbar_init(&S.cbar, kNC);
     fence_mbar_init();
     S.args = *p.args;

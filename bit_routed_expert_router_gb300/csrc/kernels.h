@@ -66,9 +66,9 @@ cudaError_t launch_persistent(PParams& p, int grid, cudaStream_t s);
 // Clustered persistent decode kernel (B = 1, resident, every layer in one
 // launch on clusters of kCCluster CTAs, one CTA per SM).
 constexpr int kCCluster = 4;           // CTAs per cluster
-constexpr int kCStages = 6;            // shared-memory ring slots (one gate/up tile or down slice each)
+constexpr int kCStages = 7;            // shared-memory ring slots (one gate/up tile or down slice each)
 constexpr int kCMaxUnits = 6;          // (source, group) units per cluster and layer
-constexpr int kCMaxD = kPMaxD;         // largest d of the clustered kernel
+constexpr int kCMaxD = 2816;           // largest d of the clustered kernel (its ring slots are sized for it)
 constexpr int kCThreads = 32 * 18;     // producer warp, 16 consumer warps, top-k warp
 
 struct CLayer {                        // one layer, device memory (the tensor maps keep it 64-byte aligned)
