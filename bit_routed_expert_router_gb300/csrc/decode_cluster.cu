@@ -104,6 +104,7 @@ struct Smem {
   alignas(8) uint64_t rrow_full;
   alignas(8) uint64_t rrow_empty;
   alignas(8) uint64_t topk_bar;                    // one phase per layer
+  alignas(8) uint64_t zero_bar;                    // one phase per layer: this CTA's share of the next vector zeroed
   alignas(8) uint64_t cbar;                        // consumer-warp barrier
   alignas(16) DevCallArgs args;
   CTask tasks[kMaxTasks];
@@ -169,7 +170,7 @@ __device__ __forceinline__ bool aborted(const CParams& p);
 // Wait sites, recorded with the CTA in p.diag by the first wait that runs out
 // (the others then see the abort flag and leave without recording).
 enum : unsigned { W_CBAR = 1, W_Y_POLL, W_RROW_EMPTY, W_P_TOPK, W_EMPTY, W_LOGITS, W_CLBAR, W_RROW_FULL, W_A_FULL,
-                  W_DN_TOPK, W_END_TOPK, W_FINISH, W_FULL };
+                  W_DN_TOPK, W_END_TOPK, W_FINISH, W_FULL, W_ZERO };
 __device__ __forceinline__ void note_timeout(const CParams& p, unsigned site) {
   atomicOr(p.err, ERR_WAIT_TIMEOUT);
   if (p.diag) atomicCAS(p.diag, 0u, (site << 16) | (blockIdx.x & 0xFFFFu));
@@ -622,25 +623,47 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
 
 // Rank 0 of each cluster picks the cluster's top-k for its four CTAs (one
 // poller per cluster, and the four see the same ranks at the same time).
+// Then, in every CTA, the warp zeroes the CTA's share of the vector layer
+// rel + 1 adds into: the layer's logits exist, so every CTA has finished the
+// previous layer's input step, the last reader of that vector.  The fence
+// that makes the zeros visible before this CTA's next reduction runs here,
+// off the layer's critical path; the zero barrier hands it to the reduction.
 __device__ void topk_warp(const CParams& p, Smem& S) {
-  if (cluster_rank() != 0) return;
   const int lane = threadIdx.x & 31;
-  const int n_rel = p.l1 - p.l0;
+  const int n_rel = p.l1 - p.l0, d = p.d;
   for (int rel = 0; rel < n_rel; ++rel) {
-    int32_t* sid = S.ids[rel & 1];
-    float* sg = S.gates[rel & 1];
-    const unsigned base = 64u * static_cast<unsigned>(rel);
-    const bool ok = p.E <= 128 ? topk_layer<4>(p, S, p.l0 + rel, sid, sg, base)
-                               : topk_layer<8>(p, S, p.l0 + rel, sid, sg, base);
-    if (!ok) return;
-    if (lane == 0) stamp(p, rel, EV_TOPK_DONE);
-    if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
-      const DevCallArgs* A = &S.args;
-      const size_t o = (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.k + lane;
-      if (A->dbg_ids) A->dbg_ids[o] = sid[lane];
-      if (A->dbg_gates) A->dbg_gates[o] = sg[lane];
+    if (cluster_rank() == 0) {
+      int32_t* sid = S.ids[rel & 1];
+      float* sg = S.gates[rel & 1];
+      const unsigned base = 64u * static_cast<unsigned>(rel);
+      const bool ok = p.E <= 128 ? topk_layer<4>(p, S, p.l0 + rel, sid, sg, base)
+                                 : topk_layer<8>(p, S, p.l0 + rel, sid, sg, base);
+      if (!ok) return;
+      if (lane == 0) stamp(p, rel, EV_TOPK_DONE);
+      if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
+        const DevCallArgs* A = &S.args;
+        const size_t o = (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * p.k + lane;
+        if (A->dbg_ids) A->dbg_ids[o] = sid[lane];
+        if (A->dbg_gates) A->dbg_gates[o] = sg[lane];
+      }
+      __syncwarp();
+    }
+    if (!mbar_wait_cluster(p, &S.topk_bar, static_cast<uint32_t>(rel) & 1u, W_DN_TOPK)) {
+      raise_abort(p);
+      return;
+    }
+    if (rel > 0) {
+      long long* yz = p.ybuf + static_cast<size_t>((rel + 1) % 3) * d;
+      const int share = (d + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+      for (int zj = lane; zj < share; zj += 32) {
+        const int zi = static_cast<int>(blockIdx.x) * share + zj;
+        if (zi < d) yz[zi] = 0;
+      }
+      __threadfence();
+      fence_proxy_async_global();
     }
     __syncwarp();
+    if (lane == 0) mbarrier_arrive(&S.zero_bar);
   }
 }
 
@@ -756,12 +779,6 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
     if (lane == 0) S.red[cw] = ss;
     if (!consumer_barrier(p, S, ++round)) return false;   // red[] and S.h complete
     if (cw == 0 && lane == 0) stamp(p, rel, EV_PREP_B1);
-    // every CTA has added into the previous layer's vector, so every CTA is
-    // done reading the one before it: zero this CTA's share of it for layer rel + 1
-    long long* yz = p.ybuf + static_cast<size_t>((rel + 1) % 3) * d;
-    const int share = (d + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-    const int zj = cw * 32 + lane, zi = static_cast<int>(blockIdx.x) * share + zj;
-    if (zj < share && zi < d) yz[zi] = 0;
     if (p.prenorm) {
       float tot = 0.f;
       for (int w = 0; w < kNC; ++w) tot += S.red[w];
@@ -1077,11 +1094,15 @@ __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round
   fence_proxy_async_smem();   // yq is read by the bulk reduction (async proxy)
   if (!consumer_barrier(p, S, ++round)) return false;
   if (cw != 0) return true;
+  // this CTA's zeroing of the next vector (fenced by the top-k warp) before its
+  // reduction; the other CTAs zeroed this vector before adding their rows of
+  // the previous one, which this CTA has read complete.  The whole warp waits
+  // and decides together.
+  if (!wait_warp(p, &S.zero_bar, static_cast<uint32_t>(rel) & 1u, W_ZERO)) {
+    raise_abort(p);
+    return false;
+  }
   if (lane == 0) {
-    // this CTA's zeroing (generic stores) before its reduction becomes
-    // visible; the other CTAs zeroed this vector before adding their rows of
-    // the previous one, which this CTA has read complete
-    __threadfence();
     fence_proxy_async_global();
     stamp(p, rel, EV_BULK_ISSUED);
     asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u64 [%0], [%1], %2;" ::"l"(
@@ -1207,6 +1228,7 @@ __global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1
     mbar_init(&S.rrow_full, 1);
     mbar_init(&S.rrow_empty, 1);
     mbar_init(&S.topk_bar, 1);
+    mbar_init(&S.zero_bar, 1);
     for (int j = 0; j < 32; ++j) S.rank_word[j] = 0;
     mbar_init(&S.cbar, kNC);
     fence_mbar_init();
