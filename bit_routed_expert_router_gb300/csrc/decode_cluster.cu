@@ -414,16 +414,18 @@ __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
 
 // ------------------------------------------------------------------ producer
 
-// The producer's bounded wait for rank j of layer rel of the top-k (written
-// by the cluster's rank-0 top-k warp); returns the expert, or -1 on abort or
-// timeout.  The tag and the expert share one 32-bit word, so the word alone
-// carries its own readiness (no fence on either side).
+// The producer's bounded wait for rank j of layer rel of the top-k, read
+// from the rank word of the cluster's rank-0 CTA (whose top-k warp picks it);
+// returns the expert, or -1 on abort or timeout.  The tag and the expert share
+// one 32-bit word, so the word alone carries its own readiness (no fence on
+// either side).
 __device__ int wait_rank(const CParams& p, const Smem& S, int rel, int j) {
   const unsigned tag = 64u * static_cast<unsigned>(rel) + static_cast<unsigned>(j) + 1u;
+  const uint32_t src = peer_addr(&S.rank_word[j], 0);
   const long long t0 = clock64();
   for (unsigned it = 0;; ++it) {
     unsigned v;
-    asm volatile("ld.volatile.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(&S.rank_word[j])) : "memory");
+    asm volatile("ld.volatile.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(src) : "memory");
     if ((v >> 8) == tag) return static_cast<int>(v & 0xFFu);
     if (clock64() - t0 > p.spin_limit) {
       note_timeout(p, W_P_TOPK);
@@ -594,16 +596,14 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
       S.topv[j] = static_cast<long long>(hk ^ 0x8000000000000000ull);
       ++head;
     }
-    // rank j is known: lane r < 4 writes it, tagged with the layer and the
-    // rank, into CTA r of the cluster, so the four producers may load its
-    // expert while the warp picks the rest
+    // rank j is known: it goes, tagged with the layer and the rank, into
+    // this CTA's rank word j, which the cluster's four producers read (three
+    // of them through distributed shared memory) to load its expert while the
+    // warp picks the rest
     __syncwarp();
-    if (lane < kCl) {
-      const unsigned word = (seq_base + static_cast<unsigned>(j) + 1u) << 8 | static_cast<unsigned>(ids[j]);
-      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_addr(&S.rank_word[j], static_cast<unsigned>(lane))),
-                   "r"(word)
-                   : "memory");
-    }
+    if (lane == 0)
+      *reinterpret_cast<volatile unsigned*>(&S.rank_word[j]) =
+          (seq_base + static_cast<unsigned>(j) + 1u) << 8 | static_cast<unsigned>(ids[j]);
   }
   float ex = 0.f;
   if (lane < p.k) ex = expf(__ll2float_rn(S.topv[lane] - S.topv[0]) * 9.094947017729282e-13f);   // 2^-40
