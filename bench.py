@@ -238,12 +238,15 @@ def time_k_steps(run_k, stream, clk, min_seconds: float = 1.0, max_reps: int = 4
         e1.record(stream)
         return e0, e1
 
+    # an untimed probe region sizes the repetitions (and keeps a slow first
+    # region, e.g. while the clock sampler's first queries hold the driver,
+    # out of the figure)
+    probe = region(0)
+    probe[1].synchronize()
+    t_probe = probe[0].elapsed_time(probe[1]) / 1e3
+    reps = max(1, min(max_reps, int(math.ceil(min_seconds / max(t_probe, 1e-6)))))
     clk.mark(True)
-    first = region(0)
-    first[1].synchronize()
-    t_first = first[0].elapsed_time(first[1]) / 1e3
-    reps = max(1, min(max_reps, int(math.ceil(min_seconds / max(t_first, 1e-6)))))
-    pairs = [first] + [region(r) for r in range(1, reps)]
+    pairs = [region(r) for r in range(1, reps + 1)]
     pairs[-1][1].synchronize()
     clk.mark(False)
     return sum(a.elapsed_time(b) for a, b in pairs) / 1e3, reps
