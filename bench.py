@@ -910,7 +910,8 @@ def run_ours_pool(args):
     sweeps = {}
     for name, policy, staging in (("lru", moe.MOE_CACHE_LRU, moe.MOE_STAGING_HOST),
                                   ("lfu", moe.MOE_CACHE_LFU, moe.MOE_STAGING_HOST),
-                                  ("lru_device", moe.MOE_CACHE_LRU, moe.MOE_STAGING_DEVICE)):
+                                  ("lru_device", moe.MOE_CACHE_LRU, moe.MOE_STAGING_DEVICE),
+                                  ("lru_fused", moe.MOE_CACHE_LRU, moe.MOE_STAGING_FUSED)):
         sweep = sweeps.setdefault(name, {})
         for n_slots in (8, 16, 32, 64):
             moe.check(moe.moe_set_slots(ctx, n_slots), ctx)
@@ -962,7 +963,8 @@ def run_ours_pool(args):
                    "routing": "router logits + Zipf(1.1)/reuse-0.6 bias trace",
                    "timing": "host wall clock around the synchronised token loop (the host drives the staging)"},
         "sweep_by_slots": sweeps["lru"], "sweep_by_slots_lfu": sweeps["lfu"],
-        "sweep_by_slots_device_staging": sweeps["lru_device"], "file_tier": file_tier,
+        "sweep_by_slots_device_staging": sweeps["lru_device"],
+        "sweep_by_slots_fused": sweeps["lru_fused"], "file_tier": file_tier,
         "chunked_prefill": chunked,
         "roofline": {"bound": "host link", "achieved": best["host_link_gbs"], "peak": link_peak, "unit": "GB/s",
                      "frac": best["host_link_gbs"] / link_peak, "traffic": None,

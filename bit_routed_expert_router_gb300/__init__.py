@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTATE, MOE_ETIMEOUT, MOE_EDOMAIN, MOE_EIO = range(8)
 MOE_RESIDENT_HBM, MOE_HOST_POOL, MOE_FILE_POOL = 0, 1, 2
 MOE_FILE_DIRECT = 1
-MOE_STAGING_HOST, MOE_STAGING_DEVICE = 0, 1
+MOE_STAGING_HOST, MOE_STAGING_DEVICE, MOE_STAGING_FUSED = 0, 1, 2
 MOE_CACHE_LRU, MOE_CACHE_LFU = 0, 1
 MOE_GELU_ERF, MOE_GELU_TANH = 0, 1
 HOOK_FAIL_NEXT_COPY, HOOK_WAIT_LIMIT_US, HOOK_PDL, HOOK_PERSISTENT, HOOK_TIMELINE, HOOK_FREE_BYTES = 1, 2, 3, 4, 5, 6

@@ -119,6 +119,12 @@ struct Smem {
   alignas(8) long long topv[32];                   // top-k logits in rank order
   int last_out;                                    // this CTA is the last to leave the launch
   unsigned rank_word[32];                          // rank j of the top-k: (64 * layer + j + 1) << 8 | expert
+  // host-pool mode: the producer's copy of the layer's plan words, and per
+  // ring slot the stage a consumer warp fills from the mapped pool (a miss)
+  unsigned long long plan_w[32];
+  const uint8_t* fill_src[kNS];                    // host-pool address of the stage's data, or null (copied by TMA)
+  uint8_t* fill_dst[kNS];                          // the same bytes' place in the device slot
+  int fill_stride[kNS];                            // 0: one contiguous tile; else bytes between 576-byte row tiles
 };
 
 static_assert(offsetof(Smem, ring) % 128 == 0 && kSlotBytes % 128 == 0, "TMA targets 128-byte aligned");
@@ -170,7 +176,7 @@ __device__ __forceinline__ bool aborted(const CParams& p);
 // Wait sites, recorded with the CTA in p.diag by the first wait that runs out
 // (the others then see the abort flag and leave without recording).
 enum : unsigned { W_CBAR = 1, W_Y_POLL, W_RROW_EMPTY, W_P_TOPK, W_EMPTY, W_LOGITS, W_CLBAR, W_RROW_FULL, W_A_FULL,
-                  W_DN_TOPK, W_END_TOPK, W_FINISH, W_FULL, W_ZERO };
+                  W_DN_TOPK, W_END_TOPK, W_FINISH, W_FULL, W_ZERO, W_PLAN };
 __device__ __forceinline__ void note_timeout(const CParams& p, unsigned site) {
   atomicOr(p.err, ERR_WAIT_TIMEOUT);
   if (p.diag) atomicCAS(p.diag, 0u, (site << 16) | (blockIdx.x & 0xFFFFu));
@@ -436,6 +442,25 @@ __device__ int wait_rank(const CParams& p, const Smem& S, int rel, int j) {
   }
 }
 
+// Host-pool mode: the producer's bounded wait for layer l's plan word of rank
+// j (published by cluster 0 after its slot-cache step; the launch's tag in the
+// high half carries its readiness).  Returns the word, or 0 on abort or timeout.
+__device__ unsigned long long wait_plan(const CParams& p, int l, int j) {
+  const unsigned long long* src = p.plan + static_cast<size_t>(l) * 32 + j;
+  const long long t0 = clock64();
+  for (unsigned it = 0;; ++it) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(src) : "memory");
+    if (static_cast<unsigned>(w >> 32) == p.tag) return w;
+    if (clock64() - t0 > p.spin_limit) {
+      note_timeout(p, W_PLAN);
+      return 0ull;
+    }
+    if ((it & 15) == 15 && aborted(p)) return 0ull;
+    __nanosleep(64);
+  }
+}
+
 __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
   const int n_rel = p.l1 - p.l0;
   const uint32_t tile_bytes = static_cast<uint32_t>(p.d / 64) * kGroupBytes;   // gate/up tile = down slice
@@ -462,6 +487,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
       rrow_last = rel;
     }
     int s = 0;
+    unsigned plan_known = 0;   // host pool: ranks whose plan word this layer has been read
     for (int i = 0; i < S.n_tasks; ++i) {
       const CTask t = S.tasks[i];
       if (t.kind == K_TOPK) continue;
@@ -472,6 +498,24 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
         stop = true;
         break;
       }
+      // host pool: where the expert is (a slot, filled by this step if a miss)
+      int se = e;
+      bool miss = false;
+      if (p.pool && t.src >= 0) {
+        if (!(plan_known & (1u << t.src))) {
+          const unsigned long long w = wait_plan(p, p.l0 + rel, t.src);
+          if (w == 0ull) {
+            raise_abort(p);
+            stop = true;
+            break;
+          }
+          S.plan_w[t.src] = w;
+          plan_known |= 1u << t.src;
+        }
+        const unsigned long long w = S.plan_w[t.src];
+        se = static_cast<int>((w >> 16) & 0xFFFFu);
+        miss = ((w >> 8) & 1u) == 0u;
+      }
       const uint32_t u = static_cast<uint32_t>(rel) * S.n_stages + s++;
       const int slot = u % kNS;
       if (!wait_one(p, &S.empty[slot], ((u / kNS) & 1u) ^ 1u, W_EMPTY)) {
@@ -479,15 +523,37 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
         stop = true;
         break;
       }
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&S.full[slot], tile_bytes);
-      if (t.kind == K_GU) {
-        const uint8_t* base = t.src < 0 ? Lsh : Lex + static_cast<long long>(e) * p.expert_stride;
-        const size_t tile = static_cast<size_t>(8 * t.G + 2 * static_cast<int>(rank) + t.tt);
-        bulk_g2s(S.ring[slot], base + tile * tile_bytes, tile_bytes, &S.full[slot]);
+      if (miss) {
+        // the consumers copy this stage from the mapped pool into the ring and
+        // into the slot (plain loads: no bulk copy reads host memory)
+        const long long gu_r = static_cast<long long>(p.f / 8) * R * kGroupBytes;
+        const uint8_t* src = L->pool + static_cast<long long>(e) * p.expert_stride;
+        uint8_t* dst = const_cast<uint8_t*>(Lex) + static_cast<long long>(se) * p.expert_stride;
+        long long off;
+        int fstride;
+        if (t.kind == K_GU) {
+          off = static_cast<long long>(8 * t.G + 2 * static_cast<int>(rank) + t.tt) * tile_bytes;
+          fstride = 0;
+        } else {
+          off = gu_r + (static_cast<long long>(R) * rank * (p.f / 64) + t.G) * kGroupBytes;
+          fstride = (p.f / 64) * kGroupBytes;
+        }
+        S.fill_src[slot] = src + off;
+        S.fill_dst[slot] = dst + off;
+        S.fill_stride[slot] = fstride;
+        mbarrier_arrive(&S.full[slot]);
       } else {
-        tma_load_3d(S.ring[slot], t.src < 0 ? &L->dn_shared : &L->dn_routed, t.G * (kGroupBytes / 4),
-                    R * static_cast<int>(rank), e, &S.full[slot]);
+        if (p.pool) S.fill_src[slot] = nullptr;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&S.full[slot], tile_bytes);
+        if (t.kind == K_GU) {
+          const uint8_t* base = t.src < 0 ? Lsh : Lex + static_cast<long long>(se) * p.expert_stride;
+          const size_t tile = static_cast<size_t>(8 * t.G + 2 * static_cast<int>(rank) + t.tt);
+          bulk_g2s(S.ring[slot], base + tile * tile_bytes, tile_bytes, &S.full[slot]);
+        } else {
+          tma_load_3d(S.ring[slot], t.src < 0 ? &L->dn_shared : &L->dn_routed, t.G * (kGroupBytes / 4),
+                      R * static_cast<int>(rank), se, &S.full[slot]);
+        }
       }
       u_issued = u + 1;
       if (t.src >= 0) stamp(p, rel, EV_ROUTED_ISSUE);
@@ -621,6 +687,126 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
   return true;
 }
 
+// Host-pool mode, cluster 0's top-k warp: the layer's slot-cache step for
+// the token (the same rules as the per-layer kernels: hits refresh their
+// slot's last use; misses, in top-k order, take among the slots this step has
+// not touched the smallest (last use, slot) under LRU, or (use count of the
+// slot's expert, last use, slot) under LFU, an empty slot counting -1), then
+// the trace record for the host, the counters, and one plan word per rank
+// for every producer of the grid.
+__device__ void pool_step(const CParams& p, Smem& S, int rel) {
+  const int lane = threadIdx.x & 31, k = p.k, N = p.n_slots, l = p.l0 + rel;
+  const CLayer* L = p.layers + l;
+  const long long t = S.args.step;
+  const bool lfu = p.policy == 1;
+  const int32_t* ids = S.ids[rel & 1];
+  int eos[8];
+  long long lu[8], uc[8];
+  unsigned used = 0, hits = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int sl = lane + 32 * i;
+    eos[i] = sl < N ? __ldcg(&L->expert_of_slot[sl]) : -1;
+    lu[i] = sl < N ? __ldcg(&L->last_use[sl]) : LLONG_MAX;
+    uc[i] = (!lfu || sl >= N) ? 0 : (eos[i] >= 0 ? __ldcg(&L->use_count[eos[i]]) : -1);
+    if (sl >= N) used |= 1u << i;
+  }
+  for (int j = 0; j < k; ++j) {
+    const int sl = __ldcg(&L->slot_of_expert[ids[j]]);
+    if (sl >= 0) {
+      hits |= 1u << j;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (lane + 32 * i == sl) {
+          used |= 1u << i;
+          lu[i] = t;
+        }
+    }
+  }
+  int32_t* rec = p.host_rec + static_cast<size_t>(rel) * (1 + 6 * k);
+  int n_miss = 0;
+  for (int j = 0; j < k; ++j) {
+    const int ej = ids[j];
+    int slot, ev = -1;
+    if (hits & (1u << j)) {
+      slot = __ldcg(&L->slot_of_expert[ej]);
+    } else {
+      long long bc = LLONG_MAX, bv = LLONG_MAX;
+      int bs = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int sl = lane + 32 * i;
+        const bool better = uc[i] < bc || (uc[i] == bc && (lu[i] < bv || (lu[i] == bv && sl < bs)));
+        if (!(used & (1u << i)) && better) {
+          bc = uc[i];
+          bv = lu[i];
+          bs = sl;
+        }
+      }
+#pragma unroll
+      for (int m = 16; m; m >>= 1) {
+        const long long oc = shfl_xor_i64(bc, m);
+        const long long ov = shfl_xor_i64(bv, m);
+        const int os = __shfl_xor_sync(kFull, bs, m);
+        if (oc < bc || (oc == bc && (ov < bv || (ov == bv && os < bs)))) {
+          bc = oc;
+          bv = ov;
+          bs = os;
+        }
+      }
+      slot = bs;
+      int my_ev = -1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (lane + 32 * i == bs) {
+          my_ev = eos[i];
+          eos[i] = ej;
+          lu[i] = t;
+          used |= 1u << i;
+        }
+      ev = __shfl_sync(kFull, my_ev, bs & 31);
+      if (lane == 0) {
+        if (ev >= 0) L->slot_of_expert[ev] = -1;
+        L->slot_of_expert[ej] = bs;
+        rec[1 + 2 * n_miss] = ej;
+        rec[2 + 2 * n_miss] = bs;
+      }
+      ++n_miss;
+    }
+    if (lane == 0) {
+      int32_t* tr = rec + 1 + 2 * k + 4 * j;
+      tr[0] = ej;
+      tr[1] = (hits >> j) & 1u;
+      tr[2] = slot;
+      tr[3] = ev;
+      // every producer of the grid reads where rank j's expert is
+      const unsigned long long w = static_cast<unsigned long long>(p.tag) << 32 |
+                                   static_cast<unsigned long long>(slot) << 16 |
+                                   static_cast<unsigned long long>((hits >> j) & 1u) << 8 |
+                                   static_cast<unsigned long long>(ej);
+      asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.plan + static_cast<size_t>(l) * 32 + j), "l"(w)
+                   : "memory");
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int sl = lane + 32 * i;
+    if (sl < N) {
+      L->expert_of_slot[sl] = eos[i];
+      L->last_use[sl] = lu[i];
+    }
+  }
+  if (lane == 0) {
+    if (lfu)
+      for (int j = 0; j < k; ++j) L->use_count[ids[j]] += 1;
+    rec[0] = n_miss;
+    p.lru_counts[2 * l + 0] += k - n_miss;
+    p.lru_counts[2 * l + 1] += n_miss;
+  }
+  __syncwarp();
+}
+
 // Rank 0 of each cluster picks the cluster's top-k for its four CTAs (one
 // poller per cluster, and the four see the same ranks at the same time).
 // Then, in every CTA, the warp zeroes the CTA's share of the vector layer
@@ -639,6 +825,7 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
       const bool ok = p.E <= 128 ? topk_layer<4>(p, S, p.l0 + rel, sid, sg, base)
                                  : topk_layer<8>(p, S, p.l0 + rel, sid, sg, base);
       if (!ok) return;
+      if (p.pool && blockIdx.x == 0) pool_step(p, S, rel);
       if (lane == 0) stamp(p, rel, EV_TOPK_DONE);
       if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
         const DevCallArgs* A = &S.args;
@@ -962,6 +1149,64 @@ __device__ void gu_push(const CParams& p, Smem& S, int rel, const CTask& t, unsi
   if (lane == 0) stamp(p, rel, EV_PUSH_LAST, true);
 }
 
+// Host-pool miss: warp qw copies the part of the stage it will multiply (its
+// groups of a gate/up tile, or its row tiles of a down slice) from the mapped
+// pool into the ring slot and into the expert's device slot, eight 16-byte
+// loads in flight per lane.
+__device__ void fill_stage(const CParams& p, Smem& S, int slot, const CTask& t, int qw) {
+  const int lane = threadIdx.x & 31;
+  const uint8_t* src = S.fill_src[slot];
+  uint8_t* dst = S.fill_dst[slot];
+  const int fs = S.fill_stride[slot];
+  uint8_t* ring = S.ring[slot];
+  const int nGd = p.d / 64;
+  constexpr int kPer = kGroupBytes / 16;   // 16-byte pieces per 576-byte block
+  int n16, g0 = 0;
+  if (t.kind == K_GU) {
+    const int cgu = (nGd + kQW - 1) / kQW;
+    g0 = qw * cgu;
+    n16 = max(0, min(nGd, g0 + cgu) - g0) * kPer;
+  } else {
+    n16 = (qw < nGd ? (nGd - qw + kQW - 1) / kQW : 0) * kPer;
+  }
+  // byte offset of piece i in the pool / slot, and in the ring
+  auto offs = [&](int i, long long& go, int& ro) {
+    if (t.kind == K_GU) {
+      ro = g0 * kGroupBytes + 16 * i;
+      go = ro;
+    } else {
+      const int T = qw + kQW * (i / kPer), o = 16 * (i % kPer);
+      ro = T * kGroupBytes + o;
+      go = static_cast<long long>(T) * fs + o;
+    }
+  };
+  for (int i0 = 0; i0 < n16; i0 += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 32 * u + lane;
+      if (i < n16) {
+        long long go;
+        int ro;
+        offs(i, go, ro);
+        v[u] = *reinterpret_cast<const uint4*>(src + go);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 32 * u + lane;
+      if (i < n16) {
+        long long go;
+        int ro;
+        offs(i, go, ro);
+        *reinterpret_cast<uint4*>(ring + ro) = v[u];
+        *reinterpret_cast<uint4*>(dst + go) = v[u];
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // Gate/up stage: warp qw of the quad takes groups [qw * cgu, (qw + 1) * cgu);
 // the last warp of the quad to finish sums the four partials in warp order and
 // pushes a.
@@ -1181,6 +1426,7 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
         acc(p, rel, t.src < 0 ? 6 : 3, t1 - t0);
       }
       unsigned long long ta = t1;
+      if (p.pool && S.fill_src[slot]) fill_stage(p, S, slot, t, qw);
       if (t.kind == K_GU) {
         stage_gu(p, S, qw, rel, slot, t, rank);
       } else if (!stage_dn(p, S, quad, qw, rel, slot, t, &ta)) {

@@ -73,10 +73,17 @@ constexpr int kCThreads = 32 * 18;     // producer warp, 16 consumer warps, top-
 
 struct CLayer {                        // one layer, device memory (the tensor maps keep it 64-byte aligned)
   CUtensorMap dn_shared;               // shared expert's down region as u32 [1][d/16][f_s/64 * 144], box 144 x d/64
-  CUtensorMap dn_routed;               // the experts' down regions as u32 [E][d/16][f/64 * 144], same box
+  CUtensorMap dn_routed;               // resident: the experts' down regions as u32 [E][d/16][f/64 * 144], same
+                                       // box; host pool: the slots' down regions, [N][d/16][f/64 * 144]
   const uint16_t* router_w;            // fp16 [E][d]
   const uint8_t* shared;               // shared expert, device layout (gate/up region first)
-  const uint8_t* experts;              // expert 0, device layout
+  const uint8_t* experts;              // resident: expert 0, device layout; host pool: slot 0
+  // host pool only (null otherwise): the layer's slot cache and its pinned pool
+  const uint8_t* pool;                 // expert 0 of the layer in the mapped host pool, device layout
+  int32_t* slot_of_expert;             // [E], -1 = not held
+  int32_t* expert_of_slot;             // [N], -1 = empty
+  long long* last_use;                 // [N], step of the slot's last use (-1: empty)
+  long long* use_count;                // [E], picks over the run (LFU)
 };
 
 struct CParams {
@@ -90,6 +97,13 @@ struct CParams {
   unsigned tag;                        // this launch's tag (never 0)
   long long spin_limit;                // bounded waits give up after this many cycles
   unsigned* diag;                      // first wait that ran out: site << 16 | CTA (0: none)
+  // host-pool mode (pool != 0): cluster 0 runs the slot-cache step and publishes
+  // each rank's (slot, hit) in plan; misses are read from the mapped pool
+  int pool, n_slots, policy;
+  unsigned long long* plan;            // [n_layers][32]: tag << 32 | slot << 16 | hit << 8 | expert
+  int32_t* host_rec;                   // mapped [n_rel][1 + 6k]: misses (expert, slot), then per rank
+                                       // (expert, hit, slot, evicted)
+  long long* lru_counts;               // [n_layers][2]: hits, misses
   long long* ybuf;                     // [3][d] layer outputs: sum over CTAs of (v << 8) + 1, v on the 2^-32 grid;
                                        // zero between launches
   unsigned* exit_cnt;

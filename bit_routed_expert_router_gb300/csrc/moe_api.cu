@@ -76,6 +76,7 @@ struct moe_ctx {
   uint8_t* pool = nullptr;
   const uint8_t* pool_dev = nullptr;     // the pool's device address (mapped), or null
   bool stage_device = false;             // moe_set_staging(MOE_STAGING_DEVICE)
+  bool stage_fused = false;              // moe_set_staging(MOE_STAGING_FUSED): the clustered kernel does it all
   size_t pool_bytes = 0;
   // expert file tier (MOE_FILE_POOL contexts)
   int file_fd = -1;
@@ -169,6 +170,7 @@ struct moe_ctx {
   bool use_cluster = true;             // test hook 9
   int c_grid = 0;                      // CTAs: resident clusters x kCCluster
   CLayer* c_layers = nullptr;          // device [n_layers]
+  unsigned long long* c_plan = nullptr;  // device [n_layers][32]: host-pool plan words of the clustered kernel
   unsigned long long* c_tlog = nullptr;  // [n_layers][n_cl][E][2] tagged logits, one replica per cluster
   long long spin_limit = 4000000000LL; // test hook 10: wait limit (cycles) of the clustered kernel's bounded waits
   long long* c_ybuf = nullptr;         // [3][d] fixed-point layer outputs
@@ -499,6 +501,32 @@ int cluster_units_max(const moe_config& c, int n_cl) {
   return m;
 }
 
+// The clustered kernel's view of a host-pool layer: its slots in place of
+// the resident experts (down tensor map over the N slots), the mapped pool and
+// the slot-cache state.  Built once the layer and its slots both exist.
+moe_status cluster_pool_layer(moe_ctx* ctx, int l) {
+  const moe_config& c = ctx->cfg;
+  LayerStore& Ls = ctx->L[static_cast<size_t>(l)];
+  if (!ctx->c_ok || !ctx->pool_dev || ctx->residency != MOE_HOST_POOL || !Ls.ready || !Ls.slots || ctx->n_slots < 1)
+    return MOE_OK;
+  CLayer cl{};
+  const size_t gu_s = static_cast<size_t>(c.f_shared / 8) * (c.d / 64) * kGroupBytes;
+  const size_t gu_r = static_cast<size_t>(c.f / 8) * (c.d / 64) * kGroupBytes;
+  if (!encode_down(&cl.dn_shared, Ls.shared + gu_s, c.f_shared / 64, c.d / 16, 1, 0) ||
+      !encode_down(&cl.dn_routed, Ls.slots + gu_r, c.f / 64, c.d / 16, ctx->n_slots, ctx->stride))
+    return fail(ctx, MOE_ECUDA, "layer %d: cuTensorMapEncodeTiled failed for the slots' down regions", l);
+  cl.router_w = Ls.router_w;
+  cl.shared = Ls.shared;
+  cl.experts = Ls.slots;
+  cl.pool = ctx->pool_dev + static_cast<size_t>(l) * c.n_experts * ctx->stride;
+  cl.slot_of_expert = Ls.slot_of_expert;
+  cl.expert_of_slot = Ls.expert_of_slot;
+  cl.last_use = Ls.last_use;
+  cl.use_count = Ls.use_count;
+  CK(cudaMemcpy(ctx->c_layers + l, &cl, sizeof(CLayer), cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
 // Resident decode of one token through [l0, l1) with the clustered kernel.
 moe_status cluster_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   const moe_config& c = ctx->cfg;
@@ -519,7 +547,16 @@ moe_status cluster_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s) {
   if (++ctx->c_tag == 0) {   // tags wrapped: no stale entry may carry the new one
     CK(cudaMemsetAsync(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * (ctx->c_grid / kCCluster) * c.n_experts * 16,
                        s));
+    CK(cudaMemsetAsync(ctx->c_plan, 0, static_cast<size_t>(c.n_layers) * 32 * 8, s));
     ctx->c_tag = 1;
+  }
+  if (ctx->residency == MOE_HOST_POOL && ctx->stage_fused) {
+    p.pool = 1;
+    p.n_slots = ctx->n_slots;
+    p.policy = ctx->policy;
+    p.plan = ctx->c_plan;
+    p.host_rec = ctx->host_rec_dev;
+    p.lru_counts = ctx->lru_counts;
   }
   p.tlog = ctx->c_tlog;
   p.tag = ctx->c_tag;
@@ -765,6 +802,36 @@ moe_status pool_run(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec*
 // reads the router's miss record and copies the missed experts from the
 // mapped host pool into their slots; the host enqueues every layer without
 // waiting and fills the trace, if asked for, once the step is done.
+// The trace records the device wrote into the mapped host record (device
+// staging and the fused step), once the step has finished.
+moe_status device_trace(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec* trace, int trace_cap,
+                        int* trace_len) {
+  const int k = ctx->cfg.top_k, n_rel = l1 - l0;
+  int n_rec = 0;
+  if (trace) {
+    CK(cudaEventRecord(ctx->ev_route, s));
+    moe_status st = wait_event(ctx, ctx->ev_route, "decode step (trace)");
+    if (st != MOE_OK) return st;
+    for (int rel = 0; rel < n_rel; ++rel) {
+      const volatile int32_t* rec = ctx->host_rec + static_cast<size_t>(rel) * (1 + 6 * k);
+      for (int j = 0; j < k && n_rec < trace_cap; ++j) {
+        const volatile int32_t* tr = rec + 1 + 2 * k + 4 * j;
+        moe_trace_rec r;
+        r.token = static_cast<int32_t>(ctx->step);
+        r.layer = l0 + rel;
+        r.k_pos = j;
+        r.expert = tr[0];
+        r.hit = tr[1];
+        r.slot = tr[2];
+        r.evicted = tr[3];
+        trace[n_rec++] = r;
+      }
+    }
+  }
+  if (trace_len) *trace_len = n_rec;
+  return MOE_OK;
+}
+
 moe_status pool_run_device(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec* trace, int trace_cap,
                            int* trace_len) {
   const int k = ctx->cfg.top_k, E = ctx->cfg.n_experts;
@@ -789,29 +856,17 @@ moe_status pool_run_device(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_tra
     p.pass = -1;
     CK(launch_down(p, 1, dn_max_items(ctx, 1), ctx->n_sm, s, false));
   }
-  int n_rec = 0;
-  if (trace) {
-    CK(cudaEventRecord(ctx->ev_route, s));
-    moe_status st = wait_event(ctx, ctx->ev_route, "decode step (trace)");
-    if (st != MOE_OK) return st;
-    for (int rel = 0; rel < n_rel; ++rel) {
-      const volatile int32_t* rec = ctx->host_rec + static_cast<size_t>(rel) * (1 + 6 * k);
-      for (int j = 0; j < k && n_rec < trace_cap; ++j) {
-        const volatile int32_t* tr = rec + 1 + 2 * k + 4 * j;
-        moe_trace_rec r;
-        r.token = static_cast<int32_t>(ctx->step);
-        r.layer = l0 + rel;
-        r.k_pos = j;
-        r.expert = tr[0];
-        r.hit = tr[1];
-        r.slot = tr[2];
-        r.evicted = tr[3];
-        trace[n_rec++] = r;
-      }
-    }
-  }
-  if (trace_len) *trace_len = n_rec;
-  return MOE_OK;
+  return device_trace(ctx, l0, l1, s, trace, trace_cap, trace_len);
+}
+
+// Host-pool step in one launch of the clustered kernel: router, slot-cache
+// step (in cluster 0), hits from the slots and misses read from the mapped
+// pool by the consumers, which also fill the slots.
+moe_status pool_run_fused(moe_ctx* ctx, int l0, int l1, cudaStream_t s, moe_trace_rec* trace, int trace_cap,
+                          int* trace_len) {
+  const moe_status st = cluster_run(ctx, l0, l1, s);
+  if (st != MOE_OK) return st;
+  return device_trace(ctx, l0, l1, s, trace, trace_cap, trace_len);
 }
 
 }  // namespace
@@ -998,6 +1053,9 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       // the tagged logits, one replica per cluster of every layer
       ctx->c_tlog = dalloc<unsigned long long>(static_cast<size_t>(c.n_layers) * n_cl * c.n_experts * 2, o, nb);
       if (!ctx->c_tlog) return bail(MOE_ENOMEM);
+      ctx->c_plan = dalloc<unsigned long long>(static_cast<size_t>(c.n_layers) * 32, o, nb);
+      if (!ctx->c_plan) return bail(MOE_ENOMEM);
+      if (cudaMemset(ctx->c_plan, 0, static_cast<size_t>(c.n_layers) * 32 * 8) != cudaSuccess) return bail(MOE_ECUDA);
       if (cudaMemset(ctx->c_tlog, 0, static_cast<size_t>(c.n_layers) * n_cl * c.n_experts * 16) != cudaSuccess)
         return bail(MOE_ECUDA);
       ctx->c_ok = true;
@@ -1192,6 +1250,7 @@ moe_status moe_init_layer(moe_ctx* ctx, int layer, const uint16_t* router_w, con
     CK(cudaMemcpy(ctx->c_layers + layer, &cl, sizeof(CLayer), cudaMemcpyHostToDevice));
   }
   Ls.ready = true;
+  if (pool) return cluster_pool_layer(ctx, layer);
   return MOE_OK;
 }
 
@@ -1232,6 +1291,10 @@ moe_status moe_set_slots(moe_ctx* ctx, int n_slots) {
     if (!Ls.use_count) CK(cudaMalloc(&Ls.use_count, static_cast<size_t>(c.n_experts) * 8));
   }
   ctx->n_slots = n_slots;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const moe_status st = cluster_pool_layer(ctx, l);
+    if (st != MOE_OK) return st;
+  }
   return moe_reset_cache(ctx);
 }
 
@@ -1302,13 +1365,17 @@ moe_status moe_set_expert_file(moe_ctx* ctx, const char* path, int n_threads, ui
 moe_status moe_set_staging(moe_ctx* ctx, int mode) {
   if (!ctx) return MOE_EINVAL;
   if (ctx->poisoned) return fail(ctx, MOE_ESTATE, "context is poisoned: %s", ctx->err.c_str());
-  if (mode != MOE_STAGING_HOST && mode != MOE_STAGING_DEVICE) return fail(ctx, MOE_EINVAL, "unknown staging mode %d", mode);
+  if (mode != MOE_STAGING_HOST && mode != MOE_STAGING_DEVICE && mode != MOE_STAGING_FUSED)
+    return fail(ctx, MOE_EINVAL, "unknown staging mode %d", mode);
   if (ctx->residency != MOE_HOST_POOL) return fail(ctx, MOE_ESTATE, "staging modes apply to host-pool contexts");
-  if (mode == MOE_STAGING_DEVICE && !ctx->pool_dev)
+  if (mode != MOE_STAGING_HOST && !ctx->pool_dev)
     return fail(ctx, MOE_ESTATE, "the host pool is not mapped into the device address space");
+  if (mode == MOE_STAGING_FUSED && !ctx->c_ok)
+    return fail(ctx, MOE_ESTATE, "the clustered decode kernel is unavailable for this configuration or device");
   CK(cudaSetDevice(ctx->device));
   CK(cudaDeviceSynchronize());
   ctx->stage_device = mode == MOE_STAGING_DEVICE;
+  ctx->stage_fused = mode == MOE_STAGING_FUSED;
   return moe_reset_cache(ctx);
 }
 
@@ -1385,8 +1452,9 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
   st = put_args(ctx, make_args(ctx, h_in, h_out, y_last, logit_bias, B, B, 0), s);
   if (st != MOE_OK) return st;
   if (pool) {
-    st = ctx->stage_device ? pool_run_device(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len)
-                           : pool_run(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len);
+    st = ctx->stage_fused    ? pool_run_fused(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len)
+         : ctx->stage_device ? pool_run_device(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len)
+                             : pool_run(ctx, layer_begin, layer_end, s, trace, trace_cap, trace_len);
     ++ctx->step;
     ++ctx->steps;
     return st;
@@ -1836,7 +1904,7 @@ moe_status moe_get_stats(moe_ctx* ctx, moe_stats* out) {
   out->n_slots = ctx->n_slots;
   out->expert_bytes = ctx->expert_bytes;
   // device-driven staging copies every miss once (the mode switch zeroed the counters)
-  if (ctx->stage_device) out->staged_bytes += out->misses * ctx->expert_bytes;
+  if (ctx->stage_device || ctx->stage_fused) out->staged_bytes += out->misses * ctx->expert_bytes;
   out->shared_bytes = ctx->shared_bytes;
   size_t dev = ctx->device_bytes;
   for (auto& Ls : ctx->L) {

@@ -69,7 +69,7 @@ typedef enum {
 
 enum { MOE_RESIDENT_HBM = 0, MOE_HOST_POOL = 1, MOE_FILE_POOL = 2 };
 enum { MOE_FILE_DIRECT = 1 };   /* moe_set_expert_file flag: read misses with O_DIRECT */
-enum { MOE_STAGING_HOST = 0, MOE_STAGING_DEVICE = 1 };   /* moe_set_staging modes */
+enum { MOE_STAGING_HOST = 0, MOE_STAGING_DEVICE = 1, MOE_STAGING_FUSED = 2 };   /* moe_set_staging modes */
 enum { MOE_CACHE_LRU = 0, MOE_CACHE_LFU = 1 };
 enum { MOE_GELU_ERF = 0, MOE_GELU_TANH = 1 };
 
@@ -329,10 +329,21 @@ moe_status moe_set_expert_file(moe_ctx *ctx, const char *path, int n_threads, ui
  * missed experts from the pinned pool (mapped into the device address space,
  * read through the host link) into their slots, so moe_decode_step enqueues
  * all layers and returns at once (after the step completes when a trace is
- * asked for, to fill it).  Both modes give the same cache decisions, traces
- * and outputs.  Empties the cache as moe_reset_cache.  Errors: MOE_EINVAL
- * (unknown mode), MOE_ESTATE (not a host-pool context, or a pool the device
- * cannot address). */
+ * asked for, to fill it).  MOE_STAGING_FUSED: the whole step is one launch
+ * of the clustered decode kernel (the write-up's section "MoE needed parallel
+ * work, reuse, and coarse overlap": persistent workers, the cache first, the
+ * shared expert overlapped with the reads): every layer's router and top-k,
+ * the slot-cache step (run once, in cluster 0, which publishes each rank's
+ * slot and hit to every CTA), hits loaded from their slots, and misses read
+ * by the consumer warps from the mapped pool straight into their stage
+ * buffers and written into the slots on the way.  Needs the clustered kernel
+ * (B = 1, d <= 2816, its shape limits) and returns once the step is enqueued
+ * (after it completes when a trace is asked for).  All three modes give the
+ * same cache decisions and traces; HOST and DEVICE run the per-layer kernels,
+ * FUSED the clustered kernel, whose outputs equal a resident context's
+ * clustered kernel bit for bit.  Empties the cache as moe_reset_cache.
+ * Errors: MOE_EINVAL (unknown mode), MOE_ESTATE (not a host-pool context, a
+ * pool the device cannot address, or FUSED without the clustered kernel). */
 moe_status moe_set_staging(moe_ctx *ctx, int mode);
 
 /* Two-tier cache (expert file -> pinned host records -> HBM slots): keeps

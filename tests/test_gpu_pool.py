@@ -471,7 +471,7 @@ def test_device_staging_without_trace_and_errors(tmp_path):
     w = to_device(gen_layer(sh, seed=155, layer=0))
     H = gen_hidden(4, sh.d, seed=155).cuda()
     with _pool_ctx(sh, 1, 2, [w]) as ctx:
-        assert moe.moe_set_staging(ctx.h, 2) == moe.MOE_EINVAL
+        assert moe.moe_set_staging(ctx.h, 3) == moe.MOE_EINVAL
         moe.check(moe.moe_set_staging(ctx.h, moe.MOE_STAGING_DEVICE), ctx.h)
         ys = [ctx.decode(H[t:t + 1], 0, 1)[1].clone() for t in range(4)]   # no trace: returns at once
         ctx.sync()
