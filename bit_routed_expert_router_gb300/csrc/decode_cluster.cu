@@ -461,6 +461,7 @@ __device__ unsigned long long wait_plan(const CParams& p, int l, int j) {
   }
 }
 
+template <bool kPool>
 __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
   const int n_rel = p.l1 - p.l0;
   const uint32_t tile_bytes = static_cast<uint32_t>(p.d / 64) * kGroupBytes;   // gate/up tile = down slice
@@ -501,7 +502,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
       // host pool: where the expert is (a slot, filled by this step if a miss)
       int se = e;
       bool miss = false;
-      if (p.pool && t.src >= 0) {
+      if (kPool && t.src >= 0) {
         if (!(plan_known & (1u << t.src))) {
           const unsigned long long w = wait_plan(p, p.l0 + rel, t.src);
           if (w == 0ull) {
@@ -543,7 +544,7 @@ __device__ void producer(const CParams& p, Smem& S, unsigned rank) {
         S.fill_stride[slot] = fstride;
         mbarrier_arrive(&S.full[slot]);
       } else {
-        if (p.pool) S.fill_src[slot] = nullptr;
+        if (kPool) S.fill_src[slot] = nullptr;
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&S.full[slot], tile_bytes);
         if (t.kind == K_GU) {
@@ -814,6 +815,7 @@ __device__ void pool_step(const CParams& p, Smem& S, int rel) {
 // previous layer's input step, the last reader of that vector.  The fence
 // that makes the zeros visible before this CTA's next reduction runs here,
 // off the layer's critical path; the zero barrier hands it to the reduction.
+template <bool kPool>
 __device__ void topk_warp(const CParams& p, Smem& S) {
   const int lane = threadIdx.x & 31;
   const int n_rel = p.l1 - p.l0, d = p.d;
@@ -825,7 +827,7 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
       const bool ok = p.E <= 128 ? topk_layer<4>(p, S, p.l0 + rel, sid, sg, base)
                                  : topk_layer<8>(p, S, p.l0 + rel, sid, sg, base);
       if (!ok) return;
-      if (p.pool && blockIdx.x == 0) pool_step(p, S, rel);
+      if (kPool && blockIdx.x == 0) pool_step(p, S, rel);
       if (lane == 0) stamp(p, rel, EV_TOPK_DONE);
       if (blockIdx.x == 0 && lane < p.k && rel < S.args.dbg_layers) {
         const DevCallArgs* A = &S.args;
@@ -1395,6 +1397,7 @@ __device__ void finish(const CParams& p, Smem& S, int cw, int rel, unsigned rank
     *reinterpret_cast<longlong2*>(p.ybuf + static_cast<size_t>((rel - 1) % 3) * d + e) = make_longlong2(0, 0);
 }
 
+template <bool kPool>
 __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
   const int lane = threadIdx.x & 31;
   const int quad = cw / kQW, qw = cw % kQW;
@@ -1426,7 +1429,7 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
         acc(p, rel, t.src < 0 ? 6 : 3, t1 - t0);
       }
       unsigned long long ta = t1;
-      if (p.pool && S.fill_src[slot]) fill_stage(p, S, slot, t, qw);
+      if (kPool && S.fill_src[slot]) fill_stage(p, S, slot, t, qw);
       if (t.kind == K_GU) {
         stage_gu(p, S, qw, rel, slot, t, rank);
       } else if (!stage_dn(p, S, quad, qw, rel, slot, t, &ta)) {
@@ -1451,6 +1454,7 @@ __device__ void consumer(const CParams& p, Smem& S, int cw, unsigned rank) {
 // registers, so a thread may hold at most 96 (launch bounds give exactly that).
 // The cluster shape is a property of the kernel (not only of the launch), so
 // every launch path, a profiler's replay included, runs it in 4-CTA clusters.
+template <bool kPool>
 __global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1) k_decode_cluster(CParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -1488,11 +1492,11 @@ __global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1
   cluster_sync_all();   // every CTA's barriers exist before any remote arrival
   if (!aborted(p)) {
     if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) producer(p, S, rank);
+      if ((threadIdx.x & 31) == 0) producer<kPool>(p, S, rank);
     } else if (warp <= kNC) {
-      consumer(p, S, warp - 1, rank);
+      consumer<kPool>(p, S, warp - 1, rank);
     } else {
-      topk_warp(p, S);
+      topk_warp<kPool>(p, S);
     }
   }
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // this thread's bulk reductions are done
@@ -1525,7 +1529,10 @@ size_t cluster_smem() { return sizeof(Smem); }
 int cluster_max_units() { return kMaxU; }
 
 cudaError_t cluster_attrs() {
-  return cudaFuncSetAttribute((const void*)k_decode_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e = cudaFuncSetAttribute((const void*)k_decode_cluster<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(Smem)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute((const void*)k_decode_cluster<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(sizeof(Smem)));
 }
 
@@ -1535,7 +1542,7 @@ cudaError_t cluster_max_active(int* n_clusters) {
   cfg.gridDim = dim3(kCCluster);
   cfg.blockDim = dim3(kCThreads);
   cfg.dynamicSmemBytes = sizeof(Smem);
-  return cudaOccupancyMaxActiveClusters(n_clusters, (const void*)k_decode_cluster, &cfg);
+  return cudaOccupancyMaxActiveClusters(n_clusters, (const void*)k_decode_cluster<false>, &cfg);
 }
 
 cudaError_t launch_cluster(CParams& p, int grid, cudaStream_t s) {
@@ -1549,7 +1556,9 @@ cudaError_t launch_cluster(CParams& p, int grid, cudaStream_t s) {
   at[0].val.cooperative = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode_cluster, p);
+  // two instances: the resident one carries none of the host-pool code
+  return p.pool ? cudaLaunchKernelEx(&cfg, k_decode_cluster<true>, p)
+                : cudaLaunchKernelEx(&cfg, k_decode_cluster<false>, p);
 }
 
 }  // namespace moe
