@@ -129,7 +129,8 @@ cudaError_t cluster_max_active(int* n_clusters);
 cudaError_t launch_cluster(CParams& p, int grid, cudaStream_t s);
 
 // Prefill (tcgen05 grouped GEMM over int4 weights).
-constexpr int kPfTileN = 128;          // token rows per GEMM tile (large groups)
+constexpr int kPfTileNBig = 256;       // token rows per GEMM tile (groups of about 200 rows and more)
+constexpr int kPfTileN = 128;          // token rows per GEMM tile (mid-sized groups)
 constexpr int kPfTileNSmall = 32;      // token rows per GEMM tile when every expert has only a few rows
 constexpr int kPfMinDecodeB = 16;     // resident decode steps of at least this many tokens take the tcgen05 path
 constexpr int kPfGraphMaxT = 512;     // tcgen05-path calls of at most this many tokens replay a CUDA graph

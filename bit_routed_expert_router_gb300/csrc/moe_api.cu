@@ -194,7 +194,7 @@ struct moe_ctx {
   int32_t* pf_cnt_host = nullptr;              // pinned [n_experts]: pairs per expert of the layer
   cudaEvent_t pf_ev_cnt = nullptr;             // pf_cnt_host filled
   cudaEvent_t pf_ev_read = nullptr;            // the GEMMs that read the arena last are done
-  CUtensorMap pf_map_xp[2]{}, pf_map_x16[2]{}, pf_map_ar[2]{}, pf_map_as[2]{};   // [0]: 128-row boxes, [1]: 32
+  CUtensorMap pf_map_xp[3]{}, pf_map_x16[3]{}, pf_map_ar[3]{}, pf_map_as[3]{};   // [0]: 128-row boxes, [1]: 32, [2]: 256
   unsigned long long* p_timeline = nullptr;   // caller device buffer [n_layers][16], test hook 5
   // per-kernel timing
   bool profiling = false;
@@ -1066,7 +1066,8 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // the tcgen05 prefill: 128-row weight tiles of the down projection, one router
   // CTA column of 128 experts, and its shared memory
   if (c.d % 128 == 0 && c.n_experts <= 128 && pf_gemm_smem(kPfTileN) <= static_cast<size_t>(max_smem) &&
-      pf_gemm_smem(kPfTileNSmall) <= static_cast<size_t>(max_smem)) {
+      pf_gemm_smem(kPfTileNSmall) <= static_cast<size_t>(max_smem) &&
+      pf_gemm_smem(kPfTileNBig) <= static_cast<size_t>(max_smem)) {
     if (pf_set_attrs() == cudaSuccess) ctx->pf_ok = true;
     cudaGetLastError();
   }
@@ -1514,8 +1515,8 @@ moe_status pf_alloc(moe_ctx* ctx) {
       !ctx->pf_ids || !ctx->pf_gates || !ctx->pf_cnt || !ctx->pf_rowpair || !ctx->pf_items || !ctx->pf_nitems ||
       !ctx->pf_ytok || !ctx->pf_approx || !ctx->pf_xn2 || !ctx->pf_xmax || !ctx->pf_ys)
     return fail(ctx, MOE_ENOMEM, "prefill scratch (%zu bytes for %zu tokens) does not fit", nb, T);
-  for (int i = 0; i < 2; ++i) {
-    const int br = i == 0 ? kPfTileN : kPfTileNSmall;
+  for (int i = 0; i < 3; ++i) {
+    const int br = i == 0 ? kPfTileN : i == 1 ? kPfTileNSmall : kPfTileNBig;
     if (!encode_rows(&ctx->pf_map_xp[i], ctx->pf_xp, c.d, static_cast<long long>(P), br) ||
         !encode_rows(&ctx->pf_map_x16[i], ctx->pf_x16, c.d, static_cast<long long>(T), br) ||
         !encode_rows(&ctx->pf_map_ar[i], ctx->pf_ar, c.f, static_cast<long long>(P), br) ||
@@ -1528,9 +1529,16 @@ moe_status pf_alloc(moe_ctx* ctx) {
 }
 
 // One layer of the batched prefill: route, group by expert, four grouped GEMMs.
-// Token tiles of 32 rows when the experts' groups are small (a few rows each), else 128.
-int pf_tile_routed(const moe_config& c, int T) { return T * c.top_k <= 16 * c.n_experts ? kPfTileNSmall : kPfTileN; }
-int pf_tile_shared(int T) { return T <= 48 ? kPfTileNSmall : kPfTileN; }
+// Token tiles of 32 rows when the experts' groups are small (a few rows each),
+// 256 when they average 192 rows or more (a dequantised weight tile then
+// serves twice the tokens), else 128.
+int pf_tile_routed(const moe_config& c, int T) {
+  const long long P = static_cast<long long>(T) * c.top_k;
+  if (P <= 16ll * c.n_experts) return kPfTileNSmall;
+  return P >= 192ll * c.n_experts ? kPfTileNBig : kPfTileN;
+}
+int pf_tile_shared(int T) { return T <= 48 ? kPfTileNSmall : T >= kPfTileNBig ? kPfTileNBig : kPfTileN; }
+int pf_map_index(int tile) { return tile == kPfTileN ? 0 : tile == kPfTileNSmall ? 1 : 2; }
 
 // One prefill layer, first part: RMS norm, router, the expert-ordered pair list
 // and the gathered token rows (pf_cnt then holds the pairs per expert).
@@ -1568,7 +1576,7 @@ PfGemm pf_gemm_base(moe_ctx* ctx) {
 // Shared expert gate/up over every token (needs no routed expert).
 moe_status pf_layer_shared_gu(moe_ctx* ctx, int l, int rel, int T, cudaStream_t s) {
   const moe_config& c = ctx->cfg;
-  const int ns = pf_tile_shared(T), ms = ns == kPfTileN ? 0 : 1;
+  const int ns = pf_tile_shared(T), ms = pf_map_index(ns);
   const int t_items = (T + ns - 1) / ns;
   PfGemm b = pf_gemm_base(ctx);
   b.w = ctx->L[l].shared;
@@ -1593,7 +1601,7 @@ moe_status pf_layer_rest(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t
   const bool dbg = rel < ctx->dbg_layers;
   const size_t xo = static_cast<size_t>(rel) * T;
   const int nr = pf_tile_routed(c, T), ns = pf_tile_shared(T);
-  const int mr = nr == kPfTileN ? 0 : 1, ms = ns == kPfTileN ? 0 : 1;
+  const int mr = pf_map_index(nr), ms = pf_map_index(ns);
   const size_t gu_r = static_cast<size_t>(c.f / 8) * (d / 64) * kGroupBytes;
   const size_t gu_s = static_cast<size_t>(c.f_shared / 8) * (d / 64) * kGroupBytes;
   const int max_items = P / nr + E + 1;

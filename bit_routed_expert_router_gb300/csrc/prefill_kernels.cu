@@ -46,14 +46,15 @@ namespace moe {
 namespace {
 
 constexpr int kM = 128;                 // weight rows per CTA tile
-// Token rows per CTA tile: 128 for large groups, 32 when every expert has only
-// a few rows (then the MMA is 4x shorter and a third k-step slot fits).
+// Token rows per CTA tile: 256 when the groups are large (each dequantised
+// weight tile then serves twice the tokens of a 128-row tile; one CTA per SM),
+// 128 for mid-sized groups, 32 when every expert has only a few rows.
 template <int N>
 struct Tile {
   static constexpr int kSlots = 4;                     // k-step slots (A in tensor memory, B in shared)
   static constexpr int kBBytes = N * 128;              // one N-row x 64-col fp16 tile
-  static constexpr int kRawStages = N == 128 ? 2 : 4;  // int4 stages (more when the tokens are few)
-  static constexpr int kTmemCols = 256;                // accumulator (N) + four 32-column A slots
+  static constexpr int kRawStages = N == 32 ? 4 : 2;   // int4 stages (more when the tokens are few)
+  static constexpr int kTmemCols = N == 256 ? 512 : 256;   // accumulator (N) + four 32-column A slots
 };
 constexpr int kRawG = 4;                // int4 groups per raw stage
 constexpr int kRawStride = kRawG * kGroupBytes;   // bytes of one 16-row tile in a raw stage
@@ -75,13 +76,16 @@ struct GemmSmem {
   int row_info[N];                      // epilogue: pair index (routed down) of each token row
 };
 static_assert(offsetof(GemmSmem<128>, b) % 1024 == 0 && offsetof(GemmSmem<32>, b) % 1024 == 0 &&
-                  Tile<32>::kBBytes % 1024 == 0,
+                  offsetof(GemmSmem<256>, b) % 1024 == 0 && Tile<32>::kBBytes % 1024 == 0,
               "swizzled tiles need 1 KB alignment");
 static_assert(offsetof(GemmSmem<128>, raw) % 128 == 0 && offsetof(GemmSmem<32>, raw) % 128 == 0 &&
+                  offsetof(GemmSmem<256>, raw) % 128 == 0 &&
                   kRawStride % 16 == 0,
               "bulk copy targets need 16 B");
-static_assert(offsetof(GemmSmem<128>, raw_full) % 8 == 0 && offsetof(GemmSmem<32>, raw_full) % 8 == 0,
+static_assert(offsetof(GemmSmem<128>, raw_full) % 8 == 0 && offsetof(GemmSmem<32>, raw_full) % 8 == 0 &&
+                  offsetof(GemmSmem<256>, raw_full) % 8 == 0,
               "mbarriers need 8 B");
+static_assert(sizeof(GemmSmem<256>) + 1024 <= 227 * 1024, "256-row token tiles fit one CTA per SM");
 
 // ------------------------------------------------------------------ tcgen05 / TMA primitives
 
@@ -327,9 +331,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
     // tensor-memory lanes 32q .. 32q + 31 its warp may access); in the epilogue it reads those
     // accumulator lanes and the column half (w - 2) / 4
     const int dw = warp - 2, q = warp & 3, b16 = 2 * q + (dw >> 2);
-    // column range of this warp's epilogue: two halves of 128 columns, or all 32 for warps 2..5
-    const int c_lo = kN == 128 ? (dw >> 2) * 64 : 0;
-    const int c_hi = kN == 128 ? c_lo + 64 : ((dw >> 2) == 0 ? 32 : 0);
+    // column range of this warp's epilogue: two halves of the kN columns, or all 32 for warps 2..5
+    const int c_lo = kN >= 128 ? (dw >> 2) * (kN / 2) : 0;
+    const int c_hi = kN >= 128 ? c_lo + kN / 2 : ((dw >> 2) == 0 ? 32 : 0);
     for (int G = 0; G < nG; ++G) {
       const int s = G / kRawG, rs = s % kRawStages, gi = G % kRawG;
       if (gi == 0 && !wait_or_abort(S, &S.raw_full[rs], (s / kRawStages) & 1, p.err)) break;
@@ -875,11 +879,16 @@ __global__ void __launch_bounds__(256) k_pf_gather(const uint16_t* x16, const in
 
 }  // namespace
 
-size_t pf_gemm_smem(int n) { return (n == 32 ? sizeof(GemmSmem<32>) : sizeof(GemmSmem<128>)) + 1024; }
+size_t pf_gemm_smem(int n) {
+  return (n == 32 ? sizeof(GemmSmem<32>) : n == 256 ? sizeof(GemmSmem<256>) : sizeof(GemmSmem<128>)) + 1024;
+}
 
 cudaError_t pf_set_attrs() {
   cudaError_t e = cudaFuncSetAttribute((const void*)k_pf_gemm<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(pf_gemm_smem(128)));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute((const void*)k_pf_gemm<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(pf_gemm_smem(256)));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute((const void*)k_pf_gemm<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(pf_gemm_smem(32)));
@@ -889,6 +898,7 @@ cudaError_t launch_pf_gemm(int n, const CUtensorMap& tmap_b, const PfGemm& p, in
                            cudaStream_t s) {
   if (m_tiles <= 0 || max_items <= 0) return cudaSuccess;
   if (n == 32) k_pf_gemm<32><<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(32), s>>>(tmap_b, p);
+  else if (n == 256) k_pf_gemm<256><<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(256), s>>>(tmap_b, p);
   else k_pf_gemm<128><<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(128), s>>>(tmap_b, p);
   return cudaGetLastError();
 }
