@@ -189,6 +189,20 @@ def test_gelu_textbook_values():
         assert abs(oracle.gelu(x, 1) - oracle.gelu(x, 0)) < 1e-3    # tanh form approximates erf form
 
 
+def test_gelu_tanh_form_against_decimal_values():
+    # the tanh variant against the formula evaluated in 50-digit decimal
+    # arithmetic by tests/golden/make_gelu_tanh.py (no float library involved):
+    # a wrong coefficient (0.044715, sqrt(2/pi)) or a dropped term moves these
+    # values by far more than the tolerance
+    import json
+    with open(os.path.join(os.path.dirname(__file__), "golden", "gelu_tanh.json")) as fh:
+        g = json.load(fh)
+    assert len(g["values"]) >= 10
+    for x, v in g["values"]:
+        got, ref = oracle.gelu(float(x), 1), float(v)
+        assert abs(got - ref) <= 1e-15 + 1e-15 * abs(ref), (x, got, ref)
+
+
 def test_matvec_matches_materialised_dense_matrix():
     sh = Shape(d=192, f=64, f_shared=64, n_experts=2, top_k=1)
     L = gen_layer(sh, seed=11, layer=0)
