@@ -27,6 +27,7 @@ HOOK_CLUSTER = 9
 HOOK_SPIN_LIMIT = 10      # bounded waits of the persistent decode kernels: cycles (<= 0: the default)
 HOOK_AT_REST = 11         # MOE_OK when the persistent kernels' launch words are back at rest
 HOOK_WAIT_DIAG = 12       # the clustered kernel's first wait that ran out (site << 16 | CTA) into a host uint32
+HOOK_SMALL_BATCH = 13     # small-batch grouped GEMVs (calls of at most 32 tokens) on / off
 
 
 class MoeConfig(C.Structure):
@@ -59,7 +60,7 @@ class MoeKernelTime(C.Structure):
 
 N_KERNEL_KINDS = 8
 KERNEL_KINDS = {0: "router_topk_plan", 1: "gateup_gelu_gemv", 2: "down_combine_gemv", 3: "decode_persistent",
-                4: "prefill_route_group", 5: "prefill_tcgen05_gemm", 6: "prefill_combine"}
+                4: "prefill_route_group", 5: "prefill_tcgen05_gemm", 6: "prefill_combine", 7: "small_batch_gemv"}
 
 
 class MoeError(RuntimeError):

@@ -19,7 +19,8 @@ BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(BUILD, "libmoe.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["decode_kernels.cu", "persistent.cu", "decode_cluster.cu", "expert_file.cu", "prefill_kernels.cu", "moe_api.cu", "no_alloc.cu"]
+SOURCES = ["decode_kernels.cu", "persistent.cu", "decode_cluster.cu", "expert_file.cu", "prefill_kernels.cu",
+           "small_batch.cu", "moe_api.cu", "no_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]

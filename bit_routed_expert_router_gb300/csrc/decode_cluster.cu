@@ -35,14 +35,14 @@
 //   warp 0, lane 0 (producer): the router row, then every stage of the CTA's
 //     units (gate/up tiles by 1-D bulk copy, down slices by a 3-D TMA tile load
 //     that gathers one group of d/64 consecutive 16-row tiles) into a ring of
-//     six shared-memory slots; routing-independent units (shared expert) come
+//     seven shared-memory slots; routing-independent units (shared expert) come
 //     first, routed units after the top-k is known.
 //   warps 1..16 (consumers): four quads of four warps; stage u of the CTA goes
 //     to quad u mod 4 (gate/up: a quarter of the groups per warp, the last
 //     warp of the quad to finish sums the partials in warp order and runs the
 //     epilogue and the push; down: row tiles strided by warp).  A unit's down
-//     stage is queued after the next unit's gate/up stages, so its 64 values
-//     of a have normally arrived from the other CTAs of the cluster by then.
+//     stage is queued after the next two units' gate/up stages, so its 64
+//     values of a have normally arrived from the other CTAs of the cluster.
 //   warp 17 (top-k): polls the layer's tagged logits, takes the top-k and the
 //     softmax gates and releases the producer.
 // Every wait is bounded and gives up through an abort flag and the device
@@ -334,7 +334,7 @@ __device__ __forceinline__ float gelu_p(float v, int variant) {
 enum : int { EV_Y_SEEN, EV_X_READY, EV_LOGIT_OUT, EV_LOGITS_IN, EV_TOPK_DONE, EV_ROUTED_ISSUE, EV_SHARED_DATA,
              EV_ROUTED_DATA, EV_PUSH_LAST, EV_DN_LAST, EV_STAGES_DONE, EV_REDUCED, EV_ISSUE_LAST, EV_DATA_LAST,
              EV_DN_A_FIRST, EV_A_WAIT_LAST, EV_PREP_B1, EV_PREP_Y, EV_PREP_B2, EV_ROUTER_B, EV_TOPK_SORTED,
-             EV_BULK_ISSUED, EV_OPS_READY };
+             EV_BULK_ISSUED, EV_OPS_READY, EV_RANKS_OUT };
 constexpr int kTlCols = 32;            // timeline row: events 0..23, accumulators 24..31
 
 __device__ __forceinline__ void stamp(const CParams& p, int rel, int ev, bool latest = false) {
@@ -374,12 +374,13 @@ __device__ __forceinline__ void acc(const CParams& p, int rel, int slot, unsigne
 // (cluster_unit_owner_shared): routed work waits for the top-k and sets the
 // layer's length, shared work fills the wait, which holds one or two units.
 // A cluster runs its shared units first.
-// Within each list a unit's down stage follows the next unit's two gate/up
-// stages.  Returns the number of units (> kMaxU: does not fit).
+// Within each list a unit's down stage follows the gate/up stages of the next
+// two units, so the other CTAs' values of a have normally arrived by the time
+// a quad takes it.  Returns the number of units (> kMaxU: does not fit).
 __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
   const int nGf = p.f / 64, nGs = p.fs / 64, Ur = p.k * nGf;
   int n = 0, t = 0;
-  int pend = -1;            // unit whose down stage is still to be queued
+  int pend = -1, pend2 = -1;   // units whose down stages are still to be queued, oldest first
   auto push = [&](int kind, int tt, int ui) {
     CTask e;
     e.kind = static_cast<int8_t>(kind);
@@ -397,13 +398,15 @@ __device__ int build_tasks(const CParams& p, Smem& S, int cl, int n_cl) {
       push(K_GU, 0, n);
       push(K_GU, 1, n);
       if (pend >= 0) push(K_DN, 0, pend);
-      pend = n;
+      pend = pend2;
+      pend2 = n;
     }
     ++n;
   };
   auto flush = [&]() {
     if (pend >= 0 && n <= kMaxU) push(K_DN, 0, pend);
-    pend = -1;
+    if (pend2 >= 0 && n <= kMaxU) push(K_DN, 0, pend2);
+    pend = pend2 = -1;
   };
   for (int G = 0; G < nGs; ++G)
     if (cluster_unit_owner_shared(G, Ur, n_cl) == cl) add_unit(-1, G);
@@ -658,20 +661,20 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
         c = c && static_cast<unsigned>(he) == me;
       }
     }
+    // the one winning lane records rank j and publishes it, tagged with the
+    // layer and the rank, in this CTA's rank word j, which the cluster's four
+    // producers read (three of them through distributed shared memory) to
+    // load its expert while the warp picks the rest
     if (c) {
       ids[j] = he;
       S.topv[j] = static_cast<long long>(hk ^ 0x8000000000000000ull);
       ++head;
-    }
-    // rank j is known: it goes, tagged with the layer and the rank, into
-    // this CTA's rank word j, which the cluster's four producers read (three
-    // of them through distributed shared memory) to load its expert while the
-    // warp picks the rest
-    __syncwarp();
-    if (lane == 0)
       *reinterpret_cast<volatile unsigned*>(&S.rank_word[j]) =
-          (seq_base + static_cast<unsigned>(j) + 1u) << 8 | static_cast<unsigned>(ids[j]);
+          (seq_base + static_cast<unsigned>(j) + 1u) << 8 | static_cast<unsigned>(he);
+    }
   }
+  __syncwarp();
+  if (lane == 0) stamp(p, l - p.l0, EV_RANKS_OUT);
   float ex = 0.f;
   if (lane < p.k) ex = expf(__ll2float_rn(S.topv[lane] - S.topv[0]) * 9.094947017729282e-13f);   // 2^-40
   float sum = 0.f;
@@ -987,20 +990,17 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
   }
   Fix40 fx;
   bool bad = false;
-  uint32_t xw[kGW];
 #pragma unroll
   for (int i = 0; i < kGW; ++i) {
     const int G = cw + kNC * i;
-    xw[i] = 0u;
-    if (G >= nGd) continue;
+    if (G >= nGd || !routes) continue;
     uint32_t xv = reinterpret_cast<const uint32_t*>(S.h)[32 * G + lane];
     if (p.prenorm) {
       const float a = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu)) * r;
       const float b = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16)) * r;
       xv = static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
     }
-    xw[i] = xv;
-    if (routes) {
+    {
       const uint32_t wv = reinterpret_cast<const uint32_t*>(S.rrow)[32 * G + lane];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -1022,56 +1022,48 @@ __device__ bool prep(const CParams& p, Smem& S, int cw, int rel, int& round, uns
   }
   if (!consumer_barrier(p, S, ++round)) return false;   // the router partials complete
   if (cw == 0 && lane == 0) stamp(p, rel, EV_X_READY);
-  router_publish(p, S, cw, rel, bias_v);
-  // the matrix operands: x as fp16 mma B fragments and its per-group sums
+  // warp 0 forms and publishes the logit (it arrives on the operands barrier
+  // first: the logit is the longer chain), the other warps build the matrix
+  // operands of x: fp16 mma B fragments and per-group sums
+  ++round;
+  if (cw == 0) {
+    __syncwarp();
+    if (lane == 0) mbarrier_arrive(&S.cbar);
+    router_publish(p, S, cw, rel, bias_v);
+  } else {
+    for (int G = cw - 1; G < nGd; G += kNC - 1) {
+      uint32_t xv = reinterpret_cast<const uint32_t*>(S.h)[32 * G + lane];
+      if (p.prenorm) {   // the same rounding as above: the same x
+        const float a = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu)) * r;
+        const float b = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16)) * r;
+        xv = static_cast<uint32_t>(float_to_bf16_bits(a)) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
+      }
+      // fp16 B fragments: element e = 2*lane of the group lands in (t4, st, pos)
+      const float xa = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu));
+      const float xb = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16));
+      const __half ha = __float2half_rn(xa), hb = __float2half_rn(xb);
+      if (__any_sync(kFull, !(fabsf(xa) < 65504.f && fabsf(xb) < 65504.f)) && lane == 0)
+        atomicOr(p.err, ERR_PF_RANGE);
+      const int e = 2 * lane, st = e >> 4, w = e & 15;
+      const int t4 = (w & 7) >> 1, hi = w >> 3;
+      reinterpret_cast<uint32_t*>(S.xp)[((G * 4 + t4) * 4 + st) * 2 + hi] =
+          static_cast<uint32_t>(__half_as_ushort(ha)) | (static_cast<uint32_t>(__half_as_ushort(hb)) << 16);
+      float gs = __half2float(ha) + __half2float(hb);
 #pragma unroll
-  for (int i = 0; i < kGW; ++i) {
-    const int G = cw + kNC * i;
-    if (G >= nGd) continue;
-    const uint32_t xv = xw[i];
-    // fp16 B fragments: element e = 2*lane of the group lands in (t4, st, pos)
-    const float xa = bf16_bits_to_float(static_cast<uint16_t>(xv & 0xFFFFu));
-    const float xb = bf16_bits_to_float(static_cast<uint16_t>(xv >> 16));
-    const __half ha = __float2half_rn(xa), hb = __float2half_rn(xb);
-    if (__any_sync(kFull, !(fabsf(xa) < 65504.f && fabsf(xb) < 65504.f)) && lane == 0) atomicOr(p.err, ERR_PF_RANGE);
-    const int e = 2 * lane, st = e >> 4, w = e & 15;
-    const int t4 = (w & 7) >> 1, hi = w >> 3;
-    reinterpret_cast<uint32_t*>(S.xp)[((G * 4 + t4) * 4 + st) * 2 + hi] =
-        static_cast<uint32_t>(__half_as_ushort(ha)) | (static_cast<uint32_t>(__half_as_ushort(hb)) << 16);
-    float gs = __half2float(ha) + __half2float(hb);
-#pragma unroll
-    for (int m = 16; m; m >>= 1) gs += __shfl_xor_sync(kFull, gs, m);
-    if (lane == 0) S.xg[G] = gs;
-    if (blockIdx.x == 0 && A->dbg_x && rel < A->dbg_layers)
-      reinterpret_cast<uint32_t*>(A->dbg_x + (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * d)[32 * G + lane] = xv;
+      for (int m = 16; m; m >>= 1) gs += __shfl_xor_sync(kFull, gs, m);
+      if (lane == 0) S.xg[G] = gs;
+      if (blockIdx.x == 0 && A->dbg_x && rel < A->dbg_layers)
+        reinterpret_cast<uint32_t*>(A->dbg_x + (static_cast<size_t>(rel) * A->tok_total + A->tok_off) * d)[32 * G + lane] =
+            xv;
+    }
+    __syncwarp();
+    if (lane == 0) mbarrier_arrive(&S.cbar);
   }
-  const bool ok = consumer_barrier(p, S, ++round);   // x's operands complete
-  if (cw == 0 && lane == 0) stamp(p, rel, EV_OPS_READY);
+  const bool ok = wait_warp(p, &S.cbar, static_cast<uint32_t>(round - 1) & 1u, W_CBAR);   // x's operands complete
+  if (!ok) raise_abort(p);
+  __syncwarp();
+  if (cw == 1 && lane == 0) stamp(p, rel, EV_OPS_READY);
   return ok;
-}
-
-// Eight packed nibbles -> four f16x2 A-fragment registers with four logic ops
-// and one shift: register r takes nibbles r (low half) and r + 4 (high half)
-// where they sit, under the fp16 exponent of 1024 (unit in the last place 1).
-// Registers 0 and 2 (fragment rows g) hold 1024 + q; registers 1 and 3 (rows
-// g + 8) keep their nibbles four bits up and hold 1024 + 16 q, which the
-// epilogue undoes per row.  (bf16 has too few mantissa bits for the second
-// form, which is why the activations of this kernel's MMAs are fp16.)
-__device__ __forceinline__ void nibbles_to_f16x2(uint32_t w, uint32_t (&a)[4]) {
-  const uint32_t w8 = w >> 8;
-  a[0] = (w & 0x000F000Fu) | 0x64006400u;
-  a[1] = (w & 0x00F000F0u) | 0x64006400u;
-  a[2] = (w8 & 0x000F000Fu) | 0x64006400u;
-  a[3] = (w8 & 0x00F000F0u) | 0x64006400u;
-}
-
-// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators, A/B from registers.
-__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // Groups [G0, G1) of a gate/up tile: partial gate and up sums of row g.  With
@@ -1327,7 +1319,9 @@ __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round
   for (int i0 = 0; i0 < rows; i0 += kNC * 32) {
     const int i = i0 + cw * 32 + lane;
     if (i < rows) {
-      const float y = ((S.dn_acc[0][i] + S.dn_acc[1][i]) + S.dn_acc[2][i]) + S.dn_acc[3][i];
+      float y = S.dn_acc[0][i];
+#pragma unroll
+      for (int q = 1; q < kNQ; ++q) y += S.dn_acc[q][i];
 #pragma unroll
       for (int q = 0; q < kNQ; ++q) S.dn_acc[q][i] = 0.f;
       // |y| < 2^17 (v < 2^49 on the 2^-32 grid): with at most 64 clusters the

@@ -2,22 +2,23 @@
 //
 // Per layer the host enqueues three kernels:
 //   k_router  - (optional RMS norm), exact fixed-point router logits, top-k
-//               with lower-index ties, softmax gates over the picked k
-//               (TurboFieldfare video transcript: "the router picks the top
-//               eight experts"), the per-layer LRU slot step in host-pool
+//               with lower-index ties, softmax gates over the picked k (the
+//               TurboFieldfare video transcript: eight of the experts are
+//               picked per token), the per-layer LRU slot step in host-pool
 //               mode, and the token-by-expert plan;
 //   k_gateup  - fused int4 gate+up GEMV with GELU(gate)*up for the shared
-//               expert and every picked expert ("one shared expert that
-//               always runs"), int4 affine groups of 64 (section
-//               "Vectorization helped when it respected the storage layout");
+//               expert, which every token runs, and every picked expert; int4
+//               affine groups of 64 (write-up section "Vectorization helped
+//               when it respected the storage layout");
 //   k_down    - int4 down GEMV per (16-row tile, source) and, by the last
 //               source to finish a tile, the fixed-order router-weighted
 //               combine y = y_shared + sum_j gate_j y_j and the residual.
 //
 // Work is split the way the TurboFieldfare write-up found fastest for its
-// routed-MoE kernel ("Persistent GPU workgroups ... claimed rows until the
-// dispatch completed"): many independent warps, each owning a row tile of one
-// expert, instead of several lanes cooperating on one expert.  On sm_103a a
+// routed-MoE kernel (section "MoE needed parallel work, reuse, and coarse
+// overlap": resident workgroups taking rows until the dispatch is done): many
+// independent warps, each owning a row tile of one expert, instead of several
+// lanes cooperating on one expert.  On sm_103a a
 // warp stages its whole tile into shared memory with one bulk (TMA-engine)
 // copy, then runs the int4 dot products on the tensor cores: nibbles become
 // bf16 (128 + q) operands in registers, the 128 offset and the affine

@@ -171,6 +171,37 @@ cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* g
 cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,
                              cudaStream_t s);
 
+// Small-batch grouped GEMVs (mma.sync from a TMA ring) for calls of at most
+// kSgMaxT tokens, after the prefill path's routing and expert grouping.
+constexpr int kSgMaxT = 32;            // tokens of a small-batch call
+constexpr int kSgMaxG = 44;            // int4 groups one ring slot holds (d, f, f_s <= 2816)
+enum : int { SG_GU = 0, SG_DN = 1 };
+
+struct SgParams {
+  int mode;                            // SG_GU or SG_DN
+  int d, f, fs, T, P, gelu;            // P = T * top_k expert-ordered rows
+  const uint8_t* experts;              // expert 0's device record (gate/up tiles, then down)
+  long long stride;                    // bytes between experts
+  const uint8_t* shared;               // the shared expert's device record
+  const int32_t* items;                // [n][3]: active expert, its first expert-ordered row, its rows (<= kSgMaxT)
+  const int32_t* n_items;              // n, on the device
+  const int32_t* row_pair;             // [P]: pair (t * k + j) of each expert-ordered row
+  const uint16_t* xv;                  // fp16 x in fragment order: [P] expert-ordered rows, then [T] token rows
+  const float* xg;                     // [P + T][d / 64]: group sums of those rows
+  uint16_t* av_r;                      // [P][f]: fp16 a of the routed rows, fragment order
+  uint16_t* av_s;                      // [T][fs]: fp16 a of the shared expert, fragment order
+  float* y_r;                          // [T * k][d]: routed down outputs by pair
+  float* y_s;                          // [T][d]: shared down output
+  uint32_t* err;
+};
+
+bool sg_shape_ok(int d, int f, int fs);
+size_t sg_smem();
+cudaError_t sg_set_attrs();
+cudaError_t launch_sg_gather(const uint16_t* x_bf, const int32_t* row_pair, int P, int T, int d, int k, uint16_t* xv,
+                             float* xg, cudaStream_t s);
+cudaError_t launch_sg(const SgParams& p, int n_sm, cudaStream_t s);
+
 size_t gateup_smem(int d);
 size_t down_smem(int cg, int nb4);
 int pick_nb(int B);

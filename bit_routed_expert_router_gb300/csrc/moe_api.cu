@@ -187,6 +187,11 @@ struct moe_ctx {
   float *pf_gates = nullptr, *pf_ytok = nullptr;
   float *pf_approx = nullptr, *pf_xn2 = nullptr, *pf_xmax = nullptr;
   float* pf_ys = nullptr;
+  // small-batch grouped GEMVs (calls of at most kSgMaxT tokens on the tcgen05 path's routing)
+  bool sg_ok = false;                  // shapes and device allow it
+  bool use_sg = true;                  // test hook 13
+  uint16_t* sg_xv = nullptr;           // [kSgMaxT * (k + 1)][d] fp16 x rows in fragment order
+  float* sg_xg = nullptr;              // [kSgMaxT * (k + 1)][d / 64] their group sums
   unsigned long long* pf_timeline = nullptr;   // test hook 8: [4][16] GEMM event times of the first layer
   // chunked prefill of host-pool / expert-file contexts: the union of a chunk's
   // experts of one layer, staged into an arena (expert e at e * stride)
@@ -1071,6 +1076,11 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     if (pf_set_attrs() == cudaSuccess) ctx->pf_ok = true;
     cudaGetLastError();
   }
+  // the small-batch GEMVs run on the tcgen05 path's routing and grouping
+  if (ctx->pf_ok && sg_shape_ok(c.d, c.f, c.f_shared) && sg_smem() <= static_cast<size_t>(max_smem)) {
+    if (sg_set_attrs() == cudaSuccess) ctx->sg_ok = true;
+    cudaGetLastError();
+  }
   if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ECUDA);
   *out = ctx;
   return MOE_OK;
@@ -1464,9 +1474,10 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
     if (ctx->c_ok && ctx->use_cluster) return cluster_run(ctx, layer_begin, layer_end, s);
     if (ctx->p_ok) return persistent_run(ctx, layer_begin, layer_end, s);
   }
-  // from about 16 tokens on, the grouped tcgen05 path beats the mma.sync GEMVs (measured crossover)
-  if (B >= kPfMinDecodeB && ctx->pf_ok && ctx->use_pf) return pf_run(ctx, h_in, B, layer_begin, layer_end, logit_bias,
-                                                                  h_out, y_last, s);
+  // the grouped path: with the small-batch GEMVs for every batch of two tokens or more, else
+  // (tcgen05 GEMMs) from about 16 tokens on (measured crossover with the per-layer GEMVs)
+  const bool grouped = ctx->pf_ok && ctx->use_pf && B >= 2 && ((ctx->sg_ok && ctx->use_sg) || B >= kPfMinDecodeB);
+  if (grouped) return pf_run(ctx, h_in, B, layer_begin, layer_end, logit_bias, h_out, y_last, s);
   return resident_run(ctx, B, layer_begin, layer_end, s);
 }
 
@@ -1511,6 +1522,12 @@ moe_status pf_alloc(moe_ctx* ctx) {
   ctx->pf_xn2 = dalloc<float>(T, o, nb);
   ctx->pf_xmax = dalloc<float>(T, o, nb);
   ctx->pf_ys = dalloc<float>(T * c.d, o, nb);
+  if (ctx->sg_ok) {
+    const size_t rows = std::min<size_t>(T, kSgMaxT) * (c.top_k + 1);
+    ctx->sg_xv = dalloc<uint16_t>(rows * c.d, o, nb);
+    ctx->sg_xg = dalloc<float>(rows * (c.d / 64), o, nb);
+    if (!ctx->sg_xv || !ctx->sg_xg) return fail(ctx, MOE_ENOMEM, "small-batch scratch does not fit");
+  }
   if (!ctx->pf_xbf || !ctx->pf_x16 || !ctx->pf_xp || !ctx->pf_ar || !ctx->pf_as || !ctx->pf_h[0] || !ctx->pf_h[1] ||
       !ctx->pf_ids || !ctx->pf_gates || !ctx->pf_cnt || !ctx->pf_rowpair || !ctx->pf_items || !ctx->pf_nitems ||
       !ctx->pf_ytok || !ctx->pf_approx || !ctx->pf_xn2 || !ctx->pf_xmax || !ctx->pf_ys)
@@ -1544,7 +1561,7 @@ int pf_map_index(int tile) { return tile == kPfTileN ? 0 : tile == kPfTileNSmall
 // One prefill layer, first part: RMS norm, router, the expert-ordered pair list
 // and the gathered token rows (pf_cnt then holds the pairs per expert).
 moe_status pf_layer_route(moe_ctx* ctx, int l, int rel, const uint16_t* hin, int T, const float* bias,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool small = false) {
   const moe_config& c = ctx->cfg;
   const LayerStore& L = ctx->L[l];
   const int d = c.d, E = c.n_experts, k = c.top_k, P = T * k;
@@ -1557,9 +1574,10 @@ moe_status pf_layer_route(moe_ctx* ctx, int l, int rel, const uint16_t* hin, int
                       ctx->pf_xn2, L.router_stats, ctx->pf_xmax, L.router_stats + E, ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
                       dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr,
                       dbg && ctx->dbg_logits ? ctx->dbg_logits + xo * E : nullptr, ctx->err_word, ctx->n_sm, s));
-  CK(launch_pf_plan(ctx->pf_ids, P, E, pf_tile_routed(c, T), ctx->pf_cnt, ctx->pf_rowpair, ctx->pf_items,
-                    ctx->pf_nitems, s));
-  CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
+  CK(launch_pf_plan(ctx->pf_ids, P, E, small ? kSgMaxT : pf_tile_routed(c, T), ctx->pf_cnt, ctx->pf_rowpair,
+                    ctx->pf_items, ctx->pf_nitems, s));
+  if (small) CK(launch_sg_gather(ctx->pf_xbf, ctx->pf_rowpair, P, T, d, k, ctx->sg_xv, ctx->sg_xg, s));
+  else CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
   PROF(-1, s);
   return MOE_OK;
 }
@@ -1649,8 +1667,61 @@ moe_status pf_layer_rest(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t
   return MOE_OK;
 }
 
+bool sg_use(const moe_ctx* ctx, int T) { return ctx->sg_ok && ctx->use_sg && T <= kSgMaxT; }
+
+// The rest of a layer of at most kSgMaxT tokens after its routing and grouping
+// (one item per active expert, expert e's record at experts + e * stride): the
+// two small-batch GEMV launches and the combine (+ residual).
+moe_status pf_layer_small_rest(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin, uint16_t* hout, int T,
+                               float* y_last, const uint8_t* experts, cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
+  const LayerStore& L = ctx->L[l];
+  const bool dbg = rel < ctx->dbg_layers;
+  const size_t xo = static_cast<size_t>(rel) * T;
+  SgParams g{};
+  g.d = c.d;
+  g.f = c.f;
+  g.fs = c.f_shared;
+  g.T = T;
+  g.P = T * c.top_k;
+  g.gelu = c.gelu_variant;
+  g.experts = experts;
+  g.stride = ctx->stride;
+  g.shared = L.shared;
+  g.items = ctx->pf_items;
+  g.n_items = ctx->pf_nitems;
+  g.row_pair = ctx->pf_rowpair;
+  g.xv = ctx->sg_xv;
+  g.xg = ctx->sg_xg;
+  g.av_r = ctx->pf_ar;
+  g.av_s = ctx->pf_as;
+  g.y_r = ctx->pf_ytok;
+  g.y_s = ctx->pf_ys;
+  g.err = ctx->err_word;
+  PROF(7, s);
+  g.mode = SG_GU;
+  CK(launch_sg(g, ctx->n_sm, s));
+  g.mode = SG_DN;
+  CK(launch_sg(g, ctx->n_sm, s));
+  PROF(-1, s);
+  PROF(6, s);
+  CK(launch_pf_combine(ctx->pf_ys, ctx->pf_ytok, ctx->pf_gates, hin, hout, rel == n_rel - 1 ? y_last : nullptr,
+                       dbg && ctx->dbg_y ? ctx->dbg_y + xo * c.d : nullptr, T, c.d, c.top_k, s));
+  PROF(-1, s);
+  return MOE_OK;
+}
+
+// A layer of at most kSgMaxT tokens: the routing and grouping, then the rest.
+moe_status pf_layer_small(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin, uint16_t* hout, int T,
+                          const float* bias, float* y_last, cudaStream_t s) {
+  moe_status st = pf_layer_route(ctx, l, rel, hin, T, bias, s, true);
+  if (st != MOE_OK) return st;
+  return pf_layer_small_rest(ctx, l, rel, n_rel, hin, hout, T, y_last, ctx->L[l].experts, s);
+}
+
 moe_status pf_layer(moe_ctx* ctx, int l, int rel, int n_rel, const uint16_t* hin, uint16_t* hout, int T,
                     const float* bias, float* y_last, cudaStream_t s) {
+  if (sg_use(ctx, T)) return pf_layer_small(ctx, l, rel, n_rel, hin, hout, T, bias, y_last, s);
   moe_status st = pf_layer_route(ctx, l, rel, hin, T, bias, s);
   if (st != MOE_OK) return st;
   PROF(5, s);
@@ -1741,13 +1812,16 @@ moe_status pf_pool_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const
     const int l = l0 + rel;
     const uint16_t* hin = rel == 0 ? static_cast<const uint16_t*>(h) : ctx->pf_h[(rel - 1) & 1];
     uint16_t* hout = rel == n_rel - 1 ? static_cast<uint16_t*>(h_out) : ctx->pf_h[rel & 1];
-    st = pf_layer_route(ctx, l, rel, hin, T, logit_bias, s);
+    const bool small = sg_use(ctx, T);
+    st = pf_layer_route(ctx, l, rel, hin, T, logit_bias, s, small);
     if (st != MOE_OK) return st;
     CK(cudaMemcpyAsync(ctx->pf_cnt_host, ctx->pf_cnt, static_cast<size_t>(E) * 4, cudaMemcpyDeviceToHost, s));
     CK(cudaEventRecord(ctx->pf_ev_cnt, s));
-    PROF(5, s);
-    st = pf_layer_shared_gu(ctx, l, rel, T, s);
-    if (st != MOE_OK) return st;
+    if (!small) {   // the shared expert's gate/up runs while the union is staged
+      PROF(5, s);
+      st = pf_layer_shared_gu(ctx, l, rel, T, s);
+      if (st != MOE_OK) return st;
+    }
     st = wait_event(ctx, ctx->pf_ev_cnt, "prefill routing");
     if (st != MOE_OK) return st;
     // the arena is rewritten only after the GEMMs that read it last are done
@@ -1756,7 +1830,8 @@ moe_status pf_pool_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const
     if (st != MOE_OK) return st;
     CK(cudaEventRecord(ctx->ev_copy, ctx->side));
     CK(cudaStreamWaitEvent(s, ctx->ev_copy, 0));
-    st = pf_layer_rest(ctx, l, rel, n_rel, hin, hout, T, y_last, ctx->pf_arena, s);
+    st = small ? pf_layer_small_rest(ctx, l, rel, n_rel, hin, hout, T, y_last, ctx->pf_arena, s)
+               : pf_layer_rest(ctx, l, rel, n_rel, hin, hout, T, y_last, ctx->pf_arena, s);
     if (st != MOE_OK) return st;
     CK(cudaEventRecord(ctx->pf_ev_read, s));
   }
@@ -1988,6 +2063,15 @@ moe_status moe_test_hook(moe_ctx* ctx, int hook, int64_t value) {
       if (value != 0 && !ctx->pf_ok)
         return fail(ctx, MOE_ESTATE, "tcgen05 prefill unavailable for this configuration or device");
       ctx->use_pf = value != 0;
+      return MOE_OK;
+    case 13:  // small-batch GEMVs on/off for calls of at most kSgMaxT tokens on the grouped path
+      if (value != 0 && !ctx->sg_ok)
+        return fail(ctx, MOE_ESTATE, "small-batch GEMVs unavailable for this configuration or device");
+      if ((value != 0) != ctx->use_sg) {   // cached graphs hold the other path
+        for (auto& kv : ctx->pf_graphs) cudaGraphExecDestroy(kv.second);
+        ctx->pf_graphs.clear();
+        ctx->use_sg = value != 0;
+      }
       return MOE_OK;
     case 9:  // clustered (1) or per-SM (0) persistent decode kernel; asking for one that cannot run is an error
       if ((value != 0 && !ctx->c_ok) || (value == 0 && !ctx->p_ok))

@@ -1,9 +1,9 @@
 // Persistent decode kernel: one cooperative launch runs a B = 1 token through
 // every layer of a resident context.
 //
-// The TurboFieldfare write-up's routed-MoE lesson ("Persistent GPU workgroups
-// ... claimed rows until the dispatch completed", section "MoE needed parallel
-// work, reuse, and coarse overlap") is taken to the whole decode step: one CTA
+// The TurboFieldfare write-up's routed-MoE lesson (section "MoE needed
+// parallel work, reuse, and coarse overlap": workgroups that stay resident and
+// take rows until the dispatch is done) is taken to the whole decode step: one CTA
 // per SM lives for the whole step, and the only things that serialise it are
 // the data dependencies of the method itself (h_l -> router -> top-k ->
 // routed gate/up -> down -> h_{l+1}).

@@ -37,6 +37,8 @@
 //                      routed outputs in top-k order, and the residual.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "kernels.h"
@@ -568,21 +570,22 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
     }
 }
 
-// Pass 2: candidates, their exact logits, top-k and gates.  A CTA takes eight
-// tokens (one warp each for the candidates and the top-k); all warps share the
-// exact dot products.
+// Pass 2: candidates, their exact logits, top-k and gates.  A CTA takes tpc <= 8
+// tokens (warp w < tpc takes the candidates and the top-k of token
+// blockIdx.x * tpc + w); all eight warps share the exact dot products, so a
+// small batch runs on one token per CTA and still spreads over the GPU.
 __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const uint16_t* router_w, const float* approx,
                                                   const float* xn2, const float* wn2, const float* xmax,
                                                   const float* wmax, const float* bias, int T, int d,
                                                   int E, int k, int32_t* ids, float* gates, int32_t* dbg_ids,
-                                                  float* dbg_gates, int64_t* dbg_logits, uint32_t* err) {
+                                                  float* dbg_gates, int64_t* dbg_logits, int tpc, uint32_t* err) {
   __shared__ int cand_all[8][128];
   __shared__ long long exact_all[8][128];
   __shared__ int n_cand_all[8];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t = blockIdx.x * 8 + warp;
-  const bool live = t < T;                       // warp-uniform
+  const int t = blockIdx.x * tpc + warp;
+  const bool live = warp < tpc && t < T;         // warp-uniform
   int* cand = cand_all[warp];
   long long* exact = exact_all[warp];
   int& n_cand = n_cand_all[warp];
@@ -657,7 +660,7 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
     int tw = 0;
     while (pi >= first[tw + 1]) ++tw;
     const int ci = pi - first[tw];
-    const int tt = blockIdx.x * 8 + tw;
+    const int tt = blockIdx.x * tpc + tw;
     const int e = cand_all[tw][ci];
     const uint16_t* xr = x_bf + static_cast<size_t>(tt) * d;
     const uint16_t* wr = router_w + static_cast<size_t>(e) * d;
@@ -789,12 +792,28 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
                                                     int32_t* row_pair, int32_t* items, int32_t* n_items) {
   const int e = blockIdx.x;
   __shared__ int s_off, s_base;
-  __shared__ int wsum[8];
+  __shared__ int wsum[8], wit[8];
+  {
+    // pairs and items of the experts before e (E <= 256: one per thread), summed over the CTA
+    const int e2 = threadIdx.x;
+    int c = e2 < e ? cnt[e2] : 0;
+    int it2 = (c + tile - 1) / tile;
+#pragma unroll
+    for (int m = 16; m; m >>= 1) {
+      c += __shfl_xor_sync(0xFFFFFFFFu, c, m);
+      it2 += __shfl_xor_sync(0xFFFFFFFFu, it2, m);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      wsum[threadIdx.x >> 5] = c;
+      wit[threadIdx.x >> 5] = it2;
+    }
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     int off = 0, it = 0;
-    for (int e2 = 0; e2 < e; ++e2) {
-      off += cnt[e2];
-      it += (cnt[e2] + tile - 1) / tile;
+    for (int w = 0; w < 8; ++w) {
+      off += wsum[w];
+      it += wit[w];
     }
     s_off = off;
     s_base = 0;
@@ -839,7 +858,8 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
   }
 }
 
-// y = shared + sum_j g_j * y_j in top-k order, h' = bf16(h + y): one CTA per token.
+// y = shared + sum_j g_j * y_j in top-k order, h' = bf16(h + y): one CTA per
+// token and block of 256 output rows.
 __global__ void __launch_bounds__(256) k_pf_combine(const float* ys, const float* ytok, const float* gates,
                                                     const uint16_t* hin, uint16_t* hout, float* y_last, float* dbg_y,
                                                     int d, int k) {
@@ -848,7 +868,9 @@ __global__ void __launch_bounds__(256) k_pf_combine(const float* ys, const float
   if (threadIdx.x < k) g[threadIdx.x] = gates[static_cast<size_t>(t) * k + threadIdx.x];
   __syncthreads();
   const float* yt = ytok + static_cast<size_t>(t) * k * d;
-  for (int R = threadIdx.x; R < d; R += 256) {
+  {
+    const int R = blockIdx.y * 256 + threadIdx.x;
+    if (R >= d) return;
     const size_t o = static_cast<size_t>(t) * d + R;
     float y = ys[o];
     int j = 0;
@@ -933,8 +955,10 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
   }
   k_pf_logits_approx<<<dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), 256, 0, s>>>(
       x_bf, router_w, T, d, E, d / slices, approx);
-  k_pf_route<<<(T + 7) / 8, 256, 0, s>>>(x_bf, router_w, approx, xn2, wn2, xmax, wmax, bias, T, d, E, k, ids, gates, dbg_ids,
-                               dbg_gates, dbg_logits, err);
+  // tokens per CTA: eight, or fewer when that leaves SMs idle
+  const int tpc = std::max(1, std::min(8, (T + n_sm - 1) / n_sm));
+  k_pf_route<<<(T + tpc - 1) / tpc, 256, 0, s>>>(x_bf, router_w, approx, xn2, wn2, xmax, wmax, bias, T, d, E, k, ids,
+                                                 gates, dbg_ids, dbg_gates, dbg_logits, tpc, err);
   return cudaGetLastError();
 }
 
@@ -947,7 +971,7 @@ cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int tile, int32_t* 
 
 cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* gates, const uint16_t* hin,
                               uint16_t* hout, float* y_last, float* dbg_y, int T, int d, int k, cudaStream_t s) {
-  k_pf_combine<<<T, 256, 0, s>>>(ys, ytok, gates, hin, hout, y_last, dbg_y, d, k);
+  k_pf_combine<<<dim3(T, (d + 255) / 256), 256, 0, s>>>(ys, ytok, gates, hin, hout, y_last, dbg_y, d, k);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,452 @@
+// Small-batch grouped GEMVs of libmoe (sm_103a): the routed-MoE FFN of at most
+// 32 tokens, after the prefill path's routing and expert grouping.
+//
+// With a few tokens per expert every int4 weight is used once or twice, so the
+// layer is bound by reading and unpacking weights, not by multiply throughput
+// (TurboFieldfare write-up, "Splitting the work improved attention and
+// prefill": the batched routed MoE).  The tcgen05 grouped GEMM writes every
+// dequantised fp16 tile into tensor memory before it multiplies; here the
+// weights go from a shared-memory ring straight into mma.sync A fragments
+// (nibbles OR-ed under the fp16 exponent of 1024, the affine of each group
+// applied in fp32), and the tokens of an expert fill the eight B columns of
+// m16n8k16.  Two launches per layer:
+//   SG_GU  gate/up tiles (8 gate + 8 up rows over d) of the shared expert, for
+//          all T tokens, and of every active expert, for its rows of the
+//          expert-ordered token matrix: a = GELU(gate) * up rounded to fp16,
+//          written in the fragment order the down launch reads;
+//   SG_DN  down tiles: per stage the shared expert's 16-row tile over all f_s
+//          columns, or an active expert's 16-row tiles over its f columns
+//          (as many as one ring slot holds); outputs per token (shared) and per
+//          (token, top-k position) pair (routed), which the prefill combine
+//          adds in top-k order with the residual.
+// Both are persistent, as the write-up's routed-MoE kernel kept its
+// workgroups resident until the whole dispatch was done (section "MoE needed
+// parallel work, reuse, and coarse overlap"): one CTA per SM takes the shared
+// expert's stages dealt round robin and then a contiguous range of the routed
+// stages; a producer lane streams the CTA's stages into a ring of
+// shared-memory slots with 1-D bulk copies; four quads of four consumer warps
+// take them in turn (stage j to quad j mod 4).  Within a quad the warps
+// split the int4 groups of a tile and the last one to finish adds the four
+// partials in warp order (deterministic), except for routed down stages,
+// where each warp owns whole 16-row tiles.
+//
+// B operands are rows in fragment order: for each 64-element group G and lane
+// quarter t4 eight 32-bit words (k16 step st, half h) holding elements
+// 64 G + 16 st + 8 h + 2 t4 + {0, 1}, so a lane loads its fragments of one
+// group as two 16-byte words.  The group sums that the affine needs come from
+// the x rows' precomputed sums (gate/up) or from one more MMA with an all-ones
+// A operand (down: column sums of a), so no atomics enter any sum.
+#include "common.cuh"
+#include "internal.h"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kNC = 16;                       // consumer warps
+constexpr int kQW = 4;                        // warps per quad
+constexpr int kNQ = kNC / kQW;
+constexpr int kNS = 6;                        // ring slots
+constexpr int kSlotBytes = kSgMaxG * kGroupBytes;
+constexpr int kMaxNB = kSgMaxT / 8;           // blocks of eight token columns
+constexpr int kThreads = 32 * (kNC + 1);
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+struct Smem {
+  alignas(128) uint8_t ring[kNS][kSlotBytes];
+  alignas(16) float4 part[kNS][kQW][kMaxNB][32];   // per slot, warp of the quad, token block, lane
+  alignas(8) uint64_t full[kNS];
+  alignas(8) uint64_t empty[kNS];
+  int cnt[kNS];
+};
+static_assert(sizeof(Smem) + 128 <= 227 * 1024, "shared memory per CTA");
+static_assert(offsetof(Smem, ring) % 128 == 0 && kSlotBytes % 16 == 0, "bulk copy targets");
+
+enum : int { ST_GU = 0, ST_DN_SHARED = 1, ST_DN_ROUTED = 2 };
+
+struct Stage {
+  const uint8_t* src;
+  int bytes;
+  int kind;
+  int tile;       // gate/up: tile index (intermediate rows 8 tile .. + 7); down: first 16-row tile
+  int nrt;        // routed down: 16-row tiles in the stage
+  int row0;       // routed: first row of the expert in the expert-ordered matrices
+  int ntok;       // token columns
+};
+
+__device__ __forceinline__ int routed_rt(const SgParams& p) { return min(p.d / 16, kSgMaxG / (p.f / 64)); }
+
+// Stages of the launch: nS of the shared expert, then nR of the active experts.
+__device__ __forceinline__ void n_stages(const SgParams& p, int n_items, int& nS, int& nR) {
+  if (p.mode == SG_GU) {
+    nS = p.fs / 8;
+    nR = n_items * (p.f / 8);
+    return;
+  }
+  const int R = p.d / 16, rt = routed_rt(p);
+  nS = R;
+  nR = n_items * ((R + rt - 1) / rt);
+}
+
+// The CTA's stages: the shared ones dealt round robin over the CTAs (each
+// multiplies all T tokens), then a contiguous range of the routed ones, so
+// consecutive stages of a CTA mostly belong to one expert and its token rows
+// stay in the L1 cache.
+struct CtaStages {
+  int nS, G, c, n_sh, r0, n;
+  __device__ int stage(int j) const { return j < n_sh ? c + j * G : nS + r0 + (j - n_sh); }
+};
+__device__ __forceinline__ CtaStages cta_stages(const SgParams& p, int n_items) {
+  CtaStages cs;
+  int nR;
+  n_stages(p, n_items, cs.nS, nR);
+  cs.G = static_cast<int>(gridDim.x);
+  cs.c = static_cast<int>(blockIdx.x);
+  cs.n_sh = cs.c < cs.nS ? (cs.nS - cs.c + cs.G - 1) / cs.G : 0;
+  cs.r0 = static_cast<int>(static_cast<long long>(nR) * cs.c / cs.G);
+  const int r1 = static_cast<int>(static_cast<long long>(nR) * (cs.c + 1) / cs.G);
+  cs.n = cs.n_sh + (r1 - cs.r0);
+  return cs;
+}
+
+// Stage s of the launch (the same on the producer and the consumer side).
+__device__ Stage stage_of(const SgParams& p, int s) {
+  const int nGd = p.d / 64, nGf = p.f / 64, nGs = p.fs / 64;
+  Stage st;
+  st.nrt = 1;
+  if (p.mode == SG_GU) {
+    const int nS = p.fs / 8, per = p.f / 8;
+    const int tile_bytes = nGd * kGroupBytes;
+    st.kind = ST_GU;
+    st.bytes = tile_bytes;
+    if (s < nS) {
+      st.tile = s;
+      st.row0 = -1;
+      st.ntok = p.T;
+      st.src = p.shared + static_cast<size_t>(s) * tile_bytes;
+    } else {
+      const int u = (s - nS) / per;
+      st.tile = (s - nS) - u * per;
+      const int e = __ldg(&p.items[3 * u]);
+      st.row0 = __ldg(&p.items[3 * u + 1]);
+      st.ntok = __ldg(&p.items[3 * u + 2]);
+      st.src = p.experts + static_cast<long long>(e) * p.stride + static_cast<size_t>(st.tile) * tile_bytes;
+    }
+    return st;
+  }
+  const int R = p.d / 16, rt = routed_rt(p), per = (R + rt - 1) / rt;
+  if (s < R) {
+    const size_t gu_s = static_cast<size_t>(p.fs / 8) * nGd * kGroupBytes;
+    st.kind = ST_DN_SHARED;
+    st.tile = s;
+    st.row0 = -1;
+    st.ntok = p.T;
+    st.bytes = nGs * kGroupBytes;
+    st.src = p.shared + gu_s + static_cast<size_t>(s) * nGs * kGroupBytes;
+  } else {
+    const size_t gu_r = static_cast<size_t>(p.f / 8) * nGd * kGroupBytes;
+    const int u = (s - R) / per, i = (s - R) - u * per;
+    const int e = __ldg(&p.items[3 * u]);
+    st.kind = ST_DN_ROUTED;
+    st.tile = i * rt;
+    st.nrt = min(rt, R - st.tile);
+    st.row0 = __ldg(&p.items[3 * u + 1]);
+    st.ntok = __ldg(&p.items[3 * u + 2]);
+    st.bytes = st.nrt * nGf * kGroupBytes;
+    st.src = p.experts + static_cast<long long>(e) * p.stride + gu_r + static_cast<size_t>(st.tile) * nGf * kGroupBytes;
+  }
+  return st;
+}
+
+// Bounded wait on a local mbarrier phase by a whole warp (the lanes decide
+// together); false after about two seconds, with the error word flagged.
+__device__ bool wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(kFull, clock64() - t0 > kSpinLimitCycles)) {
+      if ((threadIdx.x & 31) == 0) atomicOr(err, ERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Groups [G0, G1) of 16 weight rows (the slot block `blk`, one 576-byte block
+// per group) times token columns nb * 8 .. nb * 8 + 7 of the B rows: `brow` is
+// this lane's column (fragment order; null past the last token).  Returns the
+// lane's four sums: (row g, column 2 t4), (row g, 2 t4 + 1), (row g + 8, 2 t4),
+// (row g + 8, 2 t4 + 1), each s P + (b - 1024 s) X for the rows held as
+// 1024 + q, (s / 16) P + (b - 64 s) X for those held as 1024 + 16 q, X the
+// column's group sum: read from xg0 / xg1 (the two columns' rows of group
+// sums, null past the last token), or with kOnesSum from an MMA of the B
+// columns with an all-ones A operand.
+template <bool kOnesSum>
+__device__ __forceinline__ float4 tile_dot(const uint8_t* blk, int G0, int G1, const uint4* brow, const float* xg0,
+                                           const float* xg1) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+  const uint32_t one[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};   // fp16 1.0 pairs
+  // the operands of group G + 1 (global loads) are in flight while group G multiplies
+  auto load_b = [&](int G, uint4& b01, uint4& b23, float& X0, float& X1) {
+    b01 = make_uint4(0u, 0u, 0u, 0u);
+    b23 = make_uint4(0u, 0u, 0u, 0u);
+    if (brow && G < G1) {
+      const uint4* src = brow + (G * 4 + t4) * 2;
+      b01 = __ldg(src);
+      b23 = __ldg(src + 1);
+    }
+    if (!kOnesSum) {
+      X0 = xg0 && G < G1 ? __ldg(xg0 + G) : 0.f;
+      X1 = xg1 && G < G1 ? __ldg(xg1 + G) : 0.f;
+    }
+  };
+  uint4 x01, x23;
+  float X0 = 0.f, X1 = 0.f;
+  load_b(G0, x01, x23, X0, X1);
+  for (int G = G0; G < G1; ++G) {
+    uint4 n01, n23;
+    float nX0 = 0.f, nX1 = 0.f;
+    load_b(G + 1, n01, n23, nX0, nX1);
+    const uint8_t* b = blk + static_cast<size_t>(G - G0) * kGroupBytes;
+    const uint4 q = *reinterpret_cast<const uint4*>(b + lane * 16);
+    const uint2 sbv = *reinterpret_cast<const uint2*>(b + kFragBytes + g * 8);
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t a[4];
+    nibbles_to_f16x2(q.x, a);
+    mma_f16(c0, a, x01.x, x01.y);
+    nibbles_to_f16x2(q.y, a);
+    mma_f16(c1, a, x01.z, x01.w);
+    nibbles_to_f16x2(q.z, a);
+    mma_f16(c0, a, x23.x, x23.y);
+    nibbles_to_f16x2(q.w, a);
+    mma_f16(c1, a, x23.z, x23.w);
+    if (kOnesSum) {
+      float cs[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16(cs, one, x01.x, x01.y);
+      mma_f16(cs, one, x01.z, x01.w);
+      mma_f16(cs, one, x23.x, x23.y);
+      mma_f16(cs, one, x23.z, x23.w);
+      X0 = cs[0];
+      X1 = cs[1];
+    }
+    const float sA = half_lo(sbv.x), oA = half_hi(sbv.x), sB = half_lo(sbv.y), oB = half_hi(sbv.y);
+    const float bA = fmaf(-1024.f, sA, oA), bB = fmaf(-64.f, sB, oB), sB16 = sB * 0.0625f;
+    r0 += sA * (c0[0] + c1[0]) + bA * X0;
+    r1 += sA * (c0[1] + c1[1]) + bA * X1;
+    r2 += sB16 * (c0[2] + c1[2]) + bB * X0;
+    r3 += sB16 * (c0[3] + c1[3]) + bB * X1;
+    x01 = n01;
+    x23 = n23;
+    X0 = nX0;
+    X1 = nX1;
+  }
+  return make_float4(r0, r1, r2, r3);
+}
+
+__device__ __forceinline__ float gelu_of(float v, int variant) {
+  if (variant == 1) return 0.5f * v * (1.f + tanhf(0.7978845608028654f * (v + 0.044715f * v * v * v)));
+  return 0.5f * v * (1.f + erff(v * 0.7071067811865476f));
+}
+
+// Position (fp16 elements) of element i of a row in fragment order.
+__device__ __forceinline__ int frag_pos(int i) {
+  const int G = i >> 6, w = i & 63, st = w >> 4, h = (w >> 3) & 1, t4 = (w & 7) >> 1;
+  return ((((G * 4 + t4) * 4 + st) * 2 + h) << 1) | (w & 1);
+}
+
+// A stage whose int4 groups the quad's warps split (gate/up tiles and shared
+// down tiles): warp qw takes groups [qw * cg, (qw + 1) * cg) for every block of
+// eight token columns, the last warp to finish adds the partials in warp order
+// and writes the results.
+__device__ void stage_split(const SgParams& p, Smem& S, int slot, const Stage& st, int qw) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const bool gu = st.kind == ST_GU;
+  const int nG = gu ? p.d / 64 : p.fs / 64;
+  const int cg = (nG + kQW - 1) / kQW, G0 = min(nG, qw * cg), G1 = min(nG, G0 + cg);
+  const int nbu = (st.ntok + 7) >> 3;
+  const uint8_t* blk = S.ring[slot] + static_cast<size_t>(G0) * kGroupBytes;
+  // B rows: gate/up: x (expert-ordered rows, then the shared expert's token rows at P); down: the shared a rows
+  const int vlen = gu ? p.d : p.fs;
+  const int rbase = gu ? (st.row0 >= 0 ? st.row0 : p.P) : 0;
+  const uint16_t* bbase = gu ? p.xv : p.av_s;
+  for (int nb = 0; nb < nbu; ++nb) {
+    const int col = nb * 8 + g, c0 = nb * 8 + 2 * t4, c1 = c0 + 1;
+    const uint4* brow = col < st.ntok ? reinterpret_cast<const uint4*>(bbase + static_cast<size_t>(rbase + col) * vlen)
+                                      : nullptr;
+    float4 r;
+    if (gu) {
+      const int nGd = p.d / 64;
+      const float* x0 = c0 < st.ntok ? p.xg + static_cast<size_t>(rbase + c0) * nGd : nullptr;
+      const float* x1 = c1 < st.ntok ? p.xg + static_cast<size_t>(rbase + c1) * nGd : nullptr;
+      r = tile_dot<false>(blk, G0, G1, brow, x0, x1);
+    } else {
+      r = tile_dot<true>(blk, G0, G1, brow, nullptr, nullptr);
+    }
+    S.part[slot][qw][nb][lane] = r;
+  }
+  __threadfence_block();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(&S.cnt[slot], 1) == kQW - 1;
+  last = __shfl_sync(kFull, last, 0);
+  if (!last) return;
+  __threadfence_block();
+  for (int nb = 0; nb < nbu; ++nb) {
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < kQW; ++w) {
+      const volatile float* v = reinterpret_cast<const volatile float*>(&S.part[slot][w][nb][lane]);
+      r.x += v[0];
+      r.y += v[1];
+      r.z += v[2];
+      r.w += v[3];
+    }
+    const int c0 = nb * 8 + 2 * t4;
+    if (gu) {
+      // gate row g (r.x, r.y) and up row g (r.z, r.w) of intermediate row 8 tile + g, columns c0 and c0 + 1
+      const int i = 8 * st.tile + g, F = st.row0 >= 0 ? p.f : p.fs;
+      uint16_t* av = st.row0 >= 0 ? p.av_r + static_cast<size_t>(st.row0) * p.f : p.av_s;
+      const float a0 = gelu_of(r.x, p.gelu) * r.z, a1 = gelu_of(r.y, p.gelu) * r.w;
+      const bool v0 = c0 < st.ntok, v1 = c0 + 1 < st.ntok;
+      if ((v0 && !(fabsf(a0) < 65504.f)) || (v1 && !(fabsf(a1) < 65504.f))) atomicOr(p.err, ERR_PF_RANGE);
+      const int pos = frag_pos(i);
+      if (v0) av[static_cast<size_t>(c0) * F + pos] = __half_as_ushort(__float2half_rn(a0));
+      if (v1) av[static_cast<size_t>(c0 + 1) * F + pos] = __half_as_ushort(__float2half_rn(a1));
+    } else {
+      const int row = 16 * st.tile + g;
+      if (c0 < st.ntok) {
+        p.y_s[static_cast<size_t>(c0) * p.d + row] = r.x;
+        p.y_s[static_cast<size_t>(c0) * p.d + row + 8] = r.z;
+      }
+      if (c0 + 1 < st.ntok) {
+        p.y_s[static_cast<size_t>(c0 + 1) * p.d + row] = r.y;
+        p.y_s[static_cast<size_t>(c0 + 1) * p.d + row + 8] = r.w;
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) S.cnt[slot] = 0;
+}
+
+// Routed down stage: warp qw owns the stage's 16-row tiles qw, qw + 4, ...
+// over all f/64 groups; outputs go to the rows of the tokens' pairs.
+__device__ void stage_down_routed(const SgParams& p, Smem& S, int slot, const Stage& st, int qw) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int nGf = p.f / 64, nbu = (st.ntok + 7) >> 3;
+  for (int j = qw; j < st.nrt; j += kQW) {
+    const uint8_t* blk = S.ring[slot] + static_cast<size_t>(j) * nGf * kGroupBytes;
+    const int row = 16 * (st.tile + j) + g;
+    for (int nb = 0; nb < nbu; ++nb) {
+      const int col = nb * 8 + g, c0 = nb * 8 + 2 * t4;
+      const uint4* brow =
+          col < st.ntok ? reinterpret_cast<const uint4*>(p.av_r + static_cast<size_t>(st.row0 + col) * p.f) : nullptr;
+      const float4 r = tile_dot<true>(blk, 0, nGf, brow, nullptr, nullptr);
+      if (c0 < st.ntok) {
+        float* y = p.y_r + static_cast<size_t>(__ldg(&p.row_pair[st.row0 + c0])) * p.d;
+        y[row] = r.x;
+        y[row + 8] = r.z;
+      }
+      if (c0 + 1 < st.ntok) {
+        float* y = p.y_r + static_cast<size_t>(__ldg(&p.row_pair[st.row0 + c0 + 1])) * p.d;
+        y[row] = r.y;
+        y[row + 8] = r.w;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_small_batch(SgParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the ring at a 128-byte boundary (the allocation has 128 bytes to spare)
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], kQW);
+      S.cnt[i] = 0;
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const CtaStages cs = cta_stages(p, *p.n_items);
+  if (warp == kNC) {
+    // producer: the CTA's stages j = 0, 1, ... in order
+    if (lane != 0) return;
+    int j = 0;
+    for (; j < cs.n; ++j) {
+      const int slot = j % kNS;
+      if (!mbar_wait_bounded(&S.empty[slot], ((j / kNS) & 1u) ^ 1u, p.err)) break;
+      const Stage st = stage_of(p, cs.stage(j));
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(st.bytes));
+      bulk_g2s(S.ring[slot], st.src, static_cast<uint32_t>(st.bytes), &S.full[slot]);
+    }
+    // copies still in flight complete before the CTA leaves (bounded)
+    for (int v = max(0, j - kNS); v < j; ++v) mbar_wait_bounded(&S.full[v % kNS], (v / kNS) & 1u, p.err);
+    return;
+  }
+  const int quad = warp / kQW, qw = warp % kQW;
+  for (int j = quad; j < cs.n; j += kNQ) {
+    const int slot = j % kNS;
+    if (!wait_warp(&S.full[slot], (j / kNS) & 1u, p.err)) return;
+    const Stage st = stage_of(p, cs.stage(j));
+    if (st.kind == ST_DN_ROUTED) stage_down_routed(p, S, slot, st, qw);
+    else stage_split(p, S, slot, st, qw);
+    __syncwarp();
+    if (lane == 0) mbarrier_arrive(&S.empty[slot]);
+  }
+}
+
+// Row r < P: x of expert-ordered row r's token; row P + t: token t.  From the
+// bf16 rows of x to fp16 (exact unless |x| < 2^-14) in fragment order, with the
+// fp32 sum of each 64-element group.
+__global__ void __launch_bounds__(256) k_sg_gather(const uint16_t* x_bf, const int32_t* row_pair, int P, int d, int k,
+                                                   uint16_t* xv, float* xg) {
+  const int r = blockIdx.x;
+  const int t = r < P ? row_pair[r] / k : r - P;
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(x_bf + static_cast<size_t>(t) * d);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(xv + static_cast<size_t>(r) * d);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nG = d / 64;
+  // lane holds elements 64 G + 2 lane, + 1: k16 step lane / 8, half (lane / 4) % 2, quarter lane % 4
+  const int st = lane >> 3, h = (lane >> 2) & 1, t4 = lane & 3;
+  for (int Gi = warp; Gi < nG; Gi += 8) {
+    const uint32_t v = src[32 * Gi + lane];
+    const __half a = __float2half_rn(bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu)));
+    const __half b = __float2half_rn(bf16_bits_to_float(static_cast<uint16_t>(v >> 16)));
+    dst[((Gi * 4 + t4) * 4 + st) * 2 + h] =
+        static_cast<uint32_t>(__half_as_ushort(a)) | (static_cast<uint32_t>(__half_as_ushort(b)) << 16);
+    float sum = __half2float(a) + __half2float(b);
+#pragma unroll
+    for (int m = 16; m; m >>= 1) sum += __shfl_xor_sync(kFull, sum, m);
+    if (lane == 0) xg[static_cast<size_t>(r) * nG + Gi] = sum;
+  }
+}
+
+}  // namespace
+
+bool sg_shape_ok(int d, int f, int fs) {
+  return d % 64 == 0 && f % 64 == 0 && fs % 64 == 0 && d / 64 <= kSgMaxG && fs / 64 <= kSgMaxG &&
+         f / 64 <= kSgMaxG && d >= 16;
+}
+
+size_t sg_smem() { return sizeof(Smem) + 128; }
+
+cudaError_t sg_set_attrs() {
+  return cudaFuncSetAttribute((const void*)k_small_batch, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(sg_smem()));
+}
+
+cudaError_t launch_sg_gather(const uint16_t* x_bf, const int32_t* row_pair, int P, int T, int d, int k, uint16_t* xv,
+                             float* xg, cudaStream_t s) {
+  k_sg_gather<<<P + T, 256, 0, s>>>(x_bf, row_pair, P, d, k, xv, xg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sg(const SgParams& p, int n_sm, cudaStream_t s) {
+  k_small_batch<<<n_sm, kThreads, sg_smem(), s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

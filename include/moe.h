@@ -423,7 +423,9 @@ moe_status moe_route_noalloc(const moe_config *cfg, const uint16_t *router_w, co
  * 1 gate/up GEMV, 2 down GEMV + combine, 3 persistent one-token decode
  * (all layers), 4 prefill routing and grouping (norm, router, expert
  * grouping, gather; one pair of events per layer), 5 prefill GEMMs (the four
- * tcgen05 GEMMs of one layer), 6 prefill combine. */
+ * tcgen05 GEMMs of one layer), 6 prefill combine, 7 small-batch grouped GEMVs
+ * (the gate/up and the down launch of one layer of a call of at most 32
+ * tokens). */
 typedef struct {
     int64_t launches;
     double total_ms;
@@ -455,9 +457,10 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
  * 2 n_layers) steps of the first routed CTA; with 2 * n_layers + gridDim.x
  * rows also per-CTA times of the third layer (see persistent.cu).
  * hook 4, 7 or 9 with a value selecting a kernel path that cannot run on the
- * configuration returns MOE_ESTATE.  hook 7: the tcgen05 path for prefill and for
- * decode steps of 16 or more tokens on (value != 0, the default when the
- * shape allows it) or off (batched decode kernels).
+ * configuration returns MOE_ESTATE.  hook 7: the grouped path (routing and
+ * expert grouping, then tcgen05 GEMMs or small-batch GEMVs) for prefill and for
+ * batched decode steps on (value != 0, the default when the shape allows it)
+ * or off (per-layer batched decode kernels).
  * hook 8: `value` is a caller device buffer of 4 * 16 uint64 receiving event
  * times of CTA (0, 0) of each prefill GEMM of the first layer of a call, or
  * 0 to stop.  hook 10: every bounded device wait of the two persistent
@@ -472,6 +475,11 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
  * writes the clustered kernel's wait diagnostic into the host uint32 at
  * address `value` and clears it: 0 if no wait ran out, else (site << 16) |
  * CTA of the first wait that did (sites are listed in decode_cluster.cu).
+ * hook 13: decode steps of 2 to 32 tokens and prefill calls of at most 32
+ * tokens run their matrix products as small-batch grouped GEMVs (value != 0,
+ * the default when the shape allows it) or as the tcgen05 GEMMs (decode: from
+ * 16 tokens on, else the per-layer GEMVs); MOE_ESTATE when asked for where
+ * they cannot run.
  * Other hooks: MOE_EINVAL. */
 moe_status moe_test_hook(moe_ctx *ctx, int hook, int64_t value);
 

@@ -42,8 +42,8 @@ def _check_layer_outputs(ctx, lay, H, bias=None):
         assert st == 0
         assert list(ids[0, b].cpu().numpy()) == list(rid), f"token {b}: ids {ids[0, b].tolist()} vs {list(rid)}"
         assert np.allclose(gs[0, b].cpu().numpy(), rg, rtol=GATE_RTOL, atol=1e-7)
-        # the tensor-core path (16 tokens and up) evaluates only the candidates exactly
-        check_logits(lgs[b], rlg, rid, f"token {b}", candidates_only=B >= 16)
+        # the grouped path (batches) evaluates only the candidates exactly
+        check_logits(lgs[b], rlg, rid, f"token {b}", candidates_only=B >= 2)
         worst = max(worst, assert_ffn_close(y[b].cpu().numpy(), ry, f"token {b}"))
         # residual: h_out = bf16(h + y) from the GPU's own y
         ref_h = oracle.residual_bf16(oracle.as_bits(H[b]), y[b].cpu().double().numpy())
@@ -71,10 +71,20 @@ def test_tiny_layer_single_tokens(kernel):
             _check_layer_outputs(ctx, lay, H[t:t + 1])
 
 
+def use_batch_path(ctx, path):
+    """small: small-batch grouped GEMVs (the default); tc: tcgen05 GEMMs from
+    16 tokens on, per-layer GEMVs below; gemv: per-layer GEMVs."""
+    moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PREFILL_TC, 0 if path == "gemv" else 1), ctx.h)
+    if path != "gemv":
+        moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_SMALL_BATCH, 1 if path == "small" else 0), ctx.h)
+
+
+@pytest.mark.parametrize("path", ["small", "tc", "gemv"])
 @pytest.mark.parametrize("B", [2, 3, 8, 9, 31, 32])
-def test_tiny_layer_batched(B):
+def test_tiny_layer_batched(B, path):
     ctx, lay = _tiny_ctx()
     with ctx:
+        use_batch_path(ctx, path)
         H = gen_hidden(B, TINY.d, seed=100 + B).cuda()
         _check_layer_outputs(ctx, lay, H)
 
@@ -119,16 +129,20 @@ def test_odd_shapes_and_uneven_shared_chunks():
             _check_layer_outputs(ctx, lay, H[t:t + 1])
 
 
-def test_long_rows_several_stages_per_task():
-    # d/64 = 24 groups (gate/up tiles span 3 stages), f/64 = 13 (down tiles span 2 stages),
+@pytest.mark.parametrize("path", ["small", "gemv"])
+def test_long_rows_several_stages_per_task(path):
+    # d/64 = 24 groups (gate/up tiles span 3 stages), f/64 = 13 (down tiles span 2 stages;
+    # small-batch routed down stages of three 16-row tiles, the last stage short),
     # f_shared/64 = 23 (three shared down chunks, the last one short)
     sh = Shape(d=1536, f=832, f_shared=1472, n_experts=16, top_k=4)
     ctx, lay = _tiny_ctx(sh, seed=23)
     with ctx:
-        H = gen_hidden(4, sh.d, seed=23).cuda()
+        use_batch_path(ctx, path)
+        H = gen_hidden(20, sh.d, seed=23).cuda()
         for t in range(4):
             _check_layer_outputs(ctx, lay, H[t:t + 1])
-        _check_layer_outputs(ctx, lay, H)
+        _check_layer_outputs(ctx, lay, H[:4])
+        _check_layer_outputs(ctx, lay, H)      # up to 20 tokens on an expert: three token blocks
 
 
 def test_router_ties_go_to_lower_index():
@@ -272,13 +286,16 @@ def test_c1_thousand_tokens_through_the_clustered_kernel():
             worst = max(worst, assert_ffn_close(y[t], ry, f"token {t}"))
 
 
-def test_full_shape_batch32_tensor_core_path():
-    """32 tokens at full shape take the tensor-core grouped GEMM path (32-row
-    token tiles over 44 k-groups): every token's ids, gates, candidate logits
-    and FFN output on two layers against the oracle."""
+@pytest.mark.parametrize("path", ["small", "tc"])
+def test_full_shape_batch32_grouped_paths(path):
+    """32 tokens at full shape on the grouped path, with the small-batch GEMVs
+    (one item per active expert, 44 k-groups per gate/up tile) or the tcgen05
+    GEMMs (32-row token tiles): every token's ids, gates, candidate logits and
+    FFN output on two layers against the oracle."""
     sh, L, B = FULL, 2, 32
     oracle.set_threads(os.cpu_count())
     with Ctx(sh, n_layers=L, prenorm=1) as ctx:
+        use_batch_path(ctx, path)
         hosts = []
         for l in range(L):
             wd = gen_layer(sh, seed=12, layer=l, device="cuda")

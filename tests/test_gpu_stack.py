@@ -23,7 +23,7 @@ def _check_stack(ctx, weights_host, H, L, ffn_layers, bias=None, ffn_tokens=None
     end_capture(ctx)
     assert torch.equal(y_last, cap["y"][L - 1])
     check_stack(weights_host, H, cap, h_out, ctx.shape.top_k, ffn_layers, ffn_tokens, bias,
-                candidates_only=B >= 16)
+                candidates_only=B >= 2)
 
 
 @pytest.mark.parametrize("kernel", DECODE_KERNELS)
