@@ -799,7 +799,7 @@ def run_ours_batched(args):
     launches_per_step = sum(v["launches"] for v in kinds.values()) / 4
     dom = max(kinds, key=lambda k: kinds[k]["ms"])
     g = kinds[dom]
-    if dom == "prefill_tcgen05_gemm":      # the four grouped GEMMs of a layer read all of its weights
+    if dom in ("prefill_tcgen05_gemm", "small_batch_gemv"):   # a layer's GEMMs / GEMV pair read all its weights
         dom_bytes = step_bytes / N_LAYERS
     elif dom == "gateup_gelu_gemv":        # gate + up are two thirds of each expert's bytes
         dom_bytes = step_bytes * 2 / 3 / N_LAYERS
@@ -840,6 +840,7 @@ def run_ours_batched(args):
             "config": {"workload": f"batched{BATCH}_decode{N_LAYERS}_resident", "layers": N_LAYERS, "B": BATCH,
                        "d": sh.d, "f": sh.f, "f_shared": sh.f_shared, "experts": sh.n_experts, "top_k": sh.top_k,
                        "unique_experts_per_layer_mean": float(np.mean(U)), "bytes_per_step": step_bytes,
+                       "matrix_path": "small-batch grouped GEMVs: int4 -> fp16 mma.sync from a bulk-copy ring",
                        "l2": "no flush: 11.6 GB of weights per step vs 129 MB L2"},
             "hbm_roofline_frac_measured": value / ws / BATCH * step_bytes / (peak * 1e9),
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,

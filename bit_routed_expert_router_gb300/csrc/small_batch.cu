@@ -48,14 +48,25 @@ constexpr int kNC = 16;                       // consumer warps
 constexpr int kQW = 4;                        // warps per quad
 constexpr int kNQ = kNC / kQW;
 constexpr int kNS = 6;                        // ring slots
+constexpr int kXcBytes = 12 * 64 * kSgMaxG * 2; // B-row cache: twelve x rows of d = 2816 (or more, shorter rows)
+constexpr int kXcItems = 8;                   // experts the cache holds rows of
 constexpr int kSlotBytes = kSgMaxG * kGroupBytes;
 constexpr int kMaxNB = kSgMaxT / 8;           // blocks of eight token columns
 constexpr int kThreads = 32 * (kNC + 1);
 constexpr unsigned kFull = 0xFFFFFFFFu;
+#ifndef SG_UNROLL
+#define SG_UNROLL 2
+#endif
+constexpr int kUnroll = SG_UNROLL;            // int4 groups a warp's loop keeps in flight
 
 struct Smem {
   alignas(128) uint8_t ring[kNS][kSlotBytes];
-  alignas(16) float4 part[kNS][kQW][kMaxNB][32];   // per slot, warp of the quad, token block, lane
+  alignas(128) uint8_t xc[kXcBytes];            // B rows (and, gate/up, their group sums) of the CTA's experts
+  alignas(16) float xcg[kXcBytes / 128];        // group sums of cached x rows (one float per 64 fp16)
+  alignas(8) uint64_t xbar;                     // the cache is filled
+  int xc_item[kXcItems];                        // routed item whose rows the cache holds
+  int xc_off[kXcItems];                         // their byte offset in xc (row r of the item at + r * row bytes)
+  int n_xc;
   alignas(8) uint64_t full[kNS];
   alignas(8) uint64_t empty[kNS];
   int cnt[kNS];
@@ -73,6 +84,7 @@ struct Stage {
   int nrt;        // routed down: 16-row tiles in the stage
   int row0;       // routed: first row of the expert in the expert-ordered matrices
   int ntok;       // token columns
+  int item;       // routed: the item (active expert) index
 };
 
 __device__ __forceinline__ int routed_rt(const SgParams& p) { return min(p.d / 16, kSgMaxG / (p.f / 64)); }
@@ -115,6 +127,7 @@ __device__ Stage stage_of(const SgParams& p, int s) {
   const int nGd = p.d / 64, nGf = p.f / 64, nGs = p.fs / 64;
   Stage st;
   st.nrt = 1;
+  st.item = -1;
   if (p.mode == SG_GU) {
     const int nS = p.fs / 8, per = p.f / 8;
     const int tile_bytes = nGd * kGroupBytes;
@@ -127,6 +140,7 @@ __device__ Stage stage_of(const SgParams& p, int s) {
       st.src = p.shared + static_cast<size_t>(s) * tile_bytes;
     } else {
       const int u = (s - nS) / per;
+      st.item = u;
       st.tile = (s - nS) - u * per;
       const int e = __ldg(&p.items[3 * u]);
       st.row0 = __ldg(&p.items[3 * u + 1]);
@@ -147,6 +161,7 @@ __device__ Stage stage_of(const SgParams& p, int s) {
   } else {
     const size_t gu_r = static_cast<size_t>(p.f / 8) * nGd * kGroupBytes;
     const int u = (s - R) / per, i = (s - R) - u * per;
+    st.item = u;
     const int e = __ldg(&p.items[3 * u]);
     st.kind = ST_DN_ROUTED;
     st.tile = i * rt;
@@ -173,63 +188,72 @@ __device__ bool wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err) {
   }
 }
 
-// Groups [G0, G1) of 16 weight rows (the slot block `blk`, one 576-byte block
-// per group) times token columns nb * 8 .. nb * 8 + 7 of the B rows: `brow` is
-// this lane's column (fragment order; null past the last token).  Returns the
-// lane's four sums: (row g, column 2 t4), (row g, 2 t4 + 1), (row g + 8, 2 t4),
+// Groups [G0, G1) of 16 weight rows (`blk`: the slot block of group G0, one
+// 576-byte block per group) times eight token columns of the B rows: `brow` is
+// this lane's column (fragment order), `xg0` / `xg1` the rows of group sums of
+// the lane's two accumulator columns 2 t4, 2 t4 + 1.  Columns past the last
+// token repeat a valid row; their results are never used.  Returns the lane's
+// sums (row g, column 2 t4), (row g, 2 t4 + 1), (row g + 8, 2 t4),
 // (row g + 8, 2 t4 + 1), each s P + (b - 1024 s) X for the rows held as
-// 1024 + q, (s / 16) P + (b - 64 s) X for those held as 1024 + 16 q, X the
-// column's group sum: read from xg0 / xg1 (the two columns' rows of group
-// sums, null past the last token), or with kOnesSum from an MMA of the B
-// columns with an all-ones A operand.
-template <bool kOnesSum>
+// 1024 + q and (s / 16) P + (b - 64 s) X for those held as 1024 + 16 q, X the
+// column's group sum: from xg, or with kOnesSum from an MMA of the B columns
+// with an all-ones A operand.  kSmemB: the B rows and sums are in this CTA's
+// cache in shared memory (else global memory, read through the L1 cache).
+// m16n8k16 fp16 MMA without the volatile qualifier, so the compiler may
+// interleave the MMAs of several groups.
+__device__ __forceinline__ void mma16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// The same with a zero accumulator in (one zero register for all four inputs).
+__device__ __forceinline__ void mma16z(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  const float z = 0.f;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+}
+
+template <bool kOnesSum, bool kSmemB>
 __device__ __forceinline__ float4 tile_dot(const uint8_t* blk, int G0, int G1, const uint4* brow, const float* xg0,
                                            const float* xg1) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
   const uint32_t one[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};   // fp16 1.0 pairs
-  // the operands of group G + 1 (global loads) are in flight while group G multiplies
-  auto load_b = [&](int G, uint4& b01, uint4& b23, float& X0, float& X1) {
-    b01 = make_uint4(0u, 0u, 0u, 0u);
-    b23 = make_uint4(0u, 0u, 0u, 0u);
-    if (brow && G < G1) {
-      const uint4* src = brow + (G * 4 + t4) * 2;
-      b01 = __ldg(src);
-      b23 = __ldg(src + 1);
-    }
-    if (!kOnesSum) {
-      X0 = xg0 && G < G1 ? __ldg(xg0 + G) : 0.f;
-      X1 = xg1 && G < G1 ? __ldg(xg1 + G) : 0.f;
-    }
-  };
-  uint4 x01, x23;
-  float X0 = 0.f, X1 = 0.f;
-  load_b(G0, x01, x23, X0, X1);
+  const uint8_t* wq = blk + lane * 16;
+  const uint8_t* ws = blk + kFragBytes + g * 8;
+  const uint4* bp = brow + (G0 * 4 + t4) * 2;
+#pragma unroll kUnroll
   for (int G = G0; G < G1; ++G) {
-    uint4 n01, n23;
-    float nX0 = 0.f, nX1 = 0.f;
-    load_b(G + 1, n01, n23, nX0, nX1);
-    const uint8_t* b = blk + static_cast<size_t>(G - G0) * kGroupBytes;
-    const uint4 q = *reinterpret_cast<const uint4*>(b + lane * 16);
-    const uint2 sbv = *reinterpret_cast<const uint2*>(b + kFragBytes + g * 8);
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint4 q = *reinterpret_cast<const uint4*>(wq);
+    const uint2 sbv = *reinterpret_cast<const uint2*>(ws);
+    const uint4 x01 = kSmemB ? bp[0] : __ldg(bp), x23 = kSmemB ? bp[1] : __ldg(bp + 1);
+    wq += kGroupBytes;
+    ws += kGroupBytes;
+    bp += 8;
+    float X0 = 0.f, X1 = 0.f;
+    if (!kOnesSum) {
+      X0 = kSmemB ? xg0[G] : __ldg(xg0 + G);
+      X1 = kSmemB ? xg1[G] : __ldg(xg1 + G);
+    }
+    float c0[4], c1[4];
     uint32_t a[4];
     nibbles_to_f16x2(q.x, a);
-    mma_f16(c0, a, x01.x, x01.y);
+    mma16z(c0, a, x01.x, x01.y);
     nibbles_to_f16x2(q.y, a);
-    mma_f16(c1, a, x01.z, x01.w);
+    mma16z(c1, a, x01.z, x01.w);
     nibbles_to_f16x2(q.z, a);
-    mma_f16(c0, a, x23.x, x23.y);
+    mma16(c0, a, x23.x, x23.y);
     nibbles_to_f16x2(q.w, a);
-    mma_f16(c1, a, x23.z, x23.w);
-    if (kOnesSum) {
-      float cs[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_f16(cs, one, x01.x, x01.y);
-      mma_f16(cs, one, x01.z, x01.w);
-      mma_f16(cs, one, x23.x, x23.y);
-      mma_f16(cs, one, x23.z, x23.w);
-      X0 = cs[0];
-      X1 = cs[1];
+    mma16(c1, a, x23.z, x23.w);
+    if (kOnesSum) {   // column sums of B: two chains of two MMAs
+      float s0[4], s1[4];
+      mma16z(s0, one, x01.x, x01.y);
+      mma16z(s1, one, x01.z, x01.w);
+      mma16(s0, one, x23.x, x23.y);
+      mma16(s1, one, x23.z, x23.w);
+      X0 = s0[0] + s1[0];
+      X1 = s0[1] + s1[1];
     }
     const float sA = half_lo(sbv.x), oA = half_hi(sbv.x), sB = half_lo(sbv.y), oB = half_hi(sbv.y);
     const float bA = fmaf(-1024.f, sA, oA), bB = fmaf(-64.f, sB, oB), sB16 = sB * 0.0625f;
@@ -237,10 +261,6 @@ __device__ __forceinline__ float4 tile_dot(const uint8_t* blk, int G0, int G1, c
     r1 += sA * (c0[1] + c1[1]) + bA * X1;
     r2 += sB16 * (c0[2] + c1[2]) + bB * X0;
     r3 += sB16 * (c0[3] + c1[3]) + bB * X1;
-    x01 = n01;
-    x23 = n23;
-    X0 = nX0;
-    X1 = nX1;
   }
   return make_float4(r0, r1, r2, r3);
 }
@@ -254,6 +274,26 @@ __device__ __forceinline__ float gelu_of(float v, int variant) {
 __device__ __forceinline__ int frag_pos(int i) {
   const int G = i >> 6, w = i & 63, st = w >> 4, h = (w >> 3) & 1, t4 = (w & 7) >> 1;
   return ((((G * 4 + t4) * 4 + st) * 2 + h) << 1) | (w & 1);
+}
+
+// Where warp qw of the quad leaves its partial sums of token block nb (32
+// lanes x float4) in the slot it has multiplied: behind the stage's weights
+// when the slot has room there for every warp's blocks, else inside the
+// warp's own groups (then at least six, 3,456 bytes), which only this warp
+// reads and has finished reading.
+constexpr int kPartBytes = 32 * 16;
+__device__ __forceinline__ float4* part_at(Smem& S, int slot, int nG, int G0, int qw, int nb) {
+  uint8_t* base = S.ring[slot];
+  if (nG * kGroupBytes + kQW * kMaxNB * kPartBytes <= kSlotBytes)
+    return reinterpret_cast<float4*>(base + kSlotBytes - kQW * kMaxNB * kPartBytes + (qw * kMaxNB + nb) * kPartBytes);
+  return reinterpret_cast<float4*>(base + static_cast<size_t>(G0) * kGroupBytes + nb * kPartBytes);
+}
+
+// Byte offset of routed item u's B rows in the CTA's cache, or -1.
+__device__ __forceinline__ int xc_find(const Smem& S, int u) {
+  for (int i = 0; i < S.n_xc; ++i)
+    if (S.xc_item[i] == u) return S.xc_off[i];
+  return -1;
 }
 
 // A stage whose int4 groups the quad's warps split (gate/up tiles and shared
@@ -271,21 +311,39 @@ __device__ void stage_split(const SgParams& p, Smem& S, int slot, const Stage& s
   const int vlen = gu ? p.d : p.fs;
   const int rbase = gu ? (st.row0 >= 0 ? st.row0 : p.P) : 0;
   const uint16_t* bbase = gu ? p.xv : p.av_s;
-  for (int nb = 0; nb < nbu; ++nb) {
-    const int col = nb * 8 + g, c0 = nb * 8 + 2 * t4, c1 = c0 + 1;
-    const uint4* brow = col < st.ntok ? reinterpret_cast<const uint4*>(bbase + static_cast<size_t>(rbase + col) * vlen)
-                                      : nullptr;
-    float4 r;
+  const int xoff = gu && st.row0 >= 0 ? xc_find(S, st.item) : -1;
+  float4 rr[kMaxNB];
+#pragma unroll
+  for (int nb = 0; nb < kMaxNB; ++nb) {
+    rr[nb] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (nb >= nbu) continue;
+    // columns past the last token repeat its row (their results are not used)
+    const int last_col = st.ntok - 1;
+    const int col = min(nb * 8 + g, last_col), c0 = min(nb * 8 + 2 * t4, last_col), c1 = min(c0 + 1, last_col);
+    if (xoff >= 0) {   // routed gate/up with its x rows (and sums) in the cache
+      const int rb = p.d * 2;
+      const uint4* brow = reinterpret_cast<const uint4*>(S.xc + xoff + col * rb);
+      const float* x0 = S.xcg + (xoff + c0 * rb) / 128;
+      const float* x1 = S.xcg + (xoff + c1 * rb) / 128;
+      rr[nb] = tile_dot<false, true>(blk, G0, G1, brow, x0, x1);
+      continue;
+    }
+    const uint4* brow = reinterpret_cast<const uint4*>(bbase + static_cast<size_t>(rbase + col) * vlen);
     if (gu) {
       const int nGd = p.d / 64;
-      const float* x0 = c0 < st.ntok ? p.xg + static_cast<size_t>(rbase + c0) * nGd : nullptr;
-      const float* x1 = c1 < st.ntok ? p.xg + static_cast<size_t>(rbase + c1) * nGd : nullptr;
-      r = tile_dot<false>(blk, G0, G1, brow, x0, x1);
+      const float* x0 = p.xg + static_cast<size_t>(rbase + c0) * nGd;
+      const float* x1 = p.xg + static_cast<size_t>(rbase + c1) * nGd;
+      rr[nb] = tile_dot<false, false>(blk, G0, G1, brow, x0, x1);
     } else {
-      r = tile_dot<true>(blk, G0, G1, brow, nullptr, nullptr);
+      rr[nb] = tile_dot<true, false>(blk, G0, G1, brow, nullptr, nullptr);
     }
-    S.part[slot][qw][nb][lane] = r;
   }
+  // every read of this warp's groups is done: its partials may overwrite them
+  __syncwarp();
+#pragma unroll
+  for (int nb = 0; nb < kMaxNB; ++nb)
+    if (nb < nbu) part_at(S, slot, nG, G0, qw, nb)[lane] = rr[nb];
+  fence_proxy_async_smem();   // generic writes into a bulk-copy target, before the slot is refilled
   __threadfence_block();
   __syncwarp();
   int last = 0;
@@ -296,7 +354,8 @@ __device__ void stage_split(const SgParams& p, Smem& S, int slot, const Stage& s
   for (int nb = 0; nb < nbu; ++nb) {
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int w = 0; w < kQW; ++w) {
-      const volatile float* v = reinterpret_cast<const volatile float*>(&S.part[slot][w][nb][lane]);
+      const int Gw = min(nG, w * cg);
+      const volatile float* v = reinterpret_cast<const volatile float*>(part_at(S, slot, nG, Gw, w, nb) + lane);
       r.x += v[0];
       r.y += v[1];
       r.z += v[2];
@@ -334,14 +393,20 @@ __device__ void stage_split(const SgParams& p, Smem& S, int slot, const Stage& s
 __device__ void stage_down_routed(const SgParams& p, Smem& S, int slot, const Stage& st, int qw) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int nGf = p.f / 64, nbu = (st.ntok + 7) >> 3;
+  const int xoff = xc_find(S, st.item);
   for (int j = qw; j < st.nrt; j += kQW) {
     const uint8_t* blk = S.ring[slot] + static_cast<size_t>(j) * nGf * kGroupBytes;
     const int row = 16 * (st.tile + j) + g;
     for (int nb = 0; nb < nbu; ++nb) {
-      const int col = nb * 8 + g, c0 = nb * 8 + 2 * t4;
-      const uint4* brow =
-          col < st.ntok ? reinterpret_cast<const uint4*>(p.av_r + static_cast<size_t>(st.row0 + col) * p.f) : nullptr;
-      const float4 r = tile_dot<true>(blk, 0, nGf, brow, nullptr, nullptr);
+      const int col = min(nb * 8 + g, st.ntok - 1), c0 = nb * 8 + 2 * t4;   // past the last token: its row again
+      float4 r;
+      if (xoff >= 0) {
+        r = tile_dot<true, true>(blk, 0, nGf, reinterpret_cast<const uint4*>(S.xc + xoff + col * p.f * 2), nullptr,
+                                 nullptr);
+      } else {
+        const uint4* brow = reinterpret_cast<const uint4*>(p.av_r + static_cast<size_t>(st.row0 + col) * p.f);
+        r = tile_dot<true, false>(blk, 0, nGf, brow, nullptr, nullptr);
+      }
       if (c0 < st.ntok) {
         float* y = p.y_r + static_cast<size_t>(__ldg(&p.row_pair[st.row0 + c0])) * p.d;
         y[row] = r.x;
@@ -356,6 +421,49 @@ __device__ void stage_down_routed(const SgParams& p, Smem& S, int slot, const St
   }
 }
 
+// The producer lane fills the CTA's B-row cache: the rows of the active
+// experts its routed stages belong to (x rows and their group sums for gate/up,
+// rows of a for down), as many whole experts as fit, with bulk copies that
+// complete on xbar.
+__device__ void fill_cache(const SgParams& p, Smem& S, const CtaStages& cs) {
+  const bool gu = p.mode == SG_GU;
+  const int nGd = p.d / 64;
+  const int rb = gu ? p.d * 2 : p.f * 2;                        // bytes per row
+  int per;
+  if (gu) {
+    per = p.f / 8;
+  } else {
+    const int R = p.d / 16, rt = routed_rt(p);
+    per = (R + rt - 1) / rt;
+  }
+  const int nr = cs.n - cs.n_sh;                                 // routed stages of the CTA
+  int n = 0, used = 0;
+  uint32_t bytes = 0;
+  // gate/up sums are copied too, which needs 16-byte aligned rows of them
+  if (nr > 0 && (!gu || nGd % 4 == 0)) {
+    const int u0 = cs.r0 / per, u1 = (cs.r0 + nr - 1) / per;
+    for (int u = u0; u <= u1 && n < kXcItems; ++u) {
+      const int rows = __ldg(&p.items[3 * u + 2]);
+      if (used + rows * rb > kXcBytes) break;
+      S.xc_item[n] = u;
+      S.xc_off[n] = used;
+      ++n;
+      used += rows * rb;
+      bytes += static_cast<uint32_t>(rows * rb + (gu ? rows * nGd * 4 : 0));
+    }
+  }
+  S.n_xc = n;
+  mbar_arrive_expect_tx(&S.xbar, bytes);   // release: the table above is visible to the waiters
+  for (int i = 0; i < n; ++i) {
+    const int u = S.xc_item[i], row0 = __ldg(&p.items[3 * u + 1]), rows = __ldg(&p.items[3 * u + 2]);
+    const uint8_t* src = gu ? reinterpret_cast<const uint8_t*>(p.xv) : reinterpret_cast<const uint8_t*>(p.av_r);
+    bulk_g2s(S.xc + S.xc_off[i], src + static_cast<size_t>(row0) * rb, static_cast<uint32_t>(rows * rb), &S.xbar);
+    if (gu)
+      bulk_g2s(S.xcg + S.xc_off[i] / 128, p.xg + static_cast<size_t>(row0) * nGd, static_cast<uint32_t>(rows * nGd * 4),
+               &S.xbar);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_small_batch(SgParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the ring at a 128-byte boundary (the allocation has 128 bytes to spare)
@@ -367,13 +475,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_small_batch(SgParams p) {
       mbar_init(&S.empty[i], kQW);
       S.cnt[i] = 0;
     }
+    mbar_init(&S.xbar, 1);
     fence_mbar_init();
   }
   __syncthreads();
   const CtaStages cs = cta_stages(p, *p.n_items);
   if (warp == kNC) {
-    // producer: the CTA's stages j = 0, 1, ... in order
+    // producer: the B-row cache, then the CTA's stages j = 0, 1, ... in order
     if (lane != 0) return;
+    fill_cache(p, S, cs);
     int j = 0;
     for (; j < cs.n; ++j) {
       const int slot = j % kNS;
@@ -385,13 +495,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_small_batch(SgParams p) {
     }
     // copies still in flight complete before the CTA leaves (bounded)
     for (int v = max(0, j - kNS); v < j; ++v) mbar_wait_bounded(&S.full[v % kNS], (v / kNS) & 1u, p.err);
+    mbar_wait_bounded(&S.xbar, 0u, p.err);
     return;
   }
   const int quad = warp / kQW, qw = warp % kQW;
+  bool cache_ready = false;
   for (int j = quad; j < cs.n; j += kNQ) {
     const int slot = j % kNS;
     if (!wait_warp(&S.full[slot], (j / kNS) & 1u, p.err)) return;
     const Stage st = stage_of(p, cs.stage(j));
+    if (st.item >= 0 && !cache_ready) {   // the first routed stage of this warp: the cache must be complete
+      if (!wait_warp(&S.xbar, 0u, p.err)) return;
+      cache_ready = true;
+    }
     if (st.kind == ST_DN_ROUTED) stage_down_routed(p, S, slot, st, qw);
     else stage_split(p, S, slot, st, qw);
     __syncwarp();
