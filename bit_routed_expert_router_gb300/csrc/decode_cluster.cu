@@ -288,6 +288,29 @@ __device__ __forceinline__ float grid_to_float(long long v) {
   return __ll2float_rn(v) * 2.3283064365386963e-10f;                                         // 2^-32
 }
 
+// RN(v) as fp32 (the value of a 64-bit integer conversion) with 32-bit
+// conversions for |v| < 2^48: v = q 2^24 + r with both parts exact in fp32
+// and one rounding of their fused sum.
+__device__ __forceinline__ float ll_to_float(long long v) {
+  const long long q = v >> 24;
+  if (q > -(1ll << 24) && q < (1ll << 24))
+    return fmaf(static_cast<float>(static_cast<int>(q)), 16777216.f, static_cast<float>(static_cast<unsigned>(v & 0xFFFFFF)));
+  return __ll2float_rn(v);
+}
+
+// RNE(b * 2^40) for |b| < 2^20 (the bias domain) with 32-bit conversions:
+// a = |b| 2^40 is an exact fp32 value below 2^60; its multiples of 2^32 and
+// its remainder (at most 24 significant bits) are exact, and the remainder is
+// rounded to an integer, ties to even, by the one 32-bit conversion.
+__device__ __forceinline__ long long bias_fix40(float b) {
+  const float a = fabsf(b) * 1099511627776.0f;                      // 2^40
+  const float h = floorf(a * 2.3283064365386963e-10f);              // 2^-32
+  const float r = fmaf(-h, 4294967296.0f, a);                       // exact
+  const long long m = static_cast<long long>(static_cast<unsigned>(h)) * 4294967296ll +
+                      static_cast<long long>(__float2uint_rn(r));
+  return b < 0.f ? -m : m;
+}
+
 // Layer outputs carry their completeness: every CTA adds (v << 8) + 1 into
 // each of its rows (v = the row's partial on the 2^-32 grid), so a row is final
 // once its low byte equals the number of clusters (one CTA of each cluster
@@ -676,7 +699,7 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
   __syncwarp();
   if (lane == 0) stamp(p, l - p.l0, EV_RANKS_OUT);
   float ex = 0.f;
-  if (lane < p.k) ex = expf(__ll2float_rn(S.topv[lane] - S.topv[0]) * 9.094947017729282e-13f);   // 2^-40
+  if (lane < p.k) ex = expf(ll_to_float(S.topv[lane] - S.topv[0]) * 9.094947017729282e-13f);   // 2^-40
   float sum = 0.f;
   for (int j = 0; j < p.k; ++j) sum += __shfl_sync(kFull, ex, j);
   const float gv = ex / sum;
@@ -877,7 +900,7 @@ __device__ void router_publish(const CParams& p, Smem& S, int cw, int rel, float
     if (!(fabsf(bv) < 1048576.f)) {
       if (lane == 0) atomicOr(p.err, ERR_ROUTER_DOMAIN);
     } else {
-      acc += __float2ll_rn(bv * 1099511627776.0f);
+      acc += bias_fix40(bv);
     }
   }
   __syncwarp();

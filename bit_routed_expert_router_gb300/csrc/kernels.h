@@ -171,6 +171,29 @@ cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* g
 cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,
                              cudaStream_t s);
 
+// Launches of the grouped path (routing, grouping, GEMMs or GEMVs, combine):
+// with g_chain_pdl set, each may start while the previous kernel of the stream
+// finishes (programmatic dependent launch); every such kernel waits for it
+// (griddepcontrol.wait) before touching memory, so the setting changes timing
+// only.  Set by the host for each call from its context.
+extern bool g_chain_pdl;
+
+template <typename... Params, typename... Args>
+inline cudaError_t launch_chain(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_chain_pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 // Small-batch grouped GEMVs (mma.sync from a TMA ring) for calls of at most
 // kSgMaxT tokens, after the prefill path's routing and expert grouping.
 constexpr int kSgMaxT = 32;            // tokens of a small-batch call

@@ -1540,6 +1540,8 @@ moe_status pf_alloc(moe_ctx* ctx) {
         !encode_rows(&ctx->pf_map_as[i], ctx->pf_as, c.f_shared, static_cast<long long>(T), br))
       return fail(ctx, MOE_ECUDA, "cuTensorMapEncodeTiled failed for the prefill operands");
   }
+  // the router's approximate logits accumulate into zeros (each pass zeroes what it reads)
+  CK(cudaMemset(ctx->pf_approx, 0, T * c.n_experts * sizeof(float)));
   ctx->device_bytes += nb;
   ctx->pf_ready = true;
   return MOE_OK;
@@ -1791,6 +1793,7 @@ moe_status pf_pool_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const
                        float* y_last, cudaStream_t s) {
   moe_status st = pf_alloc(ctx);
   if (st != MOE_OK) return st;
+  g_chain_pdl = ctx->pdl && !ctx->profiling;
   const int E = ctx->cfg.n_experts;
   if (!ctx->pf_arena) {
     size_t nb = 0;
@@ -1842,6 +1845,7 @@ moe_status pf_run(moe_ctx* ctx, const void* h, int T, int l0, int l1, const floa
                   float* y_last, cudaStream_t s) {
   moe_status st = pf_alloc(ctx);
   if (st != MOE_OK) return st;
+  g_chain_pdl = ctx->pdl && !ctx->profiling;
   const moe_config& c = ctx->cfg;
   const bool dbg = dbg_on(ctx);
   if (ctx->profiling || dbg || T > kPfGraphMaxT || ctx->pf_timeline) {

@@ -225,6 +225,8 @@ __device__ __forceinline__ void dequant_block_tmem(const uint8_t* blk, uint32_t 
 // Two CTAs share an SM, so one's epilogue overlaps the other's main loop.
 template <int kN>
 __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__ CUtensorMap tmap_b, PfGemm p) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   constexpr int kSlots = Tile<kN>::kSlots;
   constexpr int kRawStages = Tile<kN>::kRawStages;
   constexpr int kCols = Tile<kN>::kTmemCols;
@@ -408,6 +410,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
 __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int prenorm, float eps, uint16_t* x_bf,
                                                  uint16_t* x16, uint16_t* dbg_x, float* xn2, float* xmax,
                                                  uint32_t* err) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   __shared__ float red[8], red2[8], redm[8];
   const int t = blockIdx.x;
   const uint16_t* hr = h + static_cast<size_t>(t) * d;
@@ -507,6 +511,8 @@ constexpr int kRE = 64;       // experts per CTA
 constexpr int kRK = 64;       // k chunk (one partial sum per chunk)
 __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
                                                           int E, int k_slice, float* approx) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   __shared__ __align__(16) float xs[kRK][kRT];   // K-major, so a thread reads four tokens as one float4
   __shared__ __align__(16) float ws[kRK][kRE];
   const int tid = threadIdx.x;
@@ -574,11 +580,13 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
 // tokens (warp w < tpc takes the candidates and the top-k of token
 // blockIdx.x * tpc + w); all eight warps share the exact dot products, so a
 // small batch runs on one token per CTA and still spreads over the GPU.
-__global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const uint16_t* router_w, const float* approx,
+__global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const uint16_t* router_w, float* approx,
                                                   const float* xn2, const float* wn2, const float* xmax,
                                                   const float* wmax, const float* bias, int T, int d,
                                                   int E, int k, int32_t* ids, float* gates, int32_t* dbg_ids,
                                                   float* dbg_gates, int64_t* dbg_logits, int tpc, uint32_t* err) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   __shared__ int cand_all[8][128];
   __shared__ long long exact_all[8][128];
   __shared__ int n_cand_all[8];
@@ -605,6 +613,7 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
       hi[i] = -INFINITY;
       if (e < E) {
         const float s = approx[static_cast<size_t>(t) * E + e];
+        approx[static_cast<size_t>(t) * E + e] = 0.f;   // zero again for the next accumulation
         const float b = bias ? bias[static_cast<size_t>(t) * E + e] : 0.f;
         const float L = s + b;
         const float eps = 160.f * u * xn * (sqrtf(wn2[e]) * 1.01f) + static_cast<float>(d + 1) * 4.5474735e-13f +
@@ -771,6 +780,8 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
 
 // Pairs per expert.  One CTA per expert scans every (token, position) pair.
 __global__ void __launch_bounds__(256) k_pf_count(const int32_t* ids, int P, int32_t* cnt) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   const int e = blockIdx.x;
   int n = 0;
   for (int i = threadIdx.x; i < P; i += 256) n += ids[i] == e;
@@ -790,6 +801,8 @@ __global__ void __launch_bounds__(256) k_pf_count(const int32_t* ids, int P, int
 // [off_e, off_e + n_e), and its 128-row work items.
 __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, int E, const int32_t* cnt, int tile,
                                                     int32_t* row_pair, int32_t* items, int32_t* n_items) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   const int e = blockIdx.x;
   __shared__ int s_off, s_base;
   __shared__ int wsum[8], wit[8];
@@ -863,6 +876,8 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
 __global__ void __launch_bounds__(256) k_pf_combine(const float* ys, const float* ytok, const float* gates,
                                                     const uint16_t* hin, uint16_t* hout, float* y_last, float* dbg_y,
                                                     int d, int k) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   const int t = blockIdx.x;
   __shared__ float g[32];
   if (threadIdx.x < k) g[threadIdx.x] = gates[static_cast<size_t>(t) * k + threadIdx.x];
@@ -891,6 +906,8 @@ __global__ void __launch_bounds__(256) k_pf_combine(const float* ys, const float
 // Row r of the expert-ordered matrix = fp16 x of the pair's token.
 __global__ void __launch_bounds__(256) k_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k,
                                                    uint16_t* xp) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   const int r = blockIdx.x;
   if (r >= P) return;
   const int t = row_pair[r] / k;
@@ -919,16 +936,15 @@ cudaError_t pf_set_attrs() {
 cudaError_t launch_pf_gemm(int n, const CUtensorMap& tmap_b, const PfGemm& p, int m_tiles, int max_items,
                            cudaStream_t s) {
   if (m_tiles <= 0 || max_items <= 0) return cudaSuccess;
-  if (n == 32) k_pf_gemm<32><<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(32), s>>>(tmap_b, p);
-  else if (n == 256) k_pf_gemm<256><<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(256), s>>>(tmap_b, p);
-  else k_pf_gemm<128><<<dim3(m_tiles, max_items), kThreads, pf_gemm_smem(128), s>>>(tmap_b, p);
-  return cudaGetLastError();
+  if (n == 32) return launch_chain(k_pf_gemm<32>, dim3(m_tiles, max_items), dim3(kThreads), pf_gemm_smem(32), s, tmap_b, p);
+  if (n == 256)
+    return launch_chain(k_pf_gemm<256>, dim3(m_tiles, max_items), dim3(kThreads), pf_gemm_smem(256), s, tmap_b, p);
+  return launch_chain(k_pf_gemm<128>, dim3(m_tiles, max_items), dim3(kThreads), pf_gemm_smem(128), s, tmap_b, p);
 }
 
 cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
                            uint16_t* dbg_x, float* xn2, float* xmax, uint32_t* err, cudaStream_t s) {
-  k_pf_prep<<<T, 256, 0, s>>>(h, d, prenorm, eps, x_bf, x16, dbg_x, xn2, xmax, err);
-  return cudaGetLastError();
+  return launch_chain(k_pf_prep, dim3(T), dim3(256), 0, s, h, d, prenorm, eps, x_bf, x16, dbg_x, xn2, xmax, err);
 }
 
 cudaError_t launch_pf_row_stats(const uint16_t* rows, int n, int d, float* n2, float* mx, cudaStream_t s) {
@@ -949,36 +965,35 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
       slices = c;
       if (tiles * c >= 2 * n_sm) break;
     }
-  if (slices > 1) {
-    const cudaError_t e = cudaMemsetAsync(approx, 0, static_cast<size_t>(T) * E * sizeof(float), s);
-    if (e != cudaSuccess) return e;
-  }
-  k_pf_logits_approx<<<dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), 256, 0, s>>>(
-      x_bf, router_w, T, d, E, d / slices, approx);
+  // approx is all zeros here: zeroed when allocated, and k_pf_route zeroes what it reads
+  cudaError_t e = launch_chain(k_pf_logits_approx, dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), dim3(256),
+                               0, s, x_bf, router_w, T, d, E, d / slices, approx);
+  if (e != cudaSuccess) return e;
   // tokens per CTA: eight, or fewer when that leaves SMs idle
   const int tpc = std::max(1, std::min(8, (T + n_sm - 1) / n_sm));
-  k_pf_route<<<(T + tpc - 1) / tpc, 256, 0, s>>>(x_bf, router_w, approx, xn2, wn2, xmax, wmax, bias, T, d, E, k, ids,
-                                                 gates, dbg_ids, dbg_gates, dbg_logits, tpc, err);
-  return cudaGetLastError();
+  return launch_chain(k_pf_route, dim3((T + tpc - 1) / tpc), dim3(256), 0, s, x_bf, router_w, approx, xn2, wn2, xmax,
+                      wmax, bias, T, d, E, k, ids, gates, dbg_ids, dbg_gates, dbg_logits, tpc, err);
 }
 
 cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int tile, int32_t* cnt, int32_t* row_pair,
                            int32_t* items, int32_t* n_items, cudaStream_t s) {
-  k_pf_count<<<E, 256, 0, s>>>(ids, P, cnt);
-  k_pf_scatter<<<E, 256, 0, s>>>(ids, P, E, cnt, tile, row_pair, items, n_items);
-  return cudaGetLastError();
+  const cudaError_t e = launch_chain(k_pf_count, dim3(E), dim3(256), 0, s, ids, P, cnt);
+  if (e != cudaSuccess) return e;
+  return launch_chain(k_pf_scatter, dim3(E), dim3(256), 0, s, ids, P, E, static_cast<const int32_t*>(cnt), tile, row_pair,
+                      items, n_items);
 }
 
 cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* gates, const uint16_t* hin,
                               uint16_t* hout, float* y_last, float* dbg_y, int T, int d, int k, cudaStream_t s) {
-  k_pf_combine<<<dim3(T, (d + 255) / 256), 256, 0, s>>>(ys, ytok, gates, hin, hout, y_last, dbg_y, d, k);
-  return cudaGetLastError();
+  return launch_chain(k_pf_combine, dim3(T, (d + 255) / 256), dim3(256), 0, s, ys, ytok, gates, hin, hout, y_last, dbg_y,
+                      d, k);
 }
 
 cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,
                              cudaStream_t s) {
-  k_pf_gather<<<P, 256, 0, s>>>(x16, row_pair, P, d, k, xp);
-  return cudaGetLastError();
+  return launch_chain(k_pf_gather, dim3(P), dim3(256), 0, s, x16, row_pair, P, d, k, xp);
 }
+
+bool g_chain_pdl = false;
 
 }  // namespace moe

@@ -296,47 +296,83 @@ __device__ __forceinline__ int xc_find(const Smem& S, int u) {
   return -1;
 }
 
-// A stage whose int4 groups the quad's warps split (gate/up tiles and shared
-// down tiles): warp qw takes groups [qw * cg, (qw + 1) * cg) for every block of
-// eight token columns, the last warp to finish adds the partials in warp order
-// and writes the results.
-__device__ void stage_split(const SgParams& p, Smem& S, int slot, const Stage& st, int qw) {
+// The results of token block nb of a split stage: a = GELU(gate) * up in fp16
+// at its fragment-order place (gate/up), or the shared expert's output rows
+// (down).  r holds (row g, column c0), (row g, c0 + 1), (row g + 8, c0),
+// (row g + 8, c0 + 1), c0 = nb * 8 + 2 t4.
+__device__ __forceinline__ void emit(const SgParams& p, const Stage& st, bool gu, int nb, float4 r) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int c0 = nb * 8 + 2 * t4;
+  if (gu) {
+    // gate row g (r.x, r.y) and up row g (r.z, r.w) of intermediate row 8 tile + g
+    const int i = 8 * st.tile + g, F = st.row0 >= 0 ? p.f : p.fs;
+    uint16_t* av = st.row0 >= 0 ? p.av_r + static_cast<size_t>(st.row0) * p.f : p.av_s;
+    const float a0 = gelu_of(r.x, p.gelu) * r.z, a1 = gelu_of(r.y, p.gelu) * r.w;
+    const bool v0 = c0 < st.ntok, v1 = c0 + 1 < st.ntok;
+    if ((v0 && !(fabsf(a0) < 65504.f)) || (v1 && !(fabsf(a1) < 65504.f))) atomicOr(p.err, ERR_PF_RANGE);
+    const int pos = frag_pos(i);
+    if (v0) av[static_cast<size_t>(c0) * F + pos] = __half_as_ushort(__float2half_rn(a0));
+    if (v1) av[static_cast<size_t>(c0 + 1) * F + pos] = __half_as_ushort(__float2half_rn(a1));
+  } else {
+    const int row = 16 * st.tile + g;
+    if (c0 < st.ntok) {
+      p.y_s[static_cast<size_t>(c0) * p.d + row] = r.x;
+      p.y_s[static_cast<size_t>(c0) * p.d + row + 8] = r.z;
+    }
+    if (c0 + 1 < st.ntok) {
+      p.y_s[static_cast<size_t>(c0 + 1) * p.d + row] = r.y;
+      p.y_s[static_cast<size_t>(c0 + 1) * p.d + row + 8] = r.w;
+    }
+  }
+}
+
+// One token block of a split stage over groups [G0, G1): B rows from the
+// CTA's cache (routed gate/up whose rows it holds) or global memory.
+__device__ __forceinline__ float4 split_block(const SgParams& p, Smem& S, const Stage& st, bool gu, int xoff,
+                                             const uint8_t* blk, int G0, int G1, int nb) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  // columns past the last token repeat its row (their results are not used)
+  const int last_col = st.ntok - 1;
+  const int col = min(nb * 8 + g, last_col), c0 = min(nb * 8 + 2 * t4, last_col), c1 = min(c0 + 1, last_col);
+  if (xoff >= 0) {   // routed gate/up with its x rows (and sums) in the cache
+    const int rb = p.d * 2;
+    const uint4* brow = reinterpret_cast<const uint4*>(S.xc + xoff + col * rb);
+    return tile_dot<false, true>(blk, G0, G1, brow, S.xcg + (xoff + c0 * rb) / 128, S.xcg + (xoff + c1 * rb) / 128);
+  }
+  // gate/up: x (expert-ordered rows, then the shared expert's token rows at P); down: the shared a rows
+  const int rbase = gu ? (st.row0 >= 0 ? st.row0 : p.P) : 0;
+  if (gu) {
+    const uint4* brow = reinterpret_cast<const uint4*>(p.xv + static_cast<size_t>(rbase + col) * p.d);
+    const int nGd = p.d / 64;
+    return tile_dot<false, false>(blk, G0, G1, brow, p.xg + static_cast<size_t>(rbase + c0) * nGd,
+                                  p.xg + static_cast<size_t>(rbase + c1) * nGd);
+  }
+  const uint4* brow = reinterpret_cast<const uint4*>(p.av_s + static_cast<size_t>(col) * p.fs);
+  return tile_dot<true, false>(blk, G0, G1, brow, nullptr, nullptr);
+}
+
+// A stage of 16 weight rows over nG int4 groups (gate/up tiles and shared down
+// tiles).  With four blocks of token columns each warp of the quad takes one
+// block over every group and writes its results; otherwise the warps split the
+// groups ([qw * cg, (qw + 1) * cg)) for every block, and the last warp to
+// finish adds the four partials in warp order and writes the results.
+__device__ void stage_split(const SgParams& p, Smem& S, int slot, const Stage& st, int qw) {
+  const int lane = threadIdx.x & 31;
   const bool gu = st.kind == ST_GU;
   const int nG = gu ? p.d / 64 : p.fs / 64;
-  const int cg = (nG + kQW - 1) / kQW, G0 = min(nG, qw * cg), G1 = min(nG, G0 + cg);
   const int nbu = (st.ntok + 7) >> 3;
-  const uint8_t* blk = S.ring[slot] + static_cast<size_t>(G0) * kGroupBytes;
-  // B rows: gate/up: x (expert-ordered rows, then the shared expert's token rows at P); down: the shared a rows
-  const int vlen = gu ? p.d : p.fs;
-  const int rbase = gu ? (st.row0 >= 0 ? st.row0 : p.P) : 0;
-  const uint16_t* bbase = gu ? p.xv : p.av_s;
   const int xoff = gu && st.row0 >= 0 ? xc_find(S, st.item) : -1;
+  if (nbu == kQW) {
+    emit(p, st, gu, qw, split_block(p, S, st, gu, xoff, S.ring[slot], 0, nG, qw));
+    return;
+  }
+  const int cg = (nG + kQW - 1) / kQW, G0 = min(nG, qw * cg), G1 = min(nG, G0 + cg);
+  const uint8_t* blk = S.ring[slot] + static_cast<size_t>(G0) * kGroupBytes;
   float4 rr[kMaxNB];
 #pragma unroll
   for (int nb = 0; nb < kMaxNB; ++nb) {
     rr[nb] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (nb >= nbu) continue;
-    // columns past the last token repeat its row (their results are not used)
-    const int last_col = st.ntok - 1;
-    const int col = min(nb * 8 + g, last_col), c0 = min(nb * 8 + 2 * t4, last_col), c1 = min(c0 + 1, last_col);
-    if (xoff >= 0) {   // routed gate/up with its x rows (and sums) in the cache
-      const int rb = p.d * 2;
-      const uint4* brow = reinterpret_cast<const uint4*>(S.xc + xoff + col * rb);
-      const float* x0 = S.xcg + (xoff + c0 * rb) / 128;
-      const float* x1 = S.xcg + (xoff + c1 * rb) / 128;
-      rr[nb] = tile_dot<false, true>(blk, G0, G1, brow, x0, x1);
-      continue;
-    }
-    const uint4* brow = reinterpret_cast<const uint4*>(bbase + static_cast<size_t>(rbase + col) * vlen);
-    if (gu) {
-      const int nGd = p.d / 64;
-      const float* x0 = p.xg + static_cast<size_t>(rbase + c0) * nGd;
-      const float* x1 = p.xg + static_cast<size_t>(rbase + c1) * nGd;
-      rr[nb] = tile_dot<false, false>(blk, G0, G1, brow, x0, x1);
-    } else {
-      rr[nb] = tile_dot<true, false>(blk, G0, G1, brow, nullptr, nullptr);
-    }
+    if (nb < nbu) rr[nb] = split_block(p, S, st, gu, xoff, blk, G0, G1, nb);
   }
   // every read of this warp's groups is done: its partials may overwrite them
   __syncwarp();
@@ -361,28 +397,7 @@ __device__ void stage_split(const SgParams& p, Smem& S, int slot, const Stage& s
       r.z += v[2];
       r.w += v[3];
     }
-    const int c0 = nb * 8 + 2 * t4;
-    if (gu) {
-      // gate row g (r.x, r.y) and up row g (r.z, r.w) of intermediate row 8 tile + g, columns c0 and c0 + 1
-      const int i = 8 * st.tile + g, F = st.row0 >= 0 ? p.f : p.fs;
-      uint16_t* av = st.row0 >= 0 ? p.av_r + static_cast<size_t>(st.row0) * p.f : p.av_s;
-      const float a0 = gelu_of(r.x, p.gelu) * r.z, a1 = gelu_of(r.y, p.gelu) * r.w;
-      const bool v0 = c0 < st.ntok, v1 = c0 + 1 < st.ntok;
-      if ((v0 && !(fabsf(a0) < 65504.f)) || (v1 && !(fabsf(a1) < 65504.f))) atomicOr(p.err, ERR_PF_RANGE);
-      const int pos = frag_pos(i);
-      if (v0) av[static_cast<size_t>(c0) * F + pos] = __half_as_ushort(__float2half_rn(a0));
-      if (v1) av[static_cast<size_t>(c0 + 1) * F + pos] = __half_as_ushort(__float2half_rn(a1));
-    } else {
-      const int row = 16 * st.tile + g;
-      if (c0 < st.ntok) {
-        p.y_s[static_cast<size_t>(c0) * p.d + row] = r.x;
-        p.y_s[static_cast<size_t>(c0) * p.d + row + 8] = r.z;
-      }
-      if (c0 + 1 < st.ntok) {
-        p.y_s[static_cast<size_t>(c0 + 1) * p.d + row] = r.y;
-        p.y_s[static_cast<size_t>(c0 + 1) * p.d + row + 8] = r.w;
-      }
-    }
+    emit(p, st, gu, nb, r);
   }
   __syncwarp();
   if (lane == 0) S.cnt[slot] = 0;
@@ -465,6 +480,8 @@ __device__ void fill_cache(const SgParams& p, Smem& S, const CtaStages& cs) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_small_batch(SgParams p) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the ring at a 128-byte boundary (the allocation has 128 bytes to spare)
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u));
@@ -520,6 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_small_batch(SgParams p) {
 // fp32 sum of each 64-element group.
 __global__ void __launch_bounds__(256) k_sg_gather(const uint16_t* x_bf, const int32_t* row_pair, int P, int d, int k,
                                                    uint16_t* xv, float* xg) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
   const int r = blockIdx.x;
   const int t = r < P ? row_pair[r] / k : r - P;
   const uint32_t* src = reinterpret_cast<const uint32_t*>(x_bf + static_cast<size_t>(t) * d);
@@ -556,13 +575,11 @@ cudaError_t sg_set_attrs() {
 
 cudaError_t launch_sg_gather(const uint16_t* x_bf, const int32_t* row_pair, int P, int T, int d, int k, uint16_t* xv,
                              float* xg, cudaStream_t s) {
-  k_sg_gather<<<P + T, 256, 0, s>>>(x_bf, row_pair, P, d, k, xv, xg);
-  return cudaGetLastError();
+  return launch_chain(k_sg_gather, dim3(P + T), dim3(256), 0, s, x_bf, row_pair, P, d, k, xv, xg);
 }
 
 cudaError_t launch_sg(const SgParams& p, int n_sm, cudaStream_t s) {
-  k_small_batch<<<n_sm, kThreads, sg_smem(), s>>>(p);
-  return cudaGetLastError();
+  return launch_chain(k_small_batch, dim3(n_sm), dim3(kThreads), sg_smem(), s, p);
 }
 
 }  // namespace moe
