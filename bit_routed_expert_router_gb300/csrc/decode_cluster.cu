@@ -70,10 +70,10 @@ constexpr int kMaxU = kCMaxUnits;                 // units per cluster and layer
 constexpr int kMaxRows = kMaxD / kCl;             // down output rows per CTA
 constexpr int kMaxTasks = 3 * kMaxU + 1;
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr unsigned kPollSleepNs = 32;              // back-off between polls of the cluster's logit replica
 
 static_assert(kCThreads == 32 * (kNC + 2), "producer warp, 16 consumer warps, top-k warp");
 static_assert(kCl == 4, "the a push maps 32 lanes onto 4 ranks x 8 fragment words; 8 tiles = 4 ranks x 2");
+constexpr uint32_t kAPushBytes = 2 * kCl * (8 * 4 + 4);   // a unit's pushes into one CTA: 8 tiles x (8 words + sum)
 
 enum : int { K_GU = 0, K_DN = 1, K_TOPK = 2 };
 
@@ -100,11 +100,12 @@ struct Smem {
   alignas(16) float gu_part[kNS][kQW][8][2];       // gate/up partials [slot][warp of the quad][row][gate/up]
   alignas(8) uint64_t full[kNS];
   alignas(8) uint64_t empty[kNS];
-  alignas(8) uint64_t a_full[2 * kMaxU];           // 8 remote arrivals per use (4 ranks x 2 tiles)
+  alignas(8) uint64_t a_full[2 * kMaxU];           // per use: this CTA's expect of 8 x 36 bytes, and the bytes
   alignas(8) uint64_t rrow_full;
   alignas(8) uint64_t rrow_empty;
   alignas(8) uint64_t topk_bar;                    // one phase per layer
   alignas(8) uint64_t zero_bar;                    // one phase per layer: this CTA's share of the next vector zeroed
+  alignas(8) uint64_t end_bar;                     // one phase per layer: this CTA's stages of the layer are done
   alignas(8) uint64_t cbar;                        // consumer-warp barrier
   alignas(16) DevCallArgs args;
   CTask tasks[kMaxTasks];
@@ -176,7 +177,7 @@ __device__ __forceinline__ bool aborted(const CParams& p);
 // Wait sites, recorded with the CTA in p.diag by the first wait that runs out
 // (the others then see the abort flag and leave without recording).
 enum : unsigned { W_CBAR = 1, W_Y_POLL, W_RROW_EMPTY, W_P_TOPK, W_EMPTY, W_LOGITS, W_CLBAR, W_RROW_FULL, W_A_FULL,
-                  W_DN_TOPK, W_END_TOPK, W_FINISH, W_FULL, W_ZERO, W_PLAN };
+                  W_DN_TOPK, W_END_TOPK, W_FINISH, W_FULL, W_ZERO, W_PLAN, W_END_STAGES };
 __device__ __forceinline__ void note_timeout(const CParams& p, unsigned site) {
   atomicOr(p.err, ERR_WAIT_TIMEOUT);
   if (p.diag) atomicCAS(p.diag, 0u, (site << 16) | (blockIdx.x & 0xFFFFu));
@@ -615,26 +616,32 @@ __device__ bool topk_layer(const CParams& p, Smem& S, int l, int32_t* ids, float
   const unsigned long long* lg = p.tlog + (static_cast<size_t>(l) * n_cl + cl) * p.E * 2;
   unsigned long long key[NPL];
   int idx[NPL];
+  // two polls in flight: the next one is issued before this one is checked
+  const ulonglong2 absent = make_ulonglong2(static_cast<unsigned long long>(p.tag) << 32,
+                                            static_cast<unsigned long long>(p.tag) << 32);
+  ulonglong2 cur[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) cur[i] = lane + 32 * i < p.E ? ld_volatile_u64x2(lg + 2 * (lane + 32 * i)) : absent;
   const long long t0 = clock64();
   for (unsigned it = 0;; ++it) {
+    ulonglong2 nxt[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) nxt[i] = lane + 32 * i < p.E ? ld_volatile_u64x2(lg + 2 * (lane + 32 * i)) : absent;
     bool ok = true;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       const int e = lane + 32 * i;
-      key[i] = 0ull;
-      idx[i] = 0x7fffffff;
-      if (e < p.E) {
-        const ulonglong2 v = ld_volatile_u64x2(lg + 2 * e);
-        ok = ok && static_cast<unsigned>(v.x >> 32) == p.tag && static_cast<unsigned>(v.y >> 32) == p.tag;
-        key[i] = ((v.y << 32) | (v.x & 0xFFFFFFFFull)) ^ 0x8000000000000000ull;
-        idx[i] = e;
-      }
+      const ulonglong2 v = cur[i];
+      ok = ok && static_cast<unsigned>(v.x >> 32) == p.tag && static_cast<unsigned>(v.y >> 32) == p.tag;
+      key[i] = e < p.E ? ((v.y << 32) | (v.x & 0xFFFFFFFFull)) ^ 0x8000000000000000ull : 0ull;
+      idx[i] = e < p.E ? e : 0x7fffffff;
     }
     if (__all_sync(kFull, ok)) {
       if (lane == 0) stamp(p, l - p.l0, EV_LOGITS_IN);
       break;
     }
-    __nanosleep(kPollSleepNs);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) cur[i] = nxt[i];
     if ((it & 63) == 63) {
       if (__any_sync(kFull, aborted(p))) return false;
       if (__any_sync(kFull, clock64() - t0 > p.spin_limit)) {
@@ -847,6 +854,14 @@ __device__ void topk_warp(const CParams& p, Smem& S) {
   const int n_rel = p.l1 - p.l0, d = p.d;
   for (int rel = 0; rel < n_rel; ++rel) {
     if (cluster_rank() == 0) {
+      // the layer's logits need the previous layer's output, which needs this
+      // CTA's stages of it: wait for those (suspended, not spinning) before
+      // polling, so the poll does not take issue slots from this scheduler's
+      // consumer warps during the stages
+      if (rel > 0 && !wait_warp(p, &S.end_bar, static_cast<uint32_t>(rel - 1) & 1u, W_END_STAGES)) {
+        raise_abort(p);
+        return;
+      }
       int32_t* sid = S.ids[rel & 1];
       float* sg = S.gates[rel & 1];
       const unsigned base = 64u * static_cast<unsigned>(rel);
@@ -1147,20 +1162,27 @@ __device__ void gu_push(const CParams& p, Smem& S, int rel, const CTask& t, unsi
 #pragma unroll
   for (int i = 0; i < 8; ++i) w[i] = __shfl_sync(kFull, word, i);
   // lane r < 4 writes this tile's eight words (one 32-byte block) and its sum
-  // into CTA r of the cluster, then arrives there with release semantics,
-  // which orders its own two stores before the arrival (no fence needed)
+  // into CTA r of the cluster with asynchronous remote stores that count their
+  // bytes on that CTA's a_full barrier (no fence, nothing to wait for here);
+  // each CTA expects the unit's 8 x 36 bytes on its own barrier, once per use,
+  // when it pushes its first tile of the unit
   const int aslot = (rel & 1) * kMaxU + t.ui;
   if (lane < kCl) {
     const unsigned r = static_cast<unsigned>(lane);
+    if (t.tt == 0 && r == rank) mbar_arrive_expect_tx(&S.a_full[aslot], kAPushBytes);
     const uint32_t a = peer_addr(&S.abuf[aslot][(2 * rank + t.tt) * 8], r);
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                 "r"(w[3])
+    const uint32_t bar = peer_addr(&S.a_full[aslot], r);
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(a),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(bar)
                  : "memory");
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 16), "r"(w[4]), "r"(w[5]),
-                 "r"(w[6]), "r"(w[7])
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     a + 16),
+                 "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(bar)
                  : "memory");
-    st_peer_f32(peer_addr(&S.tsum[aslot][2 * rank + t.tt], r), sh + sl);
-    arrive_peer(peer_addr(&S.a_full[aslot], r));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     peer_addr(&S.tsum[aslot][2 * rank + t.tt], r)),
+                 "r"(__float_as_uint(sh + sl)), "r"(bar)
+                 : "memory");
   }
   __syncwarp();
   if (lane == 0) stamp(p, rel, EV_PUSH_LAST, true);
@@ -1336,7 +1358,10 @@ __device__ bool layer_end(const CParams& p, Smem& S, int cw, int rel, int& round
   const unsigned long long te = p.timeline ? now_ns() : 0ull;
   if (!consumer_barrier(p, S, ++round)) return false;   // every down stage of the layer added in
   if (lane == 0 && p.timeline) acc(p, rel, 7, now_ns() - te);
-  if (cw == 0 && lane == 0) stamp(p, rel, EV_STAGES_DONE);
+  if (cw == 0 && lane == 0) {
+    stamp(p, rel, EV_STAGES_DONE);
+    mbarrier_arrive(&S.end_bar);
+  }
   const int rows = p.d / kCl;
   bool bad = false;
   for (int i0 = 0; i0 < rows; i0 += kNC * 32) {
@@ -1491,11 +1516,12 @@ __global__ void __cluster_dims__(kCCluster, 1, 1) __launch_bounds__(kCThreads, 1
       mbar_init(&S.full[i], 1);
       mbar_init(&S.empty[i], kQW);
     }
-    for (int i = 0; i < 2 * kMaxU; ++i) mbar_init(&S.a_full[i], 2 * kCl);
+    for (int i = 0; i < 2 * kMaxU; ++i) mbar_init(&S.a_full[i], 1);
     mbar_init(&S.rrow_full, 1);
     mbar_init(&S.rrow_empty, 1);
     mbar_init(&S.topk_bar, 1);
     mbar_init(&S.zero_bar, 1);
+    mbar_init(&S.end_bar, 1);
     for (int j = 0; j < 32; ++j) S.rank_word[j] = 0;
     mbar_init(&S.cbar, kNC);
     fence_mbar_init();

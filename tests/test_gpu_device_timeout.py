@@ -52,7 +52,7 @@ def test_device_wait_that_runs_out_poisons_only_its_context(kernel):
             import ctypes
             word = ctypes.c_uint32(0)
             assert moe.moe_test_hook(ctx.h, moe.HOOK_WAIT_DIAG, ctypes.addressof(word)) == moe.MOE_OK
-            assert 1 <= word.value >> 16 <= 14, hex(word.value)
+            assert 1 <= word.value >> 16 <= 16, hex(word.value)
     torch.cuda.synchronize()                          # the device still answers
     with _ctx(ws, kernel) as ctx:
         for t in range(3):
