@@ -799,17 +799,28 @@ __global__ void __launch_bounds__(256) k_pf_count(const int32_t* ids, int P, int
 
 // Stable placement: expert e's pairs in increasing pair order at
 // [off_e, off_e + n_e), and its 128-row work items.
-__global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, int E, const int32_t* cnt, int tile,
-                                                    int32_t* row_pair, int32_t* items, int32_t* n_items) {
+// With count_here (small P), every CTA first counts all pairs per expert in
+// shared memory (and CTA e writes cnt[e]), so no counting launch precedes it.
+__global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, int E, int32_t* cnt, int tile,
+                                                    int32_t* row_pair, int32_t* items, int32_t* n_items,
+                                                    int count_here) {
   pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
   pdl_trigger();
   const int e = blockIdx.x;
   __shared__ int s_off, s_base;
   __shared__ int wsum[8], wit[8];
+  __shared__ int hist[256];
+  if (count_here) {
+    for (int i = threadIdx.x; i < E; i += 256) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < P; i += 256) atomicAdd(&hist[ids[i]], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) cnt[e] = hist[e];
+  }
   {
     // pairs and items of the experts before e (E <= 256: one per thread), summed over the CTA
     const int e2 = threadIdx.x;
-    int c = e2 < e ? cnt[e2] : 0;
+    int c = e2 < e ? (count_here ? hist[e2] : cnt[e2]) : 0;
     int it2 = (c + tile - 1) / tile;
 #pragma unroll
     for (int m = 16; m; m >>= 1) {
@@ -830,7 +841,7 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
     }
     s_off = off;
     s_base = 0;
-    const int n_e = cnt[e];
+    const int n_e = count_here ? hist[e] : cnt[e];
     for (int i = 0; i * tile < n_e; ++i) {
       items[3 * (it + i)] = e;
       items[3 * (it + i) + 1] = off + i * tile;
@@ -977,10 +988,14 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
 
 cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int tile, int32_t* cnt, int32_t* row_pair,
                            int32_t* items, int32_t* n_items, cudaStream_t s) {
-  const cudaError_t e = launch_chain(k_pf_count, dim3(E), dim3(256), 0, s, ids, P, cnt);
-  if (e != cudaSuccess) return e;
-  return launch_chain(k_pf_scatter, dim3(E), dim3(256), 0, s, ids, P, E, static_cast<const int32_t*>(cnt), tile, row_pair,
-                      items, n_items);
+  // small pair lists: one launch, each CTA counting them all itself
+  const int count_here = P <= 4096 ? 1 : 0;
+  if (!count_here) {
+    const cudaError_t e = launch_chain(k_pf_count, dim3(E), dim3(256), 0, s, ids, P, cnt);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_chain(k_pf_scatter, dim3(E), dim3(256), 0, s, ids, P, E, cnt, tile, row_pair, items, n_items,
+                      count_here);
 }
 
 cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* gates, const uint16_t* hin,
