@@ -862,9 +862,13 @@ def run_ours_batched(args):
 # ---------------------------------------------------------------------------- slot-cache (host pool) decode
 
 def host_link_peak_gbs(dev, nbytes=1 << 30, reps=5):
-    """Pinned host -> device copy rate of one large cudaMemcpyAsync, CUDA events
-    on the copying stream: the host link's peak for the staging roofline."""
+    """The host link's peak for the staging roofline, measured in this run on
+    one 1 GiB pinned buffer: the rate of one large pinned host -> device copy
+    (CUDA events on the copying stream) and the rate of plain loads from every
+    SM through the link (moe_host_read_rate: how the fused step reads its
+    misses).  Returns (peak, copy rate, load rate, which one is the peak)."""
     import torch
+    import bit_routed_expert_router_gb300 as moe
     src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     dst.copy_(src, non_blocking=True)
@@ -875,9 +879,14 @@ def host_link_peak_gbs(dev, nbytes=1 << 30, reps=5):
         dst.copy_(src, non_blocking=True)
     e1.record()
     e1.synchronize()
-    gbs = reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+    copy_gbs = reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+    st, load_gbs = moe.moe_host_read_rate(src, nbytes, reps, torch.cuda.current_stream())
+    if st != moe.MOE_OK:
+        load_gbs = 0.0
     del src, dst
-    return gbs
+    if load_gbs > copy_gbs:
+        return load_gbs, copy_gbs, load_gbs, "plain loads from every SM over a 1 GiB pinned buffer, measured in this run"
+    return copy_gbs, copy_gbs, load_gbs, "one 1 GiB pinned host-to-device copy, measured in this run"
 
 
 def run_ours_pool(args):
@@ -940,7 +949,7 @@ def run_ours_pool(args):
                                    "host_link_gbs": staged / dt / 1e9}
     chunked = pool_prefill_run(args, ctx, dev, stream)
     moe.moe_destroy(ctx)
-    link_peak = host_link_peak_gbs(dev)
+    link_peak, link_copy, link_load, link_source = host_link_peak_gbs(dev)
     file_tier = None
     if args.file_dir:
         file_tier = {}
@@ -970,9 +979,9 @@ def run_ours_pool(args):
         "sweep_by_slots_fused": sweeps["lru_fused"], "file_tier": file_tier,
         "chunked_prefill": chunked,
         "roofline": {"bound": "host link", "achieved": best["host_link_gbs"], "peak": link_peak, "unit": "GB/s",
-                     "frac": best["host_link_gbs"] / link_peak, "traffic": None,
-                     "peak_source": "one 1 GiB pinned host-to-device copy, measured in this run"},
-        "gpu_launches": None, "cpu_baseline": None,
+                     "frac": best["host_link_gbs"] / link_peak, "traffic": None, "peak_source": link_source,
+                     "host_copy_gbs": link_copy, "host_load_gbs": link_load},
+        "gpu_launches": n_tok, "cpu_baseline": None,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -82,6 +82,7 @@ _SIGS = {
     "moe_set_file_cache": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_set_staging": (C.c_int, [C.c_void_p, C.c_int]),
     "moe_pread_parallel": (C.c_int, [C.c_char_p, C.c_uint64, C.c_uint64, C.c_void_p, C.c_int, C.c_uint64]),
+    "moe_host_read_rate": (C.c_int, [C.c_void_p, C.c_uint64, C.c_int, C.c_void_p, C.POINTER(C.c_double)]),
     "moe_decode_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                                   C.c_void_p, C.POINTER(MoeTraceRec), C.c_int, C.POINTER(C.c_int),
                                   C.c_void_p]),
@@ -208,6 +209,13 @@ def moe_set_staging(ctx, mode: int) -> int:
 
 def moe_set_file_cache(ctx, n_host: int) -> int:
     return lib().moe_set_file_cache(ctx, n_host)
+
+
+def moe_host_read_rate(host_buf, nbytes: int, reps: int = 5, stream=None):
+    """(status, GB/s): plain-load read rate of pinned host memory from every SM."""
+    out = C.c_double(0.0)
+    st = lib().moe_host_read_rate(_ptr(host_buf), nbytes, reps, _stream(stream), C.byref(out))
+    return st, out.value
 
 
 def moe_pread_parallel(path, offset: int, nbytes: int, dst, n_threads: int = 8, chunk_bytes: int = 0) -> int:

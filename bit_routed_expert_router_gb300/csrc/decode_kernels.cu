@@ -914,6 +914,24 @@ __global__ void __launch_bounds__(256) k_stage_misses(const int32_t* rec, const 
   for (; i < n16; i += step) dst[i] = src[i];
 }
 
+// Reads n16 16-byte words of pinned host memory through the host link (the
+// way the fused host-pool step reads its misses: plain loads, eight in flight
+// per thread) and folds them into one word, so the reads cannot be dropped.
+__global__ void __launch_bounds__(256) k_host_read(const uint4* src, long long n16, unsigned* sink) {
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  unsigned acc = 0;
+  for (; i + 7 * step < n16; i += 8 * step) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = src[i + u * step];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  for (; i < n16; i += step) acc ^= src[i].x ^ src[i].y ^ src[i].z ^ src[i].w;
+  if (acc == 0x9E3779B9u) atomicAdd(sink, 1u);   // almost never taken; keeps the loads
+}
+
 }  // namespace
 
 cudaError_t launch_stage_misses(const int32_t* rec, const uint8_t* pool_layer, uint8_t* slots, long long stride,
@@ -922,6 +940,12 @@ cudaError_t launch_stage_misses(const int32_t* rec, const uint8_t* pool_layer, u
   int per_miss = 4 * n_sm / k;
   per_miss = per_miss < 1 ? 1 : (per_miss > 128 ? 128 : per_miss);
   k_stage_misses<<<dim3(per_miss, k), 256, 0, s>>>(rec, pool_layer, slots, stride, bytes / 16, E, n_slots, k, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_host_read(const void* src, long long bytes, unsigned* sink, int n_sm, cudaStream_t s) {
+  if (bytes % 16 != 0) return cudaErrorInvalidValue;
+  k_host_read<<<4 * n_sm, 256, 0, s>>>(static_cast<const uint4*>(src), bytes / 16, sink);
   return cudaGetLastError();
 }
 

@@ -1933,6 +1933,45 @@ moe_status moe_prefill(moe_ctx* ctx, const void* h, int T, int layer_begin, int 
   return MOE_OK;
 }
 
+moe_status moe_host_read_rate(const void* host_buf, uint64_t bytes, int reps, void* stream, double* gbs) {
+  if (!host_buf || !gbs || bytes == 0 || bytes % 16 != 0 || reps < 1 ||
+      reinterpret_cast<uintptr_t>(host_buf) % 16 != 0)
+    return MOE_EINVAL;
+  *gbs = 0.0;
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, host_buf) != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return MOE_EINVAL;   // not page-locked host memory the device can read
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess)
+    return MOE_ECUDA;
+  const void* src = attr.devicePointer ? attr.devicePointer : host_buf;
+  unsigned* sink = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  moe_status st = MOE_ECUDA;
+  float ms = 0.f;
+  if (cudaMalloc(&sink, sizeof(unsigned)) == cudaSuccess && cudaEventCreate(&e0) == cudaSuccess &&
+      cudaEventCreate(&e1) == cudaSuccess &&
+      launch_host_read(src, static_cast<long long>(bytes), sink, n_sm, s) == cudaSuccess &&   // warm-up
+      cudaEventRecord(e0, s) == cudaSuccess) {
+    bool ok = true;
+    for (int r = 0; r < reps && ok; ++r) ok = launch_host_read(src, static_cast<long long>(bytes), sink, n_sm, s) == cudaSuccess;
+    if (ok && cudaEventRecord(e1, s) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && ms > 0.f) {
+      *gbs = static_cast<double>(bytes) * reps / (ms * 1e-3) / 1e9;
+      st = MOE_OK;
+    }
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (sink) cudaFree(sink);
+  cudaGetLastError();
+  return st;
+}
+
 moe_status moe_set_debug(moe_ctx* ctx, uint16_t* x_layers, int32_t* ids, float* gates, float* y_layers,
                          int max_layers) {
   if (!ctx) return MOE_EINVAL;

@@ -377,6 +377,17 @@ moe_status moe_set_file_cache(moe_ctx *ctx, int n_host);
 moe_status moe_pread_parallel(const char *path, uint64_t offset, uint64_t bytes, void *dst, int n_threads,
                               uint64_t chunk_bytes);
 
+/* Read rate of the host link as the fused host-pool step uses it: plain
+ * 16-byte loads from every SM of the current device over `bytes` (a multiple
+ * of 16) of page-locked host memory at host_buf (16-byte aligned; allocated
+ * with cudaHostAlloc / cudaMallocHost or registered, so the device reads it
+ * through the host link), repeated `reps` times after one untimed pass on
+ * `stream`; *gbs receives bytes * reps / time in GB/s (CUDA events on the
+ * stream).  A measurement for the pool workload's roofline, not part of the
+ * FFN.  MOE_EINVAL for bad arguments or memory the device cannot read,
+ * MOE_ECUDA on a failed CUDA call (no context to poison). */
+moe_status moe_host_read_rate(const void *host_buf, uint64_t bytes, int reps, void *stream, double *gbs);
+
 /* Bytes of one routed expert / of the shared expert for a config (0 on a bad config). */
 int64_t moe_expert_bytes(const moe_config *cfg);
 int64_t moe_shared_bytes(const moe_config *cfg);

@@ -96,6 +96,15 @@ def test_noalloc_routing_rejects_bad_sizes_without_cuda(lib):
     assert moe.moe_route_noalloc(cfg, None, 16, 1, None, 16, 16, 0) == moe.MOE_EINVAL
 
 
+def test_host_read_rate_rejects_bad_arguments_without_cuda(lib):
+    out = C.c_double(1.0)
+    assert lib.moe_host_read_rate(None, 1024, 1, None, C.byref(out)) == moe.MOE_EINVAL
+    buf = (C.c_uint8 * 1024)()
+    assert lib.moe_host_read_rate(buf, 1000, 1, None, C.byref(out)) == moe.MOE_EINVAL     # not a multiple of 16
+    assert lib.moe_host_read_rate(buf, 1024, 0, None, C.byref(out)) == moe.MOE_EINVAL     # no repetition
+    assert lib.moe_host_read_rate(buf, 1024, 1, None, None) == moe.MOE_EINVAL
+
+
 def test_status_strings(lib):
     for i, name in enumerate(["MOE_OK", "MOE_EINVAL", "MOE_ENOMEM", "MOE_ECUDA", "MOE_ESTATE", "MOE_ETIMEOUT",
                               "MOE_EDOMAIN"]):

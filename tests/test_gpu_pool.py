@@ -487,3 +487,15 @@ def test_device_staging_without_trace_and_errors(tmp_path):
         moe.check(moe.moe_set_expert_file(fctx.h, str(tmp_path / "e.bin"), 2, 0), fctx.h)
         fctx.init_layer(0, w, residency=moe.MOE_FILE_POOL)
         assert moe.moe_set_staging(fctx.h, moe.MOE_STAGING_DEVICE) == moe.MOE_ESTATE  # file reads are host I/O
+
+
+def test_host_read_rate():
+    # plain loads of pinned host memory from every SM (the pool line's link peak);
+    # pageable memory is refused
+    buf = torch.empty(64 << 20, dtype=torch.uint8).pin_memory()
+    st, gbs = moe.moe_host_read_rate(buf, buf.numel(), 3, torch.cuda.current_stream())
+    assert st == moe.MOE_OK and 1.0 < gbs < 2000.0, (st, gbs)
+    pageable = torch.empty(1 << 20, dtype=torch.uint8)
+    st, _ = moe.moe_host_read_rate(pageable, pageable.numel(), 1, None)
+    assert st == moe.MOE_EINVAL
+
