@@ -11,11 +11,12 @@
 // on another cluster between gate/up and down:
 //
 //   CTA rank r of the cluster computes gate/up tiles 2r and 2r + 1 of the unit
-//   (16 intermediate rows), writes their 16 values of a (as bf16 hi + lo
+//   (16 intermediate rows) and writes their 16 values of a (as fp16 hi + lo
 //   mma.sync B fragments) and their sums into the shared memory of every CTA of
-//   the cluster (distributed shared memory), and arrives on each CTA's
-//   mbarrier for the unit; then it multiplies output rows [r d/4, (r+1) d/4) of
-//   the unit's down block by the 64 values once all eight tiles have arrived.
+//   the cluster (distributed shared memory) with asynchronous remote stores
+//   that count their bytes on that CTA's barrier for the unit; then it
+//   multiplies output rows [r d/4, (r+1) d/4) of the unit's down block by the
+//   64 values once all eight tiles' bytes have arrived.
 //
 // The grid-wide exchanges left per layer are the router logits (one router
 // row per CTA, published with a per-launch tag inside each 64-bit word into
@@ -25,11 +26,9 @@
 // a 2^-32 fixed-point grid and adds (v << 8) + 1 per row into the layer's int64
 // output vector with one bulk reduction (TMA engine, integer adds in L2, so the
 // result does not depend on the order in which CTAs arrive).  The low byte of
-// a row counts its contributions, so a reader polls the rows themselves: each
-// CTA waits for its rank's quarter of the vector, adds it to the residual
-// stream and writes the result into the shared memory of all four CTAs of its
-// cluster, which then all hold the whole residual and normalise it for the
-// next layer.
+// a row counts its contributions, so a reader polls the rows themselves: every
+// CTA polls the whole vector, adds it to its copy of the residual stream and
+// normalises it for the next layer.
 //
 // Roles per CTA (18 warps):
 //   warp 0, lane 0 (producer): the router row, then every stage of the CTA's
@@ -43,8 +42,10 @@
 //     epilogue and the push; down: row tiles strided by warp).  A unit's down
 //     stage is queued after the next two units' gate/up stages, so its 64
 //     values of a have normally arrived from the other CTAs of the cluster.
-//   warp 17 (top-k): polls the layer's tagged logits, takes the top-k and the
-//     softmax gates and releases the producer.
+//   warp 17 (top-k, in the cluster's rank-0 CTA): once its CTA's stages of the
+//     previous layer are done, polls the layer's tagged logits, takes the top-k
+//     (publishing each rank for the cluster's producers as soon as it is
+//     picked) and the softmax gates.
 // Every wait is bounded and gives up through an abort flag and the device
 // error word (MOE_ETIMEOUT from moe_sync).  Output vectors rotate over three
 // buffers, each zeroed (in shares, by every CTA) once everyone has read it.
