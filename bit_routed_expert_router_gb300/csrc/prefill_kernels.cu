@@ -576,6 +576,24 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
     }
 }
 
+// Eight products x_i w_i (bf16 x, fp16 w) onto the 2^-40 grid; a product
+// outside |x_i w_i| < 2^11 is dropped and flagged.
+constexpr int kRouteChunks = 12;   // 8-column chunks per lane: 256 * 12 = 3072 columns
+__device__ __forceinline__ void exact_terms(const uint4& xv, const uint4& wv, Fix40& fx, bool& bad) {
+  const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xa[u] >> 16) : (xa[u] & 0xFFFFu)));
+      const float pw = hh ? half_hi(wa[u]) : half_lo(wa[u]);
+      const float prod = pw * px;
+      const bool ok = fabsf(prod) < 2048.f;
+      bad |= !ok;
+      fix40_add(fx, ok ? prod * 1099511627776.0f : 0.f);
+    }
+}
+
 // Pass 2: candidates, their exact logits, top-k and gates.  A CTA takes tpc <= 8
 // tokens (warp w < tpc takes the candidates and the top-k of token
 // blockIdx.x * tpc + w); all eight warps share the exact dot products, so a
@@ -674,26 +692,19 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
     const uint16_t* xr = x_bf + static_cast<size_t>(tt) * d;
     const uint16_t* wr = router_w + static_cast<size_t>(e) * d;
     Fix40 fx;
-    // eight products per lane per 256 columns (at most d / 32 <= 96 terms), two loads in flight
-#pragma unroll 2
-    for (int i0 = 0; i0 < d; i0 += 256) {
-      if (i0 + 8 * lane < d) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(xr + i0 + 8 * lane);
-        const uint4 wv = *reinterpret_cast<const uint4*>(wr + i0 + 8 * lane);
-        const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+    // eight products per lane per 256 columns (d <= 3072, checked when the
+    // context is created: at most 96 terms); every load of the pair is issued
+    // before the first product, so a pair costs one memory round trip
+    uint4 xv[kRouteChunks], wv[kRouteChunks];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float px = bf16_bits_to_float(static_cast<uint16_t>(hh ? (xa[u] >> 16) : (xa[u] & 0xFFFFu)));
-            const float pw = hh ? half_hi(wa[u]) : half_lo(wa[u]);
-            const float prod = pw * px;
-            const bool ok = fabsf(prod) < 2048.f;
-            bad |= !ok;
-            fix40_add(fx, ok ? prod * 1099511627776.0f : 0.f);
-          }
+    for (int c = 0; c < kRouteChunks; ++c)
+      if (256 * c + 8 * lane < d) {
+        xv[c] = *reinterpret_cast<const uint4*>(xr + 256 * c + 8 * lane);
+        wv[c] = *reinterpret_cast<const uint4*>(wr + 256 * c + 8 * lane);
       }
-    }
+#pragma unroll
+    for (int c = 0; c < kRouteChunks; ++c)
+      if (256 * c + 8 * lane < d) exact_terms(xv[c], wv[c], fx, bad);
     long long v = fix40_value(fx);
 #pragma unroll
     for (int m = 16; m; m >>= 1) v += shfl_xor_i64(v, m);
