@@ -524,25 +524,40 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+  // staging: thread tid converts row r = tid % 64 (token t0 + r, expert e0 + r)
+  // at columns cA .. cA + 7 and cA + 32 .. cA + 39 of each chunk, so the 32
+  // lanes of a warp store 32 consecutive rows of one column (no bank
+  // conflicts); the next chunk's loads are issued before this chunk's products
+  const int r = tid & 63, cA = (tid >> 6) * 8;
+  const bool tv = t0 + r < T, ev = e0 + r < E;
+  uint4 xv[2], wv[2];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int col = k0 + cA + 32 * j;
+      xv[j] = tv ? *reinterpret_cast<const uint4*>(x_bf + static_cast<size_t>(t0 + r) * d + col)
+                 : make_uint4(0u, 0u, 0u, 0u);
+      wv[j] = ev ? *reinterpret_cast<const uint4*>(router_w + static_cast<size_t>(e0 + r) * d + col)
+                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load(kb);
   for (int k0 = kb; k0 < kb + k_slice; k0 += kRK) {
-    __syncthreads();
-    // 64 rows x 64 columns of x and of W_r: each thread converts two runs of eight
-    for (int i = tid; i < kRT * kRK / 8; i += 256) {
-      const int r = i / (kRK / 8), c8 = (i % (kRK / 8)) * 8;
-      const int t = t0 + r, e = e0 + r;
-      uint4 xv = make_uint4(0u, 0u, 0u, 0u), wv = make_uint4(0u, 0u, 0u, 0u);
-      if (t < T) xv = *reinterpret_cast<const uint4*>(x_bf + static_cast<size_t>(t) * d + k0 + c8);
-      if (e < E) wv = *reinterpret_cast<const uint4*>(router_w + static_cast<size_t>(e) * d + k0 + c8);
-      const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+    __syncthreads();   // the previous chunk's products are done
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t xa[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w}, wa[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+      const int col = cA + 32 * j;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        xs[c8 + 2 * u][r] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] & 0xFFFFu));
-        xs[c8 + 2 * u + 1][r] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] >> 16));
-        ws[c8 + 2 * u][r] = half_lo(wa[u]);
-        ws[c8 + 2 * u + 1][r] = half_hi(wa[u]);
+        xs[col + 2 * u][r] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] & 0xFFFFu));
+        xs[col + 2 * u + 1][r] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] >> 16));
+        ws[col + 2 * u][r] = half_lo(wa[u]);
+        ws[col + 2 * u + 1][r] = half_hi(wa[u]);
       }
     }
     __syncthreads();
+    if (k0 + kRK < kb + k_slice) load(k0 + kRK);
     float c[4][4];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -550,9 +565,9 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
       for (int b = 0; b < 4; ++b) c[a][b] = 0.f;
 #pragma unroll 4
     for (int kk = 0; kk < kRK; ++kk) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
-      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+      const float4 xf = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
+      const float4 wf = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
+      const float xa[4] = {xf.x, xf.y, xf.z, xf.w}, wa[4] = {wf.x, wf.y, wf.z, wf.w};
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -861,14 +876,31 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
     if (e == E - 1) *n_items = it + (n_e + tile - 1) / tile;
   }
   __syncthreads();
-  // 2048 pairs per pass, eight consecutive ones per thread, placed in pair order
+  // 2048 pairs per pass, eight consecutive ones per thread, placed in pair
+  // order; the next pass's ids are loaded before this pass's scan
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  auto load_ids = [&](int c0, int (&v)[8]) {
+    const int i0 = c0 + 8 * threadIdx.x;
+    if (i0 + 8 <= P) {   // ids is 256-byte aligned and i0 a multiple of 8
+      const int4 a = *reinterpret_cast<const int4*>(ids + i0), b = *reinterpret_cast<const int4*>(ids + i0 + 4);
+      v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = i0 + u < P ? ids[i0 + u] : -1;
+    }
+  };
+  int cur[8];
+  load_ids(0, cur);
   for (int c0 = 0; c0 < P; c0 += 2048) {
     const int i0 = c0 + 8 * threadIdx.x;
+    int nxt[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    if (c0 + 2048 < P) load_ids(c0 + 2048, nxt);
     unsigned mask = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u)
-      if (i0 + u < P && ids[i0 + u] == e) mask |= 1u << u;
+      if (cur[u] == e) mask |= 1u << u;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) cur[u] = nxt[u];
     const int n = __popc(mask);
     int incl = n;   // inclusive scan over the warp
 #pragma unroll
