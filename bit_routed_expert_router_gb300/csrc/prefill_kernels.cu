@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(256) k_pf_row_stats(const uint16_t* rows, int 
 constexpr int kRT = 64;       // tokens per CTA
 constexpr int kRE = 64;       // experts per CTA
 constexpr int kRK = 64;       // k chunk (one partial sum per chunk)
-__global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
+__global__ void __launch_bounds__(256, 4) k_pf_logits_approx(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
                                                           int E, int k_slice, float* approx) {
   pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
   pdl_trigger();
@@ -527,7 +527,8 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
   // staging: thread tid converts row r = tid % 64 (token t0 + r, expert e0 + r)
   // at columns cA .. cA + 7 and cA + 32 .. cA + 39 of each chunk, so the 32
   // lanes of a warp store 32 consecutive rows of one column (no bank
-  // conflicts); the next chunk's loads are issued before this chunk's products
+  // conflicts); four CTAs per SM hide the loads (measured better than
+  // prefetching the next chunk into registers)
   const int r = tid & 63, cA = (tid >> 6) * 8;
   const bool tv = t0 + r < T, ev = e0 + r < E;
   uint4 xv[2], wv[2];
@@ -541,8 +542,8 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
                  : make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  load(kb);
   for (int k0 = kb; k0 < kb + k_slice; k0 += kRK) {
+    load(k0);
     __syncthreads();   // the previous chunk's products are done
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -557,7 +558,6 @@ __global__ void __launch_bounds__(256) k_pf_logits_approx(const uint16_t* x_bf, 
       }
     }
     __syncthreads();
-    if (k0 + kRK < kb + k_slice) load(k0 + kRK);
     float c[4][4];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -613,6 +613,7 @@ __device__ __forceinline__ void exact_terms(const uint4& xv, const uint4& wv, Fi
 // tokens (warp w < tpc takes the candidates and the top-k of token
 // blockIdx.x * tpc + w); all eight warps share the exact dot products, so a
 // small batch runs on one token per CTA and still spreads over the GPU.
+template <int kHold>
 __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const uint16_t* router_w, float* approx,
                                                   const float* xn2, const float* wn2, const float* xmax,
                                                   const float* wmax, const float* bias, int T, int d,
@@ -708,18 +709,23 @@ __global__ void __launch_bounds__(256) k_pf_route(const uint16_t* x_bf, const ui
     const uint16_t* wr = router_w + static_cast<size_t>(e) * d;
     Fix40 fx;
     // eight products per lane per 256 columns (d <= 3072, checked when the
-    // context is created: at most 96 terms); every load of the pair is issued
-    // before the first product, so a pair costs one memory round trip
-    uint4 xv[kRouteChunks], wv[kRouteChunks];
+    // context is created: at most 96 terms); the loads of kHold chunks are
+    // issued before their products, so with kHold = 12 a pair costs one
+    // memory round trip (few tokens per launch: latency), with fewer the
+    // kernel keeps more CTAs per SM (many tokens: throughput)
 #pragma unroll
-    for (int c = 0; c < kRouteChunks; ++c)
-      if (256 * c + 8 * lane < d) {
-        xv[c] = *reinterpret_cast<const uint4*>(xr + 256 * c + 8 * lane);
-        wv[c] = *reinterpret_cast<const uint4*>(wr + 256 * c + 8 * lane);
-      }
+    for (int c0 = 0; c0 < kRouteChunks; c0 += kHold) {
+      uint4 xv[kHold], wv[kHold];
 #pragma unroll
-    for (int c = 0; c < kRouteChunks; ++c)
-      if (256 * c + 8 * lane < d) exact_terms(xv[c], wv[c], fx, bad);
+      for (int c = 0; c < kHold; ++c)
+        if (256 * (c0 + c) + 8 * lane < d) {
+          xv[c] = *reinterpret_cast<const uint4*>(xr + 256 * (c0 + c) + 8 * lane);
+          wv[c] = *reinterpret_cast<const uint4*>(wr + 256 * (c0 + c) + 8 * lane);
+        }
+#pragma unroll
+      for (int c = 0; c < kHold; ++c)
+        if (256 * (c0 + c) + 8 * lane < d) exact_terms(xv[c], wv[c], fx, bad);
+    }
     long long v = fix40_value(fx);
 #pragma unroll
     for (int m = 16; m; m >>= 1) v += shfl_xor_i64(v, m);
@@ -1011,13 +1017,13 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
                              float* gates, int32_t* dbg_ids, float* dbg_gates, int64_t* dbg_logits, uint32_t* err, int n_sm,
                              cudaStream_t s) {
   const int tiles = ((T + kRT - 1) / kRT) * ((E + kRE - 1) / kRE);
-  // slice d (in 64-wide chunks, a divisor of d/64) until the grid covers the GPU twice
+  // slice d (in 64-wide chunks, a divisor of d/64) until the grid covers the GPU six times
   const int nc = d / kRK;
   int slices = 1;
   for (int c = 1; c <= nc; ++c)
     if (nc % c == 0) {
       slices = c;
-      if (tiles * c >= 2 * n_sm) break;
+      if (tiles * c >= 6 * n_sm) break;
     }
   // approx is all zeros here: zeroed when allocated, and k_pf_route zeroes what it reads
   cudaError_t e = launch_chain(k_pf_logits_approx, dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), dim3(256),
@@ -1025,7 +1031,10 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
   if (e != cudaSuccess) return e;
   // tokens per CTA: eight, or fewer when that leaves SMs idle
   const int tpc = std::max(1, std::min(8, (T + n_sm - 1) / n_sm));
-  return launch_chain(k_pf_route, dim3((T + tpc - 1) / tpc), dim3(256), 0, s, x_bf, router_w, approx, xn2, wn2, xmax,
+  if (tpc == 1)
+    return launch_chain(k_pf_route<kRouteChunks>, dim3((T + tpc - 1) / tpc), dim3(256), 0, s, x_bf, router_w, approx, xn2, wn2, xmax,
+                        wmax, bias, T, d, E, k, ids, gates, dbg_ids, dbg_gates, dbg_logits, tpc, err);
+  return launch_chain(k_pf_route<4>, dim3((T + tpc - 1) / tpc), dim3(256), 0, s, x_bf, router_w, approx, xn2, wn2, xmax,
                       wmax, bias, T, d, E, k, ids, gates, dbg_ids, dbg_gates, dbg_logits, tpc, err);
 }
 
