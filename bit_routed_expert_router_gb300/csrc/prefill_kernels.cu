@@ -506,83 +506,106 @@ __global__ void __launch_bounds__(256) k_pf_row_stats(const uint16_t* rows, int 
 // fixed-point logits (products rounded onto the 2^-40 grid, summed exactly with
 // Fix40), and the top-k (ties to the lower index) and the softmax gates are
 // taken from those, so the result is the exact router's.
-constexpr int kRT = 64;       // tokens per CTA
 constexpr int kRE = 64;       // experts per CTA
+constexpr int kApproxWavesBig = 3;   // grid target of the 128-token tiles, in SMs
 constexpr int kRK = 64;       // k chunk (one partial sum per chunk)
-__global__ void __launch_bounds__(256, 4) k_pf_logits_approx(const uint16_t* x_bf, const uint16_t* router_w, int T, int d,
-                                                          int E, int k_slice, float* approx) {
+// kTT tokens x 4 experts per thread, 16 kTT tokens x 64 experts per CTA: 4
+// (64 tokens) for small batches, 8 (128 tokens: twice the multiply-adds per
+// shared-memory read) for large ones, where shared-memory reads bound it.
+template <int kTT>
+__global__ void __launch_bounds__(256, kTT == 4 ? 4 : 2)
+    k_pf_logits_approx(const uint16_t* x_bf, const uint16_t* router_w, int T, int d, int E, int k_slice,
+                       float* approx) {
   pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
   pdl_trigger();
+  constexpr int kRT = 16 * kTT;                  // tokens per CTA
   __shared__ __align__(16) float xs[kRK][kRT];   // K-major, so a thread reads four tokens as one float4
   __shared__ __align__(16) float ws[kRK][kRE];
   const int tid = threadIdx.x;
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE, kb = blockIdx.z * k_slice;
   const int tx = tid & 15;             // experts e0 + 4 tx .. + 3
-  const int ty = tid >> 4;             // tokens t0 + 4 ty .. + 3
-  float acc[4][4];
+  const int ty = tid >> 4;             // tokens t0 + kTT ty .. + kTT - 1
+  float acc[kTT][4];
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int a = 0; a < kTT; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-  // staging: thread tid converts row r = tid % 64 (token t0 + r, expert e0 + r)
-  // at columns cA .. cA + 7 and cA + 32 .. cA + 39 of each chunk, so the 32
-  // lanes of a warp store 32 consecutive rows of one column (no bank
-  // conflicts); four CTAs per SM hide the loads (measured better than
-  // prefetching the next chunk into registers)
-  const int r = tid & 63, cA = (tid >> 6) * 8;
-  const bool tv = t0 + r < T, ev = e0 + r < E;
-  uint4 xv[2], wv[2];
+  // staging: runs of eight columns, each thread's rows fixed over the chunks
+  // (x: row tid % kRT; W_r: row tid % 64), so the 32 lanes of a warp store 32
+  // consecutive rows of one column (no bank conflicts); several CTAs per SM
+  // hide the loads (measured better than prefetching the next chunk into
+  // registers)
+  constexpr int kXR = kRT * kRK / 8 / 256;       // x runs per thread (2 or 4)
+  const int rx = tid % kRT, cx = (tid / kRT) * 8, rw = tid & 63, cw = (tid >> 6) * 8;
+  const bool tv = t0 + rx < T, ev = e0 + rw < E;
+  uint4 xv[kXR], wv[2];
   auto load = [&](int k0) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int col = k0 + cA + 32 * j;
-      xv[j] = tv ? *reinterpret_cast<const uint4*>(x_bf + static_cast<size_t>(t0 + r) * d + col)
+    for (int j = 0; j < kXR; ++j)
+      xv[j] = tv ? *reinterpret_cast<const uint4*>(x_bf + static_cast<size_t>(t0 + rx) * d + k0 + cx + (64 / kXR) * j)
                  : make_uint4(0u, 0u, 0u, 0u);
-      wv[j] = ev ? *reinterpret_cast<const uint4*>(router_w + static_cast<size_t>(e0 + r) * d + col)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      wv[j] = ev ? *reinterpret_cast<const uint4*>(router_w + static_cast<size_t>(e0 + rw) * d + k0 + cw + 32 * j)
                  : make_uint4(0u, 0u, 0u, 0u);
-    }
   };
   for (int k0 = kb; k0 < kb + k_slice; k0 += kRK) {
     load(k0);
     __syncthreads();   // the previous chunk's products are done
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint32_t xa[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w}, wa[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
-      const int col = cA + 32 * j;
+    for (int j = 0; j < kXR; ++j) {
+      const uint32_t xa[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+      const int col = cx + (64 / kXR) * j;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        xs[col + 2 * u][r] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] & 0xFFFFu));
-        xs[col + 2 * u + 1][r] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] >> 16));
-        ws[col + 2 * u][r] = half_lo(wa[u]);
-        ws[col + 2 * u + 1][r] = half_hi(wa[u]);
+        xs[col + 2 * u][rx] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] & 0xFFFFu));
+        xs[col + 2 * u + 1][rx] = bf16_bits_to_float(static_cast<uint16_t>(xa[u] >> 16));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t wa[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+      const int col = cw + 32 * j;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        ws[col + 2 * u][rw] = half_lo(wa[u]);
+        ws[col + 2 * u + 1][rw] = half_hi(wa[u]);
       }
     }
     __syncthreads();
-    float c[4][4];
+    float c[kTT][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < kTT; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) c[a][b] = 0.f;
 #pragma unroll 4
     for (int kk = 0; kk < kRK; ++kk) {
-      const float4 xf = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
-      const float4 wf = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
-      const float xa[4] = {xf.x, xf.y, xf.z, xf.w}, wa[4] = {wf.x, wf.y, wf.z, wf.w};
+      float xa[kTT];
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int q = 0; q < kTT / 4; ++q) {
+        const float4 xf = *reinterpret_cast<const float4*>(&xs[kk][kTT * ty + 4 * q]);
+        xa[4 * q] = xf.x;
+        xa[4 * q + 1] = xf.y;
+        xa[4 * q + 2] = xf.z;
+        xa[4 * q + 3] = xf.w;
+      }
+      const float4 wf = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
+      const float wa[4] = {wf.x, wf.y, wf.z, wf.w};
+#pragma unroll
+      for (int a = 0; a < kTT; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) c[a][b] = fmaf(xa[a], wa[b], c[a][b]);
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < kTT; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) acc[a][b] += c[a][b];
   }
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int a = 0; a < kTT; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int t = t0 + 4 * ty + a, e = e0 + 4 * tx + b;
+      const int t = t0 + kTT * ty + a, e = e0 + 4 * tx + b;
       if (t < T && e < E) {
         float* dst = approx + static_cast<size_t>(t) * E + e;
         if (gridDim.z == 1) *dst = acc[a][b];
@@ -1016,18 +1039,27 @@ cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, con
                              int k, float* approx, float* xn2, float* wn2, float* xmax, float* wmax, int32_t* ids,
                              float* gates, int32_t* dbg_ids, float* dbg_gates, int64_t* dbg_logits, uint32_t* err, int n_sm,
                              cudaStream_t s) {
-  const int tiles = ((T + kRT - 1) / kRT) * ((E + kRE - 1) / kRE);
-  // slice d (in 64-wide chunks, a divisor of d/64) until the grid covers the GPU six times
+  // 128-token tiles from 256 tokens on (kTT = 8), else 64
+  const bool big = T >= 256;
+  const int rt = big ? 128 : 64;
+  const int tiles = ((T + rt - 1) / rt) * ((E + kRE - 1) / kRE);
+  // slice d (in 64-wide chunks, a divisor of d/64) until the grid covers the
+  // GPU's CTA slots about a few times over (each slice adds one atomic add
+  // per logit)
   const int nc = d / kRK;
+  const int target = (big ? kApproxWavesBig : 6) * n_sm;
   int slices = 1;
   for (int c = 1; c <= nc; ++c)
     if (nc % c == 0) {
       slices = c;
-      if (tiles * c >= 6 * n_sm) break;
+      if (tiles * c >= target) break;
     }
   // approx is all zeros here: zeroed when allocated, and k_pf_route zeroes what it reads
-  cudaError_t e = launch_chain(k_pf_logits_approx, dim3((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, slices), dim3(256),
-                               0, s, x_bf, router_w, T, d, E, d / slices, approx);
+  const dim3 grid((T + rt - 1) / rt, (E + kRE - 1) / kRE, slices);
+  cudaError_t e = big ? launch_chain(k_pf_logits_approx<8>, grid, dim3(256), 0, s, x_bf, router_w, T, d, E, d / slices,
+                                     approx)
+                      : launch_chain(k_pf_logits_approx<4>, grid, dim3(256), 0, s, x_bf, router_w, T, d, E, d / slices,
+                                     approx);
   if (e != cudaSuccess) return e;
   // tokens per CTA: eight, or fewer when that leaves SMs idle
   const int tpc = std::max(1, std::min(8, (T + n_sm - 1) / n_sm));
