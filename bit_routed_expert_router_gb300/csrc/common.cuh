@@ -116,6 +116,38 @@ __device__ __forceinline__ void nibbles_to_f16x2(uint32_t w, uint32_t (&a)[4]) {
   a[3] = (w8 & 0x00F000F0u) | 0x64006400u;
 }
 
+// The nibbles of word w unpacked as nibbles_to_f16x2 does, straight into the
+// A operand of one m16n8k16 fp16 MMA, D = A * B + C (C = D, or zero with
+// kZero), in one asm block: the unpacked words need no moves into the MMA's
+// operand registers.  Not volatile, so the compiler may interleave the MMAs
+// of several groups.
+template <bool kZero>
+__device__ __forceinline__ void mma_nib(float (&c)[4], uint32_t w, uint32_t b0, uint32_t b1) {
+  const uint32_t lo = 0x000F000Fu, hi = 0x00F000F0u, e = 0x64006400u;
+  if (kZero) {
+    asm("{\n\t.reg .b32 a0, a1, a2, a3, w8;\n\t.reg .f32 z;\n\t"
+        "mov.f32 z, 0f00000000;\n\t"
+        "shr.b32 w8, %4, 8;\n\t"
+        "lop3.b32 a0, %4, %7, %9, 0xEA;\n\t"
+        "lop3.b32 a1, %4, %8, %9, 0xEA;\n\t"
+        "lop3.b32 a2, w8, %7, %9, 0xEA;\n\t"
+        "lop3.b32 a3, w8, %8, %9, 0xEA;\n\t"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {a0,a1,a2,a3}, {%5,%6}, {z,z,z,z};\n\t}"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(w), "r"(b0), "r"(b1), "r"(lo), "r"(hi), "r"(e));
+  } else {
+    asm("{\n\t.reg .b32 a0, a1, a2, a3, w8;\n\t"
+        "shr.b32 w8, %4, 8;\n\t"
+        "lop3.b32 a0, %4, %7, %9, 0xEA;\n\t"
+        "lop3.b32 a1, %4, %8, %9, 0xEA;\n\t"
+        "lop3.b32 a2, w8, %7, %9, 0xEA;\n\t"
+        "lop3.b32 a3, w8, %8, %9, 0xEA;\n\t"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {a0,a1,a2,a3}, {%5,%6}, {%0,%1,%2,%3};\n\t}"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(w), "r"(b0), "r"(b1), "r"(lo), "r"(hi), "r"(e));
+  }
+}
+
 // D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators, A/B from registers.
 __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(

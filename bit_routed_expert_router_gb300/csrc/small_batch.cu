@@ -237,15 +237,10 @@ __device__ __forceinline__ float4 tile_dot(const uint8_t* blk, int G0, int G1, c
       X1 = kSmemB ? xg1[G] : __ldg(xg1 + G);
     }
     float c0[4], c1[4];
-    uint32_t a[4];
-    nibbles_to_f16x2(q.x, a);
-    mma16z(c0, a, x01.x, x01.y);
-    nibbles_to_f16x2(q.y, a);
-    mma16z(c1, a, x01.z, x01.w);
-    nibbles_to_f16x2(q.z, a);
-    mma16(c0, a, x23.x, x23.y);
-    nibbles_to_f16x2(q.w, a);
-    mma16(c1, a, x23.z, x23.w);
+    mma_nib<true>(c0, q.x, x01.x, x01.y);
+    mma_nib<true>(c1, q.y, x01.z, x01.w);
+    mma_nib<false>(c0, q.z, x23.x, x23.y);
+    mma_nib<false>(c1, q.w, x23.z, x23.w);
     if (kOnesSum) {   // column sums of B: two chains of two MMAs
       float s0[4], s1[4];
       mma16z(s0, one, x01.x, x01.y);
