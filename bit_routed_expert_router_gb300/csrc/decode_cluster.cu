@@ -1118,16 +1118,11 @@ __device__ void gu_groups(Smem& S, const uint8_t* tile, int G0, int G1, float& g
     const uint2 sbv = *reinterpret_cast<const uint2*>(blk + kFragBytes + g * 8);
     const uint4* xf = reinterpret_cast<const uint4*>(S.xp) + (G * 4 + t4) * 2;
     const uint4 x01 = xf[0], x23 = xf[1];
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t a[4];
-    nibbles_to_f16x2(q.x, a);
-    mma_f16(c0, a, x01.x, x01.y);
-    nibbles_to_f16x2(q.y, a);
-    mma_f16(c1, a, x01.z, x01.w);
-    nibbles_to_f16x2(q.z, a);
-    mma_f16(c0, a, x23.x, x23.y);
-    nibbles_to_f16x2(q.w, a);
-    mma_f16(c1, a, x23.z, x23.w);
+    float c0[4], c1[4];
+    mma_nib<true>(c0, q.x, x01.x, x01.y);
+    mma_nib<true>(c1, q.y, x01.z, x01.w);
+    mma_nib<false>(c0, q.z, x23.x, x23.y);
+    mma_nib<false>(c1, q.w, x23.z, x23.w);
     const float X = S.xg[G];
     const float sg = half_lo(sbv.x), bg = half_hi(sbv.x), su = half_lo(sbv.y), bu = half_hi(sbv.y);
     ga += sg * (c0[0] + c1[0]) + fmaf(-1024.f, sg, bg) * X;
@@ -1323,16 +1318,11 @@ __device__ bool stage_dn(const CParams& p, Smem& S, int quad, int qw, int rel, i
     const uint8_t* blk = S.ring[slot] + static_cast<size_t>(T) * kGroupBytes;
     const uint4 q = *reinterpret_cast<const uint4*>(blk + lane * 16);
     const uint2 sbv = *reinterpret_cast<const uint2*>(blk + kFragBytes + g * 8);
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t a[4];
-    nibbles_to_f16x2(q.x, a);
-    mma_f16(c0, a, b01.x, b01.y);
-    nibbles_to_f16x2(q.y, a);
-    mma_f16(c1, a, b01.z, b01.w);
-    nibbles_to_f16x2(q.z, a);
-    mma_f16(c0, a, b23.x, b23.y);
-    nibbles_to_f16x2(q.w, a);
-    mma_f16(c1, a, b23.z, b23.w);
+    float c0[4], c1[4];
+    mma_nib<true>(c0, q.x, b01.x, b01.y);
+    mma_nib<true>(c1, q.y, b01.z, b01.w);
+    mma_nib<false>(c0, q.z, b23.x, b23.y);
+    mma_nib<false>(c1, q.w, b23.z, b23.w);
     const float s0 = half_lo(sbv.x), o0 = half_hi(sbv.x), s1 = half_lo(sbv.y), o1 = half_hi(sbv.y);
     const float y0 = s0 * ((c0[0] + c1[0]) + (c0[1] + c1[1])) + fmaf(-1024.f, s0, o0) * As;
     const float y1 = (s1 * 0.0625f) * ((c0[2] + c1[2]) + (c0[3] + c1[3])) + fmaf(-64.f, s1, o1) * As;
