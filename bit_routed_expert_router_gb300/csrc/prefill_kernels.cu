@@ -185,38 +185,87 @@ __host__ __device__ __forceinline__ int k16_pos(int i) {
 // fragments + per-row fp16 scale/bias) to fp16 w = s*q + b, stored into
 // tensor-memory lanes lane0 .. lane0 + 15 and 32 columns from col (the A operand
 // of four k16 MMAs), with one .16x256b store.  The caller's warp must own
-// those lanes (warp % 4 == lane0 / 32).
+// those lanes (warp % 4 == lane0 / 32).  Per nibble pair: the nibbles as fp16
+// 1024 + q (OR under the exponent of 1024), minus 1024 (exact q), then s*q + b
+// (fp16 fma); lane (g, t4)'s word st of the fragment holds nibbles j (low
+// half) and j + 4 (high half) for j = 0: row g, k 2t4..; 1: row g + 8, k 2t4..;
+// 2: row g, k 2t4 + 8..; 3: row g + 8, k 2t4 + 8..; the store's registers of
+// repetition st are (row g, col 2t4), (row g, col 2t4 + 1), (row g + 8, ...).
+// One asm block, so the sixteen results go straight into the store's
+// operand registers.
 __device__ __forceinline__ void dequant_block_tmem(const uint8_t* blk, uint32_t taddr) {
   const int lane = threadIdx.x & 31, g = lane >> 2;
   const uint4 q = *reinterpret_cast<const uint4*>(blk + lane * 16);
   const uint2 sb = *reinterpret_cast<const uint2*>(blk + kFragBytes + g * 8);
-  const __half2 s0 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.x & 0xFFFFu)));
-  const __half2 c0 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.x >> 16)));
-  const __half2 s1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.y & 0xFFFFu)));
-  const __half2 c1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sb.y >> 16)));
-  const __half2 k1024 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400u)));
-  const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-  uint32_t r[16];
-#pragma unroll
-  for (int st = 0; st < 4; ++st) {
-    const uint32_t w = words[st];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      // nibbles j (low half) and j + 4 (high half) as fp16 1024 + q, then exact q, then s*q + b;
-      // j = 0: row g, k 2t4..; 1: row g+8, k 2t4..; 2: row g, k 2t4+8..; 3: row g+8, k 2t4+8..
-      const uint32_t bits = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-      const __half2 qh = __hsub2(*reinterpret_cast<const __half2*>(&bits), k1024);
-      const bool hi_row = (j & 1) != 0;
-      const __half2 v = __hfma2(qh, hi_row ? s1 : s0, hi_row ? c1 : c0);
-      // .16x256b registers of repetition st: (row g, col 2t4), (row g, col 2t4+1), (row g+8, ...)
-      const int slot = 4 * st + (hi_row ? 2 : 0) + (j >> 1);
-      r[slot] = *reinterpret_cast<const uint32_t*>(&v);
-    }
-  }
+  const uint32_t s0 = (sb.x & 0xFFFFu) * 0x10001u, c0 = (sb.x >> 16) * 0x10001u;   // fp16 pairs (s, s), (b, b)
+  const uint32_t s1 = (sb.y & 0xFFFFu) * 0x10001u, c1 = (sb.y >> 16) * 0x10001u;
   asm volatile(
-      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      "{\n\t"
+      ".reg .b32 t<16>, r<16>;\n\t"
+      "lop3.b32 t0, %1, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t0, t0, %9;\n\t"
+      "fma.rn.f16x2 r0, t0, %5, %6;\n\t"
+      "shr.b32 t1, %1, 4;\n\t"
+      "lop3.b32 t1, t1, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t1, t1, %9;\n\t"
+      "fma.rn.f16x2 r2, t1, %7, %8;\n\t"
+      "shr.b32 t2, %1, 8;\n\t"
+      "lop3.b32 t2, t2, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t2, t2, %9;\n\t"
+      "fma.rn.f16x2 r1, t2, %5, %6;\n\t"
+      "shr.b32 t3, %1, 12;\n\t"
+      "lop3.b32 t3, t3, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t3, t3, %9;\n\t"
+      "fma.rn.f16x2 r3, t3, %7, %8;\n\t"
+      "lop3.b32 t4, %2, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t4, t4, %9;\n\t"
+      "fma.rn.f16x2 r4, t4, %5, %6;\n\t"
+      "shr.b32 t5, %2, 4;\n\t"
+      "lop3.b32 t5, t5, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t5, t5, %9;\n\t"
+      "fma.rn.f16x2 r6, t5, %7, %8;\n\t"
+      "shr.b32 t6, %2, 8;\n\t"
+      "lop3.b32 t6, t6, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t6, t6, %9;\n\t"
+      "fma.rn.f16x2 r5, t6, %5, %6;\n\t"
+      "shr.b32 t7, %2, 12;\n\t"
+      "lop3.b32 t7, t7, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t7, t7, %9;\n\t"
+      "fma.rn.f16x2 r7, t7, %7, %8;\n\t"
+      "lop3.b32 t8, %3, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t8, t8, %9;\n\t"
+      "fma.rn.f16x2 r8, t8, %5, %6;\n\t"
+      "shr.b32 t9, %3, 4;\n\t"
+      "lop3.b32 t9, t9, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t9, t9, %9;\n\t"
+      "fma.rn.f16x2 r10, t9, %7, %8;\n\t"
+      "shr.b32 t10, %3, 8;\n\t"
+      "lop3.b32 t10, t10, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t10, t10, %9;\n\t"
+      "fma.rn.f16x2 r9, t10, %5, %6;\n\t"
+      "shr.b32 t11, %3, 12;\n\t"
+      "lop3.b32 t11, t11, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t11, t11, %9;\n\t"
+      "fma.rn.f16x2 r11, t11, %7, %8;\n\t"
+      "lop3.b32 t12, %4, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t12, t12, %9;\n\t"
+      "fma.rn.f16x2 r12, t12, %5, %6;\n\t"
+      "shr.b32 t13, %4, 4;\n\t"
+      "lop3.b32 t13, t13, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t13, t13, %9;\n\t"
+      "fma.rn.f16x2 r14, t13, %7, %8;\n\t"
+      "shr.b32 t14, %4, 8;\n\t"
+      "lop3.b32 t14, t14, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t14, t14, %9;\n\t"
+      "fma.rn.f16x2 r13, t14, %5, %6;\n\t"
+      "shr.b32 t15, %4, 12;\n\t"
+      "lop3.b32 t15, t15, %10, %9, 0xEA;\n\t"
+      "sub.f16x2 t15, t15, %9;\n\t"
+      "fma.rn.f16x2 r15, t15, %7, %8;\n\t"
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {r0,r1,r2,r3,r4,r5,r6,r7,r8,r9,r10,r11,r12,r13,r14,r15};\n\t"
+      "}"
+      ::"r"(taddr), "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w), "r"(s0), "r"(c0), "r"(s1), "r"(c1), "r"(0x64006400u),
+      "r"(0x000F000Fu)
       : "memory");
 }
 
