@@ -55,7 +55,7 @@ constexpr int kMaxNB = kSgMaxT / 8;           // blocks of eight token columns
 constexpr int kThreads = 32 * (kNC + 1);
 constexpr unsigned kFull = 0xFFFFFFFFu;
 #ifndef SG_UNROLL
-#define SG_UNROLL 2
+#define SG_UNROLL 4
 #endif
 constexpr int kUnroll = SG_UNROLL;            // int4 groups a warp's loop keeps in flight
 
