@@ -101,26 +101,18 @@ __device__ __forceinline__ void nibbles_to_bf16x2(uint32_t w, uint32_t (&a)[4]) 
   a[3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
 }
 
-// Eight packed nibbles -> four f16x2 A-fragment registers with four logic ops
-// and one shift: register r takes nibbles r (low half) and r + 4 (high half)
-// where they sit, under the fp16 exponent of 1024 (unit in the last place 1).
+// One m16n8k16 fp16 MMA, D = A * B + C (C = D, or zero with kZero), whose A
+// fragment is the eight packed nibbles of word w: register r takes nibbles r
+// (low half) and r + 4 (high half) where they sit, under the fp16 exponent of
+// 1024 (unit in the last place 1), with four logic ops and one shift.
 // Registers 0 and 2 (fragment rows g) hold 1024 + q; registers 1 and 3 (rows
 // g + 8) keep their nibbles four bits up and hold 1024 + 16 q, which the
 // epilogue undoes per row.  (bf16 has too few mantissa bits for the second
-// form, which is why the activations of these MMAs are fp16.)
-__device__ __forceinline__ void nibbles_to_f16x2(uint32_t w, uint32_t (&a)[4]) {
-  const uint32_t w8 = w >> 8;
-  a[0] = (w & 0x000F000Fu) | 0x64006400u;
-  a[1] = (w & 0x00F000F0u) | 0x64006400u;
-  a[2] = (w8 & 0x000F000Fu) | 0x64006400u;
-  a[3] = (w8 & 0x00F000F0u) | 0x64006400u;
-}
-
-// The nibbles of word w unpacked as nibbles_to_f16x2 does, straight into the
-// A operand of one m16n8k16 fp16 MMA, D = A * B + C (C = D, or zero with
-// kZero), in one asm block: the unpacked words need no moves into the MMA's
-// operand registers.  Not volatile, so the compiler may interleave the MMAs
-// of several groups.
+// form, which is why the activations of these MMAs are fp16.)  Unpack and
+// MMA are one asm block: with the unpack in C++ the compiler moved every
+// unpacked word into the MMA's operand registers (about 16 extra
+// instructions per 64-wide group, by ncu instruction counts).  Not volatile,
+// so the compiler may interleave the MMAs of several groups.
 template <bool kZero>
 __device__ __forceinline__ void mma_nib(float (&c)[4], uint32_t w, uint32_t b0, uint32_t b1) {
   const uint32_t lo = 0x000F000Fu, hi = 0x00F000F0u, e = 0x64006400u;
@@ -146,15 +138,6 @@ __device__ __forceinline__ void mma_nib(float (&c)[4], uint32_t w, uint32_t b0, 
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(w), "r"(b0), "r"(b1), "r"(lo), "r"(hi), "r"(e));
   }
-}
-
-// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators, A/B from registers.
-__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
