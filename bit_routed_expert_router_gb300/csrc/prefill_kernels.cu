@@ -1004,7 +1004,9 @@ __global__ void __launch_bounds__(256) k_pf_scatter(const int32_t* ids, int P, i
 }
 
 // y = shared + sum_j g_j * y_j in top-k order, h' = bf16(h + y): one CTA per
-// token and block of 256 output rows.
+// token and block of 1024 output rows, four consecutive rows per thread
+// (16-byte loads of the fp32 rows; d is a multiple of 64), each row's sum in
+// the same order as one row per thread.
 __global__ void __launch_bounds__(256) k_pf_combine(const float* ys, const float* ytok, const float* gates,
                                                     const uint16_t* hin, uint16_t* hout, float* y_last, float* dbg_y,
                                                     int d, int k) {
@@ -1015,24 +1017,74 @@ __global__ void __launch_bounds__(256) k_pf_combine(const float* ys, const float
   if (threadIdx.x < k) g[threadIdx.x] = gates[static_cast<size_t>(t) * k + threadIdx.x];
   __syncthreads();
   const float* yt = ytok + static_cast<size_t>(t) * k * d;
-  {
-    const int R = blockIdx.y * 256 + threadIdx.x;
-    if (R >= d) return;
-    const size_t o = static_cast<size_t>(t) * d + R;
-    float y = ys[o];
-    int j = 0;
-    for (; j + 8 <= k; j += 8) {   // eight independent loads in flight, summed in top-k order
-      float v[8];
+  const int R = (blockIdx.y * 256 + threadIdx.x) * 4;
+  if (R >= d) return;
+  const size_t o = static_cast<size_t>(t) * d + R;
+  const float4 y0 = *reinterpret_cast<const float4*>(ys + o);
+  float y[4] = {y0.x, y0.y, y0.z, y0.w};
+  int j = 0;
+  for (; j + 8 <= k; j += 8) {   // eight independent 16-byte loads in flight, summed in top-k order
+    float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcs(yt + static_cast<size_t>(j + u) * d + R);   // read once: stream
+    for (int u = 0; u < 8; ++u)
+      v[u] = __ldcs(reinterpret_cast<const float4*>(yt + static_cast<size_t>(j + u) * d + R));   // read once: stream
 #pragma unroll
-      for (int u = 0; u < 8; ++u) y += g[j + u] * v[u];
+    for (int u = 0; u < 8; ++u) {
+      y[0] += g[j + u] * v[u].x;
+      y[1] += g[j + u] * v[u].y;
+      y[2] += g[j + u] * v[u].z;
+      y[3] += g[j + u] * v[u].w;
     }
-    for (; j < k; ++j) y += g[j] * __ldcs(yt + static_cast<size_t>(j) * d + R);
-    hout[o] = float_to_bf16_bits(bf16_bits_to_float(hin[o]) + y);
-    if (y_last) y_last[o] = y;
-    if (dbg_y) dbg_y[o] = y;
   }
+  for (; j < k; ++j) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(yt + static_cast<size_t>(j) * d + R));
+    y[0] += g[j] * v.x;
+    y[1] += g[j] * v.y;
+    y[2] += g[j] * v.z;
+    y[3] += g[j] * v.w;
+  }
+  const uint2 hv = *reinterpret_cast<const uint2*>(hin + o);
+  const uint16_t h4[4] = {static_cast<uint16_t>(hv.x & 0xFFFFu), static_cast<uint16_t>(hv.x >> 16),
+                          static_cast<uint16_t>(hv.y & 0xFFFFu), static_cast<uint16_t>(hv.y >> 16)};
+  uint16_t r4[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) r4[u] = float_to_bf16_bits(bf16_bits_to_float(h4[u]) + y[u]);
+  *reinterpret_cast<uint2*>(hout + o) =
+      make_uint2(r4[0] | (static_cast<uint32_t>(r4[1]) << 16), r4[2] | (static_cast<uint32_t>(r4[3]) << 16));
+  const float4 yv = make_float4(y[0], y[1], y[2], y[3]);
+  if (y_last) *reinterpret_cast<float4*>(y_last + o) = yv;
+  if (dbg_y) *reinterpret_cast<float4*>(dbg_y + o) = yv;
+}
+
+// The same, one row per thread: for small batches (more CTAs) and for caller
+// buffers that are not aligned for the vector form (h_in / h_out to 8 bytes,
+// y to 16).
+__global__ void __launch_bounds__(256) k_pf_combine1(const float* ys, const float* ytok, const float* gates,
+                                                     const uint16_t* hin, uint16_t* hout, float* y_last, float* dbg_y,
+                                                     int d, int k) {
+  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
+  pdl_trigger();
+  const int t = blockIdx.x;
+  __shared__ float g[32];
+  if (threadIdx.x < k) g[threadIdx.x] = gates[static_cast<size_t>(t) * k + threadIdx.x];
+  __syncthreads();
+  const float* yt = ytok + static_cast<size_t>(t) * k * d;
+  const int R = blockIdx.y * 256 + threadIdx.x;
+  if (R >= d) return;
+  const size_t o = static_cast<size_t>(t) * d + R;
+  float y = ys[o];
+  int j = 0;
+  for (; j + 8 <= k; j += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcs(yt + static_cast<size_t>(j + u) * d + R);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) y += g[j + u] * v[u];
+  }
+  for (; j < k; ++j) y += g[j] * __ldcs(yt + static_cast<size_t>(j) * d + R);
+  hout[o] = float_to_bf16_bits(bf16_bits_to_float(hin[o]) + y);
+  if (y_last) y_last[o] = y;
+  if (dbg_y) dbg_y[o] = y;
 }
 
 // Row r of the expert-ordered matrix = fp16 x of the pair's token.
@@ -1133,8 +1185,14 @@ cudaError_t launch_pf_plan(const int32_t* ids, int P, int E, int tile, int32_t* 
 
 cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* gates, const uint16_t* hin,
                               uint16_t* hout, float* y_last, float* dbg_y, int T, int d, int k, cudaStream_t s) {
-  return launch_chain(k_pf_combine, dim3(T, (d + 255) / 256), dim3(256), 0, s, ys, ytok, gates, hin, hout, y_last, dbg_y,
-                      d, k);
+  const auto al = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; };
+  // four rows per thread from 256 tokens on (small batches want the CTAs)
+  if (T >= 256 && d % 4 == 0 && al(ys, 16) && al(ytok, 16) && al(hin, 8) && al(hout, 8) && al(y_last, 16) &&
+      al(dbg_y, 16))
+    return launch_chain(k_pf_combine, dim3(T, (d + 1023) / 1024), dim3(256), 0, s, ys, ytok, gates, hin, hout, y_last,
+                        dbg_y, d, k);
+  return launch_chain(k_pf_combine1, dim3(T, (d + 255) / 256), dim3(256), 0, s, ys, ytok, gates, hin, hout, y_last,
+                      dbg_y, d, k);
 }
 
 cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,
