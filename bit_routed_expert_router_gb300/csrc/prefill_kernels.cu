@@ -1092,12 +1092,21 @@ __global__ void __launch_bounds__(256) k_pf_gather(const uint16_t* x16, const in
                                                    uint16_t* xp) {
   pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
   pdl_trigger();
-  const int r = blockIdx.x;
+  // one warp per row, eight rows per CTA; a lane's loads (up to 12 of 16
+  // bytes for d <= 3072) are all issued before its stores
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= P) return;
   const int t = row_pair[r] / k;
   const uint4* src = reinterpret_cast<const uint4*>(x16 + static_cast<size_t>(t) * d);
   uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(r) * d);
-  for (int i = threadIdx.x; i < d / 8; i += 256) dst[i] = src[i];
+  const int n = d / 8;
+  uint4 v[12];
+#pragma unroll
+  for (int u = 0; u < 12; ++u)
+    if (lane + 32 * u < n) v[u] = src[lane + 32 * u];
+#pragma unroll
+  for (int u = 0; u < 12; ++u)
+    if (lane + 32 * u < n) dst[lane + 32 * u] = v[u];
 }
 
 }  // namespace
@@ -1197,7 +1206,7 @@ cudaError_t launch_pf_combine(const float* ys, const float* ytok, const float* g
 
 cudaError_t launch_pf_gather(const uint16_t* x16, const int32_t* row_pair, int P, int d, int k, uint16_t* xp,
                              cudaStream_t s) {
-  return launch_chain(k_pf_gather, dim3(P), dim3(256), 0, s, x16, row_pair, P, d, k, xp);
+  return launch_chain(k_pf_gather, dim3((P + 7) / 8), dim3(256), 0, s, x16, row_pair, P, d, k, xp);
 }
 
 bool g_chain_pdl = false;
