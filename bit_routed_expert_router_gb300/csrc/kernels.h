@@ -157,8 +157,11 @@ size_t pf_gemm_smem(int n);
 cudaError_t pf_set_attrs();
 cudaError_t launch_pf_gemm(int n, const CUtensorMap& tmap_b, const PfGemm& p, int m_tiles, int max_items,
                            cudaStream_t s);
+// xv / xg (or null): the tokens' x rows for the small-batch GEMVs (fp16 in
+// their fragment order) and their 64-element group sums, [T][d] and [T][d / 64].
 cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
-                           uint16_t* dbg_x, float* xn2, float* xmax, uint32_t* err, cudaStream_t s);
+                           uint16_t* dbg_x, float* xn2, float* xmax, uint16_t* xv, float* xg, uint32_t* err,
+                           cudaStream_t s);
 cudaError_t launch_pf_row_stats(const uint16_t* rows, int n, int d, float* n2, float* mx, cudaStream_t s);
 cudaError_t launch_pf_router(const uint16_t* x_bf, const uint16_t* router_w, const float* bias, int T, int d, int E,
                              int k, float* approx, float* xn2, float* wn2, float* xmax, float* wmax, int32_t* ids,
@@ -209,8 +212,9 @@ struct SgParams {
   const int32_t* items;                // [n][3]: active expert, its first expert-ordered row, its rows (<= kSgMaxT)
   const int32_t* n_items;              // n, on the device
   const int32_t* row_pair;             // [P]: pair (t * k + j) of each expert-ordered row
-  const uint16_t* xv;                  // fp16 x in fragment order: [P] expert-ordered rows, then [T] token rows
-  const float* xg;                     // [P + T][d / 64]: group sums of those rows
+  const uint16_t* xv;                  // [T][d]: fp16 x of each token in fragment order (an expert's row c
+                                       // is token row_pair[row0 + c] / k)
+  const float* xg;                     // [T][d / 64]: group sums of those rows
   uint16_t* av_r;                      // [P][f]: fp16 a of the routed rows, fragment order
   uint16_t* av_s;                      // [T][fs]: fp16 a of the shared expert, fragment order
   float* y_r;                          // [T * k][d]: routed down outputs by pair
@@ -221,8 +225,6 @@ struct SgParams {
 bool sg_shape_ok(int d, int f, int fs);
 size_t sg_smem();
 cudaError_t sg_set_attrs();
-cudaError_t launch_sg_gather(const uint16_t* x_bf, const int32_t* row_pair, int P, int T, int d, int k, uint16_t* xv,
-                             float* xg, cudaStream_t s);
 cudaError_t launch_sg(const SgParams& p, int n_sm, cudaStream_t s);
 
 size_t gateup_smem(int d);

@@ -190,8 +190,8 @@ struct moe_ctx {
   // small-batch grouped GEMVs (calls of at most kSgMaxT tokens on the tcgen05 path's routing)
   bool sg_ok = false;                  // shapes and device allow it
   bool use_sg = true;                  // test hook 13
-  uint16_t* sg_xv = nullptr;           // [kSgMaxT * (k + 1)][d] fp16 x rows in fragment order
-  float* sg_xg = nullptr;              // [kSgMaxT * (k + 1)][d / 64] their group sums
+  uint16_t* sg_xv = nullptr;           // [kSgMaxT][d] fp16 x of each token in fragment order
+  float* sg_xg = nullptr;              // [kSgMaxT][d / 64] their group sums
   unsigned long long* pf_timeline = nullptr;   // test hook 8: [4][16] GEMM event times of the first layer
   // chunked prefill of host-pool / expert-file contexts: the union of a chunk's
   // experts of one layer, staged into an arena (expert e at e * stride)
@@ -1523,7 +1523,7 @@ moe_status pf_alloc(moe_ctx* ctx) {
   ctx->pf_xmax = dalloc<float>(T, o, nb);
   ctx->pf_ys = dalloc<float>(T * c.d, o, nb);
   if (ctx->sg_ok) {
-    const size_t rows = std::min<size_t>(T, kSgMaxT) * (c.top_k + 1);
+    const size_t rows = std::min<size_t>(T, kSgMaxT);
     ctx->sg_xv = dalloc<uint16_t>(rows * c.d, o, nb);
     ctx->sg_xg = dalloc<float>(rows * (c.d / 64), o, nb);
     if (!ctx->sg_xv || !ctx->sg_xg) return fail(ctx, MOE_ENOMEM, "small-batch scratch does not fit");
@@ -1571,15 +1571,15 @@ moe_status pf_layer_route(moe_ctx* ctx, int l, int rel, const uint16_t* hin, int
   const size_t xo = static_cast<size_t>(rel) * T;
   PROF(4, s);
   CK(launch_pf_prep(hin, T, d, c.prenorm, c.norm_eps, ctx->pf_xbf, ctx->pf_x16,
-                    dbg && ctx->dbg_x ? ctx->dbg_x + xo * d : nullptr, ctx->pf_xn2, ctx->pf_xmax, ctx->err_word, s));
+                    dbg && ctx->dbg_x ? ctx->dbg_x + xo * d : nullptr, ctx->pf_xn2, ctx->pf_xmax,
+                    small ? ctx->sg_xv : nullptr, small ? ctx->sg_xg : nullptr, ctx->err_word, s));
   CK(launch_pf_router(ctx->pf_xbf, L.router_w, bias ? bias + xo * E : nullptr, T, d, E, k, ctx->pf_approx,
                       ctx->pf_xn2, L.router_stats, ctx->pf_xmax, L.router_stats + E, ctx->pf_ids, ctx->pf_gates, dbg && ctx->dbg_ids ? ctx->dbg_ids + xo * k : nullptr,
                       dbg && ctx->dbg_gates ? ctx->dbg_gates + xo * k : nullptr,
                       dbg && ctx->dbg_logits ? ctx->dbg_logits + xo * E : nullptr, ctx->err_word, ctx->n_sm, s));
   CK(launch_pf_plan(ctx->pf_ids, P, E, small ? kSgMaxT : pf_tile_routed(c, T), ctx->pf_cnt, ctx->pf_rowpair,
                     ctx->pf_items, ctx->pf_nitems, s));
-  if (small) CK(launch_sg_gather(ctx->pf_xbf, ctx->pf_rowpair, P, T, d, k, ctx->sg_xv, ctx->sg_xg, s));
-  else CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
+  if (!small) CK(launch_pf_gather(ctx->pf_x16, ctx->pf_rowpair, P, d, k, ctx->pf_xp, s));
   PROF(-1, s);
   return MOE_OK;
 }

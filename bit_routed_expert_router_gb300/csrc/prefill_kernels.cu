@@ -454,11 +454,36 @@ __global__ void __launch_bounds__(kThreads, 2) k_pf_gemm(const __grid_constant__
 
 // ------------------------------------------------------------------ token-side kernels
 
+// A token's x row for the small-batch GEMVs (small_batch.cu): fp16 in their
+// fragment order (for each 64-element group G and lane quarter t4, eight
+// 32-bit words (k16 step st, half h) holding elements 64 G + 16 st + 8 h +
+// 2 t4 + {0, 1}) and its per-group sums of the fp16 values (each the same
+// warp-shuffle tree over the 32 element pairs); from the bf16 row x, by the
+// eight warps of the CTA, a group per warp.
+__device__ __forceinline__ void sg_token_row(const uint16_t* x, int d, uint16_t* xv, float* xg) {
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(x);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(xv);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nG = d / 64;
+  // lane holds elements 64 G + 2 lane, + 1: k16 step lane / 8, half (lane / 4) % 2, quarter lane % 4
+  const int st = lane >> 3, h = (lane >> 2) & 1, t4 = lane & 3;
+  for (int Gi = warp; Gi < nG; Gi += 8) {
+    const uint32_t v = src[32 * Gi + lane];
+    const __half a = __float2half_rn(bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu)));
+    const __half b = __float2half_rn(bf16_bits_to_float(static_cast<uint16_t>(v >> 16)));
+    dst[((Gi * 4 + t4) * 4 + st) * 2 + h] =
+        static_cast<uint32_t>(__half_as_ushort(a)) | (static_cast<uint32_t>(__half_as_ushort(b)) << 16);
+    float sum = __half2float(a) + __half2float(b);
+#pragma unroll
+    for (int m = 16; m; m >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+    if (lane == 0) xg[Gi] = sum;
+  }
+}
+
 // One CTA per token: x = RMSnorm(h) (or h) as bf16 and fp16; the sum of squares
 // is taken in a fixed order.  fp16 overflow / underflow of x is flagged.
 __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int prenorm, float eps, uint16_t* x_bf,
                                                  uint16_t* x16, uint16_t* dbg_x, float* xn2, float* xmax,
-                                                 uint32_t* err) {
+                                                 uint16_t* xv, float* xg, uint32_t* err) {
   pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
   pdl_trigger();
   __shared__ float red[8], red2[8], redm[8];
@@ -501,6 +526,12 @@ __global__ void __launch_bounds__(256) k_pf_prep(const uint16_t* h, int d, int p
   if ((threadIdx.x & 31) == 0) {
     red2[threadIdx.x >> 5] = s2;
     redm[threadIdx.x >> 5] = mx;
+  }
+  if (xv) {
+    // small batches: the token's fp16 x row in the small-batch GEMVs' fragment
+    // order, and its 64-element group sums, from the finished bf16 row
+    __syncthreads();
+    sg_token_row(x_bf + static_cast<size_t>(t) * d, d, xv + static_cast<size_t>(t) * d, xg + static_cast<size_t>(t) * (d / 64));
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, ERR_PF_RANGE);
   if (threadIdx.x == 0) {
@@ -1136,8 +1167,10 @@ cudaError_t launch_pf_gemm(int n, const CUtensorMap& tmap_b, const PfGemm& p, in
 }
 
 cudaError_t launch_pf_prep(const uint16_t* h, int T, int d, int prenorm, float eps, uint16_t* x_bf, uint16_t* x16,
-                           uint16_t* dbg_x, float* xn2, float* xmax, uint32_t* err, cudaStream_t s) {
-  return launch_chain(k_pf_prep, dim3(T), dim3(256), 0, s, h, d, prenorm, eps, x_bf, x16, dbg_x, xn2, xmax, err);
+                           uint16_t* dbg_x, float* xn2, float* xmax, uint16_t* xv, float* xg, uint32_t* err,
+                           cudaStream_t s) {
+  return launch_chain(k_pf_prep, dim3(T), dim3(256), 0, s, h, d, prenorm, eps, x_bf, x16, dbg_x, xn2, xmax, xv, xg,
+                      err);
 }
 
 cudaError_t launch_pf_row_stats(const uint16_t* rows, int n, int d, float* n2, float* mx, cudaStream_t s) {

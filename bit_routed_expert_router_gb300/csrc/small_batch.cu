@@ -334,13 +334,18 @@ __device__ __forceinline__ float4 split_block(const SgParams& p, Smem& S, const 
     const uint4* brow = reinterpret_cast<const uint4*>(S.xc + xoff + col * rb);
     return tile_dot<false, true>(blk, G0, G1, brow, S.xcg + (xoff + c0 * rb) / 128, S.xcg + (xoff + c1 * rb) / 128);
   }
-  // gate/up: x (expert-ordered rows, then the shared expert's token rows at P); down: the shared a rows
-  const int rbase = gu ? (st.row0 >= 0 ? st.row0 : p.P) : 0;
+  // gate/up: the token rows of x (an active expert's column c is the token of
+  // its pair row0 + c; the shared expert's column c is token c); down: the
+  // shared a rows
   if (gu) {
-    const uint4* brow = reinterpret_cast<const uint4*>(p.xv + static_cast<size_t>(rbase + col) * p.d);
+    const int k = p.P / p.T;
+    const int tc = st.row0 >= 0 ? __ldg(&p.row_pair[st.row0 + col]) / k : col;
+    const int t0 = st.row0 >= 0 ? __ldg(&p.row_pair[st.row0 + c0]) / k : c0;
+    const int t1 = st.row0 >= 0 ? __ldg(&p.row_pair[st.row0 + c1]) / k : c1;
+    const uint4* brow = reinterpret_cast<const uint4*>(p.xv + static_cast<size_t>(tc) * p.d);
     const int nGd = p.d / 64;
-    return tile_dot<false, false>(blk, G0, G1, brow, p.xg + static_cast<size_t>(rbase + c0) * nGd,
-                                  p.xg + static_cast<size_t>(rbase + c1) * nGd);
+    return tile_dot<false, false>(blk, G0, G1, brow, p.xg + static_cast<size_t>(t0) * nGd,
+                                  p.xg + static_cast<size_t>(t1) * nGd);
   }
   const uint4* brow = reinterpret_cast<const uint4*>(p.av_s + static_cast<size_t>(col) * p.fs);
   return tile_dot<true, false>(blk, G0, G1, brow, nullptr, nullptr);
@@ -466,11 +471,20 @@ __device__ void fill_cache(const SgParams& p, Smem& S, const CtaStages& cs) {
   mbar_arrive_expect_tx(&S.xbar, bytes);   // release: the table above is visible to the waiters
   for (int i = 0; i < n; ++i) {
     const int u = S.xc_item[i], row0 = __ldg(&p.items[3 * u + 1]), rows = __ldg(&p.items[3 * u + 2]);
-    const uint8_t* src = gu ? reinterpret_cast<const uint8_t*>(p.xv) : reinterpret_cast<const uint8_t*>(p.av_r);
-    bulk_g2s(S.xc + S.xc_off[i], src + static_cast<size_t>(row0) * rb, static_cast<uint32_t>(rows * rb), &S.xbar);
-    if (gu)
-      bulk_g2s(S.xcg + S.xc_off[i] / 128, p.xg + static_cast<size_t>(row0) * nGd, static_cast<uint32_t>(rows * nGd * 4),
-               &S.xbar);
+    if (!gu) {   // the item's rows of a, contiguous in expert order
+      bulk_g2s(S.xc + S.xc_off[i], reinterpret_cast<const uint8_t*>(p.av_r) + static_cast<size_t>(row0) * rb,
+               static_cast<uint32_t>(rows * rb), &S.xbar);
+      continue;
+    }
+    // gate/up: the x rows (and group sums) of the item's tokens, one copy each
+    const int k = p.P / p.T;
+    for (int c = 0; c < rows; ++c) {
+      const int tok = __ldg(&p.row_pair[row0 + c]) / k;
+      bulk_g2s(S.xc + S.xc_off[i] + c * rb, reinterpret_cast<const uint8_t*>(p.xv) + static_cast<size_t>(tok) * rb,
+               static_cast<uint32_t>(rb), &S.xbar);
+      bulk_g2s(S.xcg + (S.xc_off[i] + c * rb) / 128, p.xg + static_cast<size_t>(tok) * nGd,
+               static_cast<uint32_t>(nGd * 4), &S.xbar);
+    }
   }
 }
 
@@ -527,33 +541,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_small_batch(SgParams p) {
   }
 }
 
-// Row r < P: x of expert-ordered row r's token; row P + t: token t.  From the
-// bf16 rows of x to fp16 (exact unless |x| < 2^-14) in fragment order, with the
-// fp32 sum of each 64-element group.
-__global__ void __launch_bounds__(256) k_sg_gather(const uint16_t* x_bf, const int32_t* row_pair, int P, int d, int k,
-                                                   uint16_t* xv, float* xg) {
-  pdl_wait();      // the previous kernel of the stream is complete (no-op without programmatic launch)
-  pdl_trigger();
-  const int r = blockIdx.x;
-  const int t = r < P ? row_pair[r] / k : r - P;
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(x_bf + static_cast<size_t>(t) * d);
-  uint32_t* dst = reinterpret_cast<uint32_t*>(xv + static_cast<size_t>(r) * d);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nG = d / 64;
-  // lane holds elements 64 G + 2 lane, + 1: k16 step lane / 8, half (lane / 4) % 2, quarter lane % 4
-  const int st = lane >> 3, h = (lane >> 2) & 1, t4 = lane & 3;
-  for (int Gi = warp; Gi < nG; Gi += 8) {
-    const uint32_t v = src[32 * Gi + lane];
-    const __half a = __float2half_rn(bf16_bits_to_float(static_cast<uint16_t>(v & 0xFFFFu)));
-    const __half b = __float2half_rn(bf16_bits_to_float(static_cast<uint16_t>(v >> 16)));
-    dst[((Gi * 4 + t4) * 4 + st) * 2 + h] =
-        static_cast<uint32_t>(__half_as_ushort(a)) | (static_cast<uint32_t>(__half_as_ushort(b)) << 16);
-    float sum = __half2float(a) + __half2float(b);
-#pragma unroll
-    for (int m = 16; m; m >>= 1) sum += __shfl_xor_sync(kFull, sum, m);
-    if (lane == 0) xg[static_cast<size_t>(r) * nG + Gi] = sum;
-  }
-}
-
 }  // namespace
 
 bool sg_shape_ok(int d, int f, int fs) {
@@ -566,11 +553,6 @@ size_t sg_smem() { return sizeof(Smem) + 128; }
 cudaError_t sg_set_attrs() {
   return cudaFuncSetAttribute((const void*)k_small_batch, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(sg_smem()));
-}
-
-cudaError_t launch_sg_gather(const uint16_t* x_bf, const int32_t* row_pair, int P, int T, int d, int k, uint16_t* xv,
-                             float* xg, cudaStream_t s) {
-  return launch_chain(k_sg_gather, dim3(P + T), dim3(256), 0, s, x_bf, row_pair, P, d, k, xv, xg);
 }
 
 cudaError_t launch_sg(const SgParams& p, int n_sm, cudaStream_t s) {
