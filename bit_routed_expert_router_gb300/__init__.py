@@ -28,6 +28,7 @@ HOOK_SPIN_LIMIT = 10      # bounded waits of the persistent decode kernels: cycl
 HOOK_AT_REST = 11         # MOE_OK when the persistent kernels' launch words are back at rest
 HOOK_WAIT_DIAG = 12       # the clustered kernel's first wait that ran out (site << 16 | CTA) into a host uint32
 HOOK_SMALL_BATCH = 13     # small-batch grouped GEMVs (calls of at most 32 tokens) on / off
+HOOK_TOKEN_LOOP = 14      # decode steps of 2 to 4 tokens: one clustered-kernel launch per token on / off
 
 
 class MoeConfig(C.Structure):

@@ -133,6 +133,7 @@ constexpr int kPfTileNBig = 256;       // token rows per GEMM tile (groups of ab
 constexpr int kPfTileN = 128;          // token rows per GEMM tile (mid-sized groups)
 constexpr int kPfTileNSmall = 32;      // token rows per GEMM tile when every expert has only a few rows
 constexpr int kPfMinDecodeB = 16;     // resident decode steps of at least this many tokens take the tcgen05 path
+constexpr int kClusterLoopMaxB = 4;   // resident decode steps of 2 to this many tokens: one clustered launch per token
 constexpr int kPfGraphMaxT = 512;     // tcgen05-path calls of at most this many tokens replay a CUDA graph
 enum : int { PF_GU = 0, PF_DN_ROUTED = 1, PF_DN_SHARED = 2 };
 

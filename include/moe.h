@@ -491,6 +491,9 @@ moe_status moe_get_profile(moe_ctx *ctx, moe_kernel_time *out, int n);
  * the default when the shape allows it) or as the tcgen05 GEMMs (decode: from
  * 16 tokens on, else the per-layer GEMVs); MOE_ESTATE when asked for where
  * they cannot run.
+ * hook 14: resident decode steps of 2 to 4 tokens run one clustered-kernel
+ * launch per token (value != 0, the default, where that kernel can run) or
+ * take the batched paths of hook 13 (0).
  * Other hooks: MOE_EINVAL. */
 moe_status moe_test_hook(moe_ctx *ctx, int hook, int64_t value);
 

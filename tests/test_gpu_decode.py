@@ -72,16 +72,23 @@ def test_tiny_layer_single_tokens(kernel):
 
 
 def use_batch_path(ctx, path):
-    """small: small-batch grouped GEMVs (the default); tc: tcgen05 GEMMs from
-    16 tokens on, per-layer GEMVs below; gemv: per-layer GEMVs."""
+    """small: small-batch grouped GEMVs (the default from 5 tokens on); tc:
+    tcgen05 GEMMs from 16 tokens on, per-layer GEMVs below; gemv: per-layer
+    GEMVs; loop: one clustered-kernel launch per token (the default for 2 to 4
+    tokens).  All but loop switch the per-token launches off."""
+    moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_TOKEN_LOOP, 1 if path == "loop" else 0), ctx.h)
+    if path == "loop":
+        return
     moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_PREFILL_TC, 0 if path == "gemv" else 1), ctx.h)
     if path != "gemv":
         moe.check(moe.moe_test_hook(ctx.h, moe.HOOK_SMALL_BATCH, 1 if path == "small" else 0), ctx.h)
 
 
-@pytest.mark.parametrize("path", ["small", "tc", "gemv"])
+@pytest.mark.parametrize("path", ["small", "tc", "gemv", "loop"])
 @pytest.mark.parametrize("B", [2, 3, 8, 9, 31, 32])
 def test_tiny_layer_batched(B, path):
+    if path == "loop" and B > 4:
+        pytest.skip("one launch per token covers 2 to 4 tokens")
     ctx, lay = _tiny_ctx()
     with ctx:
         use_batch_path(ctx, path)
@@ -97,6 +104,34 @@ def test_tiny_layer_batch_equals_single_tokens():
         for t in range(12):
             _, y1, _ = ctx.decode(H[t:t + 1], 0, 1)
             assert_ffn_close(y1[0].cpu().numpy(), yb[t].cpu().double().numpy(), f"token {t}")
+
+
+@pytest.mark.parametrize("B", [2, 4])
+def test_few_tokens_one_launch_each(B):
+    """2 to 4 tokens take one clustered-kernel launch per token: each token's
+    h_out, y and captured ids / gates equal its own single-token call bit for
+    bit (two layers, full shape, a routing bias per token and layer)."""
+    sh, L = FULL, 2
+    with Ctx(sh, n_layers=L, prenorm=1) as ctx:
+        for l in range(L):
+            ctx.init_layer(l, gen_layer(sh, seed=9, layer=l, device="cuda"))
+        H = gen_hidden(B, sh.d, seed=9, device="cuda")
+        g = torch.Generator().manual_seed(9)
+        bias = (torch.randn(L, B, sh.n_experts, generator=g) * 0.5).cuda()
+        cap = capture(ctx, L, B)
+        h_b, y_b, _ = ctx.decode(H, 0, L, bias=bias)
+        ctx.sync()
+        ids_b, gates_b = cap["ids"].clone(), cap["gates"].clone()
+        end_capture(ctx)
+        for t in range(B):
+            cap1 = capture(ctx, L, 1)
+            h1, y1, _ = ctx.decode(H[t:t + 1], 0, L, bias=bias[:, t:t + 1].contiguous())
+            ctx.sync()
+            assert torch.equal(h1[0].view(torch.int16), h_b[t].view(torch.int16)), f"token {t}: h_out"
+            assert torch.equal(y1[0], y_b[t]), f"token {t}: y"
+            assert torch.equal(cap1["ids"][:, 0], ids_b[:, t]), f"token {t}: ids"
+            assert torch.equal(cap1["gates"][:, 0], gates_b[:, t]), f"token {t}: gates"
+            end_capture(ctx)
 
 
 def test_tanh_gelu_variant():
