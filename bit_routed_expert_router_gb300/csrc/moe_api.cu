@@ -1477,7 +1477,7 @@ moe_status moe_decode_step(moe_ctx* ctx, const void* h_in, int B, int layer_begi
   }
   // a few tokens: one clustered-kernel launch per token beats the grouped
   // path's per-layer launches (measured: 2 and 4 tokens at 1,150 and 1,787
-  // tok/s grouped against about 1,950 one at a time; 8 tokens grouped 2,850)
+  // tok/s grouped against about 1,960 one at a time; 5 tokens grouped 2,090)
   if (B <= kClusterLoopMaxB && ctx->use_persistent && ctx->c_ok && ctx->use_cluster && ctx->c_loop) {
     const int d = ctx->cfg.d;
     for (int t = 0; t < B; ++t) {
