@@ -11,9 +11,11 @@
 // applied in fp32), and the tokens of an expert fill the eight B columns of
 // m16n8k16.  Two launches per layer:
 //   SG_GU  gate/up tiles (8 gate + 8 up rows over d) of the shared expert, for
-//          all T tokens, and of every active expert, for its rows of the
-//          expert-ordered token matrix: a = GELU(gate) * up rounded to fp16,
-//          written in the fragment order the down launch reads;
+//          all T tokens, and of every active expert, for the tokens of its
+//          pairs (the x rows of those tokens, which the prefill path's norm
+//          step writes per token, read through the expert-ordered pair list):
+//          a = GELU(gate) * up rounded to fp16, in expert order and in the
+//          fragment order the down launch reads;
 //   SG_DN  down tiles: per stage the shared expert's 16-row tile over all f_s
 //          columns, or an active expert's 16-row tiles over its f columns
 //          (as many as one ring slot holds); outputs per token (shared) and per
@@ -35,7 +37,8 @@
 // 64 G + 16 st + 8 h + 2 t4 + {0, 1}, so a lane loads its fragments of one
 // group as two 16-byte words.  The group sums that the affine needs come from
 // the x rows' precomputed sums (gate/up) or from one more MMA with an all-ones
-// A operand (down: column sums of a), so no atomics enter any sum.
+// A operand (down: column sums of a), so no atomics enter any sum.  The unpack
+// of the int4 words and the MMA are one asm block (mma_nib, common.cuh).
 #include "common.cuh"
 #include "internal.h"
 #include "kernels.h"
